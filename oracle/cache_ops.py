@@ -1,0 +1,95 @@
+"""Cache write and block copy, plain NumPy (test infrastructure only).
+
+Cache write: the decode step stores the new token's K/V in the slot its
+sequence was given ([LLM-INF] 2.2, on-demand allocation: pages exist only for
+generated tokens; [KV-CB] 三, append_slot).  slot s addresses block s // 16,
+row s % 16 of the [num_blocks, Hkv, 16, D] cache.  A negative slot is a
+padding row and is skipped (a reading: the pages are silent on padding).
+
+FP8 variant ([LLM-INF] 5.3 allows per-channel or per-token scales; the
+reading taken is one float32 scale per token per tensor, over all Hkv*D
+values of that token):
+
+    amax  = max |x|                         (float32, exact)
+    scale = fl32(amax / 448)  or 1.0 when amax == 0
+    code  = E4M3_RNE_satfinite( fl32(x / scale) )
+
+where fl32 is an IEEE float32 round-to-nearest division.
+
+Block copy ([LLM-INF] 2.2 copy-on-write; [KV-CB] 4.2): for each (src, dst)
+pair the whole K block, V block and, for FP8, the 16 scales of each are
+copied.  Pairs must not write a block that another pair reads or writes.
+"""
+import numpy as np
+
+from .fp8_e4m3 import e4m3_encode, E4M3_MAX
+
+BLOCK_SIZE = 16
+
+
+def fp8_quantize_token(x):
+    """Quantise one token's values (any shape) -> (uint8 codes, float32 scale)."""
+    xf = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(xf))) if xf.size else np.float32(0)
+    if amax == 0:
+        scale = np.float32(1.0)
+    else:
+        scale = np.float32(amax) / np.float32(E4M3_MAX)
+    y = (xf / scale).astype(np.float32)
+    return e4m3_encode(y), np.float32(scale)
+
+
+def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None):
+    """Return new (k_cache, v_cache, k_scale, v_scale) after writing T tokens.
+
+    k, v: [T, Hkv, D] (float16/float32 values); caches: [num_blocks, Hkv, 16, D]
+    in the storage dtype (float16, float32 holding bf16 values, or uint8 codes
+    when k_scale/v_scale [num_blocks, 16] float32 are given).
+    """
+    k_cache = np.array(k_cache, copy=True)
+    v_cache = np.array(v_cache, copy=True)
+    fp8 = k_scale is not None
+    if fp8:
+        k_scale = np.array(k_scale, dtype=np.float32, copy=True)
+        v_scale = np.array(v_scale, dtype=np.float32, copy=True)
+    slots = np.asarray(slot_mapping).astype(np.int64)
+    used = slots[slots >= 0]
+    if len(np.unique(used)) != len(used):
+        raise ValueError("duplicate slots in one cache write")
+    nslots = k_cache.shape[0] * BLOCK_SIZE
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        if s >= nslots:
+            raise ValueError("slot out of range")
+        blk, off = s // BLOCK_SIZE, s % BLOCK_SIZE
+        if fp8:
+            kc, ks = fp8_quantize_token(k[i])
+            vc, vs = fp8_quantize_token(v[i])
+            k_cache[blk, :, off, :] = kc
+            v_cache[blk, :, off, :] = vc
+            k_scale[blk, off] = ks
+            v_scale[blk, off] = vs
+        else:
+            k_cache[blk, :, off, :] = k[i]
+            v_cache[blk, :, off, :] = v[i]
+    return k_cache, v_cache, k_scale, v_scale
+
+
+def copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None):
+    """Return new caches with block dst := block src for each (src, dst) pair."""
+    pairs = np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+    srcs, dsts = pairs[:, 0], pairs[:, 1]
+    if len(np.unique(dsts)) != len(dsts) or np.intersect1d(srcs, dsts).size:
+        raise ValueError("copy pairs overlap: a dst repeats or is also a src")
+    k_new = np.array(k_cache, copy=True)
+    v_new = np.array(v_cache, copy=True)
+    ks = None if k_scale is None else np.array(k_scale, copy=True)
+    vs = None if v_scale is None else np.array(v_scale, copy=True)
+    for s, d in pairs:
+        k_new[d] = k_cache[s]
+        v_new[d] = v_cache[s]
+        if ks is not None:
+            ks[d] = k_scale[s]
+            vs[d] = v_scale[s]
+    return k_new, v_new, ks, vs
