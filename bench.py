@@ -1,0 +1,608 @@
+#!/usr/bin/env python
+"""Paged decode attention benchmark on GB300.
+
+One step = one pass of the whole decode hot path over one batch:
+  host block manager appends this step's slot for every sequence and builds
+  the block tables (one pinned host->device copy), pa_cache_write stores the
+  new token's K/V, pa_decode computes attention over the paged context
+  (split-K partitions + merge).  The shared-prefix workload adds beam
+  reselection (fork / release) and the pa_copy_blocks copy-on-write step.
+
+Metric: KV-read GB/s of algorithmic bytes (K+V of every context token once,
+plus Q, output, table entries and lengths, plus the cache-write and block-copy
+bytes) per second of device time, and decode tokens/s (one token per
+sequence per step).  Sequences grow by one token per step; every 64 steps the
+batch is released and re-admitted at its starting lengths (as continuous
+batching does when requests finish), so the workload stays the stated one.
+
+`python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]`
+prints one JSON line on rank 0.  `--impl reference` times the float64 CPU
+oracle on host cores instead (bounded sample per step).
+"""
+import argparse
+import ctypes as C
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+RESET_EVERY = 64
+RING = 4              # pinned staging buffers in flight
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+METRIC = "paged decode attention KV-read GB/s and tokens/s; % of GB300 HBM peak"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="llama7b_b32",
+                   choices=["tiny", "llama7b_b32", "gqa70b_b64", "longctx_b8_f16", "longctx_b8_fp8"])
+    p.add_argument("--split", type=int, default=0, help="split_tokens (0 = library choice)")
+    p.add_argument("--e2e-steps", type=int, default=300)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args(argv)
+
+
+# ---- multi-process plumbing (replicas only: no data-path collective) ----------
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate(local_seconds, local_units, world):
+    """Max of the ranks' timed seconds and sum of their units (replicas)."""
+    if world <= 1:
+        return local_seconds, local_units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- measured peaks, profile traffic, clocks -----------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_copy_gbs", "hbm_GBps"):
+            if key in d:
+                return float(d[key]), "measured"
+        for v in d.values():
+            if isinstance(v, dict) and "hbm_gbs" in v:
+                return float(v["hbm_gbs"]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "device_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_191_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config):
+    """DRAM bytes per decode launch from the committed ncu summary, or None
+    when the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", f"traffic_decode_{config}.txt")
+    try:
+        kv = dict(line.split(":", 1) for line in open(path) if ":" in line)
+    except OSError:
+        return None
+    if kv.get("kernel_source_sha256_16", "").strip() != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.proc = None
+        self.lines = []
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, t0, t1):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                rows.append((ts, float(f[1]), float(f[2]), f[5:9]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "no nvidia-smi samples"}
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        window = "timed region"
+        if not inside:
+            inside = rows
+            window = "whole run (timed region shorter than the 100 ms sampling period)"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ---- workloads ------------------------------------------------------------------
+def load_workload(name):
+    from paged_kv_cache_191_gb300 import workloads as W
+    if name == "shared_prefix_16x4":
+        return W.config_shared_prefix()
+    return W.CONFIGS[name]()
+
+
+def decode_bytes(lens, Hq, Hkv, D, kv_e, q_e, out_e):
+    """Algorithmic bytes of one decode launch (K+V once, Q, out, tables, lens)."""
+    lens = np.asarray(lens, dtype=np.int64)
+    kv = int(lens.sum()) * Hkv * D * 2 * kv_e
+    scales = int(lens.sum()) * 2 * 4 if kv_e == 1 else 0
+    B = len(lens)
+    tables = int(((lens + 15) // 16).sum()) * 4 + B * 4
+    return kv + scales + B * Hq * D * (q_e + out_e) + tables
+
+
+class DecodeStep:
+    """Device-side state and the per-step host logic for a decode workload."""
+
+    def __init__(self, w, split_tokens, steps_total, device):
+        import torch
+        from paged_kv_cache_191_gb300 import ops
+        self.torch, self.ops, self.L = torch, ops, ops.lib()
+        self.w = w
+        self.B, self.Hq, self.Hkv, self.D = w.B, w.Hq, w.Hkv, w.D
+        self.fp8 = w.kv_dtype == "fp8"
+        self.dev = device
+        self.lens0 = np.asarray(w.context_lens, dtype=np.int64)
+        # capacity: lengths grow by at most RESET_EVERY tokens before a reset
+        self.max_len = int(self.lens0.max()) + RESET_EVERY + 1
+        self.cap = -(-self.max_len // 16)
+        grow_blocks = self.B * (RESET_EVERY // 16 + 2)
+        self.num_blocks = w.num_blocks + grow_blocks
+        rng = np.random.Generator(np.random.PCG64(12345))
+        order = np.concatenate([w.free_order, w.num_blocks + rng.permutation(grow_blocks)])
+        self.order = order
+        self.alloc = ops.BlockAllocator(self.num_blocks, order)
+        self.ids = list(range(self.B))
+        self._admit()
+
+        kvdt = torch.float16 if w.kv_dtype in ("f16", "fp8") else torch.bfloat16
+        extra = torch.zeros((grow_blocks, self.Hkv, 16, self.D), dtype=kvdt)
+        kp = torch.cat([w.k_pool, extra]).to(device)
+        vp = torch.cat([w.v_pool, extra]).to(device)
+        if self.fp8:  # the cache is filled by the quantiser (set-up, not timed)
+            N = self.num_blocks
+            self.kc = torch.empty((N, self.Hkv, 16, self.D), dtype=torch.uint8, device=device)
+            self.vc = torch.empty_like(self.kc)
+            self.ks = torch.empty((N, 16), dtype=torch.float32, device=device)
+            self.vs = torch.empty_like(self.ks)
+            kin = kp.permute(0, 2, 1, 3).reshape(N * 16, self.Hkv, self.D).contiguous()
+            vin = vp.permute(0, 2, 1, 3).reshape(N * 16, self.Hkv, self.D).contiguous()
+            ops.cache_write(kin, vin, torch.arange(N * 16, device=device), self.kc, self.vc, self.ks, self.vs)
+            del kin, vin, kp, vp
+        else:
+            self.kc, self.vc, self.ks, self.vs = kp, vp, None, None
+        self.q = w.q.to(device)
+        self.new_k, self.new_v = w.new_k.to(device), w.new_v.to(device)
+        self.out = torch.empty((self.B, self.Hq, self.D), dtype=w.q.dtype, device=device)
+        self.desc = ops.cache_desc(self.kc)
+        self.ws_bytes = ops.decode_workspace_size(self.B, self.Hq, self.max_len, self.kc, split_tokens)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        self.split = split_tokens
+
+        # one pinned meta buffer per ring slot: slots int64[B] | lens int32[B] | tables int32[B, cap]
+        self.meta_bytes = self.B * 8 + self.B * 4 + self.B * self.cap * 4
+        self.meta_host = [torch.empty(self.meta_bytes, dtype=torch.uint8).pin_memory()
+                          for _ in range(RING)]
+        self.meta_dev = torch.empty(self.meta_bytes, dtype=torch.uint8, device=device)
+        self.slots_dev = self.meta_dev[: self.B * 8].view(torch.int64)
+        self.lens_dev = self.meta_dev[self.B * 8: self.B * 12].view(torch.int32)
+        self.tables_dev = self.meta_dev[self.B * 12:].view(torch.int32).view(self.B, self.cap)
+        self.ring_ev = [None] * RING
+        self.ring = 0
+        self.ids_c = (C.c_uint64 * self.B)(*self.ids)
+        self.pairs_c = (C.c_int64 * (2 * self.B))()
+        self.ncow = C.c_int32()
+        self.cur_lens = self.lens0.copy() - 1
+        self.steps_since_reset = 0
+
+    def _admit(self):
+        for b in self.ids:
+            self.alloc.alloc_seq(b, int(self.w.context_lens[b]) - 1)
+
+    def host_prepare(self):
+        """a1: reset if due, append one slot per sequence, tables -> pinned."""
+        ops = self.ops
+        if self.steps_since_reset == RESET_EVERY:
+            for b in self.ids:
+                self.alloc.free_seq(b)
+            self._admit()
+            self.cur_lens = self.lens0.copy() - 1
+            self.steps_since_reset = 0
+        buf = self.meta_host[self.ring]
+        if self.ring_ev[self.ring] is not None:
+            self.ring_ev[self.ring].synchronize()
+        base = buf.data_ptr()
+        slots_p = C.cast(base, C.POINTER(C.c_int64))
+        lens_p = C.cast(base + self.B * 8, C.POINTER(C.c_int32))
+        tab_p = C.cast(base + self.B * 12, C.POINTER(C.c_int32))
+        ops._check(self.L.pa_append_slots(self.alloc._h, self.ids_c, self.B, slots_p, self.pairs_c,
+                                          C.byref(self.ncow)), "pa_append_slots")
+        ops._check(self.L.pa_block_tables(self.alloc._h, self.ids_c, self.B, tab_p, self.cap, lens_p),
+                   "pa_block_tables")
+        self.cur_lens += 1
+        self.steps_since_reset += 1
+        return buf
+
+    def enqueue(self, buf, stream, ev_pair=None):
+        """a1 H2D, a2 cache write, a4+a5 decode on `stream`."""
+        torch, L = self.torch, self.L
+        self.meta_dev.copy_(buf, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        self.ring_ev[self.ring] = ev
+        self.ring = (self.ring + 1) % RING
+        sp = C.c_void_p(stream.cuda_stream)
+        self.ops._check(L.pa_cache_write(self.new_k.data_ptr(), self.new_v.data_ptr(),
+                                         self.ops._TORCH_DT[self.new_k.dtype], self.slots_dev.data_ptr(),
+                                         self.B, self.kc.data_ptr(), self.vc.data_ptr(),
+                                         self.ks.data_ptr() if self.fp8 else None,
+                                         self.vs.data_ptr() if self.fp8 else None,
+                                         C.byref(self.desc), sp), "pa_cache_write")
+        if ev_pair is not None:
+            ev_pair[0].record(stream)
+        self.ops._check(L.pa_decode(self.q.data_ptr(), self.ops._TORCH_DT[self.q.dtype],
+                                    self.kc.data_ptr(), self.vc.data_ptr(),
+                                    self.ks.data_ptr() if self.fp8 else None,
+                                    self.vs.data_ptr() if self.fp8 else None,
+                                    self.tables_dev.data_ptr(), self.cap, self.lens_dev.data_ptr(),
+                                    self.max_len, self.B, self.Hq, C.c_float(self.w.scale),
+                                    self.out.data_ptr(), self.ops._TORCH_DT[self.out.dtype],
+                                    C.byref(self.desc), self.ws.data_ptr(), self.ws.numel(),
+                                    self.split, sp), "pa_decode")
+        if ev_pair is not None:
+            ev_pair[1].record(stream)
+
+    def step_bytes(self):
+        """(decode bytes, whole-step bytes) of the step just prepared."""
+        e = 1 if self.fp8 else 2
+        qe = self.q.element_size()
+        dec = decode_bytes(self.cur_lens, self.Hq, self.Hkv, self.D, e, qe, qe)
+        write = 2 * self.B * self.Hkv * self.D * (qe + e) + (2 * self.B * 4 if self.fp8 else 0) + self.B * 8
+        meta = self.meta_bytes
+        return dec, dec + write + meta
+
+    def launches_per_step(self):
+        ws = self.ws_bytes
+        return 2 + (1 if ws else 0)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = load_workload(args.config)
+    st = DecodeStep(w, args.split, args.steps + args.warmup, dev)
+    stream = torch.cuda.Stream(device=dev)
+    total_steps = args.warmup + args.steps
+    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            st.enqueue(st.host_prepare(), stream)
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        dec_b = step_b = 0
+        wall0 = time.time()
+        t_start.record(stream)
+        for i in range(args.steps):
+            buf = st.host_prepare()
+            d, s = st.step_bytes()
+            dec_b += d
+            step_b += s
+            st.enqueue(buf, stream, dec_events[i])
+        t_end.record(stream)
+        stream.synchronize()
+        wall1 = time.time()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.stop()
+    errs = st.ops.device_errors(clear=True)
+    if errs:
+        raise RuntimeError(f"device error flags {errs:#x} during the benchmark")
+    local_s = t_start.elapsed_time(t_end) / 1e3
+    dec_ms = sum(a.elapsed_time(b) for a, b in dec_events) / args.steps
+    max_s, tot_bytes = aggregate(local_s, float(step_b), world)
+    _, tot_tokens = aggregate(local_s, float(st.B * args.steps), world)
+
+    # e2e: public Python API, host (pinned) inputs in, result out, every step
+    e2e = run_e2e(st, args, stream)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+    peak, peak_kind = hbm_peak()
+    avg_dec_bytes = dec_b / args.steps
+    achieved = avg_dec_bytes / (dec_ms / 1e3) / 1e9
+    traffic = profiled_traffic(args.config)
+    res = {
+        "metric": METRIC,
+        "value": round(tot_bytes / max_s / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s * 1e3 / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {"f16": "f16", "bf16": "bf16", "fp8": "fp8e4m3(kv)/f16"}[w.kv_dtype] + "+f32acc",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
+            "block_size": 16, "kv_dtype": w.kv_dtype,
+            "context_lens": f"start {int(st.lens0.min())}..{int(st.lens0.max())} (mean {st.lens0.mean():.0f}),"
+                            f" +1 per step, batch re-admitted every {RESET_EVERY} steps",
+            "split_tokens": args.split or "auto",
+            "l2": f"no flush: K+V per step {avg_dec_bytes / 1e6:.0f} MB vs 129 MB L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "tokens_per_s": round(tot_tokens / max_s, 1),
+        "kv_gbs_decode_only": round(achieved, 2),
+        "pct_of_nominal_8TBs": round(100 * tot_bytes / max_s / 1e9 / NOMINAL_HBM_GBS, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "traffic": traffic, "kernel": "pa_decode (decode_main + decode_reduce)",
+                     "bytes_per_launch": int(avg_dec_bytes), "launch_ms": round(dec_ms, 5)},
+        "e2e": e2e,
+        "gpu_launches": st.launches_per_step() * args.steps,
+        "clocks": clocks.summary(wall0, wall1),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def run_e2e(st, args, stream):
+    """Same step through ops.* with pinned host q/k/v in and out back, synced."""
+    import torch
+    ops = st.ops
+    n = max(1, min(args.e2e_steps, args.steps))
+    hq = st.w.q.pin_memory()
+    hk, hv = st.w.new_k.pin_memory(), st.w.new_v.pin_memory()
+    hout = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    dq = torch.empty_like(st.q)
+    dk, dv = torch.empty_like(st.new_k), torch.empty_like(st.new_v)
+    total_b = 0
+    h2d = hq.numel() * hq.element_size() + 2 * hk.numel() * hk.element_size() + st.meta_bytes
+    d2h = hout.numel() * hout.element_size()
+    with torch.cuda.stream(stream):
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            buf = st.host_prepare()
+            _, s = st.step_bytes()
+            total_b += s
+            st.meta_dev.copy_(buf, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            ops.cache_write(dk, dv, st.slots_dev, st.kc, st.vc, st.ks, st.vs, stream=stream)
+            ops.decode(dq, st.kc, st.vc, st.tables_dev, st.lens_dev, st.max_len, st.w.scale,
+                       out=st.out, k_scale=st.ks, v_scale=st.vs, workspace=st.ws,
+                       split_tokens=st.split, stream=stream)
+            hout.copy_(st.out, non_blocking=True)
+            stream.synchronize()
+        t1 = time.perf_counter()
+    return {"value": round(total_b / (t1 - t0) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
+            "tokens_per_s": round(st.B * n / (t1 - t0), 1),
+            "api": "paged_kv_cache_191_gb300.ops (pinned host buffers, stream sync per step)"}
+
+
+# ---- CPU oracle (baseline and reference arm) --------------------------------------
+def _oracle_task(task):
+    import numpy as np  # noqa: F811
+    from oracle.attention import paged_decode
+    q, kb, vb, n, scale, ks, vs = task
+    tab = np.arange(kb.shape[0], dtype=np.int64)[None, :]
+    paged_decode(q[None], kb, vb, tab, np.array([n]), scale, ks, vs)
+    return n
+
+
+def oracle_tasks(w, seqs, fp8_codes=None):
+    """Per-sequence oracle inputs: that sequence's blocks (de-duplicated pool view)."""
+    from paged_kv_cache_191_gb300.workloads import BLOCK
+    tasks = []
+    for b in seqs:
+        n = int(w.context_lens[b])
+        blocks = w.block_tables[b][: -(-n // BLOCK)]
+        kb = w.k_pool[blocks]
+        vb = w.v_pool[blocks]
+        kb = kb.float().numpy() if str(kb.dtype) == "torch.bfloat16" else kb.numpy()
+        vb = vb.float().numpy() if str(vb.dtype) == "torch.bfloat16" else vb.numpy()
+        q = w.q[b].float().numpy() if str(w.q.dtype) == "torch.bfloat16" else w.q[b].numpy()
+        if fp8_codes is not None:
+            from oracle.cache_ops import fp8_quantize_rows
+            H, D = kb.shape[1], kb.shape[3]
+            kcodes, ks = fp8_quantize_rows(kb.transpose(0, 2, 1, 3).reshape(-1, H, D))
+            vcodes, vs = fp8_quantize_rows(vb.transpose(0, 2, 1, 3).reshape(-1, H, D))
+            kb = kcodes.reshape(-1, 16, H, D).transpose(0, 2, 1, 3).copy()
+            vb = vcodes.reshape(-1, 16, H, D).transpose(0, 2, 1, 3).copy()
+            tasks.append((q, kb, vb, n, w.scale, ks.reshape(-1, 16), vs.reshape(-1, 16)))
+        else:
+            tasks.append((q, kb, vb, n, w.scale, None, None))
+    return tasks
+
+
+def _pool(cores):
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    for k in env_keys:
+        os.environ[k] = "1"
+    return ctx.Pool(cores)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, seconds):
+    """The oracle as it stands over whole sequences of the workload, in a spawn
+    pool over the host cores, repeated until about `seconds` have passed."""
+    cores = cpu_cores()
+    seqs = list(range(w.B))
+    tasks = oracle_tasks(w, seqs, fp8_codes=(w.kv_dtype == "fp8") or None)
+    e = 1 if w.kv_dtype == "fp8" else 2
+    per_seq = [decode_bytes([int(w.context_lens[b])], w.Hq, w.Hkv, w.D, e, 2, 2) for b in seqs]
+    with _pool(cores) as pool:
+        t0 = time.perf_counter()
+        done_b = 0
+        rounds = 0
+        while True:
+            pool.map(_oracle_task, tasks, chunksize=1)
+            done_b += sum(per_seq)
+            rounds += 1
+            if time.perf_counter() - t0 >= seconds or rounds >= 50:
+                break
+        t1 = time.perf_counter()
+    return {"value": round(done_b / (t1 - t0) / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rounds} pass(es) over all {w.B} sequences x {w.Hq} heads of {w.name} "
+                      f"(float64 NumPy oracle, spawn pool of {cores} single-threaded workers)",
+            "tokens_per_s": round(rounds * w.B / (t1 - t0), 2)}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the float64 CPU oracle on host cores, K bounded steps."""
+    if rank != 0:
+        return
+    w = load_workload(args.config)
+    cores = cpu_cores()
+    fp8 = w.kv_dtype == "fp8"
+    e = 1 if fp8 else 2
+    seqs = list(range(w.B))
+    tasks = oracle_tasks(w, seqs, fp8_codes=fp8 or None)
+    per = [decode_bytes([int(w.context_lens[b])], w.Hq, w.Hkv, w.D, e, 2, 2) for b in seqs]
+    budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step
+    with _pool(cores) as pool:
+        t = time.perf_counter()
+        pool.map(_oracle_task, tasks[:cores], chunksize=1)
+        per_task = (time.perf_counter() - t) / max(1, min(cores, len(tasks))) * cores
+        n_per_step = int(max(1, min(len(tasks), budget / max(per_task / cores, 1e-6))))
+        order = [i % len(tasks) for i in range(n_per_step * (args.steps + args.warmup))]
+        k = 0
+        for _ in range(args.warmup):
+            pool.map(_oracle_task, [tasks[order[k + j]] for j in range(n_per_step)], chunksize=1)
+            k += n_per_step
+        t0 = time.perf_counter()
+        done_b = 0
+        for _ in range(args.steps):
+            idx = [order[k + j] for j in range(n_per_step)]
+            pool.map(_oracle_task, [tasks[i] for i in idx], chunksize=1)
+            done_b += sum(per[i] for i in idx)
+            k += n_per_step
+        t1 = time.perf_counter()
+    val = round(done_b / (t1 - t0) / 1e9, 4)
+    sample = (f"each step: {n_per_step} of {w.B} sequences (all {w.Hq} heads) of {w.name}, "
+              f"float64 NumPy oracle, spawn pool of {cores} workers")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round((t1 - t0) * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+                   "head_dim": w.D, "kv_dtype": w.kv_dtype, "parallelism": "host cores"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,240 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: paged-KV decode attention for GB300
+ * (sm_103a), plus the host-side block manager that feeds it.
+ *
+ * Sources, cited by page title and section:
+ *   [LLM-INF] "LLM推理引擎深度实战：从PagedAttention到分布式推理部署" (ybb.press)
+ *             2.2 paging with 16-token pages, per-request page tables,
+ *                 on-demand allocation, copy-on-write via refcounts;
+ *             2.3 the attention kernel resolves the page table itself and
+ *                 gathers scattered K/V, transparent to the model;
+ *             5.3 FP8 KV cache with per-token or per-channel scales.
+ *   [KV-CB]   "大模型推理引擎优化：KV Cache 与连续批处理" (devpress.csdn.net)
+ *             2.2 16-token blocks;
+ *             三   the block manager: block table, free list, refcount,
+ *                 allocate / append / free / utilisation;
+ *             4.2 copy-on-write when a shared block is written.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Block size is fixed at PA_BLOCK_SIZE = 16 tokens.
+ * - A KV cache is two device arrays k_cache, v_cache, each laid out
+ *   [num_blocks][num_kv_heads][16][head_dim] in kv_dtype, so one (block,
+ *   kv head) tile of 16 tokens is contiguous.  FP8 caches hold E4M3 codes and
+ *   carry two float32 arrays k_scale, v_scale laid out [num_blocks][16]: one
+ *   scale per stored token, shared by all of that token's heads and dims.
+ * - "slot" s addresses block s / 16, row s % 16.
+ * - Ownership: the caller owns and allocates every device buffer (queues,
+ *   tables, caches, outputs, workspace).  The library never allocates device
+ *   memory, never synchronises the stream it is given, and keeps no pointer
+ *   after a call returns.
+ * - Streams: device work is enqueued on `stream` (a cudaStream_t passed as
+ *   void*; NULL = legacy default stream) in call order.
+ * - Errors: every call returns a pa_status.  Host arguments are validated
+ *   before anything is enqueued, so a call that returns an error launched
+ *   nothing.  pa_last_error() gives a message for the calling thread's last
+ *   failed call.  Values that live on the device (slots, block ids, context
+ *   lengths) cannot be checked on the host: the kernels bounds-check them,
+ *   skip the offending access (a bad block id reads as zeros) and set a bit in
+ *   a per-device error word, read with pa_device_errors().  No kernel traps.
+ * - Device pointers must be 16-byte aligned.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_BLOCK_SIZE 16
+#define PA_MAX_GROUP 8      /* query heads per kv head supported by pa_decode */
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = 1,      /* bad argument (null, shape, alignment, range) */
+  PA_ERR_OOM = 2,          /* block manager: not enough free blocks */
+  PA_ERR_NOT_FOUND = 3,    /* block manager: unknown sequence id */
+  PA_ERR_UNSUPPORTED = 4,  /* valid but not built (head_dim, dtype, group) */
+  PA_ERR_CUDA = 5          /* a CUDA runtime call or launch failed */
+} pa_status;
+
+typedef enum {
+  PA_DTYPE_F16 = 0,
+  PA_DTYPE_BF16 = 1,
+  PA_DTYPE_FP8_E4M3 = 2,
+  PA_DTYPE_F32 = 3
+} pa_dtype;
+
+/* Bits of the per-device error word (pa_device_errors). */
+#define PA_DEVERR_SLOT_RANGE   0x1u  /* cache write: slot >= num_blocks*16 */
+#define PA_DEVERR_BLOCK_RANGE  0x2u  /* decode/copy: block id outside the pool */
+#define PA_DEVERR_CONTEXT_LEN  0x4u  /* decode: length < 0 or above a stated bound */
+#define PA_DEVERR_TIMEOUT      0x8u  /* a bounded barrier wait gave up */
+
+/* Shape of a paged KV cache. */
+typedef struct {
+  int32_t num_blocks;    /* physical blocks in the pool, > 0 */
+  int32_t num_kv_heads;  /* Hkv, > 0 */
+  int32_t head_dim;      /* D: 64 or 128 (FP8: 128) */
+  int32_t block_size;    /* must be PA_BLOCK_SIZE */
+  int32_t kv_dtype;      /* pa_dtype: F16, BF16 or FP8_E4M3 */
+} pa_cache_desc;
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char* pa_last_error(void);
+
+/* ABI version of this header (major * 100 + minor). */
+int32_t pa_version(void);
+
+/*
+ * pa_cache_write -- store this step's K/V rows in their slots.
+ * [LLM-INF] 2.2 (pages exist only for generated tokens), [KV-CB] 三 (append).
+ *
+ * k, v         device, [num_tokens][num_kv_heads][head_dim] in in_dtype
+ *              (F16, BF16 or F32).  For F16/BF16 caches in_dtype must equal
+ *              kv_dtype or be F32 (rounded to nearest even); the copy of a
+ *              same-dtype row is exact.
+ * slot_mapping device int64 [num_tokens]; slot < 0 skips the row (padding).
+ *              Slots must be distinct; a slot >= num_blocks*16 is skipped and
+ *              flagged PA_DEVERR_SLOT_RANGE.
+ * k_scale, v_scale  FP8 only (else NULL): device float32 [num_blocks][16].
+ *              FP8 rows are quantised per token: amax = max|x| over all
+ *              heads and dims of the token, scale = amax/448 (float32 RN
+ *              division; 1 when amax = 0), code = E4M3(x/scale) with
+ *              round-to-nearest-even and saturation to +-448.
+ */
+pa_status pa_cache_write(const void* k, const void* v, int32_t in_dtype,
+                         const int64_t* slot_mapping, int64_t num_tokens,
+                         void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                         const pa_cache_desc* desc, void* stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
+ * the same (B, num_q_heads, max_context_len, desc, split_tokens).  0 when a
+ * single partition covers max_context_len (no split-K pass).
+ */
+size_t pa_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                                const pa_cache_desc* desc, int32_t split_tokens);
+
+/*
+ * pa_decode -- one decode step of paged attention.
+ * [LLM-INF] 2.3: the kernel translates logical token t of sequence b into
+ * physical block block_tables[b][t/16], row t%16, and gathers K/V from there.
+ * For every sequence b < B and query head h (kv head g = h / G, G =
+ * num_q_heads / num_kv_heads, contiguous groups):
+ *     out[b][h] = sum_t softmax_t(scale * q[b][h] . K_t) V_t,  t < context_lens[b]
+ * context_lens[b] = 0 gives a zero row.
+ *
+ * q            device [B][num_q_heads][head_dim] in q_dtype.  For F16/BF16
+ *              caches q_dtype must equal kv_dtype; for FP8 caches F16 or BF16.
+ * k_scale, v_scale  FP8 caches only (else NULL), as in pa_cache_write.
+ * block_tables device int32 [B][max_blocks_per_seq]; entries past
+ *              ceil(context_lens[b]/16) are never read.
+ * context_lens device int32 [B]; each must be <= max_context_len and
+ *              <= max_blocks_per_seq*16 (else clamped and flagged).
+ * max_context_len host upper bound on context_lens, sizes the split.
+ * out          device [B][num_q_heads][head_dim] in out_dtype (q_dtype or F32).
+ * workspace    device, >= pa_decode_workspace_size(...) bytes, 16-byte
+ *              aligned; may be NULL when that size is 0.  Contents are
+ *              scratch: overwritten by the call, meaningless afterwards.
+ * split_tokens tokens per split-K partition (multiple of 16, 16..1024), or 0
+ *              to let the library choose from the shape and the SM count.
+ *
+ * Work: one CTA per (sequence, kv head, partition); all G query heads of a
+ * kv head share every K/V tile load; partitions are merged by a second
+ * kernel when more than one exists.
+ */
+pa_status pa_decode(const void* q, int32_t q_dtype,
+                    const void* k_cache, const void* v_cache,
+                    const float* k_scale, const float* v_scale,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* context_lens, int32_t max_context_len,
+                    int32_t B, int32_t num_q_heads, float scale,
+                    void* out, int32_t out_dtype,
+                    const pa_cache_desc* desc,
+                    void* workspace, size_t workspace_bytes,
+                    int32_t split_tokens, void* stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write block copies.
+ * [LLM-INF] 2.2 and [KV-CB] 4.2: before a shared block is written, its
+ * contents are copied to a private block.  For each pair (src, dst) in
+ * `pairs` (device int64 [num_pairs][2]) the whole K block, V block and, for
+ * FP8, both 16-entry scale rows are copied.  No dst may repeat or appear as a
+ * src (the block manager never emits such pairs); ids outside the pool are
+ * skipped and flagged PA_DEVERR_BLOCK_RANGE.
+ */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                         const int64_t* pairs, int64_t num_pairs,
+                         const pa_cache_desc* desc, void* stream);
+
+/*
+ * pa_device_errors -- read (and optionally clear) the current device's error
+ * word (PA_DEVERR_* bits).  Synchronises the device.
+ */
+pa_status pa_device_errors(uint32_t* flags, int32_t clear);
+
+/* ------------------------------------------------------------------------
+ * Host block manager ([KV-CB] 三; copy-on-write per [LLM-INF] 2.2).
+ * Single-threaded: a handle must not be used by two threads at once.
+ * Free list is FIFO: allocation takes from the front, release appends at the
+ * back, a table is released in logical order.  Every mutating call is
+ * all-or-nothing: on error the state is unchanged.
+ * ------------------------------------------------------------------------ */
+typedef struct pa_alloc pa_alloc;
+
+/* num_blocks > 0; block_size must be 16; free_order (host int64
+ * [num_blocks], a permutation of 0..num_blocks-1) sets the initial free-list
+ * order, NULL = ascending. */
+pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size,
+                          const int64_t* free_order, pa_alloc** out);
+void pa_alloc_destroy(pa_alloc* a);
+
+/* New sequence holding num_tokens tokens: takes ceil(num_tokens/16) blocks.
+ * PA_ERR_INVALID if seq_id exists, PA_ERR_OOM if too few blocks are free. */
+pa_status pa_alloc_seq(pa_alloc* a, uint64_t seq_id, int64_t num_tokens);
+
+/* Reserve the slot of the sequence's next token; returns slot = block*16 +
+ * row.  If the last block is full a fresh block is appended.  If the last
+ * block is partial and shared (refcount > 1) the sequence first moves to a
+ * fresh block: *cow_src, *cow_dst name the copy the caller must perform
+ * (pa_copy_blocks) before writing; otherwise both are -1. */
+pa_status pa_append_slot(pa_alloc* a, uint64_t seq_id, int64_t* slot,
+                         int64_t* cow_src, int64_t* cow_dst);
+
+/* Batched pa_append_slot over n distinct sequences, in order, all or
+ * nothing.  slots: host int64 [n]; cow_pairs: host int64 [n][2] receives the
+ * copies (src, dst) packed at the front; *n_cow their number. */
+pa_status pa_append_slots(pa_alloc* a, const uint64_t* seq_ids, int32_t n,
+                          int64_t* slots, int64_t* cow_pairs, int32_t* n_cow);
+
+/* child shares every block of parent (refcount + 1 each); same token count. */
+pa_status pa_fork(pa_alloc* a, uint64_t parent, uint64_t child);
+
+/* Release a sequence: refcount - 1 per block, freed at 0. */
+pa_status pa_free_seq(pa_alloc* a, uint64_t seq_id);
+
+/* Copy one table (cap entries max) and its token count. */
+pa_status pa_block_table(const pa_alloc* a, uint64_t seq_id, int32_t* out, int32_t cap,
+                         int32_t* n_blocks, int64_t* n_tokens);
+
+/* Tables of n sequences as a host int32 [n][cap] array padded with -1, and
+ * their token counts as int32 [n] (the decode kernel's context_lens). */
+pa_status pa_block_tables(const pa_alloc* a, const uint64_t* seq_ids, int32_t n,
+                          int32_t* tables, int32_t cap, int32_t* context_lens);
+
+/* Pool statistics; refcounts (optional, int32 [num_blocks]) receives every
+ * block's refcount.  Utilisation = (total - free) / total ([KV-CB] 三). */
+pa_status pa_alloc_stats(const pa_alloc* a, int32_t* total, int32_t* free_blocks,
+                         int32_t* refcounts);
+
+/* Free list front to back (cap entries max); *n = its full length. */
+pa_status pa_free_list(const pa_alloc* a, int32_t* out, int32_t cap, int32_t* n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

@@ -27,16 +27,26 @@ from .fp8_e4m3 import e4m3_encode, E4M3_MAX
 BLOCK_SIZE = 16
 
 
+def fp8_quantize_rows(x):
+    """Quantise each row of x [T, ...] -> (uint8 codes [T, ...], float32 scales [T]).
+
+    Row t is one token (all its heads and dims): amax over the row, scale =
+    fl32(amax / 448) (1.0 for an all-zero row), codes = E4M3(fl32(x / scale)).
+    """
+    xf = np.asarray(x, dtype=np.float32)
+    T = xf.shape[0]
+    flat = xf.reshape(T, -1)
+    amax = np.abs(flat).max(axis=1) if flat.shape[1] else np.zeros(T, np.float32)
+    scale = np.where(amax == 0, np.float32(1.0),
+                     amax.astype(np.float32) / np.float32(E4M3_MAX)).astype(np.float32)
+    y = (flat / scale[:, None]).astype(np.float32)
+    return e4m3_encode(y).reshape(xf.shape), scale
+
+
 def fp8_quantize_token(x):
     """Quantise one token's values (any shape) -> (uint8 codes, float32 scale)."""
-    xf = np.asarray(x, dtype=np.float32)
-    amax = np.float32(np.max(np.abs(xf))) if xf.size else np.float32(0)
-    if amax == 0:
-        scale = np.float32(1.0)
-    else:
-        scale = np.float32(amax) / np.float32(E4M3_MAX)
-    y = (xf / scale).astype(np.float32)
-    return e4m3_encode(y), np.float32(scale)
+    codes, scale = fp8_quantize_rows(np.asarray(x)[None])
+    return codes[0], np.float32(scale[0])
 
 
 def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None):
@@ -57,22 +67,22 @@ def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None
     if len(np.unique(used)) != len(used):
         raise ValueError("duplicate slots in one cache write")
     nslots = k_cache.shape[0] * BLOCK_SIZE
-    for i, s in enumerate(slots):
-        if s < 0:
-            continue
-        if s >= nslots:
-            raise ValueError("slot out of range")
-        blk, off = s // BLOCK_SIZE, s % BLOCK_SIZE
+    if (slots >= nslots).any():
+        raise ValueError("slot out of range")
+    idx = np.nonzero(slots >= 0)[0]
+    for c0 in range(0, len(idx), 4096):          # chunks bound the float64 temporaries
+        rows = idx[c0:c0 + 4096]
+        blk, off = slots[rows] // BLOCK_SIZE, slots[rows] % BLOCK_SIZE
         if fp8:
-            kc, ks = fp8_quantize_token(k[i])
-            vc, vs = fp8_quantize_token(v[i])
+            kc, ks = fp8_quantize_rows(np.asarray(k)[rows])
+            vc, vs = fp8_quantize_rows(np.asarray(v)[rows])
             k_cache[blk, :, off, :] = kc
             v_cache[blk, :, off, :] = vc
             k_scale[blk, off] = ks
             v_scale[blk, off] = vs
         else:
-            k_cache[blk, :, off, :] = k[i]
-            v_cache[blk, :, off, :] = v[i]
+            k_cache[blk, :, off, :] = np.asarray(k)[rows]
+            v_cache[blk, :, off, :] = np.asarray(v)[rows]
     return k_cache, v_cache, k_scale, v_scale
 
 

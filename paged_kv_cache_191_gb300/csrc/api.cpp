@@ -1,0 +1,231 @@
+// C-ABI entry points: host-side validation, then dispatch to the launchers.
+// Nothing is enqueued unless every host-visible argument checks out.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+static thread_local std::string g_last_error;
+
+pa_status fail(pa_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+static pa_status check_desc(const pa_cache_desc* d, const char* fn) {
+  if (!d) return fail(PA_ERR_INVALID, "%s: desc is NULL", fn);
+  if (d->block_size != PA_BLOCK_SIZE)
+    return fail(PA_ERR_UNSUPPORTED, "%s: block_size must be 16", fn);
+  if (d->num_blocks <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0)
+    return fail(PA_ERR_INVALID, "%s: num_blocks, num_kv_heads, head_dim must be > 0", fn);
+  if (d->kv_dtype != PA_DTYPE_F16 && d->kv_dtype != PA_DTYPE_BF16 &&
+      d->kv_dtype != PA_DTYPE_FP8_E4M3)
+    return fail(PA_ERR_INVALID, "%s: kv_dtype must be F16, BF16 or FP8_E4M3", fn);
+  if (d->head_dim != 64 && d->head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "%s: head_dim %d not built (64, 128)", fn, d->head_dim);
+  if (d->kv_dtype == PA_DTYPE_FP8_E4M3 && d->head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "%s: FP8 caches need head_dim 128", fn);
+  return PA_OK;
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+pa_status plan_decode(int32_t B, int32_t Hq, int32_t max_context_len, const pa_cache_desc* d,
+                      int32_t split_tokens, DecodePlan* plan) {
+  const int64_t nblk_max = max_context_len <= 0 ? 1 : (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+  int32_t bpp;
+  if (split_tokens > 0) {
+    if (split_tokens % PA_BLOCK_SIZE || split_tokens > 1024)
+      return fail(PA_ERR_INVALID, "split_tokens must be a multiple of 16 in [16, 1024]");
+    bpp = split_tokens / PA_BLOCK_SIZE;
+  } else {
+    // 256-token partitions by default; shrink them while the grid would give
+    // fewer than two partitions per SM.
+    const int64_t units = static_cast<int64_t>(B) * d->num_kv_heads;
+    const int64_t sms = sm_count();
+    bpp = 16;
+    while (bpp > 4 && units * ((nblk_max + bpp - 1) / bpp) < 2 * sms) bpp /= 2;
+  }
+  const int64_t parts = (nblk_max + bpp - 1) / bpp;
+  if (parts > 65535) return fail(PA_ERR_UNSUPPORTED, "context too long for the partition grid");
+  plan->blocks_per_part = bpp;
+  plan->max_parts = static_cast<int32_t>(parts);
+  if (parts > 1) {
+    const size_t rows = static_cast<size_t>(B) * Hq * parts;
+    size_t bytes = rows * d->head_dim * sizeof(float) + 2 * rows * sizeof(float);
+    plan->workspace_bytes = (bytes + 255) & ~static_cast<size_t>(255);
+  } else {
+    plan->workspace_bytes = 0;
+  }
+  return PA_OK;
+}
+
+}  // namespace pa
+
+using pa::fail;
+
+extern "C" {
+
+const char* pa_last_error(void) { return pa::g_last_error.c_str(); }
+
+int32_t pa_version(void) { return 100; }
+
+pa_status pa_cache_write(const void* k, const void* v, int32_t in_dtype,
+                         const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                         void* v_cache, float* k_scale, float* v_scale, const pa_cache_desc* desc,
+                         void* stream) {
+  pa_status st = pa::check_desc(desc, "pa_cache_write");
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return fail(PA_ERR_INVALID, "pa_cache_write: num_tokens < 0");
+  if (num_tokens == 0) return PA_OK;
+  if (num_tokens > INT32_MAX) return fail(PA_ERR_INVALID, "pa_cache_write: too many tokens");
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return fail(PA_ERR_INVALID, "pa_cache_write: null pointer");
+  if (!pa::aligned16(k) || !pa::aligned16(v) || !pa::aligned16(k_cache) || !pa::aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return fail(PA_ERR_INVALID, "pa_cache_write: misaligned pointer");
+  const bool fp8 = desc->kv_dtype == PA_DTYPE_FP8_E4M3;
+  if (fp8) {
+    if (in_dtype != PA_DTYPE_F16 && in_dtype != PA_DTYPE_BF16 && in_dtype != PA_DTYPE_F32)
+      return fail(PA_ERR_INVALID, "pa_cache_write: FP8 cache needs F16, BF16 or F32 input");
+    if (!k_scale || !v_scale || !pa::aligned16(k_scale) || !pa::aligned16(v_scale))
+      return fail(PA_ERR_INVALID, "pa_cache_write: FP8 cache needs 16-byte aligned scales");
+  } else {
+    if (in_dtype != desc->kv_dtype && in_dtype != PA_DTYPE_F32)
+      return fail(PA_ERR_INVALID, "pa_cache_write: in_dtype must equal kv_dtype or be F32");
+    if (k_scale || v_scale)
+      return fail(PA_ERR_INVALID, "pa_cache_write: scales are only for FP8 caches");
+  }
+  return pa::launch_cache_write(k, v, in_dtype, slot_mapping, num_tokens, k_cache, v_cache,
+                                k_scale, v_scale, desc, stream);
+}
+
+size_t pa_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                                const pa_cache_desc* desc, int32_t split_tokens) {
+  if (pa::check_desc(desc, "pa_decode_workspace_size") != PA_OK || B < 0 || num_q_heads <= 0)
+    return 0;
+  pa::DecodePlan plan;
+  if (pa::plan_decode(B, num_q_heads, max_context_len, desc, split_tokens, &plan) != PA_OK)
+    return 0;
+  return plan.workspace_bytes;
+}
+
+pa_status pa_decode(const void* q, int32_t q_dtype, const void* k_cache, const void* v_cache,
+                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    int32_t max_context_len, int32_t B, int32_t num_q_heads, float scale,
+                    void* out, int32_t out_dtype, const pa_cache_desc* desc, void* workspace,
+                    size_t workspace_bytes, int32_t split_tokens, void* stream) {
+  pa_status st = pa::check_desc(desc, "pa_decode");
+  if (st != PA_OK) return st;
+  if (B < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0)
+    return fail(PA_ERR_INVALID, "pa_decode: B, num_q_heads, max_blocks_per_seq, max_context_len out of range");
+  if (num_q_heads % desc->num_kv_heads)
+    return fail(PA_ERR_INVALID, "pa_decode: num_q_heads must be a multiple of num_kv_heads");
+  if (num_q_heads / desc->num_kv_heads > PA_MAX_GROUP)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: more than %d query heads per kv head", PA_MAX_GROUP);
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "pa_decode: scale is not finite");
+  const bool fp8 = desc->kv_dtype == PA_DTYPE_FP8_E4M3;
+  if (fp8) {
+    if (q_dtype != PA_DTYPE_F16 && q_dtype != PA_DTYPE_BF16)
+      return fail(PA_ERR_INVALID, "pa_decode: q_dtype must be F16 or BF16 for an FP8 cache");
+    if (!k_scale || !v_scale || !pa::aligned16(k_scale) || !pa::aligned16(v_scale))
+      return fail(PA_ERR_INVALID, "pa_decode: FP8 cache needs 16-byte aligned scales");
+  } else {
+    if (q_dtype != desc->kv_dtype)
+      return fail(PA_ERR_INVALID, "pa_decode: q_dtype must equal kv_dtype");
+    if (k_scale || v_scale) return fail(PA_ERR_INVALID, "pa_decode: scales are only for FP8 caches");
+  }
+  if (out_dtype != q_dtype && out_dtype != PA_DTYPE_F32)
+    return fail(PA_ERR_INVALID, "pa_decode: out_dtype must be q_dtype or F32");
+  if (B == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return fail(PA_ERR_INVALID, "pa_decode: null pointer");
+  if (!pa::aligned16(q) || !pa::aligned16(k_cache) || !pa::aligned16(v_cache) ||
+      !pa::aligned16(out) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PA_ERR_INVALID, "pa_decode: misaligned pointer");
+  pa::DecodePlan plan;
+  st = pa::plan_decode(B, num_q_heads, max_context_len, desc, split_tokens, &plan);
+  if (st != PA_OK) return st;
+  if (plan.workspace_bytes) {
+    if (!workspace || !pa::aligned16(workspace))
+      return fail(PA_ERR_INVALID, "pa_decode: workspace NULL or misaligned (%zu bytes needed)",
+                  plan.workspace_bytes);
+    if (workspace_bytes < plan.workspace_bytes)
+      return fail(PA_ERR_INVALID, "pa_decode: workspace has %zu bytes, %zu needed", workspace_bytes,
+                  plan.workspace_bytes);
+  }
+  pa::DecodeLaunch a;
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.max_context_len = max_context_len;
+  a.B = B;
+  a.Hq = num_q_heads;
+  a.Hkv = desc->num_kv_heads;
+  a.D = desc->head_dim;
+  a.num_blocks = desc->num_blocks;
+  a.kv_dtype = desc->kv_dtype;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.workspace = workspace;
+  a.plan = plan;
+  return pa::launch_decode(a, stream);
+}
+
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                         const int64_t* pairs, int64_t num_pairs, const pa_cache_desc* desc,
+                         void* stream) {
+  pa_status st = pa::check_desc(desc, "pa_copy_blocks");
+  if (st != PA_OK) return st;
+  if (num_pairs < 0) return fail(PA_ERR_INVALID, "pa_copy_blocks: num_pairs < 0");
+  if (num_pairs == 0) return PA_OK;
+  if (num_pairs > 65535) return fail(PA_ERR_INVALID, "pa_copy_blocks: at most 65535 pairs per call");
+  if (!k_cache || !v_cache || !pairs) return fail(PA_ERR_INVALID, "pa_copy_blocks: null pointer");
+  if (!pa::aligned16(k_cache) || !pa::aligned16(v_cache) || (reinterpret_cast<uintptr_t>(pairs) & 7u))
+    return fail(PA_ERR_INVALID, "pa_copy_blocks: misaligned pointer");
+  const bool fp8 = desc->kv_dtype == PA_DTYPE_FP8_E4M3;
+  if (fp8 && (!k_scale || !v_scale))
+    return fail(PA_ERR_INVALID, "pa_copy_blocks: FP8 cache needs scales");
+  if (!fp8 && (k_scale || v_scale))
+    return fail(PA_ERR_INVALID, "pa_copy_blocks: scales are only for FP8 caches");
+  return pa::launch_copy_blocks(k_cache, v_cache, k_scale, v_scale, pairs, num_pairs, desc, stream);
+}
+
+pa_status pa_device_errors(uint32_t* flags, int32_t clear) {
+  if (!flags) return fail(PA_ERR_INVALID, "pa_device_errors: flags is NULL");
+  uint32_t a = 0, b = 0;
+  pa_status st = pa::read_errors_decode(&a, clear != 0);
+  if (st != PA_OK) return st;
+  st = pa::read_errors_cache_ops(&b, clear != 0);
+  if (st != PA_OK) return st;
+  *flags = a | b;
+  return PA_OK;
+}
+
+}  // extern "C"

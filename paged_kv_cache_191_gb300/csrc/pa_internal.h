@@ -1,0 +1,72 @@
+// Internal host-side declarations shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pa {
+
+// Record `msg` as the calling thread's last error and return `st`.
+pa_status fail(pa_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+inline pa_status ok() { return PA_OK; }
+
+// Element size in bytes of a pa_dtype (0 for an unknown value).
+inline int dtype_bytes(int32_t dt) {
+  switch (dt) {
+    case PA_DTYPE_F16:
+    case PA_DTYPE_BF16: return 2;
+    case PA_DTYPE_FP8_E4M3: return 1;
+    case PA_DTYPE_F32: return 4;
+    default: return 0;
+  }
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Split-K plan for one pa_decode shape (pure function of its arguments and
+// the device's SM count).
+struct DecodePlan {
+  int32_t blocks_per_part;  // 16-token blocks per partition
+  int32_t max_parts;        // partitions of the longest allowed context
+  size_t workspace_bytes;   // 0 when max_parts == 1
+};
+pa_status plan_decode(int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                      const pa_cache_desc* desc, int32_t split_tokens, DecodePlan* plan);
+
+// Arguments of the decode launch after host validation.
+struct DecodeLaunch {
+  const void* q;
+  int32_t q_dtype;
+  const void* k_cache;
+  const void* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const int32_t* context_lens;
+  int32_t max_context_len;
+  int32_t B, Hq, Hkv, D, num_blocks, kv_dtype;
+  float scale;
+  void* out;
+  int32_t out_dtype;
+  void* workspace;
+  DecodePlan plan;
+};
+pa_status launch_decode(const DecodeLaunch& a, void* stream);
+
+pa_status launch_cache_write(const void* k, const void* v, int32_t in_dtype,
+                             const int64_t* slots, int64_t T, void* k_cache, void* v_cache,
+                             float* k_scale, float* v_scale, const pa_cache_desc* d,
+                             void* stream);
+
+pa_status launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                             const int64_t* pairs, int64_t n, const pa_cache_desc* d,
+                             void* stream);
+
+// Per-translation-unit device error words, OR-ed by pa_device_errors.
+pa_status read_errors_decode(uint32_t* flags, bool clear);
+pa_status read_errors_cache_ops(uint32_t* flags, bool clear);
+
+}  // namespace pa

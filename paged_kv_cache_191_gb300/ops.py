@@ -1,0 +1,292 @@
+"""Python binding of libpagedkv.so (argument marshalling only).
+
+Every device step runs in the library's CUDA kernels; this module checks
+tensor device/dtype/shape/contiguity, passes raw pointers and the current
+torch stream through the C ABI declared in include/pagedkv.h, and turns a
+non-zero pa_status into an exception.  PyTorch is used for device memory and
+streams only.  There is no fallback: if the library is missing, every call
+raises.
+"""
+import ctypes as C
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
+
+PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_NOT_FOUND, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = range(6)
+F16, BF16, FP8_E4M3, F32 = 0, 1, 2, 3
+BLOCK_SIZE = 16
+DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+_TORCH_DT = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
+             torch.uint8: FP8_E4M3, torch.float8_e4m3fn: FP8_E4M3}
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"[pa_status {status}] {msg}")
+        self.status = status
+
+
+class OutOfBlocks(PagedKVError):
+    pass
+
+
+class UnknownSequence(PagedKVError):
+    pass
+
+
+class CacheDesc(C.Structure):
+    _fields_ = [("num_blocks", C.c_int32), ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("block_size", C.c_int32), ("kv_dtype", C.c_int32)]
+
+
+_P = C.c_void_p
+_I32, _I64, _U64, _F = C.c_int32, C.c_int64, C.c_uint64, C.c_float
+_I32P, _I64P, _U64P = C.POINTER(C.c_int32), C.POINTER(C.c_int64), C.POINTER(C.c_uint64)
+
+# name -> (restype, argtypes); mirrors include/pagedkv.h
+SIGNATURES = {
+    "pa_last_error": (C.c_char_p, []),
+    "pa_version": (_I32, []),
+    "pa_cache_write": (C.c_int, [_P, _P, _I32, _P, _I64, _P, _P, _P, _P, C.POINTER(CacheDesc), _P]),
+    "pa_decode_workspace_size": (C.c_size_t, [_I32, _I32, _I32, C.POINTER(CacheDesc), _I32]),
+    "pa_decode": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F, _P, _I32,
+                            C.POINTER(CacheDesc), _P, C.c_size_t, _I32, _P]),
+    "pa_copy_blocks": (C.c_int, [_P, _P, _P, _P, _P, _I64, C.POINTER(CacheDesc), _P]),
+    "pa_device_errors": (C.c_int, [C.POINTER(C.c_uint32), _I32]),
+    "pa_alloc_create": (C.c_int, [_I32, _I32, _I64P, C.POINTER(_P)]),
+    "pa_alloc_destroy": (None, [_P]),
+    "pa_alloc_seq": (C.c_int, [_P, _U64, _I64]),
+    "pa_append_slot": (C.c_int, [_P, _U64, _I64P, _I64P, _I64P]),
+    "pa_append_slots": (C.c_int, [_P, _U64P, _I32, _I64P, _I64P, _I32P]),
+    "pa_fork": (C.c_int, [_P, _U64, _U64]),
+    "pa_free_seq": (C.c_int, [_P, _U64]),
+    "pa_block_table": (C.c_int, [_P, _U64, _I32P, _I32, _I32P, _I64P]),
+    "pa_block_tables": (C.c_int, [_P, _U64P, _I32, _I32P, _I32, _I32P]),
+    "pa_alloc_stats": (C.c_int, [_P, _I32P, _I32P, _I32P]),
+    "pa_free_list": (C.c_int, [_P, _I32P, _I32, _I32P]),
+}
+
+_lib = None
+
+
+def lib():
+    """Load libpagedkv.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m paged_kv_cache_191_gb300.build` (needs nvcc)")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status, what=""):
+    if status == PA_OK:
+        return
+    msg = lib().pa_last_error().decode(errors="replace")
+    cls = {PA_ERR_OOM: OutOfBlocks, PA_ERR_NOT_FOUND: UnknownSequence}.get(status, PagedKVError)
+    raise cls(status, f"{what}: {msg}" if what else msg)
+
+
+def _ptr(t):
+    return C.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _dev(t, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def kv_dtype_of(cache):
+    if cache.dtype not in _TORCH_DT or cache.dtype == torch.float32:
+        raise ValueError(f"unsupported cache dtype {cache.dtype}")
+    return _TORCH_DT[cache.dtype]
+
+
+def cache_desc(k_cache):
+    """CacheDesc of a [num_blocks, Hkv, 16, D] cache tensor."""
+    if k_cache.dim() != 4 or k_cache.shape[2] != BLOCK_SIZE:
+        raise ValueError("cache must be [num_blocks, num_kv_heads, 16, head_dim]")
+    nb, h, _, d = k_cache.shape
+    return CacheDesc(nb, h, d, BLOCK_SIZE, kv_dtype_of(k_cache))
+
+
+def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None, stream=None):
+    """Store rows k, v [T, Hkv, D] at slot_mapping [T] (int64; <0 skips)."""
+    for t, n in ((k, "k"), (v, "v"), (slot_mapping, "slot_mapping"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _dev(t, n)
+    desc = cache_desc(k_cache)
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache differ")
+    T = k.shape[0]
+    if k.shape != (T, desc.num_kv_heads, desc.head_dim) or v.shape != k.shape:
+        raise ValueError("k, v must be [T, num_kv_heads, head_dim]")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T:
+        raise ValueError("slot_mapping must be int64 [T]")
+    if k.dtype != v.dtype or k.dtype not in (torch.float16, torch.bfloat16, torch.float32):
+        raise ValueError("k, v must share dtype f16 / bf16 / f32")
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t is not None:
+            _dev(t, n)
+    _check(lib().pa_cache_write(_ptr(k), _ptr(v), _TORCH_DT[k.dtype], _ptr(slot_mapping), T,
+                                _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                C.byref(desc), _stream(stream)), "pa_cache_write")
+
+
+def decode_workspace_size(B, num_q_heads, max_context_len, k_cache, split_tokens=0):
+    desc = cache_desc(k_cache)
+    return int(lib().pa_decode_workspace_size(B, num_q_heads, max_context_len, C.byref(desc), split_tokens))
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
+           out=None, out_dtype=None, k_scale=None, v_scale=None, workspace=None,
+           split_tokens=0, stream=None):
+    """Paged decode attention; returns out [B, Hq, D] (q dtype, or out_dtype)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (context_lens, "context_lens")):
+        _dev(t, n)
+    desc = cache_desc(k_cache)
+    B, Hq, D = q.shape
+    if D != desc.head_dim:
+        raise ValueError("q head_dim differs from the cache")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be int32 [B, max_blocks]")
+    if context_lens.dtype != torch.int32 or context_lens.numel() != B:
+        raise ValueError("context_lens must be int32 [B]")
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=odt, device=q.device)
+    else:
+        _dev(out, "out")
+        if out.shape != (B, Hq, D):
+            raise ValueError("out must be [B, Hq, D]")
+        odt = out.dtype
+    need = int(lib().pa_decode_workspace_size(B, Hq, max_context_len, C.byref(desc), split_tokens))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().pa_decode(_ptr(q), _TORCH_DT[q.dtype], _ptr(k_cache), _ptr(v_cache),
+                           _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
+                           _ptr(context_lens), int(max_context_len), B, Hq, float(scale),
+                           _ptr(out), _TORCH_DT[odt], C.byref(desc), _ptr(workspace), ws_bytes,
+                           int(split_tokens), _stream(stream)), "pa_decode")
+    return out
+
+
+def copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None, stream=None):
+    """Copy whole blocks for each (src, dst) row of pairs (int64 [n, 2])."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (pairs, "pairs")):
+        _dev(t, n)
+    if pairs.dtype != torch.int64 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int64 [n, 2]")
+    desc = cache_desc(k_cache)
+    _check(lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                _ptr(pairs), pairs.shape[0], C.byref(desc), _stream(stream)),
+           "pa_copy_blocks")
+
+
+def device_errors(clear=True):
+    """Device error word (DEVERR_* bits); synchronises the device."""
+    flags = C.c_uint32(0)
+    _check(lib().pa_device_errors(C.byref(flags), 1 if clear else 0), "pa_device_errors")
+    return flags.value
+
+
+class BlockAllocator:
+    """Host block manager (C++): FIFO free list, block tables, refcounts, CoW."""
+
+    def __init__(self, num_blocks, free_order=None):
+        h = C.c_void_p()
+        order = None
+        if free_order is not None:
+            self._order = (C.c_int64 * num_blocks)(*[int(x) for x in free_order])
+            order = C.cast(self._order, _I64P)
+        _check(lib().pa_alloc_create(num_blocks, BLOCK_SIZE, order, C.byref(h)), "pa_alloc_create")
+        self._h = h
+        self.num_blocks = num_blocks
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.pa_alloc_destroy(h)
+            self._h = None
+
+    def alloc_seq(self, seq_id, num_tokens):
+        _check(lib().pa_alloc_seq(self._h, seq_id, num_tokens), "pa_alloc_seq")
+
+    def append_slot(self, seq_id):
+        s, a, b = C.c_int64(), C.c_int64(), C.c_int64()
+        _check(lib().pa_append_slot(self._h, seq_id, C.byref(s), C.byref(a), C.byref(b)), "pa_append_slot")
+        return s.value, a.value, b.value
+
+    def append_slots(self, seq_ids):
+        """-> (slots list, [(src, dst), ...])"""
+        n = len(seq_ids)
+        ids = (C.c_uint64 * max(n, 1))(*seq_ids)
+        slots = (C.c_int64 * max(n, 1))()
+        pairs = (C.c_int64 * max(2 * n, 2))()
+        nc = C.c_int32()
+        _check(lib().pa_append_slots(self._h, ids, n, slots, pairs, C.byref(nc)), "pa_append_slots")
+        return list(slots[:n]), [(pairs[2 * i], pairs[2 * i + 1]) for i in range(nc.value)]
+
+    def append_slots_into(self, ids, n, slots, pairs, n_cow):
+        """Zero-copy variant over caller-owned ctypes/numpy buffers (pointers)."""
+        _check(lib().pa_append_slots(self._h, ids, n, slots, pairs, n_cow), "pa_append_slots")
+
+    def fork(self, parent, child):
+        _check(lib().pa_fork(self._h, parent, child), "pa_fork")
+
+    def free_seq(self, seq_id):
+        _check(lib().pa_free_seq(self._h, seq_id), "pa_free_seq")
+
+    def table(self, seq_id):
+        nb, nt = C.c_int32(), C.c_int64()
+        _check(lib().pa_block_table(self._h, seq_id, None, 0, C.byref(nb), C.byref(nt)), "pa_block_table")
+        buf = (C.c_int32 * max(nb.value, 1))()
+        _check(lib().pa_block_table(self._h, seq_id, buf, nb.value, C.byref(nb), C.byref(nt)), "pa_block_table")
+        return list(buf[:nb.value]), nt.value
+
+    def tables(self, seq_ids, cap):
+        """-> (tables int32 [n][cap] as nested lists, context_lens list)"""
+        import numpy as np
+        n = len(seq_ids)
+        ids = (C.c_uint64 * max(n, 1))(*seq_ids)
+        tab = np.empty((max(n, 1), cap), dtype=np.int32)
+        lens = np.empty(max(n, 1), dtype=np.int32)
+        _check(lib().pa_block_tables(self._h, ids, n, tab.ctypes.data_as(_I32P), cap,
+                                     lens.ctypes.data_as(_I32P)), "pa_block_tables")
+        return tab[:n], lens[:n]
+
+    def stats(self):
+        tot, fr = C.c_int32(), C.c_int32()
+        rc = (C.c_int32 * self.num_blocks)()
+        _check(lib().pa_alloc_stats(self._h, C.byref(tot), C.byref(fr), rc), "pa_alloc_stats")
+        return tot.value, fr.value, list(rc)
+
+    def free_list(self):
+        n = C.c_int32()
+        _check(lib().pa_free_list(self._h, None, 0, C.byref(n)), "pa_free_list")
+        buf = (C.c_int32 * max(n.value, 1))()
+        _check(lib().pa_free_list(self._h, buf, n.value, C.byref(n)), "pa_free_list")
+        return list(buf[:n.value])
+
+    def utilization(self):
+        tot, fr, _ = self.stats()
+        return (tot - fr) / tot

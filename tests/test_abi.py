@@ -1,0 +1,91 @@
+"""The C ABI: every declared entry point is exported, and host-side
+validation rejects bad calls before anything is launched (no GPU needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_191_gb300 import ops
+from tests.libfixture import palib  # noqa: F401
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pagedkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(palib):
+    names = declared_functions()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(palib, n), f"{n} not exported by libpagedkv.so"
+    assert set(names) == set(ops.SIGNATURES), "binding and header disagree"
+
+
+def test_version(palib):
+    assert palib.pa_version() == 100
+
+
+def _desc(**kw):
+    d = dict(num_blocks=8, num_kv_heads=2, head_dim=128, block_size=16, kv_dtype=ops.F16)
+    d.update(kw)
+    return ops.CacheDesc(**d)
+
+
+FAKE = 0x10000  # 16-byte aligned dummy address; never dereferenced on a rejected call
+
+
+def _decode(desc, **kw):
+    a = dict(q=FAKE, q_dtype=ops.F16, k=FAKE, v=FAKE, ks=None, vs=None, bt=FAKE, maxb=4, cl=FAKE,
+             maxl=64, B=2, Hq=4, scale=0.1, out=FAKE, odt=ops.F16, ws=None, wsb=0, split=0)
+    a.update(kw)
+    lib = ops.lib()
+    return lib.pa_decode(a["q"], a["q_dtype"], a["k"], a["v"], a["ks"], a["vs"], a["bt"], a["maxb"],
+                         a["cl"], a["maxl"], a["B"], a["Hq"], a["scale"], a["out"], a["odt"],
+                         C.byref(desc), a["ws"], a["wsb"], a["split"], None)
+
+
+@pytest.mark.parametrize("desc_kw,call_kw,status", [
+    ({"block_size": 32}, {}, ops.PA_ERR_UNSUPPORTED),
+    ({"head_dim": 96}, {}, ops.PA_ERR_UNSUPPORTED),
+    ({"kv_dtype": 7}, {}, ops.PA_ERR_INVALID),
+    ({"kv_dtype": ops.FP8_E4M3, "head_dim": 64}, {}, ops.PA_ERR_UNSUPPORTED),
+    ({}, {"Hq": 3}, ops.PA_ERR_INVALID),                 # not a multiple of Hkv
+    ({}, {"Hq": 32}, ops.PA_ERR_UNSUPPORTED),            # group of 16 > 8
+    ({}, {"q": None}, ops.PA_ERR_INVALID),
+    ({}, {"out": FAKE + 4}, ops.PA_ERR_INVALID),         # misaligned
+    ({}, {"q_dtype": ops.BF16}, ops.PA_ERR_INVALID),     # q dtype != cache dtype
+    ({}, {"odt": ops.BF16}, ops.PA_ERR_INVALID),
+    ({}, {"scale": float("nan")}, ops.PA_ERR_INVALID),
+    ({}, {"maxl": 4096, "split": 256}, ops.PA_ERR_INVALID),  # needs a workspace
+    ({}, {"maxl": 4096, "split": 24}, ops.PA_ERR_INVALID),   # not a multiple of 16
+    ({"kv_dtype": ops.FP8_E4M3}, {}, ops.PA_ERR_INVALID),    # FP8 without scales
+    ({}, {"ks": FAKE}, ops.PA_ERR_INVALID),                  # scales on a 16-bit cache
+])
+def test_decode_rejects_bad_arguments(palib, desc_kw, call_kw, status):
+    assert _decode(_desc(**desc_kw), **call_kw) == status
+    assert palib.pa_last_error()
+
+
+def test_decode_workspace_size_is_zero_for_one_partition(palib):
+    d = _desc()
+    assert palib.pa_decode_workspace_size(4, 4, 256, C.byref(d), 256) == 0
+    ws = palib.pa_decode_workspace_size(4, 4, 1000, C.byref(d), 256)
+    # 4 partitions of 256 tokens: o [B*Hq*4*128] f32 + m, l [B*Hq*4] f32
+    assert ws >= 4 * 4 * 4 * (128 + 2) * 4 and ws % 256 == 0
+
+
+def test_cache_write_and_copy_reject_bad_arguments(palib):
+    d = _desc()
+    lib = ops.lib()
+    assert lib.pa_cache_write(FAKE, FAKE, ops.BF16, FAKE, 3, FAKE, FAKE, None, None, C.byref(d), None) == ops.PA_ERR_INVALID
+    assert lib.pa_cache_write(FAKE, None, ops.F16, FAKE, 3, FAKE, FAKE, None, None, C.byref(d), None) == ops.PA_ERR_INVALID
+    assert lib.pa_cache_write(FAKE, FAKE, ops.F16, FAKE, 0, FAKE, FAKE, None, None, C.byref(d), None) == ops.PA_OK
+    assert lib.pa_copy_blocks(FAKE, FAKE, None, None, FAKE, -1, C.byref(d), None) == ops.PA_ERR_INVALID
+    assert lib.pa_copy_blocks(FAKE, FAKE, None, None, FAKE, 0, C.byref(d), None) == ops.PA_OK
+    d8 = _desc(kv_dtype=ops.FP8_E4M3)
+    assert lib.pa_copy_blocks(FAKE, FAKE, None, None, FAKE, 2, C.byref(d8), None) == ops.PA_ERR_INVALID

@@ -1,0 +1,236 @@
+"""GPU parity of pa_decode against the float64 oracle.
+
+Tolerances: max-abs 2e-3 for f16/bf16 caches and 2e-2 for FP8 caches, judged
+on float32 outputs (a bf16 output alone carries up to 2^-9 relative rounding,
+which exceeds 2e-3 near |o| = 1); the 16-bit outputs are checked within the
+tolerance plus half an ulp of the output dtype.  Small ragged cases are
+compared element by element; the full-size workloads on sampled
+(sequence, head) rows in the same launch configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle.attention import paged_decode
+from oracle.cache_ops import cache_write as oracle_cache_write
+from paged_kv_cache_191_gb300 import ops, workloads as W
+from tests.gpu_util import TOL, np_exact, half_ulp, assert_close, requires_cuda
+
+pytestmark = [pytest.mark.gpu, requires_cuda]
+DEV = "cuda"
+
+
+def gpu_decode(w, out_dtype=torch.float32, split_tokens=0, tables=None, lens=None, pools=None,
+               scales=(None, None), max_len=None):
+    tables = w.block_tables if tables is None else tables
+    lens = w.context_lens if lens is None else lens
+    kp, vp = (w.k_pool, w.v_pool) if pools is None else pools
+    q = w.q.to(DEV)
+    kc, vc = kp.to(DEV), vp.to(DEV)
+    bt = torch.from_numpy(np.ascontiguousarray(tables, dtype=np.int32)).to(DEV)
+    cl = torch.from_numpy(np.ascontiguousarray(lens, dtype=np.int32)).to(DEV)
+    ks = scales[0].to(DEV) if scales[0] is not None else None
+    vs = scales[1].to(DEV) if scales[1] is not None else None
+    ml = int(max(lens)) if max_len is None else max_len
+    out = ops.decode(q, kc, vc, bt, cl, ml, w.scale, out_dtype=out_dtype, k_scale=ks, v_scale=vs,
+                     split_tokens=split_tokens)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def oracle(w, heads=None, tables=None, lens=None, pools=None, scales=(None, None)):
+    tables = w.block_tables if tables is None else tables
+    lens = w.context_lens if lens is None else lens
+    kp, vp = (w.k_pool, w.v_pool) if pools is None else pools
+    return paged_decode(np_exact(w.q), np_exact(kp), np_exact(vp), tables, lens, w.scale,
+                        k_scale=None if scales[0] is None else np_exact(scales[0]),
+                        v_scale=None if scales[1] is None else np_exact(scales[1]), heads=heads)
+
+
+def check_out_dtype(w, ref, split_tokens=0, **kw):
+    """The 16-bit output: within tol + half an ulp of the output dtype."""
+    out = gpu_decode(w, out_dtype=w.q.dtype, split_tokens=split_tokens, **kw).float().numpy()
+    tol = TOL[w.kv_dtype]
+    err = np.abs(out - ref)
+    assert np.all(err <= tol + half_ulp(ref, w.q.dtype)), float(err.max())
+
+
+@pytest.fixture(autouse=True)
+def no_device_errors():
+    ops.device_errors(clear=True)
+    yield
+    assert ops.device_errors(clear=True) == 0, "kernel flagged a device error"
+
+
+def test_tiny_workload():
+    w = W.config_tiny()
+    ref = oracle(w)
+    assert_close(gpu_decode(w).numpy(), ref, TOL["f16"], "tiny f32 out")
+    check_out_dtype(w, ref)
+
+
+SHAPES = [  # Hq, Hkv, D, kv dtype
+    (4, 4, 64, "f16"), (8, 2, 128, "f16"), (8, 1, 128, "bf16"), (64, 8, 128, "bf16"),
+    (32, 8, 128, "f16"), (2, 2, 128, "f16"), (16, 2, 64, "bf16"), (3, 1, 128, "f16"),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dt", SHAPES)
+@pytest.mark.parametrize("split", [0, 16, 64, 256])
+def test_random_ragged(Hq, Hkv, D, dt, split):
+    w = W.random_small(300 + Hq * 7 + Hkv + D, B=6, Hq=Hq, Hkv=Hkv, D=D, kv_dtype=dt, max_len=700)
+    ref = oracle(w)
+    assert_close(gpu_decode(w, split_tokens=split).numpy(), ref, TOL[dt], f"{Hq}/{Hkv}/{D}/{dt}/s{split}")
+    if split == 0:
+        check_out_dtype(w, ref)
+
+
+EDGE_LENS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 255, 256, 257, 511, 512, 513, 1000, 1024]
+
+
+@pytest.mark.parametrize("dt,Hq,Hkv", [("f16", 4, 4), ("bf16", 16, 2)])
+@pytest.mark.parametrize("split", [0, 256])
+def test_edge_lengths(dt, Hq, Hkv, split):
+    w = W.make_decode("edge", 77, len(EDGE_LENS), Hq, Hkv, 128, dt, EDGE_LENS, pool_factor=1.1)
+    ref = oracle(w)
+    out = gpu_decode(w, split_tokens=split).numpy()
+    assert_close(out, ref, TOL[dt], "edge lengths")
+    assert not out[0].any(), "empty context must give a zero row"
+
+
+def test_one_token_context_returns_v_exactly():
+    w = W.make_decode("one", 5, 3, 8, 2, 128, "f16", [1, 1, 1])
+    out = gpu_decode(w).numpy()
+    for b in range(3):
+        blk = w.block_tables[b, 0]
+        for h in range(8):
+            assert np.array_equal(out[b, h], np_exact(w.v_pool)[blk, h // 4, 0].astype(np.float32))
+
+
+def test_physical_relabelling_is_bit_identical():
+    w = W.random_small(41, B=5, Hq=8, Hkv=2, D=128, kv_dtype="bf16", max_len=900)
+    rng = np.random.Generator(np.random.PCG64(2))
+    pi = rng.permutation(w.num_blocks)
+    kp = torch.empty_like(w.k_pool)
+    vp = torch.empty_like(w.v_pool)
+    kp[torch.from_numpy(pi)] = w.k_pool
+    vp[torch.from_numpy(pi)] = w.v_pool
+    tab2 = np.where(w.block_tables >= 0, pi[np.maximum(w.block_tables, 0)], -1)
+    a = gpu_decode(w).numpy()
+    b = gpu_decode(w, tables=tab2, pools=(kp, vp)).numpy()
+    assert np.array_equal(a, b)
+
+
+def test_split_invariance():
+    w = W.random_small(42, B=4, Hq=16, Hkv=2, D=128, kv_dtype="f16", max_len=3000, min_len=1500)
+    a = gpu_decode(w, split_tokens=16).numpy()
+    b = gpu_decode(w, split_tokens=1024).numpy()
+    c = gpu_decode(w).numpy()
+    assert np.abs(a - b).max() <= 1e-5 and np.abs(a - c).max() <= 1e-5
+
+
+def test_constant_values_give_constant_output():
+    w = W.random_small(43, B=4, Hq=8, Hkv=8, D=64, kv_dtype="f16", max_len=600)
+    ones = torch.full_like(w.v_pool, 1.5)
+    out = gpu_decode(w, pools=(w.k_pool, ones)).numpy()
+    live = w.context_lens > 0
+    assert np.abs(out[live] - 1.5).max() <= 1e-6
+
+
+def test_bad_block_id_is_flagged_not_faulted():
+    w = W.random_small(44, B=2, Hq=4, Hkv=4, D=64, kv_dtype="f16", max_len=60, min_len=40)
+    tab = w.block_tables.copy()
+    tab[1, 1] = w.num_blocks + 5
+    gpu_decode(w, tables=tab)
+    assert ops.device_errors(clear=True) & ops.DEVERR_BLOCK_RANGE
+    lens = w.context_lens.copy()
+    lens[0] = 10 ** 6
+    gpu_decode(w, lens=lens, max_len=int(w.context_lens.max()))
+    assert ops.device_errors(clear=True) & ops.DEVERR_CONTEXT_LEN
+
+
+# ---- FP8 E4M3 caches ---------------------------------------------------------------
+def fp8_pool_gpu(w):
+    """Quantise the whole f16 pool through pa_cache_write (one token per slot)."""
+    N, H, _, D = w.k_pool.shape
+    kin = w.k_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(DEV)
+    vin = w.v_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(DEV)
+    slots = torch.arange(N * 16, dtype=torch.int64, device=DEV)
+    kc = torch.zeros((N, H, 16, D), dtype=torch.uint8, device=DEV)
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros((N, 16), dtype=torch.float32, device=DEV)
+    vs = torch.zeros_like(ks)
+    ops.cache_write(kin, vin, slots, kc, vc, ks, vs)
+    torch.cuda.synchronize()
+    return kc.cpu(), vc.cpu(), ks.cpu(), vs.cpu()
+
+
+def fp8_pool_oracle(w, blocks=None):
+    """The oracle's own quantisation of the listed blocks (all by default)."""
+    N, H, _, D = w.k_pool.shape
+    blocks = np.arange(N) if blocks is None else np.asarray(sorted(set(blocks)))
+    slots = (blocks[:, None] * 16 + np.arange(16)[None, :]).reshape(-1)
+    kin = np_exact(w.k_pool[torch.from_numpy(blocks)]).transpose(0, 2, 1, 3).reshape(-1, H, D)
+    vin = np_exact(w.v_pool[torch.from_numpy(blocks)]).transpose(0, 2, 1, 3).reshape(-1, H, D)
+    kc = np.zeros((N, H, 16, D), np.uint8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((N, 16), np.float32)
+    vs = np.zeros_like(ks)
+    return oracle_cache_write(kin, vin, slots, kc, vc, ks, vs), blocks
+
+
+@pytest.mark.parametrize("qdt", ["f16", "bf16"])
+@pytest.mark.parametrize("split", [0, 64])
+def test_fp8_small(qdt, split):
+    w = W.random_small(51, B=5, Hq=16, Hkv=4, D=128, kv_dtype="fp8", max_len=800)
+    if qdt == "bf16":
+        w.q = w.q.to(torch.bfloat16)
+    kc, vc, ks, vs = fp8_pool_gpu(w)
+    (okc, ovc, oks, ovs), _ = fp8_pool_oracle(w)
+    assert np.array_equal(kc.numpy(), okc) and np.array_equal(vc.numpy(), ovc)
+    assert np.array_equal(ks.numpy(), oks) and np.array_equal(vs.numpy(), ovs)
+    ref = paged_decode(np_exact(w.q), okc, ovc, w.block_tables, w.context_lens, w.scale, oks, ovs)
+    got = gpu_decode(w, split_tokens=split, pools=(kc, vc), scales=(ks, vs)).numpy()
+    assert_close(got, ref, TOL["fp8"], f"fp8 q={qdt}")
+    # against the unquantised cache: reported, loosely bounded at small contexts
+    ref16 = oracle(w)
+    assert np.abs(got - ref16).max() < 0.25
+
+
+# ---- full-size workloads, sampled rows ------------------------------------------------
+def sample_heads(w, n, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    bs = rng.choice(w.B, size=min(n, w.B), replace=False)
+    return [(int(b), int(rng.integers(w.Hq))) for b in bs] + [(int(bs[0]), w.Hq - 1)]
+
+
+def check_sampled(w, got, heads, ref, tol):
+    for b, h in heads:
+        assert_close(got[b, h], ref[b, h], tol, f"{w.name} b={b} h={h}")
+
+
+@pytest.mark.parametrize("cfg", ["llama7b_b32", "gqa70b_b64", "longctx_b8_f16"])
+def test_full_size_sampled(cfg):
+    w = W.CONFIGS[cfg]()
+    got = gpu_decode(w).numpy()
+    heads = sample_heads(w, 12, 7)
+    ref = oracle(w, heads=heads)
+    check_sampled(w, got, heads, ref, TOL[w.kv_dtype])
+    assert np.all(np.isfinite(got))
+
+
+def test_full_size_fp8_longctx_sampled():
+    w = W.config_longctx("fp8")
+    kc, vc, ks, vs = fp8_pool_gpu(w)
+    heads = sample_heads(w, 3, 9)
+    seqs = sorted({b for b, _ in heads})
+    blocks = np.concatenate([w.block_tables[b][w.block_tables[b] >= 0] for b in seqs])
+    (okc, ovc, oks, ovs), used = fp8_pool_oracle(w, blocks)
+    assert np.array_equal(kc.numpy()[used], okc[used]) and np.array_equal(vc.numpy()[used], ovc[used])
+    assert np.array_equal(ks.numpy()[used], oks[used]) and np.array_equal(vs.numpy()[used], ovs[used])
+    got = gpu_decode(w, pools=(kc, vc), scales=(ks, vs)).numpy()
+    ref = paged_decode(np_exact(w.q), okc, ovc, w.block_tables, w.context_lens, w.scale, oks, ovs,
+                       heads=heads)
+    check_sampled(w, got, heads, ref, TOL["fp8"])
+    ref16 = oracle(w, heads=heads)
+    check_sampled(w, got, heads, ref16, TOL["fp8"])
