@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(kWriteThreads)
     cache_write_16(const void* __restrict__ k, const void* __restrict__ v,
                    const int64_t* __restrict__ slots, void* __restrict__ kc, void* __restrict__ vc,
                    int Hkv, int D, int num_blocks) {
+  dev::grid_dependency_wait();
+  dev::grid_launch_dependents();  // a dependent decode waits for our completion itself
   const int t = blockIdx.x;
   const int64_t slot = slots[t];
   if (slot < 0) return;
@@ -114,6 +116,8 @@ __global__ void __launch_bounds__(kWriteThreads)
                     uint8_t* __restrict__ vc, float* __restrict__ ks, float* __restrict__ vs,
                     int Hkv, int D, int num_blocks) {
   __shared__ float red[33];
+  dev::grid_dependency_wait();
+  dev::grid_launch_dependents();
   const int t = blockIdx.x;
   const int64_t slot = slots[t];
   if (slot < 0) return;

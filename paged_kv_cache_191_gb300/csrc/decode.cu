@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(kNW * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv, p = blockIdx.y;
 
+  // Launched as a dependent of the preceding kernel (normally the cache
+  // write): everything below may read what it wrote.
+  dev::grid_dependency_wait();
   const int L = checked_len(a, b, threadIdx.x == 0 && p == 0);
   const int nblk = (L + 15) >> 4;
   const int j0 = p * a.bpp;
@@ -357,6 +360,7 @@ __global__ void __launch_bounds__(kNW * 32)
   }
 
   // ---- merge the warps' partial softmax states ----------------------------------
+  dev::grid_launch_dependents();  // the merge kernel may start being scheduled
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(FULL, l0, off);
@@ -422,6 +426,7 @@ __global__ void __launch_bounds__(kNW * 32)
 template <typename QT, int D>
 __global__ void __launch_bounds__(D) decode_reduce(const DecodeArgs a) {
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  dev::grid_dependency_wait();  // partials of decode_main are complete and visible
   const int L = checked_len(a, b, false);
   const int nblk = (L + 15) >> 4;
   const int nparts = (nblk + a.bpp - 1) / a.bpp;
@@ -520,10 +525,13 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   if (attr_err != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(attr_err));
 
   const dim3 grid(static_cast<unsigned>(l.B * l.Hkv), static_cast<unsigned>(l.plan.max_parts));
-  decode_main<KT, QT, D><<<grid, kNW * 32, TL::SMEM, stream>>>(tmK, tmV, a);
-  if (l.plan.max_parts > 1)
-    decode_reduce<QT, D><<<dim3(static_cast<unsigned>(l.Hq), static_cast<unsigned>(l.B)), D, 0, stream>>>(a);
-  const cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(decode_main<KT, QT, D>, grid, dim3(kNW * 32), TL::SMEM, stream,
+                                   tmK, tmV, a);
+  if (e == cudaSuccess && l.plan.max_parts > 1)
+    e = launch_dependent(decode_reduce<QT, D>,
+                         dim3(static_cast<unsigned>(l.Hq), static_cast<unsigned>(l.B)), dim3(D), 0,
+                         stream, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode launch: %s", cudaGetErrorString(e));
   return PA_OK;
 }

@@ -4,6 +4,10 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
+#include <cuda_runtime.h>
+
 #include "../../include/pagedkv.h"
 
 namespace pa {
@@ -64,6 +68,25 @@ pa_status launch_cache_write(const void* k, const void* v, int32_t in_dtype,
 pa_status launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                              const int64_t* pairs, int64_t n, const pa_cache_desc* d,
                              void* stream);
+
+// Launch `kernel` on `stream` as a programmatic dependent of the previous
+// kernel in the stream: it may be scheduled while that kernel drains, and
+// must call griddepcontrol.wait before touching memory the predecessor wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Per-translation-unit device error words, OR-ed by pa_device_errors.
 pa_status read_errors_decode(uint32_t* flags, bool clear);
