@@ -159,6 +159,39 @@ pa_status pa_decode(const void* q, int32_t q_dtype,
                     int32_t split_tokens, void* stream);
 
 /*
+ * pa_decode_static_ws -- pa_decode that allocates nothing.  The pages have no
+ * counterpart: this entry point exists for callers of this library that
+ * cannot allocate device memory when they decode -- code running as a plugin
+ * inside an engine whose allocator owns the whole device and offers no
+ * scratch hook, or a latency-critical loop where cudaMalloc/cudaFree would add
+ * latency and device-wide synchronisation.
+ *
+ * Arguments and results are those of pa_decode without workspace /
+ * workspace_bytes: the split-K partials live in one static device array of
+ * PA_STATIC_WS_BYTES compiled into the library.  The caller still passes
+ * inputs and outputs.
+ * - A shape whose pa_decode_workspace_size exceeds PA_STATIC_WS_BYTES returns
+ *   PA_ERR_INVALID and launches nothing.
+ * - The first call made with a device current sets the array up on that
+ *   device (one cudaGetSymbolAddress); make it before any stream capture.
+ *   The array stays resident on that device until the process exits.
+ * - All calls on a device share the array, which keeps the last call's
+ *   contents; calls whose kernels overlap on the GPU race on it, so
+ *   serialise them (one stream, or events).
+ * - No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define PA_STATIC_WS_BYTES (32u * 1024u * 1024u)
+pa_status pa_decode_static_ws(const void* q, int32_t q_dtype,
+                              const void* k_cache, const void* v_cache,
+                              const float* k_scale, const float* v_scale,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t max_context_len,
+                              int32_t B, int32_t num_q_heads, float scale,
+                              void* out, int32_t out_dtype,
+                              const pa_cache_desc* desc,
+                              int32_t split_tokens, void* stream);
+
+/*
  * pa_copy_blocks -- copy-on-write block copies.
  * [LLM-INF] 2.2 and [KV-CB] 4.2: before a shared block is written, its
  * contents are copied to a private block.  For each pair (src, dst) in

@@ -55,6 +55,8 @@ SIGNATURES = {
     "pa_decode_workspace_size": (C.c_size_t, [_I32, _I32, _I32, C.POINTER(CacheDesc), _I32]),
     "pa_decode": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F, _P, _I32,
                             C.POINTER(CacheDesc), _P, C.c_size_t, _I32, _P]),
+    "pa_decode_static_ws": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F, _P,
+                                      _I32, C.POINTER(CacheDesc), _I32, _P]),
     "pa_copy_blocks": (C.c_int, [_P, _P, _P, _P, _P, _I64, C.POINTER(CacheDesc), _P]),
     "pa_device_errors": (C.c_int, [C.POINTER(C.c_uint32), _I32]),
     "pa_alloc_create": (C.c_int, [_I32, _I32, _I64P, C.POINTER(_P)]),
