@@ -182,6 +182,49 @@ class ClockSampler:
                 "samples": len(inside), "window": window}
 
 
+# ---- thin CUDA driver access for the timed loop (copies and events) --------------
+class Driver:
+    """cuMemcpyHtoDAsync / cuEvent* through ctypes: a few microseconds less host
+    time per step than the equivalent torch calls, so the loop stays ahead of
+    the GPU."""
+
+    def __init__(self):
+        cu = C.CDLL("libcuda.so.1")
+        cu.cuMemcpyHtoDAsync_v2.argtypes = [C.c_uint64, C.c_void_p, C.c_size_t, C.c_void_p]
+        cu.cuEventCreate.argtypes = [C.POINTER(C.c_void_p), C.c_uint]
+        cu.cuEventRecord.argtypes = [C.c_void_p, C.c_void_p]
+        cu.cuEventSynchronize.argtypes = [C.c_void_p]
+        cu.cuEventElapsedTime.argtypes = [C.POINTER(C.c_float), C.c_void_p, C.c_void_p]
+        cu.cuStreamWaitEvent.argtypes = [C.c_void_p, C.c_void_p, C.c_uint]
+        self.cu = cu
+
+    def _ok(self, rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what} failed with CUresult {rc}")
+
+    def event(self, timing=False):
+        ev = C.c_void_p()
+        self._ok(self.cu.cuEventCreate(C.byref(ev), 0 if timing else 2), "cuEventCreate")
+        return ev
+
+    def record(self, ev, stream):
+        self._ok(self.cu.cuEventRecord(ev, stream), "cuEventRecord")
+
+    def sync(self, ev):
+        self._ok(self.cu.cuEventSynchronize(ev), "cuEventSynchronize")
+
+    def elapsed_ms(self, a, b):
+        ms = C.c_float()
+        self._ok(self.cu.cuEventElapsedTime(C.byref(ms), a, b), "cuEventElapsedTime")
+        return ms.value
+
+    def wait(self, stream, ev):
+        self._ok(self.cu.cuStreamWaitEvent(stream, ev, 0), "cuStreamWaitEvent")
+
+    def h2d(self, dst_ptr, src_ptr, nbytes, stream):
+        self._ok(self.cu.cuMemcpyHtoDAsync_v2(dst_ptr, src_ptr, nbytes, stream), "cuMemcpyHtoDAsync")
+
+
 # ---- workloads ------------------------------------------------------------------
 def load_workload(name):
     from paged_kv_cache_191_gb300 import workloads as W
@@ -252,17 +295,26 @@ class DecodeStep:
         self.meta_bytes = self.B * 8 + self.B * 4 + self.B * self.cap * 4
         self.meta_host = [torch.empty(self.meta_bytes, dtype=torch.uint8).pin_memory()
                           for _ in range(RING)]
-        self.meta_dev = torch.empty(self.meta_bytes, dtype=torch.uint8, device=device)
-        self.slots_dev = self.meta_dev[: self.B * 8].view(torch.int64)
-        self.lens_dev = self.meta_dev[self.B * 8: self.B * 12].view(torch.int32)
-        self.tables_dev = self.meta_dev[self.B * 12:].view(torch.int32).view(self.B, self.cap)
-        self.ring_ev = [None] * RING
+        # two device copies of the meta buffer: step i+1's upload (on a copy
+        # stream) overlaps step i's kernels
+        self.meta_devs = [torch.empty(self.meta_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+        self.use_meta(0)
+        self.drv = Driver()
+        self.ring_ev = [self.drv.event() for _ in range(RING)]
+        self.ring_used = [False] * RING
         self.ring = 0
         self.ids_c = (C.c_uint64 * self.B)(*self.ids)
         self.pairs_c = (C.c_int64 * (2 * self.B))()
         self.ncow = C.c_int32()
         self.cur_lens = self.lens0.copy() - 1
         self.steps_since_reset = 0
+        self.blocked_s = 0.0
+
+    def use_meta(self, i):
+        self.meta_dev = self.meta_devs[i]
+        self.slots_dev = self.meta_dev[: self.B * 8].view(self.torch.int64)
+        self.lens_dev = self.meta_dev[self.B * 8: self.B * 12].view(self.torch.int32)
+        self.tables_dev = self.meta_dev[self.B * 12:].view(self.torch.int32).view(self.B, self.cap)
 
     def _admit(self):
         for b in self.ids:
@@ -278,8 +330,10 @@ class DecodeStep:
             self.cur_lens = self.lens0.copy() - 1
             self.steps_since_reset = 0
         buf = self.meta_host[self.ring]
-        if self.ring_ev[self.ring] is not None:
-            self.ring_ev[self.ring].synchronize()
+        if self.ring_used[self.ring]:
+            t0 = time.perf_counter()
+            self.drv.sync(self.ring_ev[self.ring])
+            self.blocked_s += time.perf_counter() - t0
         base = buf.data_ptr()
         slots_p = C.cast(base, C.POINTER(C.c_int64))
         lens_p = C.cast(base + self.B * 8, C.POINTER(C.c_int32))
@@ -292,43 +346,73 @@ class DecodeStep:
         self.steps_since_reset += 1
         return buf
 
-    def enqueue(self, buf, stream, ev_pair=None):
-        """a1 H2D, a2 cache write, a4+a5 decode on `stream`."""
-        torch, L = self.torch, self.L
-        self.meta_dev.copy_(buf, non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record(stream)
-        self.ring_ev[self.ring] = ev
-        self.ring = (self.ring + 1) % RING
+    def prebuild(self, stream):
+        """ctypes argument tuples of this step's C calls, per device meta buffer."""
+        ops, fp8 = self.ops, self.fp8
         sp = C.c_void_p(stream.cuda_stream)
-        self.ops._check(L.pa_cache_write(self.new_k.data_ptr(), self.new_v.data_ptr(),
-                                         self.ops._TORCH_DT[self.new_k.dtype], self.slots_dev.data_ptr(),
-                                         self.B, self.kc.data_ptr(), self.vc.data_ptr(),
-                                         self.ks.data_ptr() if self.fp8 else None,
-                                         self.vs.data_ptr() if self.fp8 else None,
-                                         C.byref(self.desc), sp), "pa_cache_write")
+        self.copy_stream = self.torch.cuda.Stream(device=self.dev)
+        self.cp = C.c_void_p(self.copy_stream.cuda_stream)
+        ks = C.c_void_p(self.ks.data_ptr()) if fp8 else None
+        vs = C.c_void_p(self.vs.data_ptr()) if fp8 else None
+        self.sp = sp
+        self.write_args, self.decode_args = [], []
+        for i in range(2):
+            self.use_meta(i)
+            self.write_args.append((C.c_void_p(self.new_k.data_ptr()), C.c_void_p(self.new_v.data_ptr()),
+                                    ops._TORCH_DT[self.new_k.dtype], C.c_void_p(self.slots_dev.data_ptr()),
+                                    self.B, C.c_void_p(self.kc.data_ptr()), C.c_void_p(self.vc.data_ptr()),
+                                    ks, vs, C.byref(self.desc), sp))
+            self.decode_args.append((C.c_void_p(self.q.data_ptr()), ops._TORCH_DT[self.q.dtype],
+                                     C.c_void_p(self.kc.data_ptr()), C.c_void_p(self.vc.data_ptr()), ks, vs,
+                                     C.c_void_p(self.tables_dev.data_ptr()), self.cap,
+                                     C.c_void_p(self.lens_dev.data_ptr()), self.max_len, self.B, self.Hq,
+                                     C.c_float(self.w.scale), C.c_void_p(self.out.data_ptr()),
+                                     ops._TORCH_DT[self.out.dtype], C.byref(self.desc),
+                                     C.c_void_p(self.ws.data_ptr()), self.ws.numel(), self.split, sp))
+        self.use_meta(0)
+        self.dbuf = 0
+        self.copy_done = [self.drv.event() for _ in range(2)]
+        self.used_done = [self.drv.event() for _ in range(2)]
+        self.used_rec = [False, False]
+
+    def enqueue(self, buf, ev_pair=None):
+        """a1 H2D (copy stream), a2 cache write, a4+a5 decode (compute stream)."""
+        L, drv, sp, cp, i = self.L, self.drv, self.sp, self.cp, self.dbuf
+        if self.used_rec[i]:            # the kernels that read this device buffer are done
+            drv.wait(cp, self.used_done[i])
+        drv.h2d(self.meta_devs[i].data_ptr(), buf.data_ptr(), self.meta_bytes, cp)
+        drv.record(self.ring_ev[self.ring], cp)
+        drv.record(self.copy_done[i], cp)
+        self.ring_used[self.ring] = True
+        self.ring = (self.ring + 1) % RING
+        drv.wait(sp, self.copy_done[i])
+        st = L.pa_cache_write(*self.write_args[i])
+        if st:
+            self.ops._check(st, "pa_cache_write")
         if ev_pair is not None:
-            ev_pair[0].record(stream)
-        self.ops._check(L.pa_decode(self.q.data_ptr(), self.ops._TORCH_DT[self.q.dtype],
-                                    self.kc.data_ptr(), self.vc.data_ptr(),
-                                    self.ks.data_ptr() if self.fp8 else None,
-                                    self.vs.data_ptr() if self.fp8 else None,
-                                    self.tables_dev.data_ptr(), self.cap, self.lens_dev.data_ptr(),
-                                    self.max_len, self.B, self.Hq, C.c_float(self.w.scale),
-                                    self.out.data_ptr(), self.ops._TORCH_DT[self.out.dtype],
-                                    C.byref(self.desc), self.ws.data_ptr(), self.ws.numel(),
-                                    self.split, sp), "pa_decode")
+            drv.record(ev_pair[0], sp)
+        st = L.pa_decode(*self.decode_args[i])
+        if st:
+            self.ops._check(st, "pa_decode")
         if ev_pair is not None:
-            ev_pair[1].record(stream)
+            drv.record(ev_pair[1], sp)
+        drv.record(self.used_done[i], sp)
+        self.used_rec[i] = True
+        self.dbuf ^= 1
+
+    def _bytes_of(self, lens):
+        e = 1 if self.fp8 else 2
+        qe = self.q.element_size()
+        dec = decode_bytes(lens, self.Hq, self.Hkv, self.D, e, qe, qe)
+        write = 2 * self.B * self.Hkv * self.D * (qe + e) + (2 * self.B * 4 if self.fp8 else 0) + self.B * 8
+        return dec, dec + write + self.meta_bytes
 
     def step_bytes(self):
         """(decode bytes, whole-step bytes) of the step just prepared."""
-        e = 1 if self.fp8 else 2
-        qe = self.q.element_size()
-        dec = decode_bytes(self.cur_lens, self.Hq, self.Hkv, self.D, e, qe, qe)
-        write = 2 * self.B * self.Hkv * self.D * (qe + e) + (2 * self.B * 4 if self.fp8 else 0) + self.B * 8
-        meta = self.meta_bytes
-        return dec, dec + write + meta
+        k = self.steps_since_reset  # 1..RESET_EVERY: lengths are lens0 - 1 + k
+        if not hasattr(self, "_bytes_table"):
+            self._bytes_table = [self._bytes_of(self.lens0 - 1 + j) for j in range(RESET_EVERY + 1)]
+        return self._bytes_table[k]
 
     def launches_per_step(self):
         ws = self.ws_bytes
@@ -343,28 +427,29 @@ def run_ours(args, rank, world, local_rank):
     st = DecodeStep(w, args.split, args.steps + args.warmup, dev)
     stream = torch.cuda.Stream(device=dev)
     total_steps = args.warmup + args.steps
-    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
+    st.prebuild(stream)
+    dec_events = [(st.drv.event(True), st.drv.event(True)) for _ in range(args.steps)]
+    t_start, t_end = st.drv.event(True), st.drv.event(True)
     clocks = ClockSampler(local_rank)
     clocks.start()
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            st.enqueue(st.host_prepare(), stream)
+            st.enqueue(st.host_prepare())
         stream.synchronize()
         barrier(world)
         torch.cuda.synchronize()
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
         dec_b = step_b = 0
+        st.blocked_s = 0.0
         wall0 = time.time()
-        t_start.record(stream)
+        st.drv.record(t_start, st.sp)
         for i in range(args.steps):
             buf = st.host_prepare()
             d, s = st.step_bytes()
             dec_b += d
             step_b += s
-            st.enqueue(buf, stream, dec_events[i])
-        t_end.record(stream)
+            st.enqueue(buf, dec_events[i])
+        st.drv.record(t_end, st.sp)
+        host_done = time.time()
         stream.synchronize()
         wall1 = time.time()
     torch.cuda.synchronize()
@@ -373,8 +458,8 @@ def run_ours(args, rank, world, local_rank):
     errs = st.ops.device_errors(clear=True)
     if errs:
         raise RuntimeError(f"device error flags {errs:#x} during the benchmark")
-    local_s = t_start.elapsed_time(t_end) / 1e3
-    dec_ms = sum(a.elapsed_time(b) for a, b in dec_events) / args.steps
+    local_s = st.drv.elapsed_ms(t_start, t_end) / 1e3
+    dec_ms = sum(st.drv.elapsed_ms(a, b) for a, b in dec_events) / args.steps
     max_s, tot_bytes = aggregate(local_s, float(step_b), world)
     _, tot_tokens = aggregate(local_s, float(st.B * args.steps), world)
 
@@ -410,6 +495,8 @@ def run_ours(args, rank, world, local_rank):
             "parallelism": f"replicas x{world}",
         },
         "tokens_per_s": round(tot_tokens / max_s, 1),
+        "host_us_per_step": {"busy": round((host_done - wall0 - st.blocked_s) * 1e6 / args.steps, 2),
+                             "blocked_on_gpu": round(st.blocked_s * 1e6 / args.steps, 2)},
         "kv_gbs_decode_only": round(achieved, 2),
         "pct_of_nominal_8TBs": round(100 * tot_bytes / max_s / 1e9 / NOMINAL_HBM_GBS, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -445,6 +532,7 @@ def run_e2e(st, args, stream):
             buf = st.host_prepare()
             _, s = st.step_bytes()
             total_b += s
+            st.use_meta(0)
             st.meta_dev.copy_(buf, non_blocking=True)
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)

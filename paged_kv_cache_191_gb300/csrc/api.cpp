@@ -56,11 +56,12 @@ pa_status plan_decode(int32_t B, int32_t Hq, int32_t max_context_len, const pa_c
       return fail(PA_ERR_INVALID, "split_tokens must be a multiple of 16 in [16, 1024]");
     bpp = split_tokens / PA_BLOCK_SIZE;
   } else {
-    // 256-token partitions by default; shrink them while the grid would give
-    // fewer than two partitions per SM.
+    // 512-token partitions by default and 1024 for contexts of 8K and more
+    // (fewer partials to merge; one-warp CTAs keep the grid fine-grained);
+    // shrink them while the grid would give fewer than two partitions per SM.
     const int64_t units = static_cast<int64_t>(B) * d->num_kv_heads;
     const int64_t sms = sm_count();
-    bpp = 16;
+    bpp = max_context_len >= 8192 ? 64 : 32;
     while (bpp > 4 && units * ((nblk_max + bpp - 1) / bpp) < 2 * sms) bpp /= 2;
   }
   const int64_t parts = (nblk_max + bpp - 1) / bpp;

@@ -7,28 +7,34 @@
 // K/V tiles from there.
 //
 // Design (GB300):
-// * Work unit = one CTA per (sequence b, kv head g, partition p of
-//   `bpp` 16-token blocks).  All G query heads of kv head g share every K/V
-//   tile, so K/V bytes are read from HBM exactly once per step.
-// * Each (block, kv head) tile is 16 rows x D contiguous elements.  It is
-//   fetched by TMA (cp.async.bulk.tensor, 128-byte swizzle) into a per-warp
-//   ring of shared-memory stages completed by mbarriers; each of the 4 warps
-//   owns blocks w, w+4, w+8, ... of the partition and refills its own stages,
-//   so warps never wait on one another inside the loop.
+// * Work item = (sequence b, kv head g, partition p of `bpp` 16-token
+//   blocks), one single-warp CTA per item (grid: b*Hkv + g, p).  All G query
+//   heads of kv head g share every K/V tile, so K/V bytes are read from HBM
+//   once per step.  Small one-warp CTAs keep many independent load streams per
+//   SM (six or more), which is what hides HBM latency here; an item needs no
+//   block-wide barrier and no cross-warp merge, and an empty grid cell (a
+//   partition past a short sequence's end) costs one warp launch.
+// * The warp streams its item's (block, kv head) tiles -- 16 rows x D,
+//   contiguous -- through a ring of shared-memory stages with TMA
+//   (cp.async.bulk.tensor, 128-byte swizzle) completed by mbarriers.  As soon
+//   as a tile's fragments are in registers the stage is refilled with the
+//   tile NS blocks ahead.
 // * Scores on tensor cores, transposed: S^T[16 tokens x 8 heads] =
 //   K_tile[16 x D] . Q^T[D x 8] with mma.m16n8k16 (A = K from ldmatrix,
-//   B = Q from registers; G < 8 pads the N dimension with zero heads).
-//   Online softmax in fp32 (exp2 with log2e folded into the scale), then
-//   O^T[D x 8] += V^T[D x 16] . P^T[16 x 8] with A = V via ldmatrix.trans and
-//   B = P^T obtained from the score fragment by movmatrix.  bf16 P is split
-//   into hi + lo bf16 parts so its rounding error stays ~2^-17.
+//   B = Q from registers; G < 8 pads N with zero heads).  Online softmax in
+//   fp32 (exp2, log2e folded into the scale), then O^T[D x 8] += V^T[D x 16] .
+//   P^T[16 x 8] with A = V via ldmatrix.trans and B = P^T from the score
+//   fragment by movmatrix.  bf16 P is carried as hi + lo bf16 parts (rounding
+//   error ~2^-17).
 // * FP8 E4M3 caches: codes are converted exactly to f16/bf16 in registers;
 //   the per-token K scale multiplies the score, the per-token V scale
 //   multiplies p before the PV product.
-// * Partitions of one (b, g) are merged by decode_reduce with the usual
-//   log-sum-exp weights; a single-partition sequence is written directly.
+// * A one-partition sequence is written directly; otherwise the partition
+//   writes (o, m, l) and decode_reduce merges the partitions with log-sum-exp
+//   weights, launched as a programmatic dependent.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -39,10 +45,12 @@ namespace {
 
 __device__ uint32_t g_decode_err;
 
-constexpr int kNW = 4;   // warps per CTA
-constexpr int kNSW = 2;  // pipeline stages per warp
-constexpr int kNS = kNW * kNSW;
+#ifndef PA_RING_KB
+#define PA_RING_KB 16  // two 8 KB stages for 16-bit D=128: ~12 CTAs per SM
+#endif
+constexpr int kRingBytes = PA_RING_KB * 1024;  // K/V stage ring of one warp-CTA
 constexpr int kMaxBpp = 64;
+constexpr int kMaxDevices = 64;
 
 struct DecodeArgs {
   const void* q;
@@ -66,8 +74,12 @@ struct Tile {
   static constexpr int BYTES = 16 * ROWB;                          // one (block, head) tile
   static constexpr int NBOX = ROWB / 128;                          // 128-byte swizzle boxes
   static constexpr int BOXE = 128 / static_cast<int>(sizeof(KT));  // elements per box row
-  static constexpr int SMEM = 1024 + kNS * 2 * BYTES + kNS * 128 + kNS * 8 + kMaxBpp * 4;
+  static constexpr int NS = kRingBytes / (2 * BYTES);             // K+V stages in the ring
+  static constexpr int OFF_SC = NS * 2 * BYTES;                    // FP8 scales [NS][32] f32
+  static constexpr int OFF_BAR = OFF_SC + NS * 128;                // full barriers [NS]
+  static constexpr int SMEM = 1024 + OFF_BAR + NS * 8;
   static_assert(ROWB % 128 == 0, "rows must be whole 128-byte swizzle spans");
+  static_assert(NS >= 2, "stage ring too small");
 };
 
 // Byte offset of 16-byte chunk `c` of row `r` inside a swizzled tile.
@@ -90,19 +102,18 @@ template <typename QT>
 __device__ __forceinline__ void store_out(const DecodeArgs& a, size_t idx, float v) {
   if (a.out_f32)
     static_cast<float*>(a.out)[idx] = v;
-  else if constexpr (sizeof(QT) == 2) {
-    if constexpr (std::is_same<QT, __half>::value)
-      static_cast<__half*>(a.out)[idx] = __float2half_rn(v);
-    else
-      static_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(v);
-  }
+  else if constexpr (std::is_same<QT, __half>::value)
+    static_cast<__half*>(a.out)[idx] = __float2half_rn(v);
+  else
+    static_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(v);
 }
 
 template <typename KT, typename QT, int D>
-__global__ void __launch_bounds__(kNW * 32)
+__global__ void __launch_bounds__(32)
     decode_main(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const DecodeArgs a) {
   using TL = Tile<KT, D>;
+  constexpr int NS = TL::NS;
   constexpr bool FP8 = sizeof(KT) == 1;
   constexpr int KSTEPS = D / 16;
   constexpr int MT = D / 16;
@@ -114,80 +125,32 @@ __global__ void __launch_bounds__(kNW * 32)
   const uint32_t raw = dev::smem_addr(smem_raw);
   const uint32_t tiles = (raw + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (tiles - raw);
-  float* s_scale = reinterpret_cast<float*>(base + kNS * 2 * TL::BYTES);  // [kNS][32]
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(base + kNS * 2 * TL::BYTES + kNS * 128);
-  int32_t* s_tab = reinterpret_cast<int32_t*>(s_bar + kNS);
+  float* s_scale = reinterpret_cast<float*>(base + TL::OFF_SC);
+  const uint32_t bar_full = tiles + TL::OFF_BAR;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x;
   const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv, p = blockIdx.y;
 
   // Launched as a dependent of the preceding kernel (normally the cache
   // write): everything below may read what it wrote.
   dev::grid_dependency_wait();
-  const int L = checked_len(a, b, threadIdx.x == 0 && p == 0);
-  const int nblk = (L + 15) >> 4;
   const int j0 = p * a.bpp;
-  if (j0 >= nblk) {
-    if (p == 0)  // empty context: zero rows
-      for (int i = threadIdx.x; i < a.G * D; i += blockDim.x)
-        store_out<QT>(a, (static_cast<size_t>(b) * a.Hq + g * a.G + i / D) * D + i % D, 0.f);
-    return;
-  }
-  const int nb = min(a.bpp, nblk - j0);
-  const int nparts = (nblk + a.bpp - 1) / a.bpp;
-
-  // Block ids of this partition -> shared memory (one coalesced read).
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
-    int pb = a.block_tables[static_cast<size_t>(b) * a.max_blocks + j0 + i];
-    if (pb < 0 || pb >= a.num_blocks) {
-      atomicOr(&g_decode_err, PA_DEVERR_BLOCK_RANGE);
-      pb = 0;  // read a valid block instead; the result is flagged
-    }
-    s_tab[i] = pb;
-  }
-  if (threadIdx.x == 0) {
-    dev::prefetch_tensormap(&tmK);
-    dev::prefetch_tensormap(&tmV);
-    for (int s = 0; s < kNS; ++s) dev::mbar_init(dev::smem_addr(&s_bar[s]), 1);
-    dev::fence_barrier_init();
-  }
-  __syncthreads();
-
-  auto issue = [&](int jj, int s) {
-    const int pb = s_tab[jj];
-    const uint32_t bar = dev::smem_addr(&s_bar[s]);
-    const uint32_t kdst = tiles + s * 2 * TL::BYTES, vdst = kdst + TL::BYTES;
-    dev::mbar_arrive_expect_tx(bar, STAGE_TX);
-#pragma unroll
-    for (int bx = 0; bx < TL::NBOX; ++bx) {
-      dev::tma_load_3d(kdst + bx * 2048, &tmK, bar, bx * TL::BOXE, g * 16, pb);
-      dev::tma_load_3d(vdst + bx * 2048, &tmV, bar, bx * TL::BOXE, g * 16, pb);
-    }
-    if constexpr (FP8) {
-      dev::bulk_load(dev::smem_addr(s_scale + s * 32), a.k_scale + static_cast<size_t>(pb) * 16, 64, bar);
-      dev::bulk_load(dev::smem_addr(s_scale + s * 32 + 16), a.v_scale + static_cast<size_t>(pb) * 16, 64,
-                     bar);
-    }
-  };
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < kNSW; ++i) {
-      const int jj = warp + i * kNW;
-      if (jj < nb) issue(jj, warp * kNSW + i);
-    }
-  }
-
+  // The length, this partition's block ids (one or two per lane, read up to
+  // the partition size and the row end before the length is known) and Q are
+  // independent loads, so they share one memory round trip.
+  const int32_t* row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + j0;
+  const int row_left = a.max_blocks - j0;
+  int t0 = (lane < a.bpp && lane < row_left) ? row[lane] : 0;
+  int t1 = (lane + 32 < a.bpp && lane + 32 < row_left) ? row[lane + 32] : 0;
   // Q as the B operand (k = head dim, n = query head of the group).
   const int r = lane >> 2, q4 = lane & 3;
   uint32_t qf[KSTEPS][2];
   {
-    const int n = r;
-    const QT* qrow = static_cast<const QT*>(a.q) + (static_cast<size_t>(b) * a.Hq + g * a.G + n) * D;
+    const QT* qrow = static_cast<const QT*>(a.q) + (static_cast<size_t>(b) * a.Hq + g * a.G + r) * D;
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
-      if (n < a.G) {
-        if constexpr (FP8) {
-          // permuted k order matching the register-converted K fragment
+      if (r < a.G) {
+        if constexpr (FP8) {  // permuted k order matching the register-converted K fragment
           const uint2 w = *reinterpret_cast<const uint2*>(qrow + 32 * q4 + 4 * kk);
           qf[kk][0] = w.x;
           qf[kk][1] = w.y;
@@ -201,64 +164,138 @@ __global__ void __launch_bounds__(kNW * 32)
     }
   }
 
+  const int L = checked_len(a, b, lane == 0 && p == 0);
+  const int nblk = (L + 15) >> 4;
+  if (j0 >= nblk) {
+    if (p == 0)  // empty context: zero rows
+      for (int i = lane; i < a.G * D; i += 32)
+        store_out<QT>(a, (static_cast<size_t>(b) * a.Hq + g * a.G + i / D) * D + i % D, 0.f);
+    return;
+  }
+  const int nb = min(a.bpp, nblk - j0);
+  const int nparts = (nblk + a.bpp - 1) / a.bpp;
+  const bool bad = (lane < nb && (t0 < 0 || t0 >= a.num_blocks)) ||
+                   (lane + 32 < nb && (t1 < 0 || t1 >= a.num_blocks));
+  if (bad) {
+    atomicOr(&g_decode_err, PA_DEVERR_BLOCK_RANGE);  // read a valid block instead; flagged
+    if (t0 < 0 || t0 >= a.num_blocks) t0 = 0;
+    if (t1 < 0 || t1 >= a.num_blocks) t1 = 0;
+  }
+  if (lane == 0) {
+    dev::prefetch_tensormap(&tmK);
+    dev::prefetch_tensormap(&tmV);
+    for (int s = 0; s < NS; ++s) dev::mbar_init(bar_full + 8 * s, 1);
+    dev::fence_barrier_init();
+  }
+  __syncwarp();
+
+  auto block_id = [&](int j) { return __shfl_sync(FULL, j < 32 ? t0 : t1, j & 31); };
+  auto issue = [&](int pb, int s) {  // lane 0 only
+    const uint32_t bar = bar_full + 8 * s;
+    const uint32_t kdst = tiles + s * 2 * TL::BYTES, vdst = kdst + TL::BYTES;
+    dev::mbar_arrive_expect_tx(bar, STAGE_TX);
+#pragma unroll
+    for (int bx = 0; bx < TL::NBOX; ++bx) {
+      dev::tma_load_3d(kdst + bx * 2048, &tmK, bar, bx * TL::BOXE, g * 16, pb);
+      dev::tma_load_3d(vdst + bx * 2048, &tmV, bar, bx * TL::BOXE, g * 16, pb);
+    }
+    if constexpr (FP8) {
+      dev::bulk_load(dev::smem_addr(s_scale + s * 32), a.k_scale + static_cast<size_t>(pb) * 16, 64, bar);
+      dev::bulk_load(dev::smem_addr(s_scale + s * 32 + 16), a.v_scale + static_cast<size_t>(pb) * 16, 64, bar);
+    }
+  };
+#pragma unroll
+  for (int j = 0; j < NS; ++j) {
+    const int pb = block_id(j);
+    if (j < nb && lane == 0) issue(pb, j);
+  }
+
   float o[MT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const float sl2 = a.scale_log2;
 
-  for (int i = 0;; ++i) {
-    const int jj = warp + i * kNW;
-    if (jj >= nb) break;
-    const int s = warp * kNSW + (i % kNSW);
-    if (!dev::mbar_wait_bounded(dev::smem_addr(&s_bar[s]), (i / kNSW) & 1)) {
+  for (int j = 0; j < nb; ++j) {
+    const int s = j % NS;
+    const int next_pb = block_id(min(j + NS, 63));  // block id of the refill (all lanes shuffle)
+    if (!dev::mbar_wait_bounded(bar_full + 8 * s, (j / NS) & 1)) {
       if (lane == 0) atomicOr(&g_decode_err, PA_DEVERR_TIMEOUT);
-      // drain this warp's other copies in flight (bounded), then stop
-      for (int i2 = i + 1; i2 < i + kNSW; ++i2) {
-        const int j2 = warp + i2 * kNW;
-        if (j2 < nb)
-          dev::mbar_wait_bounded(dev::smem_addr(&s_bar[warp * kNSW + (i2 % kNSW)]), (i2 / kNSW) & 1,
-                                 100000000ull);
-      }
-      break;
+      // let this warp's other copies in flight land (bounded), then stop
+      for (int j2 = j + 1; j2 < min(nb, j + NS); ++j2)
+        dev::mbar_wait_bounded(bar_full + 8 * (j2 % NS), (j2 / NS) & 1, 100000000ull);
+      return;
     }
     const uint32_t kb = tiles + s * 2 * TL::BYTES, vb = kb + TL::BYTES;
-    const int nvalid = min(16, L - (j0 + jj) * 16);
+    const int nvalid = min(16, L - (j0 + j) * 16);
 
-    // ---- S^T = K . Q^T -----------------------------------------------------
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- K and V fragments -> registers, then refill the stage ---------------
+    uint32_t kf[KSTEPS][4], vf[MT][4];
+    float c_r = sl2, c_r8 = sl2, vs_r = 1.f, vs_r8 = 1.f;
     if constexpr (FP8) {
       const uint4 x0 = dev::lds128(kb + swz(r, 2 * q4));
       const uint4 x1 = dev::lds128(kb + swz(r, 2 * q4 + 1));
       const uint4 y0 = dev::lds128(kb + swz(r + 8, 2 * q4));
       const uint4 y1 = dev::lds128(kb + swz(r + 8, 2 * q4 + 1));
+      const int tt = 2 * q4;
+      const uint4 X = dev::lds128(vb + swz(tt, r));
+      const uint4 Y = dev::lds128(vb + swz(tt + 1, r));
+      const uint4 Z = dev::lds128(vb + swz(tt + 8, r));
+      const uint4 W = dev::lds128(vb + swz(tt + 9, r));
+      c_r *= s_scale[s * 32 + r];
+      c_r8 *= s_scale[s * 32 + r + 8];
+      vs_r = s_scale[s * 32 + 16 + r];
+      vs_r8 = s_scale[s * 32 + 16 + r + 8];
       const uint32_t wr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       const uint32_t wr8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
       for (int kk = 0; kk < KSTEPS; ++kk) {
-        uint32_t af[4];
-        af[0] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(wr[kk] & 0xffffu));
-        af[1] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(wr8[kk] & 0xffffu));
-        af[2] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(wr[kk] >> 16));
-        af[3] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(wr8[kk] >> 16));
-        dev::Mma<QT>::run(sacc, af, qf[kk][0], qf[kk][1]);
+        kf[kk][0] = wr[kk];
+        kf[kk][1] = wr8[kk];
+      }
+      const uint32_t xw[4] = {X.x, X.y, X.z, X.w}, yw[4] = {Y.x, Y.y, Y.z, Y.w};
+      const uint32_t zw[4] = {Z.x, Z.y, Z.z, Z.w}, ww[4] = {W.x, W.y, W.z, W.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        vf[i][0] = xw[i];
+        vf[i][1] = yw[i];
+        vf[i][2] = zw[i];
+        vf[i][3] = ww[i];
       }
     } else {
       const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int vrow = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        uint32_t af[4];
-        dev::ldmatrix_x4(af, kb + swz(krow, 2 * kk + (lane >> 4)));
-        dev::Mma<QT>::run(sacc, af, qf[kk][0], qf[kk][1]);
+      for (int kk = 0; kk < KSTEPS; ++kk) dev::ldmatrix_x4(kf[kk], kb + swz(krow, 2 * kk + (lane >> 4)));
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) dev::ldmatrix_x4_trans(vf[mt], vb + swz(vrow, 2 * mt + ((lane >> 3) & 1)));
+    }
+    __syncwarp();
+    if (lane == 0 && j + NS < nb) {
+      dev::fence_proxy_async_smem();
+      issue(next_pb, s);
+    }
+
+    // ---- S^T = K . Q^T -----------------------------------------------------
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      uint32_t af[4];
+      if constexpr (FP8) {
+        af[0] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(kf[kk][0] & 0xffffu));
+        af[1] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(kf[kk][1] & 0xffffu));
+        af[2] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(kf[kk][0] >> 16));
+        af[3] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(kf[kk][1] >> 16));
+      } else {
+        af[0] = kf[kk][0];
+        af[1] = kf[kk][1];
+        af[2] = kf[kk][2];
+        af[3] = kf[kk][3];
       }
+      dev::Mma<QT>::run(sacc, af, qf[kk][0], qf[kk][1]);
     }
 
     // ---- online softmax over this block's 16 tokens ---------------------------
-    float c_r = sl2, c_r8 = sl2;
-    if constexpr (FP8) {
-      c_r *= s_scale[s * 32 + r];
-      c_r8 *= s_scale[s * 32 + r + 8];
-    }
     const bool v_r = r < nvalid, v_r8 = r + 8 < nvalid;
     const float x0 = v_r ? sacc[0] * c_r : -INFINITY;
     const float x1 = v_r ? sacc[1] * c_r : -INFINITY;
@@ -280,7 +317,6 @@ __global__ void __launch_bounds__(kNW * 32)
     if constexpr (FP8) {
       l0 = l0 * al0 + (p0 + p2);
       l1 = l1 * al1 + (p1 + p3);
-      const float vs_r = s_scale[s * 32 + 16 + r], vs_r8 = s_scale[s * 32 + 16 + r + 8];
       p0 *= vs_r;
       p1 *= vs_r;
       p2 *= vs_r8;
@@ -316,133 +352,158 @@ __global__ void __launch_bounds__(kNW * 32)
       o[mt][1] *= al1;
       o[mt][2] *= al0;
       o[mt][3] *= al1;
-    }
-    if constexpr (FP8) {
-      const int t0 = 2 * q4;
-      const uint4 X = dev::lds128(vb + swz(t0, r));
-      const uint4 Y = dev::lds128(vb + swz(t0 + 1, r));
-      const uint4 Z = dev::lds128(vb + swz(t0 + 8, r));
-      const uint4 W = dev::lds128(vb + swz(t0 + 9, r));
-      const uint32_t xw[4] = {X.x, X.y, X.z, X.w}, yw[4] = {Y.x, Y.y, Y.z, Y.w};
-      const uint32_t zw[4] = {Z.x, Z.y, Z.z, Z.w}, ww[4] = {W.x, W.y, W.z, W.w};
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
+      uint32_t af[4];
+      if constexpr (FP8) {
         const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-        const uint32_t xy = dev::prmt(xw[mt >> 1], yw[mt >> 1], sel);
-        const uint32_t zv = dev::prmt(zw[mt >> 1], ww[mt >> 1], sel);
-        uint32_t af[4];
+        const uint32_t xy = dev::prmt(vf[mt >> 1][0], vf[mt >> 1][1], sel);
+        const uint32_t zv = dev::prmt(vf[mt >> 1][2], vf[mt >> 1][3], sel);
         af[0] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(xy & 0xffffu));
         af[1] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(xy >> 16));
         af[2] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(zv & 0xffffu));
         af[3] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(zv >> 16));
-        dev::Mma<QT>::run(o[mt], af, bh0, bh1);
-        if constexpr (SPLIT_P) dev::Mma<QT>::run(o[mt], af, bl0, bl1);
+      } else {
+        af[0] = vf[mt][0];
+        af[1] = vf[mt][1];
+        af[2] = vf[mt][2];
+        af[3] = vf[mt][3];
       }
-    } else {
-      const int vrow = (lane & 7) + (lane >> 4) * 8;
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        uint32_t af[4];
-        dev::ldmatrix_x4_trans(af, vb + swz(vrow, 2 * mt + ((lane >> 3) & 1)));
-        dev::Mma<QT>::run(o[mt], af, bh0, bh1);
-        if constexpr (SPLIT_P) dev::Mma<QT>::run(o[mt], af, bl0, bl1);
-      }
-    }
-
-    __syncwarp();
-    if (lane == 0) {
-      const int jn = jj + kNSW * kNW;
-      if (jn < nb) {
-        dev::fence_proxy_async_smem();
-        issue(jn, s);
-      }
+      dev::Mma<QT>::run(o[mt], af, bh0, bh1);
+      if constexpr (SPLIT_P) dev::Mma<QT>::run(o[mt], af, bl0, bl1);
     }
   }
-
-  // ---- merge the warps' partial softmax states ----------------------------------
   dev::grid_launch_dependents();  // the merge kernel may start being scheduled
+
+  // ---- output: this item's (o, m, l) or, for one partition, o / l -----------------
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(FULL, l0, off);
     l1 += __shfl_xor_sync(FULL, l1, off);
   }
-  __syncthreads();  // every stage consumed: tile memory is free
-  float* s_o = reinterpret_cast<float*>(base);  // [kNW][8][D]
-  float* s_m = s_o + kNW * 8 * D;                // [kNW][8]
-  float* s_l = s_m + kNW * 8;
-  {
-    const int hA = 2 * q4, hB = 2 * q4 + 1;
-    float* ow = s_o + warp * 8 * D;
+  const int hA = 2 * q4, hB = 2 * q4 + 1;
+  const size_t headA = static_cast<size_t>(b) * a.Hq + g * a.G + hA;
+  const size_t headB = headA + 1;
+  const bool okA = hA < a.G, okB = hB < a.G;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      int d_r, d_r8;
-      if constexpr (FP8) {
-        d_r = 16 * r + 2 * mt;
-        d_r8 = d_r + 1;
-      } else {
-        d_r = 16 * mt + r;
-        d_r8 = d_r + 8;
-      }
-      ow[hA * D + d_r] = o[mt][0];
-      ow[hB * D + d_r] = o[mt][1];
-      ow[hA * D + d_r8] = o[mt][2];
-      ow[hB * D + d_r8] = o[mt][3];
+  for (int mt = 0; mt < MT; ++mt) {
+    int d_r, d_r8;
+    if constexpr (FP8) {
+      d_r = 16 * r + 2 * mt;
+      d_r8 = d_r + 1;
+    } else {
+      d_r = 16 * mt + r;
+      d_r8 = d_r + 8;
     }
-    if (lane < 4) {
-      s_m[warp * 8 + hA] = m0;
-      s_m[warp * 8 + hB] = m1;
-      s_l[warp * 8 + hA] = l0;
-      s_l[warp * 8 + hB] = l1;
+    if (nparts == 1) {
+      if (okA) {
+        store_out<QT>(a, headA * D + d_r, o[mt][0] / l0);
+        store_out<QT>(a, headA * D + d_r8, o[mt][2] / l0);
+      }
+      if (okB) {
+        store_out<QT>(a, headB * D + d_r, o[mt][1] / l1);
+        store_out<QT>(a, headB * D + d_r8, o[mt][3] / l1);
+      }
+    } else {
+      const size_t rowA = headA * a.max_parts + p, rowB = headB * a.max_parts + p;
+      if (okA) {
+        a.part_o[rowA * D + d_r] = o[mt][0];
+        a.part_o[rowA * D + d_r8] = o[mt][2];
+      }
+      if (okB) {
+        a.part_o[rowB * D + d_r] = o[mt][1];
+        a.part_o[rowB * D + d_r8] = o[mt][3];
+      }
     }
   }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < a.G * D; idx += blockDim.x) {
-    const int h = idx / D, d = idx - h * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kNW; ++w) M = fmaxf(M, s_m[w * 8 + h]);
-    float acc = 0.f, ls = 0.f;
-#pragma unroll
-    for (int w = 0; w < kNW; ++w) {
-      const float f = exp2f(s_m[w * 8 + h] - M);
-      acc += f * s_o[(w * 8 + h) * D + d];
-      ls += f * s_l[w * 8 + h];
+  if (nparts > 1 && lane < 4) {
+    if (okA) {
+      a.part_m[headA * a.max_parts + p] = m0;
+      a.part_l[headA * a.max_parts + p] = l0;
     }
-    const size_t head = static_cast<size_t>(b) * a.Hq + g * a.G + h;
-    if (nparts == 1) {
-      store_out<QT>(a, head * D + d, acc / ls);
-    } else {
-      const size_t row = head * a.max_parts + p;
-      a.part_o[row * D + d] = acc;
-      if (d == 0) {
-        a.part_m[row] = M;
-        a.part_l[row] = ls;
-      }
+    if (okB) {
+      a.part_m[headB * a.max_parts + p] = m1;
+      a.part_l[headB * a.max_parts + p] = l1;
     }
   }
 }
 
-// Merge the partitions of one (sequence, query head): log-sum-exp weights.
+// Merge the partitions of each (sequence, query head): log-sum-exp weights.
+// One warp per query head, G warps per CTA (one CTA per sequence and kv head).
+// Partitions are taken 16 at a time: lane i holds partition i's (m, l), every
+// lane holds its D/32 dims of the chunk's partial rows, and chunks merge online
+// (running max).  The first chunk's (m, l) are read together with the context
+// length (rows up to max_parts always exist); partial rows are read only for
+// partitions that exist.
 template <typename QT, int D>
-__global__ void __launch_bounds__(D) decode_reduce(const DecodeArgs a) {
-  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+__global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce(const DecodeArgs a) {
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int CH = 16;      // partitions per chunk
+  constexpr int V = D / 32;   // dims per lane (4 or 2)
+  const int bg = blockIdx.x, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int h = g * a.G + static_cast<int>(threadIdx.x >> 5), lane = threadIdx.x & 31;
   dev::grid_dependency_wait();  // partials of decode_main are complete and visible
+  const size_t row0 = (static_cast<size_t>(b) * a.Hq + h) * a.max_parts;
+  const float* po = a.part_o + row0 * D + lane * V;
+  float mv = lane < min(CH, a.max_parts) ? a.part_m[row0 + lane] : -INFINITY;
+  float lv = lane < min(CH, a.max_parts) ? a.part_l[row0 + lane] : 0.f;
   const int L = checked_len(a, b, false);
   const int nblk = (L + 15) >> 4;
   const int nparts = (nblk + a.bpp - 1) / a.bpp;
-  if (nparts <= 1) return;
-  const size_t row0 = (static_cast<size_t>(b) * a.Hq + h) * a.max_parts;
-  float M = -INFINITY;
-  for (int p = 0; p < nparts; ++p) M = fmaxf(M, a.part_m[row0 + p]);
-  float acc = 0.f, ls = 0.f;
-  for (int p = 0; p < nparts; ++p) {
-    const float f = exp2f(a.part_m[row0 + p] - M);
-    acc += f * a.part_o[(row0 + p) * D + d];
-    ls += f * a.part_l[row0 + p];
+  if (nparts <= 1) return;  // written by decode_main (zero rows included)
+  float M = -INFINITY, ls = 0.f, acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  for (int c0 = 0; c0 < nparts; c0 += CH) {
+    const int n = min(CH, nparts - c0);
+    if (c0 > 0) {
+      mv = lane < n ? a.part_m[row0 + c0 + lane] : -INFINITY;
+      lv = lane < n ? a.part_l[row0 + c0 + lane] : 0.f;
+    }
+    if (lane >= n) {  // stale scratch past nparts (possibly NaN) never enters the sums
+      mv = -INFINITY;
+      lv = 0.f;
+    }
+    float x[CH][V];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      if (i < n) {
+        if constexpr (V == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(po + static_cast<size_t>(c0 + i) * D);
+          x[i][0] = t.x; x[i][1] = t.y; x[i][2] = t.z; x[i][3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(po + static_cast<size_t>(c0 + i) * D);
+          x[i][0] = t.x; x[i][1] = t.y;
+        }
+      }
+    }
+    float cm = mv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, off));
+    const float nm = fmaxf(M, cm);
+    const float rescale = exp2f(M - nm);  // 0 on the first chunk
+    M = nm;
+    const float w = exp2f(mv - nm);       // this lane's partition weight
+    float wl = w * lv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(FULL, wl, off);
+    ls = ls * rescale + wl;
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] *= rescale;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      const float wi = __shfl_sync(FULL, w, i);
+      if (i < n) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] += wi * x[i][v];
+      }
+    }
   }
-  store_out<QT>(a, (static_cast<size_t>(b) * a.Hq + h) * D + d, acc / ls);
+  const size_t orow = (static_cast<size_t>(b) * a.Hq + h) * D + lane * V;
+#pragma unroll
+  for (int v = 0; v < V; ++v) store_out<QT>(a, orow + v, acc[v] / ls);
 }
 
+// ---- host side -------------------------------------------------------------------
+// ---- host side -------------------------------------------------------------------
 // ---- host side -------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -512,25 +573,21 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: no CUDA device");
-  static std::once_flag attr_once[64];
-  cudaError_t attr_err = cudaSuccess;
-  auto set_attr = [&] {
-    attr_err = cudaFuncSetAttribute(decode_main<KT, QT, D>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, TL::SMEM);
-  };
-  if (dev < 64)
-    std::call_once(attr_once[dev], set_attr);
-  else
-    set_attr();
-  if (attr_err != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(attr_err));
+  if (dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "pa_decode: device index %d", dev);
+  static std::once_flag once[kMaxDevices];  // raise the smem limit once per device
+  static cudaError_t setup_err[kMaxDevices];
+  std::call_once(once[dev], [dev] {
+    setup_err[dev] = cudaFuncSetAttribute(decode_main<KT, QT, D>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, TL::SMEM);
+  });
+  if (setup_err[dev] != cudaSuccess)
+    return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(setup_err[dev]));
 
   const dim3 grid(static_cast<unsigned>(l.B * l.Hkv), static_cast<unsigned>(l.plan.max_parts));
-  cudaError_t e = launch_dependent(decode_main<KT, QT, D>, grid, dim3(kNW * 32), TL::SMEM, stream,
-                                   tmK, tmV, a);
+  cudaError_t e = launch_dependent(decode_main<KT, QT, D>, grid, dim3(32), TL::SMEM, stream, tmK, tmV, a);
   if (e == cudaSuccess && l.plan.max_parts > 1)
-    e = launch_dependent(decode_reduce<QT, D>,
-                         dim3(static_cast<unsigned>(l.Hq), static_cast<unsigned>(l.B)), dim3(D), 0,
-                         stream, a);
+    e = launch_dependent(decode_reduce<QT, D>, dim3(static_cast<unsigned>(l.B * l.Hkv)),
+                         dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode launch: %s", cudaGetErrorString(e));
   return PA_OK;

@@ -32,8 +32,11 @@ def gpu_decode(w, out_dtype=torch.float32, split_tokens=0, tables=None, lens=Non
     ks = scales[0].to(DEV) if scales[0] is not None else None
     vs = scales[1].to(DEV) if scales[1] is not None else None
     ml = int(max(lens)) if max_len is None else max_len
+    # scratch starts as 0xFF bytes (NaN floats): stale rows must never leak into results
+    need = ops.decode_workspace_size(q.shape[0], q.shape[1], ml, kc, split_tokens)
+    ws = torch.full((max(need, 16),), 255, dtype=torch.uint8, device=DEV)
     out = ops.decode(q, kc, vc, bt, cl, ml, w.scale, out_dtype=out_dtype, k_scale=ks, v_scale=vs,
-                     split_tokens=split_tokens)
+                     workspace=ws, split_tokens=split_tokens)
     torch.cuda.synchronize()
     return out.cpu()
 
