@@ -50,7 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="llama7b_b32",
-                   choices=["tiny", "llama7b_b32", "gqa70b_b64", "longctx_b8_f16", "longctx_b8_fp8"])
+                   choices=["tiny", "llama7b_b32", "gqa70b_b64", "longctx_b8_f16", "longctx_b8_fp8",
+                            "shared_prefix_16x4"])
     p.add_argument("--split", type=int, default=0, help="split_tokens (0 = library choice)")
     p.add_argument("--e2e-steps", type=int, default=300)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -419,12 +420,197 @@ class DecodeStep:
         return 2 + (1 if ws else 0)
 
 
+class SharedPrefixStep(DecodeStep):
+    """Beam search over shared prompts: every step each group's beams are
+    reselected from parent beams (fork all children, then release the old
+    beams), one slot is appended per beam -- copy-on-write where siblings
+    share a partially filled block -- and pa_copy_blocks runs before the
+    cache write and the decode."""
+
+    def __init__(self, w, split_tokens, steps_total, device):
+        import torch
+        from paged_kv_cache_191_gb300 import ops
+        self.torch, self.ops, self.L = torch, ops, ops.lib()
+        self.w = w
+        self.B, self.Hq, self.Hkv, self.D = w.B, w.Hq, w.Hkv, w.D
+        self.fp8 = False
+        self.dev = device
+        self.alloc = ops.BlockAllocator(w.num_blocks, w.free_order)
+        self.roots = [10 ** 9 + g for g in range(w.groups)]
+        for r in self.roots:
+            self.alloc.alloc_seq(r, w.prompt_len)
+        self.next_id = 0
+        self._admit()
+        self.max_len = w.prompt_len + int(w.tail_lens.max()) + RESET_EVERY + 1
+        self.cap = -(-self.max_len // 16)
+        self.kc, self.vc = w.k_pool.to(device), w.v_pool.to(device)
+        self.ks = self.vs = None
+        self.q = w.q.to(device)
+        self.new_k, self.new_v = w.new_k.to(device), w.new_v.to(device)
+        self.out = torch.empty((self.B, self.Hq, self.D), dtype=w.q.dtype, device=device)
+        self.desc = ops.cache_desc(self.kc)
+        self.ws_bytes = ops.decode_workspace_size(self.B, self.Hq, self.max_len, self.kc, split_tokens)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        self.split = split_tokens
+        # meta: slots int64[B] | pairs int64[B, 2] | lens int32[B] | tables int32[B, cap]
+        self.meta_bytes = self.B * 8 + self.B * 16 + self.B * 4 + self.B * self.cap * 4
+        self.meta_host = [torch.empty(self.meta_bytes, dtype=torch.uint8).pin_memory() for _ in range(RING)]
+        self.meta_devs = [torch.empty(self.meta_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+        self.use_meta(0)
+        self.drv = Driver()
+        self.ring_ev = [self.drv.event() for _ in range(RING)]
+        self.ring_used = [False] * RING
+        self.ring = 0
+        self.ncow_c = C.c_int32()
+        self.blocked_s = 0.0
+        self.steps_since_reset = 0
+        self.step_idx = 0
+        self.lens0 = np.full(self.B, w.prompt_len) + w.tail_lens.reshape(-1)
+        self.cur_lens = self.lens0.copy()
+        self.history = []  # per timed step: (tables, lens, n_cow) for the byte count
+
+    def use_meta(self, i):
+        T = self.torch
+        self.meta_dev = self.meta_devs[i]
+        B = self.B
+        self.slots_dev = self.meta_dev[: B * 8].view(T.int64)
+        self.pairs_dev = self.meta_dev[B * 8: B * 24].view(T.int64).view(B, 2)
+        self.lens_dev = self.meta_dev[B * 24: B * 28].view(T.int32)
+        self.tables_dev = self.meta_dev[B * 28:].view(T.int32).view(B, self.cap)
+
+    def _fresh(self, n):
+        ids = np.arange(self.next_id, self.next_id + n, dtype=np.uint64)
+        self.next_id += n
+        return ids
+
+    def _admit(self):
+        """Beams forked from their group's prompt, grown by their tails."""
+        w = self.w
+        self.ids = self._fresh(self.B)
+        self.ids_c = self.ids.ctypes.data_as(C.POINTER(C.c_uint64))
+        self.alloc.fork_seqs([self.roots[i // w.beams] for i in range(self.B)], [int(x) for x in self.ids])
+        for i, sid in enumerate(self.ids):
+            _, cow = self.alloc.append_tokens(int(sid), int(w.tail_lens.reshape(-1)[i]), want_slots=False)
+            assert cow[0] < 0  # the 1024-token prompt fills its last block
+        # parent row of every new beam, per reselection pattern
+        if not hasattr(self, "par_rows"):
+            g = np.arange(w.groups)[:, None] * w.beams
+            self.par_rows = [(g + w.parents[k]).reshape(-1).astype(np.int32) for k in range(len(w.parents))]
+
+    def host_prepare(self):
+        w, B = self.w, self.B
+        if self.steps_since_reset == RESET_EVERY:
+            self.alloc.free_seqs([int(x) for x in self.ids])
+            self._admit()
+            self.cur_lens = self.lens0.copy()
+            self.steps_since_reset = 0
+        # beam reselection: beam i continues from beam par[i] of its group
+        par = self.par_rows[self.step_idx % len(self.par_rows)]
+        self.ops._check(self.L.pa_reselect(self.alloc._h, self.ids_c, par.ctypes.data_as(C.POINTER(C.c_int32)), B),
+                        "pa_reselect")
+        buf = self.meta_host[self.ring]
+        if self.ring_used[self.ring]:
+            t0 = time.perf_counter()
+            self.drv.sync(self.ring_ev[self.ring])
+            self.blocked_s += time.perf_counter() - t0
+        base = buf.data_ptr()
+        self.ops._check(self.L.pa_append_slots(self.alloc._h, self.ids_c, B, C.cast(base, C.POINTER(C.c_int64)),
+                                               C.cast(base + B * 8, C.POINTER(C.c_int64)), C.byref(self.ncow_c)),
+                        "pa_append_slots")
+        self.ops._check(self.L.pa_block_tables(self.alloc._h, self.ids_c, B, C.cast(base + B * 28, C.POINTER(C.c_int32)),
+                                               self.cap, C.cast(base + B * 24, C.POINTER(C.c_int32))),
+                        "pa_block_tables")
+        self.n_cow = self.ncow_c.value
+        self.steps_since_reset += 1
+        self.step_idx += 1
+        return buf
+
+    def enqueue(self, buf, ev_pair=None):
+        """a1 H2D (copy stream), a3 block copies, a2 cache write, a4+a5 decode."""
+        L, drv, sp, cp, i = self.L, self.drv, self.sp, self.cp, self.dbuf
+        if self.used_rec[i]:
+            drv.wait(cp, self.used_done[i])
+        drv.h2d(self.meta_devs[i].data_ptr(), buf.data_ptr(), self.meta_bytes, cp)
+        drv.record(self.ring_ev[self.ring], cp)
+        drv.record(self.copy_done[i], cp)
+        self.ring_used[self.ring] = True
+        self.ring = (self.ring + 1) % RING
+        drv.wait(sp, self.copy_done[i])
+        if self.n_cow:
+            st = L.pa_copy_blocks(C.c_void_p(self.kc.data_ptr()), C.c_void_p(self.vc.data_ptr()), None, None,
+                                  C.c_void_p(self.meta_devs[i].data_ptr() + self.B * 8), self.n_cow,
+                                  C.byref(self.desc), sp)
+            if st:
+                self.ops._check(st, "pa_copy_blocks")
+        st = L.pa_cache_write(*self.write_args[i])
+        if st:
+            self.ops._check(st, "pa_cache_write")
+        if ev_pair is not None:
+            drv.record(ev_pair[0], sp)
+        st = L.pa_decode(*self.decode_args[i])
+        if st:
+            self.ops._check(st, "pa_decode")
+        if ev_pair is not None:
+            drv.record(ev_pair[1], sp)
+        drv.record(self.used_done[i], sp)
+        self.used_rec[i] = True
+        self.dbuf ^= 1
+
+    def step_bytes(self):
+        """Recorded now, counted after the timed loop (unique physical bytes)."""
+        buf = self.meta_host[(self.ring - 0) % RING]
+        B = self.B
+        raw = buf.numpy()
+        lens = raw[B * 24: B * 28].view(np.int32).copy()
+        tables = raw[B * 28:].view(np.int32).reshape(B, self.cap).copy()
+        self.history.append((tables, lens, self.n_cow))
+        return 0, 0
+
+    def as_decode_workload(self):
+        """The current batch as a plain decode workload (for the CPU oracle)."""
+        from types import SimpleNamespace
+        tables, lens = self.alloc.tables([int(x) for x in self.ids], self.cap)
+        w = self.w
+        return SimpleNamespace(name=w.name, B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, kv_dtype="f16",
+                               context_lens=lens, block_tables=tables, k_pool=w.k_pool, v_pool=w.v_pool,
+                               q=w.q, scale=w.scale)
+
+    def count_bytes(self, history=None):
+        """(decode bytes, whole-step bytes, logical decode bytes) summed over history.
+
+        Shared-prefix blocks count once per step (unique physical bytes); the
+        logical figure counts every beam's context separately."""
+        e, qe = 2, self.q.element_size()
+        row = self.Hkv * self.D * 2 * e                # K+V bytes of one token
+        block_bytes = self.Hkv * 16 * self.D * e
+        dec_u = step_u = dec_l = 0
+        j = np.arange(self.cap)[None, :]
+        for tables, lens, ncow in (self.history if history is None else history):
+            nb = (lens[:, None] + 15) // 16
+            rows = np.where(j < nb - 1, 16, np.where(j == nb - 1, lens[:, None] - 16 * (nb - 1), 0))
+            live = rows > 0
+            blk, used = tables[live], rows[live]
+            order = np.lexsort((-used, blk))          # per block, largest use first
+            blk, used = blk[order], used[order]
+            first = np.r_[True, blk[1:] != blk[:-1]]
+            extra = self.B * self.Hq * self.D * 2 * qe + int(nb.sum()) * 4 + self.B * 4
+            d = int(used[first].sum()) * row + extra
+            dl = int(lens.sum()) * row + extra
+            write = 2 * self.B * self.Hkv * self.D * 2 * e + self.B * 8
+            copy = ncow * 2 * 2 * block_bytes
+            dec_u += d
+            dec_l += dl
+            step_u += d + write + copy + self.meta_bytes
+        return dec_u, step_u, dec_l
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = load_workload(args.config)
-    st = DecodeStep(w, args.split, args.steps + args.warmup, dev)
+    shared = args.config == "shared_prefix_16x4"
+    st = (SharedPrefixStep if shared else DecodeStep)(w, args.split, args.steps + args.warmup, dev)
     stream = torch.cuda.Stream(device=dev)
     total_steps = args.warmup + args.steps
     st.prebuild(stream)
@@ -435,6 +621,8 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             st.enqueue(st.host_prepare())
+        if shared:
+            st.history.clear()
         stream.synchronize()
         barrier(world)
         torch.cuda.synchronize()
@@ -450,6 +638,9 @@ def run_ours(args, rank, world, local_rank):
             st.enqueue(buf, dec_events[i])
         st.drv.record(t_end, st.sp)
         host_done = time.time()
+        if shared:
+            dec_b, step_b, dec_logical = st.count_bytes()
+            copies = sum(h[2] for h in st.history) / args.steps
         stream.synchronize()
         wall1 = time.time()
     torch.cuda.synchronize()
@@ -467,7 +658,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = run_e2e(st, args, stream)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_seconds)
+        cpu = cpu_baseline(st.as_decode_workload() if shared else w, args.cpu_seconds)
     peak, peak_kind = hbm_peak()
     avg_dec_bytes = dec_b / args.steps
     achieved = avg_dec_bytes / (dec_ms / 1e3) / 1e9
@@ -490,11 +681,17 @@ def run_ours(args, rank, world, local_rank):
             "block_size": 16, "kv_dtype": w.kv_dtype,
             "context_lens": f"start {int(st.lens0.min())}..{int(st.lens0.max())} (mean {st.lens0.mean():.0f}),"
                             f" +1 per step, batch re-admitted every {RESET_EVERY} steps",
+            **({"sharing": "16 groups x 4 beams share a 1024-token prompt; beams reselected from "
+                           "parents every step (fork + release), copy-on-write before each decode; "
+                           "bytes count shared blocks once (logical bytes reported separately)"}
+               if shared else {}),
             "split_tokens": args.split or "auto",
             "l2": f"no flush: K+V per step {avg_dec_bytes / 1e6:.0f} MB vs 129 MB L2",
             "parallelism": f"replicas x{world}",
         },
         "tokens_per_s": round(tot_tokens / max_s, 1),
+        **({"logical_decode_gbs": round(dec_logical / args.steps / (dec_ms / 1e3) / 1e9, 2),
+            "copies_per_step": round(copies, 2)} if shared else {}),
         "host_us_per_step": {"busy": round((host_done - wall0 - st.blocked_s) * 1e6 / args.steps, 2),
                              "blocked_on_gpu": round(st.blocked_s * 1e6 / args.steps, 2)},
         "kv_gbs_decode_only": round(achieved, 2),
@@ -525,6 +722,9 @@ def run_e2e(st, args, stream):
     total_b = 0
     h2d = hq.numel() * hq.element_size() + 2 * hk.numel() * hk.element_size() + st.meta_bytes
     d2h = hout.numel() * hout.element_size()
+    shared = isinstance(st, SharedPrefixStep)
+    if shared:
+        st.history.clear()
     with torch.cuda.stream(stream):
         stream.synchronize()
         t0 = time.perf_counter()
@@ -534,6 +734,8 @@ def run_e2e(st, args, stream):
             total_b += s
             st.use_meta(0)
             st.meta_dev.copy_(buf, non_blocking=True)
+            if getattr(st, "n_cow", 0):
+                ops.copy_blocks(st.kc, st.vc, st.pairs_dev[: st.n_cow], stream=stream)
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
@@ -544,6 +746,9 @@ def run_e2e(st, args, stream):
             hout.copy_(st.out, non_blocking=True)
             stream.synchronize()
         t1 = time.perf_counter()
+    if shared:
+        total_b = st.count_bytes()[1]
+        st.history.clear()
     return {"value": round(total_b / (t1 - t0) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
             "tokens_per_s": round(st.B * n / (t1 - t0), 1),

@@ -244,8 +244,31 @@ pa_status pa_append_slot(pa_alloc* a, uint64_t seq_id, int64_t* slot,
 pa_status pa_append_slots(pa_alloc* a, const uint64_t* seq_ids, int32_t n,
                           int64_t* slots, int64_t* cow_pairs, int32_t* n_cow);
 
+/* Append n tokens to a sequence at once (n successive pa_append_slot): all
+ * or nothing.  slots (optional, host int64 [n]) receives their slots; only the
+ * first token can need a copy-on-write, reported in *cow_src, *cow_dst (else
+ * -1, -1).  Used to grow a sequence by a prompt chunk. */
+pa_status pa_append_tokens(pa_alloc* a, uint64_t seq_id, int64_t n, int64_t* slots,
+                           int64_t* cow_src, int64_t* cow_dst);
+
 /* child shares every block of parent (refcount + 1 each); same token count. */
 pa_status pa_fork(pa_alloc* a, uint64_t parent, uint64_t child);
+
+/* n forks parents[i] -> children[i] in order, all or nothing (a child may
+ * serve as a later parent).  Beam search reselects beams this way. */
+pa_status pa_fork_seqs(pa_alloc* a, const uint64_t* parents, const uint64_t* children,
+                       int32_t n);
+
+/* Release n distinct sequences in order, all or nothing. */
+pa_status pa_free_seqs(pa_alloc* a, const uint64_t* ids, int32_t n);
+
+/* Beam reselection in place: sequence ids[i] takes over the table and token
+ * count of ids[parent_idx[i]] (0 <= parent_idx[i] < n).  Equivalent to forking
+ * every ids[parent_idx[i]] into a new sequence, then releasing the n old
+ * sequences in order, then renaming the forks to ids[i]; shared blocks keep
+ * refcounts, so the next pa_append_slots copies a shared partial block
+ * ([LLM-INF] 2.2 copy-on-write for beam search).  All or nothing. */
+pa_status pa_reselect(pa_alloc* a, const uint64_t* ids, const int32_t* parent_idx, int32_t n);
 
 /* Release a sequence: refcount - 1 per block, freed at 0. */
 pa_status pa_free_seq(pa_alloc* a, uint64_t seq_id);

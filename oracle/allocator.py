@@ -130,6 +130,70 @@ class BlockAllocator:
             raise OutOfBlocks(f"batch append needs {need} blocks, {len(self.free)} free")
         return [self.append_slot(s) for s in seqs]
 
+    def append_tokens(self, seq, n):
+        """n successive appends, all or nothing -> (slots, (cow_src, cow_dst))."""
+        if seq not in self.tables:
+            raise UnknownSeq(seq)
+        tab, ntok = self.tables[seq], self.ntokens[seq]
+        rc = list(self.refcount)
+        need = 0
+        cap = len(tab) * BLOCK_SIZE
+        if n > 0 and ntok < cap:
+            need += self._append_need(seq, rc)
+        if ntok + n > cap:
+            need += blocks_for(ntok + n - cap)
+        if need > len(self.free):
+            raise OutOfBlocks(f"append of {n} tokens needs {need} blocks")
+        slots, cow = [], (-1, -1)
+        for _ in range(n):
+            slot, src, dst = self.append_slot(seq)
+            slots.append(slot)
+            if src >= 0:
+                cow = (src, dst)
+        return slots, cow
+
+    def fork_seqs(self, parents, children):
+        """Forks in order, all or nothing."""
+        made = set()
+        for p, c in zip(parents, children):
+            if p not in self.tables and p not in made:
+                raise UnknownSeq(p)
+            if c in self.tables or c in made:
+                raise InvalidOp("child exists")
+            made.add(c)
+        for p, c in zip(parents, children):
+            self.fork(p, c)
+
+    def free_seqs(self, seqs):
+        """Releases in order, all or nothing."""
+        if len(set(seqs)) != len(seqs):
+            raise InvalidOp("duplicate sequence")
+        for s in seqs:
+            if s not in self.tables:
+                raise UnknownSeq(s)
+        for s in seqs:
+            self.free_seq(s)
+
+    def reselect(self, seqs, parent_idx):
+        """Sequence seqs[i] takes over seqs[parent_idx[i]]'s table: fork every
+        parent into a temporary sequence, release the old ones in order, then
+        rename.  All or nothing."""
+        if len(set(seqs)) != len(seqs):
+            raise InvalidOp("duplicate sequence")
+        for s in seqs:
+            if s not in self.tables:
+                raise UnknownSeq(s)
+        if any(not 0 <= p < len(seqs) for p in parent_idx):
+            raise InvalidOp("parent index out of range")
+        tmp = [("reselect", i) for i in range(len(seqs))]
+        for i, p in enumerate(parent_idx):
+            self.fork(seqs[p], tmp[i])
+        for s in seqs:
+            self.free_seq(s)
+        for i, s in enumerate(seqs):
+            self.tables[s] = self.tables.pop(tmp[i])
+            self.ntokens[s] = self.ntokens.pop(tmp[i])
+
     def fork(self, parent, child):
         if parent not in self.tables:
             raise UnknownSeq(parent)

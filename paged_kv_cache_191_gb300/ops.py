@@ -64,7 +64,11 @@ SIGNATURES = {
     "pa_alloc_seq": (C.c_int, [_P, _U64, _I64]),
     "pa_append_slot": (C.c_int, [_P, _U64, _I64P, _I64P, _I64P]),
     "pa_append_slots": (C.c_int, [_P, _U64P, _I32, _I64P, _I64P, _I32P]),
+    "pa_append_tokens": (C.c_int, [_P, _U64, _I64, _I64P, _I64P, _I64P]),
     "pa_fork": (C.c_int, [_P, _U64, _U64]),
+    "pa_fork_seqs": (C.c_int, [_P, _U64P, _U64P, _I32]),
+    "pa_free_seqs": (C.c_int, [_P, _U64P, _I32]),
+    "pa_reselect": (C.c_int, [_P, _U64P, _I32P, _I32]),
     "pa_free_seq": (C.c_int, [_P, _U64]),
     "pa_block_table": (C.c_int, [_P, _U64, _I32P, _I32, _I32P, _I64P]),
     "pa_block_tables": (C.c_int, [_P, _U64P, _I32, _I32P, _I32, _I32P]),
@@ -252,8 +256,32 @@ class BlockAllocator:
         """Zero-copy variant over caller-owned ctypes/numpy buffers (pointers)."""
         _check(lib().pa_append_slots(self._h, ids, n, slots, pairs, n_cow), "pa_append_slots")
 
+    def append_tokens(self, seq_id, n, want_slots=True):
+        """-> (slots list or None, (cow_src, cow_dst))"""
+        buf = (C.c_int64 * max(n, 1))() if want_slots else None
+        a, b = C.c_int64(), C.c_int64()
+        _check(lib().pa_append_tokens(self._h, seq_id, n, buf, C.byref(a), C.byref(b)), "pa_append_tokens")
+        return (list(buf[:n]) if want_slots else None), (a.value, b.value)
+
     def fork(self, parent, child):
         _check(lib().pa_fork(self._h, parent, child), "pa_fork")
+
+    def fork_seqs(self, parents, children):
+        n = len(parents)
+        P = (C.c_uint64 * max(n, 1))(*parents)
+        Q = (C.c_uint64 * max(n, 1))(*children)
+        _check(lib().pa_fork_seqs(self._h, P, Q, n), "pa_fork_seqs")
+
+    def reselect(self, ids, parent_idx):
+        n = len(ids)
+        A = (C.c_uint64 * max(n, 1))(*[int(x) for x in ids])
+        P = (C.c_int32 * max(n, 1))(*[int(x) for x in parent_idx])
+        _check(lib().pa_reselect(self._h, A, P, n), "pa_reselect")
+
+    def free_seqs(self, ids):
+        n = len(ids)
+        A = (C.c_uint64 * max(n, 1))(*ids)
+        _check(lib().pa_free_seqs(self._h, A, n), "pa_free_seqs")
 
     def free_seq(self, seq_id):
         _check(lib().pa_free_seq(self._h, seq_id), "pa_free_seq")

@@ -149,6 +149,8 @@ class SharedPrefixWorkload:
     new_k: torch.Tensor           # [groups*beams, Hkv, D]
     new_v: torch.Tensor
     scale: float
+    name: str = "shared_prefix_16x4"
+    kv_dtype: str = "f16"
 
     @property
     def B(self):

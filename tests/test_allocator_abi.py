@@ -70,7 +70,8 @@ def test_matches_oracle_model_on_random_operations(palib, seed):
     c, o = ops.BlockAllocator(pool, order), OracleAlloc(pool, order)
     live, nxt = [], 1
     for _ in range(300):
-        op = rnd.choice(["alloc", "append", "append", "batch", "fork", "free", "bad"])
+        op = rnd.choice(["alloc", "append", "append", "batch", "fork", "free", "bad",
+                         "tokens", "forks", "frees", "reselect"])
         if op == "alloc":
             n = rnd.randint(0, 50)
             exp = None
@@ -115,12 +116,53 @@ def test_matches_oracle_model_on_random_operations(palib, seed):
             s = live.pop(rnd.randrange(len(live)))
             o.free_seq(s)
             c.free_seq(s)
+        elif op == "tokens" and live:
+            sq, n = rnd.choice(live), rnd.randint(0, 40)
+            try:
+                want = o.append_tokens(sq, n)
+            except OOOM:
+                with pytest.raises(ops.OutOfBlocks):
+                    c.append_tokens(sq, n)
+            else:
+                got = c.append_tokens(sq, n)
+                assert got[0] == want[0] and got[1] == want[1]
+        elif op == "forks" and live:
+            k = rnd.randint(1, 4)
+            parents, children = [], []
+            for _ in range(k):  # a child may be a later parent
+                parents.append(rnd.choice(live + children))
+                children.append(nxt)
+                nxt += 1
+            o.fork_seqs(parents, children)
+            c.fork_seqs(parents, children)
+            live.extend(children)
+        elif op == "frees" and live:
+            k = rnd.randint(1, min(4, len(live)))
+            ids = rnd.sample(live, k)
+            o.free_seqs(ids)
+            c.free_seqs(ids)
+            for i in ids:
+                live.remove(i)
+        elif op == "reselect" and live:
+            k = rnd.randint(1, min(6, len(live)))
+            ids = rnd.sample(live, k)
+            par = [rnd.randrange(k) for _ in range(k)]
+            o.reselect(ids, par)
+            c.reselect(ids, par)
         elif op == "bad":
             with pytest.raises(ops.UnknownSequence):
                 c.append_slot(10 ** 9)
             with pytest.raises(ops.UnknownSequence):
                 c.free_seq(10 ** 9)
+            with pytest.raises(ops.UnknownSequence):
+                c.fork_seqs([10 ** 9], [nxt])
+            with pytest.raises(ops.UnknownSequence):
+                c.append_tokens(10 ** 9, 3)
             if live:
+                with pytest.raises(ops.PagedKVError):
+                    c.free_seqs([live[0], live[0]])
+                with pytest.raises(ops.PagedKVError):
+                    c.fork_seqs([live[0]], [live[0]])
                 with pytest.raises(ops.PagedKVError):
                     c.alloc_seq(live[0], 1)
                 with pytest.raises(ops.PagedKVError):

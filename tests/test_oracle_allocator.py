@@ -72,7 +72,8 @@ def _random_ops(rng_seed, n_ops=400, pool=24):
     live = []
     next_id = 1
     for _ in range(n_ops):
-        op = rnd.choice(["alloc", "append", "append", "append", "fork", "free", "batch"])
+        op = rnd.choice(["alloc", "append", "append", "append", "fork", "free", "batch", "tokens",
+                         "forks", "frees", "reselect"])
         before = _state(a)
         try:
             if op == "alloc":
@@ -92,6 +93,28 @@ def _random_ops(rng_seed, n_ops=400, pool=24):
             elif op == "batch" and live:
                 seqs = rnd.sample(live, min(len(live), rnd.randint(1, 4)))
                 a.append_slots(seqs)
+            elif op == "tokens" and live:
+                sq = rnd.choice(live)
+                n0 = a.ntokens[sq]
+                slots, cow = a.append_tokens(sq, rnd.randint(0, 40))
+                assert len(set(slots)) == len(slots)
+                assert a.ntokens[sq] == n0 + len(slots)
+            elif op == "forks" and live:
+                kids = [next_id + i for i in range(rnd.randint(1, 3))]
+                a.fork_seqs([rnd.choice(live) for _ in kids], kids)
+                live.extend(kids)
+                next_id += len(kids)
+            elif op == "frees" and live:
+                ids = rnd.sample(live, min(len(live), rnd.randint(1, 3)))
+                a.free_seqs(ids)
+                for i in ids:
+                    live.remove(i)
+            elif op == "reselect" and live:
+                ids = rnd.sample(live, min(len(live), rnd.randint(1, 5)))
+                par = [rnd.randrange(len(ids)) for _ in ids]
+                want = [a.table(ids[p]) for p in par]
+                a.reselect(ids, par)
+                assert [a.table(s) for s in ids] == want
         except OutOfBlocks:
             assert _state(a) == before, "failed op changed the state"
         a.check_invariants()
@@ -150,3 +173,19 @@ def test_errors_leave_state_unchanged():
     with pytest.raises(OutOfBlocks):
         a.append_slots([1, 2])          # both need a fresh block, none free
     assert _state(a) == before
+
+
+def test_append_tokens_equals_repeated_appends():
+    import random
+    for seed in range(5):
+        rnd = random.Random(seed)
+        a, b = BlockAllocator(64), BlockAllocator(64)
+        for al in (a, b):
+            al.alloc_seq(1, 20)
+            al.fork(1, 2)
+        n = rnd.randint(1, 60)
+        slots, cow = a.append_tokens(2, n)
+        singles = [b.append_slot(2) for _ in range(n)]
+        assert slots == [x[0] for x in singles]
+        assert cow == next(((s, d) for _, s, d in singles if s >= 0), (-1, -1))
+        assert a.tables == b.tables and list(a.free) == list(b.free) and a.refcount == b.refcount
