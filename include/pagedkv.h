@@ -159,6 +159,30 @@ pa_status pa_decode(const void* q, int32_t q_dtype,
                     int32_t split_tokens, void* stream);
 
 /*
+ * pa_decode_append -- pa_cache_write of this step's tokens fused into
+ * pa_decode: sequence b's new token (row b of k_new, v_new [B][Hkv][head_dim]
+ * in new_dtype) is stored at slot_mapping[b] (< 0: none), then attention runs
+ * as in pa_decode.  Results, cache contents and FP8 scales are identical to
+ * the two calls in sequence; the store is done inside the decode launch by the
+ * work item that reads that block, before it reads it.  Requires the
+ * block-manager invariant that slot_mapping[b] is the slot of sequence b's
+ * last token (position context_lens[b] - 1 of its table).  Other arguments
+ * and errors as in pa_cache_write and pa_decode.
+ */
+pa_status pa_decode_append(const void* k_new, const void* v_new, int32_t new_dtype,
+                           const int64_t* slot_mapping,
+                           const void* q, int32_t q_dtype,
+                           void* k_cache, void* v_cache,
+                           float* k_scale, float* v_scale,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t max_context_len,
+                           int32_t B, int32_t num_q_heads, float scale,
+                           void* out, int32_t out_dtype,
+                           const pa_cache_desc* desc,
+                           void* workspace, size_t workspace_bytes,
+                           int32_t split_tokens, void* stream);
+
+/*
  * pa_decode_static_ws -- pa_decode that allocates nothing.  The pages have no
  * counterpart: this entry point exists for callers of this library that
  * cannot allocate device memory when they decode -- code running as a plugin

@@ -128,12 +128,14 @@ size_t pa_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_cont
   return plan.workspace_bytes;
 }
 
-pa_status pa_decode(const void* q, int32_t q_dtype, const void* k_cache, const void* v_cache,
-                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
-                    int32_t max_blocks_per_seq, const int32_t* context_lens,
-                    int32_t max_context_len, int32_t B, int32_t num_q_heads, float scale,
-                    void* out, int32_t out_dtype, const pa_cache_desc* desc, void* workspace,
-                    size_t workspace_bytes, int32_t split_tokens, void* stream) {
+static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache, const void* v_cache,
+                             const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                             int32_t max_context_len, int32_t B, int32_t num_q_heads, float scale,
+                             void* out, int32_t out_dtype, const pa_cache_desc* desc, void* workspace,
+                             size_t workspace_bytes, int32_t split_tokens, void* stream,
+                             const void* k_new, const void* v_new, int32_t new_dtype,
+                             const int64_t* slot_mapping) {
   pa_status st = pa::check_desc(desc, "pa_decode");
   if (st != PA_OK) return st;
   if (B < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0)
@@ -196,7 +198,43 @@ pa_status pa_decode(const void* q, int32_t q_dtype, const void* k_cache, const v
   a.out_dtype = out_dtype;
   a.workspace = workspace;
   a.plan = plan;
+  if (slot_mapping) {
+    if (!k_new || !v_new) return fail(PA_ERR_INVALID, "pa_decode_append: k_new / v_new is NULL");
+    if (!pa::aligned16(k_new) || !pa::aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+      return fail(PA_ERR_INVALID, "pa_decode_append: misaligned pointer");
+    if (fp8 ? (new_dtype != PA_DTYPE_F16 && new_dtype != PA_DTYPE_BF16 && new_dtype != PA_DTYPE_F32)
+            : (new_dtype != desc->kv_dtype && new_dtype != PA_DTYPE_F32))
+      return fail(PA_ERR_INVALID, "pa_decode_append: new_dtype does not match the cache");
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.slot_mapping = slot_mapping;
+    a.new_dtype = new_dtype;
+  }
   return pa::launch_decode(a, stream);
+}
+
+pa_status pa_decode(const void* q, int32_t q_dtype, const void* k_cache, const void* v_cache,
+                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    int32_t max_context_len, int32_t B, int32_t num_q_heads, float scale,
+                    void* out, int32_t out_dtype, const pa_cache_desc* desc, void* workspace,
+                    size_t workspace_bytes, int32_t split_tokens, void* stream) {
+  return decode_impl(q, q_dtype, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                     context_lens, max_context_len, B, num_q_heads, scale, out, out_dtype, desc, workspace,
+                     workspace_bytes, split_tokens, stream, nullptr, nullptr, 0, nullptr);
+}
+
+pa_status pa_decode_append(const void* k_new, const void* v_new, int32_t new_dtype,
+                           const int64_t* slot_mapping, const void* q, int32_t q_dtype, void* k_cache,
+                           void* v_cache, float* k_scale, float* v_scale, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t max_context_len, int32_t B, int32_t num_q_heads, float scale,
+                           void* out, int32_t out_dtype, const pa_cache_desc* desc, void* workspace,
+                           size_t workspace_bytes, int32_t split_tokens, void* stream) {
+  if (!slot_mapping) return fail(PA_ERR_INVALID, "pa_decode_append: slot_mapping is NULL");
+  return decode_impl(q, q_dtype, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                     context_lens, max_context_len, B, num_q_heads, scale, out, out_dtype, desc, workspace,
+                     workspace_bytes, split_tokens, stream, k_new, v_new, new_dtype, slot_mapping);
 }
 
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,

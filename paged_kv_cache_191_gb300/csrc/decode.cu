@@ -66,7 +66,68 @@ struct DecodeArgs {
   int32_t bpp, max_parts;
   float scale_log2;
   int32_t out_f32;
+  // fused cache write (pa_decode_append): sequence b's new token, row b of
+  // k_new / v_new [B][Hkv][D] in new_dtype, goes to slot_mapping[b] first
+  const void* k_new;
+  const void* v_new;
+  void* k_cache_w;  // the caches, for the fused row store
+  void* v_cache_w;
+  const int64_t* slot_mapping;
+  float* k_scale_w;  // FP8 scales, writable views of k_scale / v_scale
+  float* v_scale_w;
+  int32_t new_dtype;
+  int32_t fuse_write;
 };
+
+// Element i (of a contiguous row) of a K/V input in f16, bf16 or f32, as float.
+__device__ __forceinline__ float load_in(const void* p, size_t i, int dt) {
+  if (dt == PA_DTYPE_F32) return static_cast<const float*>(p)[i];
+  if (dt == PA_DTYPE_F16) return __half2float(static_cast<const __half*>(p)[i]);
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+
+// One warp stores kv head g's row of this step's new token (K and V) into
+// the cache slot, exactly as pa_cache_write does: a same-dtype copy, a
+// round-to-nearest-even conversion from f32, or for FP8 the per-token
+// amax / scale / E4M3 encoding over all Hkv*D values of the token (each kv
+// head's warp recomputes the token's amax; the g == 0 warp stores the scale).
+template <typename KT, int D>
+__device__ __forceinline__ void write_new_row(const DecodeArgs& a, KT* kc, KT* vc, int b, int g,
+                                              int64_t slot, int lane) {
+  constexpr bool FP8 = sizeof(KT) == 1;
+  const int64_t blk = slot / 16, off = slot % 16;
+  const size_t dst = ((static_cast<size_t>(blk) * a.Hkv + g) * 16 + off) * D;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const void* src = which ? a.v_new : a.k_new;
+    KT* cache = which ? vc : kc;
+    const size_t row = (static_cast<size_t>(b) * a.Hkv + g) * D;
+    if constexpr (FP8) {
+      float amax = 0.f;
+      const size_t tok = static_cast<size_t>(b) * a.Hkv * D;
+      for (int i = lane; i < a.Hkv * D; i += 32) amax = fmaxf(amax, fabsf(load_in(src, tok + i, a.new_dtype)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      for (int d = lane; d < D; d += 32)
+        cache[dst + d] = static_cast<KT>(
+            __nv_cvt_float_to_fp8(__fdiv_rn(load_in(src, row + d, a.new_dtype), scale), __NV_SATFINITE, __NV_E4M3));
+      if (g == 0 && lane == 0) (which ? a.v_scale_w : a.k_scale_w)[slot] = scale;
+    } else {
+      for (int d = lane; d < D; d += 32) {
+        if (a.new_dtype == PA_DTYPE_F32) {
+          const float x = static_cast<const float*>(src)[row + d];
+          if constexpr (std::is_same<KT, __half>::value)
+            cache[dst + d] = __float2half_rn(x);
+          else
+            cache[dst + d] = __float2bfloat16_rn(x);
+        } else {
+          cache[dst + d] = static_cast<const KT*>(src)[row + d];
+        }
+      }
+    }
+  }
+}
 
 template <typename KT, int D>
 struct Tile {
@@ -180,6 +241,19 @@ __global__ void __launch_bounds__(32)
     atomicOr(&g_decode_err, PA_DEVERR_BLOCK_RANGE);  // read a valid block instead; flagged
     if (t0 < 0 || t0 >= a.num_blocks) t0 = 0;
     if (t1 < 0 || t1 >= a.num_blocks) t1 = 0;
+  }
+  if (a.fuse_write && j0 + nb == nblk) {
+    // This partition holds the sequence's last token: store the new row of
+    // kv head g before any tile of it is read, and make the stores visible
+    // to the TMA (async proxy) reads that follow.
+    const int64_t slot = a.slot_mapping[b];
+    if (slot >= static_cast<int64_t>(a.num_blocks) * 16) {
+      if (lane == 0) atomicOr(&g_decode_err, PA_DEVERR_SLOT_RANGE);
+    } else if (slot >= 0) {
+      write_new_row<KT, D>(a, static_cast<KT*>(const_cast<void*>(a.k_cache_w)),
+                           static_cast<KT*>(const_cast<void*>(a.v_cache_w)), b, g, slot, lane);
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
   }
   if (lane == 0) {
     dev::prefetch_tensormap(&tmK);
@@ -570,6 +644,15 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   a.max_parts = l.plan.max_parts;
   a.scale_log2 = l.scale * 1.4426950408889634f;
   a.out_f32 = l.out_dtype == PA_DTYPE_F32;
+  a.k_new = l.k_new;
+  a.v_new = l.v_new;
+  a.slot_mapping = l.slot_mapping;
+  a.k_cache_w = const_cast<void*>(l.k_cache);
+  a.v_cache_w = const_cast<void*>(l.v_cache);
+  a.k_scale_w = const_cast<float*>(l.k_scale);
+  a.v_scale_w = const_cast<float*>(l.v_scale);
+  a.new_dtype = l.new_dtype;
+  a.fuse_write = l.slot_mapping != nullptr;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: no CUDA device");

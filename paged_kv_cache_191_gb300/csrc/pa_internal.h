@@ -57,6 +57,11 @@ struct DecodeLaunch {
   int32_t out_dtype;
   void* workspace;
   DecodePlan plan;
+  // fused cache write of this step's token (pa_decode_append), else null
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  const int64_t* slot_mapping = nullptr;
+  int32_t new_dtype = 0;
 };
 pa_status launch_decode(const DecodeLaunch& a, void* stream);
 

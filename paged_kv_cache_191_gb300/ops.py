@@ -55,6 +55,8 @@ SIGNATURES = {
     "pa_decode_workspace_size": (C.c_size_t, [_I32, _I32, _I32, C.POINTER(CacheDesc), _I32]),
     "pa_decode": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F, _P, _I32,
                             C.POINTER(CacheDesc), _P, C.c_size_t, _I32, _P]),
+    "pa_decode_append": (C.c_int, [_P, _P, _I32, _P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
+                                   _I32, _F, _P, _I32, C.POINTER(CacheDesc), _P, C.c_size_t, _I32, _P]),
     "pa_decode_static_ws": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F, _P,
                                       _I32, C.POINTER(CacheDesc), _I32, _P]),
     "pa_copy_blocks": (C.c_int, [_P, _P, _P, _P, _P, _I64, C.POINTER(CacheDesc), _P]),
@@ -193,6 +195,43 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, sca
                            _ptr(context_lens), int(max_context_len), B, Hq, float(scale),
                            _ptr(out), _TORCH_DT[odt], C.byref(desc), _ptr(workspace), ws_bytes,
                            int(split_tokens), _stream(stream)), "pa_decode")
+    return out
+
+
+def decode_append(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables, context_lens,
+                  max_context_len, scale, out=None, out_dtype=None, k_scale=None, v_scale=None,
+                  workspace=None, split_tokens=0, stream=None):
+    """cache_write(k_new, v_new, slot_mapping) fused into decode (one launch)."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (slot_mapping, "slot_mapping"), (q, "q"),
+                 (k_cache, "k_cache"), (v_cache, "v_cache"), (block_tables, "block_tables"),
+                 (context_lens, "context_lens")):
+        _dev(t, n)
+    desc = cache_desc(k_cache)
+    B, Hq, D = q.shape
+    if k_new.shape != (B, desc.num_kv_heads, D) or v_new.shape != k_new.shape or k_new.dtype != v_new.dtype:
+        raise ValueError("k_new, v_new must be [B, num_kv_heads, head_dim] of one dtype")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != B:
+        raise ValueError("slot_mapping must be int64 [B]")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be int32 [B, max_blocks]")
+    if context_lens.dtype != torch.int32 or context_lens.numel() != B:
+        raise ValueError("context_lens must be int32 [B]")
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=odt, device=q.device)
+    else:
+        _dev(out, "out")
+        odt = out.dtype
+    need = int(lib().pa_decode_workspace_size(B, Hq, max_context_len, C.byref(desc), split_tokens))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().pa_decode_append(_ptr(k_new), _ptr(v_new), _TORCH_DT[k_new.dtype], _ptr(slot_mapping),
+                                  _ptr(q), _TORCH_DT[q.dtype], _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                  _ptr(v_scale), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                  int(max_context_len), B, Hq, float(scale), _ptr(out), _TORCH_DT[odt],
+                                  C.byref(desc), _ptr(workspace), ws_bytes, int(split_tokens), _stream(stream)),
+           "pa_decode_append")
     return out
 
 

@@ -1,0 +1,83 @@
+"""pa_decode_append (cache write fused into decode) against the two separate
+calls: outputs, cache contents and FP8 scales must be bit-identical, and both
+within tolerance of the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from oracle.attention import paged_decode
+from oracle.cache_ops import cache_write as o_write
+from paged_kv_cache_191_gb300 import ops, workloads as W
+from tests.gpu_util import TOL, np_exact, assert_close, requires_cuda
+
+pytestmark = [pytest.mark.gpu, requires_cuda]
+DEV = "cuda"
+TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@pytest.fixture(autouse=True)
+def no_device_errors():
+    ops.device_errors(clear=True)
+    yield
+    assert ops.device_errors(clear=True) == 0
+
+
+def last_slots(w):
+    """Slot of each sequence's last token through its table (-1 for L = 0)."""
+    L = w.context_lens.astype(np.int64)
+    blk = w.block_tables[np.arange(w.B), np.maximum(L - 1, 0) // 16].astype(np.int64)
+    return np.where(L > 0, blk * 16 + (L - 1) % 16, -1)
+
+
+def fp8_caches(w):
+    N, H, _, D = w.k_pool.shape
+    kin = w.k_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(DEV)
+    vin = w.v_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(DEV)
+    kc = torch.empty((N, H, 16, D), dtype=torch.uint8, device=DEV)
+    vc = torch.empty_like(kc)
+    ks = torch.empty((N, 16), dtype=torch.float32, device=DEV)
+    vs = torch.empty_like(ks)
+    ops.cache_write(kin, vin, torch.arange(N * 16, device=DEV), kc, vc, ks, vs)
+    return kc, vc, ks, vs
+
+
+@pytest.mark.parametrize("Hq,Hkv,kv,inp,split", [
+    (8, 8, "f16", "f16", 0), (32, 4, "bf16", "bf16", 64), (16, 2, "f16", "f32", 16),
+    (16, 4, "fp8", "f16", 0), (8, 2, "fp8", "f32", 64), (8, 8, "fp8", "bf16", 0),
+])
+def test_fused_equals_write_then_decode(Hq, Hkv, kv, inp, split):
+    w = W.random_small(71 + Hq + Hkv, B=7, Hq=Hq, Hkv=Hkv, D=128, kv_dtype=kv, max_len=600, min_len=1)
+    q = w.q.to(torch.bfloat16) if kv == "bf16" else w.q
+    slots = last_slots(w)
+    slots[3] = -1                      # a padding row: nothing stored
+    rng = W.rng_for(3)
+    k_new = W.randn(rng, (w.B, Hkv, 128), TD[inp]).to(DEV)
+    v_new = W.randn(rng, (w.B, Hkv, 128), TD[inp]).to(DEV)
+    sl = torch.from_numpy(slots).to(DEV)
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    cl = torch.from_numpy(w.context_lens).to(DEV)
+    ml = int(w.context_lens.max())
+    results = []
+    for fused in (False, True):
+        if kv == "fp8":
+            kc, vc, ks, vs = fp8_caches(w)
+        else:
+            kc, vc, ks, vs = w.k_pool.to(DEV), w.v_pool.to(DEV), None, None
+        if fused:
+            out = ops.decode_append(k_new, v_new, sl, q.to(DEV), kc, vc, bt, cl, ml, w.scale,
+                                    out_dtype=torch.float32, k_scale=ks, v_scale=vs, split_tokens=split)
+        else:
+            ops.cache_write(k_new, v_new, sl, kc, vc, ks, vs)
+            out = ops.decode(q.to(DEV), kc, vc, bt, cl, ml, w.scale, out_dtype=torch.float32,
+                             k_scale=ks, v_scale=vs, split_tokens=split)
+        torch.cuda.synchronize()
+        results.append([t.cpu() for t in (out, kc, vc) + ((ks, vs) if ks is not None else ())])
+    for a, b in zip(*results):
+        assert torch.equal(a, b), "fused and separate paths differ"
+    if kv != "fp8":
+        kin = np_exact(k_new.cpu().to(TD[kv])) if inp == "f32" else np_exact(k_new.cpu())
+        vin = np_exact(v_new.cpu().to(TD[kv])) if inp == "f32" else np_exact(v_new.cpu())
+        okc, ovc, _, _ = o_write(kin, vin, slots, np_exact(w.k_pool), np_exact(w.v_pool))
+        assert np.array_equal(np_exact(results[1][1]), okc) and np.array_equal(np_exact(results[1][2]), ovc)
+        ref = paged_decode(np_exact(q), okc, ovc, w.block_tables, w.context_lens, w.scale)
+        assert_close(results[1][0].numpy(), ref, TOL[kv], "fused vs oracle")
