@@ -68,6 +68,10 @@ pa_status plan_decode(int32_t B, int32_t Hq, int32_t max_context_len, const pa_c
   if (parts > 65535) return fail(PA_ERR_UNSUPPORTED, "context too long for the partition grid");
   plan->blocks_per_part = bpp;
   plan->max_parts = static_cast<int32_t>(parts);
+  // FP8 tiles cost more register-side work per byte (exact conversion of the
+  // codes), so four warps share a partition there; 16-bit caches keep one
+  // warp per partition (measured best for both).
+  plan->item_warps = d->kv_dtype == PA_DTYPE_FP8_E4M3 ? 4 : 1;
   if (parts > 1) {
     const size_t rows = static_cast<size_t>(B) * Hq * parts;
     size_t bytes = rows * d->head_dim * sizeof(float) + 2 * rows * sizeof(float);

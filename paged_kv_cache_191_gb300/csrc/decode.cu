@@ -89,8 +89,9 @@ __device__ __forceinline__ float load_in(const void* p, size_t i, int dt) {
 // One warp stores kv head g's row of this step's new token (K and V) into
 // the cache slot, exactly as pa_cache_write does: a same-dtype copy, a
 // round-to-nearest-even conversion from f32, or for FP8 the per-token
-// amax / scale / E4M3 encoding over all Hkv*D values of the token (each kv
-// head's warp recomputes the token's amax; the g == 0 warp stores the scale).
+// amax / scale / E4M3 encoding over all Hkv*D values of the token.  Every kv
+// head's warp recomputes the token's amax and stores the (identical) scale:
+// its own later read of the scale row must not depend on another CTA.
 template <typename KT, int D>
 __device__ __forceinline__ void write_new_row(const DecodeArgs& a, KT* kc, KT* vc, int b, int g,
                                               int64_t slot, int lane) {
@@ -112,7 +113,7 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs& a, KT* kc, KT* v
       for (int d = lane; d < D; d += 32)
         cache[dst + d] = static_cast<KT>(
             __nv_cvt_float_to_fp8(__fdiv_rn(load_in(src, row + d, a.new_dtype), scale), __NV_SATFINITE, __NV_E4M3));
-      if (g == 0 && lane == 0) (which ? a.v_scale_w : a.k_scale_w)[slot] = scale;
+      if (lane == 0) (which ? a.v_scale_w : a.k_scale_w)[slot] = scale;
     } else {
       for (int d = lane; d < D; d += 32) {
         if (a.new_dtype == PA_DTYPE_F32) {
@@ -135,12 +136,16 @@ struct Tile {
   static constexpr int BYTES = 16 * ROWB;                          // one (block, head) tile
   static constexpr int NBOX = ROWB / 128;                          // 128-byte swizzle boxes
   static constexpr int BOXE = 128 / static_cast<int>(sizeof(KT));  // elements per box row
-  static constexpr int NS = kRingBytes / (2 * BYTES);             // K+V stages in the ring
-  static constexpr int OFF_SC = NS * 2 * BYTES;                    // FP8 scales [NS][32] f32
-  static constexpr int OFF_BAR = OFF_SC + NS * 128;                // full barriers [NS]
-  static constexpr int SMEM = 1024 + OFF_BAR + NS * 8;
+  static constexpr int NS = kRingBytes / (2 * BYTES);             // K+V stages per warp
+  static constexpr int RING = NS * 2 * BYTES;                      // one warp's ring
+  // shared memory of a W-warp CTA: rings [W], FP8 scales [W][NS][32] f32,
+  // full barriers [W][NS]
+  static constexpr int off_sc(int W) { return W * RING; }
+  static constexpr int off_bar(int W) { return off_sc(W) + W * NS * 128; }
+  static constexpr int smem(int W) { return 1024 + off_bar(W) + W * NS * 8; }
   static_assert(ROWB % 128 == 0, "rows must be whole 128-byte swizzle spans");
   static_assert(NS >= 2, "stage ring too small");
+  static_assert(RING >= (8 * D + 16) * 4, "a warp's ring must hold its merge state");
 };
 
 // Byte offset of 16-byte chunk `c` of row `r` inside a swizzled tile.
@@ -169,8 +174,8 @@ __device__ __forceinline__ void store_out(const DecodeArgs& a, size_t idx, float
     static_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(v);
 }
 
-template <typename KT, typename QT, int D>
-__global__ void __launch_bounds__(32)
+template <typename KT, typename QT, int D, int W>
+__global__ void __launch_bounds__(32 * W)
     decode_main(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const DecodeArgs a) {
   using TL = Tile<KT, D>;
@@ -184,13 +189,20 @@ __global__ void __launch_bounds__(32)
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
-  const uint32_t tiles = (raw + 1023u) & ~1023u;
-  uint8_t* base = smem_raw + (tiles - raw);
-  float* s_scale = reinterpret_cast<float*>(base + TL::OFF_SC);
-  const uint32_t bar_full = tiles + TL::OFF_BAR;
-
-  const int lane = threadIdx.x;
-  const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv, p = blockIdx.y;
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (sbase - raw);
+  // Each warp of the CTA owns a ring, scales and barriers, and takes blocks
+  // wid, wid + W, wid + 2W, ... of the item.
+  const int wid = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const uint32_t tiles = sbase + wid * TL::RING;
+  float* s_scale = reinterpret_cast<float*>(base + TL::off_sc(W)) + wid * NS * 32;
+  const uint32_t bar_full = sbase + TL::off_bar(W) + wid * NS * 8;
+  // Partitions are dispatched last-first (blockIdx.y = 0 is the last
+  // partition): the long sequences' full partitions start early and the
+  // short sequences' single small partitions fill in around them, which
+  // approximates longest-first scheduling of the items.
+  const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv;
+  const int p = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
 
   // Launched as a dependent of the preceding kernel (normally the cache
   // write): everything below may read what it wrote.
@@ -242,7 +254,7 @@ __global__ void __launch_bounds__(32)
     if (t0 < 0 || t0 >= a.num_blocks) t0 = 0;
     if (t1 < 0 || t1 >= a.num_blocks) t1 = 0;
   }
-  if (a.fuse_write && j0 + nb == nblk) {
+  if (a.fuse_write && j0 + nb == nblk && wid == 0) {
     // This partition holds the sequence's last token: store the new row of
     // kv head g before any tile of it is read, and make the stores visible
     // to the TMA (async proxy) reads that follow.
@@ -261,7 +273,11 @@ __global__ void __launch_bounds__(32)
     for (int s = 0; s < NS; ++s) dev::mbar_init(bar_full + 8 * s, 1);
     dev::fence_barrier_init();
   }
-  __syncwarp();
+  if constexpr (W > 1)
+    __syncthreads();  // the fused row store (warp 0) precedes every warp's reads
+  else
+    __syncwarp();
+  if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
 
   auto block_id = [&](int j) { return __shfl_sync(FULL, j < 32 ? t0 : t1, j & 31); };
   auto issue = [&](int pb, int s) {  // lane 0 only
@@ -279,9 +295,10 @@ __global__ void __launch_bounds__(32)
     }
   };
 #pragma unroll
-  for (int j = 0; j < NS; ++j) {
-    const int pb = block_id(j);
-    if (j < nb && lane == 0) issue(pb, j);
+  for (int i = 0; i < NS; ++i) {
+    const int j = wid + i * W;
+    const int pb = block_id(min(j, 63));
+    if (j < nb && lane == 0) issue(pb, i);
   }
 
   float o[MT][4];
@@ -290,15 +307,17 @@ __global__ void __launch_bounds__(32)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const float sl2 = a.scale_log2;
 
-  for (int j = 0; j < nb; ++j) {
-    const int s = j % NS;
-    const int next_pb = block_id(min(j + NS, 63));  // block id of the refill (all lanes shuffle)
-    if (!dev::mbar_wait_bounded(bar_full + 8 * s, (j / NS) & 1)) {
+  for (int i = 0;; ++i) {
+    const int j = wid + i * W;  // this warp's i-th block of the item
+    if (j >= nb) break;
+    const int s = i % NS;
+    const int next_pb = block_id(min(j + NS * W, 63));  // block id of the refill (all lanes shuffle)
+    if (!dev::mbar_wait_bounded(bar_full + 8 * s, (i / NS) & 1)) {
       if (lane == 0) atomicOr(&g_decode_err, PA_DEVERR_TIMEOUT);
       // let this warp's other copies in flight land (bounded), then stop
-      for (int j2 = j + 1; j2 < min(nb, j + NS); ++j2)
-        dev::mbar_wait_bounded(bar_full + 8 * (j2 % NS), (j2 / NS) & 1, 100000000ull);
-      return;
+      for (int i2 = i + 1; i2 < i + NS && wid + i2 * W < nb; ++i2)
+        dev::mbar_wait_bounded(bar_full + 8 * (i2 % NS), (i2 / NS) & 1, 100000000ull);
+      break;
     }
     const uint32_t kb = tiles + s * 2 * TL::BYTES, vb = kb + TL::BYTES;
     const int nvalid = min(16, L - (j0 + j) * 16);
@@ -345,7 +364,7 @@ __global__ void __launch_bounds__(32)
       for (int mt = 0; mt < MT; ++mt) dev::ldmatrix_x4_trans(vf[mt], vb + swz(vrow, 2 * mt + ((lane >> 3) & 1)));
     }
     __syncwarp();
-    if (lane == 0 && j + NS < nb) {
+    if (lane == 0 && j + NS * W < nb) {
       dev::fence_proxy_async_smem();
       issue(next_pb, s);
     }
@@ -454,6 +473,59 @@ __global__ void __launch_bounds__(32)
     l1 += __shfl_xor_sync(FULL, l1, off);
   }
   const int hA = 2 * q4, hB = 2 * q4 + 1;
+  if constexpr (W > 1) {
+    // Merge the W warps' softmax states through their (now idle) rings.
+    float* ow = reinterpret_cast<float*>(base + wid * TL::RING);  // [8][D], then m[8], l[8]
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      int d_r, d_r8;
+      if constexpr (FP8) {
+        d_r = 16 * r + 2 * mt;
+        d_r8 = d_r + 1;
+      } else {
+        d_r = 16 * mt + r;
+        d_r8 = d_r + 8;
+      }
+      ow[hA * D + d_r] = o[mt][0];
+      ow[hB * D + d_r] = o[mt][1];
+      ow[hA * D + d_r8] = o[mt][2];
+      ow[hB * D + d_r8] = o[mt][3];
+    }
+    if (lane < 4) {
+      ow[8 * D + hA] = m0;
+      ow[8 * D + hB] = m1;
+      ow[8 * D + 8 + hA] = l0;
+      ow[8 * D + 8 + hB] = l1;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < a.G * D; idx += 32 * W) {
+      const int h = idx / D, d = idx - h * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < W; ++w)
+        M = fmaxf(M, reinterpret_cast<const float*>(base + w * TL::RING)[8 * D + h]);
+      float acc = 0.f, ls = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float* ov = reinterpret_cast<const float*>(base + w * TL::RING);
+        const float f = exp2f(ov[8 * D + h] - M);  // 0 for a warp without blocks
+        acc += f * ov[h * D + d];
+        ls += f * ov[8 * D + 8 + h];
+      }
+      const size_t head = static_cast<size_t>(b) * a.Hq + g * a.G + h;
+      if (nparts == 1) {
+        store_out<QT>(a, head * D + d, acc / ls);
+      } else {
+        const size_t rowp = head * a.max_parts + p;
+        a.part_o[rowp * D + d] = acc;
+        if (d == 0) {
+          a.part_m[rowp] = M;
+          a.part_l[rowp] = ls;
+        }
+      }
+    }
+    return;
+  }
   const size_t headA = static_cast<size_t>(b) * a.Hq + g * a.G + hA;
   const size_t headB = headA + 1;
   const bool okA = hA < a.G, okB = hB < a.G;
@@ -660,14 +732,28 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   static std::once_flag once[kMaxDevices];  // raise the smem limit once per device
   static cudaError_t setup_err[kMaxDevices];
   std::call_once(once[dev], [dev] {
-    setup_err[dev] = cudaFuncSetAttribute(decode_main<KT, QT, D>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, TL::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(decode_main<KT, QT, D, 1>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TL::smem(1));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_main<KT, QT, D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               TL::smem(2));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_main<KT, QT, D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               TL::smem(4));
+    setup_err[dev] = e;
   });
   if (setup_err[dev] != cudaSuccess)
     return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(setup_err[dev]));
 
   const dim3 grid(static_cast<unsigned>(l.B * l.Hkv), static_cast<unsigned>(l.plan.max_parts));
-  cudaError_t e = launch_dependent(decode_main<KT, QT, D>, grid, dim3(32), TL::SMEM, stream, tmK, tmV, a);
+  const int W = l.plan.item_warps;
+  cudaError_t e;
+  if (W == 4)
+    e = launch_dependent(decode_main<KT, QT, D, 4>, grid, dim3(128), TL::smem(4), stream, tmK, tmV, a);
+  else if (W == 2)
+    e = launch_dependent(decode_main<KT, QT, D, 2>, grid, dim3(64), TL::smem(2), stream, tmK, tmV, a);
+  else
+    e = launch_dependent(decode_main<KT, QT, D, 1>, grid, dim3(32), TL::smem(1), stream, tmK, tmV, a);
   if (e == cudaSuccess && l.plan.max_parts > 1)
     e = launch_dependent(decode_reduce<QT, D>, dim3(static_cast<unsigned>(l.B * l.Hkv)),
                          dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);

@@ -35,6 +35,7 @@ struct DecodePlan {
   int32_t blocks_per_part;  // 16-token blocks per partition
   int32_t max_parts;        // partitions of the longest allowed context
   size_t workspace_bytes;   // 0 when max_parts == 1
+  int32_t item_warps;       // warps sharing one partition (1, 2 or 4)
 };
 pa_status plan_decode(int32_t B, int32_t num_q_heads, int32_t max_context_len,
                       const pa_cache_desc* desc, int32_t split_tokens, DecodePlan* plan);

@@ -81,3 +81,11 @@ def test_fused_equals_write_then_decode(Hq, Hkv, kv, inp, split):
         assert np.array_equal(np_exact(results[1][1]), okc) and np.array_equal(np_exact(results[1][2]), ovc)
         ref = paged_decode(np_exact(q), okc, ovc, w.block_tables, w.context_lens, w.scale)
         assert_close(results[1][0].numpy(), ref, TOL[kv], "fused vs oracle")
+
+
+@pytest.mark.parametrize("rep", range(6))
+@pytest.mark.parametrize("Hkv", [8, 2])
+def test_fused_fp8_scales_are_race_free(rep, Hkv):
+    """Every kv head of a token reads the token's fresh scale: repeated runs
+    with many heads per sequence (the scale row is shared by all of them)."""
+    test_fused_equals_write_then_decode(8 * (Hkv // 2) if Hkv > 2 else 8, Hkv, "fp8", "bf16", 0)
