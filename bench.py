@@ -676,6 +676,7 @@ def run_ours(args, rank, world, local_rank):
 
     # e2e: public Python API, host (pinned) inputs in, result out, every step
     e2e = run_e2e(st, args, stream)
+    swap = measure_swap(st, stream)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(st.as_decode_workload() if shared else w, args.cpu_seconds)
@@ -723,12 +724,51 @@ def run_ours(args, rank, world, local_rank):
                                 if st.fused else "pa_decode (decode_main + decode_reduce)"),
                      "bytes_per_launch": int(avg_dec_bytes), "launch_ms": round(dec_ms, 5)},
         "e2e": e2e,
+        "swap": swap,
         "gpu_launches": st.launches_per_step() * args.steps,
         "clocks": clocks.summary(wall0, wall1),
         "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(res), flush=True)
+
+
+def measure_swap(st, stream, n_seqs=8, reps=5):
+    """Preemption traffic: the blocks of n_seqs sequences to a pinned host pool
+    and back (pa_swap_blocks, one gather launch per direction), event-timed."""
+    import torch
+    ids = [int(x) for x in (st.ids[:n_seqs] if hasattr(st, "ids") and not isinstance(st.ids, list)
+                            else list(range(n_seqs)))]
+    tables, lens = st.alloc.tables(ids, st.cap)
+    blocks = [int(b) for row, n in zip(tables, lens) for b in row[: -(-int(n) // 16)]]
+    nb = len(blocks)
+    shape = (nb,) + tuple(st.kc.shape[1:])
+    hk = torch.empty(shape, dtype=st.kc.dtype).pin_memory()
+    hv = torch.empty(shape, dtype=st.kc.dtype).pin_memory()
+    hks = torch.empty((nb, 16)).pin_memory() if st.fp8 else None
+    hvs = torch.empty((nb, 16)).pin_memory() if st.fp8 else None
+    out_pairs = torch.tensor([[b, i] for i, b in enumerate(blocks)], dtype=torch.int64, device=st.dev)
+    in_pairs = torch.tensor([[i, b] for i, b in enumerate(blocks)], dtype=torch.int64, device=st.dev)
+    ev = [st.drv.event(True) for _ in range(3)]
+    sp = C.c_void_p(stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        for _ in range(2):  # warm-up
+            st.ops.swap_blocks(hk, hv, st.kc, st.vc, out_pairs, hks, hvs, st.ks, st.vs, stream=stream)
+            st.ops.swap_blocks(st.kc, st.vc, hk, hv, in_pairs, st.ks, st.vs, hks, hvs, stream=stream)
+        st.drv.record(ev[0], sp)
+        for _ in range(reps):
+            st.ops.swap_blocks(hk, hv, st.kc, st.vc, out_pairs, hks, hvs, st.ks, st.vs, stream=stream)
+        st.drv.record(ev[1], sp)
+        for _ in range(reps):
+            st.ops.swap_blocks(st.kc, st.vc, hk, hv, in_pairs, st.ks, st.vs, hks, hvs, stream=stream)
+        st.drv.record(ev[2], sp)
+        stream.synchronize()
+    nbytes = 2 * hk[0].numel() * hk.element_size() * nb + (2 * 64 * nb if st.fp8 else 0)
+    t_out = st.drv.elapsed_ms(ev[0], ev[1]) / reps / 1e3
+    t_in = st.drv.elapsed_ms(ev[1], ev[2]) / reps / 1e3
+    return {"sequences": len(ids), "blocks": nb, "bytes_per_direction": nbytes,
+            "out_gbs": round(nbytes / t_out / 1e9, 1), "in_gbs": round(nbytes / t_in / 1e9, 1),
+            "path": "GPU cache <-> pinned host pool, device-side gather (NVLink-C2C)"}
 
 
 def run_e2e(st, args, stream):

@@ -229,6 +229,28 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_
                          const pa_cache_desc* desc, void* stream);
 
 /*
+ * pa_swap_blocks -- move whole blocks between two pools of the same shape,
+ * for preemption and resume: a request's pages go to CPU memory when the GPU
+ * runs short and come back when it is scheduled again ([LLM-INF] 3.2).
+ * Each pool is laid out like a cache, k and v [num_blocks][Hkv][16][D] (+ FP8
+ * scale rows [num_blocks][16]); either may be device memory or page-locked
+ * host memory that the device addresses directly (cudaHostAlloc /
+ * cudaHostRegister under unified addressing, e.g. torch pin_memory()).
+ * pairs: device-accessible int64 [num_pairs][2], (src block of the src pool,
+ * dst block of the dst pool); no dst may repeat.  desc gives Hkv, head_dim,
+ * block_size and kv_dtype (its num_blocks is not used).  One kernel launch
+ * (a gather, not one copy per block); ids outside a pool are skipped and
+ * flagged PA_DEVERR_BLOCK_RANGE.
+ */
+pa_status pa_swap_blocks(void* dst_k, void* dst_v, float* dst_k_scale, float* dst_v_scale,
+                         int32_t dst_num_blocks,
+                         const void* src_k, const void* src_v,
+                         const float* src_k_scale, const float* src_v_scale,
+                         int32_t src_num_blocks,
+                         const int64_t* pairs, int64_t num_pairs,
+                         const pa_cache_desc* desc, void* stream);
+
+/*
  * pa_device_errors -- read (and optionally clear) the current device's error
  * word (PA_DEVERR_* bits).  Synchronises the device.
  */

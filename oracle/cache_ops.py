@@ -103,3 +103,24 @@ def copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None):
             ks[d] = k_scale[s]
             vs[d] = v_scale[s]
     return k_new, v_new, ks, vs
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs, dst_ks=None, dst_vs=None, src_ks=None, src_vs=None):
+    """Return new dst pools with dst block d := src block s for each (s, d).
+
+    Preemption moves a request's pages between the GPU cache and a CPU pool
+    ([LLM-INF] 3.2); both pools are laid out like a cache.  No dst may repeat.
+    """
+    pairs = np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+    if len(np.unique(pairs[:, 1])) != len(pairs):
+        raise ValueError("a dst block repeats")
+    k_new, v_new = np.array(dst_k, copy=True), np.array(dst_v, copy=True)
+    ks = None if dst_ks is None else np.array(dst_ks, copy=True)
+    vs = None if dst_vs is None else np.array(dst_vs, copy=True)
+    for s, d in pairs:
+        k_new[d] = src_k[s]
+        v_new[d] = src_v[s]
+        if ks is not None:
+            ks[d] = src_ks[s]
+            vs[d] = src_vs[s]
+    return k_new, v_new, ks, vs

@@ -260,6 +260,32 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_
   return pa::launch_copy_blocks(k_cache, v_cache, k_scale, v_scale, pairs, num_pairs, desc, stream);
 }
 
+pa_status pa_swap_blocks(void* dst_k, void* dst_v, float* dst_k_scale, float* dst_v_scale,
+                         int32_t dst_num_blocks, const void* src_k, const void* src_v,
+                         const float* src_k_scale, const float* src_v_scale, int32_t src_num_blocks,
+                         const int64_t* pairs, int64_t num_pairs, const pa_cache_desc* desc,
+                         void* stream) {
+  pa_status st = pa::check_desc(desc, "pa_swap_blocks");
+  if (st != PA_OK) return st;
+  if (num_pairs < 0) return fail(PA_ERR_INVALID, "pa_swap_blocks: num_pairs < 0");
+  if (num_pairs == 0) return PA_OK;
+  if (num_pairs > 65535) return fail(PA_ERR_INVALID, "pa_swap_blocks: at most 65535 pairs per call");
+  if (dst_num_blocks <= 0 || src_num_blocks <= 0)
+    return fail(PA_ERR_INVALID, "pa_swap_blocks: pool sizes must be > 0");
+  if (!dst_k || !dst_v || !src_k || !src_v || !pairs)
+    return fail(PA_ERR_INVALID, "pa_swap_blocks: null pointer");
+  if (!pa::aligned16(dst_k) || !pa::aligned16(dst_v) || !pa::aligned16(src_k) || !pa::aligned16(src_v) ||
+      (reinterpret_cast<uintptr_t>(pairs) & 7u))
+    return fail(PA_ERR_INVALID, "pa_swap_blocks: misaligned pointer");
+  const bool fp8 = desc->kv_dtype == PA_DTYPE_FP8_E4M3;
+  if (fp8 != (dst_k_scale && dst_v_scale && src_k_scale && src_v_scale))
+    return fail(PA_ERR_INVALID, "pa_swap_blocks: FP8 pools need all four scale arrays, others none");
+  if (!fp8 && (dst_k_scale || dst_v_scale || src_k_scale || src_v_scale))
+    return fail(PA_ERR_INVALID, "pa_swap_blocks: scales are only for FP8 pools");
+  return pa::launch_swap_blocks(dst_k, dst_v, dst_k_scale, dst_v_scale, dst_num_blocks, src_k, src_v,
+                                src_k_scale, src_v_scale, src_num_blocks, pairs, num_pairs, desc, stream);
+}
+
 pa_status pa_device_errors(uint32_t* flags, int32_t clear) {
   if (!flags) return fail(PA_ERR_INVALID, "pa_device_errors: flags is NULL");
   uint32_t a = 0, b = 0;

@@ -1,4 +1,4 @@
-// Cache write and copy-on-write block copy for sm_103a.
+// Cache write, copy-on-write block copy and block swap for sm_103a.
 //
 // Cache write ("LLM推理引擎深度实战：从PagedAttention到分布式推理部署", 2.2:
 // physical pages hold only generated tokens; "大模型推理引擎优化：KV Cache 与
@@ -13,7 +13,10 @@
 // input bits.
 //
 // Block copy ("LLM推理引擎深度实战" 2.2 copy-on-write; "大模型推理引擎优化" 4.2):
-// whole K and V blocks (and their scale rows) are copied src -> dst.
+// whole K and V blocks (and their scale rows) are copied src -> dst.  Block
+// swap ("LLM推理引擎深度实战" 3.2, preemption by moving a request's pages to CPU
+// memory and back) is the same copy between two pools, one of them in
+// page-locked host memory that the kernel addresses directly.
 #include "device_common.cuh"
 #include "pa_internal.h"
 
@@ -166,29 +169,40 @@ __global__ void __launch_bounds__(kWriteThreads)
 constexpr int kCopyThreads = 256;
 constexpr int kCopyChunk = 16384;  // bytes of one block copied by one CTA
 
+// A pool of whole blocks: K, V (and FP8 scales) laid out like a cache.
+struct BlockPool {
+  uint8_t* k;
+  uint8_t* v;
+  float* ks;  // [num_blocks][16] or null
+  float* vs;
+  int num_blocks;
+};
+
+// Copy block pairs[i] = (src, dst) from pool `from` to pool `to` (the same
+// pool for copy-on-write, a pinned host pool for swapping).  One CTA per
+// (pair, 16 KB chunk); ids outside either pool are skipped and flagged.
 __global__ void __launch_bounds__(kCopyThreads)
-    copy_blocks_kernel(uint8_t* __restrict__ kc, uint8_t* __restrict__ vc, float* __restrict__ ks,
-                       float* __restrict__ vs, const int64_t* __restrict__ pairs,
-                       size_t block_bytes, int num_blocks) {
+    copy_blocks_kernel(BlockPool to, BlockPool from, const int64_t* __restrict__ pairs,
+                       size_t block_bytes) {
   const int64_t src = pairs[2 * blockIdx.x], dst = pairs[2 * blockIdx.x + 1];
-  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+  if (src < 0 || src >= from.num_blocks || dst < 0 || dst >= to.num_blocks) {
     if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(&g_cache_err, PA_DEVERR_BLOCK_RANGE);
     return;
   }
   const size_t begin = static_cast<size_t>(blockIdx.y) * kCopyChunk;
   const size_t end = min(begin + kCopyChunk, block_bytes);
-  const uint4* ksrc = reinterpret_cast<const uint4*>(kc + src * block_bytes);
-  const uint4* vsrc = reinterpret_cast<const uint4*>(vc + src * block_bytes);
-  uint4* kdst = reinterpret_cast<uint4*>(kc + dst * block_bytes);
-  uint4* vdst = reinterpret_cast<uint4*>(vc + dst * block_bytes);
+  const uint4* ksrc = reinterpret_cast<const uint4*>(from.k + src * block_bytes);
+  const uint4* vsrc = reinterpret_cast<const uint4*>(from.v + src * block_bytes);
+  uint4* kdst = reinterpret_cast<uint4*>(to.k + dst * block_bytes);
+  uint4* vdst = reinterpret_cast<uint4*>(to.v + dst * block_bytes);
   for (size_t i = begin / 16 + threadIdx.x; i < end / 16; i += blockDim.x) {
     const uint4 a = ksrc[i], b = vsrc[i];
     kdst[i] = a;
     vdst[i] = b;
   }
-  if (ks && blockIdx.y == 0 && threadIdx.x < PA_BLOCK_SIZE) {
-    ks[dst * PA_BLOCK_SIZE + threadIdx.x] = ks[src * PA_BLOCK_SIZE + threadIdx.x];
-    vs[dst * PA_BLOCK_SIZE + threadIdx.x] = vs[src * PA_BLOCK_SIZE + threadIdx.x];
+  if (from.ks && blockIdx.y == 0 && threadIdx.x < PA_BLOCK_SIZE) {
+    to.ks[dst * PA_BLOCK_SIZE + threadIdx.x] = from.ks[src * PA_BLOCK_SIZE + threadIdx.x];
+    to.vs[dst * PA_BLOCK_SIZE + threadIdx.x] = from.vs[src * PA_BLOCK_SIZE + threadIdx.x];
   }
 }
 
@@ -235,18 +249,31 @@ pa_status launch_cache_write(const void* k, const void* v, int32_t in_dtype, con
   return PA_OK;
 }
 
-pa_status launch_copy_blocks(void* kc, void* vc, float* ks, float* vs, const int64_t* pairs,
-                             int64_t n, const pa_cache_desc* d, void* stream) {
+static pa_status launch_pool_copy(const BlockPool& to, const BlockPool& from, const int64_t* pairs,
+                                  int64_t n, const pa_cache_desc* d, void* stream, const char* what) {
   const size_t block_bytes = static_cast<size_t>(d->num_kv_heads) * PA_BLOCK_SIZE * d->head_dim *
                              dtype_bytes(d->kv_dtype);
   const unsigned chunks = static_cast<unsigned>((block_bytes + kCopyChunk - 1) / kCopyChunk);
   copy_blocks_kernel<<<dim3(static_cast<unsigned>(n), chunks), kCopyThreads, 0,
-                       static_cast<cudaStream_t>(stream)>>>(
-      static_cast<uint8_t*>(kc), static_cast<uint8_t*>(vc), ks, vs, pairs, block_bytes,
-      d->num_blocks);
+                       static_cast<cudaStream_t>(stream)>>>(to, from, pairs, block_bytes);
   const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_copy_blocks launch: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
   return PA_OK;
+}
+
+pa_status launch_copy_blocks(void* kc, void* vc, float* ks, float* vs, const int64_t* pairs,
+                             int64_t n, const pa_cache_desc* d, void* stream) {
+  const BlockPool pool{static_cast<uint8_t*>(kc), static_cast<uint8_t*>(vc), ks, vs, d->num_blocks};
+  return launch_pool_copy(pool, pool, pairs, n, d, stream, "pa_copy_blocks");
+}
+
+pa_status launch_swap_blocks(void* dk, void* dv, float* dks, float* dvs, int32_t dnb, const void* sk,
+                             const void* sv, const float* sks, const float* svs, int32_t snb,
+                             const int64_t* pairs, int64_t n, const pa_cache_desc* d, void* stream) {
+  const BlockPool to{static_cast<uint8_t*>(dk), static_cast<uint8_t*>(dv), dks, dvs, dnb};
+  const BlockPool from{static_cast<uint8_t*>(const_cast<void*>(sk)), static_cast<uint8_t*>(const_cast<void*>(sv)),
+                       const_cast<float*>(sks), const_cast<float*>(svs), snb};
+  return launch_pool_copy(to, from, pairs, n, d, stream, "pa_swap_blocks");
 }
 
 pa_status read_errors_cache_ops(uint32_t* flags, bool clear) {

@@ -75,6 +75,10 @@ pa_status launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float
                              const int64_t* pairs, int64_t n, const pa_cache_desc* d,
                              void* stream);
 
+pa_status launch_swap_blocks(void* dk, void* dv, float* dks, float* dvs, int32_t dnb, const void* sk,
+                             const void* sv, const float* sks, const float* svs, int32_t snb,
+                             const int64_t* pairs, int64_t n, const pa_cache_desc* d, void* stream);
+
 // Launch `kernel` on `stream` as a programmatic dependent of the previous
 // kernel in the stream: it may be scheduled while that kernel drains, and
 // must call griddepcontrol.wait before touching memory the predecessor wrote.

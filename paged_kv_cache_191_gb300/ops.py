@@ -60,6 +60,8 @@ SIGNATURES = {
     "pa_decode_static_ws": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F, _P,
                                       _I32, C.POINTER(CacheDesc), _I32, _P]),
     "pa_copy_blocks": (C.c_int, [_P, _P, _P, _P, _P, _I64, C.POINTER(CacheDesc), _P]),
+    "pa_swap_blocks": (C.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _I32, _P, _I64,
+                                 C.POINTER(CacheDesc), _P]),
     "pa_device_errors": (C.c_int, [C.POINTER(C.c_uint32), _I32]),
     "pa_alloc_create": (C.c_int, [_I32, _I32, _I64P, C.POINTER(_P)]),
     "pa_alloc_destroy": (None, [_P]),
@@ -245,6 +247,27 @@ def copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None, stream=None
     _check(lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                 _ptr(pairs), pairs.shape[0], C.byref(desc), _stream(stream)),
            "pa_copy_blocks")
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs, dst_k_scale=None, dst_v_scale=None,
+                src_k_scale=None, src_v_scale=None, stream=None):
+    """Copy blocks pairs[i] = (src, dst) from pool (src_k, src_v) to (dst_k, dst_v).
+
+    Pools are [num_blocks, Hkv, 16, D] tensors on the GPU or in pinned host
+    memory; pairs is an int64 [n, 2] tensor on the GPU or pinned."""
+    for t, n in ((dst_k, "dst_k"), (dst_v, "dst_v"), (src_k, "src_k"), (src_v, "src_v"), (pairs, "pairs")):
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous tensor")
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{n} must be on the GPU or in pinned host memory")
+    if pairs.dtype != torch.int64 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int64 [n, 2]")
+    if dst_k.shape[1:] != src_k.shape[1:] or dst_k.dtype != src_k.dtype:
+        raise ValueError("pools differ in shape or dtype")
+    desc = cache_desc(src_k)
+    _check(lib().pa_swap_blocks(_ptr(dst_k), _ptr(dst_v), _ptr(dst_k_scale), _ptr(dst_v_scale), dst_k.shape[0],
+                                _ptr(src_k), _ptr(src_v), _ptr(src_k_scale), _ptr(src_v_scale), src_k.shape[0],
+                                _ptr(pairs), pairs.shape[0], C.byref(desc), _stream(stream)), "pa_swap_blocks")
 
 
 def device_errors(clear=True):

@@ -84,3 +84,16 @@ def test_copy_blocks_copies_whole_blocks():
         copy_blocks(kc, vc, [[0, 3], [3, 4]])
     with pytest.raises(ValueError):
         copy_blocks(kc, vc, [[0, 3], [1, 3]])
+
+
+def test_swap_blocks_moves_blocks_between_pools():
+    from oracle.cache_ops import swap_blocks
+    rng = np.random.Generator(np.random.PCG64(9))
+    gk, gv = rng.standard_normal((5, 2, BS, 4)), rng.standard_normal((5, 2, BS, 4))
+    hk, hv = np.zeros((3, 2, BS, 4)), np.zeros((3, 2, BS, 4))
+    hk2, hv2, _, _ = swap_blocks(hk, hv, gk, gv, [[4, 0], [1, 2]])
+    assert np.array_equal(hk2[0], gk[4]) and np.array_equal(hv2[2], gv[1]) and not hk2[1].any()
+    gk2, gv2, _, _ = swap_blocks(gk, gv, hk2, hv2, [[0, 3]])
+    assert np.array_equal(gk2[3], gk[4]) and np.array_equal(gk2[0], gk[0])
+    with pytest.raises(ValueError):
+        swap_blocks(hk, hv, gk, gv, [[0, 1], [2, 1]])
