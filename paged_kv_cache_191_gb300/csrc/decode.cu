@@ -136,6 +136,9 @@ struct Tile {
   static constexpr int BYTES = 16 * ROWB;                          // one (block, head) tile
   static constexpr int NBOX = ROWB / 128;                          // 128-byte swizzle boxes
   static constexpr int BOXE = 128 / static_cast<int>(sizeof(KT));  // elements per box row
+  // a tile two 128-byte swizzle spans wide is fetched as one 5-D box
+  // (d_lo, row, d_hi, head, block): one TMA issue per tile instead of two
+  static constexpr bool ONE_BOX = NBOX == 2;
   static constexpr int NS = kRingBytes / (2 * BYTES);             // K+V stages per warp
   static constexpr int RING = NS * 2 * BYTES;                      // one warp's ring
   // shared memory of a W-warp CTA: rings [W], FP8 scales [W][NS][32] f32,
@@ -284,10 +287,15 @@ __global__ void __launch_bounds__(32 * W)
     const uint32_t bar = bar_full + 8 * s;
     const uint32_t kdst = tiles + s * 2 * TL::BYTES, vdst = kdst + TL::BYTES;
     dev::mbar_arrive_expect_tx(bar, STAGE_TX);
+    if constexpr (TL::ONE_BOX) {
+      dev::tma_load_5d(kdst, &tmK, bar, 0, 0, 0, g, pb);
+      dev::tma_load_5d(vdst, &tmV, bar, 0, 0, 0, g, pb);
+    } else {
 #pragma unroll
-    for (int bx = 0; bx < TL::NBOX; ++bx) {
-      dev::tma_load_3d(kdst + bx * 2048, &tmK, bar, bx * TL::BOXE, g * 16, pb);
-      dev::tma_load_3d(vdst + bx * 2048, &tmV, bar, bx * TL::BOXE, g * 16, pb);
+      for (int bx = 0; bx < TL::NBOX; ++bx) {
+        dev::tma_load_3d(kdst + bx * 2048, &tmK, bar, bx * TL::BOXE, g * 16, pb);
+        dev::tma_load_3d(vdst + bx * 2048, &tmV, bar, bx * TL::BOXE, g * 16, pb);
+      }
     }
     if constexpr (FP8) {
       dev::bulk_load(dev::smem_addr(s_scale + s * 32), a.k_scale + static_cast<size_t>(pb) * 16, 64, bar);
@@ -672,15 +680,27 @@ pa_status make_map(CUtensorMap* m, const void* cache, int Hkv, int num_blocks, C
   using TL = Tile<KT, D>;
   auto fn = encode_fn();
   if (!fn) return fail(PA_ERR_CUDA, "pa_decode: cuTensorMapEncodeTiled unavailable");
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(16) * Hkv,
-                              static_cast<cuuint64_t>(num_blocks)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(TL::ROWB),
-                                 static_cast<cuuint64_t>(TL::ROWB) * 16 * Hkv};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(TL::BOXE), 16, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, dt, 3, const_cast<void*>(cache), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if constexpr (TL::ONE_BOX) {
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(TL::BOXE), 16, 2, static_cast<cuuint64_t>(Hkv),
+                                static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[4] = {static_cast<cuuint64_t>(TL::ROWB), 128,
+                                   static_cast<cuuint64_t>(TL::ROWB) * 16,
+                                   static_cast<cuuint64_t>(TL::ROWB) * 16 * Hkv};
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(TL::BOXE), 16, 2, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    r = fn(m, dt, 5, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(16) * Hkv,
+                                static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(TL::ROWB),
+                                   static_cast<cuuint64_t>(TL::ROWB) * 16 * Hkv};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(TL::BOXE), 16, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(m, dt, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "pa_decode: tensor map encode failed (%d)", static_cast<int>(r));
   return PA_OK;
 }
