@@ -1,4 +1,4 @@
-"""Paged decode attention by its definition, in float64 (test infrastructure).
+"""Paged attention by its definition, in float64 (test infrastructure).
 
 What is computed
 ----------------
@@ -92,4 +92,62 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
             K, V = cache_rows[g]
             p = softmax_weights(q[b, h], K, scale)
             out[b, h] = p @ V
+    return out
+
+
+def paged_prefill(q, q_start, k_cache, v_cache, block_tables, context_lens, scale,
+                  k_scale=None, v_scale=None, rows=None):
+    """Paged attention for several query tokens per sequence, float64 [T, Hq, D].
+
+    What is computed: [KV-CB] section 4.1 splits a long prompt into chunks
+    whose prefill runs beside decode steps, and [LLM-INF] section 6.1 has
+    the large model check the draft's gamma tokens in one pass.  Both are
+    attention of n_b > 1 new query tokens of sequence b over its paged
+    context.  Readings where the pages are silent:
+
+    * the chunk's own K/V are already in the cache (written by the cache
+      write beforehand), so context_lens[b] = L_b counts them, and the chunk
+      is the last n_b tokens of the context;
+    * query token i (0 <= i < n_b) sits at position L_b - n_b + i and sees
+      keys 0 .. L_b - n_b + i: the ordinary causal mask, so that splitting a
+      prompt into chunks gives the rows a single pass over the whole prompt
+      would give;
+    * queries are packed: the tokens of sequence b are q[q_start[b] :
+      q_start[b+1]]; n_b = 0 is allowed (no rows); a token whose position
+      would be negative (n_b > L_b) has no keys and gives a zero row.
+
+    q: [T, Hq, D]; q_start: [B + 1] ints, q_start[0] = 0, nondecreasing;
+    other arguments as paged_decode.  rows: optional list of (token, head)
+    pairs to evaluate (others stay 0).
+    """
+    q = np.asarray(q)
+    T, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    assert Hq % Hkv == 0, "query heads must be a multiple of kv heads"
+    G = Hq // Hkv
+    q_start = [int(x) for x in q_start]
+    B = len(q_start) - 1
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    seq_of = np.zeros(T, dtype=np.int64)
+    for b in range(B):
+        seq_of[q_start[b]:q_start[b + 1]] = b
+    wanted = rows if rows is not None else [(t, h) for t in range(T) for h in range(Hq)]
+    by_seq = {}
+    for t, h in wanted:
+        by_seq.setdefault(int(seq_of[int(t)]), []).append((int(t), int(h)))
+    for b, pairs in by_seq.items():
+        n = q_start[b + 1] - q_start[b]
+        L = int(context_lens[b])
+        kv = {}
+        for t, h in pairs:
+            pos = L - n + (t - q_start[b])
+            if pos < 0:
+                continue
+            g = h // G
+            if g not in kv:
+                kv[g] = (gather_kv(k_cache, block_tables[b], L, g, k_scale),
+                         gather_kv(v_cache, block_tables[b], L, g, v_scale))
+            K, V = kv[g]
+            p = softmax_weights(q[t, h], K[:pos + 1], scale)
+            out[t, h] = p @ V[:pos + 1]
     return out
