@@ -41,6 +41,8 @@ RING = 4              # pinned staging buffers in flight
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 METRIC = "paged decode attention KV-read GB/s and tokens/s; % of GB300 HBM peak"
+METRIC_PREFILL = "multi-token paged attention KV-read GB/s and query tokens/s; % of GB300 HBM peak"
+PREFILL_CONFIGS = ("prefill_mix_llama7b", "spec_verify_gqa70b")
 
 
 def parse_args(argv=None):
@@ -51,7 +53,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="llama7b_b32",
                    choices=["tiny", "llama7b_b32", "gqa70b_b64", "longctx_b8_f16", "longctx_b8_fp8",
-                            "shared_prefix_16x4"])
+                            "shared_prefix_16x4"] + list(PREFILL_CONFIGS))
     p.add_argument("--split", type=int, default=0, help="split_tokens (0 = library choice)")
     p.add_argument("--e2e-steps", type=int, default=300)
     p.add_argument("--unfused", action="store_true",
@@ -817,6 +819,229 @@ def run_e2e(st, args, stream):
             "api": "paged_kv_cache_191_gb300.ops (pinned host buffers, stream sync per step)"}
 
 
+# ---- multi-token workloads (chunked prefill, speculative verify) ------------------
+def prefill_cost(w):
+    """(algorithmic bytes, flops) of one pa_chunked_prefill launch: K+V of every
+    context token of every (sequence, kv head) once, Q, out, tables, lengths;
+    4 * D flops per (query row, visible key)."""
+    e = 2
+    lens = np.asarray(w.context_lens, dtype=np.int64)
+    ql = np.asarray(w.q_lens, dtype=np.int64)
+    kv = int(lens.sum()) * w.Hkv * w.D * 2 * e
+    io = w.T * w.Hq * w.D * 2 * e
+    meta = int(((lens + 15) // 16).sum()) * 4 + len(lens) * 8 + 4
+    # visible keys of query i of sequence b: L_b - n_b + i + 1
+    keys = int(sum(n * (L - n) + n * (n + 1) // 2 for L, n in zip(lens, ql)))
+    return kv + io + meta, 4 * w.D * w.Hq * keys
+
+
+class PrefillStep:
+    """One step: pa_cache_write of every query token's K/V into the slots the
+    block manager assigned, then pa_chunked_prefill over the paged context.
+    The block manager admits each sequence's prior context and appends its
+    chunk once at set-up; every step rewrites the same slots with the same
+    values, so each timed step sees the same workload."""
+
+    def __init__(self, w, split_tokens, device):
+        import torch
+        from paged_kv_cache_191_gb300 import ops
+        self.torch, self.ops, self.L, self.w, self.dev = torch, ops, ops.lib(), w, device
+        alloc = ops.BlockAllocator(w.num_blocks, w.free_order)
+        slots = []
+        for b in range(w.B):
+            n, L = int(w.q_lens[b]), int(w.context_lens[b])
+            alloc.alloc_seq(b, L - n)
+            s, _ = alloc.append_tokens(b, n)
+            slots.extend(s)
+        self.cap = w.block_tables.shape[1]
+        tables, lens = alloc.tables(list(range(w.B)), self.cap)
+        if not np.array_equal(tables, w.block_tables) or not np.array_equal(lens, w.context_lens):
+            raise RuntimeError("block manager tables differ from the workload's")
+        slots = np.asarray(slots, dtype=np.int64)
+        blk, row = slots // 16, slots % 16
+        # the rows the chunk writes are the values the pool holds there
+        new_k = w.k_pool[blk, :, row, :].contiguous()
+        new_v = w.v_pool[blk, :, row, :].contiguous()
+        self.kc, self.vc = w.k_pool.to(device), w.v_pool.to(device)
+        self.q = w.q.to(device)
+        self.new_k, self.new_v = new_k.to(device), new_v.to(device)
+        self.h_q, self.h_k, self.h_v = w.q.pin_memory(), new_k.pin_memory(), new_v.pin_memory()
+        self.slots = torch.from_numpy(slots).to(device)
+        self.q_start = torch.from_numpy(w.q_start.astype(np.int32)).to(device)
+        self.tables = torch.from_numpy(tables.astype(np.int32)).to(device)
+        self.lens = torch.from_numpy(lens.astype(np.int32)).to(device)
+        self.out = torch.empty_like(self.q)
+        self.max_len = int(lens.max())
+        self.max_q = int(w.q_lens.max())
+        self.split = split_tokens
+        desc = ops.cache_desc(self.kc)
+        self.ws_bytes = int(self.L.pa_chunked_prefill_workspace_size(w.T, w.B, w.Hq, self.max_q, self.max_len,
+                                                                     C.byref(desc), split_tokens))
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        self.bytes, self.flops = prefill_cost(w)
+        self.write_bytes = 2 * w.T * w.Hkv * w.D * 2 * 2 + w.T * 8
+
+    def enqueue(self, stream, ev=None, q=None, k=None, v=None):
+        ops = self.ops
+        ops.cache_write(k if k is not None else self.new_k, v if v is not None else self.new_v, self.slots,
+                        self.kc, self.vc, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        ops.chunked_prefill(q if q is not None else self.q, self.q_start, self.kc, self.vc, self.tables,
+                            self.lens, self.max_len, self.max_q, self.w.scale, out=self.out, workspace=self.ws,
+                            split_tokens=self.split, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def launches_per_step(self):
+        return 2 + (1 if self.ws_bytes else 0)
+
+
+def _prefill_oracle_task(task):
+    from oracle.attention import paged_prefill
+    q, qs, kb, vb, L, scale = task
+    tab = np.arange(kb.shape[0], dtype=np.int64)[None, :]
+    paged_prefill(q, qs, kb, vb, tab, np.array([L]), scale)
+    return L
+
+
+def prefill_oracle_tasks(w):
+    """Per-sequence oracle inputs (that sequence's blocks and query tokens)."""
+    from paged_kv_cache_191_gb300.workloads import BLOCK
+    tasks, per = [], []
+    qs = w.q_start
+    for b in range(w.B):
+        L, n = int(w.context_lens[b]), int(w.q_lens[b])
+        blocks = w.block_tables[b][: -(-L // BLOCK)]
+        f = (lambda t: t.float().numpy() if str(t.dtype) == "torch.bfloat16" else t.numpy())
+        tasks.append((f(w.q[qs[b]:qs[b + 1]]), [0, n], f(w.k_pool[blocks]), f(w.v_pool[blocks]), L, w.scale))
+        sub = type("S", (), {})()
+        sub.context_lens, sub.q_lens, sub.Hkv, sub.Hq, sub.D, sub.T = [L], [n], w.Hkv, w.Hq, w.D, n
+        per.append(prefill_cost(sub)[0])
+    return tasks, per
+
+
+def run_prefill(args, rank, world, local_rank):
+    import torch
+    from paged_kv_cache_191_gb300 import workloads as W
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = W.PREFILL_CONFIGS[args.config]()
+    st = PrefillStep(w, args.split, dev)
+    stream = torch.cuda.Stream(device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            st.enqueue(stream)
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        t0e.record(stream)
+        for i in range(args.steps):
+            st.enqueue(stream, evs[i])
+        t1e.record(stream)
+        stream.synchronize()
+        wall1 = time.time()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.stop()
+    errs = st.ops.device_errors(clear=True)
+    if errs:
+        raise RuntimeError(f"device error flags {errs:#x} during the benchmark")
+    local_s = t0e.elapsed_time(t1e) / 1e3
+    k_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    step_bytes = st.bytes + st.write_bytes
+    max_s, tot_bytes = aggregate(local_s, float(step_bytes * args.steps), world)
+    _, tot_tokens = aggregate(local_s, float(w.T * args.steps), world)
+
+    # e2e: public API with pinned host q / new K/V in and the output back, synced per step
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    hout = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(st.q), torch.empty_like(st.new_k), torch.empty_like(st.new_v)
+    with torch.cuda.stream(stream):
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            dq.copy_(st.h_q, non_blocking=True)
+            dk.copy_(st.h_k, non_blocking=True)
+            dv.copy_(st.h_v, non_blocking=True)
+            st.enqueue(stream, q=dq, k=dk, v=dv)
+            hout.copy_(st.out, non_blocking=True)
+            stream.synchronize()
+        t1 = time.perf_counter()
+    h2d = sum(t.numel() * t.element_size() for t in (st.h_q, st.h_k, st.h_v))
+    e2e = {"value": round(step_bytes * n_e2e / (t1 - t0) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size()),
+           "steps": n_e2e, "tokens_per_s": round(w.T * n_e2e / (t1 - t0), 1),
+           "api": "paged_kv_cache_191_gb300.ops (pinned host buffers, stream sync per step)"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tasks, per = prefill_oracle_tasks(w)
+        cores = cpu_cores()
+        order = sorted(range(w.B), key=lambda b: -int(w.q_lens[b]) * int(w.context_lens[b]))
+        with _pool(cores) as pool:
+            t0 = time.perf_counter()
+            done_b = done_t = 0
+            k = 0
+            while time.perf_counter() - t0 < args.cpu_seconds and k < w.B:
+                idx = order[k:k + cores]
+                pool.map(_prefill_oracle_task, [tasks[i] for i in idx], chunksize=1)
+                done_b += sum(per[i] for i in idx)
+                done_t += sum(int(w.q_lens[i]) for i in idx)
+                k += len(idx)
+            t1 = time.perf_counter()
+        cpu = {"value": round(done_b / (t1 - t0) / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{k} of {w.B} sequences of {w.name} (all heads, heaviest first), float64 NumPy "
+                         f"oracle, spawn pool of {cores} single-threaded workers",
+               "tokens_per_s": round(done_t / (t1 - t0), 2)}
+    peak, peak_kind = hbm_peak()
+    achieved = st.bytes / (k_ms / 1e3) / 1e9
+    tflops = st.flops / (k_ms / 1e3) / 1e12
+    res = {
+        "metric": METRIC_PREFILL,
+        "value": round(tot_bytes / max_s / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s * 1e3 / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.kv_dtype + "+f32acc",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "sequences": w.B, "query_tokens": w.T, "q_heads": w.Hq, "kv_heads": w.Hkv,
+            "head_dim": w.D, "block_size": 16, "kv_dtype": w.kv_dtype,
+            "q_lens": f"{int(w.q_lens.min())}..{int(w.q_lens.max())}",
+            "context_lens": f"{int(w.context_lens.min())}..{int(w.context_lens.max())} "
+                            f"(mean {w.context_lens.mean():.0f}), chunk K/V rewritten every step",
+            "split_tokens": args.split or "auto",
+            "l2": f"no flush: K+V per step {st.bytes / 1e6:.0f} MB vs 129 MB L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "tokens_per_s": round(tot_tokens / max_s, 1),
+        "tflops_attention": round(tflops, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind, "traffic": None,
+                     "intensity_flop_per_byte": round(st.flops / st.bytes, 1),
+                     "kernel": "pa_chunked_prefill (prefill_main + prefill_reduce)",
+                     "bytes_per_launch": int(st.bytes), "flops_per_launch": int(st.flops),
+                     "launch_ms": round(k_ms, 5)},
+        "e2e": e2e,
+        "gpu_launches": st.launches_per_step() * args.steps,
+        "clocks": clocks.summary(wall0, wall1),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
 # ---- CPU oracle (baseline and reference arm) --------------------------------------
 def _oracle_task(task):
     import numpy as np  # noqa: F811
@@ -893,10 +1118,53 @@ def cpu_baseline(w, seconds):
             "tokens_per_s": round(rounds * w.B / (t1 - t0), 2)}
 
 
+def run_reference_prefill(args, world):
+    """Reference arm for the multi-token workloads: the oracle over a bounded
+    sample of sequences per step, on host cores."""
+    from paged_kv_cache_191_gb300 import workloads as W
+    w = W.PREFILL_CONFIGS[args.config]()
+    tasks, per = prefill_oracle_tasks(w)
+    cores = cpu_cores()
+    budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step
+    with _pool(cores) as pool:
+        t = time.perf_counter()
+        pool.map(_prefill_oracle_task, tasks[:cores], chunksize=1)
+        per_task = (time.perf_counter() - t) / max(1, min(cores, len(tasks))) * cores
+        n_per_step = int(max(1, min(len(tasks), budget / max(per_task / cores, 1e-6))))
+        order = [i % len(tasks) for i in range(n_per_step * (args.steps + args.warmup))]
+        k = 0
+        for _ in range(args.warmup):
+            pool.map(_prefill_oracle_task, [tasks[order[k + j]] for j in range(n_per_step)], chunksize=1)
+            k += n_per_step
+        t0 = time.perf_counter()
+        done_b = 0
+        for _ in range(args.steps):
+            idx = [order[k + j] for j in range(n_per_step)]
+            pool.map(_prefill_oracle_task, [tasks[i] for i in idx], chunksize=1)
+            done_b += sum(per[i] for i in idx)
+            k += n_per_step
+        t1 = time.perf_counter()
+    val = round(done_b / (t1 - t0) / 1e9, 4)
+    sample = (f"each step: {n_per_step} of {w.B} sequences (all {w.Hq} heads) of {w.name}, "
+              f"float64 NumPy oracle, spawn pool of {cores} workers")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_PREFILL, "value": val, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round((t1 - t0) * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sequences": w.B, "query_tokens": w.T, "q_heads": w.Hq,
+                   "kv_heads": w.Hkv, "head_dim": w.D, "kv_dtype": w.kv_dtype, "parallelism": "host cores"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def run_reference(args, rank, world):
     """Reference arm: the float64 CPU oracle on host cores, K bounded steps."""
     if rank != 0:
         return
+    if args.config in PREFILL_CONFIGS:
+        return run_reference_prefill(args, world)
     w = load_workload(args.config)
     cores = cpu_cores()
     fp8 = w.kv_dtype == "fp8"
@@ -951,6 +1219,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.config in PREFILL_CONFIGS:
+            run_prefill(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

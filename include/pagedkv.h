@@ -8,11 +8,14 @@
  *                 on-demand allocation, copy-on-write via refcounts;
  *             2.3 the attention kernel resolves the page table itself and
  *                 gathers scattered K/V, transparent to the model;
- *             5.3 FP8 KV cache with per-token or per-channel scales.
+ *             5.3 FP8 KV cache with per-token or per-channel scales;
+ *             6.1 speculative decoding: the target model verifies the draft
+ *                 tokens in one pass.
  *   [KV-CB]   "大模型推理引擎优化：KV Cache 与连续批处理" (devpress.csdn.net)
  *             2.2 16-token blocks;
  *             三   the block manager: block table, free list, refcount,
  *                 allocate / append / free / utilisation;
+ *             4.1 chunked prefill: prompt chunks run beside decode steps;
  *             4.2 copy-on-write when a shared block is written.
  *
  * Conventions shared by every call
@@ -35,7 +38,7 @@
  *   nothing.  pa_last_error() gives a message for the calling thread's last
  *   failed call.  Values that live on the device (slots, block ids, context
  *   lengths) cannot be checked on the host: the kernels bounds-check them,
- *   skip the offending access (a bad block id reads as zeros) and set a bit in
+ *   replace the offending access (a bad block id reads block 0) and set a bit in
  *   a per-device error word, read with pa_device_errors().  No kernel traps.
  * - Device pointers must be 16-byte aligned.
  */
@@ -73,6 +76,7 @@ typedef enum {
 #define PA_DEVERR_BLOCK_RANGE  0x2u  /* decode/copy: block id outside the pool */
 #define PA_DEVERR_CONTEXT_LEN  0x4u  /* decode: length < 0 or above a stated bound */
 #define PA_DEVERR_TIMEOUT      0x8u  /* a bounded barrier wait gave up */
+#define PA_DEVERR_QUERY_RANGE  0x10u /* chunked prefill: q_start out of order or range */
 
 /* Shape of a paged KV cache. */
 typedef struct {
@@ -181,6 +185,59 @@ pa_status pa_decode_append(const void* k_new, const void* v_new, int32_t new_dty
                            const pa_cache_desc* desc,
                            void* workspace, size_t workspace_bytes,
                            int32_t split_tokens, void* stream);
+
+/*
+ * pa_chunked_prefill_workspace_size -- bytes of device workspace
+ * pa_chunked_prefill needs for the same arguments; 0 when one partition
+ * covers max_context_len (or on an invalid argument).
+ */
+size_t pa_chunked_prefill_workspace_size(int32_t num_tokens, int32_t B, int32_t num_q_heads,
+                                         int32_t max_q_len, int32_t max_context_len,
+                                         const pa_cache_desc* desc, int32_t split_tokens);
+
+/*
+ * pa_chunked_prefill -- paged attention for several query tokens per
+ * sequence: a prompt chunk whose prefill runs beside decode steps ([KV-CB]
+ * 4.1), or the gamma + 1 tokens a target model checks in one pass when
+ * verifying a draft ([LLM-INF] 6.1).  Decode steps may ride in the same
+ * call as one-token chunks.
+ *
+ * The n_b = q_start[b+1] - q_start[b] query tokens of sequence b are the
+ * last n_b of its context_lens[b] = L_b tokens; their K/V must already be in
+ * the cache (pa_cache_write first).  Query token i (0 <= i < n_b) is at
+ * position L_b - n_b + i and attends, causally, to keys 0 .. L_b - n_b + i:
+ *     out[q_start[b]+i][h] = sum_t softmax_t(scale * q[q_start[b]+i][h] . K_t) V_t,
+ *                            t <= L_b - n_b + i,  kv head g = h / G.
+ * A token with no key (n_b > L_b, flagged PA_DEVERR_CONTEXT_LEN) gets a
+ * zero row.  n_b = 0 is allowed.
+ *
+ * q            device [num_tokens][num_q_heads][head_dim] in q_dtype, the
+ *              sequences' tokens packed in order.  q_dtype must equal kv_dtype
+ *              (F16 or BF16; FP8 caches return PA_ERR_UNSUPPORTED).
+ * q_start      device int32 [B + 1], q_start[0] = 0, nondecreasing,
+ *              q_start[B] <= num_tokens, each n_b <= max_q_len (else that
+ *              sequence is skipped and PA_DEVERR_QUERY_RANGE is set).
+ * max_q_len    host upper bound on n_b (<= 65535), sizes the grid.
+ * block_tables, context_lens, max_context_len, scale, desc, workspace,
+ * split_tokens  as pa_decode (split_tokens up to 4096 here).
+ * out          device [num_tokens][num_q_heads][head_dim] in out_dtype
+ *              (q_dtype or F32); rows of tokens outside every sequence's range
+ *              are not written.
+ *
+ * Work: one CTA per (sequence, kv head, 64-row tile of (token, head) rows,
+ * partition); K/V tiles of a partition are loaded once per CTA by TMA and
+ * shared by its four compute warps; partitions are merged by a second
+ * kernel when a row's keys span more than one.
+ */
+pa_status pa_chunked_prefill(const void* q, int32_t q_dtype, const int32_t* q_start,
+                             int32_t num_tokens, int32_t max_q_len,
+                             const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t max_context_len,
+                             int32_t B, int32_t num_q_heads, float scale,
+                             void* out, int32_t out_dtype, const pa_cache_desc* desc,
+                             void* workspace, size_t workspace_bytes,
+                             int32_t split_tokens, void* stream);
 
 /*
  * pa_decode_static_ws -- pa_decode that allocates nothing.  The pages have no

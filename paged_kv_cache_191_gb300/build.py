@@ -20,8 +20,8 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
           "--expt-relaxed-constexpr"]
-SOURCES = ["decode.cu", "decode_static.cu", "cache_ops.cu", "api.cpp", "allocator.cpp"]
-HEADERS = ["device_common.cuh", "pa_internal.h"]
+SOURCES = ["decode.cu", "decode_static.cu", "prefill.cu", "cache_ops.cu", "api.cpp", "allocator.cpp"]
+HEADERS = ["device_common.cuh", "pa_internal.h", "kv_map.h"]
 
 
 def nvcc():
@@ -71,7 +71,7 @@ def build(force=False, verbose=False, extra=()):
 
 if __name__ == "__main__":
     args = sys.argv[1:]
-    extra = []
+    extra = [a for a in args if a.startswith("-D")]  # tuning macros, e.g. -DPA_RING_KB=32
     if "--ptxas-v" in args:
-        extra = ["-Xptxas", "-v"]
-    print(build(force="--force" in args or bool(extra), verbose=bool(extra), extra=extra))
+        extra += ["-Xptxas", "-v"]
+    print(build(force="--force" in args or bool(extra), verbose="--ptxas-v" in args, extra=extra))

@@ -1,5 +1,6 @@
 // C-ABI entry points: host-side validation, then dispatch to the launchers.
 // Nothing is enqueued unless every host-visible argument checks out.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -74,6 +75,49 @@ pa_status plan_decode(int32_t B, int32_t Hq, int32_t max_context_len, const pa_c
   plan->item_warps = d->kv_dtype == PA_DTYPE_FP8_E4M3 ? 4 : 1;
   if (parts > 1) {
     const size_t rows = static_cast<size_t>(B) * Hq * parts;
+    size_t bytes = rows * d->head_dim * sizeof(float) + 2 * rows * sizeof(float);
+    plan->workspace_bytes = (bytes + 255) & ~static_cast<size_t>(255);
+  } else {
+    plan->workspace_bytes = 0;
+  }
+  return PA_OK;
+}
+
+pa_status plan_prefill(int32_t T, int32_t B, int32_t Hq, int32_t max_q_len, int32_t max_context_len,
+                       const pa_cache_desc* d, int32_t split_tokens, PrefillPlan* plan) {
+  const int64_t G = Hq / d->num_kv_heads;
+  const int64_t nblk_max = max_context_len <= 0 ? 1 : (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+  const int64_t tiles = max_q_len <= 0 ? 1 : (static_cast<int64_t>(max_q_len) * G + 63) / 64;
+  int64_t bpp;
+  if (split_tokens > 0) {
+    if (split_tokens % PA_BLOCK_SIZE || split_tokens > 4096)
+      return fail(PA_ERR_INVALID, "split_tokens must be a multiple of 16 in [16, 4096]");
+    bpp = split_tokens / PA_BLOCK_SIZE;
+  } else {
+    // Row tiles that can hold rows: at most one partial tile per sequence
+    // beyond the T * G / 64 full ones.  With eight or more such tiles per SM
+    // the grid is full without splitting the context (a split costs partial
+    // rows written and merged); otherwise 1024-token partitions, halved
+    // while the grid would give fewer than four CTAs per SM.
+    const int64_t units =
+        d->num_kv_heads * std::min<int64_t>(static_cast<int64_t>(B) * tiles, (static_cast<int64_t>(T) * G + 63) / 64 + B);
+    const int64_t sms = sm_count();
+    if (units >= 8 * sms) {
+      bpp = std::max<int64_t>(nblk_max, 1);
+    } else {
+      bpp = 64;
+      while (bpp > 8 && units * ((nblk_max + bpp - 1) / bpp) < 4 * sms) bpp /= 2;
+    }
+  }
+  const int64_t parts = (nblk_max + bpp - 1) / bpp;
+  if (parts > 65535) return fail(PA_ERR_UNSUPPORTED, "context too long for the partition grid");
+  if (static_cast<int64_t>(B) * d->num_kv_heads * tiles > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "too many row tiles for one grid");
+  plan->row_tiles = static_cast<int32_t>(tiles);
+  plan->blocks_per_part = static_cast<int32_t>(bpp);
+  plan->max_parts = static_cast<int32_t>(parts);
+  if (parts > 1) {
+    const size_t rows = static_cast<size_t>(T) * Hq * parts;
     size_t bytes = rows * d->head_dim * sizeof(float) + 2 * rows * sizeof(float);
     plan->workspace_bytes = (bytes + 255) & ~static_cast<size_t>(255);
   } else {
@@ -241,6 +285,91 @@ pa_status pa_decode_append(const void* k_new, const void* v_new, int32_t new_dty
                      workspace_bytes, split_tokens, stream, k_new, v_new, new_dtype, slot_mapping);
 }
 
+static pa_status check_prefill(int32_t T, int32_t B, int32_t num_q_heads, int32_t max_q_len,
+                               int32_t max_context_len, const pa_cache_desc* desc) {
+  pa_status st = pa::check_desc(desc, "pa_chunked_prefill");
+  if (st != PA_OK) return st;
+  if (T < 0 || B < 0 || num_q_heads <= 0 || max_q_len < 0 || max_context_len < 0)
+    return fail(PA_ERR_INVALID, "pa_chunked_prefill: negative size or num_q_heads <= 0");
+  if (T > 0 && max_q_len == 0) return fail(PA_ERR_INVALID, "pa_chunked_prefill: max_q_len is 0 with tokens");
+  if (max_q_len > 65535) return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: max_q_len above 65535");
+  if (num_q_heads % desc->num_kv_heads)
+    return fail(PA_ERR_INVALID, "pa_chunked_prefill: num_q_heads must be a multiple of num_kv_heads");
+  if (num_q_heads / desc->num_kv_heads > PA_MAX_GROUP)
+    return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: more than %d query heads per kv head", PA_MAX_GROUP);
+  if (desc->kv_dtype == PA_DTYPE_FP8_E4M3)
+    return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: FP8 caches are not built");
+  return PA_OK;
+}
+
+size_t pa_chunked_prefill_workspace_size(int32_t num_tokens, int32_t B, int32_t num_q_heads,
+                                         int32_t max_q_len, int32_t max_context_len,
+                                         const pa_cache_desc* desc, int32_t split_tokens) {
+  if (check_prefill(num_tokens, B, num_q_heads, max_q_len, max_context_len, desc) != PA_OK) return 0;
+  pa::PrefillPlan plan;
+  if (pa::plan_prefill(num_tokens, B, num_q_heads, max_q_len, max_context_len, desc, split_tokens, &plan) !=
+      PA_OK)
+    return 0;
+  return plan.workspace_bytes;
+}
+
+pa_status pa_chunked_prefill(const void* q, int32_t q_dtype, const int32_t* q_start, int32_t num_tokens,
+                             int32_t max_q_len, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t max_context_len, int32_t B,
+                             int32_t num_q_heads, float scale, void* out, int32_t out_dtype,
+                             const pa_cache_desc* desc, void* workspace, size_t workspace_bytes,
+                             int32_t split_tokens, void* stream) {
+  pa_status st = check_prefill(num_tokens, B, num_q_heads, max_q_len, max_context_len, desc);
+  if (st != PA_OK) return st;
+  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID, "pa_chunked_prefill: max_blocks_per_seq <= 0");
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "pa_chunked_prefill: scale is not finite");
+  if (q_dtype != desc->kv_dtype) return fail(PA_ERR_INVALID, "pa_chunked_prefill: q_dtype must equal kv_dtype");
+  if (out_dtype != q_dtype && out_dtype != PA_DTYPE_F32)
+    return fail(PA_ERR_INVALID, "pa_chunked_prefill: out_dtype must be q_dtype or F32");
+  if (B == 0 || num_tokens == 0) return PA_OK;
+  if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return fail(PA_ERR_INVALID, "pa_chunked_prefill: null pointer");
+  if (!pa::aligned16(q) || !pa::aligned16(k_cache) || !pa::aligned16(v_cache) || !pa::aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(q_start) & 3u) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PA_ERR_INVALID, "pa_chunked_prefill: misaligned pointer");
+  pa::PrefillPlan plan;
+  st = pa::plan_prefill(num_tokens, B, num_q_heads, max_q_len, max_context_len, desc, split_tokens, &plan);
+  if (st != PA_OK) return st;
+  if (plan.workspace_bytes) {
+    if (!workspace || !pa::aligned16(workspace))
+      return fail(PA_ERR_INVALID, "pa_chunked_prefill: workspace NULL or misaligned (%zu bytes needed)",
+                  plan.workspace_bytes);
+    if (workspace_bytes < plan.workspace_bytes)
+      return fail(PA_ERR_INVALID, "pa_chunked_prefill: workspace has %zu bytes, %zu needed", workspace_bytes,
+                  plan.workspace_bytes);
+  }
+  pa::PrefillLaunch a;
+  a.q = q;
+  a.q_start = q_start;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.max_context_len = max_context_len;
+  a.max_q_len = max_q_len;
+  a.B = B;
+  a.T = num_tokens;
+  a.Hq = num_q_heads;
+  a.Hkv = desc->num_kv_heads;
+  a.D = desc->head_dim;
+  a.num_blocks = desc->num_blocks;
+  a.kv_dtype = desc->kv_dtype;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.workspace = workspace;
+  a.plan = plan;
+  return pa::launch_prefill(a, stream);
+}
+
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                          const int64_t* pairs, int64_t num_pairs, const pa_cache_desc* desc,
                          void* stream) {
@@ -288,12 +417,14 @@ pa_status pa_swap_blocks(void* dst_k, void* dst_v, float* dst_k_scale, float* ds
 
 pa_status pa_device_errors(uint32_t* flags, int32_t clear) {
   if (!flags) return fail(PA_ERR_INVALID, "pa_device_errors: flags is NULL");
-  uint32_t a = 0, b = 0;
+  uint32_t a = 0, b = 0, c = 0;
   pa_status st = pa::read_errors_decode(&a, clear != 0);
   if (st != PA_OK) return st;
   st = pa::read_errors_cache_ops(&b, clear != 0);
   if (st != PA_OK) return st;
-  *flags = a | b;
+  st = pa::read_errors_prefill(&c, clear != 0);
+  if (st != PA_OK) return st;
+  *flags = a | b | c;
   return PA_OK;
 }
 

@@ -38,6 +38,7 @@
 #include <mutex>
 
 #include "device_common.cuh"
+#include "kv_map.h"
 #include "pa_internal.h"
 
 namespace pa {
@@ -49,7 +50,6 @@ __device__ uint32_t g_decode_err;
 #define PA_RING_KB 16  // two 8 KB stages for 16-bit D=128: ~12 CTAs per SM
 #endif
 constexpr int kRingBytes = PA_RING_KB * 1024;  // K/V stage ring of one warp-CTA
-constexpr int kMaxBpp = 64;
 constexpr int kMaxDevices = 64;
 
 struct DecodeArgs {
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(32 * W)
       const uint4 X = dev::lds128(vb + swz(tt, r));
       const uint4 Y = dev::lds128(vb + swz(tt + 1, r));
       const uint4 Z = dev::lds128(vb + swz(tt + 8, r));
-      const uint4 W = dev::lds128(vb + swz(tt + 9, r));
+      const uint4 Wq = dev::lds128(vb + swz(tt + 9, r));
       c_r *= s_scale[s * 32 + r];
       c_r8 *= s_scale[s * 32 + r + 8];
       vs_r = s_scale[s * 32 + 16 + r];
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(32 * W)
         kf[kk][1] = wr8[kk];
       }
       const uint32_t xw[4] = {X.x, X.y, X.z, X.w}, yw[4] = {Y.x, Y.y, Y.z, Y.w};
-      const uint32_t zw[4] = {Z.x, Z.y, Z.z, Z.w}, ww[4] = {W.x, W.y, W.z, W.w};
+      const uint32_t zw[4] = {Z.x, Z.y, Z.z, Z.w}, ww[4] = {Wq.x, Wq.y, Wq.z, Wq.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         vf[i][0] = xw[i];
@@ -657,52 +657,11 @@ __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce(const DecodeA
 }
 
 // ---- host side -------------------------------------------------------------------
-// ---- host side -------------------------------------------------------------------
-// ---- host side -------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// Tensor map over a cache viewed as [num_blocks][Hkv*16 rows][D], box = one
-// 128-byte span of 16 rows (one kv head of one block), 128-byte swizzle.
 template <typename KT, int D>
 pa_status make_map(CUtensorMap* m, const void* cache, int Hkv, int num_blocks, CUtensorMapDataType dt) {
   using TL = Tile<KT, D>;
-  auto fn = encode_fn();
-  if (!fn) return fail(PA_ERR_CUDA, "pa_decode: cuTensorMapEncodeTiled unavailable");
-  CUresult r;
-  if constexpr (TL::ONE_BOX) {
-    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(TL::BOXE), 16, 2, static_cast<cuuint64_t>(Hkv),
-                                static_cast<cuuint64_t>(num_blocks)};
-    const cuuint64_t strides[4] = {static_cast<cuuint64_t>(TL::ROWB), 128,
-                                   static_cast<cuuint64_t>(TL::ROWB) * 16,
-                                   static_cast<cuuint64_t>(TL::ROWB) * 16 * Hkv};
-    const cuuint32_t box[5] = {static_cast<cuuint32_t>(TL::BOXE), 16, 2, 1, 1};
-    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    r = fn(m, dt, 5, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  } else {
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(16) * Hkv,
-                                static_cast<cuuint64_t>(num_blocks)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(TL::ROWB),
-                                   static_cast<cuuint64_t>(TL::ROWB) * 16 * Hkv};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(TL::BOXE), 16, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    r = fn(m, dt, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  }
-  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "pa_decode: tensor map encode failed (%d)", static_cast<int>(r));
-  return PA_OK;
+  static_assert(TL::ONE_BOX == (TL::ROWB == 256), "the 5-D box covers exactly two swizzle spans");
+  return make_kv_map(m, cache, Hkv, num_blocks, TL::ROWB, static_cast<int>(sizeof(KT)), dt, "pa_decode");
 }
 
 template <typename KT, typename QT, int D>
@@ -783,6 +742,47 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
 }
 
 }  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+pa_status make_kv_map(CUtensorMap* m, const void* cache, int Hkv, int num_blocks, int row_bytes,
+                      int elem_bytes, CUtensorMapDataType dt, const char* what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PA_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", what);
+  if (row_bytes != 128 && row_bytes != 256) return fail(PA_ERR_UNSUPPORTED, "%s: row of %d bytes", what, row_bytes);
+  const cuuint64_t boxe = static_cast<cuuint64_t>(128 / elem_bytes);  // elements per 128-byte span
+  const cuuint64_t rowb = static_cast<cuuint64_t>(row_bytes);
+  CUresult r;
+  if (row_bytes == 256) {
+    const cuuint64_t dims[5] = {boxe, 16, 2, static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[4] = {rowb, 128, rowb * 16, rowb * 16 * Hkv};
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(boxe), 16, 2, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    r = fn(m, dt, 5, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[3] = {boxe, static_cast<cuuint64_t>(16) * Hkv, static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[2] = {rowb, rowb * 16 * Hkv};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(boxe), 16, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(m, dt, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "%s: tensor map encode failed (%d)", what, static_cast<int>(r));
+  return PA_OK;
+}
 
 pa_status launch_decode(const DecodeLaunch& l, void* stream_ptr) {
   cudaStream_t st = static_cast<cudaStream_t>(stream_ptr);

@@ -66,6 +66,35 @@ struct DecodeLaunch {
 };
 pa_status launch_decode(const DecodeLaunch& a, void* stream);
 
+// Split-K plan for one pa_chunked_prefill shape.
+struct PrefillPlan {
+  int32_t row_tiles;        // 64-row tiles per (sequence, kv head) for max_q_len
+  int32_t blocks_per_part;  // 16-token blocks per partition
+  int32_t max_parts;        // partitions of the longest allowed context
+  size_t workspace_bytes;   // 0 when max_parts == 1
+};
+pa_status plan_prefill(int32_t num_tokens, int32_t B, int32_t num_q_heads, int32_t max_q_len,
+                       int32_t max_context_len, const pa_cache_desc* desc, int32_t split_tokens,
+                       PrefillPlan* plan);
+
+struct PrefillLaunch {
+  const void* q;
+  const int32_t* q_start;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const int32_t* context_lens;
+  int32_t max_context_len, max_q_len;
+  int32_t B, T, Hq, Hkv, D, num_blocks, kv_dtype;
+  float scale;
+  void* out;
+  int32_t out_dtype;
+  void* workspace;
+  PrefillPlan plan;
+};
+pa_status launch_prefill(const PrefillLaunch& a, void* stream);
+
 pa_status launch_cache_write(const void* k, const void* v, int32_t in_dtype,
                              const int64_t* slots, int64_t T, void* k_cache, void* v_cache,
                              float* k_scale, float* v_scale, const pa_cache_desc* d,
@@ -101,5 +130,6 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 // Per-translation-unit device error words, OR-ed by pa_device_errors.
 pa_status read_errors_decode(uint32_t* flags, bool clear);
 pa_status read_errors_cache_ops(uint32_t* flags, bool clear);
+pa_status read_errors_prefill(uint32_t* flags, bool clear);
 
 }  // namespace pa

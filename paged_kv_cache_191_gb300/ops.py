@@ -19,6 +19,7 @@ PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_NOT_FOUND, PA_ERR_UNSUPPORTED, PA_ERR_
 F16, BF16, FP8_E4M3, F32 = 0, 1, 2, 3
 BLOCK_SIZE = 16
 DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_QUERY_RANGE = 16
 
 _TORCH_DT = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
              torch.uint8: FP8_E4M3, torch.float8_e4m3fn: FP8_E4M3}
@@ -59,6 +60,10 @@ SIGNATURES = {
                                    _I32, _F, _P, _I32, C.POINTER(CacheDesc), _P, C.c_size_t, _I32, _P]),
     "pa_decode_static_ws": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F, _P,
                                       _I32, C.POINTER(CacheDesc), _I32, _P]),
+    "pa_chunked_prefill_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32, C.POINTER(CacheDesc),
+                                                       _I32]),
+    "pa_chunked_prefill": (C.c_int, [_P, _I32, _P, _I32, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F,
+                                     _P, _I32, C.POINTER(CacheDesc), _P, C.c_size_t, _I32, _P]),
     "pa_copy_blocks": (C.c_int, [_P, _P, _P, _P, _P, _I64, C.POINTER(CacheDesc), _P]),
     "pa_swap_blocks": (C.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _I32, _P, _I64,
                                  C.POINTER(CacheDesc), _P]),
@@ -197,6 +202,49 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, sca
                            _ptr(context_lens), int(max_context_len), B, Hq, float(scale),
                            _ptr(out), _TORCH_DT[odt], C.byref(desc), _ptr(workspace), ws_bytes,
                            int(split_tokens), _stream(stream)), "pa_decode")
+    return out
+
+
+def chunked_prefill(q, q_start, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                    max_q_len, scale, out=None, out_dtype=None, workspace=None, split_tokens=0,
+                    stream=None):
+    """Multi-token paged attention (chunked prefill / speculative verify).
+
+    q: [T, Hq, D] packed query tokens; q_start: int32 [B + 1] offsets.
+    Returns out [T, Hq, D] (q dtype, or out_dtype).
+    """
+    for t, n in ((q, "q"), (q_start, "q_start"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (context_lens, "context_lens")):
+        _dev(t, n)
+    desc = cache_desc(k_cache)
+    T, Hq, D = q.shape
+    B = context_lens.numel()
+    if D != desc.head_dim:
+        raise ValueError("q head_dim differs from the cache")
+    if q_start.dtype != torch.int32 or q_start.numel() != B + 1:
+        raise ValueError("q_start must be int32 [B + 1]")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be int32 [B, max_blocks]")
+    if context_lens.dtype != torch.int32:
+        raise ValueError("context_lens must be int32 [B]")
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=odt, device=q.device)
+    else:
+        _dev(out, "out")
+        if out.shape != (T, Hq, D):
+            raise ValueError("out must be [T, Hq, D]")
+        odt = out.dtype
+    need = int(lib().pa_chunked_prefill_workspace_size(T, B, Hq, int(max_q_len), int(max_context_len),
+                                                       C.byref(desc), int(split_tokens)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().pa_chunked_prefill(_ptr(q), _TORCH_DT[q.dtype], _ptr(q_start), T, int(max_q_len),
+                                    _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                                    _ptr(context_lens), int(max_context_len), B, Hq, float(scale),
+                                    _ptr(out), _TORCH_DT[odt], C.byref(desc), _ptr(workspace), ws_bytes,
+                                    int(split_tokens), _stream(stream)), "pa_chunked_prefill")
     return out
 
 

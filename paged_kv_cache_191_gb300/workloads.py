@@ -204,6 +204,96 @@ def random_pairs(seed, num_blocks, n):
     return ids.reshape(n, 2)
 
 
+@dataclass
+class PrefillWorkload:
+    """Several query tokens per sequence: the last q_lens[b] of its context."""
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    kv_dtype: str
+    context_lens: np.ndarray      # int32 [B], includes the chunk
+    q_lens: np.ndarray            # int32 [B]
+    num_blocks: int
+    free_order: np.ndarray
+    block_tables: np.ndarray      # int32 [B, max_blocks], -1 padded
+    q: torch.Tensor               # [T, Hq, D], sequences' tokens packed in order
+    k_pool: torch.Tensor          # [num_blocks, Hkv, 16, D] (chunk K/V included)
+    v_pool: torch.Tensor
+    scale: float
+
+    @property
+    def B(self):
+        return len(self.context_lens)
+
+    @property
+    def q_start(self):
+        return np.concatenate([[0], np.cumsum(self.q_lens)]).astype(np.int32)
+
+    @property
+    def T(self):
+        return int(self.q_lens.sum())
+
+    @property
+    def G(self):
+        return self.Hq // self.Hkv
+
+
+def make_prefill(name, seed, Hq, Hkv, D, kv_dtype, ctx_lens, q_lens, pool_factor=1.2, extra_blocks=0):
+    rng = rng_for(seed)
+    lens = np.asarray(ctx_lens, dtype=np.int32)
+    ql = np.asarray(q_lens, dtype=np.int32)
+    demand = int(sum(-(-int(n) // BLOCK) for n in lens))
+    num_blocks = max(int(math.ceil(pool_factor * demand)) + extra_blocks, 1)
+    order = rng.permutation(num_blocks).astype(np.int64)
+    mb = max(1, max(-(-int(n) // BLOCK) for n in lens))
+    tables = _tables_from_order(order, lens, mb)
+    tdt = KV_TORCH[kv_dtype]
+    q = randn(rng, (int(ql.sum()), Hq, D), tdt)
+    k_pool = randn(rng, (num_blocks, Hkv, BLOCK, D), tdt)
+    v_pool = randn(rng, (num_blocks, Hkv, BLOCK, D), tdt)
+    return PrefillWorkload(name, Hq, Hkv, D, kv_dtype, lens, ql, num_blocks, order, tables, q,
+                           k_pool, v_pool, 1.0 / math.sqrt(D))
+
+
+def config_prefill_mix(chunks=4, chunk=512, decodes=28):
+    """LLaMA-7B shapes (32/32 heads, D=128, fp16): `chunks` prompt chunks of
+    `chunk` tokens at prior contexts uniform in [0, 4096 - chunk], batched with
+    `decodes` one-token decode steps at contexts uniform in [1, 2048]."""
+    rng = rng_for(SEED_BASE + 6)
+    prior = rng.integers(0, 4096 - chunk, size=chunks, endpoint=True)
+    dec = rng.integers(1, 2048, size=decodes, endpoint=True)
+    ctx = np.concatenate([prior + chunk, dec])
+    ql = np.concatenate([np.full(chunks, chunk), np.ones(decodes, dtype=np.int64)])
+    return make_prefill("prefill_mix_llama7b", SEED_BASE + 6 + 100, 32, 32, 128, "f16", ctx, ql)
+
+
+def config_spec_verify(B=64, gamma=4):
+    """GQA-70B shapes (64 q / 8 kv heads, D=128, bf16): each of B sequences
+    verifies gamma draft tokens plus the bonus token (gamma + 1 queries) at
+    contexts log-uniform in [16, 4096]."""
+    rng = rng_for(SEED_BASE + 7)
+    base = np.rint(np.exp(rng.uniform(math.log(16), math.log(4096), size=B))).astype(np.int64)
+    ql = np.full(B, gamma + 1)
+    return make_prefill("spec_verify_gqa70b", SEED_BASE + 7 + 100, 64, 8, 128, "bf16", base + gamma + 1, ql)
+
+
+def random_prefill_small(seed, Hq, Hkv, D, kv_dtype, q_lens, max_prior=80):
+    """Small ragged multi-token case: each sequence's context is its chunk
+    plus a prior context uniform in [0, max_prior]."""
+    rng = rng_for(seed)
+    ql = np.asarray(q_lens, dtype=np.int64)
+    prior = rng.integers(0, max_prior, size=len(ql), endpoint=True)
+    return make_prefill(f"prefill{seed}", seed + 11, Hq, Hkv, D, kv_dtype, prior + ql, ql,
+                        pool_factor=1.0, extra_blocks=3)
+
+
+PREFILL_CONFIGS = {
+    "prefill_mix_llama7b": config_prefill_mix,
+    "spec_verify_gqa70b": config_spec_verify,
+}
+
+
 CONFIGS = {
     "tiny": config_tiny,
     "llama7b_b32": config_llama7b,

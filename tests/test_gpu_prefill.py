@@ -1,0 +1,160 @@
+"""GPU parity of pa_chunked_prefill (multi-token paged attention) against the
+float64 oracle.
+
+Tolerance as for decode: max-abs 2e-3 on float32 outputs for f16 / bf16
+caches; 16-bit outputs within 2e-3 plus half an ulp of the output dtype.
+Small ragged cases (chunks of 0 .. 130 tokens, several row tiles, ragged
+tails, forced partition sizes) are compared element by element; the two
+full-size workloads on sampled (token, head) rows in the launch
+configuration the benchmark uses.  A prompt run as several chunks must give
+bit-identical rows to one chunk (same partition size): each row's
+arithmetic does not depend on the other rows of its tile.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle.attention import paged_prefill
+from paged_kv_cache_191_gb300 import ops, workloads as W
+from tests.gpu_util import TOL, np_exact, half_ulp, assert_close, requires_cuda
+
+pytestmark = [pytest.mark.gpu, requires_cuda]
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def no_device_errors():
+    ops.device_errors(clear=True)
+    yield
+    assert ops.device_errors(clear=True) == 0, "kernel flagged a device error"
+
+
+def _dev_inputs(w, q_start=None, lens=None):
+    qs = w.q_start if q_start is None else q_start
+    lens = w.context_lens if lens is None else lens
+    return (w.q.to(DEV), torch.from_numpy(np.ascontiguousarray(qs, dtype=np.int32)).to(DEV),
+            w.k_pool.to(DEV), w.v_pool.to(DEV),
+            torch.from_numpy(np.ascontiguousarray(w.block_tables, dtype=np.int32)).to(DEV),
+            torch.from_numpy(np.ascontiguousarray(lens, dtype=np.int32)).to(DEV))
+
+
+def gpu_prefill(w, out_dtype=torch.float32, split_tokens=0, q_start=None, lens=None, max_q_len=None):
+    q, qs, kc, vc, bt, cl = _dev_inputs(w, q_start, lens)
+    lens_np = w.context_lens if lens is None else lens
+    ml = max(int(max(lens_np)), 1)
+    mq = int(w.q_lens.max()) if max_q_len is None else max_q_len
+    desc = ops.cache_desc(kc)
+    need = int(ops.lib().pa_chunked_prefill_workspace_size(q.shape[0], len(lens_np), q.shape[1], mq, ml,
+                                                          ops.C.byref(desc), split_tokens))
+    # scratch starts as 0xFF bytes (NaN floats): stale rows must never leak into results
+    ws = torch.full((max(need, 16),), 255, dtype=torch.uint8, device=DEV)
+    out = torch.full((q.shape[0], q.shape[1], q.shape[2]), float("nan"), dtype=out_dtype, device=DEV)
+    ops.chunked_prefill(q, qs, kc, vc, bt, cl, ml, mq, w.scale, out=out, workspace=ws,
+                        split_tokens=split_tokens)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def oracle(w, rows=None, q_start=None, lens=None):
+    return paged_prefill(np_exact(w.q), w.q_start if q_start is None else q_start, np_exact(w.k_pool),
+                         np_exact(w.v_pool), w.block_tables, w.context_lens if lens is None else lens,
+                         w.scale, rows=rows)
+
+
+SHAPES = [  # Hq, Hkv, D, kv dtype
+    (4, 4, 64, "f16"), (8, 2, 128, "f16"), (8, 1, 128, "bf16"), (64, 8, 128, "bf16"),
+    (32, 32, 128, "f16"), (6, 2, 64, "bf16"), (3, 1, 128, "f16"),
+]
+QLENS = [[1, 17, 64, 65], [130, 0, 3, 1, 40], [5, 5, 5, 5, 5, 5], [33]]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"{s[0]}x{s[1]}x{s[2]}{s[3]}")
+@pytest.mark.parametrize("qi", range(len(QLENS)))
+@pytest.mark.parametrize("split", [0, 16, 48])
+def test_small_ragged(shape, qi, split):
+    Hq, Hkv, D, dt = shape
+    w = W.random_prefill_small(100 + 7 * qi + Hq, Hq, Hkv, D, dt, QLENS[qi], max_prior=90)
+    ref = oracle(w)
+    out = gpu_prefill(w, split_tokens=split)
+    assert_close(out.numpy(), ref, TOL[dt], f"{shape} q_lens {QLENS[qi]} split {split}")
+
+
+@pytest.mark.parametrize("shape", [(8, 2, 128, "f16"), (8, 1, 128, "bf16"), (4, 4, 64, "bf16")])
+def test_16bit_output(shape):
+    Hq, Hkv, D, dt = shape
+    w = W.random_prefill_small(7, Hq, Hkv, D, dt, [70, 1, 9], max_prior=200)
+    ref = oracle(w)
+    out = gpu_prefill(w, out_dtype=w.q.dtype, split_tokens=64).float().numpy()
+    err = np.abs(out - ref)
+    assert np.all(err <= TOL[dt] + half_ulp(ref, w.q.dtype)), float(err.max())
+
+
+def test_chunks_equal_one_pass_bitwise():
+    """A 300-token prompt (after 37 tokens of prior context) run as chunks of
+    100, 64, 1, 135 with growing context gives the rows of one 300-token pass."""
+    Hq, Hkv, D = 16, 4, 128
+    prior = 37
+    L = prior + 300
+    w = W.make_prefill("p", 99, Hq, Hkv, D, "bf16", [L], [300])
+    whole = gpu_prefill(w, split_tokens=64)
+    pieces, done = [], 0
+    for c in (100, 64, 1, 135):
+        sub = W.PrefillWorkload("c", Hq, Hkv, D, "bf16", np.array([prior + done + c], np.int32),
+                                np.array([c], np.int32), w.num_blocks, w.free_order, w.block_tables,
+                                w.q[done:done + c].contiguous(), w.k_pool, w.v_pool, w.scale)
+        pieces.append(gpu_prefill(sub, split_tokens=64))
+        done += c
+    assert torch.equal(torch.cat(pieces), whole)
+    assert_close(whole.numpy(), oracle(w), TOL["bf16"], "one pass")
+
+
+def test_single_token_chunks_match_oracle_decode_rows():
+    w = W.random_prefill_small(31, 8, 2, 128, "f16", [1] * 9, max_prior=300)
+    assert_close(gpu_prefill(w).numpy(), oracle(w), TOL["f16"], "one-token chunks")
+
+
+def test_more_queries_than_context_gives_zero_rows_and_flags():
+    w = W.random_prefill_small(41, 4, 2, 64, "f16", [20, 6], max_prior=0)
+    lens = np.array([12, 6], np.int32)  # sequence 0: 20 queries, 12 keys
+    out = gpu_prefill(w, lens=lens)
+    assert ops.device_errors(clear=True) & ops.DEVERR_CONTEXT_LEN
+    ref = oracle(w, lens=lens)
+    assert_close(out.numpy(), ref, TOL["f16"], "short context")
+    assert torch.count_nonzero(out[:8]) == 0
+
+
+def test_bad_query_range_is_flagged_and_skipped():
+    w = W.random_prefill_small(43, 4, 4, 64, "f16", [5, 5], max_prior=10)
+    bad = np.array([0, 7, 3], np.int32)  # sequence 1 would have -4 tokens
+    out = gpu_prefill(w, q_start=bad, max_q_len=8)
+    assert ops.device_errors(clear=True) & ops.DEVERR_QUERY_RANGE
+    ref = oracle(w, q_start=np.array([0, 7, 7]))  # sequence 0 as given; sequence 1 skipped
+    assert_close(out[:7].numpy(), ref[:7], TOL["f16"], "valid sequence")
+    assert torch.isnan(out[7:]).all(), "a skipped sequence's rows were written"
+
+
+def test_empty_batch_and_no_tokens():
+    w = W.random_prefill_small(45, 4, 4, 64, "f16", [0, 0], max_prior=10)
+    out = gpu_prefill(w, max_q_len=1)
+    assert out.shape[0] == 0
+
+
+@pytest.mark.parametrize("name", sorted(W.PREFILL_CONFIGS))
+def test_full_size_sampled(name):
+    """The benchmark's workloads at full size, its launch configuration
+    (library-chosen split), checked on sampled (token, head) rows that cover
+    every sequence's first and last query tokens."""
+    w = W.PREFILL_CONFIGS[name]()
+    out = gpu_prefill(w).numpy()
+    rng = np.random.Generator(np.random.PCG64(5))
+    qs = w.q_start
+    rows = set()
+    for b in range(w.B):
+        for t in (qs[b], qs[b + 1] - 1):
+            rows.add((int(t), int(rng.integers(w.Hq))))
+    for t in rng.integers(0, w.T, size=64):
+        rows.add((int(t), int(rng.integers(w.Hq))))
+    rows = sorted(rows)
+    ref = oracle(w, rows=rows)
+    idx = tuple(np.array(rows).T)
+    assert_close(out[idx], ref[idx], TOL[w.kv_dtype], name)
