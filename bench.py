@@ -43,6 +43,8 @@ NOMINAL_HBM_GBS = 8000.0
 METRIC = "paged decode attention KV-read GB/s and tokens/s; % of GB300 HBM peak"
 METRIC_PREFILL = "multi-token paged attention KV-read GB/s and query tokens/s; % of GB300 HBM peak"
 PREFILL_CONFIGS = ("prefill_mix_llama7b", "spec_verify_gqa70b")
+SERVING_CONFIGS = ("serving_llama7b",)
+METRIC_SERVING = "continuous-batching serving iterations: tokens/s through scheduler + swap + cache write + attention"
 
 
 def parse_args(argv=None):
@@ -53,7 +55,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="llama7b_b32",
                    choices=["tiny", "llama7b_b32", "gqa70b_b64", "longctx_b8_f16", "longctx_b8_fp8",
-                            "shared_prefix_16x4"] + list(PREFILL_CONFIGS))
+                            "shared_prefix_16x4"] + list(PREFILL_CONFIGS) + list(SERVING_CONFIGS))
     p.add_argument("--split", type=int, default=0, help="split_tokens (0 = library choice)")
     p.add_argument("--e2e-steps", type=int, default=300)
     p.add_argument("--unfused", action="store_true",
@@ -1042,6 +1044,153 @@ def run_prefill(args, rank, world, local_rank):
         print(json.dumps(res), flush=True)
 
 
+# ---- continuous-batching serving loop -------------------------------------------------
+def run_serving(args, rank, world, local_rank):
+    """K iterations of the serving loop after W warm-up iterations: the C++
+    scheduler's step on the host, one H2D copy of its decisions, swap-out,
+    cache write, multi-token attention, swap-in on the device.  Requests keep
+    arriving (Poisson) for the whole run."""
+    import torch
+    from paged_kv_cache_191_gb300 import workloads as W
+    from paged_kv_cache_191_gb300.serving import ServingLoop
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    tr = W.serving_llama7b()
+    tdt = W.KV_TORCH[tr.kv_dtype]
+    loop = ServingLoop(tr.num_blocks, tr.host_blocks, tr.Hkv, tr.Hq, tr.D, tdt, tr.max_batch, tr.max_tokens,
+                       tr.max_context, device=dev, split_tokens=args.split)
+    T_max = tr.max_batch + tr.max_tokens
+    rng = W.rng_for(tr.seed)
+    q = W.randn(rng, (T_max, tr.Hq, tr.D), tdt).to(dev)
+    kn = W.randn(rng, (T_max, tr.Hkv, tr.D), tdt).to(dev)
+    vn = W.randn(rng, (T_max, tr.Hkv, tr.D), tdt).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stats = {"tokens": 0, "prefill_tokens": 0, "decode_tokens": 0, "swap_out_blocks": 0, "swap_in_blocks": 0,
+             "recomputed": 0, "finished": 0, "kv_bytes": 0, "flops": 0, "attn_launches": 0}
+    e = 2
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    it = 0
+
+    def one(timed_i=None):
+        nonlocal it
+        for rid, p, m in tr.arrivals(it):
+            loop.add(rid, p, m)
+        st = loop.step(q, kn, vn, stream=stream, attn_events=att[timed_i] if timed_i is not None else None)
+        it += 1
+        return st
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one()
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        host0 = time.perf_counter()
+        t0e.record(stream)
+        timed_attn = []
+        for i in range(args.steps):
+            st = one(i)
+            ctx = st["starts"] + st["lens"]
+            stats["tokens"] += st["T"]
+            stats["decode_tokens"] += int((st["kinds"] == 1).sum())
+            stats["swap_out_blocks"] += len(st["swap_out"])
+            stats["swap_in_blocks"] += len(st["swap_in"])
+            stats["recomputed"] += len(st["recomputed"])
+            stats["finished"] += len(st["finished"])
+            if st["T"]:
+                stats["kv_bytes"] += int(ctx.sum()) * tr.Hkv * tr.D * 2 * e + st["T"] * tr.Hq * tr.D * 2 * e
+                n, s0 = st["lens"].astype(np.int64), st["starts"].astype(np.int64)
+                stats["flops"] += int(4 * tr.D * tr.Hq * (n * s0 + n * (n + 1) // 2).sum())
+                stats["attn_launches"] += 1
+                timed_attn.append(i)
+        t1e.record(stream)
+        host1 = time.perf_counter()
+        stream.synchronize()
+        wall1 = time.time()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.stop()
+    stats["prefill_tokens"] = stats["tokens"] - stats["decode_tokens"]
+    from paged_kv_cache_191_gb300 import ops
+    errs = ops.device_errors(clear=True)
+    if errs:
+        raise RuntimeError(f"device error flags {errs:#x} during the benchmark")
+    local_s = t0e.elapsed_time(t1e) / 1e3
+
+    # e2e: the same loop with this iteration's queries and new K/V rows copied
+    # from pinned host memory and the attention output read back, synced
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    hq, hk, hv = q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory()
+    hout = torch.empty((T_max, tr.Hq, tr.D), dtype=tdt).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+    e2e_tokens = h2d = d2h = 0
+    with torch.cuda.stream(stream):
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            for rid, p, m in tr.arrivals(it):
+                loop.add(rid, p, m)
+            # the rows this iteration needs are known only after scheduling;
+            # copy the batch bound, as a model feeding the loop would
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            st = loop.step(dq, dk, dv, stream=stream)
+            it += 1
+            T = st["T"]
+            if T:
+                hout[:T].copy_(st["out"], non_blocking=True)
+            stream.synchronize()
+            e2e_tokens += T
+            d2h += T * tr.Hq * tr.D * e
+        t1 = time.perf_counter()
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * e + loop.meta_bytes
+    attn_s = sum(att[i][0].elapsed_time(att[i][1]) for i in timed_attn) / 1e3
+    max_s, tot_tokens = aggregate(local_s, float(stats["tokens"]), world)
+    peak, peak_kind = hbm_peak()
+    achieved = stats["kv_bytes"] / attn_s / 1e9 if attn_s else 0.0
+    res = {
+        "metric": METRIC_SERVING,
+        "value": round(tot_tokens / max_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s * 1e3 / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": tr.kv_dtype + "+f32acc",
+        "data": "synthetic",
+        "config": {"workload": tr.name, "q_heads": tr.Hq, "kv_heads": tr.Hkv, "head_dim": tr.D,
+                   "gpu_blocks": tr.num_blocks, "host_blocks": tr.host_blocks, "max_batch": tr.max_batch,
+                   "max_tokens_per_iteration": tr.max_tokens, "arrivals_per_iteration": tr.rate,
+                   "prompt": f"log-uniform {tr.prompt_min}..{tr.prompt_max}",
+                   "output": f"uniform {tr.out_min}..{tr.out_max}", "split_tokens": args.split or "auto",
+                   "parallelism": f"replicas x{world}"},
+        "iteration_stats": stats,
+        "host_us_per_step": round((host1 - host0) * 1e6 / args.steps, 2),
+        "attention_ms_per_step": round(attn_s * 1e3 / args.steps, 5),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind, "traffic": None,
+                     "kernel": "pa_chunked_prefill inside the serving loop (prefill_main + prefill_reduce)",
+                     "tflops": round(stats["flops"] / attn_s / 1e12, 2) if attn_s else 0.0},
+        "e2e": {"value": round(e2e_tokens / (t1 - t0), 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h / n_e2e), "steps": n_e2e,
+                "api": "paged_kv_cache_191_gb300.serving.ServingLoop with pinned host q / K / V in and the "
+                       "attention output back every iteration, stream sync per iteration"},
+        "gpu_launches": int(stats["attn_launches"] * 3 + args.steps),
+        "clocks": clocks.summary(wall0, wall1),
+        "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
 # ---- CPU oracle (baseline and reference arm) --------------------------------------
 def _oracle_task(task):
     import numpy as np  # noqa: F811
@@ -1221,6 +1370,8 @@ def main(argv=None):
             run_reference(args, rank, world)
         elif args.config in PREFILL_CONFIGS:
             run_prefill(args, rank, world, local_rank)
+        elif args.config in SERVING_CONFIGS:
+            run_serving(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -9,12 +9,16 @@
  *             2.3 the attention kernel resolves the page table itself and
  *                 gathers scattered K/V, transparent to the model;
  *             5.3 FP8 KV cache with per-token or per-channel scales;
+ *             3.1 continuous (iteration-level) batching;
+ *             3.2 preemption by swapping to host memory or dropping;
+ *             3.3 first-come-first-served scheduling;
  *             6.1 speculative decoding: the target model verifies the draft
  *                 tokens in one pass.
  *   [KV-CB]   "大模型推理引擎优化：KV Cache 与连续批处理" (devpress.csdn.net)
  *             2.2 16-token blocks;
  *             三   the block manager: block table, free list, refcount,
- *                 allocate / append / free / utilisation;
+ *                 allocate / append / free / utilisation; the continuous
+ *                 batching scheduler;
  *             4.1 chunked prefill: prompt chunks run beside decode steps;
  *             4.2 copy-on-write when a shared block is written.
  *
@@ -392,6 +396,73 @@ pa_status pa_alloc_stats(const pa_alloc* a, int32_t* total, int32_t* free_blocks
 
 /* Free list front to back (cap entries max); *n = its full length. */
 pa_status pa_free_list(const pa_alloc* a, int32_t* out, int32_t cap, int32_t* n);
+
+/* ---------------------------------------------------------------------------
+ * Continuous-batching scheduler ([LLM-INF] 3.1-3.3, [KV-CB] 三 and 4.1).
+ * Host only.  It owns a block manager of num_blocks GPU blocks and a host
+ * swap pool of host_blocks blocks, and decides every iteration which
+ * requests run and which tokens they bring:
+ *   1. requests that produced their last output in the previous step retire
+ *      (their blocks are released);
+ *   2. every decoding request gets one slot; while the free blocks do not
+ *      cover them, a running request is preempted: the one holding the most
+ *      blocks (later arrival on a tie) is swapped to the host pool if it
+ *      fits there, else the one holding the fewest (later arrival on a tie)
+ *      is dropped and goes back to the waiting queue to start over;
+ *   3. running requests continue their prompt in chunks bounded by the token
+ *      budget left (max_tokens minus the decodes) and the blocks they can get;
+ *   4. swapped requests come back in arrival order while their blocks fit
+ *      and the batch (max_batch) has room; they run from the next step;
+ *   5. waiting requests are admitted in arrival order with a first chunk
+ *      while the batch has room, budget is left and the chunk's blocks fit
+ *      (each admission lowers the free count); admission stops at the first
+ *      request that does not fit;
+ *   6. if nothing could run while requests are running, one is preempted.
+ * A request preempted in a step comes back in a later one at the earliest.
+ * The step that prefills a prompt's last token yields its first output;
+ * every later step appends the previous output's K/V and yields the next;
+ * after max_new_tokens outputs the request retires at the next step.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_sched pa_sched;
+
+#define PA_SCHED_PREFILL 0
+#define PA_SCHED_DECODE  1
+
+/* One step's decisions.  Arrays are caller-owned and must hold at least:
+ * ids, kinds, starts, lens, finished, recomputed: max_batch entries;
+ * slots: max_batch + max_tokens; swap_out, swap_in: 2 * num_blocks. */
+typedef struct {
+  int32_t   n_items;      /* requests that run this step, in batch order */
+  uint64_t* ids;
+  int32_t*  kinds;        /* PA_SCHED_PREFILL (a prompt chunk) or PA_SCHED_DECODE */
+  int32_t*  starts;       /* position of the item's first new token */
+  int32_t*  lens;         /* new tokens of the item (1 for a decode) */
+  int64_t   n_slots;      /* sum of lens */
+  int64_t*  slots;        /* cache slots of the new tokens, items in order */
+  int32_t   n_finished;
+  uint64_t* finished;     /* retired at the start of this step */
+  int32_t   n_swap_out;
+  int64_t*  swap_out;     /* [n][2] (GPU block, host block): copy before this step's writes */
+  int32_t   n_swap_in;
+  int64_t*  swap_in;      /* [n][2] (host block, GPU block): copy before the next step */
+  int32_t   n_recomputed;
+  uint64_t* recomputed;   /* dropped back to the waiting queue */
+} pa_sched_step_out;
+
+/* free_order: host int64 permutation of the GPU pool, or NULL for 0..n-1;
+ * max_batch, max_tokens > 0; host_blocks >= 0 (0 = preempt by recompute). */
+pa_status pa_sched_create(int32_t num_blocks, const int64_t* free_order, int32_t max_batch,
+                          int32_t max_tokens, int32_t host_blocks, pa_sched** out);
+void pa_sched_destroy(pa_sched* s);
+/* Queue a request.  PA_ERR_INVALID for an id in use, a prompt or output
+ * length < 1, or ceil((prompt_len + max_new_tokens) / 16) > num_blocks. */
+pa_status pa_sched_add(pa_sched* s, uint64_t id, int32_t prompt_len, int32_t max_new_tokens);
+pa_status pa_sched_step(pa_sched* s, pa_sched_step_out* out);
+/* The scheduler's block manager, for pa_block_tables on the running ids
+ * (read only: the scheduler is its only writer). */
+const pa_alloc* pa_sched_allocator(const pa_sched* s);
+pa_status pa_sched_stats(const pa_sched* s, int32_t* n_waiting, int32_t* n_running, int32_t* n_swapped,
+                         int32_t* free_blocks, int32_t* free_host_blocks);
 
 #ifdef __cplusplus
 }

@@ -49,6 +49,16 @@ _I32, _I64, _U64, _F = C.c_int32, C.c_int64, C.c_uint64, C.c_float
 _I32P, _I64P, _U64P = C.POINTER(C.c_int32), C.POINTER(C.c_int64), C.POINTER(C.c_uint64)
 
 # name -> (restype, argtypes); mirrors include/pagedkv.h
+class SchedStepOut(C.Structure):
+    _fields_ = [("n_items", C.c_int32), ("ids", C.POINTER(C.c_uint64)), ("kinds", C.POINTER(C.c_int32)),
+                ("starts", C.POINTER(C.c_int32)), ("lens", C.POINTER(C.c_int32)),
+                ("n_slots", C.c_int64), ("slots", C.POINTER(C.c_int64)),
+                ("n_finished", C.c_int32), ("finished", C.POINTER(C.c_uint64)),
+                ("n_swap_out", C.c_int32), ("swap_out", C.POINTER(C.c_int64)),
+                ("n_swap_in", C.c_int32), ("swap_in", C.POINTER(C.c_int64)),
+                ("n_recomputed", C.c_int32), ("recomputed", C.POINTER(C.c_uint64))]
+
+
 SIGNATURES = {
     "pa_last_error": (C.c_char_p, []),
     "pa_version": (_I32, []),
@@ -82,6 +92,12 @@ SIGNATURES = {
     "pa_block_table": (C.c_int, [_P, _U64, _I32P, _I32, _I32P, _I64P]),
     "pa_block_tables": (C.c_int, [_P, _U64P, _I32, _I32P, _I32, _I32P]),
     "pa_alloc_stats": (C.c_int, [_P, _I32P, _I32P, _I32P]),
+    "pa_sched_create": (C.c_int, [_I32, _I64P, _I32, _I32, _I32, C.POINTER(_P)]),
+    "pa_sched_destroy": (None, [_P]),
+    "pa_sched_add": (C.c_int, [_P, _U64, _I32, _I32]),
+    "pa_sched_step": (C.c_int, [_P, C.POINTER(SchedStepOut)]),
+    "pa_sched_allocator": (_P, [_P]),
+    "pa_sched_stats": (C.c_int, [_P, _I32P, _I32P, _I32P, _I32P, _I32P]),
     "pa_free_list": (C.c_int, [_P, _I32P, _I32, _I32P]),
 }
 
@@ -430,3 +446,81 @@ class BlockAllocator:
     def utilization(self):
         tot, fr, _ = self.stats()
         return (tot - fr) / tot
+
+
+class Scheduler:
+    """Continuous-batching scheduler (C++) over its own block manager.
+
+    step() -> (items, finished, swap_out, swap_in, recomputed) with items as
+    (id, "prefill" | "decode", start position, [slots]) in batch order and
+    the pairs as (from block, to block) tuples.
+    """
+
+    def __init__(self, num_blocks, max_batch, max_tokens, host_blocks, free_order=None):
+        h = C.c_void_p()
+        order = None
+        if free_order is not None:
+            self._order = (C.c_int64 * num_blocks)(*[int(x) for x in free_order])
+            order = C.cast(self._order, _I64P)
+        _check(lib().pa_sched_create(num_blocks, order, max_batch, max_tokens, host_blocks, C.byref(h)),
+               "pa_sched_create")
+        self._h = h
+        self.num_blocks, self.max_batch, self.max_tokens = num_blocks, max_batch, max_tokens
+        nb, nt = max_batch, max_batch + max_tokens
+        self._ids, self._kinds = (C.c_uint64 * nb)(), (C.c_int32 * nb)()
+        self._starts, self._lens = (C.c_int32 * nb)(), (C.c_int32 * nb)()
+        self._slots = (C.c_int64 * nt)()
+        self._fin, self._rec = (C.c_uint64 * nb)(), (C.c_uint64 * nb)()
+        self._out, self._in = (C.c_int64 * (2 * num_blocks))(), (C.c_int64 * (2 * num_blocks))()
+        o = SchedStepOut()
+        o.ids, o.kinds, o.starts, o.lens = self._ids, self._kinds, self._starts, self._lens
+        o.slots, o.finished, o.recomputed = self._slots, self._fin, self._rec
+        o.swap_out, o.swap_in = self._out, self._in
+        self._o = o
+        self.alloc_handle = C.c_void_p(lib().pa_sched_allocator(h))
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.pa_sched_destroy(h)
+            self._h = None
+
+    def add(self, rid, prompt_len, max_new_tokens):
+        _check(lib().pa_sched_add(self._h, rid, prompt_len, max_new_tokens), "pa_sched_add")
+
+    def step_raw(self):
+        """Run one step; the decisions stay in the ctypes arrays of self._o."""
+        _check(lib().pa_sched_step(self._h, C.byref(self._o)), "pa_sched_step")
+        return self._o
+
+    def step(self):
+        o = self.step_raw()
+        items, k = [], 0
+        for i in range(o.n_items):
+            n = o.lens[i]
+            items.append((o.ids[i], "decode" if o.kinds[i] == 1 else "prefill", o.starts[i],
+                          list(self._slots[k:k + n])))
+            k += n
+        pairs = lambda a, n: [(a[2 * i], a[2 * i + 1]) for i in range(n)]
+        return (items, list(self._fin[:o.n_finished]), pairs(self._out, o.n_swap_out),
+                pairs(self._in, o.n_swap_in), list(self._rec[:o.n_recomputed]))
+
+    def stats(self):
+        v = [C.c_int32() for _ in range(5)]
+        _check(lib().pa_sched_stats(self._h, *[C.byref(x) for x in v]), "pa_sched_stats")
+        return tuple(x.value for x in v)  # waiting, running, swapped, free blocks, free host blocks
+
+    def idle(self):
+        w, r, s, _, _ = self.stats()
+        return w == 0 and r == 0 and s == 0
+
+    def tables(self, ids, cap):
+        """(int32 [n, cap] tables, int32 [n] context lengths) of running ids."""
+        import numpy as np
+        n = len(ids)
+        tab = np.full((max(n, 1), cap), -1, dtype=np.int32)
+        lens = np.zeros(max(n, 1), dtype=np.int32)
+        arr = (C.c_uint64 * max(n, 1))(*ids)
+        _check(lib().pa_block_tables(self.alloc_handle, arr, n, tab.ctypes.data_as(_I32P), cap,
+                                     lens.ctypes.data_as(_I32P)), "pa_block_tables")
+        return tab[:n], lens[:n]

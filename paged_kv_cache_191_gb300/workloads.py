@@ -288,6 +288,52 @@ def random_prefill_small(seed, Hq, Hkv, D, kv_dtype, q_lens, max_prior=80):
                         pool_factor=1.0, extra_blocks=3)
 
 
+@dataclass
+class ServingTrace:
+    """Synthetic request stream for the serving loop: Poisson arrivals of
+    `rate` requests per iteration, prompts log-uniform in [prompt_min,
+    prompt_max], outputs uniform in [out_min, out_max]; iteration i's
+    arrivals are drawn from their own seeded generator."""
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    kv_dtype: str
+    num_blocks: int
+    host_blocks: int
+    max_batch: int
+    max_tokens: int
+    rate: float
+    prompt_min: int
+    prompt_max: int
+    out_min: int
+    out_max: int
+    seed: int
+
+    @property
+    def max_context(self):
+        return self.prompt_max + self.out_max
+
+    def arrivals(self, it):
+        rng = rng_for(self.seed * 1_000_003 + it)
+        out = []
+        for j in range(int(rng.poisson(self.rate))):
+            p = int(np.rint(np.exp(rng.uniform(math.log(self.prompt_min), math.log(self.prompt_max)))))
+            m = int(rng.integers(self.out_min, self.out_max, endpoint=True))
+            out.append((it * 1000 + j, p, m))
+        return out
+
+
+def serving_llama7b():
+    """LLaMA-7B shapes (32/32 heads, D=128, fp16); 4096 GPU blocks (64K
+    tokens, 2 GB of K+V) and 2048 host blocks for swapping; batch <= 64,
+    2048 tokens per iteration; prompts 32..2048, outputs 16..512, 1.5
+    arrivals per iteration (more than the pool sustains, so requests queue
+    and are preempted)."""
+    return ServingTrace("serving_llama7b", 32, 32, 128, "f16", 4096, 2048, 64, 2048, 1.5,
+                        32, 2048, 16, 512, SEED_BASE + 8)
+
+
 PREFILL_CONFIGS = {
     "prefill_mix_llama7b": config_prefill_mix,
     "spec_verify_gqa70b": config_spec_verify,

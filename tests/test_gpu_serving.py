@@ -1,0 +1,91 @@
+"""The whole serving iteration on the GPU against the oracle, step by step:
+the C++ scheduler's decisions (admission, chunked prefill, decode, swap-out,
+swap-in, drop) drive pa_swap_blocks, pa_cache_write and pa_chunked_prefill;
+the oracle applies the same copies and writes to its own cache mirror and
+computes the attention of every new token.  Outputs must agree within the
+attention tolerance (plus half an ulp of the 16-bit output) and the device
+caches must equal the mirror bit for bit.  The pool is small enough that
+requests are preempted both by swap and by drop."""
+import numpy as np
+import pytest
+import torch
+
+from oracle.attention import paged_prefill
+from oracle.scheduler import Scheduler as OSched
+from paged_kv_cache_191_gb300 import ops, workloads as W
+from paged_kv_cache_191_gb300.serving import ServingLoop
+from tests.gpu_util import TOL, np_exact, half_ulp, requires_cuda
+
+pytestmark = [pytest.mark.gpu, requires_cuda]
+
+
+@pytest.fixture(autouse=True)
+def no_device_errors():
+    ops.device_errors(clear=True)
+    yield
+    assert ops.device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_serving_iterations_match_oracle(dtype):
+    tdt = W.KV_TORCH[dtype]
+    nb, hb, Hkv, Hq, D, mb, mt = 12, 6, 2, 8, 128, 4, 48
+    loop = ServingLoop(nb, hb, Hkv, Hq, D, tdt, mb, mt, 256)
+    ref = OSched(nb, mb, mt, hb)
+    rng = W.rng_for(77)
+    reqs = []
+    for i in range(12):
+        while True:
+            p, m = int(rng.integers(1, 121)), int(rng.integers(1, 41))
+            if -(-(p + m) // 16) <= nb:
+                break
+        reqs.append((int(rng.integers(0, 25)), 500 + i, p, m))
+    kc = np.zeros((nb, Hkv, 16, D), np.float32)
+    vc = np.zeros_like(kc)
+    kh = np.zeros((hb, Hkv, 16, D), np.float32)
+    vh = np.zeros_like(kh)
+    events = {"swap_out": 0, "swap_in": 0, "recomputed": 0, "tokens": 0}
+    for it in range(2000):
+        for t, rid, p, m in reqs:
+            if t == it:
+                loop.add(rid, p, m)
+                ref.add(rid, p, m)
+        T_max = mb + mt
+        q = W.randn(rng, (T_max, Hq, D), tdt).cuda()
+        kn = W.randn(rng, (T_max, Hkv, D), tdt).cuda()
+        vn = W.randn(rng, (T_max, Hkv, D), tdt).cuda()
+        st = loop.step(q, kn, vn)
+        torch.cuda.synchronize()
+        r = ref.step()
+        # the scheduler decisions are the oracle's
+        assert [(i, s, n) for i, s, n in zip(st["ids"], st["starts"], st["lens"])] == \
+            [(i, s, len(sl)) for i, _, s, sl in r.items]
+        assert list(st["slots"]) == [x for *_, sl in r.items for x in sl]
+        assert [tuple(x) for x in st["swap_out"]] == r.swap_out
+        assert [tuple(x) for x in st["swap_in"]] == r.swap_in
+        # the same device work on the mirror, in the same order
+        for g, h in r.swap_out:
+            kh[h], vh[h] = kc[g], vc[g]
+        T = st["T"]
+        if T:
+            slots = st["slots"]
+            kc[slots // 16, :, slots % 16, :] = np_exact(kn[:T].cpu())
+            vc[slots // 16, :, slots % 16, :] = np_exact(vn[:T].cpu())
+            qs = np.concatenate([[0], np.cumsum(st["lens"])])
+            lens = st["starts"] + st["lens"]
+            want = paged_prefill(np_exact(q[:T].cpu()), qs, kc, vc, st["tables"], lens, 1.0 / np.sqrt(D))
+            got = st["out"].float().cpu().numpy()
+            err = np.abs(got - want)
+            assert np.all(err <= TOL[dtype] + half_ulp(want, tdt)), (it, float(err.max()))
+        for h, g in r.swap_in:
+            kc[g], vc[g] = kh[h], vh[h]
+        events["swap_out"] += len(r.swap_out)
+        events["swap_in"] += len(r.swap_in)
+        events["recomputed"] += len(r.recomputed)
+        events["tokens"] += T
+        if ref.idle() and it > 25:
+            break
+    assert loop.idle()
+    torch.cuda.synchronize()
+    assert np.array_equal(np_exact(loop.k_cache.cpu()), kc) and np.array_equal(np_exact(loop.v_cache.cpu()), vc)
+    assert events["swap_out"] and events["swap_in"] and events["recomputed"], events
