@@ -1078,7 +1078,8 @@ def run_serving(args, rank, world, local_rank):
         nonlocal it
         for rid, p, m in tr.arrivals(it):
             loop.add(rid, p, m)
-        st = loop.step(q, kn, vn, stream=stream, attn_events=att[timed_i] if timed_i is not None else None)
+        st = loop.step(q, kn, vn, stream=stream, attn_events=att[timed_i] if timed_i is not None else None,
+                       decisions=False)
         it += 1
         return st
 
@@ -1092,21 +1093,29 @@ def run_serving(args, rank, world, local_rank):
         host0 = time.perf_counter()
         t0e.record(stream)
         timed_attn = []
+        sc = loop.sched
+        v_kinds = np.ctypeslib.as_array(sc._kinds)
+        v_starts = np.ctypeslib.as_array(sc._starts)
+        v_lens = np.ctypeslib.as_array(sc._lens)
+        o = sc._o
         for i in range(args.steps):
             st = one(i)
-            ctx = st["starts"] + st["lens"]
+            n_it = st["n_items"]
+            kinds, s0, n = v_kinds[:n_it], v_starts[:n_it].astype(np.int64), v_lens[:n_it].astype(np.int64)
+            n_dec = int((kinds == 1).sum())
             stats["tokens"] += st["T"]
-            stats["decode_tokens"] += int((st["kinds"] == 1).sum())
-            stats["swap_out_blocks"] += len(st["swap_out"])
-            stats["swap_in_blocks"] += len(st["swap_in"])
-            stats["recomputed"] += len(st["recomputed"])
-            stats["finished"] += len(st["finished"])
+            stats["decode_tokens"] += n_dec
+            stats["swap_out_blocks"] += o.n_swap_out
+            stats["swap_in_blocks"] += o.n_swap_in
+            stats["recomputed"] += o.n_recomputed
+            stats["finished"] += o.n_finished
+            timed_attn.append(i)
             if st["T"]:
-                stats["kv_bytes"] += int(ctx.sum()) * tr.Hkv * tr.D * 2 * e + st["T"] * tr.Hq * tr.D * 2 * e
-                n, s0 = st["lens"].astype(np.int64), st["starts"].astype(np.int64)
+                stats["kv_bytes"] += int((s0 + n).sum()) * tr.Hkv * tr.D * 2 * e + st["T"] * tr.Hq * tr.D * 2 * e
                 stats["flops"] += int(4 * tr.D * tr.Hq * (n * s0 + n * (n + 1) // 2).sum())
-                stats["attn_launches"] += 1
-                timed_attn.append(i)
+                # decode_main (+ decode_reduce), cache write + prefill_main (+ prefill_reduce), swaps
+                stats["attn_launches"] += (2 if n_dec else 0) + (3 if n_dec < n_it else 0) + \
+                    (1 if o.n_swap_out else 0) + (1 if o.n_swap_in else 0)
         t1e.record(stream)
         host1 = time.perf_counter()
         stream.synchronize()
@@ -1134,21 +1143,22 @@ def run_serving(args, rank, world, local_rank):
         for _ in range(n_e2e):
             for rid, p, m in tr.arrivals(it):
                 loop.add(rid, p, m)
-            # the rows this iteration needs are known only after scheduling;
-            # copy the batch bound, as a model feeding the loop would
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            st = loop.step(dq, dk, dv, stream=stream)
+            # plan first: the iteration's T new tokens are known before their
+            # rows are copied, as a model producing them would need
+            T = loop.plan()
+            dq[:T].copy_(hq[:T], non_blocking=True)
+            dk[:T].copy_(hk[:T], non_blocking=True)
+            dv[:T].copy_(hv[:T], non_blocking=True)
+            loop.launch(dq, dk, dv, stream=stream)
             it += 1
-            T = st["T"]
             if T:
-                hout[:T].copy_(st["out"], non_blocking=True)
+                hout[:T].copy_(loop.out[:T], non_blocking=True)
             stream.synchronize()
             e2e_tokens += T
+            h2d += T * (tr.Hq + 2 * tr.Hkv) * tr.D * e + loop.meta_bytes
             d2h += T * tr.Hq * tr.D * e
         t1 = time.perf_counter()
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * e + loop.meta_bytes
+
     attn_s = sum(att[i][0].elapsed_time(att[i][1]) for i in timed_attn) / 1e3
     max_s, tot_tokens = aggregate(local_s, float(stats["tokens"]), world)
     peak, peak_kind = hbm_peak()
@@ -1174,16 +1184,18 @@ def run_serving(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}"},
         "iteration_stats": stats,
         "host_us_per_step": round((host1 - host0) * 1e6 / args.steps, 2),
-        "attention_ms_per_step": round(attn_s * 1e3 / args.steps, 5),
+        "device_ms_per_step": round(attn_s * 1e3 / args.steps, 5),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind, "traffic": None,
-                     "kernel": "pa_chunked_prefill inside the serving loop (prefill_main + prefill_reduce)",
+                     "kernel": "device work of pa_serve_step: staging copy, swaps, decode_main(+reduce) with the "
+                               "fused write for decode items, cache write + prefill_main(+reduce) for chunks",
                      "tflops": round(stats["flops"] / attn_s / 1e12, 2) if attn_s else 0.0},
-        "e2e": {"value": round(e2e_tokens / (t1 - t0), 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": round(e2e_tokens / (t1 - t0), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d / n_e2e),
                 "d2h_bytes_per_step": int(d2h / n_e2e), "steps": n_e2e,
-                "api": "paged_kv_cache_191_gb300.serving.ServingLoop with pinned host q / K / V in and the "
-                       "attention output back every iteration, stream sync per iteration"},
-        "gpu_launches": int(stats["attn_launches"] * 3 + args.steps),
+                "api": "paged_kv_cache_191_gb300.serving.ServingLoop plan / launch: the iteration's q / K / V "
+                       "rows in from pinned host memory, its attention output back, stream sync per iteration"},
+        "gpu_launches": int(stats["attn_launches"]),
         "clocks": clocks.summary(wall0, wall1),
         "cpu_baseline": None,
     }

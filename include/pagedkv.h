@@ -463,6 +463,62 @@ pa_status pa_sched_step(pa_sched* s, pa_sched_step_out* out);
 const pa_alloc* pa_sched_allocator(const pa_sched* s);
 pa_status pa_sched_stats(const pa_sched* s, int32_t* n_waiting, int32_t* n_running, int32_t* n_swapped,
                          int32_t* free_blocks, int32_t* free_host_blocks);
+/* The limits the scheduler was created with. */
+pa_status pa_sched_limits(const pa_sched* s, int32_t* max_batch, int32_t* max_tokens, int32_t* num_blocks);
+
+/* ---------------------------------------------------------------------------
+ * Serving iteration engine: one scheduler step turned into device work on one
+ * stream -- one host-to-device copy of the staged decisions; swap-out copies
+ * (GPU -> host pool) of preempted requests; the decode items' cache write
+ * fused into pa_decode; pa_cache_write + pa_chunked_prefill for the prompt
+ * chunks; swap-in copies (host pool -> GPU) of requests that run next step.
+ * F16 / BF16 caches.  Every buffer is caller-owned.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_serve pa_serve;
+
+typedef struct {
+  void*   k_cache;          /* device pools of the scheduler's num_blocks blocks */
+  void*   v_cache;
+  void*   k_host;           /* pinned host swap pools [host_blocks][Hkv][16][D] (NULL if 0) */
+  void*   v_host;
+  int32_t host_blocks;      /* as given to pa_sched_create */
+  int32_t num_q_heads;
+  int32_t max_context;      /* bound on a request's prompt + outputs (tokens) */
+  int32_t split_tokens;     /* partition size of the chunk kernel (> 0, multiple of 16) */
+  void*   staging_host;     /* pinned, 2 * pa_serve_staging_bytes() bytes, 16-byte aligned */
+  void*   staging_dev;      /* device, pa_serve_staging_bytes() bytes, 16-byte aligned */
+  void*   workspace;        /* device, >= pa_serve_workspace_bytes() bytes (may be NULL if 0) */
+  size_t  workspace_bytes;
+} pa_serve_buffers;
+
+size_t pa_serve_staging_bytes(const pa_sched* s, int32_t max_context);
+size_t pa_serve_workspace_bytes(const pa_sched* s, int32_t num_q_heads, int32_t max_context,
+                                const pa_cache_desc* desc, int32_t split_tokens);
+/* The engine keeps pointers to s and to the buffers until destroyed. */
+pa_status pa_serve_create(pa_sched* s, const pa_cache_desc* desc, const pa_serve_buffers* bufs,
+                          pa_serve** out);
+void pa_serve_destroy(pa_serve* e);
+/* Plan the next iteration: run the scheduler step and stage its decisions
+ * (host only; waits for the staging copy of two iterations before).
+ * decisions: arrays as for pa_sched_step, or NULL to keep them internal;
+ * *num_tokens (if not NULL) = T, the new tokens the iteration brings.  A plan
+ * must be launched before the next one is made. */
+pa_status pa_serve_plan(pa_serve* e, pa_sched_step_out* decisions, int64_t* num_tokens);
+/* Launch the planned iteration on `stream`: q: device [>= T][num_q_heads][D],
+ * k_new / v_new: device [>= T][Hkv][D], all in_dtype (= the cache dtype),
+ * row t for the t-th new token (items in order; decodes come first); out:
+ * device [>= T][num_q_heads][D] in in_dtype. */
+pa_status pa_serve_launch(pa_serve* e, const void* q, const void* k_new, const void* v_new, int32_t in_dtype,
+                          void* out, void* stream);
+/* pa_serve_plan followed by pa_serve_launch.
+ * One iteration.  q: device [>= T][num_q_heads][D], k_new / v_new: device
+ * [>= T][Hkv][D], all in_dtype (= the cache dtype), row t for the t-th new
+ * token of the step (items in order; decodes come first); out: device
+ * [>= T][num_q_heads][D] in in_dtype.  decisions: arrays as for
+ * pa_sched_step, or NULL to keep them internal.  Blocks the host only to
+ * wait for the staging copy of two steps before. */
+pa_status pa_serve_step(pa_serve* e, const void* q, const void* k_new, const void* v_new, int32_t in_dtype,
+                        void* out, pa_sched_step_out* decisions, void* stream);
 
 #ifdef __cplusplus
 }

@@ -321,6 +321,14 @@ pa_status pa_sched_step(pa_sched* s, pa_sched_step_out* o) {
 
 const pa_alloc* pa_sched_allocator(const pa_sched* s) { return s ? s->alloc : nullptr; }
 
+pa_status pa_sched_limits(const pa_sched* s, int32_t* max_batch, int32_t* max_tokens, int32_t* num_blocks) {
+  if (!s || !max_batch || !max_tokens || !num_blocks) return pa::fail(PA_ERR_INVALID, "pa_sched_limits: null argument");
+  *max_batch = s->max_batch;
+  *max_tokens = s->max_tokens;
+  *num_blocks = s->num_blocks;
+  return pa::ok();
+}
+
 pa_status pa_sched_stats(const pa_sched* s, int32_t* n_waiting, int32_t* n_running, int32_t* n_swapped,
                          int32_t* free_blocks, int32_t* free_host_blocks) {
   if (!s || !n_waiting || !n_running || !n_swapped || !free_blocks || !free_host_blocks)

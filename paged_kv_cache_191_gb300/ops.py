@@ -59,6 +59,13 @@ class SchedStepOut(C.Structure):
                 ("n_recomputed", C.c_int32), ("recomputed", C.POINTER(C.c_uint64))]
 
 
+class ServeBuffers(C.Structure):
+    _fields_ = [("k_cache", C.c_void_p), ("v_cache", C.c_void_p), ("k_host", C.c_void_p), ("v_host", C.c_void_p),
+                ("host_blocks", C.c_int32), ("num_q_heads", C.c_int32), ("max_context", C.c_int32),
+                ("split_tokens", C.c_int32), ("staging_host", C.c_void_p), ("staging_dev", C.c_void_p),
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
+
+
 SIGNATURES = {
     "pa_last_error": (C.c_char_p, []),
     "pa_version": (_I32, []),
@@ -98,6 +105,14 @@ SIGNATURES = {
     "pa_sched_step": (C.c_int, [_P, C.POINTER(SchedStepOut)]),
     "pa_sched_allocator": (_P, [_P]),
     "pa_sched_stats": (C.c_int, [_P, _I32P, _I32P, _I32P, _I32P, _I32P]),
+    "pa_sched_limits": (C.c_int, [_P, _I32P, _I32P, _I32P]),
+    "pa_serve_staging_bytes": (C.c_size_t, [_P, _I32]),
+    "pa_serve_workspace_bytes": (C.c_size_t, [_P, _I32, _I32, C.POINTER(CacheDesc), _I32]),
+    "pa_serve_create": (C.c_int, [_P, C.POINTER(CacheDesc), C.POINTER(ServeBuffers), C.POINTER(_P)]),
+    "pa_serve_destroy": (None, [_P]),
+    "pa_serve_plan": (C.c_int, [_P, C.POINTER(SchedStepOut), _I64P]),
+    "pa_serve_launch": (C.c_int, [_P, _P, _P, _P, _I32, _P, _P]),
+    "pa_serve_step": (C.c_int, [_P, _P, _P, _P, _I32, _P, C.POINTER(SchedStepOut), _P]),
     "pa_free_list": (C.c_int, [_P, _I32P, _I32, _I32P]),
 }
 

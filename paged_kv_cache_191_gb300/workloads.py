@@ -325,12 +325,12 @@ class ServingTrace:
 
 
 def serving_llama7b():
-    """LLaMA-7B shapes (32/32 heads, D=128, fp16); 4096 GPU blocks (64K
-    tokens, 2 GB of K+V) and 2048 host blocks for swapping; batch <= 64,
+    """LLaMA-7B shapes (32/32 heads, D=128, fp16); 2048 GPU blocks (32K
+    tokens, 1 GB of K+V) and 1024 host blocks for swapping; batch <= 64,
     2048 tokens per iteration; prompts 32..2048, outputs 16..512, 1.5
     arrivals per iteration (more than the pool sustains, so requests queue
     and are preempted)."""
-    return ServingTrace("serving_llama7b", 32, 32, 128, "f16", 4096, 2048, 64, 2048, 1.5,
+    return ServingTrace("serving_llama7b", 32, 32, 128, "f16", 2048, 1024, 64, 2048, 1.5,
                         32, 2048, 16, 512, SEED_BASE + 8)
 
 

@@ -1,6 +1,8 @@
 """The whole serving iteration on the GPU against the oracle, step by step:
-the C++ scheduler's decisions (admission, chunked prefill, decode, swap-out,
-swap-in, drop) drive pa_swap_blocks, pa_cache_write and pa_chunked_prefill;
+the native engine (pa_serve_step) turns the C++ scheduler's decisions
+(admission, chunked prefill, decode, swap-out, swap-in, drop) into
+pa_swap_blocks, pa_decode_append for the decode items and pa_cache_write +
+pa_chunked_prefill for the prompt chunks;
 the oracle applies the same copies and writes to its own cache mirror and
 computes the attention of every new token.  Outputs must agree within the
 attention tolerance (plus half an ulp of the 16-bit output) and the device
@@ -26,8 +28,10 @@ def no_device_errors():
     assert ops.device_errors(clear=True) == 0
 
 
-@pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_serving_iterations_match_oracle(dtype):
+@pytest.mark.parametrize("dtype,two_phase", [("f16", False), ("bf16", False), ("f16", True)])
+def test_serving_iterations_match_oracle(dtype, two_phase):
+    """two_phase: plan() first, then exactly T rows of q / K / V, then
+    launch() -- the order a model feeding the loop follows."""
     tdt = W.KV_TORCH[dtype]
     nb, hb, Hkv, Hq, D, mb, mt = 12, 6, 2, 8, 128, 4, 48
     loop = ServingLoop(nb, hb, Hkv, Hq, D, tdt, mb, mt, 256)
@@ -50,17 +54,25 @@ def test_serving_iterations_match_oracle(dtype):
             if t == it:
                 loop.add(rid, p, m)
                 ref.add(rid, p, m)
-        T_max = mb + mt
-        q = W.randn(rng, (T_max, Hq, D), tdt).cuda()
-        kn = W.randn(rng, (T_max, Hkv, D), tdt).cuda()
-        vn = W.randn(rng, (T_max, Hkv, D), tdt).cuda()
-        st = loop.step(q, kn, vn)
+        if two_phase:
+            T_rows = max(loop.plan(), 1)
+        else:
+            T_rows = mb + mt
+        q = W.randn(rng, (T_rows, Hq, D), tdt).cuda()
+        kn = W.randn(rng, (T_rows, Hkv, D), tdt).cuda()
+        vn = W.randn(rng, (T_rows, Hkv, D), tdt).cuda()
+        if two_phase:
+            loop.launch(q, kn, vn)
+            st = loop.decisions()
+        else:
+            st = loop.step(q, kn, vn)
         torch.cuda.synchronize()
         r = ref.step()
         # the scheduler decisions are the oracle's
         assert [(i, s, n) for i, s, n in zip(st["ids"], st["starts"], st["lens"])] == \
             [(i, s, len(sl)) for i, _, s, sl in r.items]
         assert list(st["slots"]) == [x for *_, sl in r.items for x in sl]
+        assert np.array_equal(st["context_lens"], st["starts"] + st["lens"])
         assert [tuple(x) for x in st["swap_out"]] == r.swap_out
         assert [tuple(x) for x in st["swap_in"]] == r.swap_in
         # the same device work on the mirror, in the same order
