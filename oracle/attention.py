@@ -20,8 +20,9 @@ Readings where the pages are silent (each is listed with the design notes):
 * grouped query heads use contiguous groups, kv head = h // (Hq / Hkv);
 * context_lens[b] counts the token written in the same decode step;
   a length of 0 gives an all-zero output row;
-* FP8 caches hold E4M3 codes with one float32 scale per (block, slot) for
-  K and one for V; the stored value is decode(code) * scale.
+* FP8 caches hold E4M3 codes (uint8) and INT8 caches signed integer codes
+  (int8), with one float32 scale per (block, slot) for K and one for V; the
+  stored value is decode(code) * scale (for INT8, code * scale).
 
 No blocking, split or reordering is applied: one softmax per (b, h) over the
 whole context, as the definition reads.
@@ -41,7 +42,7 @@ def gather_kv(cache, block_tables_row, n_tokens, kv_head, scales=None):
     """Return float64 [n_tokens, D] of one kv head of one sequence.
 
     cache: [num_blocks, Hkv, 16, D] array (float16/float32 values, or uint8
-    E4M3 codes when ``scales`` is given); scales: [num_blocks, 16] float32.
+    E4M3 / int8 codes when ``scales`` is given); scales: [num_blocks, 16] float32.
     """
     t = np.arange(n_tokens)
     blk = np.asarray(block_tables_row)[t // BLOCK_SIZE].astype(np.int64)
@@ -49,7 +50,8 @@ def gather_kv(cache, block_tables_row, n_tokens, kv_head, scales=None):
     rows = cache[blk, kv_head, off, :]
     if scales is None:
         return _as_f64(rows)
-    return e4m3_decode(rows) * _as_f64(scales)[blk, off][:, None]
+    codes = _as_f64(rows) if rows.dtype == np.int8 else e4m3_decode(rows)  # INT8 or E4M3 codes
+    return codes * _as_f64(scales)[blk, off][:, None]
 
 
 def softmax_weights(q_row, K, scale):

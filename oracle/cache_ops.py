@@ -16,6 +16,16 @@ values of that token):
 
 where fl32 is an IEEE float32 round-to-nearest division.
 
+INT8 variant ([LLM-INF] 5.3 names INT8 beside FP8 for the KV cache, at
+per-channel or per-token granularity; the reading taken is the FP8 one --
+one float32 scale per token per tensor -- with symmetric integer codes):
+
+    scale = fl32(amax / 127)  or 1.0 when amax == 0
+    code  = clamp( round_half_even( fl32(x / scale) ), -127, 127 )   (int8)
+
+and the stored value is code * scale.  The cache dtype tells the formats
+apart: uint8 caches hold E4M3 codes, int8 caches hold INT8 codes.
+
 Block copy ([LLM-INF] 2.2 copy-on-write; [KV-CB] 4.2): for each (src, dst)
 pair the whole K block, V block and, for FP8, the 16 scales of each are
 copied.  Pairs must not write a block that another pair reads or writes.
@@ -43,6 +53,32 @@ def fp8_quantize_rows(x):
     return e4m3_encode(y).reshape(xf.shape), scale
 
 
+INT8_MAX = 127
+
+
+def int8_quantize_rows(x):
+    """Quantise each row of x [T, ...] -> (int8 codes [T, ...], float32 scales [T]).
+
+    Row t is one token: amax over the row, scale = fl32(amax / 127) (1.0 for
+    an all-zero row), codes = round-half-even(fl32(x / scale)) clamped to
+    [-127, 127] (the clamp only guards the rounding of the scale).
+    """
+    xf = np.asarray(x, dtype=np.float32)
+    T = xf.shape[0]
+    flat = xf.reshape(T, -1)
+    amax = np.abs(flat).max(axis=1) if flat.shape[1] else np.zeros(T, np.float32)
+    scale = np.where(amax == 0, np.float32(1.0),
+                     amax.astype(np.float32) / np.float32(INT8_MAX)).astype(np.float32)
+    y = (flat / scale[:, None]).astype(np.float32)
+    codes = np.clip(np.rint(y), -INT8_MAX, INT8_MAX).astype(np.int8)  # rint: ties to even
+    return codes.reshape(xf.shape), scale
+
+
+def quantize_rows(x, cache_dtype):
+    """Per-token quantiser of a cache's format: uint8 -> E4M3, int8 -> INT8."""
+    return int8_quantize_rows(x) if np.dtype(cache_dtype) == np.int8 else fp8_quantize_rows(x)
+
+
 def fp8_quantize_token(x):
     """Quantise one token's values (any shape) -> (uint8 codes, float32 scale)."""
     codes, scale = fp8_quantize_rows(np.asarray(x)[None])
@@ -53,8 +89,8 @@ def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None
     """Return new (k_cache, v_cache, k_scale, v_scale) after writing T tokens.
 
     k, v: [T, Hkv, D] (float16/float32 values); caches: [num_blocks, Hkv, 16, D]
-    in the storage dtype (float16, float32 holding bf16 values, or uint8 codes
-    when k_scale/v_scale [num_blocks, 16] float32 are given).
+    in the storage dtype (float16, float32 holding bf16 values, or uint8 E4M3 /
+    int8 codes when k_scale/v_scale [num_blocks, 16] float32 are given).
     """
     k_cache = np.array(k_cache, copy=True)
     v_cache = np.array(v_cache, copy=True)
@@ -74,8 +110,8 @@ def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None
         rows = idx[c0:c0 + 4096]
         blk, off = slots[rows] // BLOCK_SIZE, slots[rows] % BLOCK_SIZE
         if fp8:
-            kc, ks = fp8_quantize_rows(np.asarray(k)[rows])
-            vc, vs = fp8_quantize_rows(np.asarray(v)[rows])
+            kc, ks = quantize_rows(np.asarray(k)[rows], k_cache.dtype)
+            vc, vs = quantize_rows(np.asarray(v)[rows], v_cache.dtype)
             k_cache[blk, :, off, :] = kc
             v_cache[blk, :, off, :] = vc
             k_scale[blk, off] = ks
