@@ -54,7 +54,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="llama7b_b32",
-                   choices=["tiny", "llama7b_b32", "gqa70b_b64", "longctx_b8_f16", "longctx_b8_fp8",
+                   choices=["tiny", "llama7b_b32", "gqa70b_b64", "longctx_b8_f16", "longctx_b8_fp8", "longctx_b8_int8",
                             "shared_prefix_16x4"] + list(PREFILL_CONFIGS) + list(SERVING_CONFIGS))
     p.add_argument("--split", type=int, default=0, help="split_tokens (0 = library choice)")
     p.add_argument("--e2e-steps", type=int, default=300)
@@ -259,7 +259,7 @@ class DecodeStep:
         self.torch, self.ops, self.L = torch, ops, ops.lib()
         self.w = w
         self.B, self.Hq, self.Hkv, self.D = w.B, w.Hq, w.Hkv, w.D
-        self.fp8 = w.kv_dtype == "fp8"
+        self.fp8 = w.kv_dtype in ("fp8", "int8")  # 1-byte codes + per-token scales
         self.dev = device
         self.lens0 = np.asarray(w.context_lens, dtype=np.int64)
         # capacity: lengths grow by at most RESET_EVERY tokens before a reset
@@ -274,13 +274,14 @@ class DecodeStep:
         self.ids = list(range(self.B))
         self._admit()
 
-        kvdt = torch.float16 if w.kv_dtype in ("f16", "fp8") else torch.bfloat16
+        kvdt = torch.float16 if w.kv_dtype in ("f16", "fp8", "int8") else torch.bfloat16
         extra = torch.zeros((grow_blocks, self.Hkv, 16, self.D), dtype=kvdt)
         kp = torch.cat([w.k_pool, extra]).to(device)
         vp = torch.cat([w.v_pool, extra]).to(device)
         if self.fp8:  # the cache is filled by the quantiser (set-up, not timed)
             N = self.num_blocks
-            self.kc = torch.empty((N, self.Hkv, 16, self.D), dtype=torch.uint8, device=device)
+            code_dt = torch.int8 if w.kv_dtype == "int8" else torch.uint8
+            self.kc = torch.empty((N, self.Hkv, 16, self.D), dtype=code_dt, device=device)
             self.vc = torch.empty_like(self.kc)
             self.ks = torch.empty((N, 16), dtype=torch.float32, device=device)
             self.vs = torch.empty_like(self.ks)
@@ -699,7 +700,8 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {"f16": "f16", "bf16": "bf16", "fp8": "fp8e4m3(kv)/f16"}[w.kv_dtype] + "+f32acc",
+        "dtype": {"f16": "f16", "bf16": "bf16", "fp8": "fp8e4m3(kv)/f16", "int8": "int8(kv)/f16"}[w.kv_dtype]
+                 + "+f32acc",
         "data": "synthetic",
         "config": {
             "workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
@@ -1213,7 +1215,7 @@ def _oracle_task(task):
     return n
 
 
-def oracle_tasks(w, seqs, fp8_codes=None):
+def oracle_tasks(w, seqs, codes=None):
     """Per-sequence oracle inputs: that sequence's blocks (de-duplicated pool view)."""
     from paged_kv_cache_191_gb300.workloads import BLOCK
     tasks = []
@@ -1225,11 +1227,12 @@ def oracle_tasks(w, seqs, fp8_codes=None):
         kb = kb.float().numpy() if str(kb.dtype) == "torch.bfloat16" else kb.numpy()
         vb = vb.float().numpy() if str(vb.dtype) == "torch.bfloat16" else vb.numpy()
         q = w.q[b].float().numpy() if str(w.q.dtype) == "torch.bfloat16" else w.q[b].numpy()
-        if fp8_codes is not None:
-            from oracle.cache_ops import fp8_quantize_rows
+        if codes is not None:  # "fp8" or "int8": the oracle's own quantiser of that format
+            from oracle.cache_ops import quantize_rows
             H, D = kb.shape[1], kb.shape[3]
-            kcodes, ks = fp8_quantize_rows(kb.transpose(0, 2, 1, 3).reshape(-1, H, D))
-            vcodes, vs = fp8_quantize_rows(vb.transpose(0, 2, 1, 3).reshape(-1, H, D))
+            cdt = np.int8 if codes == "int8" else np.uint8
+            kcodes, ks = quantize_rows(kb.transpose(0, 2, 1, 3).reshape(-1, H, D), cdt)
+            vcodes, vs = quantize_rows(vb.transpose(0, 2, 1, 3).reshape(-1, H, D), cdt)
             kb = kcodes.reshape(-1, 16, H, D).transpose(0, 2, 1, 3).copy()
             vb = vcodes.reshape(-1, 16, H, D).transpose(0, 2, 1, 3).copy()
             tasks.append((q, kb, vb, n, w.scale, ks.reshape(-1, 16), vs.reshape(-1, 16)))
@@ -1259,8 +1262,9 @@ def cpu_baseline(w, seconds):
     pool over the host cores, repeated until about `seconds` have passed."""
     cores = cpu_cores()
     seqs = list(range(w.B))
-    tasks = oracle_tasks(w, seqs, fp8_codes=(w.kv_dtype == "fp8") or None)
-    e = 1 if w.kv_dtype == "fp8" else 2
+    q8 = w.kv_dtype in ("fp8", "int8")
+    tasks = oracle_tasks(w, seqs, codes=w.kv_dtype if q8 else None)
+    e = 1 if q8 else 2
     per_seq = [decode_bytes([int(w.context_lens[b])], w.Hq, w.Hkv, w.D, e, 2, 2) for b in seqs]
     with _pool(cores) as pool:
         t0 = time.perf_counter()
@@ -1328,10 +1332,10 @@ def run_reference(args, rank, world):
         return run_reference_prefill(args, world)
     w = load_workload(args.config)
     cores = cpu_cores()
-    fp8 = w.kv_dtype == "fp8"
+    fp8 = w.kv_dtype in ("fp8", "int8")
     e = 1 if fp8 else 2
     seqs = list(range(w.B))
-    tasks = oracle_tasks(w, seqs, fp8_codes=fp8 or None)
+    tasks = oracle_tasks(w, seqs, codes=w.kv_dtype if fp8 else None)
     per = [decode_bytes([int(w.context_lens[b])], w.Hq, w.Hkv, w.D, e, 2, 2) for b in seqs]
     budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step
     with _pool(cores) as pool:

@@ -71,8 +71,9 @@ typedef enum {
 typedef enum {
   PA_DTYPE_F16 = 0,
   PA_DTYPE_BF16 = 1,
-  PA_DTYPE_FP8_E4M3 = 2,
-  PA_DTYPE_F32 = 3
+  PA_DTYPE_FP8_E4M3 = 2,   /* OCP E4M3 codes + per-token float32 scales */
+  PA_DTYPE_F32 = 3,
+  PA_DTYPE_INT8 = 4        /* symmetric int8 codes + per-token float32 scales */
 } pa_dtype;
 
 /* Bits of the per-device error word (pa_device_errors). */

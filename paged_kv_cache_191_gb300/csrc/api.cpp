@@ -30,13 +30,12 @@ static pa_status check_desc(const pa_cache_desc* d, const char* fn) {
     return fail(PA_ERR_UNSUPPORTED, "%s: block_size must be 16", fn);
   if (d->num_blocks <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0)
     return fail(PA_ERR_INVALID, "%s: num_blocks, num_kv_heads, head_dim must be > 0", fn);
-  if (d->kv_dtype != PA_DTYPE_F16 && d->kv_dtype != PA_DTYPE_BF16 &&
-      d->kv_dtype != PA_DTYPE_FP8_E4M3)
-    return fail(PA_ERR_INVALID, "%s: kv_dtype must be F16, BF16 or FP8_E4M3", fn);
+  if (d->kv_dtype != PA_DTYPE_F16 && d->kv_dtype != PA_DTYPE_BF16 && !quantised(d->kv_dtype))
+    return fail(PA_ERR_INVALID, "%s: kv_dtype must be F16, BF16, FP8_E4M3 or INT8", fn);
   if (d->head_dim != 64 && d->head_dim != 128)
     return fail(PA_ERR_UNSUPPORTED, "%s: head_dim %d not built (64, 128)", fn, d->head_dim);
-  if (d->kv_dtype == PA_DTYPE_FP8_E4M3 && d->head_dim != 128)
-    return fail(PA_ERR_UNSUPPORTED, "%s: FP8 caches need head_dim 128", fn);
+  if (quantised(d->kv_dtype) && d->head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "%s: FP8 / INT8 caches need head_dim 128", fn);
   return PA_OK;
 }
 
@@ -69,10 +68,10 @@ pa_status plan_decode(int32_t B, int32_t Hq, int32_t max_context_len, const pa_c
   if (parts > 65535) return fail(PA_ERR_UNSUPPORTED, "context too long for the partition grid");
   plan->blocks_per_part = bpp;
   plan->max_parts = static_cast<int32_t>(parts);
-  // FP8 tiles cost more register-side work per byte (exact conversion of the
-  // codes), so four warps share a partition there; 16-bit caches keep one
-  // warp per partition (measured best for both).
-  plan->item_warps = d->kv_dtype == PA_DTYPE_FP8_E4M3 ? 4 : 1;
+  // 1-byte codes cost more register-side work per byte (exact conversion of
+  // the codes), so four warps share a partition there; 16-bit caches keep
+  // one warp per partition (measured best for both).
+  plan->item_warps = quantised(d->kv_dtype) ? 4 : 1;
   if (parts > 1) {
     const size_t rows = static_cast<size_t>(B) * Hq * parts;
     size_t bytes = rows * d->head_dim * sizeof(float) + 2 * rows * sizeof(float);
@@ -150,17 +149,17 @@ pa_status pa_cache_write(const void* k, const void* v, int32_t in_dtype,
   if (!pa::aligned16(k) || !pa::aligned16(v) || !pa::aligned16(k_cache) || !pa::aligned16(v_cache) ||
       (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
     return fail(PA_ERR_INVALID, "pa_cache_write: misaligned pointer");
-  const bool fp8 = desc->kv_dtype == PA_DTYPE_FP8_E4M3;
-  if (fp8) {
+  const bool q8 = pa::quantised(desc->kv_dtype);
+  if (q8) {
     if (in_dtype != PA_DTYPE_F16 && in_dtype != PA_DTYPE_BF16 && in_dtype != PA_DTYPE_F32)
-      return fail(PA_ERR_INVALID, "pa_cache_write: FP8 cache needs F16, BF16 or F32 input");
+      return fail(PA_ERR_INVALID, "pa_cache_write: FP8 / INT8 cache needs F16, BF16 or F32 input");
     if (!k_scale || !v_scale || !pa::aligned16(k_scale) || !pa::aligned16(v_scale))
-      return fail(PA_ERR_INVALID, "pa_cache_write: FP8 cache needs 16-byte aligned scales");
+      return fail(PA_ERR_INVALID, "pa_cache_write: FP8 / INT8 cache needs 16-byte aligned scales");
   } else {
     if (in_dtype != desc->kv_dtype && in_dtype != PA_DTYPE_F32)
       return fail(PA_ERR_INVALID, "pa_cache_write: in_dtype must equal kv_dtype or be F32");
     if (k_scale || v_scale)
-      return fail(PA_ERR_INVALID, "pa_cache_write: scales are only for FP8 caches");
+      return fail(PA_ERR_INVALID, "pa_cache_write: scales are only for FP8 / INT8 caches");
   }
   return pa::launch_cache_write(k, v, in_dtype, slot_mapping, num_tokens, k_cache, v_cache,
                                 k_scale, v_scale, desc, stream);
@@ -193,16 +192,16 @@ static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache
   if (num_q_heads / desc->num_kv_heads > PA_MAX_GROUP)
     return fail(PA_ERR_UNSUPPORTED, "pa_decode: more than %d query heads per kv head", PA_MAX_GROUP);
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "pa_decode: scale is not finite");
-  const bool fp8 = desc->kv_dtype == PA_DTYPE_FP8_E4M3;
-  if (fp8) {
+  const bool q8 = pa::quantised(desc->kv_dtype);
+  if (q8) {
     if (q_dtype != PA_DTYPE_F16 && q_dtype != PA_DTYPE_BF16)
-      return fail(PA_ERR_INVALID, "pa_decode: q_dtype must be F16 or BF16 for an FP8 cache");
+      return fail(PA_ERR_INVALID, "pa_decode: q_dtype must be F16 or BF16 for an FP8 / INT8 cache");
     if (!k_scale || !v_scale || !pa::aligned16(k_scale) || !pa::aligned16(v_scale))
-      return fail(PA_ERR_INVALID, "pa_decode: FP8 cache needs 16-byte aligned scales");
+      return fail(PA_ERR_INVALID, "pa_decode: FP8 / INT8 cache needs 16-byte aligned scales");
   } else {
     if (q_dtype != desc->kv_dtype)
       return fail(PA_ERR_INVALID, "pa_decode: q_dtype must equal kv_dtype");
-    if (k_scale || v_scale) return fail(PA_ERR_INVALID, "pa_decode: scales are only for FP8 caches");
+    if (k_scale || v_scale) return fail(PA_ERR_INVALID, "pa_decode: scales are only for FP8 / INT8 caches");
   }
   if (out_dtype != q_dtype && out_dtype != PA_DTYPE_F32)
     return fail(PA_ERR_INVALID, "pa_decode: out_dtype must be q_dtype or F32");
@@ -250,7 +249,7 @@ static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache
     if (!k_new || !v_new) return fail(PA_ERR_INVALID, "pa_decode_append: k_new / v_new is NULL");
     if (!pa::aligned16(k_new) || !pa::aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
       return fail(PA_ERR_INVALID, "pa_decode_append: misaligned pointer");
-    if (fp8 ? (new_dtype != PA_DTYPE_F16 && new_dtype != PA_DTYPE_BF16 && new_dtype != PA_DTYPE_F32)
+    if (q8 ? (new_dtype != PA_DTYPE_F16 && new_dtype != PA_DTYPE_BF16 && new_dtype != PA_DTYPE_F32)
             : (new_dtype != desc->kv_dtype && new_dtype != PA_DTYPE_F32))
       return fail(PA_ERR_INVALID, "pa_decode_append: new_dtype does not match the cache");
     a.k_new = k_new;
@@ -297,8 +296,8 @@ static pa_status check_prefill(int32_t T, int32_t B, int32_t num_q_heads, int32_
     return fail(PA_ERR_INVALID, "pa_chunked_prefill: num_q_heads must be a multiple of num_kv_heads");
   if (num_q_heads / desc->num_kv_heads > PA_MAX_GROUP)
     return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: more than %d query heads per kv head", PA_MAX_GROUP);
-  if (desc->kv_dtype == PA_DTYPE_FP8_E4M3)
-    return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: FP8 caches are not built");
+  if (pa::quantised(desc->kv_dtype))
+    return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: FP8 / INT8 caches are not built");
   return PA_OK;
 }
 
@@ -381,11 +380,11 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_
   if (!k_cache || !v_cache || !pairs) return fail(PA_ERR_INVALID, "pa_copy_blocks: null pointer");
   if (!pa::aligned16(k_cache) || !pa::aligned16(v_cache) || (reinterpret_cast<uintptr_t>(pairs) & 7u))
     return fail(PA_ERR_INVALID, "pa_copy_blocks: misaligned pointer");
-  const bool fp8 = desc->kv_dtype == PA_DTYPE_FP8_E4M3;
-  if (fp8 && (!k_scale || !v_scale))
-    return fail(PA_ERR_INVALID, "pa_copy_blocks: FP8 cache needs scales");
-  if (!fp8 && (k_scale || v_scale))
-    return fail(PA_ERR_INVALID, "pa_copy_blocks: scales are only for FP8 caches");
+  const bool q8 = pa::quantised(desc->kv_dtype);
+  if (q8 && (!k_scale || !v_scale))
+    return fail(PA_ERR_INVALID, "pa_copy_blocks: FP8 / INT8 cache needs scales");
+  if (!q8 && (k_scale || v_scale))
+    return fail(PA_ERR_INVALID, "pa_copy_blocks: scales are only for FP8 / INT8 caches");
   return pa::launch_copy_blocks(k_cache, v_cache, k_scale, v_scale, pairs, num_pairs, desc, stream);
 }
 
@@ -406,11 +405,11 @@ pa_status pa_swap_blocks(void* dst_k, void* dst_v, float* dst_k_scale, float* ds
   if (!pa::aligned16(dst_k) || !pa::aligned16(dst_v) || !pa::aligned16(src_k) || !pa::aligned16(src_v) ||
       (reinterpret_cast<uintptr_t>(pairs) & 7u))
     return fail(PA_ERR_INVALID, "pa_swap_blocks: misaligned pointer");
-  const bool fp8 = desc->kv_dtype == PA_DTYPE_FP8_E4M3;
-  if (fp8 != (dst_k_scale && dst_v_scale && src_k_scale && src_v_scale))
-    return fail(PA_ERR_INVALID, "pa_swap_blocks: FP8 pools need all four scale arrays, others none");
-  if (!fp8 && (dst_k_scale || dst_v_scale || src_k_scale || src_v_scale))
-    return fail(PA_ERR_INVALID, "pa_swap_blocks: scales are only for FP8 pools");
+  const bool q8 = pa::quantised(desc->kv_dtype);
+  if (q8 != (dst_k_scale && dst_v_scale && src_k_scale && src_v_scale))
+    return fail(PA_ERR_INVALID, "pa_swap_blocks: FP8 / INT8 pools need all four scale arrays, others none");
+  if (!q8 && (dst_k_scale || dst_v_scale || src_k_scale || src_v_scale))
+    return fail(PA_ERR_INVALID, "pa_swap_blocks: scales are only for FP8 / INT8 pools");
   return pa::launch_swap_blocks(dst_k, dst_v, dst_k_scale, dst_v_scale, dst_num_blocks, src_k, src_v,
                                 src_k_scale, src_v_scale, src_num_blocks, pairs, num_pairs, desc, stream);
 }

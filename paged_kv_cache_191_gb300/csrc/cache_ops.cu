@@ -7,8 +7,9 @@
 // movers: 16-byte vector loads and stores, one CTA per token (write) or per
 // (pair, chunk) (copy).
 //
-// FP8 E4M3 caches ("LLM推理引擎深度实战" 5.3): one float32 scale per token
-// per tensor, scale = amax/448 (IEEE division), code = RNE-satfinite E4M3 of
+// FP8 E4M3 and INT8 caches ("LLM推理引擎深度实战" 5.3): one float32 scale per
+// token per tensor, scale = amax/448 (E4M3) or amax/127 (INT8) by IEEE
+// division, code = RNE-satfinite E4M3, or round-to-nearest-even INT8, of
 // x/scale (IEEE division), so the codes are a deterministic function of the
 // input bits.
 //
@@ -111,10 +112,21 @@ __device__ __forceinline__ float block_max(float x, float* red) {
   return red[32];
 }
 
-// FP8 cache: per-token amax -> scale -> E4M3 codes, for K then V.
-template <int IN>
+// One code of a quantised cache from a float already divided by the scale:
+// E4M3 round-to-nearest-even saturating to finite, or INT8 round-to-nearest-
+// even (the scale makes |x| <= 127 up to its own rounding; clamped).
+template <bool INT8>
+__device__ __forceinline__ uint32_t encode_q8(float x) {
+  if constexpr (INT8)
+    return static_cast<uint32_t>(static_cast<uint8_t>(static_cast<int8_t>(max(-127, min(127, __float2int_rn(x))))));
+  else
+    return __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Quantised cache (E4M3 or INT8): per-token amax -> scale -> codes, for K then V.
+template <int IN, bool INT8>
 __global__ void __launch_bounds__(kWriteThreads)
-    cache_write_fp8(const void* __restrict__ k, const void* __restrict__ v,
+    cache_write_q8(const void* __restrict__ k, const void* __restrict__ v,
                     const int64_t* __restrict__ slots, uint8_t* __restrict__ kc,
                     uint8_t* __restrict__ vc, float* __restrict__ ks, float* __restrict__ vs,
                     int Hkv, int D, int num_blocks) {
@@ -143,7 +155,7 @@ __global__ void __launch_bounds__(kWriteThreads)
       for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
     }
     amax = block_max(amax, red);
-    const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const float scale = amax > 0.f ? __fdiv_rn(amax, INT8 ? 127.0f : 448.0f) : 1.0f;
     for (int j = threadIdx.x; j < nvec; j += blockDim.x) {
       const int h = j / vpr, c = j - h * vpr;
       float x[8];
@@ -151,8 +163,7 @@ __global__ void __launch_bounds__(kWriteThreads)
       uint32_t lo = 0, hi = 0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const uint32_t code =
-            __nv_cvt_float_to_fp8(__fdiv_rn(x[e], scale), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t code = encode_q8<INT8>(__fdiv_rn(x[e], scale));
         if (e < 4)
           lo |= code << (8 * e);
         else
@@ -207,9 +218,10 @@ __global__ void __launch_bounds__(kCopyThreads)
 }
 
 template <int IN>
-void launch_fp8(const void* k, const void* v, const int64_t* s, int64_t T, void* kc, void* vc,
-                float* ks, float* vs, const pa_cache_desc* d, cudaStream_t st) {
-  cache_write_fp8<IN><<<static_cast<unsigned>(T), kWriteThreads, 0, st>>>(
+void launch_q8(const void* k, const void* v, const int64_t* s, int64_t T, void* kc, void* vc,
+               float* ks, float* vs, const pa_cache_desc* d, cudaStream_t st) {
+  auto kernel = d->kv_dtype == PA_DTYPE_INT8 ? cache_write_q8<IN, true> : cache_write_q8<IN, false>;
+  kernel<<<static_cast<unsigned>(T), kWriteThreads, 0, st>>>(
       k, v, s, static_cast<uint8_t*>(kc), static_cast<uint8_t*>(vc), ks, vs, d->num_kv_heads,
       d->head_dim, d->num_blocks);
 }
@@ -237,11 +249,11 @@ pa_status launch_cache_write(const void* k, const void* v, int32_t in_dtype, con
       break;
     default:
       if (in_dtype == PA_DTYPE_F16)
-        launch_fp8<PA_DTYPE_F16>(k, v, slots, T, kc, vc, ks, vs, d, st);
+        launch_q8<PA_DTYPE_F16>(k, v, slots, T, kc, vc, ks, vs, d, st);
       else if (in_dtype == PA_DTYPE_BF16)
-        launch_fp8<PA_DTYPE_BF16>(k, v, slots, T, kc, vc, ks, vs, d, st);
+        launch_q8<PA_DTYPE_BF16>(k, v, slots, T, kc, vc, ks, vs, d, st);
       else
-        launch_fp8<PA_DTYPE_F32>(k, v, slots, T, kc, vc, ks, vs, d, st);
+        launch_q8<PA_DTYPE_F32>(k, v, slots, T, kc, vc, ks, vs, d, st);
       break;
   }
   const cudaError_t e = cudaGetLastError();

@@ -26,9 +26,9 @@
 //   P^T[16 x 8] with A = V via ldmatrix.trans and B = P^T from the score
 //   fragment by movmatrix.  bf16 P is carried as hi + lo bf16 parts (rounding
 //   error ~2^-17).
-// * FP8 E4M3 caches: codes are converted exactly to f16/bf16 in registers;
-//   the per-token K scale multiplies the score, the per-token V scale
-//   multiplies p before the PV product.
+// * FP8 E4M3 and INT8 caches (1-byte codes): codes are converted exactly to
+//   f16/bf16 in registers; the per-token K scale multiplies the score, the
+//   per-token V scale multiplies p before the PV product.
 // * A one-partition sequence is written directly; otherwise the partition
 //   writes (o, m, l) and decode_reduce merges the partitions with log-sum-exp
 //   weights, launched as a programmatic dependent.
@@ -73,7 +73,7 @@ struct DecodeArgs {
   void* k_cache_w;  // the caches, for the fused row store
   void* v_cache_w;
   const int64_t* slot_mapping;
-  float* k_scale_w;  // FP8 scales, writable views of k_scale / v_scale
+  float* k_scale_w;  // FP8 / INT8 scales, writable views of k_scale / v_scale
   float* v_scale_w;
   int32_t new_dtype;
   int32_t fuse_write;
@@ -88,14 +88,14 @@ __device__ __forceinline__ float load_in(const void* p, size_t i, int dt) {
 
 // One warp stores kv head g's row of this step's new token (K and V) into
 // the cache slot, exactly as pa_cache_write does: a same-dtype copy, a
-// round-to-nearest-even conversion from f32, or for FP8 the per-token
-// amax / scale / E4M3 encoding over all Hkv*D values of the token.  Every kv
+// round-to-nearest-even conversion from f32, or for FP8 / INT8 the per-token
+// amax / scale / code encoding over all Hkv*D values of the token.  Every kv
 // head's warp recomputes the token's amax and stores the (identical) scale:
 // its own later read of the scale row must not depend on another CTA.
 template <typename KT, int D>
 __device__ __forceinline__ void write_new_row(const DecodeArgs& a, KT* kc, KT* vc, int b, int g,
                                               int64_t slot, int lane) {
-  constexpr bool FP8 = sizeof(KT) == 1;
+  constexpr bool Q8 = sizeof(KT) == 1;  // 1-byte codes: E4M3 or INT8
   const int64_t blk = slot / 16, off = slot % 16;
   const size_t dst = ((static_cast<size_t>(blk) * a.Hkv + g) * 16 + off) * D;
 #pragma unroll
@@ -103,16 +103,21 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs& a, KT* kc, KT* v
     const void* src = which ? a.v_new : a.k_new;
     KT* cache = which ? vc : kc;
     const size_t row = (static_cast<size_t>(b) * a.Hkv + g) * D;
-    if constexpr (FP8) {
+    if constexpr (Q8) {
       float amax = 0.f;
       const size_t tok = static_cast<size_t>(b) * a.Hkv * D;
       for (int i = lane; i < a.Hkv * D; i += 32) amax = fmaxf(amax, fabsf(load_in(src, tok + i, a.new_dtype)));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-      for (int d = lane; d < D; d += 32)
-        cache[dst + d] = static_cast<KT>(
-            __nv_cvt_float_to_fp8(__fdiv_rn(load_in(src, row + d, a.new_dtype), scale), __NV_SATFINITE, __NV_E4M3));
+      constexpr bool INT8 = std::is_same<KT, int8_t>::value;
+      const float scale = amax > 0.f ? __fdiv_rn(amax, INT8 ? 127.0f : 448.0f) : 1.0f;
+      for (int d = lane; d < D; d += 32) {
+        const float x = __fdiv_rn(load_in(src, row + d, a.new_dtype), scale);
+        if constexpr (INT8)
+          cache[dst + d] = static_cast<KT>(max(-127, min(127, __float2int_rn(x))));
+        else
+          cache[dst + d] = static_cast<KT>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+      }
       if (lane == 0) (which ? a.v_scale_w : a.k_scale_w)[slot] = scale;
     } else {
       for (int d = lane; d < D; d += 32) {
@@ -141,7 +146,7 @@ struct Tile {
   static constexpr bool ONE_BOX = NBOX == 2;
   static constexpr int NS = kRingBytes / (2 * BYTES);             // K+V stages per warp
   static constexpr int RING = NS * 2 * BYTES;                      // one warp's ring
-  // shared memory of a W-warp CTA: rings [W], FP8 scales [W][NS][32] f32,
+  // shared memory of a W-warp CTA: rings [W], code scales [W][NS][32] f32,
   // full barriers [W][NS]
   static constexpr int off_sc(int W) { return W * RING; }
   static constexpr int off_bar(int W) { return off_sc(W) + W * NS * 128; }
@@ -183,10 +188,10 @@ __global__ void __launch_bounds__(32 * W)
                 const DecodeArgs a) {
   using TL = Tile<KT, D>;
   constexpr int NS = TL::NS;
-  constexpr bool FP8 = sizeof(KT) == 1;
+  constexpr bool Q8 = sizeof(KT) == 1;  // 1-byte codes: E4M3 or INT8
   constexpr int KSTEPS = D / 16;
   constexpr int MT = D / 16;
-  constexpr uint32_t STAGE_TX = 2 * TL::BYTES + (FP8 ? 128 : 0);
+  constexpr uint32_t STAGE_TX = 2 * TL::BYTES + (Q8 ? 128 : 0);
   constexpr bool SPLIT_P = std::is_same<QT, __nv_bfloat16>::value;
   constexpr unsigned FULL = 0xffffffffu;
 
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(32 * W)
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
       if (r < a.G) {
-        if constexpr (FP8) {  // permuted k order matching the register-converted K fragment
+        if constexpr (Q8) {  // permuted k order matching the register-converted K fragment
           const uint2 w = *reinterpret_cast<const uint2*>(qrow + 32 * q4 + 4 * kk);
           qf[kk][0] = w.x;
           qf[kk][1] = w.y;
@@ -297,7 +302,7 @@ __global__ void __launch_bounds__(32 * W)
         dev::tma_load_3d(vdst + bx * 2048, &tmV, bar, bx * TL::BOXE, g * 16, pb);
       }
     }
-    if constexpr (FP8) {
+    if constexpr (Q8) {
       dev::bulk_load(dev::smem_addr(s_scale + s * 32), a.k_scale + static_cast<size_t>(pb) * 16, 64, bar);
       dev::bulk_load(dev::smem_addr(s_scale + s * 32 + 16), a.v_scale + static_cast<size_t>(pb) * 16, 64, bar);
     }
@@ -333,7 +338,7 @@ __global__ void __launch_bounds__(32 * W)
     // ---- K and V fragments -> registers, then refill the stage ---------------
     uint32_t kf[KSTEPS][4], vf[MT][4];
     float c_r = sl2, c_r8 = sl2, vs_r = 1.f, vs_r8 = 1.f;
-    if constexpr (FP8) {
+    if constexpr (Q8) {
       const uint4 x0 = dev::lds128(kb + swz(r, 2 * q4));
       const uint4 x1 = dev::lds128(kb + swz(r, 2 * q4 + 1));
       const uint4 y0 = dev::lds128(kb + swz(r + 8, 2 * q4));
@@ -382,11 +387,11 @@ __global__ void __launch_bounds__(32 * W)
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
       uint32_t af[4];
-      if constexpr (FP8) {
-        af[0] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(kf[kk][0] & 0xffffu));
-        af[1] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(kf[kk][1] & 0xffffu));
-        af[2] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(kf[kk][0] >> 16));
-        af[3] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(kf[kk][1] >> 16));
+      if constexpr (Q8) {
+        af[0] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(kf[kk][0] & 0xffffu));
+        af[1] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(kf[kk][1] & 0xffffu));
+        af[2] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(kf[kk][0] >> 16));
+        af[3] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(kf[kk][1] >> 16));
       } else {
         af[0] = kf[kk][0];
         af[1] = kf[kk][1];
@@ -415,7 +420,7 @@ __global__ void __launch_bounds__(32 * W)
     float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1), p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
 
     uint32_t ph_r, ph_r8, pl_r = 0, pl_r8 = 0;
-    if constexpr (FP8) {
+    if constexpr (Q8) {
       l0 = l0 * al0 + (p0 + p2);
       l1 = l1 * al1 + (p1 + p3);
       p0 *= vs_r;
@@ -429,11 +434,11 @@ __global__ void __launch_bounds__(32 * W)
       const float2 h_r = dev::unpack2<QT>(ph_r), h_r8 = dev::unpack2<QT>(ph_r8);
       pl_r = dev::pack2<QT>(p0 - h_r.x, p1 - h_r.y);
       pl_r8 = dev::pack2<QT>(p2 - h_r8.x, p3 - h_r8.y);
-      if constexpr (!FP8) {
+      if constexpr (!Q8) {
         l0 = l0 * al0 + (p0 + p2);
         l1 = l1 * al1 + (p1 + p3);
       }
-    } else if constexpr (!FP8) {
+    } else if constexpr (!Q8) {
       // normalise with the rounded weights actually used in the PV product
       const float2 h_r = dev::unpack2<QT>(ph_r), h_r8 = dev::unpack2<QT>(ph_r8);
       l0 = l0 * al0 + (h_r.x + h_r8.x);
@@ -454,14 +459,14 @@ __global__ void __launch_bounds__(32 * W)
       o[mt][2] *= al0;
       o[mt][3] *= al1;
       uint32_t af[4];
-      if constexpr (FP8) {
+      if constexpr (Q8) {
         const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
         const uint32_t xy = dev::prmt(vf[mt >> 1][0], vf[mt >> 1][1], sel);
         const uint32_t zv = dev::prmt(vf[mt >> 1][2], vf[mt >> 1][3], sel);
-        af[0] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(xy & 0xffffu));
-        af[1] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(xy >> 16));
-        af[2] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(zv & 0xffffu));
-        af[3] = dev::e4m3x2_to<QT>(static_cast<uint16_t>(zv >> 16));
+        af[0] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(xy & 0xffffu));
+        af[1] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(xy >> 16));
+        af[2] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(zv & 0xffffu));
+        af[3] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(zv >> 16));
       } else {
         af[0] = vf[mt][0];
         af[1] = vf[mt][1];
@@ -487,7 +492,7 @@ __global__ void __launch_bounds__(32 * W)
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       int d_r, d_r8;
-      if constexpr (FP8) {
+      if constexpr (Q8) {
         d_r = 16 * r + 2 * mt;
         d_r8 = d_r + 1;
       } else {
@@ -540,7 +545,7 @@ __global__ void __launch_bounds__(32 * W)
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     int d_r, d_r8;
-    if constexpr (FP8) {
+    if constexpr (Q8) {
       d_r = 16 * r + 2 * mt;
       d_r8 = d_r + 1;
     } else {
@@ -794,7 +799,12 @@ pa_status launch_decode(const DecodeLaunch& l, void* stream_ptr) {
     if (l.D == 64) return launch_t<__nv_bfloat16, __nv_bfloat16, 64>(l, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, st);
     return launch_t<__nv_bfloat16, __nv_bfloat16, 128>(l, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, st);
   }
-  // FP8 E4M3 codes, head_dim 128 (checked by the caller)
+  // 1-byte codes (E4M3 as uint8_t, INT8 as int8_t), head_dim 128 (checked by
+  // the caller); the tensor map moves raw bytes either way
+  if (l.kv_dtype == PA_DTYPE_INT8) {
+    if (l.q_dtype == PA_DTYPE_F16) return launch_t<int8_t, __half, 128>(l, CU_TENSOR_MAP_DATA_TYPE_UINT8, st);
+    return launch_t<int8_t, __nv_bfloat16, 128>(l, CU_TENSOR_MAP_DATA_TYPE_UINT8, st);
+  }
   if (l.q_dtype == PA_DTYPE_F16) return launch_t<uint8_t, __half, 128>(l, CU_TENSOR_MAP_DATA_TYPE_UINT8, st);
   return launch_t<uint8_t, __nv_bfloat16, 128>(l, CU_TENSOR_MAP_DATA_TYPE_UINT8, st);
 }

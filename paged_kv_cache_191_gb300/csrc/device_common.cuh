@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace pa {
 namespace dev {
 
@@ -215,6 +217,36 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
+}
+
+// Two INT8 codes (lo byte first) -> two 16-bit floats of type T, exactly.
+// Flipping the sign bit gives the biased byte c + 128 in [0, 255]; placed
+// under the exponent byte 0x64 it reads as the f16 value 1024 + c + 128, and
+// subtracting 1152 (exact: all terms are integers below 2^11) leaves c.
+template <typename T>
+__device__ __forceinline__ uint32_t i8x2_to(uint16_t codes);
+template <>
+__device__ __forceinline__ uint32_t i8x2_to<__half>(uint16_t codes) {
+  const uint32_t biased = prmt(static_cast<uint32_t>(codes) ^ 0x8080u, 0x64646464u, 0x4140u);
+  __half2 h = *reinterpret_cast<const __half2*>(&biased);
+  h = __hsub2(h, __half2half2(__ushort_as_half(0x6480u)));  // 1152
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t i8x2_to<__nv_bfloat16>(uint16_t codes) {
+  const uint32_t h = i8x2_to<__half>(codes);
+  const float2 f = unpack2<__half>(h);   // exact
+  return pack2<__nv_bfloat16>(f.x, f.y);  // exact: |c| <= 128 fits 8 bits
+}
+
+// Two 1-byte codes of a quantised cache -> two 16-bit floats of type T:
+// E4M3 for uint8_t storage, INT8 for int8_t storage.
+template <typename KT, typename T>
+__device__ __forceinline__ uint32_t code8x2_to(uint16_t codes) {
+  if constexpr (std::is_same<KT, int8_t>::value)
+    return i8x2_to<T>(codes);
+  else
+    return e4m3x2_to<T>(codes);
 }
 
 }  // namespace dev

@@ -21,11 +21,15 @@ inline int dtype_bytes(int32_t dt) {
   switch (dt) {
     case PA_DTYPE_F16:
     case PA_DTYPE_BF16: return 2;
-    case PA_DTYPE_FP8_E4M3: return 1;
+    case PA_DTYPE_FP8_E4M3:
+    case PA_DTYPE_INT8: return 1;
     case PA_DTYPE_F32: return 4;
     default: return 0;
   }
 }
+
+// Caches of 1-byte codes with per-token scale rows (FP8 E4M3, INT8).
+inline bool quantised(int32_t dt) { return dt == PA_DTYPE_FP8_E4M3 || dt == PA_DTYPE_INT8; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

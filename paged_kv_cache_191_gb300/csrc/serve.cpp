@@ -117,8 +117,8 @@ pa_status pa_serve_create(pa_sched* s, const pa_cache_desc* desc, const pa_serve
   if (!out) return pa::fail(PA_ERR_INVALID, "pa_serve_create: out is NULL");
   *out = nullptr;
   if (!s || !desc || !b) return pa::fail(PA_ERR_INVALID, "pa_serve_create: null argument");
-  if (desc->kv_dtype == PA_DTYPE_FP8_E4M3)
-    return pa::fail(PA_ERR_UNSUPPORTED, "pa_serve_create: FP8 caches are not built for the chunk kernel");
+  if (pa::quantised(desc->kv_dtype))
+    return pa::fail(PA_ERR_UNSUPPORTED, "pa_serve_create: FP8 / INT8 caches are not built for the chunk kernel");
   int32_t mb = 0, mt = 0, nb = 0;
   pa_status st = pa_sched_limits(s, &mb, &mt, &nb);
   if (st != PA_OK) return st;

@@ -16,13 +16,13 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 
 PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_NOT_FOUND, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = range(6)
-F16, BF16, FP8_E4M3, F32 = 0, 1, 2, 3
+F16, BF16, FP8_E4M3, F32, INT8 = 0, 1, 2, 3, 4
 BLOCK_SIZE = 16
 DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 DEVERR_QUERY_RANGE = 16
 
 _TORCH_DT = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
-             torch.uint8: FP8_E4M3, torch.float8_e4m3fn: FP8_E4M3}
+             torch.uint8: FP8_E4M3, torch.float8_e4m3fn: FP8_E4M3, torch.int8: INT8}
 
 
 class PagedKVError(RuntimeError):

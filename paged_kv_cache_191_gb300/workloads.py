@@ -46,7 +46,7 @@ class DecodeWorkload:
     Hq: int
     Hkv: int
     D: int
-    kv_dtype: str                 # "f16", "bf16" or "fp8" (fp8: pools hold the f16 source)
+    kv_dtype: str                 # "f16", "bf16", "fp8" or "int8" (fp8 / int8: pools hold the f16 source)
     context_lens: np.ndarray      # int32 [B], includes this step's new token
     num_blocks: int
     free_order: np.ndarray        # int64 permutation of the pool
@@ -89,7 +89,7 @@ def make_decode(name, seed, B, Hq, Hkv, D, kv_dtype, lens, pool_factor=1.2,
     order = rng.permutation(num_blocks).astype(np.int64)
     mb = max_blocks or max(1, max(-(-int(n) // BLOCK) for n in lens))
     tables = _tables_from_order(order, lens, mb)
-    tdt = torch.float16 if kv_dtype in ("f16", "fp8") else torch.bfloat16
+    tdt = torch.float16 if kv_dtype in ("f16", "fp8", "int8") else torch.bfloat16
     q = randn(rng, (B, Hq, D), tdt)
     k_pool = randn(rng, (num_blocks, Hkv, BLOCK, D), tdt)
     v_pool = randn(rng, (num_blocks, Hkv, BLOCK, D), tdt)
@@ -346,4 +346,5 @@ CONFIGS = {
     "gqa70b_b64": config_gqa70b,
     "longctx_b8_f16": lambda: config_longctx("f16"),
     "longctx_b8_fp8": lambda: config_longctx("fp8"),
+    "longctx_b8_int8": lambda: config_longctx("int8"),
 }

@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 import torch
 
-TOL = {"f16": 2e-3, "bf16": 2e-3, "fp8": 2e-2}
+TOL = {"f16": 2e-3, "bf16": 2e-3, "fp8": 2e-2, "int8": 2e-2}
 
 requires_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
 

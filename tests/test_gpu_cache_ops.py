@@ -47,15 +47,17 @@ def test_write_16bit(kv, inp, H, D, T):
 
 @pytest.mark.parametrize("inp", ["f16", "bf16", "f32"])
 @pytest.mark.parametrize("H,T", [(8, 33), (2, 7)])
-def test_write_fp8(inp, H, T):
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+def test_write_fp8(inp, H, T, fmt):
     N, D = 24, 128
     rng = W.rng_for(4)
     k = W.randn(rng, (T, H, D), TD[inp]) * 3
     v = W.randn(rng, (T, H, D), TD[inp])
     k[0].zero_()                              # all-zero token -> scale 1, zero codes
     slots = W.random_slots(5, T, N, n_skip=2)
-    kc = torch.randint(0, 255, (N, H, 16, D), dtype=torch.uint8)
-    vc = torch.randint(0, 255, (N, H, 16, D), dtype=torch.uint8)
+    cdt, lo = (torch.int8, -128) if fmt == "int8" else (torch.uint8, 0)
+    kc = torch.randint(lo, lo + 255, (N, H, 16, D), dtype=cdt)
+    vc = torch.randint(lo, lo + 255, (N, H, 16, D), dtype=cdt)
     ks = torch.rand((N, 16), dtype=torch.float32)
     vs = torch.rand((N, 16), dtype=torch.float32)
     gk, gv, gks, gvs = kc.to(DEV), vc.to(DEV), ks.to(DEV), vs.to(DEV)
@@ -78,15 +80,16 @@ def test_write_out_of_range_slot_is_flagged_and_skipped():
     assert np.array_equal(np_exact(gk), ek)
 
 
-@pytest.mark.parametrize("dt", ["f16", "bf16", "fp8"])
+@pytest.mark.parametrize("dt", ["f16", "bf16", "fp8", "int8"])
 @pytest.mark.parametrize("H,D,n", [(32, 128, 19), (8, 128, 1), (4, 64, 40)])
 def test_copy_blocks(dt, H, D, n):
-    if dt == "fp8" and D != 128:
-        pytest.skip("FP8 caches are built for head_dim 128")
+    if dt in ("fp8", "int8") and D != 128:
+        pytest.skip("FP8 / INT8 caches are built for head_dim 128")
     N = 100
-    if dt == "fp8":
-        kc = torch.randint(0, 255, (N, H, 16, D), dtype=torch.uint8)
-        vc = torch.randint(0, 255, (N, H, 16, D), dtype=torch.uint8)
+    if dt in ("fp8", "int8"):
+        cdt, lo = (torch.int8, -128) if dt == "int8" else (torch.uint8, 0)
+        kc = torch.randint(lo, lo + 255, (N, H, 16, D), dtype=cdt)
+        vc = torch.randint(lo, lo + 255, (N, H, 16, D), dtype=cdt)
         ks, vs = torch.rand((N, 16)), torch.rand((N, 16))
     else:
         kc, vc = _pool(7, N, H, D, TD[dt])

@@ -1,6 +1,6 @@
 """GPU parity of pa_decode against the float64 oracle.
 
-Tolerances: max-abs 2e-3 for f16/bf16 caches and 2e-2 for FP8 caches, judged
+Tolerances: max-abs 2e-3 for f16/bf16 caches and 2e-2 for FP8 / INT8 caches, judged
 on float32 outputs (a bf16 output alone carries up to 2^-9 relative rounding,
 which exceeds 2e-3 near |o| = 1); the 16-bit outputs are checked within the
 tolerance plus half an ulp of the output dtype.  Small ragged cases are
@@ -164,7 +164,7 @@ def fp8_pool_gpu(w):
     kin = w.k_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(DEV)
     vin = w.v_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(DEV)
     slots = torch.arange(N * 16, dtype=torch.int64, device=DEV)
-    kc = torch.zeros((N, H, 16, D), dtype=torch.uint8, device=DEV)
+    kc = torch.zeros((N, H, 16, D), dtype=torch.int8 if w.kv_dtype == "int8" else torch.uint8, device=DEV)
     vc = torch.zeros_like(kc)
     ks = torch.zeros((N, 16), dtype=torch.float32, device=DEV)
     vs = torch.zeros_like(ks)
@@ -180,7 +180,7 @@ def fp8_pool_oracle(w, blocks=None):
     slots = (blocks[:, None] * 16 + np.arange(16)[None, :]).reshape(-1)
     kin = np_exact(w.k_pool[torch.from_numpy(blocks)]).transpose(0, 2, 1, 3).reshape(-1, H, D)
     vin = np_exact(w.v_pool[torch.from_numpy(blocks)]).transpose(0, 2, 1, 3).reshape(-1, H, D)
-    kc = np.zeros((N, H, 16, D), np.uint8)
+    kc = np.zeros((N, H, 16, D), np.int8 if w.kv_dtype == "int8" else np.uint8)
     vc = np.zeros_like(kc)
     ks = np.zeros((N, 16), np.float32)
     vs = np.zeros_like(ks)
@@ -189,8 +189,9 @@ def fp8_pool_oracle(w, blocks=None):
 
 @pytest.mark.parametrize("qdt", ["f16", "bf16"])
 @pytest.mark.parametrize("split", [0, 64])
-def test_fp8_small(qdt, split):
-    w = W.random_small(51, B=5, Hq=16, Hkv=4, D=128, kv_dtype="fp8", max_len=800)
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+def test_fp8_small(qdt, split, fmt):
+    w = W.random_small(51, B=5, Hq=16, Hkv=4, D=128, kv_dtype=fmt, max_len=800)
     if qdt == "bf16":
         w.q = w.q.to(torch.bfloat16)
     kc, vc, ks, vs = fp8_pool_gpu(w)
@@ -199,7 +200,7 @@ def test_fp8_small(qdt, split):
     assert np.array_equal(ks.numpy(), oks) and np.array_equal(vs.numpy(), ovs)
     ref = paged_decode(np_exact(w.q), okc, ovc, w.block_tables, w.context_lens, w.scale, oks, ovs)
     got = gpu_decode(w, split_tokens=split, pools=(kc, vc), scales=(ks, vs)).numpy()
-    assert_close(got, ref, TOL["fp8"], f"fp8 q={qdt}")
+    assert_close(got, ref, TOL[fmt], f"{fmt} q={qdt}")
     # against the unquantised cache: reported, loosely bounded at small contexts
     ref16 = oracle(w)
     assert np.abs(got - ref16).max() < 0.25
@@ -227,8 +228,9 @@ def test_full_size_sampled(cfg):
     assert np.all(np.isfinite(got))
 
 
-def test_full_size_fp8_longctx_sampled():
-    w = W.config_longctx("fp8")
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+def test_full_size_fp8_longctx_sampled(fmt):
+    w = W.config_longctx(fmt)
     kc, vc, ks, vs = fp8_pool_gpu(w)
     heads = sample_heads(w, 3, 9)
     seqs = sorted({b for b, _ in heads})
@@ -239,6 +241,6 @@ def test_full_size_fp8_longctx_sampled():
     got = gpu_decode(w, pools=(kc, vc), scales=(ks, vs)).numpy()
     ref = paged_decode(np_exact(w.q), okc, ovc, w.block_tables, w.context_lens, w.scale, oks, ovs,
                        heads=heads)
-    check_sampled(w, got, heads, ref, TOL["fp8"])
+    check_sampled(w, got, heads, ref, TOL[fmt])
     ref16 = oracle(w, heads=heads)
-    check_sampled(w, got, heads, ref16, TOL["fp8"])
+    check_sampled(w, got, heads, ref16, TOL[fmt])

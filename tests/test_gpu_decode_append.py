@@ -1,6 +1,6 @@
 """pa_decode_append (cache write fused into decode) against the two separate
-calls: outputs, cache contents and FP8 scales must be bit-identical, and both
-within tolerance of the oracle."""
+calls: outputs, cache contents and FP8 / INT8 scales must be bit-identical,
+and both within tolerance of the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -33,7 +33,7 @@ def fp8_caches(w):
     N, H, _, D = w.k_pool.shape
     kin = w.k_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(DEV)
     vin = w.v_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(DEV)
-    kc = torch.empty((N, H, 16, D), dtype=torch.uint8, device=DEV)
+    kc = torch.empty((N, H, 16, D), dtype=torch.int8 if w.kv_dtype == "int8" else torch.uint8, device=DEV)
     vc = torch.empty_like(kc)
     ks = torch.empty((N, 16), dtype=torch.float32, device=DEV)
     vs = torch.empty_like(ks)
@@ -44,6 +44,7 @@ def fp8_caches(w):
 @pytest.mark.parametrize("Hq,Hkv,kv,inp,split", [
     (8, 8, "f16", "f16", 0), (32, 4, "bf16", "bf16", 64), (16, 2, "f16", "f32", 16),
     (16, 4, "fp8", "f16", 0), (8, 2, "fp8", "f32", 64), (8, 8, "fp8", "bf16", 0),
+    (16, 4, "int8", "f16", 0), (8, 2, "int8", "f32", 64), (8, 8, "int8", "bf16", 0),
 ])
 def test_fused_equals_write_then_decode(Hq, Hkv, kv, inp, split):
     w = W.random_small(71 + Hq + Hkv, B=7, Hq=Hq, Hkv=Hkv, D=128, kv_dtype=kv, max_len=600, min_len=1)
@@ -59,7 +60,7 @@ def test_fused_equals_write_then_decode(Hq, Hkv, kv, inp, split):
     ml = int(w.context_lens.max())
     results = []
     for fused in (False, True):
-        if kv == "fp8":
+        if kv in ("fp8", "int8"):
             kc, vc, ks, vs = fp8_caches(w)
         else:
             kc, vc, ks, vs = w.k_pool.to(DEV), w.v_pool.to(DEV), None, None
@@ -74,7 +75,7 @@ def test_fused_equals_write_then_decode(Hq, Hkv, kv, inp, split):
         results.append([t.cpu() for t in (out, kc, vc) + ((ks, vs) if ks is not None else ())])
     for a, b in zip(*results):
         assert torch.equal(a, b), "fused and separate paths differ"
-    if kv != "fp8":
+    if kv not in ("fp8", "int8"):
         kin = np_exact(k_new.cpu().to(TD[kv])) if inp == "f32" else np_exact(k_new.cpu())
         vin = np_exact(v_new.cpu().to(TD[kv])) if inp == "f32" else np_exact(v_new.cpu())
         okc, ovc, _, _ = o_write(kin, vin, slots, np_exact(w.k_pool), np_exact(w.v_pool))
@@ -85,7 +86,8 @@ def test_fused_equals_write_then_decode(Hq, Hkv, kv, inp, split):
 
 @pytest.mark.parametrize("rep", range(6))
 @pytest.mark.parametrize("Hkv", [8, 2])
-def test_fused_fp8_scales_are_race_free(rep, Hkv):
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+def test_fused_fp8_scales_are_race_free(rep, Hkv, fmt):
     """Every kv head of a token reads the token's fresh scale: repeated runs
     with many heads per sequence (the scale row is shared by all of them)."""
-    test_fused_equals_write_then_decode(8 * (Hkv // 2) if Hkv > 2 else 8, Hkv, "fp8", "bf16", 0)
+    test_fused_equals_write_then_decode(8 * (Hkv // 2) if Hkv > 2 else 8, Hkv, fmt, "bf16", 0)

@@ -20,15 +20,16 @@ def no_device_errors():
     assert ops.device_errors(clear=True) == 0
 
 
-@pytest.mark.parametrize("dt", ["f16", "bf16", "fp8"])
+@pytest.mark.parametrize("dt", ["f16", "bf16", "fp8", "int8"])
 def test_swap_out_and_in(dt):
     rng = W.rng_for(21)
     N, NH, H, D = 64, 40, 8, 128
-    if dt == "fp8":
-        gk = torch.randint(0, 255, (N, H, 16, D), dtype=torch.uint8)
-        gv = torch.randint(0, 255, (N, H, 16, D), dtype=torch.uint8)
+    if dt in ("fp8", "int8"):
+        cdt, lo = (torch.int8, -128) if dt == "int8" else (torch.uint8, 0)
+        gk = torch.randint(lo, lo + 255, (N, H, 16, D), dtype=cdt)
+        gv = torch.randint(lo, lo + 255, (N, H, 16, D), dtype=cdt)
         gks, gvs = torch.rand((N, 16)), torch.rand((N, 16))
-        hk = torch.zeros((NH, H, 16, D), dtype=torch.uint8).pin_memory()
+        hk = torch.zeros((NH, H, 16, D), dtype=cdt).pin_memory()
         hv = torch.zeros_like(hk).pin_memory()
         hks, hvs = torch.zeros((NH, 16)).pin_memory(), torch.zeros((NH, 16)).pin_memory()
     else:
