@@ -86,7 +86,12 @@ pa_status plan_prefill(int32_t T, int32_t B, int32_t Hq, int32_t max_q_len, int3
                        const pa_cache_desc* d, int32_t split_tokens, PrefillPlan* plan) {
   const int64_t G = Hq / d->num_kv_heads;
   const int64_t nblk_max = max_context_len <= 0 ? 1 : (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
-  const int64_t tiles = max_q_len <= 0 ? 1 : (static_cast<int64_t>(max_q_len) * G + 63) / 64;
+  // Rows of one (sequence, kv head) are (query token, head of the group)
+  // pairs.  More than 64 of them at head_dim 128 run the tcgen05 kernel
+  // (128-row tiles); otherwise the mma.sync kernel (64-row tiles) wastes less
+  // of its tile.  Two CTAs per SM either way.
+  const int64_t tile_rows = prefill_uses_tc(max_q_len, Hq, d) ? 128 : 64;
+  const int64_t tiles = max_q_len <= 0 ? 1 : (static_cast<int64_t>(max_q_len) * G + tile_rows - 1) / tile_rows;
   int64_t bpp;
   if (split_tokens > 0) {
     if (split_tokens % PA_BLOCK_SIZE || split_tokens > 4096)
@@ -98,20 +103,22 @@ pa_status plan_prefill(int32_t T, int32_t B, int32_t Hq, int32_t max_q_len, int3
     // the grid is full without splitting the context (a split costs partial
     // rows written and merged); otherwise 1024-token partitions, halved
     // while the grid would give fewer than four CTAs per SM.
-    const int64_t units =
-        d->num_kv_heads * std::min<int64_t>(static_cast<int64_t>(B) * tiles, (static_cast<int64_t>(T) * G + 63) / 64 + B);
+    const int64_t units = d->num_kv_heads * std::min<int64_t>(static_cast<int64_t>(B) * tiles,
+                                                             (static_cast<int64_t>(T) * G + tile_rows - 1) / tile_rows + B);
     const int64_t sms = sm_count();
-    if (units >= 8 * sms) {
+    const int64_t per_sm = 2;  // resident CTAs per SM (both kernels)
+    if (units >= 4 * per_sm * sms) {
       bpp = std::max<int64_t>(nblk_max, 1);
     } else {
       bpp = 64;
-      while (bpp > 8 && units * ((nblk_max + bpp - 1) / bpp) < 4 * sms) bpp /= 2;
+      while (bpp > 8 && units * ((nblk_max + bpp - 1) / bpp) < 2 * per_sm * sms) bpp /= 2;
     }
   }
   const int64_t parts = (nblk_max + bpp - 1) / bpp;
   if (parts > 65535) return fail(PA_ERR_UNSUPPORTED, "context too long for the partition grid");
   if (static_cast<int64_t>(B) * d->num_kv_heads * tiles > INT32_MAX)
     return fail(PA_ERR_UNSUPPORTED, "too many row tiles for one grid");
+  plan->tc = tile_rows == 128 ? 1 : 0;
   plan->row_tiles = static_cast<int32_t>(tiles);
   plan->blocks_per_part = static_cast<int32_t>(bpp);
   plan->max_parts = static_cast<int32_t>(parts);

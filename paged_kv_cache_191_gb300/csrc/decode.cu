@@ -763,14 +763,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 pa_status make_kv_map(CUtensorMap* m, const void* cache, int Hkv, int num_blocks, int row_bytes,
-                      int elem_bytes, CUtensorMapDataType dt, const char* what) {
+                      int elem_bytes, CUtensorMapDataType dt, const char* what, bool one_box) {
   auto fn = encode_fn();
   if (!fn) return fail(PA_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", what);
   if (row_bytes != 128 && row_bytes != 256) return fail(PA_ERR_UNSUPPORTED, "%s: row of %d bytes", what, row_bytes);
   const cuuint64_t boxe = static_cast<cuuint64_t>(128 / elem_bytes);  // elements per 128-byte span
   const cuuint64_t rowb = static_cast<cuuint64_t>(row_bytes);
   CUresult r;
-  if (row_bytes == 256) {
+  if (row_bytes == 256 && one_box) {
     const cuuint64_t dims[5] = {boxe, 16, 2, static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t strides[4] = {rowb, 128, rowb * 16, rowb * 16 * Hkv};
     const cuuint32_t box[5] = {static_cast<cuuint32_t>(boxe), 16, 2, 1, 1};
@@ -778,7 +778,8 @@ pa_status make_kv_map(CUtensorMap* m, const void* cache, int Hkv, int num_blocks
     r = fn(m, dt, 5, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
-    const cuuint64_t dims[3] = {boxe, static_cast<cuuint64_t>(16) * Hkv, static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t dims[3] = {rowb / elem_bytes, static_cast<cuuint64_t>(16) * Hkv,
+                                static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t strides[2] = {rowb, rowb * 16 * Hkv};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(boxe), 16, 1};
     const cuuint32_t estr[3] = {1, 1, 1};

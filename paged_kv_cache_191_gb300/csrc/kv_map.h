@@ -13,8 +13,10 @@ namespace pa {
 //   head, block), landing in shared memory as two 2 KB [row][128 B] halves;
 // * row_bytes == 128: a 3-D box (128 bytes, 16 rows of head h at row 16h,
 //   block).
-// `what` names the caller in error messages.
+// `what` names the caller in error messages.  one_box = false asks for the
+// 3-D map with 128-byte boxes on 256-byte rows too (the caller places the
+// two halves of a tile itself).
 pa_status make_kv_map(CUtensorMap* m, const void* cache, int Hkv, int num_blocks, int row_bytes,
-                      int elem_bytes, CUtensorMapDataType dt, const char* what);
+                      int elem_bytes, CUtensorMapDataType dt, const char* what, bool one_box = true);
 
 }  // namespace pa

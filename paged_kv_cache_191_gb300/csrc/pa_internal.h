@@ -72,11 +72,17 @@ pa_status launch_decode(const DecodeLaunch& a, void* stream);
 
 // Split-K plan for one pa_chunked_prefill shape.
 struct PrefillPlan {
-  int32_t row_tiles;        // 64-row tiles per (sequence, kv head) for max_q_len
+  int32_t tc;               // 1: tcgen05 kernel with 128-row tiles; 0: mma.sync, 64-row tiles
+  int32_t row_tiles;        // row tiles per (sequence, kv head) for max_q_len
   int32_t blocks_per_part;  // 16-token blocks per partition
   int32_t max_parts;        // partitions of the longest allowed context
   size_t workspace_bytes;   // 0 when max_parts == 1
 };
+// Whether pa_chunked_prefill runs its tcgen05 kernel (128-row tiles) for
+// this shape: head_dim 128 and more than 64 rows per (sequence, kv head).
+inline bool prefill_uses_tc(int32_t max_q_len, int32_t num_q_heads, const pa_cache_desc* d) {
+  return d->head_dim == 128 && static_cast<int64_t>(max_q_len) * (num_q_heads / d->num_kv_heads) > 64;
+}
 pa_status plan_prefill(int32_t num_tokens, int32_t B, int32_t num_q_heads, int32_t max_q_len,
                        int32_t max_context_len, const pa_cache_desc* desc, int32_t split_tokens,
                        PrefillPlan* plan);

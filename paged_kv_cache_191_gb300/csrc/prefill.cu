@@ -65,7 +65,7 @@ struct PrefillArgs {
   float* part_m;
   float* part_l;
   int32_t B, T, Hq, Hkv, G, max_blocks, num_blocks, max_context_len, max_q_len;
-  int32_t QT;  // row tiles per (sequence, kv head): ceil(max_q_len * G / 64)
+  int32_t QT;  // row tiles per (sequence, kv head): ceil(max_q_len * G / tile rows)
   int32_t bpp, max_parts;
   float scale_log2;
   int32_t out_f32;
@@ -487,13 +487,473 @@ __global__ void __launch_bounds__(32 * kReduceRows) prefill_reduce(const Prefill
   for (int v = 0; v < V; v += 2) store_pair<T>(a, head * D + lane * V + v, acc[v] * inv, acc[v + 1] * inv);
 }
 
+// ---- tensor-core (tcgen05) kernel for head_dim 128 ------------------------------------
+// Same work decomposition as prefill_main with 128-row tiles, two CTAs per SM:
+//   warp 0      TMA producer: 64-key chunks (4 blocks) of K and V into two
+//               32 KB stages laid out [d half][64 keys][128 B] (128-byte
+//               swizzle), so a chunk is one UMMA operand;
+//   warp 1      allocates 256 TMEM columns (S0 | S1 | O) and issues, from one
+//               thread, S(c) = Q . K(c)^T (M 128, N 64, K 128, both operands
+//               K-major in shared memory) into S buffer c % 2, and
+//               O += P(c) . V(c) (M 128, N 128, K 64) with P read from TMEM
+//               and V as an MN-major operand in shared memory;
+//   warps 2..5  the softmax warpgroup: thread r owns query row r = TMEM lane r;
+//               reads S(c), masks it (causal, partition end), keeps a
+//               reference max per row that moves only when the chunk max
+//               exceeds it by more than 2^8 (then O and l are rescaled in
+//               TMEM), and writes P = exp2(s - ref) back over S(c) as 16-bit
+//               pairs (bf16 as hi + lo halves of the buffer); at the end it
+//               reads O and writes the row.
+// S(c + 1) is issued before O += P(c) V(c) waits for P(c), so scores of the
+// next chunk are computed while the softmax works.  MMA completion is
+// signalled with tcgen05.commit on mbarriers; all waits are bounded; TMEM is
+// released on every path.
+namespace tcg {
+constexpr int kRows = 128;
+constexpr int kKeys = 64;
+#ifndef PA_TC_STAGES
+#define PA_TC_STAGES 2
+#endif
+constexpr int kStages = PA_TC_STAGES;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;
+constexpr float kRescale = 8.f;
+
+struct Smem {  // byte offsets from the 1024-aligned base
+  static constexpr int Q = 0;                                  // [2][128][128 B]
+  static constexpr int STAGE0 = 32768;                         // K [2][64][128 B] | V same
+  static constexpr int STAGE_BYTES = 32768;
+  static constexpr int BAR = STAGE0 + kStages * STAGE_BYTES;
+  static constexpr int NBAR = 2 * kStages + 8;
+  static constexpr int TSLOT = BAR + NBAR * 8;
+  static constexpr int SMEM = TSLOT + 16 + 1024;
+};
+
+// tcgen05 shared-memory descriptor: 128-byte swizzle, version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16, f32 accumulate, M = 128.
+template <typename T>
+__device__ __forceinline__ uint32_t idesc(int N, bool b_mn_major) {
+  const uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(kRows >> 4) << 24);
+}
+// D (TMEM) (+)= A (shared memory descriptor) . B (shared memory descriptor)
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+// D (TMEM) (+)= A (TMEM: lane = row, 16-bit pairs along K) . B (shared memory descriptor)
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 2^x with one MUFU operation (flushes denormal results to zero; the
+// arguments here are <= 8 and a flushed weight is below 2^-126).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+#ifndef PA_TC_SPIN
+#define PA_TC_SPIN 0
+#endif
+// Bounded wait polled with plain try_wait (no suspend-time hint): these
+// handoffs sit on the per-chunk critical path.
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  if (dev::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = dev::global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (dev::mbar_try_wait(bar, parity)) return true;
+    if (dev::global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+// A bounded wait whose outcome is the same in every lane (lane 0's), so the
+// warp-collective tcgen05 instructions that follow stay converged.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
+  const bool ok = PA_TC_SPIN ? wait_spin(bar, parity) : dev::mbar_wait_bounded(bar, parity);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+}  // namespace tcg
+
+template <typename T>
+__global__ void __launch_bounds__(tcg::kThreads, 2)
+    prefill_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const PrefillArgs a) {
+  using namespace tcg;
+  using L = Smem;
+  constexpr int D = 128;
+  constexpr bool SPLIT = std::is_same<T, __nv_bfloat16>::value;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = dev::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gb = smem_raw + (base - raw);
+
+  const int wid = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const int qt = static_cast<int>(blockIdx.x) % a.QT, bg = static_cast<int>(blockIdx.x) / a.QT;
+  const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int p = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+
+  dev::grid_dependency_wait();
+  const SeqView sv = seq_view(a, b, g == 0 && qt == 0 && p == 0 && threadIdx.x == 0);
+  const int nrows = sv.n * a.G;
+  const int R0 = qt * tcg::kRows;
+  if (R0 >= nrows) return;
+  const int shift = sv.L - sv.n;
+  const int j0 = p * a.bpp;
+  const int pos_cta = shift + (min(R0 + tcg::kRows, nrows) - 1) / a.G;
+  const int nb = min(a.bpp, (pos_cta + 16) / 16 - j0);
+  // this thread's row (softmax warps 2..5; TMEM lane 32 * (warp % 4) + lane)
+  const int r = 32 * (wid & 3) + lane;
+  const int rr = R0 + r;
+  const bool has = wid >= 2 && rr < nrows;
+  const int pos = has ? shift + rr / a.G : -1;
+  const size_t head = has ? static_cast<size_t>(sv.qs + rr / a.G) * a.Hq + g * a.G + rr % a.G : 0;
+  if (nb <= 0) {  // no key in this partition; partition 0 owns the zero rows of tokens without keys
+    if (p == 0 && has && pos < 0)
+      for (int d = 0; d < D; d += 2) store_pair<T>(a, head * D + d, 0.f, 0.f);
+    return;
+  }
+  const int nc = (nb + 3) / 4;                 // 64-key chunks
+  const int kend = min(sv.L, (j0 + nb) * 16);  // keys past this are masked (and their V rows zeroed)
+
+  const uint32_t bar = base + L::BAR;
+  auto full = [&](int s) { return bar + 8 * s; };
+  auto empty = [&](int s) { return bar + 8 * (kStages + s); };
+  const uint32_t qfull = bar + 8 * (2 * kStages);
+  auto sfull = [&](int i) { return bar + 8 * (2 * kStages + 1 + i); };  // S(c) in TMEM
+  auto pfull = [&](int i) { return bar + 8 * (2 * kStages + 3 + i); };  // P(c) in TMEM (over S(c))
+  auto pfree = [&](int i) { return bar + 8 * (2 * kStages + 5 + i); };  // O += P(c) V(c) complete
+  const uint32_t mdone = bar + 8 * (2 * kStages + 7);
+  auto stage = [&](int s) { return base + L::STAGE0 + s * L::STAGE_BYTES; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      dev::mbar_init(full(s), 1);
+      dev::mbar_init(empty(s), 1);
+    }
+    dev::mbar_init(qfull, 4);
+    for (int i = 0; i < 2; ++i) {
+      dev::mbar_init(sfull(i), 1);
+      dev::mbar_init(pfull(i), 4);
+      dev::mbar_init(pfree(i), 1);
+    }
+    dev::mbar_init(mdone, 1);
+    dev::fence_barrier_init();
+  }
+  if (wid == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + L::TSLOT),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + L::TSLOT);
+
+  if (wid == 0) {
+    // ---- producer ---------------------------------------------------------------------
+    const int32_t* row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + j0;
+    int issued = 0;
+    bool ok = true;
+    if (lane == 0) {
+      dev::prefetch_tensormap(&tmK);
+      dev::prefetch_tensormap(&tmV);
+    }
+    for (int c = 0; c < nc && ok; ++c) {
+      const int s = c % kStages;
+      int id = 0;
+      if (lane < 4) {  // padding blocks past the partition repeat its last block (masked)
+        id = row[min(4 * c + lane, nb - 1)];
+        if (id < 0 || id >= a.num_blocks) {
+          atomicOr(&g_prefill_err, PA_DEVERR_BLOCK_RANGE);
+          id = 0;
+        }
+      }
+      int pb[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pb[k] = __shfl_sync(FULL, id, k);
+      if (lane == 0) {
+        if (c >= kStages && !dev::mbar_wait_bounded(empty(s), ((c / kStages) - 1) & 1)) {
+          atomicOr(&g_prefill_err, PA_DEVERR_TIMEOUT);
+          ok = false;
+        } else {
+          dev::mbar_arrive_expect_tx(full(s), L::STAGE_BYTES);
+          const uint32_t kd = stage(s), vd = kd + 16384;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              dev::tma_load_3d(kd + h * 8192 + k * 2048, &tmK, full(s), h * 64, g * 16, pb[k]);
+              dev::tma_load_3d(vd + h * 8192 + k * 2048, &tmV, full(s), h * 64, g * 16, pb[k]);
+            }
+          issued = c + 1;
+        }
+      }
+      ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0)  // no copy may still be landing when the CTA exits
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        dev::mbar_wait_bounded(full(i % kStages), (i / kStages) & 1, 100000000ull);
+  } else if (wid == 1) {
+    // ---- MMA issuer -----------------------------------------------------------------------
+    const uint32_t id_s = idesc<T>(kKeys, false), id_o = idesc<T>(D, true);
+    bool ok = wait_warp(qfull, 0);
+    auto qk = [&](int c) {  // S(c) into buffer c % 2, free once O += P(c - 2) V(c - 2) is done
+      const int s = c % kStages;
+      if (!wait_warp(full(s), (c / kStages) & 1)) return false;
+      if (c >= 2 && !wait_warp(pfree(c & 1), ((c >> 1) - 1) & 1)) return false;
+      fence_after();
+      if (lane == 0) {
+        const uint32_t kd = stage(s);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 64 * (c & 1), sdesc(base + L::Q + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 sdesc(kd + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+        commit(sfull(c & 1));
+      }
+      __syncwarp();
+      return true;
+    };
+    auto pv = [&](int c) {
+      const int s = c % kStages;
+      if (!wait_warp(pfull(c & 1), (c >> 1) & 1)) return false;
+      fence_after();
+      const int key0 = (j0 + 4 * c) * 16;
+      const int first_bad = max(0, min(kKeys, kend - key0));  // V rows from here on are zeroed
+      if (first_bad < kKeys) {
+        uint8_t* v = gb + (stage(s) - base) + 16384;
+        for (int i = first_bad * 16 + lane; i < kKeys * 16; i += 32) {  // (row, 16-B chunk) pairs
+          const int kr = i >> 4, ch = i & 15;
+          *reinterpret_cast<uint4*>(v + (ch >> 3) * 8192 + kr * 128 + ((ch & 7) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+        dev::fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        const uint32_t pt = tmem + 64 * (c & 1), vd = stage(s) + 16384;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bv = sdesc(vd + kk * 2048, 8192, 1024);
+          mma_ts(tmem + 128, pt + 8 * kk, bv, id_o, (c > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (SPLIT) mma_ts(tmem + 128, pt + 32 + 8 * kk, bv, id_o, 1u);
+        }
+        commit(pfree(c & 1));
+        commit(empty(s));
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok) ok = qk(0);
+    for (int c = 0; c < nc && ok; ++c) {
+      if (c + 1 < nc && !qk(c + 1)) {
+        ok = false;
+        break;
+      }
+      if (!pv(c)) ok = false;
+    }
+    if (!ok && lane == 0) atomicOr(&g_prefill_err, PA_DEVERR_TIMEOUT);
+    // every MMA issued has completed before TMEM is released
+    if (lane == 0) commit(mdone);
+    __syncwarp();
+    dev::mbar_wait_bounded(mdone, 0, 100000000ull);
+  } else {
+    // ---- softmax warpgroup ------------------------------------------------------------------
+    {  // Q row -> shared memory (zeros for padding rows), K-major, 128-byte swizzle
+      const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + head * D);
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const uint4 v = has ? qrow[ch] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(gb + L::Q + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
+      }
+      dev::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qfull);
+    }
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * (wid & 3)) << 16);
+    const float sl2 = a.scale_log2;
+    float ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int c = 0; c < nc; ++c) {
+      if (!wait_warp(sfull(c & 1), (c >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      fence_after();
+      const uint32_t sb = trow + 64 * (c & 1);
+      float x[kKeys];
+      {
+        uint32_t u[32], v[32];
+        ld32(sb, u);
+        ld32(sb + 32, v);
+        wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          x[j] = __uint_as_float(u[j]);
+          x[32 + j] = __uint_as_float(v[j]);
+        }
+      }
+      // raw scores; the scale (> 0) is applied to the max and folded into
+      // the exponent's FFMA below
+      const int key0 = (j0 + 4 * c) * 16;
+      float cm[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) cm[k] = -INFINITY;
+      if (key0 + kKeys - 1 <= pos && key0 + kKeys <= kend) {  // every key of the chunk is visible
+#pragma unroll
+        for (int j = 0; j < kKeys; ++j) cm[j & 7] = fmaxf(cm[j & 7], x[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kKeys; ++j) {
+          const int t = key0 + j;
+          x[j] = (t <= pos && t < kend) ? x[j] : -INFINITY;
+          cm[j & 7] = fmaxf(cm[j & 7], x[j]);
+        }
+      }
+      const float cmax = fmaxf(fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3])),
+                               fmaxf(fmaxf(cm[4], cm[5]), fmaxf(cm[6], cm[7]))) * sl2;
+      // move the reference when the chunk max outgrows it; O and l follow
+      const bool move = cmax > ref + kRescale;
+      if (__any_sync(FULL, move && ref != -INFINITY)) {
+        if (!wait_warp(pfree((c - 1) & 1), ((c - 1) >> 1) & 1)) {  // O += P(c-1) V(c-1) done
+          ok = false;
+          break;
+        }
+        fence_after();
+        const float alpha = (move && ref != -INFINITY) ? ex2(ref - cmax) : 1.f;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          uint32_t u[32];
+          ld32(trow + 128 + 32 * q, u);
+          wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
+          st32(trow + 128 + 32 * q, u);
+        }
+        wait_st();
+        l *= alpha;
+      }
+      if (move) ref = cmax;
+      // P over S(c): 16-bit pairs, bf16 as hi (columns 0..31) and lo (32..63)
+      uint32_t hi[32], lo[32];
+      float ls[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+      // p = 2^(s * scale * log2 e - ref); a row without keys so far keeps
+      // ref = -inf and gets p = 0 (its masked scores are -inf too)
+      const float nref = ref == -INFINITY ? 0.f : -ref;
+#pragma unroll
+      for (int j = 0; j < kKeys; j += 2) {
+        const float p0 = ex2(fmaf(x[j], sl2, nref));
+        const float p1 = ex2(fmaf(x[j + 1], sl2, nref));
+        hi[j >> 1] = dev::pack2<T>(p0, p1);
+        const float2 h = dev::unpack2<T>(hi[j >> 1]);
+        if constexpr (SPLIT) {
+          lo[j >> 1] = dev::pack2<T>(p0 - h.x, p1 - h.y);
+          ls[(j >> 1) & 7] += p0 + p1;
+        } else {
+          ls[(j >> 1) & 7] += h.x + h.y;  // normalise with the rounded weights the product uses
+        }
+      }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      st32(sb, hi);
+      if constexpr (SPLIT) st32(sb + 32, lo);
+      wait_st();
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull(c & 1));
+    }
+    dev::grid_launch_dependents();
+    if (!ok && lane == 0) atomicOr(&g_prefill_err, PA_DEVERR_TIMEOUT);
+    // ---- epilogue: O row -> output, partial, zero row or nothing ----
+    if (ok && wait_warp(pfree((nc - 1) & 1), ((nc - 1) >> 1) & 1)) {
+      fence_after();
+      const int np = pos < 0 ? 0 : ((pos + 16) / 16 + a.bpp - 1) / a.bpp;
+      const bool direct = has && pos >= 0 && np == 1 && p == 0;  // later partitions hold it without keys
+      const bool partial = has && pos >= 0 && np > 1 && p < np;
+      const bool zero = has && pos < 0 && p == 0;
+      const float inv = direct ? 1.f / l : 1.f;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t u[32];
+        ld32(trow + 128 + 32 * q, u);
+        wait_ld();
+        if (direct || zero) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2)
+            store_pair<T>(a, head * D + 32 * q + j, zero ? 0.f : __uint_as_float(u[j]) * inv,
+                          zero ? 0.f : __uint_as_float(u[j + 1]) * inv);
+        } else if (partial) {
+          float* po = a.part_o + (head * a.max_parts + p) * D + 32 * q;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(po + j) = make_float4(__uint_as_float(u[j]), __uint_as_float(u[j + 1]),
+                                                             __uint_as_float(u[j + 2]), __uint_as_float(u[j + 3]));
+        }
+      }
+      if (partial) {
+        a.part_m[head * a.max_parts + p] = ref;
+        a.part_l[head * a.max_parts + p] = l;
+      }
+    } else if (lane == 0) {
+      atomicOr(&g_prefill_err, PA_DEVERR_TIMEOUT);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (wid == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
 template <typename T, int D>
 pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t stream) {
   using TL = PTile<D>;
+  // tcgen05 kernel (128-row tiles) or mma.sync kernel (64-row tiles), as planned
+  const bool TC = D == 128 && l.plan.tc;
   CUtensorMap tmK, tmV;
-  pa_status st = make_kv_map(&tmK, l.k_cache, l.Hkv, l.num_blocks, TL::ROWB, 2, dt, "pa_chunked_prefill");
+  pa_status st = make_kv_map(&tmK, l.k_cache, l.Hkv, l.num_blocks, TL::ROWB, 2, dt, "pa_chunked_prefill", !TC);
   if (st != PA_OK) return st;
-  st = make_kv_map(&tmV, l.v_cache, l.Hkv, l.num_blocks, TL::ROWB, 2, dt, "pa_chunked_prefill");
+  st = make_kv_map(&tmV, l.v_cache, l.Hkv, l.num_blocks, TL::ROWB, 2, dt, "pa_chunked_prefill", !TC);
   if (st != PA_OK) return st;
 
   PrefillArgs a;
@@ -526,15 +986,22 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
   if (dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: device index %d", dev);
   static std::once_flag once[kMaxDevices];
   static cudaError_t setup_err[kMaxDevices];
+  using TS = tcg::Smem;
   std::call_once(once[dev], [dev] {
-    setup_err[dev] =
-        cudaFuncSetAttribute(prefill_main<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TL::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(prefill_main<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TL::SMEM);
+    if (e == cudaSuccess && D == 128)
+      e = cudaFuncSetAttribute(prefill_tc<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, TS::SMEM);
+    setup_err[dev] = e;
   });
   if (setup_err[dev] != cudaSuccess)
     return fail(PA_ERR_CUDA, "pa_chunked_prefill: %s", cudaGetErrorString(setup_err[dev]));
 
   const dim3 grid(static_cast<unsigned>(l.B * l.Hkv * l.plan.row_tiles), static_cast<unsigned>(l.plan.max_parts));
-  cudaError_t e = launch_dependent(prefill_main<T, D>, grid, dim3(kThreads), TL::SMEM, stream, tmK, tmV, a);
+  cudaError_t e;
+  if (TC)
+    e = launch_dependent(prefill_tc<T>, grid, dim3(tcg::kThreads), TS::SMEM, stream, tmK, tmV, a);
+  else
+    e = launch_dependent(prefill_main<T, D>, grid, dim3(kThreads), TL::SMEM, stream, tmK, tmV, a);
   if (e == cudaSuccess && l.plan.max_parts > 1)
     e = launch_dependent(prefill_reduce<T, D>,
                          dim3(static_cast<unsigned>((static_cast<int64_t>(l.T) * l.Hq + kReduceRows - 1) / kReduceRows)),
