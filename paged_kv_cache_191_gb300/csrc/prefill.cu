@@ -521,10 +521,12 @@ constexpr float kRescale = 8.f;
 
 struct Smem {  // byte offsets from the 1024-aligned base
   static constexpr int Q = 0;                                  // [2][128][128 B]
-  static constexpr int STAGE0 = 32768;                         // K [2][64][128 B] | V same
-  static constexpr int STAGE_BYTES = 32768;
-  static constexpr int BAR = STAGE0 + kStages * STAGE_BYTES;
-  static constexpr int NBAR = 2 * kStages + 8;
+  static constexpr int K0 = 32768;                             // K ring: [stage][2][64][128 B]
+  static constexpr int V0 = K0 + kStages * 16384;              // V ring, same layout
+  static constexpr int HALF = 16384;                           // one K or V chunk
+  static constexpr int IDS = V0 + kStages * 16384;             // block ids of the last 8 chunks [8][4]
+  static constexpr int BAR = IDS + 8 * 4 * 4;
+  static constexpr int NBAR = 4 * kStages + 8;
   static constexpr int TSLOT = BAR + NBAR * 8;
   static constexpr int SMEM = TSLOT + 16 + 1024;
 };
@@ -654,20 +656,27 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
   const int nc = (nb + 3) / 4;                 // 64-key chunks
   const int kend = min(sv.L, (j0 + nb) * 16);  // keys past this are masked (and their V rows zeroed)
 
+  // K(c) is released when S(c) completes, V(c) when O += P(c) V(c) does, so
+  // the producer runs up to two chunks ahead on K independently of V
   const uint32_t bar = base + L::BAR;
-  auto full = [&](int s) { return bar + 8 * s; };
-  auto empty = [&](int s) { return bar + 8 * (kStages + s); };
-  const uint32_t qfull = bar + 8 * (2 * kStages);
-  auto sfull = [&](int i) { return bar + 8 * (2 * kStages + 1 + i); };  // S(c) in TMEM
-  auto pfull = [&](int i) { return bar + 8 * (2 * kStages + 3 + i); };  // P(c) in TMEM (over S(c))
-  auto pfree = [&](int i) { return bar + 8 * (2 * kStages + 5 + i); };  // O += P(c) V(c) complete
-  const uint32_t mdone = bar + 8 * (2 * kStages + 7);
-  auto stage = [&](int s) { return base + L::STAGE0 + s * L::STAGE_BYTES; };
+  auto kfull = [&](int s) { return bar + 8 * s; };
+  auto kempty = [&](int s) { return bar + 8 * (kStages + s); };
+  auto vfull = [&](int s) { return bar + 8 * (2 * kStages + s); };
+  auto vempty = [&](int s) { return bar + 8 * (3 * kStages + s); };
+  const uint32_t qfull = bar + 8 * (4 * kStages);
+  auto sfull = [&](int i) { return bar + 8 * (4 * kStages + 1 + i); };  // S(c) in TMEM
+  auto pfull = [&](int i) { return bar + 8 * (4 * kStages + 3 + i); };  // P(c) in TMEM (over S(c))
+  auto pfree = [&](int i) { return bar + 8 * (4 * kStages + 5 + i); };  // O += P(c) V(c) complete
+  const uint32_t mdone = bar + 8 * (4 * kStages + 7);
+  auto kstage = [&](int s) { return base + L::K0 + s * L::HALF; };
+  auto vstage = [&](int s) { return base + L::V0 + s * L::HALF; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      dev::mbar_init(full(s), 1);
-      dev::mbar_init(empty(s), 1);
+      dev::mbar_init(kfull(s), 1);
+      dev::mbar_init(kempty(s), 1);
+      dev::mbar_init(vfull(s), 1);
+      dev::mbar_init(vempty(s), 1);
     }
     dev::mbar_init(qfull, 4);
     for (int i = 0; i < 2; ++i) {
@@ -690,65 +699,75 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + L::TSLOT);
 
   if (wid == 0) {
-    // ---- producer ---------------------------------------------------------------------
-    const int32_t* row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + j0;
-    int issued = 0;
-    bool ok = true;
+    // ---- producer: lane 0 polls both rings and issues whichever is free ---------------
     if (lane == 0) {
+      const int32_t* row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + j0;
+      int32_t* ids = reinterpret_cast<int32_t*>(gb + L::IDS);
       dev::prefetch_tensormap(&tmK);
       dev::prefetch_tensormap(&tmV);
-    }
-    for (int c = 0; c < nc && ok; ++c) {
-      const int s = c % kStages;
-      int id = 0;
-      if (lane < 4) {  // padding blocks past the partition repeat its last block (masked)
-        id = row[min(4 * c + lane, nb - 1)];
-        if (id < 0 || id >= a.num_blocks) {
-          atomicOr(&g_prefill_err, PA_DEVERR_BLOCK_RANGE);
-          id = 0;
-        }
-      }
-      int pb[4];
+      int ck = 0, cv = 0;
+      bool ok = true;
+      uint64_t t0 = dev::global_timer_ns();
+      auto load = [&](const CUtensorMap* m, uint32_t dst, uint32_t bar_full, const int32_t* pb) {
+        dev::mbar_arrive_expect_tx(bar_full, L::HALF);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) pb[k] = __shfl_sync(FULL, id, k);
-      if (lane == 0) {
-        if (c >= kStages && !dev::mbar_wait_bounded(empty(s), ((c / kStages) - 1) & 1)) {
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) dev::tma_load_3d(dst + h * 8192 + k * 2048, m, bar_full, h * 64, g * 16, pb[k]);
+      };
+      while (ok && cv < nc) {
+        bool progressed = false;
+        if (ck < nc && (ck < kStages || dev::mbar_try_wait(kempty(ck % kStages), ((ck / kStages) - 1) & 1))) {
+          int32_t* id = ids + 4 * (ck & 7);  // padding blocks past the partition repeat its last block (masked)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            int v = row[min(4 * ck + k, nb - 1)];
+            if (v < 0 || v >= a.num_blocks) {
+              atomicOr(&g_prefill_err, PA_DEVERR_BLOCK_RANGE);
+              v = 0;
+            }
+            id[k] = v;
+          }
+          load(&tmK, kstage(ck % kStages), kfull(ck % kStages), id);
+          ++ck;
+          progressed = true;
+        }
+        if (cv < ck && (cv < kStages || dev::mbar_try_wait(vempty(cv % kStages), ((cv / kStages) - 1) & 1))) {
+          load(&tmV, vstage(cv % kStages), vfull(cv % kStages), ids + 4 * (cv & 7));
+          ++cv;
+          progressed = true;
+        }
+        if (progressed) {
+          t0 = dev::global_timer_ns();
+        } else if (dev::global_timer_ns() - t0 > 2000000000ull) {
           atomicOr(&g_prefill_err, PA_DEVERR_TIMEOUT);
           ok = false;
-        } else {
-          dev::mbar_arrive_expect_tx(full(s), L::STAGE_BYTES);
-          const uint32_t kd = stage(s), vd = kd + 16384;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              dev::tma_load_3d(kd + h * 8192 + k * 2048, &tmK, full(s), h * 64, g * 16, pb[k]);
-              dev::tma_load_3d(vd + h * 8192 + k * 2048, &tmV, full(s), h * 64, g * 16, pb[k]);
-            }
-          issued = c + 1;
         }
       }
-      ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+      // no copy may still be landing when the CTA exits
+      for (int i = max(0, ck - kStages); i < ck; ++i)
+        dev::mbar_wait_bounded(kfull(i % kStages), (i / kStages) & 1, 100000000ull);
+      for (int i = max(0, cv - kStages); i < cv; ++i)
+        dev::mbar_wait_bounded(vfull(i % kStages), (i / kStages) & 1, 100000000ull);
     }
-    if (lane == 0)  // no copy may still be landing when the CTA exits
-      for (int i = max(0, issued - kStages); i < issued; ++i)
-        dev::mbar_wait_bounded(full(i % kStages), (i / kStages) & 1, 100000000ull);
+    __syncwarp();
   } else if (wid == 1) {
     // ---- MMA issuer -----------------------------------------------------------------------
     const uint32_t id_s = idesc<T>(kKeys, false), id_o = idesc<T>(D, true);
     bool ok = wait_warp(qfull, 0);
     auto qk = [&](int c) {  // S(c) into buffer c % 2, free once O += P(c - 2) V(c - 2) is done
       const int s = c % kStages;
-      if (!wait_warp(full(s), (c / kStages) & 1)) return false;
+      if (!wait_warp(kfull(s), (c / kStages) & 1)) return false;
       if (c >= 2 && !wait_warp(pfree(c & 1), ((c >> 1) - 1) & 1)) return false;
       fence_after();
       if (lane == 0) {
-        const uint32_t kd = stage(s);
+        const uint32_t kd = kstage(s);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + 64 * (c & 1), sdesc(base + L::Q + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                  sdesc(kd + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         commit(sfull(c & 1));
+        commit(kempty(s));
       }
       __syncwarp();
       return true;
@@ -756,11 +775,12 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
     auto pv = [&](int c) {
       const int s = c % kStages;
       if (!wait_warp(pfull(c & 1), (c >> 1) & 1)) return false;
+      if (!wait_warp(vfull(s), (c / kStages) & 1)) return false;
       fence_after();
       const int key0 = (j0 + 4 * c) * 16;
       const int first_bad = max(0, min(kKeys, kend - key0));  // V rows from here on are zeroed
       if (first_bad < kKeys) {
-        uint8_t* v = gb + (stage(s) - base) + 16384;
+        uint8_t* v = gb + (vstage(s) - base);
         for (int i = first_bad * 16 + lane; i < kKeys * 16; i += 32) {  // (row, 16-B chunk) pairs
           const int kr = i >> 4, ch = i & 15;
           *reinterpret_cast<uint4*>(v + (ch >> 3) * 8192 + kr * 128 + ((ch & 7) << 4)) = make_uint4(0, 0, 0, 0);
@@ -769,7 +789,7 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
         __syncwarp();
       }
       if (lane == 0) {
-        const uint32_t pt = tmem + 64 * (c & 1), vd = stage(s) + 16384;
+        const uint32_t pt = tmem + 64 * (c & 1), vd = vstage(s);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t bv = sdesc(vd + kk * 2048, 8192, 1024);
@@ -777,7 +797,7 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
           if constexpr (SPLIT) mma_ts(tmem + 128, pt + 32 + 8 * kk, bv, id_o, 1u);
         }
         commit(pfree(c & 1));
-        commit(empty(s));
+        commit(vempty(s));
       }
       __syncwarp();
       return true;
