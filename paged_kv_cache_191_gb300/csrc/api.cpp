@@ -114,6 +114,9 @@ pa_status plan_prefill(int32_t T, int32_t B, int32_t Hq, int32_t max_q_len, int3
       while (bpp > 8 && units * ((nblk_max + bpp - 1) / bpp) < 2 * per_sm * sms) bpp /= 2;
     }
   }
+  // the tcgen05 kernel stages a partition's block ids in shared memory: at
+  // most 1024 blocks (16K tokens) per partition
+  if (tile_rows == 128 && bpp > 1024) bpp = 1024;
   const int64_t parts = (nblk_max + bpp - 1) / bpp;
   if (parts > 65535) return fail(PA_ERR_UNSUPPORTED, "context too long for the partition grid");
   if (static_cast<int64_t>(B) * d->num_kv_heads * tiles > INT32_MAX)

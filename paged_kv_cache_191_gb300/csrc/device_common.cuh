@@ -41,6 +41,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// Non-blocking test of phase `parity` (mbarrier.test_wait never suspends the
+// thread, unlike try_wait): for loops that poll several barriers.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 // As mbar_try_wait, but the thread may sleep up to `hint_ns` waiting for the
 // phase (it wakes when the phase completes), so a waiting warp does not spin
 // on the issue slots that computing warps need.

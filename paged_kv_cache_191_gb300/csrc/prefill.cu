@@ -518,14 +518,15 @@ constexpr int kStages = PA_TC_STAGES;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 256;
 constexpr float kRescale = 8.f;
+constexpr int kMaxIds = 1024;  // blocks of one partition (the plan keeps partitions within this)
 
 struct Smem {  // byte offsets from the 1024-aligned base
   static constexpr int Q = 0;                                  // [2][128][128 B]
   static constexpr int K0 = 32768;                             // K ring: [stage][2][64][128 B]
   static constexpr int V0 = K0 + kStages * 16384;              // V ring, same layout
   static constexpr int HALF = 16384;                           // one K or V chunk
-  static constexpr int IDS = V0 + kStages * 16384;             // block ids of the last 8 chunks [8][4]
-  static constexpr int BAR = IDS + 8 * 4 * 4;
+  static constexpr int IDS = V0 + kStages * 16384;             // the partition's block ids [kMaxIds]
+  static constexpr int BAR = IDS + kMaxIds * 4;
   static constexpr int NBAR = 4 * kStages + 8;
   static constexpr int TSLOT = BAR + NBAR * 8;
   static constexpr int SMEM = TSLOT + 16 + 1024;
@@ -653,8 +654,8 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
       for (int d = 0; d < D; d += 2) store_pair<T>(a, head * D + d, 0.f, 0.f);
     return;
   }
-  const int nc = (nb + 3) / 4;                 // 64-key chunks
-  const int kend = min(sv.L, (j0 + nb) * 16);  // keys past this are masked (and their V rows zeroed)
+  const int nc = (min(nb, kMaxIds) + 3) / 4;                 // 64-key chunks
+  const int kend = min(sv.L, (j0 + min(nb, kMaxIds)) * 16);  // keys past this are masked (V rows zeroed)
 
   // K(c) is released when S(c) completes, V(c) when O += P(c) V(c) does, so
   // the producer runs up to two chunks ahead on K independently of V
@@ -699,41 +700,51 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + L::TSLOT);
 
   if (wid == 0) {
-    // ---- producer: lane 0 polls both rings and issues whichever is free ---------------
-    if (lane == 0) {
+    // ---- producer: the warp stages the partition's block ids in shared memory
+    // (coalesced, checked), then lane 0 polls both rings and issues whichever
+    // is free ----------------------------------------------------------------------
+    int32_t* ids = reinterpret_cast<int32_t*>(gb + L::IDS);
+    {
       const int32_t* row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + j0;
-      int32_t* ids = reinterpret_cast<int32_t*>(gb + L::IDS);
+      const int n_ids = min(nb, kMaxIds);
+      bool bad = nb > kMaxIds;
+      for (int i = lane; i < n_ids; i += 32) {
+        int v = row[i];
+        if (v < 0 || v >= a.num_blocks) {
+          bad = true;
+          v = 0;  // read block 0 instead; flagged
+        }
+        ids[i] = v;
+      }
+      if (__any_sync(FULL, bad) && lane == 0) atomicOr(&g_prefill_err, PA_DEVERR_BLOCK_RANGE);
+      __syncwarp();
+    }
+    if (lane == 0) {
       dev::prefetch_tensormap(&tmK);
       dev::prefetch_tensormap(&tmV);
+      const int last = min(nb, kMaxIds) - 1;
       int ck = 0, cv = 0;
       bool ok = true;
       uint64_t t0 = dev::global_timer_ns();
-      auto load = [&](const CUtensorMap* m, uint32_t dst, uint32_t bar_full, const int32_t* pb) {
+      // chunk c's blocks 4c .. 4c + 3; padding past the partition repeats its last block (masked)
+      auto load = [&](const CUtensorMap* m, uint32_t dst, uint32_t bar_full, int c) {
         dev::mbar_arrive_expect_tx(bar_full, L::HALF);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 4; ++k) {
+          const int pb = ids[min(4 * c + k, last)];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) dev::tma_load_3d(dst + h * 8192 + k * 2048, m, bar_full, h * 64, g * 16, pb[k]);
+          for (int h = 0; h < 2; ++h) dev::tma_load_3d(dst + h * 8192 + k * 2048, m, bar_full, h * 64, g * 16, pb);
+        }
       };
       while (ok && cv < nc) {
         bool progressed = false;
-        if (ck < nc && (ck < kStages || dev::mbar_try_wait(kempty(ck % kStages), ((ck / kStages) - 1) & 1))) {
-          int32_t* id = ids + 4 * (ck & 7);  // padding blocks past the partition repeat its last block (masked)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            int v = row[min(4 * ck + k, nb - 1)];
-            if (v < 0 || v >= a.num_blocks) {
-              atomicOr(&g_prefill_err, PA_DEVERR_BLOCK_RANGE);
-              v = 0;
-            }
-            id[k] = v;
-          }
-          load(&tmK, kstage(ck % kStages), kfull(ck % kStages), id);
+        if (ck < nc && (ck < kStages || dev::mbar_test(kempty(ck % kStages), ((ck / kStages) - 1) & 1))) {
+          load(&tmK, kstage(ck % kStages), kfull(ck % kStages), ck);
           ++ck;
           progressed = true;
         }
-        if (cv < ck && (cv < kStages || dev::mbar_try_wait(vempty(cv % kStages), ((cv / kStages) - 1) & 1))) {
-          load(&tmV, vstage(cv % kStages), vfull(cv % kStages), ids + 4 * (cv & 7));
+        if (cv < ck && (cv < kStages || dev::mbar_test(vempty(cv % kStages), ((cv / kStages) - 1) & 1))) {
+          load(&tmV, vstage(cv % kStages), vfull(cv % kStages), cv);
           ++cv;
           progressed = true;
         }
@@ -755,60 +766,71 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
     // ---- MMA issuer -----------------------------------------------------------------------
     const uint32_t id_s = idesc<T>(kKeys, false), id_o = idesc<T>(D, true);
     bool ok = wait_warp(qfull, 0);
-    auto qk = [&](int c) {  // S(c) into buffer c % 2, free once O += P(c - 2) V(c - 2) is done
-      const int s = c % kStages;
-      if (!wait_warp(kfull(s), (c / kStages) & 1)) return false;
-      if (c >= 2 && !wait_warp(pfree(c & 1), ((c >> 1) - 1) & 1)) return false;
-      fence_after();
-      if (lane == 0) {
-        const uint32_t kd = kstage(s);
+    // The warp polls (lane 0 tests, the warp follows) and issues whichever is
+    // ready: S(cs) = Q . K(cs)^T once K(cs) has landed and S buffer cs % 2 is
+    // free (O += P(cs - 2) V(cs - 2) done), or O += P(cp) V(cp) once the
+    // softmax has written P(cp) and V(cp) has landed.
+    int cs = 0, cp = 0;
+    uint64_t t0 = dev::global_timer_ns();
+    while (ok && cp < nc) {
+      bool progressed = false;
+      int go = 0;
+      if (lane == 0 && cs < nc && cs <= cp + 1 && dev::mbar_test(kfull(cs % kStages), (cs / kStages) & 1) &&
+          (cs < 2 || dev::mbar_test(pfree(cs & 1), ((cs >> 1) - 1) & 1)))
+        go = 1;
+      if (__shfl_sync(FULL, go, 0)) {
+        fence_after();
+        if (lane == 0) {
+          const uint32_t kd = kstage(cs % kStages);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 64 * (c & 1), sdesc(base + L::Q + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sdesc(kd + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-        commit(sfull(c & 1));
-        commit(kempty(s));
-      }
-      __syncwarp();
-      return true;
-    };
-    auto pv = [&](int c) {
-      const int s = c % kStages;
-      if (!wait_warp(pfull(c & 1), (c >> 1) & 1)) return false;
-      if (!wait_warp(vfull(s), (c / kStages) & 1)) return false;
-      fence_after();
-      const int key0 = (j0 + 4 * c) * 16;
-      const int first_bad = max(0, min(kKeys, kend - key0));  // V rows from here on are zeroed
-      if (first_bad < kKeys) {
-        uint8_t* v = gb + (vstage(s) - base);
-        for (int i = first_bad * 16 + lane; i < kKeys * 16; i += 32) {  // (row, 16-B chunk) pairs
-          const int kr = i >> 4, ch = i & 15;
-          *reinterpret_cast<uint4*>(v + (ch >> 3) * 8192 + kr * 128 + ((ch & 7) << 4)) = make_uint4(0, 0, 0, 0);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + 64 * (cs & 1), sdesc(base + L::Q + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                   sdesc(kd + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          commit(sfull(cs & 1));
+          commit(kempty(cs % kStages));
         }
-        dev::fence_proxy_async_smem();
         __syncwarp();
+        ++cs;
+        progressed = true;
       }
-      if (lane == 0) {
-        const uint32_t pt = tmem + 64 * (c & 1), vd = vstage(s);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bv = sdesc(vd + kk * 2048, 8192, 1024);
-          mma_ts(tmem + 128, pt + 8 * kk, bv, id_o, (c > 0 || kk > 0) ? 1u : 0u);
-          if constexpr (SPLIT) mma_ts(tmem + 128, pt + 32 + 8 * kk, bv, id_o, 1u);
+      go = 0;
+      if (lane == 0 && cp < cs && dev::mbar_test(pfull(cp & 1), (cp >> 1) & 1) &&
+          dev::mbar_test(vfull(cp % kStages), (cp / kStages) & 1))
+        go = 1;
+      if (__shfl_sync(FULL, go, 0)) {
+        fence_after();
+        const int sv_ = cp % kStages;
+        const int key0 = (j0 + 4 * cp) * 16;
+        const int first_bad = max(0, min(kKeys, kend - key0));  // V rows from here on are zeroed
+        if (first_bad < kKeys) {
+          uint8_t* v = gb + (vstage(sv_) - base);
+          for (int i = first_bad * 16 + lane; i < kKeys * 16; i += 32) {  // (row, 16-B chunk) pairs
+            const int kr = i >> 4, ch = i & 15;
+            *reinterpret_cast<uint4*>(v + (ch >> 3) * 8192 + kr * 128 + ((ch & 7) << 4)) = make_uint4(0, 0, 0, 0);
+          }
+          dev::fence_proxy_async_smem();
+          __syncwarp();
         }
-        commit(pfree(c & 1));
-        commit(vempty(s));
+        if (lane == 0) {
+          const uint32_t pt = tmem + 64 * (cp & 1), vd = vstage(sv_);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bv = sdesc(vd + kk * 2048, 8192, 1024);
+            mma_ts(tmem + 128, pt + 8 * kk, bv, id_o, (cp > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (SPLIT) mma_ts(tmem + 128, pt + 32 + 8 * kk, bv, id_o, 1u);
+          }
+          commit(pfree(cp & 1));
+          commit(vempty(sv_));
+        }
+        __syncwarp();
+        ++cp;
+        progressed = true;
       }
-      __syncwarp();
-      return true;
-    };
-    if (ok) ok = qk(0);
-    for (int c = 0; c < nc && ok; ++c) {
-      if (c + 1 < nc && !qk(c + 1)) {
+      if (progressed) {
+        t0 = dev::global_timer_ns();
+      } else if (dev::global_timer_ns() - t0 > 2000000000ull) {
         ok = false;
-        break;
       }
-      if (!pv(c)) ok = false;
     }
     if (!ok && lane == 0) atomicOr(&g_prefill_err, PA_DEVERR_TIMEOUT);
     // every MMA issued has completed before TMEM is released
