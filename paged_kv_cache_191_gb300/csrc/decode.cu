@@ -344,14 +344,20 @@ __global__ void __launch_bounds__(32 * W)
       const uint4 y0 = dev::lds128(kb + swz(r + 8, 2 * q4));
       const uint4 y1 = dev::lds128(kb + swz(r + 8, 2 * q4 + 1));
       const int tt = 2 * q4;
-      const uint4 X = dev::lds128(vb + swz(tt, r));
-      const uint4 Y = dev::lds128(vb + swz(tt + 1, r));
-      const uint4 Z = dev::lds128(vb + swz(tt + 8, r));
-      const uint4 Wq = dev::lds128(vb + swz(tt + 9, r));
+      uint4 X = dev::lds128(vb + swz(tt, r));
+      uint4 Y = dev::lds128(vb + swz(tt + 1, r));
+      uint4 Z = dev::lds128(vb + swz(tt + 8, r));
+      uint4 Wq = dev::lds128(vb + swz(tt + 9, r));
       c_r *= s_scale[s * 32 + r];
       c_r8 *= s_scale[s * 32 + r + 8];
-      vs_r = s_scale[s * 32 + 16 + r];
-      vs_r8 = s_scale[s * 32 + 16 + r + 8];
+      vs_r = r < nvalid ? s_scale[s * 32 + 16 + r] : 0.f;  // a stale scale past the context may be NaN
+      vs_r8 = r + 8 < nvalid ? s_scale[s * 32 + 16 + r + 8] : 0.f;
+      if (nvalid < 16) {  // rows past the context: weight 0, and their stale bytes must not be NaN codes
+        if (tt >= nvalid) X = make_uint4(0, 0, 0, 0);
+        if (tt + 1 >= nvalid) Y = make_uint4(0, 0, 0, 0);
+        if (tt + 8 >= nvalid) Z = make_uint4(0, 0, 0, 0);
+        if (tt + 9 >= nvalid) Wq = make_uint4(0, 0, 0, 0);
+      }
       const uint32_t wr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       const uint32_t wr8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
@@ -375,6 +381,20 @@ __global__ void __launch_bounds__(32 * W)
       for (int kk = 0; kk < KSTEPS; ++kk) dev::ldmatrix_x4(kf[kk], kb + swz(krow, 2 * kk + (lane >> 4)));
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) dev::ldmatrix_x4_trans(vf[mt], vb + swz(vrow, 2 * mt + ((lane >> 3) & 1)));
+      if (nvalid < 16) {
+        // V rows past the context get weight 0, but 0 * NaN is NaN: clear the
+        // halves of tokens >= nvalid (a0/a1: tokens 2q4, 2q4+1; a2/a3: +8)
+        const int t0 = 2 * q4;
+        const uint32_t m0 = (t0 < nvalid ? 0xFFFFu : 0u) | (t0 + 1 < nvalid ? 0xFFFF0000u : 0u);
+        const uint32_t m8 = (t0 + 8 < nvalid ? 0xFFFFu : 0u) | (t0 + 9 < nvalid ? 0xFFFF0000u : 0u);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          vf[mt][0] &= m0;
+          vf[mt][1] &= m0;
+          vf[mt][2] &= m8;
+          vf[mt][3] &= m8;
+        }
+      }
     }
     __syncwarp();
     if (lane == 0 && j + NS * W < nb) {

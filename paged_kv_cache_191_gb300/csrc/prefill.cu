@@ -358,10 +358,22 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
           lB = lB * alB + (h1.x + h1.y + h3.x + h3.y);
         }
         // ---- O = O * alpha + P . V ---------------------------------------------
+        // V rows past the context get weight 0, but 0 * NaN is NaN: masks for
+        // the halves of tokens past it (b0b1: tokens 2q4, 2q4+1; b2b3: +8)
+        uint32_t m0 = 0xFFFFFFFFu, m8 = 0xFFFFFFFFu;
+        if (tok0 + 16 > sv.L) {
+          const int t0 = tok0 + 2 * q4;
+          m0 = (t0 < sv.L ? 0xFFFFu : 0u) | (t0 + 1 < sv.L ? 0xFFFF0000u : 0u);
+          m8 = (t0 + 8 < sv.L ? 0xFFFFu : 0u) | (t0 + 9 < sv.L ? 0xFFFF0000u : 0u);
+        }
 #pragma unroll
         for (int t2 = 0; t2 < D / 16; ++t2) {
           uint32_t vf[4];
           dev::ldmatrix_x4_trans(vf, vb + swz(vrow, 2 * t2 + vcol));
+          vf[0] &= m0;
+          vf[1] &= m8;
+          vf[2] &= m0;
+          vf[3] &= m8;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float* oo = o[2 * t2 + h];

@@ -244,3 +244,38 @@ def test_full_size_fp8_longctx_sampled(fmt):
     check_sampled(w, got, heads, ref, TOL[fmt])
     ref16 = oracle(w, heads=heads)
     check_sampled(w, got, heads, ref16, TOL[fmt])
+
+
+@pytest.mark.parametrize("kv", ["f16", "bf16", "fp8", "int8"])
+def test_stale_nan_rows_never_reach_the_output(kv):
+    """Cache rows past each context (the tail of its last block, and blocks
+    no table names) hold NaN bit patterns, as an uninitialised pool may: they
+    carry weight 0 and must not turn the output into NaN."""
+    D = 128
+    w = W.random_small(61, B=6, Hq=8, Hkv=2, D=D, kv_dtype=kv, max_len=200, min_len=1)
+    used = np.zeros((w.num_blocks, 16), bool)
+    for b in range(w.B):
+        n = int(w.context_lens[b])
+        for t in range(n):
+            used[w.block_tables[b][t // 16], t % 16] = True
+    if kv in ("fp8", "int8"):
+        kc, vc, ks, vs = fp8_pool_gpu(w)
+        (okc, ovc, oks, ovs), _ = fp8_pool_oracle(w)
+        nan_code = 0x7F  # E4M3 NaN; for INT8 any code is finite, the scale carries the NaN
+        kc, vc, ks, vs = kc.clone(), vc.clone(), ks.clone(), vs.clone()
+        m = torch.from_numpy(~used)
+        kc.view(torch.uint8)[m.nonzero(as_tuple=True)[0], :, m.nonzero(as_tuple=True)[1], :] = nan_code
+        vc.view(torch.uint8)[m.nonzero(as_tuple=True)[0], :, m.nonzero(as_tuple=True)[1], :] = nan_code
+        ks[m] = float("nan")
+        vs[m] = float("nan")
+        got = gpu_decode(w, pools=(kc, vc), scales=(ks, vs)).numpy()
+        ref = paged_decode(np_exact(w.q), okc, ovc, w.block_tables, w.context_lens, w.scale, oks, ovs)
+    else:
+        kp, vp = w.k_pool.clone(), w.v_pool.clone()
+        m = torch.from_numpy(~used)
+        bi, ri = m.nonzero(as_tuple=True)
+        kp[bi, :, ri, :] = float("nan")
+        vp[bi, :, ri, :] = float("nan")
+        got = gpu_decode(w, pools=(kp, vp)).numpy()
+        ref = oracle(w, pools=(kp, vp))
+    assert_close(got, ref, TOL[kv], f"{kv} with NaN in unused rows")

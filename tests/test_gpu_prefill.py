@@ -168,3 +168,23 @@ def test_full_size_sampled(name):
     ref = oracle(w, rows=rows)
     idx = tuple(np.array(rows).T)
     assert_close(out[idx], ref[idx], TOL[w.kv_dtype], name)
+
+
+@pytest.mark.parametrize("shape", [(8, 2, 128, "f16"), (8, 8, 128, "bf16"), (4, 4, 64, "f16")])
+def test_stale_nan_rows_never_reach_the_output(shape):
+    """Rows past each context hold NaN: weight 0, and the output stays finite
+    (both kernels: 8x2 and 8x8 at head_dim 128 run the tensor-memory kernel for
+    the 40-token chunk, the 64-row kernel for the 3-token one)."""
+    Hq, Hkv, D, dt = shape
+    w = W.random_prefill_small(71, Hq, Hkv, D, dt, [40, 3, 17], max_prior=50)
+    used = np.zeros((w.num_blocks, 16), bool)
+    for b in range(w.B):
+        for t in range(int(w.context_lens[b])):
+            used[w.block_tables[b][t // 16], t % 16] = True
+    m = torch.from_numpy(~used)
+    bi, ri = m.nonzero(as_tuple=True)
+    w.k_pool = w.k_pool.clone()
+    w.v_pool = w.v_pool.clone()
+    w.k_pool[bi, :, ri, :] = float("nan")
+    w.v_pool[bi, :, ri, :] = float("nan")
+    assert_close(gpu_prefill(w).numpy(), oracle(w), TOL[dt], f"{shape} with NaN in unused rows")
