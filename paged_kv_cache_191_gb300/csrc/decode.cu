@@ -314,6 +314,11 @@ __global__ void __launch_bounds__(32 * W)
     if (j < nb && lane == 0) issue(pb, i);
   }
 
+  // Every CTA of this grid has started once all of them pass here, so the
+  // merge kernel may be scheduled now: its CTAs become resident as slots
+  // free up and wait (griddepcontrol.wait) for this grid's completion
+  // instead of being launched after it.
+  dev::grid_launch_dependents();
   float o[MT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -497,7 +502,6 @@ __global__ void __launch_bounds__(32 * W)
       if constexpr (SPLIT_P) dev::Mma<QT>::run(o[mt], af, bl0, bl1);
     }
   }
-  dev::grid_launch_dependents();  // the merge kernel may start being scheduled
 
   // ---- output: this item's (o, m, l) or, for one partition, o / l -----------------
 #pragma unroll

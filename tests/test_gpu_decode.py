@@ -279,3 +279,16 @@ def test_stale_nan_rows_never_reach_the_output(kv):
         got = gpu_decode(w, pools=(kp, vp)).numpy()
         ref = oracle(w, pools=(kp, vp))
     assert_close(got, ref, TOL[kv], f"{kv} with NaN in unused rows")
+
+
+@pytest.mark.parametrize("B,max_len,split", [(300, 300, 64), (5, 1100, 16), (70, 900, 64)])
+def test_item_mappings(B, max_len, split):
+    """Split launches over many sequences (300), many partitions (69 of 16
+    tokens) and a mix (70 sequences, 15 partitions), every seventh sequence
+    empty: the (sequence x kv head, partition) grid against the oracle."""
+    w = W.random_small(900 + B, B=B, Hq=4, Hkv=2, D=64, kv_dtype="f16", max_len=max_len)
+    lens = w.context_lens.copy()
+    lens[::7] = 0
+    ref = oracle(w, lens=lens)
+    assert_close(gpu_decode(w, split_tokens=split, lens=lens, max_len=max_len).numpy(), ref, TOL["f16"],
+                 f"B={B} split={split}")
