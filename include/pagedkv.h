@@ -217,8 +217,12 @@ size_t pa_chunked_prefill_workspace_size(int32_t num_tokens, int32_t B, int32_t 
  * zero row.  n_b = 0 is allowed.
  *
  * q            device [num_tokens][num_q_heads][head_dim] in q_dtype, the
- *              sequences' tokens packed in order.  q_dtype must equal kv_dtype
- *              (F16 or BF16; FP8 caches return PA_ERR_UNSUPPORTED).
+ *              sequences' tokens packed in order.  q_dtype equals kv_dtype for
+ *              F16 / BF16 caches; for FP8_E4M3 / INT8 caches it is F16 or BF16
+ *              (codes are converted to it exactly; head_dim 128).
+ * k_scale, v_scale  FP8 / INT8 caches: device float [num_blocks][16] per-token
+ *              scales as pa_cache_write stores them (16-byte aligned); NULL
+ *              for F16 / BF16 caches.
  * q_start      device int32 [B + 1], q_start[0] = 0, nondecreasing,
  *              q_start[B] <= num_tokens, each n_b <= max_q_len (else that
  *              sequence is skipped and PA_DEVERR_QUERY_RANGE is set).
@@ -232,11 +236,13 @@ size_t pa_chunked_prefill_workspace_size(int32_t num_tokens, int32_t B, int32_t 
  * Work: one CTA per (sequence, kv head, 64-row tile of (token, head) rows,
  * partition); K/V tiles of a partition are loaded once per CTA by TMA and
  * shared by its four compute warps; partitions are merged by a second
- * kernel when a row's keys span more than one.
+ * kernel when a row's keys span more than one.  16-bit caches at head_dim
+ * 128 with more than 64 rows per kv head use 128-row tiles on tcgen05.
  */
 pa_status pa_chunked_prefill(const void* q, int32_t q_dtype, const int32_t* q_start,
                              int32_t num_tokens, int32_t max_q_len,
                              const void* k_cache, const void* v_cache,
+                             const float* k_scale, const float* v_scale,
                              const int32_t* block_tables, int32_t max_blocks_per_seq,
                              const int32_t* context_lens, int32_t max_context_len,
                              int32_t B, int32_t num_q_heads, float scale,
@@ -473,7 +479,8 @@ pa_status pa_sched_limits(const pa_sched* s, int32_t* max_batch, int32_t* max_to
  * (GPU -> host pool) of preempted requests; the decode items' cache write
  * fused into pa_decode; pa_cache_write + pa_chunked_prefill for the prompt
  * chunks; swap-in copies (host pool -> GPU) of requests that run next step.
- * F16 / BF16 caches.  Every buffer is caller-owned.
+ * F16 / BF16 caches, or FP8_E4M3 / INT8 caches with per-token scales (the
+ * model's q / K / V then in F16 or BF16).  Every buffer is caller-owned.
  * ------------------------------------------------------------------------- */
 typedef struct pa_serve pa_serve;
 
@@ -490,6 +497,10 @@ typedef struct {
   void*   staging_dev;      /* device, pa_serve_staging_bytes() bytes, 16-byte aligned */
   void*   workspace;        /* device, >= pa_serve_workspace_bytes() bytes (may be NULL if 0) */
   size_t  workspace_bytes;
+  float*  k_scale;          /* FP8 / INT8 caches: device per-token scales [num_blocks][16], */
+  float*  v_scale;          /*   16-byte aligned; NULL for F16 / BF16 caches */
+  float*  k_host_scale;     /* FP8 / INT8 caches with host_blocks > 0: pinned [host_blocks][16] */
+  float*  v_host_scale;
 } pa_serve_buffers;
 
 size_t pa_serve_staging_bytes(const pa_sched* s, int32_t max_context);

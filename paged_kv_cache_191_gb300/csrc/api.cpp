@@ -306,8 +306,6 @@ static pa_status check_prefill(int32_t T, int32_t B, int32_t num_q_heads, int32_
     return fail(PA_ERR_INVALID, "pa_chunked_prefill: num_q_heads must be a multiple of num_kv_heads");
   if (num_q_heads / desc->num_kv_heads > PA_MAX_GROUP)
     return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: more than %d query heads per kv head", PA_MAX_GROUP);
-  if (pa::quantised(desc->kv_dtype))
-    return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: FP8 / INT8 caches are not built");
   return PA_OK;
 }
 
@@ -324,6 +322,7 @@ size_t pa_chunked_prefill_workspace_size(int32_t num_tokens, int32_t B, int32_t 
 
 pa_status pa_chunked_prefill(const void* q, int32_t q_dtype, const int32_t* q_start, int32_t num_tokens,
                              int32_t max_q_len, const void* k_cache, const void* v_cache,
+                             const float* k_scale, const float* v_scale,
                              const int32_t* block_tables, int32_t max_blocks_per_seq,
                              const int32_t* context_lens, int32_t max_context_len, int32_t B,
                              int32_t num_q_heads, float scale, void* out, int32_t out_dtype,
@@ -333,7 +332,18 @@ pa_status pa_chunked_prefill(const void* q, int32_t q_dtype, const int32_t* q_st
   if (st != PA_OK) return st;
   if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID, "pa_chunked_prefill: max_blocks_per_seq <= 0");
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "pa_chunked_prefill: scale is not finite");
-  if (q_dtype != desc->kv_dtype) return fail(PA_ERR_INVALID, "pa_chunked_prefill: q_dtype must equal kv_dtype");
+  const bool q8 = pa::quantised(desc->kv_dtype);
+  if (q8) {
+    if (q_dtype != PA_DTYPE_F16 && q_dtype != PA_DTYPE_BF16)
+      return fail(PA_ERR_INVALID, "pa_chunked_prefill: q_dtype must be F16 or BF16 for an FP8 / INT8 cache");
+    if (!k_scale || !v_scale || !pa::aligned16(k_scale) || !pa::aligned16(v_scale))
+      return fail(PA_ERR_INVALID, "pa_chunked_prefill: FP8 / INT8 cache needs 16-byte aligned scales");
+  } else {
+    if (q_dtype != desc->kv_dtype)
+      return fail(PA_ERR_INVALID, "pa_chunked_prefill: q_dtype must equal kv_dtype");
+    if (k_scale || v_scale)
+      return fail(PA_ERR_INVALID, "pa_chunked_prefill: scales are only for FP8 / INT8 caches");
+  }
   if (out_dtype != q_dtype && out_dtype != PA_DTYPE_F32)
     return fail(PA_ERR_INVALID, "pa_chunked_prefill: out_dtype must be q_dtype or F32");
   if (B == 0 || num_tokens == 0) return PA_OK;
@@ -356,9 +366,12 @@ pa_status pa_chunked_prefill(const void* q, int32_t q_dtype, const int32_t* q_st
   }
   pa::PrefillLaunch a;
   a.q = q;
+  a.q_dtype = q_dtype;
   a.q_start = q_start;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.block_tables = block_tables;
   a.max_blocks = max_blocks_per_seq;
   a.context_lens = context_lens;

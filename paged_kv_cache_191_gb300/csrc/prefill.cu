@@ -29,6 +29,16 @@
 //   registers and V via ldmatrix.trans.  bf16 P is carried as hi + lo bf16
 //   parts (rounding error ~2^-17), f16 P once, normalised by the rounded
 //   weights.
+// * FP8 E4M3 and INT8 caches (1-byte codes, head_dim 128; this kernel
+//   only): the stage also carries the block's 16 K and 16 V per-token scales
+//   (two bulk copies on the same barrier).  Codes are converted exactly to
+//   the query's 16-bit type in registers.  For Q . K^T the head dimension is
+//   visited in a permuted order (lane q4 takes dims 32 q4 .. 32 q4 + 31, four
+//   per k-step, Q loaded the same way), so a lane reads 32 contiguous bytes of
+//   a key row; the K scale multiplies the score.  For P . V a lane reads one
+//   32-bit word (4 dims) of each of its four token rows and byte-permutes
+//   them into the B fragments of four column tiles, so the output columns
+//   come out permuted (undone at the store); the V scale multiplies p.
 // * A row whose keys fit one partition is written directly; otherwise each
 //   partition writes (o, m, l) and prefill_reduce merges them with
 //   log-sum-exp weights, launched as a programmatic dependent.
@@ -69,14 +79,20 @@ struct PrefillArgs {
   int32_t bpp, max_parts;
   float scale_log2;
   int32_t out_f32;
+  const float* k_scale;  // FP8 / INT8 caches: [num_blocks][16] per-token scales
+  const float* v_scale;
 };
 
-template <int D>
+// Shared memory of prefill_main: the K/V stage ring, full and empty
+// barriers, and for 1-byte codes each stage's 16 K and 16 V scales.
+template <typename KT, int D>
 struct PTile {
-  static constexpr int ROWB = 2 * D;                       // bytes per token row
-  static constexpr int TB = 16 * ROWB;                     // one (block, head) tile
-  static constexpr int NS = kRingBytes / (2 * TB);         // K+V stages
-  static constexpr int SMEM = 1024 + NS * 2 * TB + NS * 16;
+  static constexpr bool Q8 = sizeof(KT) == 1;
+  static constexpr int ROWB = D * static_cast<int>(sizeof(KT));  // bytes per token row
+  static constexpr int TB = 16 * ROWB;                             // one (block, head) tile
+  static constexpr int NS = kRingBytes / (2 * TB);                 // K+V stages
+  static constexpr int SCALES = Q8 ? NS * 128 : 0;
+  static constexpr int SMEM = 1024 + NS * 2 * TB + NS * 16 + SCALES;
   static_assert(ROWB == 128 || ROWB == 256, "rows of one or two 128-byte swizzle spans");
   static_assert(NS >= 2, "stage ring too small");
 };
@@ -123,19 +139,24 @@ __device__ __forceinline__ void store_pair(const PrefillArgs& a, size_t idx, flo
     *reinterpret_cast<uint32_t*>(static_cast<T*>(a.out) + idx) = dev::pack2<T>(x, y);
 }
 
-template <typename T, int D>
+template <typename KT, typename T, int D>
 __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
     prefill_main(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const PrefillArgs a) {
-  using TL = PTile<D>;
+  using TL = PTile<KT, D>;
+  constexpr bool Q8 = TL::Q8;
+  static_assert(!Q8 || D == 128, "1-byte codes at head_dim 128");
   constexpr int NS = TL::NS;
   constexpr int KSTEPS = D / 16;
   constexpr int DT = D / 8;  // 8-wide column tiles of O
   constexpr bool SPLIT_P = std::is_same<T, __nv_bfloat16>::value;
+  constexpr uint32_t STAGE_TX = 2 * TL::TB + (Q8 ? 128 : 0);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t ring = (dev::smem_addr(smem_raw) + 1023u) & ~1023u;
   const uint32_t bar_full = ring + NS * 2 * TL::TB, bar_empty = bar_full + NS * 8;
+  const uint32_t scales = bar_empty + NS * 8;  // Q8: stage s holds K scales [16], V scales [16]
+  const float* s_scale = reinterpret_cast<const float*>(smem_raw + (scales - dev::smem_addr(smem_raw)));
 
   const int wid = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const int qt = static_cast<int>(blockIdx.x) % a.QT, bg = static_cast<int>(blockIdx.x) / a.QT;
@@ -218,13 +239,17 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
             // consumers' reads of this stage precede the refill's writes
             dev::fence_proxy_async_smem();
             const uint32_t bar = bar_full + 8 * s, kdst = ring + s * 2 * TL::TB, vdst = kdst + TL::TB;
-            dev::mbar_arrive_expect_tx(bar, 2 * TL::TB);
+            dev::mbar_arrive_expect_tx(bar, STAGE_TX);
             if constexpr (TL::ROWB == 256) {
               dev::tma_load_5d(kdst, &tmK, bar, 0, 0, 0, g, pb);
               dev::tma_load_5d(vdst, &tmV, bar, 0, 0, 0, g, pb);
             } else {
               dev::tma_load_3d(kdst, &tmK, bar, 0, g * 16, pb);
               dev::tma_load_3d(vdst, &tmV, bar, 0, g * 16, pb);
+            }
+            if constexpr (Q8) {
+              dev::bulk_load(scales + s * 128, a.k_scale + static_cast<size_t>(pb) * 16, 64, bar);
+              dev::bulk_load(scales + s * 128 + 64, a.v_scale + static_cast<size_t>(pb) * 16, 64, bar);
             }
             issued = i + 1;
           }
@@ -265,11 +290,20 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
       const T* qb = static_cast<const T*>(a.q) + headB * D;
 #pragma unroll
       for (int kk = 0; kk < KSTEPS; ++kk) {
-        const int c = 16 * kk + 2 * q4;
-        qf[kk][0] = hasA ? *reinterpret_cast<const uint32_t*>(qa + c) : 0u;
-        qf[kk][1] = hasB ? *reinterpret_cast<const uint32_t*>(qb + c) : 0u;
-        qf[kk][2] = hasA ? *reinterpret_cast<const uint32_t*>(qa + c + 8) : 0u;
-        qf[kk][3] = hasB ? *reinterpret_cast<const uint32_t*>(qb + c + 8) : 0u;
+        if constexpr (Q8) {  // permuted head dims: lane q4 takes 32 q4 + 4 kk .. + 3
+          const uint2 wa = hasA ? *reinterpret_cast<const uint2*>(qa + 32 * q4 + 4 * kk) : make_uint2(0u, 0u);
+          const uint2 wb = hasB ? *reinterpret_cast<const uint2*>(qb + 32 * q4 + 4 * kk) : make_uint2(0u, 0u);
+          qf[kk][0] = wa.x;
+          qf[kk][1] = wb.x;
+          qf[kk][2] = wa.y;
+          qf[kk][3] = wb.y;
+        } else {
+          const int c = 16 * kk + 2 * q4;
+          qf[kk][0] = hasA ? *reinterpret_cast<const uint32_t*>(qa + c) : 0u;
+          qf[kk][1] = hasB ? *reinterpret_cast<const uint32_t*>(qb + c) : 0u;
+          qf[kk][2] = hasA ? *reinterpret_cast<const uint32_t*>(qa + c + 8) : 0u;
+          qf[kk][3] = hasB ? *reinterpret_cast<const uint32_t*>(qb + c + 8) : 0u;
+        }
       }
     }
     const float sl2 = a.scale_log2;
@@ -291,14 +325,31 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
         float sc[2][4], sd[2][4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) sc[0][k] = sc[1][k] = sd[0][k] = sd[1][k] = 0.f;
+        if constexpr (Q8) {
+          // key rows r (tile 0) and r + 8 (tile 1): bytes 32 q4 .. 32 q4 + 31
+          const uint4 x0 = dev::lds128(kb + swz(r, 2 * q4)), x1 = dev::lds128(kb + swz(r, 2 * q4 + 1));
+          const uint4 y0 = dev::lds128(kb + swz(r + 8, 2 * q4)), y1 = dev::lds128(kb + swz(r + 8, 2 * q4 + 1));
+          const uint32_t wx[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          const uint32_t wy[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-          uint32_t kf[4];
-          dev::ldmatrix_x4(kf, kb + swz(krow, 2 * kk + kcol));
-          float(&acc0)[4] = (kk & 1) ? sd[0] : sc[0];
-          float(&acc1)[4] = (kk & 1) ? sd[1] : sc[1];
-          dev::Mma<T>::run(acc0, qf[kk], kf[0], kf[1]);
-          dev::Mma<T>::run(acc1, qf[kk], kf[2], kf[3]);
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            float(&acc0)[4] = (kk & 1) ? sd[0] : sc[0];
+            float(&acc1)[4] = (kk & 1) ? sd[1] : sc[1];
+            dev::Mma<T>::run(acc0, qf[kk], dev::code8x2_to<KT, T>(static_cast<uint16_t>(wx[kk] & 0xffffu)),
+                             dev::code8x2_to<KT, T>(static_cast<uint16_t>(wx[kk] >> 16)));
+            dev::Mma<T>::run(acc1, qf[kk], dev::code8x2_to<KT, T>(static_cast<uint16_t>(wy[kk] & 0xffffu)),
+                             dev::code8x2_to<KT, T>(static_cast<uint16_t>(wy[kk] >> 16)));
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            uint32_t kf[4];
+            dev::ldmatrix_x4(kf, kb + swz(krow, 2 * kk + kcol));
+            float(&acc0)[4] = (kk & 1) ? sd[0] : sc[0];
+            float(&acc1)[4] = (kk & 1) ? sd[1] : sc[1];
+            dev::Mma<T>::run(acc0, qf[kk], kf[0], kf[1]);
+            dev::Mma<T>::run(acc1, qf[kk], kf[2], kf[3]);
+          }
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -312,8 +363,9 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int t = tok0 + nt * 8 + 2 * q4 + e;
-            x[nt][e] = t <= posA ? sc[nt][e] * sl2 : -INFINITY;
-            x[nt][2 + e] = t <= posB ? sc[nt][2 + e] * sl2 : -INFINITY;
+            const float c = Q8 ? sl2 * s_scale[s * 32 + nt * 8 + 2 * q4 + e] : sl2;  // K scale of token t
+            x[nt][e] = t <= posA ? sc[nt][e] * c : -INFINITY;
+            x[nt][2 + e] = t <= posB ? sc[nt][2 + e] * c : -INFINITY;
           }
         float bA = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
         float bB = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
@@ -335,6 +387,21 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
           pv[nt][2] = exp2f(x[nt][2] - zB);
           pv[nt][3] = exp2f(x[nt][3] - zB);
         }
+        if constexpr (Q8) {
+          // l sums the weights; V's per-token scale rides on p (0 past the
+          // context, where a stale scale may be NaN)
+          lA = lA * alA + (pv[0][0] + pv[0][1] + pv[1][0] + pv[1][1]);
+          lB = lB * alB + (pv[0][2] + pv[0][3] + pv[1][2] + pv[1][3]);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int tt = nt * 8 + 2 * q4 + e;
+              const float vs = tok0 + tt < sv.L ? s_scale[s * 32 + 16 + tt] : 0.f;
+              pv[nt][e] *= vs;
+              pv[nt][2 + e] *= vs;
+            }
+        }
         // P as the A operand: rows r / r + 8, tokens 2q4.. of each 8-token tile
         uint32_t ph[4], pl[4] = {0u, 0u, 0u, 0u};
         ph[0] = dev::pack2<T>(pv[0][0], pv[0][1]);
@@ -348,9 +415,11 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
             const int nt = k >> 1, e = (k & 1) * 2;
             pl[k] = dev::pack2<T>(pv[nt][e] - h.x, pv[nt][e + 1] - h.y);
           }
-          lA = lA * alA + (pv[0][0] + pv[0][1] + pv[1][0] + pv[1][1]);
-          lB = lB * alB + (pv[0][2] + pv[0][3] + pv[1][2] + pv[1][3]);
-        } else {
+          if constexpr (!Q8) {
+            lA = lA * alA + (pv[0][0] + pv[0][1] + pv[1][0] + pv[1][1]);
+            lB = lB * alB + (pv[0][2] + pv[0][3] + pv[1][2] + pv[1][3]);
+          }
+        } else if constexpr (!Q8) {
           // normalise with the rounded weights the PV product uses
           const float2 h0 = dev::unpack2<T>(ph[0]), h1 = dev::unpack2<T>(ph[1]);
           const float2 h2 = dev::unpack2<T>(ph[2]), h3 = dev::unpack2<T>(ph[3]);
@@ -361,28 +430,66 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
         // V rows past the context get weight 0, but 0 * NaN is NaN: masks for
         // the halves of tokens past it (b0b1: tokens 2q4, 2q4+1; b2b3: +8)
         uint32_t m0 = 0xFFFFFFFFu, m8 = 0xFFFFFFFFu;
+        uint32_t m0x = 0xFFFFFFFFu, m0y = 0xFFFFFFFFu, m8x = 0xFFFFFFFFu, m8y = 0xFFFFFFFFu;  // 1-byte rows
         if (tok0 + 16 > sv.L) {
           const int t0 = tok0 + 2 * q4;
           m0 = (t0 < sv.L ? 0xFFFFu : 0u) | (t0 + 1 < sv.L ? 0xFFFF0000u : 0u);
           m8 = (t0 + 8 < sv.L ? 0xFFFFu : 0u) | (t0 + 9 < sv.L ? 0xFFFF0000u : 0u);
+          m0x = t0 < sv.L ? 0xFFFFFFFFu : 0u;
+          m0y = t0 + 1 < sv.L ? 0xFFFFFFFFu : 0u;
+          m8x = t0 + 8 < sv.L ? 0xFFFFFFFFu : 0u;
+          m8y = t0 + 9 < sv.L ? 0xFFFFFFFFu : 0u;
         }
+        if constexpr (Q8) {
+          // Column tile 4 mm + c holds, in this lane's column slot, dim
+          // 4 (r + 8 mm) + c: one word at that offset from each of the lane's
+          // token rows 2q4, 2q4+1 (first B register) and 2q4+8, 2q4+9 (second)
 #pragma unroll
-        for (int t2 = 0; t2 < D / 16; ++t2) {
-          uint32_t vf[4];
-          dev::ldmatrix_x4_trans(vf, vb + swz(vrow, 2 * t2 + vcol));
-          vf[0] &= m0;
-          vf[1] &= m8;
-          vf[2] &= m0;
-          vf[3] &= m8;
+          for (int mm = 0; mm < 4; ++mm) {
+            const uint32_t off = 4u * static_cast<uint32_t>(r & 3);
+            const int ch = (r >> 2) + 2 * mm;
+            const uint32_t X = dev::lds32(vb + swz(2 * q4, ch) + off) & m0x;
+            const uint32_t Y = dev::lds32(vb + swz(2 * q4 + 1, ch) + off) & m0y;
+            const uint32_t Z = dev::lds32(vb + swz(2 * q4 + 8, ch) + off) & m8x;
+            const uint32_t W = dev::lds32(vb + swz(2 * q4 + 9, ch) + off) & m8y;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float* oo = o[2 * t2 + h];
-            oo[0] *= alA;
-            oo[1] *= alA;
-            oo[2] *= alB;
-            oo[3] *= alB;
-            dev::Mma<T>::run(o[2 * t2 + h], ph, vf[2 * h], vf[2 * h + 1]);
-            if constexpr (SPLIT_P) dev::Mma<T>::run(o[2 * t2 + h], pl, vf[2 * h], vf[2 * h + 1]);
+            for (int cp = 0; cp < 2; ++cp) {  // dims c = 2 cp, 2 cp + 1
+              const uint32_t sel = cp ? 0x7362u : 0x5140u;
+              const uint32_t xy = dev::prmt(X, Y, sel), zw = dev::prmt(Z, W, sel);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int ct = 4 * mm + 2 * cp + h;
+                const uint32_t b0 = dev::code8x2_to<KT, T>(static_cast<uint16_t>(h ? xy >> 16 : xy & 0xffffu));
+                const uint32_t b1 = dev::code8x2_to<KT, T>(static_cast<uint16_t>(h ? zw >> 16 : zw & 0xffffu));
+                float* oo = o[ct];
+                oo[0] *= alA;
+                oo[1] *= alA;
+                oo[2] *= alB;
+                oo[3] *= alB;
+                dev::Mma<T>::run(o[ct], ph, b0, b1);
+                if constexpr (SPLIT_P) dev::Mma<T>::run(o[ct], pl, b0, b1);
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int t2 = 0; t2 < D / 16; ++t2) {
+            uint32_t vf[4];
+            dev::ldmatrix_x4_trans(vf, vb + swz(vrow, 2 * t2 + vcol));
+            vf[0] &= m0;
+            vf[1] &= m8;
+            vf[2] &= m0;
+            vf[3] &= m8;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float* oo = o[2 * t2 + h];
+              oo[0] *= alA;
+              oo[1] *= alA;
+              oo[2] *= alB;
+              oo[3] *= alB;
+              dev::Mma<T>::run(o[2 * t2 + h], ph, vf[2 * h], vf[2 * h + 1]);
+              if constexpr (SPLIT_P) dev::Mma<T>::run(o[2 * t2 + h], pl, vf[2 * h], vf[2 * h + 1]);
+            }
           }
         }
       }
@@ -399,6 +506,19 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
   // Row with position pos needs ceil(ceil((pos + 1) / 16) / bpp) partitions:
   // one -> written here as o / l (partition 0); more -> partial (o, m, l).
   auto parts_of = [&](int pos) { return ((pos + 16) / 16 + a.bpp - 1) / a.bpp; };
+  // pair t (0 .. DT-1) of this lane's row values: its first output dim and
+  // the two values.  16-bit: column tile t, dims 8 t + 2 q4 (+1).  1-byte
+  // codes: tile 4 mm + c holds dim 32 mm + 8 q4 + 4 e + c in slot e, so pair
+  // t = 4 mm + jp is dims 32 mm + 8 q4 + 2 jp (+1).
+  auto pair_dim = [&](int t) { return Q8 ? 32 * (t >> 2) + 8 * q4 + 2 * (t & 3) : 8 * t + 2 * q4; };
+  auto pair_val = [&](int t, int half) {
+    if constexpr (Q8) {
+      const int c0 = 4 * (t >> 2) + 2 * (t & 1), e = 2 * half + ((t >> 1) & 1);
+      return make_float2(o[c0][e], o[c0 + 1][e]);
+    } else {
+      return make_float2(o[t][2 * half], o[t][2 * half + 1]);
+    }
+  };
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const bool has = half ? hasB : hasA;
@@ -417,14 +537,15 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
     if (np == 1) {
       const float inv = 1.f / l;
 #pragma unroll
-      for (int t = 0; t < DT; ++t)
-        store_pair<T>(a, head * D + 8 * t + 2 * q4, o[t][2 * half] * inv, o[t][2 * half + 1] * inv);
+      for (int t = 0; t < DT; ++t) {
+        const float2 v = pair_val(t, half);
+        store_pair<T>(a, head * D + pair_dim(t), v.x * inv, v.y * inv);
+      }
     } else {
       const size_t prow = head * a.max_parts + p;
       float* po = a.part_o + prow * D;
 #pragma unroll
-      for (int t = 0; t < DT; ++t)
-        *reinterpret_cast<float2*>(po + 8 * t + 2 * q4) = make_float2(o[t][2 * half], o[t][2 * half + 1]);
+      for (int t = 0; t < DT; ++t) *reinterpret_cast<float2*>(po + pair_dim(t)) = pair_val(t, half);
       if (q4 == 0) {
         a.part_m[prow] = m;
         a.part_l[prow] = l;
@@ -999,15 +1120,17 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
   }
 }
 
-template <typename T, int D>
+template <typename KT, typename T, int D>
 pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t stream) {
-  using TL = PTile<D>;
+  using TL = PTile<KT, D>;
+  constexpr bool SAME = std::is_same<KT, T>::value;  // 16-bit cache read as the query type
   // tcgen05 kernel (128-row tiles) or mma.sync kernel (64-row tiles), as planned
-  const bool TC = D == 128 && l.plan.tc;
+  const bool TC = SAME && D == 128 && l.plan.tc;
+  constexpr int EB = static_cast<int>(sizeof(KT));
   CUtensorMap tmK, tmV;
-  pa_status st = make_kv_map(&tmK, l.k_cache, l.Hkv, l.num_blocks, TL::ROWB, 2, dt, "pa_chunked_prefill", !TC);
+  pa_status st = make_kv_map(&tmK, l.k_cache, l.Hkv, l.num_blocks, TL::ROWB, EB, dt, "pa_chunked_prefill", !TC);
   if (st != PA_OK) return st;
-  st = make_kv_map(&tmV, l.v_cache, l.Hkv, l.num_blocks, TL::ROWB, 2, dt, "pa_chunked_prefill", !TC);
+  st = make_kv_map(&tmV, l.v_cache, l.Hkv, l.num_blocks, TL::ROWB, EB, dt, "pa_chunked_prefill", !TC);
   if (st != PA_OK) return st;
 
   PrefillArgs a;
@@ -1034,6 +1157,8 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
   a.max_parts = l.plan.max_parts;
   a.scale_log2 = l.scale * 1.4426950408889634f;
   a.out_f32 = l.out_dtype == PA_DTYPE_F32;
+  a.k_scale = l.k_scale;
+  a.v_scale = l.v_scale;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(PA_ERR_CUDA, "pa_chunked_prefill: no CUDA device");
@@ -1042,9 +1167,11 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
   static cudaError_t setup_err[kMaxDevices];
   using TS = tcg::Smem;
   std::call_once(once[dev], [dev] {
-    cudaError_t e = cudaFuncSetAttribute(prefill_main<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TL::SMEM);
-    if (e == cudaSuccess && D == 128)
-      e = cudaFuncSetAttribute(prefill_tc<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, TS::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_main<KT, T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TL::SMEM);
+    if constexpr (SAME && D == 128)
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(prefill_tc<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, TS::SMEM);
     setup_err[dev] = e;
   });
   if (setup_err[dev] != cudaSuccess)
@@ -1052,10 +1179,14 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
 
   const dim3 grid(static_cast<unsigned>(l.B * l.Hkv * l.plan.row_tiles), static_cast<unsigned>(l.plan.max_parts));
   cudaError_t e;
-  if (TC)
-    e = launch_dependent(prefill_tc<T>, grid, dim3(tcg::kThreads), TS::SMEM, stream, tmK, tmV, a);
-  else
-    e = launch_dependent(prefill_main<T, D>, grid, dim3(kThreads), TL::SMEM, stream, tmK, tmV, a);
+  if constexpr (SAME && D == 128) {
+    if (TC)
+      e = launch_dependent(prefill_tc<T>, grid, dim3(tcg::kThreads), TS::SMEM, stream, tmK, tmV, a);
+    else
+      e = launch_dependent(prefill_main<KT, T, D>, grid, dim3(kThreads), TL::SMEM, stream, tmK, tmV, a);
+  } else {
+    e = launch_dependent(prefill_main<KT, T, D>, grid, dim3(kThreads), TL::SMEM, stream, tmK, tmV, a);
+  }
   if (e == cudaSuccess && l.plan.max_parts > 1)
     e = launch_dependent(prefill_reduce<T, D>,
                          dim3(static_cast<unsigned>((static_cast<int64_t>(l.T) * l.Hq + kReduceRows - 1) / kReduceRows)),
@@ -1070,11 +1201,21 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
 pa_status launch_prefill(const PrefillLaunch& l, void* stream_ptr) {
   cudaStream_t st = static_cast<cudaStream_t>(stream_ptr);
   if (l.kv_dtype == PA_DTYPE_F16) {
-    if (l.D == 64) return launch_t<__half, 64>(l, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, st);
-    return launch_t<__half, 128>(l, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, st);
+    if (l.D == 64) return launch_t<__half, __half, 64>(l, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, st);
+    return launch_t<__half, __half, 128>(l, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, st);
   }
-  if (l.D == 64) return launch_t<__nv_bfloat16, 64>(l, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, st);
-  return launch_t<__nv_bfloat16, 128>(l, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, st);
+  if (l.kv_dtype == PA_DTYPE_BF16) {
+    if (l.D == 64) return launch_t<__nv_bfloat16, __nv_bfloat16, 64>(l, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, st);
+    return launch_t<__nv_bfloat16, __nv_bfloat16, 128>(l, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, st);
+  }
+  // 1-byte codes (E4M3 as uint8_t, INT8 as int8_t), head_dim 128 (checked by
+  // the caller), read as the query's 16-bit type; the map moves raw bytes
+  const bool f16 = l.q_dtype == PA_DTYPE_F16;
+  if (l.kv_dtype == PA_DTYPE_INT8)
+    return f16 ? launch_t<int8_t, __half, 128>(l, CU_TENSOR_MAP_DATA_TYPE_UINT8, st)
+               : launch_t<int8_t, __nv_bfloat16, 128>(l, CU_TENSOR_MAP_DATA_TYPE_UINT8, st);
+  return f16 ? launch_t<uint8_t, __half, 128>(l, CU_TENSOR_MAP_DATA_TYPE_UINT8, st)
+             : launch_t<uint8_t, __nv_bfloat16, 128>(l, CU_TENSOR_MAP_DATA_TYPE_UINT8, st);
 }
 
 pa_status read_errors_prefill(uint32_t* flags, bool clear) {

@@ -9,6 +9,8 @@
 //   any write can reuse the blocks they released;
 //   decode items: cache write of the new token fused into paged decode
 //   (pa_decode_append), one warp-sized partition per (sequence, kv head);
+//   FP8 / INT8 caches carry their per-token scales through every step (the
+//   writes store them, attention reads them, swaps move them with the blocks);
 //   prompt chunks: pa_cache_write of their tokens, then pa_chunked_prefill
 //   (causal inside each chunk);
 //   swap-in copies (pinned host pool -> GPU) of requests that run next step.
@@ -59,6 +61,13 @@ struct pa_serve {
 namespace {
 
 size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+// The model's q / K / V dtype: the cache's for 16-bit caches, F16 or BF16
+// for 1-byte caches.
+bool input_dtype_ok(int32_t kv_dtype, int32_t in_dtype) {
+  if (pa::quantised(kv_dtype)) return in_dtype == PA_DTYPE_F16 || in_dtype == PA_DTYPE_BF16;
+  return in_dtype == kv_dtype;
+}
 
 struct Layout {
   size_t slots, out, in, qs, lens, tab, bytes;
@@ -117,8 +126,14 @@ pa_status pa_serve_create(pa_sched* s, const pa_cache_desc* desc, const pa_serve
   if (!out) return pa::fail(PA_ERR_INVALID, "pa_serve_create: out is NULL");
   *out = nullptr;
   if (!s || !desc || !b) return pa::fail(PA_ERR_INVALID, "pa_serve_create: null argument");
-  if (pa::quantised(desc->kv_dtype))
-    return pa::fail(PA_ERR_UNSUPPORTED, "pa_serve_create: FP8 / INT8 caches are not built for the chunk kernel");
+  const bool q8 = pa::quantised(desc->kv_dtype);
+  if (q8) {
+    if (!b->k_scale || !b->v_scale || !pa::aligned16(b->k_scale) || !pa::aligned16(b->v_scale) ||
+        (b->host_blocks && (!b->k_host_scale || !b->v_host_scale)))
+      return pa::fail(PA_ERR_INVALID, "pa_serve_create: FP8 / INT8 caches need device (and host) scales");
+  } else if (b->k_scale || b->v_scale || b->k_host_scale || b->v_host_scale) {
+    return pa::fail(PA_ERR_INVALID, "pa_serve_create: scales are only for FP8 / INT8 caches");
+  }
   int32_t mb = 0, mt = 0, nb = 0;
   pa_status st = pa_sched_limits(s, &mb, &mt, &nb);
   if (st != PA_OK) return st;
@@ -229,8 +244,8 @@ pa_status pa_serve_launch(pa_serve* e, const void* q, const void* k_new, const v
                           void* out, void* stream) {
   if (!e) return pa::fail(PA_ERR_INVALID, "pa_serve_launch: null handle");
   if (!e->planned) return pa::fail(PA_ERR_INVALID, "pa_serve_launch: no planned step");
-  if (in_dtype != e->desc.kv_dtype)
-    return pa::fail(PA_ERR_INVALID, "pa_serve_launch: in_dtype must be the cache dtype");
+  if (!input_dtype_ok(e->desc.kv_dtype, in_dtype))
+    return pa::fail(PA_ERR_INVALID, "pa_serve_launch: in_dtype must be the cache dtype (F16 / BF16 for FP8 / INT8)");
   if (e->T && (!q || !k_new || !v_new || !out)) return pa::fail(PA_ERR_INVALID, "pa_serve_launch: null argument");
   const pa_serve_buffers& b = e->b;
   const int32_t Hq = b.num_q_heads, Hkv = e->desc.num_kv_heads, D = e->desc.head_dim;
@@ -253,13 +268,13 @@ pa_status pa_serve_launch(pa_serve* e, const void* q, const void* k_new, const v
   const int32_t n = e->n, n_dec = e->n_dec;
   pa_status st;
   if (e->n_out) {
-    st = pa_swap_blocks(b.k_host, b.v_host, nullptr, nullptr, b.host_blocks, b.k_cache, b.v_cache, nullptr, nullptr,
-                        e->desc.num_blocks, reinterpret_cast<const int64_t*>(dv + e->o_out), e->n_out, &e->desc,
-                        stream);
+    st = pa_swap_blocks(b.k_host, b.v_host, b.k_host_scale, b.v_host_scale, b.host_blocks, b.k_cache, b.v_cache,
+                        b.k_scale, b.v_scale, e->desc.num_blocks, reinterpret_cast<const int64_t*>(dv + e->o_out),
+                        e->n_out, &e->desc, stream);
     if (st != PA_OK) return st;
   }
   if (n_dec) {
-    st = pa_decode_append(k_new, v_new, in_dtype, d_slots, q, in_dtype, b.k_cache, b.v_cache, nullptr, nullptr, d_tab,
+    st = pa_decode_append(k_new, v_new, in_dtype, d_slots, q, in_dtype, b.k_cache, b.v_cache, b.k_scale, b.v_scale, d_tab,
                           e->cap, d_lens, max_ctx, n_dec, Hq, scale, out, in_dtype, &e->desc, b.workspace,
                           e->ws_decode, 0, stream);
     if (st != PA_OK) return st;
@@ -268,12 +283,13 @@ pa_status pa_serve_launch(pa_serve* e, const void* q, const void* k_new, const v
   if (Tc > 0) {
     const uint8_t* kc = static_cast<const uint8_t*>(k_new) + n_dec * kvrow;
     const uint8_t* vc = static_cast<const uint8_t*>(v_new) + n_dec * kvrow;
-    st = pa_cache_write(kc, vc, in_dtype, d_slots + n_dec, Tc, b.k_cache, b.v_cache, nullptr, nullptr, &e->desc,
+    st = pa_cache_write(kc, vc, in_dtype, d_slots + n_dec, Tc, b.k_cache, b.v_cache, b.k_scale, b.v_scale, &e->desc,
                         stream);
     if (st != PA_OK) return st;
     st = pa_chunked_prefill(static_cast<const uint8_t*>(q) + n_dec * qrow, in_dtype,
                             reinterpret_cast<const int32_t*>(dv + e->o_qs), static_cast<int32_t>(Tc), e->max_q,
-                            b.k_cache, b.v_cache, d_tab + static_cast<size_t>(n_dec) * e->cap, e->cap,
+                            b.k_cache, b.v_cache, b.k_scale, b.v_scale, d_tab + static_cast<size_t>(n_dec) * e->cap,
+                            e->cap,
                             d_lens + n_dec, max_ctx, n - n_dec, Hq, scale,
                             static_cast<uint8_t*>(out) + n_dec * qrow, in_dtype, &e->desc,
                             static_cast<uint8_t*>(b.workspace) + e->ws_decode, b.workspace_bytes - e->ws_decode,
@@ -281,9 +297,9 @@ pa_status pa_serve_launch(pa_serve* e, const void* q, const void* k_new, const v
     if (st != PA_OK) return st;
   }
   if (e->n_in) {
-    st = pa_swap_blocks(b.k_cache, b.v_cache, nullptr, nullptr, e->desc.num_blocks, b.k_host, b.v_host, nullptr,
-                        nullptr, b.host_blocks, reinterpret_cast<const int64_t*>(dv + e->o_in), e->n_in, &e->desc,
-                        stream);
+    st = pa_swap_blocks(b.k_cache, b.v_cache, b.k_scale, b.v_scale, e->desc.num_blocks, b.k_host, b.v_host,
+                        b.k_host_scale, b.v_host_scale, b.host_blocks, reinterpret_cast<const int64_t*>(dv + e->o_in),
+                        e->n_in, &e->desc, stream);
     if (st != PA_OK) return st;
   }
   return pa::ok();
@@ -292,7 +308,8 @@ pa_status pa_serve_launch(pa_serve* e, const void* q, const void* k_new, const v
 pa_status pa_serve_step(pa_serve* e, const void* q, const void* k_new, const void* v_new, int32_t in_dtype,
                         void* out, pa_sched_step_out* d, void* stream) {
   if (!e) return pa::fail(PA_ERR_INVALID, "pa_serve_step: null handle");
-  if (in_dtype != e->desc.kv_dtype) return pa::fail(PA_ERR_INVALID, "pa_serve_step: in_dtype must be the cache dtype");
+  if (!input_dtype_ok(e->desc.kv_dtype, in_dtype))
+    return pa::fail(PA_ERR_INVALID, "pa_serve_step: in_dtype must be the cache dtype (F16 / BF16 for FP8 / INT8)");
   pa_status st = pa_serve_plan(e, d, nullptr);
   if (st != PA_OK) return st;
   return pa_serve_launch(e, q, k_new, v_new, in_dtype, out, stream);

@@ -63,7 +63,9 @@ class ServeBuffers(C.Structure):
     _fields_ = [("k_cache", C.c_void_p), ("v_cache", C.c_void_p), ("k_host", C.c_void_p), ("v_host", C.c_void_p),
                 ("host_blocks", C.c_int32), ("num_q_heads", C.c_int32), ("max_context", C.c_int32),
                 ("split_tokens", C.c_int32), ("staging_host", C.c_void_p), ("staging_dev", C.c_void_p),
-                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
+                ("k_scale", C.c_void_p), ("v_scale", C.c_void_p), ("k_host_scale", C.c_void_p),
+                ("v_host_scale", C.c_void_p)]
 
 
 SIGNATURES = {
@@ -79,8 +81,8 @@ SIGNATURES = {
                                       _I32, C.POINTER(CacheDesc), _I32, _P]),
     "pa_chunked_prefill_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32, C.POINTER(CacheDesc),
                                                        _I32]),
-    "pa_chunked_prefill": (C.c_int, [_P, _I32, _P, _I32, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F,
-                                     _P, _I32, C.POINTER(CacheDesc), _P, C.c_size_t, _I32, _P]),
+    "pa_chunked_prefill": (C.c_int, [_P, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
+                                     _F, _P, _I32, C.POINTER(CacheDesc), _P, C.c_size_t, _I32, _P]),
     "pa_copy_blocks": (C.c_int, [_P, _P, _P, _P, _P, _I64, C.POINTER(CacheDesc), _P]),
     "pa_swap_blocks": (C.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _I32, _P, _I64,
                                  C.POINTER(CacheDesc), _P]),
@@ -238,10 +240,11 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, sca
 
 def chunked_prefill(q, q_start, k_cache, v_cache, block_tables, context_lens, max_context_len,
                     max_q_len, scale, out=None, out_dtype=None, workspace=None, split_tokens=0,
-                    stream=None):
+                    stream=None, k_scale=None, v_scale=None):
     """Multi-token paged attention (chunked prefill / speculative verify).
 
-    q: [T, Hq, D] packed query tokens; q_start: int32 [B + 1] offsets.
+    q: [T, Hq, D] packed query tokens; q_start: int32 [B + 1] offsets;
+    k_scale, v_scale: float32 [num_blocks, 16] for FP8 / INT8 caches.
     Returns out [T, Hq, D] (q dtype, or out_dtype).
     """
     for t, n in ((q, "q"), (q_start, "q_start"), (k_cache, "k_cache"), (v_cache, "v_cache"),
@@ -272,7 +275,8 @@ def chunked_prefill(q, q_start, k_cache, v_cache, block_tables, context_lens, ma
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().pa_chunked_prefill(_ptr(q), _TORCH_DT[q.dtype], _ptr(q_start), T, int(max_q_len),
-                                    _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                                    _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                    _ptr(block_tables), block_tables.shape[1],
                                     _ptr(context_lens), int(max_context_len), B, Hq, float(scale),
                                     _ptr(out), _TORCH_DT[odt], C.byref(desc), _ptr(workspace), ws_bytes,
                                     int(split_tokens), _stream(stream)), "pa_chunked_prefill")

@@ -8,7 +8,9 @@ write fused into paged decode, the prompt chunks' cache write and
 multi-token attention, and the swap-in copies of returning requests.  The
 model around attention is not part of this library: queries and new K/V
 rows come from caller-provided device buffers (row t for the t-th new token
-of the iteration, decodes first).
+of the iteration, decodes first).  The cache is 16-bit (the model's dtype)
+or 1-byte codes with per-token scales (kv_dtype torch.uint8: FP8 E4M3,
+torch.int8: INT8), whose scales the engine moves with every write and swap.
 """
 import ctypes as C
 
@@ -20,7 +22,7 @@ from . import ops
 
 class ServingLoop:
     def __init__(self, num_blocks, host_blocks, num_kv_heads, num_q_heads, head_dim, dtype, max_batch,
-                 max_tokens, max_context, device="cuda", free_order=None, split_tokens=0):
+                 max_tokens, max_context, device="cuda", free_order=None, split_tokens=0, kv_dtype=None):
         L = ops.lib()
         self.sched = ops.Scheduler(num_blocks, max_batch, max_tokens, host_blocks, free_order)
         self.Hq, self.Hkv, self.D, self.dtype, self.dev = num_q_heads, num_kv_heads, head_dim, dtype, device
@@ -28,12 +30,23 @@ class ServingLoop:
         self.cap = -(-max_context // 16)
         self.max_context = self.cap * 16
         self.split = split_tokens or 1024
+        kv_dtype = kv_dtype or dtype
+        self.q8 = kv_dtype in (torch.uint8, torch.int8)
         shape = (num_blocks, num_kv_heads, 16, head_dim)
-        self.k_cache = torch.zeros(shape, dtype=dtype, device=device)
-        self.v_cache = torch.zeros(shape, dtype=dtype, device=device)
+        self.k_cache = torch.zeros(shape, dtype=kv_dtype, device=device)
+        self.v_cache = torch.zeros(shape, dtype=kv_dtype, device=device)
         hshape = (max(host_blocks, 1), num_kv_heads, 16, head_dim)
-        self.k_host = torch.zeros(hshape, dtype=dtype).pin_memory()
-        self.v_host = torch.zeros(hshape, dtype=dtype).pin_memory()
+        self.k_host = torch.zeros(hshape, dtype=kv_dtype).pin_memory()
+        self.v_host = torch.zeros(hshape, dtype=kv_dtype).pin_memory()
+        scales = [None] * 4
+        if self.q8:
+            self.k_scale = torch.zeros((num_blocks, 16), dtype=torch.float32, device=device)
+            self.v_scale = torch.zeros_like(self.k_scale)
+            self.k_host_scale = torch.zeros((max(host_blocks, 1), 16), dtype=torch.float32).pin_memory()
+            self.v_host_scale = torch.zeros_like(self.k_host_scale).pin_memory()
+            scales = [self.k_scale.data_ptr(), self.v_scale.data_ptr(),
+                      self.k_host_scale.data_ptr() if host_blocks else None,
+                      self.v_host_scale.data_ptr() if host_blocks else None]
         self.desc = ops.cache_desc(self.k_cache)
         h = self.sched._h
         self.meta_bytes = int(L.pa_serve_staging_bytes(h, self.max_context))
@@ -45,7 +58,8 @@ class ServingLoop:
                              self.k_host.data_ptr() if host_blocks else None,
                              self.v_host.data_ptr() if host_blocks else None,
                              host_blocks, num_q_heads, self.max_context, self.split,
-                             self.staging_host.data_ptr(), self.staging_dev.data_ptr(), self.ws.data_ptr(), ws)
+                             self.staging_host.data_ptr(), self.staging_dev.data_ptr(), self.ws.data_ptr(), ws,
+                             *scales)
         e = C.c_void_p()
         ops._check(L.pa_serve_create(h, C.byref(self.desc), C.byref(b), C.byref(e)), "pa_serve_create")
         self._e, self._L = e, L

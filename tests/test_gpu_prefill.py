@@ -188,3 +188,80 @@ def test_stale_nan_rows_never_reach_the_output(shape):
     w.k_pool[bi, :, ri, :] = float("nan")
     w.v_pool[bi, :, ri, :] = float("nan")
     assert_close(gpu_prefill(w).numpy(), oracle(w), TOL[dt], f"{shape} with NaN in unused rows")
+
+
+# ---- FP8 E4M3 and INT8 caches (the 64-row kernel) ------------------------------------
+def quantised_pools(w, fmt):
+    """The f16 pool quantised through pa_cache_write (one token per slot):
+    device codes and per-token scales."""
+    N, H, _, D = w.k_pool.shape
+    kin = w.k_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(DEV)
+    vin = w.v_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(DEV)
+    slots = torch.arange(N * 16, dtype=torch.int64, device=DEV)
+    kc = torch.zeros((N, H, 16, D), dtype=torch.int8 if fmt == "int8" else torch.uint8, device=DEV)
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros((N, 16), dtype=torch.float32, device=DEV)
+    vs = torch.zeros_like(ks)
+    ops.cache_write(kin, vin, slots, kc, vc, ks, vs)
+    torch.cuda.synchronize()
+    return kc, vc, ks, vs
+
+
+def gpu_prefill_q8(w, pools, out_dtype=torch.float32, split_tokens=0):
+    kc, vc, ks, vs = pools
+    q = w.q.to(DEV)
+    qs = torch.from_numpy(np.ascontiguousarray(w.q_start, dtype=np.int32)).to(DEV)
+    bt = torch.from_numpy(np.ascontiguousarray(w.block_tables, dtype=np.int32)).to(DEV)
+    cl = torch.from_numpy(np.ascontiguousarray(w.context_lens, dtype=np.int32)).to(DEV)
+    ml = max(int(w.context_lens.max()), 1)
+    out = torch.full(tuple(q.shape), float("nan"), dtype=out_dtype, device=DEV)
+    ops.chunked_prefill(q, qs, kc, vc, bt, cl, ml, int(w.q_lens.max()), w.scale, out=out,
+                        split_tokens=split_tokens, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def oracle_q8(w, pools, rows=None):
+    kc, vc, ks, vs = (t.cpu().numpy() for t in pools)
+    return paged_prefill(np_exact(w.q), w.q_start, kc, vc, w.block_tables, w.context_lens, w.scale,
+                         k_scale=ks, v_scale=vs, rows=rows)
+
+
+Q8_SHAPES = [(8, 2, "f16"), (8, 2, "bf16"), (64, 8, "bf16"), (4, 4, "f16"), (3, 1, "f16")]
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("Hq,Hkv,qdt", Q8_SHAPES)
+@pytest.mark.parametrize("split", [0, 64])
+def test_quantised_caches(fmt, Hq, Hkv, qdt, split):
+    """1-byte caches against the oracle on the same stored codes and scales
+    (chunks of 0 .. 130 tokens, row tiles with ragged tails, forced
+    partitions): within the FP8 / INT8 tolerance."""
+    w = W.random_prefill_small(400 + Hq + Hkv, Hq, Hkv, 128, "f16", [130, 0, 3, 1, 40, 17], max_prior=150)
+    if qdt == "bf16":
+        w.q = w.q.to(torch.bfloat16)
+    pools = quantised_pools(w, fmt)
+    assert_close(gpu_prefill_q8(w, pools, split_tokens=split).numpy(), oracle_q8(w, pools), TOL[fmt],
+                 f"{fmt} {Hq}/{Hkv} {qdt} split {split}")
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+def test_quantised_16bit_output_and_stale_rows(fmt):
+    """16-bit outputs within the tolerance plus half an ulp; codes and scales
+    of the rows past each context set to NaN patterns change nothing."""
+    w = W.random_prefill_small(91, 16, 4, 128, "f16", [33, 5, 64], max_prior=60)
+    kc, vc, ks, vs = quantised_pools(w, fmt)
+    ref = oracle_q8(w, (kc, vc, ks, vs))
+    used = np.zeros((w.num_blocks, 16), bool)
+    for b in range(w.B):
+        for t in range(int(w.context_lens[b])):
+            used[w.block_tables[b][t // 16], t % 16] = True
+    bi, ri = torch.from_numpy(~used).nonzero(as_tuple=True)
+    bi, ri = bi.to(DEV), ri.to(DEV)
+    kc.view(torch.uint8)[bi, :, ri, :] = 0x7F  # E4M3 NaN (a finite INT8 code)
+    vc.view(torch.uint8)[bi, :, ri, :] = 0x7F
+    ks[bi, ri] = float("nan")
+    vs[bi, ri] = float("nan")
+    out = gpu_prefill_q8(w, (kc, vc, ks, vs), out_dtype=torch.float16).float().numpy()
+    err = np.abs(out - ref)
+    assert np.all(err <= TOL[fmt] + half_ulp(ref, torch.float16)), float(np.nanmax(err))
