@@ -42,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 METRIC = "paged decode attention KV-read GB/s and tokens/s; % of GB300 HBM peak"
 METRIC_PREFILL = "multi-token paged attention KV-read GB/s and query tokens/s; % of GB300 HBM peak"
-PREFILL_CONFIGS = ("prefill_mix_llama7b", "spec_verify_gqa70b")
+PREFILL_CONFIGS = ("prefill_mix_llama7b", "prefill_mix_llama7b_fp8", "spec_verify_gqa70b")
 SERVING_CONFIGS = ("serving_llama7b",)
 METRIC_SERVING = "continuous-batching serving iterations: tokens/s through scheduler + swap + cache write + attention"
 
@@ -828,11 +828,12 @@ def prefill_cost(w):
     """(algorithmic bytes, flops) of one pa_chunked_prefill launch: K+V of every
     context token of every (sequence, kv head) once, Q, out, tables, lengths;
     4 * D flops per (query row, visible key)."""
-    e = 2
+    q8 = getattr(w, "kv_dtype", "f16") in ("fp8", "int8")
+    e = 1 if q8 else 2  # cache element bytes; queries and outputs are 16-bit
     lens = np.asarray(w.context_lens, dtype=np.int64)
     ql = np.asarray(w.q_lens, dtype=np.int64)
-    kv = int(lens.sum()) * w.Hkv * w.D * 2 * e
-    io = w.T * w.Hq * w.D * 2 * e
+    kv = int(lens.sum()) * w.Hkv * w.D * 2 * e + (int(lens.sum()) * 8 if q8 else 0)
+    io = w.T * w.Hq * w.D * 2 * 2
     meta = int(((lens + 15) // 16).sum()) * 4 + len(lens) * 8 + 4
     # visible keys of query i of sequence b: L_b - n_b + i + 1
     keys = int(sum(n * (L - n) + n * (n + 1) // 2 for L, n in zip(lens, ql)))
@@ -866,7 +867,21 @@ class PrefillStep:
         # the rows the chunk writes are the values the pool holds there
         new_k = w.k_pool[blk, :, row, :].contiguous()
         new_v = w.v_pool[blk, :, row, :].contiguous()
-        self.kc, self.vc = w.k_pool.to(device), w.v_pool.to(device)
+        self.q8 = w.kv_dtype in ("fp8", "int8")
+        self.ks = self.vs = None
+        if self.q8:  # the whole pool quantised on the device (set-up, not timed)
+            N, H, _, D = w.k_pool.shape
+            cdt = torch.int8 if w.kv_dtype == "int8" else torch.uint8
+            self.kc = torch.zeros((N, H, 16, D), dtype=cdt, device=device)
+            self.vc = torch.zeros_like(self.kc)
+            self.ks = torch.zeros((N, 16), dtype=torch.float32, device=device)
+            self.vs = torch.zeros_like(self.ks)
+            ops.cache_write(w.k_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(device),
+                            w.v_pool.permute(0, 2, 1, 3).reshape(N * 16, H, D).contiguous().to(device),
+                            torch.arange(N * 16, dtype=torch.int64, device=device), self.kc, self.vc, self.ks,
+                            self.vs)
+        else:
+            self.kc, self.vc = w.k_pool.to(device), w.v_pool.to(device)
         self.q = w.q.to(device)
         self.new_k, self.new_v = new_k.to(device), new_v.to(device)
         self.h_q, self.h_k, self.h_v = w.q.pin_memory(), new_k.pin_memory(), new_v.pin_memory()
@@ -883,17 +898,17 @@ class PrefillStep:
                                                                      C.byref(desc), split_tokens))
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
         self.bytes, self.flops = prefill_cost(w)
-        self.write_bytes = 2 * w.T * w.Hkv * w.D * 2 * 2 + w.T * 8
+        self.write_bytes = 2 * w.T * w.Hkv * w.D * (2 + (1 if self.q8 else 2)) + w.T * (16 if self.q8 else 8)
 
     def enqueue(self, stream, ev=None, q=None, k=None, v=None):
         ops = self.ops
         ops.cache_write(k if k is not None else self.new_k, v if v is not None else self.new_v, self.slots,
-                        self.kc, self.vc, stream=stream)
+                        self.kc, self.vc, self.ks, self.vs, stream=stream)
         if ev is not None:
             ev[0].record(stream)
         ops.chunked_prefill(q if q is not None else self.q, self.q_start, self.kc, self.vc, self.tables,
                             self.lens, self.max_len, self.max_q, self.w.scale, out=self.out, workspace=self.ws,
-                            split_tokens=self.split, stream=stream)
+                            split_tokens=self.split, stream=stream, k_scale=self.ks, v_scale=self.vs)
         if ev is not None:
             ev[1].record(stream)
 
@@ -903,14 +918,30 @@ class PrefillStep:
 
 def _prefill_oracle_task(task):
     from oracle.attention import paged_prefill
-    q, qs, kb, vb, L, scale = task
+    q, qs, kb, vb, L, scale, kvs = task
     tab = np.arange(kb.shape[0], dtype=np.int64)[None, :]
-    paged_prefill(q, qs, kb, vb, tab, np.array([L]), scale)
+    paged_prefill(q, qs, kb, vb, tab, np.array([L]), scale,
+                  k_scale=kvs[0] if kvs else None, v_scale=kvs[1] if kvs else None)
     return L
 
 
-def prefill_oracle_tasks(w):
-    """Per-sequence oracle inputs (that sequence's blocks and query tokens)."""
+def _quantise_prefill_task(task):
+    """A task's f16 context blocks as 1-byte codes + per-token scales, by the
+    oracle's quantiser (the cache write of an FP8 / INT8 cache)."""
+    from oracle.cache_ops import quantize_rows
+    q, qs, kb, vb, L, scale, fmt = task
+    N, H, _, D = kb.shape
+    cdt = np.int8 if fmt == "int8" else np.uint8
+    out = []
+    for blk in (kb, vb):
+        c, s = quantize_rows(blk.transpose(0, 2, 1, 3).reshape(N * 16, H, D), cdt)
+        out.append((c.reshape(N, 16, H, D).transpose(0, 2, 1, 3).copy(), s.reshape(N, 16)))
+    return (q, qs, out[0][0], out[1][0], L, scale, (out[0][1], out[1][1]))
+
+
+def prefill_oracle_tasks(w, codes=None):
+    """Per-sequence oracle inputs (that sequence's blocks and query tokens);
+    codes = (k codes, v codes, k scales, v scales) for a 1-byte cache."""
     from paged_kv_cache_191_gb300.workloads import BLOCK
     tasks, per = [], []
     qs = w.q_start
@@ -918,9 +949,14 @@ def prefill_oracle_tasks(w):
         L, n = int(w.context_lens[b]), int(w.q_lens[b])
         blocks = w.block_tables[b][: -(-L // BLOCK)]
         f = (lambda t: t.float().numpy() if str(t.dtype) == "torch.bfloat16" else t.numpy())
-        tasks.append((f(w.q[qs[b]:qs[b + 1]]), [0, n], f(w.k_pool[blocks]), f(w.v_pool[blocks]), L, w.scale))
+        if codes is not None:
+            kb, vb, kvs = codes[0][blocks], codes[1][blocks], (codes[2][blocks], codes[3][blocks])
+        else:
+            kb, vb, kvs = f(w.k_pool[blocks]), f(w.v_pool[blocks]), None
+        tasks.append((f(w.q[qs[b]:qs[b + 1]]), [0, n], kb, vb, L, w.scale, kvs))
         sub = type("S", (), {})()
         sub.context_lens, sub.q_lens, sub.Hkv, sub.Hq, sub.D, sub.T = [L], [n], w.Hkv, w.Hq, w.D, n
+        sub.kv_dtype = w.kv_dtype
         per.append(prefill_cost(sub)[0])
     return tasks, per
 
@@ -985,7 +1021,8 @@ def run_prefill(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        tasks, per = prefill_oracle_tasks(w)
+        tasks, per = prefill_oracle_tasks(w, (st.kc.cpu().numpy(), st.vc.cpu().numpy(), st.ks.cpu().numpy(),
+                                              st.vs.cpu().numpy()) if st.q8 else None)
         cores = cpu_cores()
         order = sorted(range(w.B), key=lambda b: -int(w.q_lens[b]) * int(w.context_lens[b]))
         with _pool(cores) as pool:
@@ -1292,6 +1329,8 @@ def run_reference_prefill(args, world):
     cores = cpu_cores()
     budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step
     with _pool(cores) as pool:
+        if w.kv_dtype in ("fp8", "int8"):  # the cache's codes and scales (set-up, not timed)
+            tasks = pool.map(_quantise_prefill_task, [t[:6] + (w.kv_dtype,) for t in tasks], chunksize=1)
         t = time.perf_counter()
         pool.map(_prefill_oracle_task, tasks[:cores], chunksize=1)
         per_task = (time.perf_counter() - t) / max(1, min(cores, len(tasks))) * cores

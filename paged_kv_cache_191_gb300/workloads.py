@@ -248,7 +248,7 @@ def make_prefill(name, seed, Hq, Hkv, D, kv_dtype, ctx_lens, q_lens, pool_factor
     order = rng.permutation(num_blocks).astype(np.int64)
     mb = max(1, max(-(-int(n) // BLOCK) for n in lens))
     tables = _tables_from_order(order, lens, mb)
-    tdt = KV_TORCH[kv_dtype]
+    tdt = KV_TORCH.get(kv_dtype, torch.float16)  # 1-byte caches: f16 values, quantised on the device
     q = randn(rng, (int(ql.sum()), Hq, D), tdt)
     k_pool = randn(rng, (num_blocks, Hkv, BLOCK, D), tdt)
     v_pool = randn(rng, (num_blocks, Hkv, BLOCK, D), tdt)
@@ -256,16 +256,18 @@ def make_prefill(name, seed, Hq, Hkv, D, kv_dtype, ctx_lens, q_lens, pool_factor
                            k_pool, v_pool, 1.0 / math.sqrt(D))
 
 
-def config_prefill_mix(chunks=4, chunk=512, decodes=28):
+def config_prefill_mix(chunks=4, chunk=512, decodes=28, kv="f16"):
     """LLaMA-7B shapes (32/32 heads, D=128, fp16): `chunks` prompt chunks of
     `chunk` tokens at prior contexts uniform in [0, 4096 - chunk], batched with
-    `decodes` one-token decode steps at contexts uniform in [1, 2048]."""
+    `decodes` one-token decode steps at contexts uniform in [1, 2048].  kv
+    "fp8" / "int8": the same values in a 1-byte cache (f16 queries)."""
     rng = rng_for(SEED_BASE + 6)
     prior = rng.integers(0, 4096 - chunk, size=chunks, endpoint=True)
     dec = rng.integers(1, 2048, size=decodes, endpoint=True)
     ctx = np.concatenate([prior + chunk, dec])
     ql = np.concatenate([np.full(chunks, chunk), np.ones(decodes, dtype=np.int64)])
-    return make_prefill("prefill_mix_llama7b", SEED_BASE + 6 + 100, 32, 32, 128, "f16", ctx, ql)
+    name = "prefill_mix_llama7b" + ("" if kv == "f16" else "_" + kv)
+    return make_prefill(name, SEED_BASE + 6 + 100, 32, 32, 128, kv, ctx, ql)
 
 
 def config_spec_verify(B=64, gamma=4):
@@ -336,6 +338,7 @@ def serving_llama7b():
 
 PREFILL_CONFIGS = {
     "prefill_mix_llama7b": config_prefill_mix,
+    "prefill_mix_llama7b_fp8": lambda: config_prefill_mix(kv="fp8"),
     "spec_verify_gqa70b": config_spec_verify,
 }
 
