@@ -318,180 +318,196 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
       }
       const int tok0 = (j0 + i) * 16;
       if (tok0 <= last_pos) {
-        const uint32_t kb = ring + s * 2 * TL::TB, vb = kb + TL::TB;
-        // ---- S = Q . K^T over this block's 16 tokens (two 8-token tiles) -----
-        // even and odd k-steps accumulate separately: four independent MMA
-        // chains instead of two, summed once
-        float sc[2][4], sd[2][4];
+        // The block holding the context's end (its rows past the end may
+        // hold stale bytes, NaN included) runs a copy of the body that masks
+        // them out of P . V; every other block runs the copy without masks.
+        auto block = [&](auto tail_c) {
+          constexpr bool TAIL = decltype(tail_c)::value;
+          const uint32_t kb = ring + s * 2 * TL::TB, vb = kb + TL::TB;
+          // ---- S = Q . K^T over this block's 16 tokens (two 8-token tiles) -----
+          // even and odd k-steps accumulate separately: four independent MMA
+          // chains instead of two, summed once
+          float sc[2][4], sd[2][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sc[0][k] = sc[1][k] = sd[0][k] = sd[1][k] = 0.f;
-        if constexpr (Q8) {
-          // key rows r (tile 0) and r + 8 (tile 1): bytes 32 q4 .. 32 q4 + 31
-          const uint4 x0 = dev::lds128(kb + swz(r, 2 * q4)), x1 = dev::lds128(kb + swz(r, 2 * q4 + 1));
-          const uint4 y0 = dev::lds128(kb + swz(r + 8, 2 * q4)), y1 = dev::lds128(kb + swz(r + 8, 2 * q4 + 1));
-          const uint32_t wx[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          const uint32_t wy[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+          for (int k = 0; k < 4; ++k) sc[0][k] = sc[1][k] = sd[0][k] = sd[1][k] = 0.f;
+          if constexpr (Q8) {
+            // key rows r (tile 0) and r + 8 (tile 1): bytes 32 q4 .. 32 q4 + 31
+            const uint4 x0 = dev::lds128(kb + swz(r, 2 * q4)), x1 = dev::lds128(kb + swz(r, 2 * q4 + 1));
+            const uint4 y0 = dev::lds128(kb + swz(r + 8, 2 * q4)), y1 = dev::lds128(kb + swz(r + 8, 2 * q4 + 1));
+            const uint32_t wx[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const uint32_t wy[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-          for (int kk = 0; kk < KSTEPS; ++kk) {
-            float(&acc0)[4] = (kk & 1) ? sd[0] : sc[0];
-            float(&acc1)[4] = (kk & 1) ? sd[1] : sc[1];
-            dev::Mma<T>::run(acc0, qf[kk], dev::code8x2_to<KT, T>(static_cast<uint16_t>(wx[kk] & 0xffffu)),
-                             dev::code8x2_to<KT, T>(static_cast<uint16_t>(wx[kk] >> 16)));
-            dev::Mma<T>::run(acc1, qf[kk], dev::code8x2_to<KT, T>(static_cast<uint16_t>(wy[kk] & 0xffffu)),
-                             dev::code8x2_to<KT, T>(static_cast<uint16_t>(wy[kk] >> 16)));
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+              float(&acc0)[4] = (kk & 1) ? sd[0] : sc[0];
+              float(&acc1)[4] = (kk & 1) ? sd[1] : sc[1];
+              dev::Mma<T>::run(acc0, qf[kk], dev::code8x2_to<KT, T>(static_cast<uint16_t>(wx[kk] & 0xffffu)),
+                               dev::code8x2_to<KT, T>(static_cast<uint16_t>(wx[kk] >> 16)));
+              dev::Mma<T>::run(acc1, qf[kk], dev::code8x2_to<KT, T>(static_cast<uint16_t>(wy[kk] & 0xffffu)),
+                               dev::code8x2_to<KT, T>(static_cast<uint16_t>(wy[kk] >> 16)));
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+              uint32_t kf[4];
+              dev::ldmatrix_x4(kf, kb + swz(krow, 2 * kk + kcol));
+              float(&acc0)[4] = (kk & 1) ? sd[0] : sc[0];
+              float(&acc1)[4] = (kk & 1) ? sd[1] : sc[1];
+              dev::Mma<T>::run(acc0, qf[kk], kf[0], kf[1]);
+              dev::Mma<T>::run(acc1, qf[kk], kf[2], kf[3]);
+            }
           }
-        } else {
 #pragma unroll
-          for (int kk = 0; kk < KSTEPS; ++kk) {
-            uint32_t kf[4];
-            dev::ldmatrix_x4(kf, kb + swz(krow, 2 * kk + kcol));
-            float(&acc0)[4] = (kk & 1) ? sd[0] : sc[0];
-            float(&acc1)[4] = (kk & 1) ? sd[1] : sc[1];
-            dev::Mma<T>::run(acc0, qf[kk], kf[0], kf[1]);
-            dev::Mma<T>::run(acc1, qf[kk], kf[2], kf[3]);
+          for (int k = 0; k < 4; ++k) {
+            sc[0][k] += sd[0][k];
+            sc[1][k] += sd[1][k];
           }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          sc[0][k] += sd[0][k];
-          sc[1][k] += sd[1][k];
-        }
-        // ---- causal / length mask, online softmax ------------------------------
-        float x[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int t = tok0 + nt * 8 + 2 * q4 + e;
-            const float c = Q8 ? sl2 * s_scale[s * 32 + nt * 8 + 2 * q4 + e] : sl2;  // K scale of token t
-            x[nt][e] = t <= posA ? sc[nt][e] * c : -INFINITY;
-            x[nt][2 + e] = t <= posB ? sc[nt][2 + e] * c : -INFINITY;
-          }
-        float bA = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-        float bB = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-        bA = fmaxf(bA, __shfl_xor_sync(FULL, bA, 1));
-        bB = fmaxf(bB, __shfl_xor_sync(FULL, bB, 1));
-        bA = fmaxf(bA, __shfl_xor_sync(FULL, bA, 2));
-        bB = fmaxf(bB, __shfl_xor_sync(FULL, bB, 2));
-        const float nA = fmaxf(mA, bA), nB = fmaxf(mB, bB);
-        // a row without any key so far keeps m = -inf; its weights are 0
-        const float zA = nA == -INFINITY ? 0.f : nA, zB = nB == -INFINITY ? 0.f : nB;
-        const float alA = exp2f(mA - zA), alB = exp2f(mB - zB);
-        mA = nA;
-        mB = nB;
-        float pv[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          pv[nt][0] = exp2f(x[nt][0] - zA);
-          pv[nt][1] = exp2f(x[nt][1] - zA);
-          pv[nt][2] = exp2f(x[nt][2] - zB);
-          pv[nt][3] = exp2f(x[nt][3] - zB);
-        }
-        if constexpr (Q8) {
-          // l sums the weights; V's per-token scale rides on p (0 past the
-          // context, where a stale scale may be NaN)
-          lA = lA * alA + (pv[0][0] + pv[0][1] + pv[1][0] + pv[1][1]);
-          lB = lB * alB + (pv[0][2] + pv[0][3] + pv[1][2] + pv[1][3]);
+          // ---- causal / length mask, online softmax ------------------------------
+          float x[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int tt = nt * 8 + 2 * q4 + e;
-              const float vs = tok0 + tt < sv.L ? s_scale[s * 32 + 16 + tt] : 0.f;
-              pv[nt][e] *= vs;
-              pv[nt][2 + e] *= vs;
+              const int t = tok0 + nt * 8 + 2 * q4 + e;
+              const float c = Q8 ? sl2 * s_scale[s * 32 + nt * 8 + 2 * q4 + e] : sl2;  // K scale of token t
+              x[nt][e] = t <= posA ? sc[nt][e] * c : -INFINITY;
+              x[nt][2 + e] = t <= posB ? sc[nt][2 + e] * c : -INFINITY;
             }
-        }
-        // P as the A operand: rows r / r + 8, tokens 2q4.. of each 8-token tile
-        uint32_t ph[4], pl[4] = {0u, 0u, 0u, 0u};
-        ph[0] = dev::pack2<T>(pv[0][0], pv[0][1]);
-        ph[1] = dev::pack2<T>(pv[0][2], pv[0][3]);
-        ph[2] = dev::pack2<T>(pv[1][0], pv[1][1]);
-        ph[3] = dev::pack2<T>(pv[1][2], pv[1][3]);
-        if constexpr (SPLIT_P) {
+          float bA = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+          float bB = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+          bA = fmaxf(bA, __shfl_xor_sync(FULL, bA, 1));
+          bB = fmaxf(bB, __shfl_xor_sync(FULL, bB, 1));
+          bA = fmaxf(bA, __shfl_xor_sync(FULL, bA, 2));
+          bB = fmaxf(bB, __shfl_xor_sync(FULL, bB, 2));
+          const float nA = fmaxf(mA, bA), nB = fmaxf(mB, bB);
+          // a row without any key so far keeps m = -inf; its weights are 0
+          const float zA = nA == -INFINITY ? 0.f : nA, zB = nB == -INFINITY ? 0.f : nB;
+          const float alA = exp2f(mA - zA), alB = exp2f(mB - zB);
+          mA = nA;
+          mB = nB;
+          float pv[2][4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 h = dev::unpack2<T>(ph[k]);
-            const int nt = k >> 1, e = (k & 1) * 2;
-            pl[k] = dev::pack2<T>(pv[nt][e] - h.x, pv[nt][e + 1] - h.y);
+          for (int nt = 0; nt < 2; ++nt) {
+            pv[nt][0] = exp2f(x[nt][0] - zA);
+            pv[nt][1] = exp2f(x[nt][1] - zA);
+            pv[nt][2] = exp2f(x[nt][2] - zB);
+            pv[nt][3] = exp2f(x[nt][3] - zB);
           }
-          if constexpr (!Q8) {
+          if constexpr (Q8) {
+            // l sums the weights; V's per-token scale rides on p (0 past the
+            // context, where a stale scale may be NaN)
             lA = lA * alA + (pv[0][0] + pv[0][1] + pv[1][0] + pv[1][1]);
             lB = lB * alB + (pv[0][2] + pv[0][3] + pv[1][2] + pv[1][3]);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int tt = nt * 8 + 2 * q4 + e;
+                const float vs = tok0 + tt < sv.L ? s_scale[s * 32 + 16 + tt] : 0.f;
+                pv[nt][e] *= vs;
+                pv[nt][2 + e] *= vs;
+              }
           }
-        } else if constexpr (!Q8) {
-          // normalise with the rounded weights the PV product uses
-          const float2 h0 = dev::unpack2<T>(ph[0]), h1 = dev::unpack2<T>(ph[1]);
-          const float2 h2 = dev::unpack2<T>(ph[2]), h3 = dev::unpack2<T>(ph[3]);
-          lA = lA * alA + (h0.x + h0.y + h2.x + h2.y);
-          lB = lB * alB + (h1.x + h1.y + h3.x + h3.y);
-        }
-        // ---- O = O * alpha + P . V ---------------------------------------------
-        // V rows past the context get weight 0, but 0 * NaN is NaN: masks for
-        // the halves of tokens past it (b0b1: tokens 2q4, 2q4+1; b2b3: +8)
-        uint32_t m0 = 0xFFFFFFFFu, m8 = 0xFFFFFFFFu;
-        uint32_t m0x = 0xFFFFFFFFu, m0y = 0xFFFFFFFFu, m8x = 0xFFFFFFFFu, m8y = 0xFFFFFFFFu;  // 1-byte rows
-        if (tok0 + 16 > sv.L) {
-          const int t0 = tok0 + 2 * q4;
-          m0 = (t0 < sv.L ? 0xFFFFu : 0u) | (t0 + 1 < sv.L ? 0xFFFF0000u : 0u);
-          m8 = (t0 + 8 < sv.L ? 0xFFFFu : 0u) | (t0 + 9 < sv.L ? 0xFFFF0000u : 0u);
-          m0x = t0 < sv.L ? 0xFFFFFFFFu : 0u;
-          m0y = t0 + 1 < sv.L ? 0xFFFFFFFFu : 0u;
-          m8x = t0 + 8 < sv.L ? 0xFFFFFFFFu : 0u;
-          m8y = t0 + 9 < sv.L ? 0xFFFFFFFFu : 0u;
-        }
-        if constexpr (Q8) {
-          // Column tile 4 mm + c holds, in this lane's column slot, dim
-          // 4 (r + 8 mm) + c: one word at that offset from each of the lane's
-          // token rows 2q4, 2q4+1 (first B register) and 2q4+8, 2q4+9 (second)
+          // P as the A operand: rows r / r + 8, tokens 2q4.. of each 8-token tile
+          uint32_t ph[4], pl[4] = {0u, 0u, 0u, 0u};
+          ph[0] = dev::pack2<T>(pv[0][0], pv[0][1]);
+          ph[1] = dev::pack2<T>(pv[0][2], pv[0][3]);
+          ph[2] = dev::pack2<T>(pv[1][0], pv[1][1]);
+          ph[3] = dev::pack2<T>(pv[1][2], pv[1][3]);
+          if constexpr (SPLIT_P) {
 #pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            const uint32_t off = 4u * static_cast<uint32_t>(r & 3);
-            const int ch = (r >> 2) + 2 * mm;
-            const uint32_t X = dev::lds32(vb + swz(2 * q4, ch) + off) & m0x;
-            const uint32_t Y = dev::lds32(vb + swz(2 * q4 + 1, ch) + off) & m0y;
-            const uint32_t Z = dev::lds32(vb + swz(2 * q4 + 8, ch) + off) & m8x;
-            const uint32_t W = dev::lds32(vb + swz(2 * q4 + 9, ch) + off) & m8y;
+            for (int k = 0; k < 4; ++k) {
+              const float2 h = dev::unpack2<T>(ph[k]);
+              const int nt = k >> 1, e = (k & 1) * 2;
+              pl[k] = dev::pack2<T>(pv[nt][e] - h.x, pv[nt][e + 1] - h.y);
+            }
+            if constexpr (!Q8) {
+              lA = lA * alA + (pv[0][0] + pv[0][1] + pv[1][0] + pv[1][1]);
+              lB = lB * alB + (pv[0][2] + pv[0][3] + pv[1][2] + pv[1][3]);
+            }
+          } else if constexpr (!Q8) {
+            // normalise with the rounded weights the PV product uses
+            const float2 h0 = dev::unpack2<T>(ph[0]), h1 = dev::unpack2<T>(ph[1]);
+            const float2 h2 = dev::unpack2<T>(ph[2]), h3 = dev::unpack2<T>(ph[3]);
+            lA = lA * alA + (h0.x + h0.y + h2.x + h2.y);
+            lB = lB * alB + (h1.x + h1.y + h3.x + h3.y);
+          }
+          // ---- O = O * alpha + P . V ---------------------------------------------
+          // V rows past the context get weight 0, but 0 * NaN is NaN: masks for
+          // the halves of tokens past it (b0b1: tokens 2q4, 2q4+1; b2b3: +8)
+          uint32_t m0 = 0xFFFFFFFFu, m8 = 0xFFFFFFFFu;
+          uint32_t m0x = 0xFFFFFFFFu, m0y = 0xFFFFFFFFu, m8x = 0xFFFFFFFFu, m8y = 0xFFFFFFFFu;  // 1-byte rows
+          if constexpr (TAIL) {
+            const int t0 = tok0 + 2 * q4;
+            m0 = (t0 < sv.L ? 0xFFFFu : 0u) | (t0 + 1 < sv.L ? 0xFFFF0000u : 0u);
+            m8 = (t0 + 8 < sv.L ? 0xFFFFu : 0u) | (t0 + 9 < sv.L ? 0xFFFF0000u : 0u);
+            m0x = t0 < sv.L ? 0xFFFFFFFFu : 0u;
+            m0y = t0 + 1 < sv.L ? 0xFFFFFFFFu : 0u;
+            m8x = t0 + 8 < sv.L ? 0xFFFFFFFFu : 0u;
+            m8y = t0 + 9 < sv.L ? 0xFFFFFFFFu : 0u;
+          }
+          if constexpr (Q8) {
+            // Column tile 4 mm + c holds, in this lane's column slot, dim
+            // 4 (r + 8 mm) + c: one word at that offset from each of the lane's
+            // token rows 2q4, 2q4+1 (first B register) and 2q4+8, 2q4+9 (second)
 #pragma unroll
-            for (int cp = 0; cp < 2; ++cp) {  // dims c = 2 cp, 2 cp + 1
-              const uint32_t sel = cp ? 0x7362u : 0x5140u;
-              const uint32_t xy = dev::prmt(X, Y, sel), zw = dev::prmt(Z, W, sel);
+            for (int mm = 0; mm < 4; ++mm) {
+              const uint32_t off = 4u * static_cast<uint32_t>(r & 3);
+              const int ch = (r >> 2) + 2 * mm;
+              uint32_t X = dev::lds32(vb + swz(2 * q4, ch) + off), Y = dev::lds32(vb + swz(2 * q4 + 1, ch) + off);
+              uint32_t Z = dev::lds32(vb + swz(2 * q4 + 8, ch) + off), W = dev::lds32(vb + swz(2 * q4 + 9, ch) + off);
+              if constexpr (TAIL) {
+                X &= m0x;
+                Y &= m0y;
+                Z &= m8x;
+                W &= m8y;
+              }
+#pragma unroll
+              for (int cp = 0; cp < 2; ++cp) {  // dims c = 2 cp, 2 cp + 1
+                const uint32_t sel = cp ? 0x7362u : 0x5140u;
+                const uint32_t xy = dev::prmt(X, Y, sel), zw = dev::prmt(Z, W, sel);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int ct = 4 * mm + 2 * cp + h;
+                  const uint32_t b0 = dev::code8x2_to<KT, T>(static_cast<uint16_t>(h ? xy >> 16 : xy & 0xffffu));
+                  const uint32_t b1 = dev::code8x2_to<KT, T>(static_cast<uint16_t>(h ? zw >> 16 : zw & 0xffffu));
+                  float* oo = o[ct];
+                  oo[0] *= alA;
+                  oo[1] *= alA;
+                  oo[2] *= alB;
+                  oo[3] *= alB;
+                  dev::Mma<T>::run(o[ct], ph, b0, b1);
+                  if constexpr (SPLIT_P) dev::Mma<T>::run(o[ct], pl, b0, b1);
+                }
+              }
+            }
+          } else {
+#pragma unroll
+            for (int t2 = 0; t2 < D / 16; ++t2) {
+              uint32_t vf[4];
+              dev::ldmatrix_x4_trans(vf, vb + swz(vrow, 2 * t2 + vcol));
+              if constexpr (TAIL) {
+                vf[0] &= m0;
+                vf[1] &= m8;
+                vf[2] &= m0;
+                vf[3] &= m8;
+              }
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
-                const int ct = 4 * mm + 2 * cp + h;
-                const uint32_t b0 = dev::code8x2_to<KT, T>(static_cast<uint16_t>(h ? xy >> 16 : xy & 0xffffu));
-                const uint32_t b1 = dev::code8x2_to<KT, T>(static_cast<uint16_t>(h ? zw >> 16 : zw & 0xffffu));
-                float* oo = o[ct];
+                float* oo = o[2 * t2 + h];
                 oo[0] *= alA;
                 oo[1] *= alA;
                 oo[2] *= alB;
                 oo[3] *= alB;
-                dev::Mma<T>::run(o[ct], ph, b0, b1);
-                if constexpr (SPLIT_P) dev::Mma<T>::run(o[ct], pl, b0, b1);
+                dev::Mma<T>::run(o[2 * t2 + h], ph, vf[2 * h], vf[2 * h + 1]);
+                if constexpr (SPLIT_P) dev::Mma<T>::run(o[2 * t2 + h], pl, vf[2 * h], vf[2 * h + 1]);
               }
             }
           }
-        } else {
-#pragma unroll
-          for (int t2 = 0; t2 < D / 16; ++t2) {
-            uint32_t vf[4];
-            dev::ldmatrix_x4_trans(vf, vb + swz(vrow, 2 * t2 + vcol));
-            vf[0] &= m0;
-            vf[1] &= m8;
-            vf[2] &= m0;
-            vf[3] &= m8;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              float* oo = o[2 * t2 + h];
-              oo[0] *= alA;
-              oo[1] *= alA;
-              oo[2] *= alB;
-              oo[3] *= alB;
-              dev::Mma<T>::run(o[2 * t2 + h], ph, vf[2 * h], vf[2 * h + 1]);
-              if constexpr (SPLIT_P) dev::Mma<T>::run(o[2 * t2 + h], pl, vf[2 * h], vf[2 * h + 1]);
-            }
-          }
-        }
+        };
+        if (tok0 + 16 > sv.L)
+          block(std::true_type{});
+        else
+          block(std::false_type{});
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);  // stage s may be refilled
