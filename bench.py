@@ -680,6 +680,8 @@ def run_ours(args, rank, world, local_rank):
     _, tot_tokens = aggregate(local_s, float(st.B * args.steps), world)
 
     # e2e: public Python API, host (pinned) inputs in, result out, every step
+    dec_list = [st.drv.elapsed_ms(a, b) for a, b in dec_events]
+    timing = timing_detail(st, stream, dec_list) if not shared else {"per_launch_ms": pct(dec_list)}
     e2e = run_e2e(st, args, stream)
     swap = measure_swap(st, stream)
     cpu = None
@@ -729,6 +731,7 @@ def run_ours(args, rank, world, local_rank):
                      "kernel": ("pa_decode_append (decode_main with the fused cache write + decode_reduce)"
                                 if st.fused else "pa_decode (decode_main + decode_reduce)"),
                      "bytes_per_launch": int(avg_dec_bytes), "launch_ms": round(dec_ms, 5)},
+        "timing": timing,
         "e2e": e2e,
         "swap": swap,
         "gpu_launches": st.launches_per_step() * args.steps,
@@ -739,10 +742,66 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(res), flush=True)
 
 
+def pct(xs):
+    xs = np.asarray(xs, dtype=np.float64)
+    return {"median": round(float(np.median(xs)), 5), "p10": round(float(np.percentile(xs, 10)), 5),
+            "p90": round(float(np.percentile(xs, 90)), 5), "n": int(len(xs))}
+
+
+def timing_detail(st, stream, dec_ms, reps=100):
+    """The decode launch timed three more ways, on the last step's inputs
+    (the fused write rewrites the same slots, so every rep is the same work):
+    after an L2 flush (a 2 x L2 buffer written between reps, outside the
+    events), back to back on the stream, and replayed from a CUDA graph."""
+    torch = st.torch
+    L, drv, sp = st.L, st.drv, st.sp
+    args = st.append_args[st.dbuf ^ 1] if st.fused else st.decode_args[st.dbuf ^ 1]
+    fn = L.pa_decode_append if st.fused else L.pa_decode
+    out = {"per_launch_ms": pct(dec_ms)}
+    l2 = int(getattr(torch.cuda.get_device_properties(st.dev), "L2_cache_size", 128 << 20))
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=st.dev)
+    evs = [(drv.event(True), drv.event(True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        stream.synchronize()
+        for a, b in evs:
+            flush.zero_()
+            drv.record(a, sp)
+            st.ops._check(fn(*args), "decode")
+            drv.record(b, sp)
+        stream.synchronize()
+        out["l2_flushed_ms"] = dict(pct([drv.elapsed_ms(a, b) for a, b in evs]), flush_bytes=2 * l2)
+        t0, t1 = drv.event(True), drv.event(True)
+        drv.record(t0, sp)
+        for _ in range(reps):
+            st.ops._check(fn(*args), "decode")
+        drv.record(t1, sp)
+        stream.synchronize()
+        out["stream_ms_per_launch"] = round(drv.elapsed_ms(t0, t1) / reps, 5)
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            st.ops._check(fn(*args), "decode")
+        with torch.cuda.stream(stream):
+            g.replay()
+            stream.synchronize()
+            drv.record(t0, sp)
+            for _ in range(reps):
+                g.replay()
+            drv.record(t1, sp)
+            stream.synchronize()
+        out["graph_ms_per_launch"] = round(drv.elapsed_ms(t0, t1) / reps, 5)
+    except Exception as e:  # reported, not fatal: the graph figure is supplementary
+        out["graph_ms_per_launch"] = None
+        out["graph_error"] = str(e)[:200]
+    del flush
+    return out
+
+
 def measure_swap(st, stream, n_seqs=8, reps=5):
     """Preemption traffic: the blocks of n_seqs sequences to a pinned host pool
     and back (pa_swap_blocks, one gather launch per direction), event-timed."""
     import torch
+    n_seqs = min(n_seqs, st.B)
     ids = [int(x) for x in (st.ids[:n_seqs] if hasattr(st, "ids") and not isinstance(st.ids, list)
                             else list(range(n_seqs)))]
     tables, lens = st.alloc.tables(ids, st.cap)
