@@ -61,6 +61,8 @@ def parse_args(argv=None):
     p.add_argument("--unfused", action="store_true",
                    help="pa_cache_write + pa_decode instead of the fused pa_decode_append")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--ungrouped", action="store_true",
+                   help="shared_prefix_16x4: read shared prompt blocks once per beam (pa_decode_append)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args(argv)
 
@@ -467,7 +469,13 @@ class SharedPrefixStep(DecodeStep):
         self.out = torch.empty((self.B, self.Hq, self.D), dtype=w.q.dtype, device=device)
         self.desc = ops.cache_desc(self.kc)
         self.ws_bytes = ops.decode_workspace_size(self.B, self.Hq, self.max_len, self.kc, split_tokens)
-        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        # shared-prefix groups: each group's beams share the prompt's blocks
+        self.grouped = True
+        self.group_start = torch.arange(0, self.B + 1, w.beams, dtype=torch.int32, device=device)
+        self.prefix_blocks = torch.full((w.groups,), w.prompt_len // 16, dtype=torch.int32, device=device)
+        gws = int(self.L.pa_decode_grouped_workspace_size(self.B, self.Hq, self.max_len, w.groups, w.beams,
+                                                          w.prompt_len // 16, C.byref(self.desc), split_tokens))
+        self.ws = torch.empty(max(self.ws_bytes, gws, 16), dtype=torch.uint8, device=device)
         self.split = split_tokens
         # meta: slots int64[B] | pairs int64[B, 2] | lens int32[B] | tables int32[B, cap]
         self.meta_bytes = self.B * 8 + self.B * 16 + self.B * 4 + self.B * self.cap * 4
@@ -494,6 +502,14 @@ class SharedPrefixStep(DecodeStep):
         self.pairs_dev = self.meta_dev[B * 8: B * 24].view(T.int64).view(B, 2)
         self.lens_dev = self.meta_dev[B * 24: B * 28].view(T.int32)
         self.tables_dev = self.meta_dev[B * 28:].view(T.int32).view(B, self.cap)
+
+    def prebuild(self, stream):
+        super().prebuild(stream)
+        w = self.w
+        extra = (C.c_void_p(self.group_start.data_ptr()), C.c_void_p(self.prefix_blocks.data_ptr()), w.groups,
+                 w.beams, w.prompt_len // 16)
+        # pa_decode_append's arguments with the group description after `scale`
+        self.grouped_args = [a[:17] + extra + a[17:] for a in self.append_args]
 
     def _fresh(self, n):
         ids = np.arange(self.next_id, self.next_id + n, dtype=np.uint64)
@@ -559,7 +575,13 @@ class SharedPrefixStep(DecodeStep):
                                   C.byref(self.desc), sp)
             if st:
                 self.ops._check(st, "pa_copy_blocks")
-        if self.fused:
+        if self.fused and self.grouped:
+            if ev_pair is not None:
+                drv.record(ev_pair[0], sp)
+            st = L.pa_decode_append_grouped(*self.grouped_args[i])
+            if st:
+                self.ops._check(st, "pa_decode_append_grouped")
+        elif self.fused:
             if ev_pair is not None:
                 drv.record(ev_pair[0], sp)
             st = L.pa_decode_append(*self.append_args[i])
@@ -636,6 +658,8 @@ def run_ours(args, rank, world, local_rank):
     shared = args.config == "shared_prefix_16x4"
     st = (SharedPrefixStep if shared else DecodeStep)(w, args.split, args.steps + args.warmup, dev)
     st.fused = not args.unfused
+    if shared:
+        st.grouped = not args.ungrouped
     stream = torch.cuda.Stream(device=dev)
     total_steps = args.warmup + args.steps
     st.prebuild(stream)
@@ -712,7 +736,9 @@ def run_ours(args, rank, world, local_rank):
                             f" +1 per step, batch re-admitted every {RESET_EVERY} steps",
             **({"sharing": "16 groups x 4 beams share a 1024-token prompt; beams reselected from "
                            "parents every step (fork + release), copy-on-write before each decode; "
-                           "bytes count shared blocks once (logical bytes reported separately)"}
+                           "bytes count shared blocks once (logical bytes reported separately)",
+                "prompt_reads": ("once per group of 4 beams (pa_decode_append_grouped)"
+                                 if st.fused and st.grouped else "once per beam")}
                if shared else {}),
             "split_tokens": args.split or "auto",
             "l2": f"no flush: K+V per step {avg_dec_bytes / 1e6:.0f} MB vs 129 MB L2",
@@ -728,7 +754,9 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic,
-                     "kernel": ("pa_decode_append (decode_main with the fused cache write + decode_reduce)"
+                     "kernel": ("pa_decode_append_grouped (decode_main over shared-prefix groups with the fused "
+                                "cache write + decode_reduce_grouped)" if shared and st.fused and st.grouped else
+                                "pa_decode_append (decode_main with the fused cache write + decode_reduce)"
                                 if st.fused else "pa_decode (decode_main + decode_reduce)"),
                      "bytes_per_launch": int(avg_dec_bytes), "launch_ms": round(dec_ms, 5)},
         "timing": timing,

@@ -82,6 +82,7 @@ typedef enum {
 #define PA_DEVERR_CONTEXT_LEN  0x4u  /* decode: length < 0 or above a stated bound */
 #define PA_DEVERR_TIMEOUT      0x8u  /* a bounded barrier wait gave up */
 #define PA_DEVERR_QUERY_RANGE  0x10u /* chunked prefill: q_start out of order or range */
+#define PA_DEVERR_GROUP        0x20u /* grouped decode: bad group bounds, or members' shared blocks differ */
 
 /* Shape of a paged KV cache. */
 typedef struct {
@@ -190,6 +191,59 @@ pa_status pa_decode_append(const void* k_new, const void* v_new, int32_t new_dty
                            const pa_cache_desc* desc,
                            void* workspace, size_t workspace_bytes,
                            int32_t split_tokens, void* stream);
+
+/*
+ * pa_decode_grouped_workspace_size -- bytes of device workspace
+ * pa_decode_append_grouped needs for the same arguments (0 on an invalid
+ * argument).
+ */
+size_t pa_decode_grouped_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                                        int32_t n_groups, int32_t max_group_size, int32_t max_prefix_blocks,
+                                        const pa_cache_desc* desc, int32_t split_tokens);
+
+/*
+ * pa_decode_append_grouped -- pa_decode_append for a batch whose sequences
+ * come in groups sharing the leading blocks of their tables: the beams or
+ * samples of one prompt after fork, which share those blocks by reference
+ * count and copy on write ([LLM-INF] 2.2, [KV-CB] 4.2).  The results are
+ * those of pa_decode_append up to float32 summation order.  What changes is
+ * how the shared blocks are read.  One work item per (group, kv head,
+ * partition of the shared prefix) loads each shared K/V tile once and scores
+ * it against the queries of every member of the group; pa_decode_append reads
+ * the tile once per member.  The members' private tails run as ordinary
+ * partitions, and a merge kernel combines each member's prefix and tail
+ * partitions.
+ *
+ * group_start   device int32 [n_groups + 1].  Group k is sequences
+ *               group_start[k] .. group_start[k+1] - 1, with group_start[0] = 0
+ *               and group_start[n_groups] = B.  Every group is non-empty and at
+ *               most max_group_size long; a sequence in no group is a group of
+ *               one.  Bad bounds skip the group and set PA_DEVERR_GROUP.
+ * prefix_blocks device int32 [n_groups]: the number of leading table entries
+ *               every member of group k has in common.  The kernel shares
+ *               E_k = min(prefix_blocks[k], (L_m - 1) / 16 over the members'
+ *               lengths L_m) blocks, so a shared block never holds a member's
+ *               last token, where the fused write lands.  Members whose table
+ *               entries differ within those blocks set PA_DEVERR_GROUP, and
+ *               their rows are then unspecified.
+ * n_groups      number of groups (1 .. B).
+ * max_group_size host bound on group sizes, with
+ *               max_group_size * num_q_heads / num_kv_heads <= 8.
+ * max_prefix_blocks host bound on prefix_blocks; it sizes the grid.
+ * workspace     device, >= pa_decode_grouped_workspace_size bytes.
+ * Other arguments and errors as pa_decode_append.
+ */
+pa_status pa_decode_append_grouped(const void* k_new, const void* v_new, int32_t new_dtype,
+                                   const int64_t* slot_mapping, const void* q, int32_t q_dtype,
+                                   void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, int32_t max_context_len,
+                                   int32_t B, int32_t num_q_heads, float scale,
+                                   const int32_t* group_start, const int32_t* prefix_blocks,
+                                   int32_t n_groups, int32_t max_group_size, int32_t max_prefix_blocks,
+                                   void* out, int32_t out_dtype, const pa_cache_desc* desc,
+                                   void* workspace, size_t workspace_bytes,
+                                   int32_t split_tokens, void* stream);
 
 /*
  * pa_chunked_prefill_workspace_size -- bytes of device workspace

@@ -185,6 +185,38 @@ size_t pa_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_cont
   return plan.workspace_bytes;
 }
 
+// Shared-prefix groups of a grouped decode call (none: n_groups == 0).
+struct Groups {
+  const int32_t* start = nullptr;
+  const int32_t* prefix = nullptr;
+  int32_t n = 0, max_size = 0, max_prefix = 0;
+};
+
+// The grouped grid's partition counts on top of the plain plan: prefix
+// partitions of the longest allowed shared prefix, tail partitions of the
+// longest context; every member's rows are partials.
+static pa_status plan_grouped(int32_t B, int32_t Hq, int32_t max_context_len, const pa_cache_desc* d,
+                              const Groups& gr, pa::DecodePlan* plan) {
+  if (gr.n <= 0 || gr.n > B || gr.max_size <= 0 || gr.max_size > B || gr.max_prefix < 0)
+    return fail(PA_ERR_INVALID, "pa_decode_append_grouped: n_groups, max_group_size or max_prefix_blocks out of range");
+  if (static_cast<int64_t>(gr.max_size) * (Hq / d->num_kv_heads) > 8)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_append_grouped: max_group_size * G above 8 query columns");
+  const int64_t nblk_max = max_context_len <= 0 ? 1 : (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+  const int64_t bpp = plan->blocks_per_part;
+  const int64_t pre = (std::min<int64_t>(gr.max_prefix, nblk_max) + bpp - 1) / bpp;
+  const int64_t tail = (nblk_max + bpp - 1) / bpp;
+  if (pre + static_cast<int64_t>(gr.max_size) * tail > 65535 ||
+      static_cast<int64_t>(gr.n) * d->num_kv_heads * gr.max_size > (int64_t{1} << 31) - 1)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_append_grouped: grid too large");
+  plan->pre_parts = static_cast<int32_t>(pre);
+  plan->tail_parts = static_cast<int32_t>(tail);
+  plan->max_parts = static_cast<int32_t>(pre + tail);
+  const size_t rows = static_cast<size_t>(B) * Hq * plan->max_parts;
+  const size_t bytes = rows * d->head_dim * sizeof(float) + 2 * rows * sizeof(float);
+  plan->workspace_bytes = (bytes + 255) & ~static_cast<size_t>(255);
+  return PA_OK;
+}
+
 static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache, const void* v_cache,
                              const float* k_scale, const float* v_scale, const int32_t* block_tables,
                              int32_t max_blocks_per_seq, const int32_t* context_lens,
@@ -192,7 +224,7 @@ static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache
                              void* out, int32_t out_dtype, const pa_cache_desc* desc, void* workspace,
                              size_t workspace_bytes, int32_t split_tokens, void* stream,
                              const void* k_new, const void* v_new, int32_t new_dtype,
-                             const int64_t* slot_mapping) {
+                             const int64_t* slot_mapping, const Groups& gr = Groups()) {
   pa_status st = pa::check_desc(desc, "pa_decode");
   if (st != PA_OK) return st;
   if (B < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0)
@@ -225,6 +257,13 @@ static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache
   pa::DecodePlan plan;
   st = pa::plan_decode(B, num_q_heads, max_context_len, desc, split_tokens, &plan);
   if (st != PA_OK) return st;
+  if (gr.n > 0) {
+    if (!gr.start || !gr.prefix || (reinterpret_cast<uintptr_t>(gr.start) & 3u) ||
+        (reinterpret_cast<uintptr_t>(gr.prefix) & 3u))
+      return fail(PA_ERR_INVALID, "pa_decode_append_grouped: group_start / prefix_blocks NULL or misaligned");
+    st = plan_grouped(B, num_q_heads, max_context_len, desc, gr, &plan);
+    if (st != PA_OK) return st;
+  }
   if (plan.workspace_bytes) {
     if (!workspace || !pa::aligned16(workspace))
       return fail(PA_ERR_INVALID, "pa_decode: workspace NULL or misaligned (%zu bytes needed)",
@@ -267,6 +306,10 @@ static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache
     a.slot_mapping = slot_mapping;
     a.new_dtype = new_dtype;
   }
+  a.group_start = gr.start;
+  a.prefix_blocks = gr.prefix;
+  a.n_groups = gr.n;
+  a.max_members = gr.max_size;
   return pa::launch_decode(a, stream);
 }
 
@@ -292,6 +335,45 @@ pa_status pa_decode_append(const void* k_new, const void* v_new, int32_t new_dty
   return decode_impl(q, q_dtype, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
                      context_lens, max_context_len, B, num_q_heads, scale, out, out_dtype, desc, workspace,
                      workspace_bytes, split_tokens, stream, k_new, v_new, new_dtype, slot_mapping);
+}
+
+size_t pa_decode_grouped_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                                        int32_t n_groups, int32_t max_group_size, int32_t max_prefix_blocks,
+                                        const pa_cache_desc* desc, int32_t split_tokens) {
+  if (pa::check_desc(desc, "pa_decode_grouped_workspace_size") != PA_OK || B <= 0 || num_q_heads <= 0 ||
+      num_q_heads % desc->num_kv_heads)
+    return 0;
+  pa::DecodePlan plan;
+  if (pa::plan_decode(B, num_q_heads, max_context_len, desc, split_tokens, &plan) != PA_OK) return 0;
+  Groups gr;
+  gr.n = n_groups;
+  gr.max_size = max_group_size;
+  gr.max_prefix = max_prefix_blocks;
+  if (plan_grouped(B, num_q_heads, max_context_len, desc, gr, &plan) != PA_OK) return 0;
+  return plan.workspace_bytes;
+}
+
+pa_status pa_decode_append_grouped(const void* k_new, const void* v_new, int32_t new_dtype,
+                                   const int64_t* slot_mapping, const void* q, int32_t q_dtype, void* k_cache,
+                                   void* v_cache, float* k_scale, float* v_scale, const int32_t* block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                   int32_t max_context_len, int32_t B, int32_t num_q_heads, float scale,
+                                   const int32_t* group_start, const int32_t* prefix_blocks, int32_t n_groups,
+                                   int32_t max_group_size, int32_t max_prefix_blocks, void* out,
+                                   int32_t out_dtype, const pa_cache_desc* desc, void* workspace,
+                                   size_t workspace_bytes, int32_t split_tokens, void* stream) {
+  if (!slot_mapping) return fail(PA_ERR_INVALID, "pa_decode_append_grouped: slot_mapping is NULL");
+  if (B <= 0) return B == 0 ? PA_OK : fail(PA_ERR_INVALID, "pa_decode_append_grouped: B < 0");
+  Groups gr;
+  gr.start = group_start;
+  gr.prefix = prefix_blocks;
+  gr.n = n_groups;
+  gr.max_size = max_group_size;
+  gr.max_prefix = max_prefix_blocks;
+  if (n_groups <= 0) return fail(PA_ERR_INVALID, "pa_decode_append_grouped: n_groups must be > 0");
+  return decode_impl(q, q_dtype, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                     context_lens, max_context_len, B, num_q_heads, scale, out, out_dtype, desc, workspace,
+                     workspace_bytes, split_tokens, stream, k_new, v_new, new_dtype, slot_mapping, gr);
 }
 
 static pa_status check_prefill(int32_t T, int32_t B, int32_t num_q_heads, int32_t max_q_len,

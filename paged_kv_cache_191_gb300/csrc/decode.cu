@@ -77,7 +77,25 @@ struct DecodeArgs {
   float* v_scale_w;
   int32_t new_dtype;
   int32_t fuse_write;
+  // shared-prefix groups (pa_decode_append_grouped), else n_groups == 0:
+  // group k = sequences group_start[k] .. group_start[k+1]-1 sharing their
+  // first prefix_blocks[k] blocks
+  const int32_t* group_start;
+  const int32_t* prefix_blocks;
+  int32_t n_groups, max_members;
+  int32_t pre_parts, tail_parts;  // grid rows: shared-prefix partitions, tail partitions
 };
+
+// A group's usable shared prefix: whole blocks every member has before the
+// block of its last token (so the fused write never lands in a shared
+// block), at most the caller's prefix_blocks.  Lane m < members holds member
+// m's clamped length in `Lm`; every lane gets the result.
+__device__ __forceinline__ int group_prefix(int pre, int members, int Lm, int lane) {
+  int e = lane < members ? (Lm > 0 ? (Lm - 1) >> 4 : 0) : 0x7fffffff;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) e = min(e, __shfl_xor_sync(0xffffffffu, e, o));
+  return max(0, min(pre, e));
+}
 
 // Element i (of a contiguous row) of a K/V input in f16, bf16 or f32, as float.
 __device__ __forceinline__ float load_in(const void* p, size_t i, int dt) {
@@ -209,28 +227,28 @@ __global__ void __launch_bounds__(32 * W)
   // partition): the long sequences' full partitions start early and the
   // short sequences' single small partitions fill in around them, which
   // approximates longest-first scheduling of the items.
-  const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv;
-  const int p = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
-
-  // Launched as a dependent of the preceding kernel (normally the cache
-  // write): everything below may read what it wrote.
-  dev::grid_dependency_wait();
-  const int j0 = p * a.bpp;
-  // The length, this partition's block ids (one or two per lane, read up to
-  // the partition size and the row end before the length is known) and Q are
-  // independent loads, so they share one memory round trip.
-  const int32_t* row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + j0;
-  const int row_left = a.max_blocks - j0;
-  int t0 = (lane < a.bpp && lane < row_left) ? row[lane] : 0;
-  int t1 = (lane + 32 < a.bpp && lane + 32 < row_left) ? row[lane + 32] : 0;
-  // Q as the B operand (k = head dim, n = query head of the group).
+  // Work item.  Plain grid: (sequence b, kv head g, partition p), the G
+  // query heads of (b, g) as MMA columns.  Grouped grid (shared prefixes):
+  // row y < pre_parts is partition pre_parts-1-y of group k's shared prefix,
+  // whose columns are the G heads of every member (members x G <= 8), read
+  // through member 0's table; the other rows are partitions of one member's
+  // tail (blocks after the prefix).  Column c is query head g*G + c % G of
+  // sequence seq0 + c / G.
+  int b, g, p;       // table owner (and fused-write sequence), kv head, partition of its rows
+  int seq0, ncols;   // query columns
+  int j0, L, nb;     // first block, owner's length, blocks of this item
+  bool direct;       // one partition covers the rows: write the output itself
+  bool write_new;    // this item reads the owner's last block (fused write)
   const int r = lane >> 2, q4 = lane & 3;
   uint32_t qf[KSTEPS][2];
-  {
-    const QT* qrow = static_cast<const QT*>(a.q) + (static_cast<size_t>(b) * a.Hq + g * a.G + r) * D;
+  int t0, t1;        // block ids j0 + lane, j0 + 32 + lane
+  auto load_q = [&]() {
+    const int c = r < ncols ? r : 0;
+    const QT* qrow = static_cast<const QT*>(a.q) +
+                     (static_cast<size_t>(seq0 + c / a.G) * a.Hq + g * a.G + c % a.G) * D;
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
-      if (r < a.G) {
+      if (r < ncols) {
         if constexpr (Q8) {  // permuted k order matching the register-converted K fragment
           const uint2 w = *reinterpret_cast<const uint2*>(qrow + 32 * q4 + 4 * kk);
           qf[kk][0] = w.x;
@@ -243,18 +261,96 @@ __global__ void __launch_bounds__(32 * W)
         qf[kk][0] = qf[kk][1] = 0u;
       }
     }
-  }
+  };
+  auto zero_rows = [&](int bz) {  // empty context: zero rows of (bz, g)
+    for (int i = lane; i < a.G * D; i += 32)
+      store_out<QT>(a, (static_cast<size_t>(bz) * a.Hq + g * a.G + i / D) * D + i % D, 0.f);
+  };
 
-  const int L = checked_len(a, b, lane == 0 && p == 0);
-  const int nblk = (L + 15) >> 4;
-  if (j0 >= nblk) {
-    if (p == 0)  // empty context: zero rows
-      for (int i = lane; i < a.G * D; i += 32)
-        store_out<QT>(a, (static_cast<size_t>(b) * a.Hq + g * a.G + i / D) * D + i % D, 0.f);
-    return;
+  // Launched as a dependent of the preceding kernel (normally the cache
+  // write): everything below may read what it wrote.
+  dev::grid_dependency_wait();
+  if (a.n_groups == 0) {
+    b = blockIdx.x / a.Hkv;
+    g = blockIdx.x - b * a.Hkv;
+    p = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+    seq0 = b;
+    ncols = a.G;
+    j0 = p * a.bpp;
+    // The length, this partition's block ids (one or two per lane, read up to
+    // the partition size and the row end before the length is known) and Q
+    // are independent loads, so they share one memory round trip.
+    const int32_t* row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + j0;
+    const int row_left = a.max_blocks - j0;
+    t0 = (lane < a.bpp && lane < row_left) ? row[lane] : 0;
+    t1 = (lane + 32 < a.bpp && lane + 32 < row_left) ? row[lane + 32] : 0;
+    load_q();
+    L = checked_len(a, b, lane == 0 && p == 0);
+    const int nblk = (L + 15) >> 4;
+    if (j0 >= nblk) {
+      if (p == 0) zero_rows(b);
+      return;
+    }
+    nb = min(a.bpp, nblk - j0);
+    direct = (nblk + a.bpp - 1) / a.bpp == 1;
+    write_new = j0 + nb == nblk;
+  } else {
+    const int k = blockIdx.x / a.Hkv, y = static_cast<int>(blockIdx.y);
+    g = blockIdx.x - k * a.Hkv;
+    const int gs0 = a.group_start[k], gs1 = a.group_start[k + 1], pre = a.prefix_blocks[k];
+    const int members = gs1 - gs0;
+    if (gs0 < 0 || members <= 0 || gs1 > a.B || members > a.max_members) {
+      if (lane == 0 && g == 0 && y == 0) atomicOr(&g_decode_err, PA_DEVERR_GROUP);
+      return;
+    }
+    const int Lm = lane < members ? checked_len(a, gs0 + lane, g == 0 && y == a.pre_parts) : 0;
+    const int E = group_prefix(pre, members, Lm, lane);
+    if (y < a.pre_parts) {  // shared prefix
+      p = a.pre_parts - 1 - y;
+      j0 = p * a.bpp;
+      if (j0 >= E) return;
+      nb = min(a.bpp, E - j0);
+      b = gs0;
+      seq0 = gs0;
+      ncols = members * a.G;
+      L = __shfl_sync(FULL, Lm, 0);
+      direct = false;
+      write_new = false;
+      const int32_t* row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + j0;
+      t0 = lane < nb ? row[lane] : 0;
+      t1 = lane + 32 < nb ? row[lane + 32] : 0;
+      load_q();
+      // every member must hold the same blocks here
+      bool differ = false;
+      for (int m = 1; m < members; ++m) {
+        const int32_t* rm = a.block_tables + static_cast<size_t>(gs0 + m) * a.max_blocks + j0;
+        differ |= (lane < nb && rm[lane] != t0) || (lane + 32 < nb && rm[lane + 32] != t1);
+      }
+      if (__any_sync(FULL, differ) && lane == 0) atomicOr(&g_decode_err, PA_DEVERR_GROUP);
+    } else {  // one member's tail
+      const int t = y - a.pre_parts;
+      const int m = t % a.max_members, pt = a.tail_parts - 1 - t / a.max_members;
+      if (m >= members) return;
+      b = gs0 + m;
+      seq0 = b;
+      ncols = a.G;
+      L = __shfl_sync(FULL, Lm, m);
+      const int nblk = (L + 15) >> 4, pp = (E + a.bpp - 1) / a.bpp;
+      j0 = E + pt * a.bpp;
+      if (j0 >= nblk) {
+        if (pt == 0 && L == 0) zero_rows(b);
+        return;
+      }
+      nb = min(a.bpp, nblk - j0);
+      p = pp + pt;
+      direct = pp + (nblk - E + a.bpp - 1) / a.bpp == 1;
+      write_new = j0 + nb == nblk;
+      const int32_t* row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + j0;
+      t0 = lane < nb ? row[lane] : 0;
+      t1 = lane + 32 < nb ? row[lane + 32] : 0;
+      load_q();
+    }
   }
-  const int nb = min(a.bpp, nblk - j0);
-  const int nparts = (nblk + a.bpp - 1) / a.bpp;
   const bool bad = (lane < nb && (t0 < 0 || t0 >= a.num_blocks)) ||
                    (lane + 32 < nb && (t1 < 0 || t1 >= a.num_blocks));
   if (bad) {
@@ -262,7 +358,7 @@ __global__ void __launch_bounds__(32 * W)
     if (t0 < 0 || t0 >= a.num_blocks) t0 = 0;
     if (t1 < 0 || t1 >= a.num_blocks) t1 = 0;
   }
-  if (a.fuse_write && j0 + nb == nblk && wid == 0) {
+  if (a.fuse_write && write_new && wid == 0) {
     // This partition holds the sequence's last token: store the new row of
     // kv head g before any tile of it is read, and make the stores visible
     // to the TMA (async proxy) reads that follow.
@@ -535,7 +631,7 @@ __global__ void __launch_bounds__(32 * W)
       ow[8 * D + 8 + hB] = l1;
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < a.G * D; idx += 32 * W) {
+    for (int idx = threadIdx.x; idx < ncols * D; idx += 32 * W) {
       const int h = idx / D, d = idx - h * D;
       float M = -INFINITY;
 #pragma unroll
@@ -549,8 +645,8 @@ __global__ void __launch_bounds__(32 * W)
         acc += f * ov[h * D + d];
         ls += f * ov[8 * D + 8 + h];
       }
-      const size_t head = static_cast<size_t>(b) * a.Hq + g * a.G + h;
-      if (nparts == 1) {
+      const size_t head = static_cast<size_t>(seq0 + h / a.G) * a.Hq + g * a.G + h % a.G;
+      if (direct) {
         store_out<QT>(a, head * D + d, acc / ls);
       } else {
         const size_t rowp = head * a.max_parts + p;
@@ -563,9 +659,9 @@ __global__ void __launch_bounds__(32 * W)
     }
     return;
   }
-  const size_t headA = static_cast<size_t>(b) * a.Hq + g * a.G + hA;
-  const size_t headB = headA + 1;
-  const bool okA = hA < a.G, okB = hB < a.G;
+  const bool okA = hA < ncols, okB = hB < ncols;
+  const size_t headA = static_cast<size_t>(seq0 + hA / a.G) * a.Hq + g * a.G + hA % a.G;
+  const size_t headB = static_cast<size_t>(seq0 + hB / a.G) * a.Hq + g * a.G + hB % a.G;
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     int d_r, d_r8;
@@ -576,7 +672,7 @@ __global__ void __launch_bounds__(32 * W)
       d_r = 16 * mt + r;
       d_r8 = d_r + 8;
     }
-    if (nparts == 1) {
+    if (direct) {
       if (okA) {
         store_out<QT>(a, headA * D + d_r, o[mt][0] / l0);
         store_out<QT>(a, headA * D + d_r8, o[mt][2] / l0);
@@ -597,7 +693,7 @@ __global__ void __launch_bounds__(32 * W)
       }
     }
   }
-  if (nparts > 1 && lane < 4) {
+  if (!direct && lane < 4) {
     if (okA) {
       a.part_m[headA * a.max_parts + p] = m0;
       a.part_l[headA * a.max_parts + p] = l0;
@@ -609,46 +705,36 @@ __global__ void __launch_bounds__(32 * W)
   }
 }
 
-// Merge the partitions of each (sequence, query head): log-sum-exp weights.
-// One warp per query head, G warps per CTA (one CTA per sequence and kv head).
-// Partitions are taken 16 at a time: lane i holds partition i's (m, l), every
-// lane holds its D/32 dims of the chunk's partial rows, and chunks merge online
-// (running max).  The first chunk's (m, l) are read together with the context
-// length (rows up to max_parts always exist); partial rows are read only for
-// partitions that exist.
+// Merge n partition rows of one query head (rows row0 .. row0 + n - 1) with
+// log-sum-exp weights into output row `orow`.  Partitions are taken 16 at a
+// time: lane i holds partition i's (m, l), every lane holds its D/32 dims of
+// the chunk's partial rows, and chunks merge online (running max).  `mv`, `lv`
+// are the first chunk's (m, l) as the caller loaded them; lanes past n are
+// reset here, so stale scratch never enters a sum.
 template <typename QT, int D>
-__global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce(const DecodeArgs a) {
+__device__ __forceinline__ void merge_rows(const DecodeArgs& a, size_t row0, int n, float mv, float lv,
+                                           size_t orow, int lane) {
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int CH = 16;      // partitions per chunk
   constexpr int V = D / 32;   // dims per lane (4 or 2)
-  const int bg = blockIdx.x, b = bg / a.Hkv, g = bg - b * a.Hkv;
-  const int h = g * a.G + static_cast<int>(threadIdx.x >> 5), lane = threadIdx.x & 31;
-  dev::grid_dependency_wait();  // partials of decode_main are complete and visible
-  const size_t row0 = (static_cast<size_t>(b) * a.Hq + h) * a.max_parts;
   const float* po = a.part_o + row0 * D + lane * V;
-  float mv = lane < min(CH, a.max_parts) ? a.part_m[row0 + lane] : -INFINITY;
-  float lv = lane < min(CH, a.max_parts) ? a.part_l[row0 + lane] : 0.f;
-  const int L = checked_len(a, b, false);
-  const int nblk = (L + 15) >> 4;
-  const int nparts = (nblk + a.bpp - 1) / a.bpp;
-  if (nparts <= 1) return;  // written by decode_main (zero rows included)
   float M = -INFINITY, ls = 0.f, acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  for (int c0 = 0; c0 < nparts; c0 += CH) {
-    const int n = min(CH, nparts - c0);
+  for (int c0 = 0; c0 < n; c0 += CH) {
+    const int cn = min(CH, n - c0);
     if (c0 > 0) {
-      mv = lane < n ? a.part_m[row0 + c0 + lane] : -INFINITY;
-      lv = lane < n ? a.part_l[row0 + c0 + lane] : 0.f;
+      mv = lane < cn ? a.part_m[row0 + c0 + lane] : -INFINITY;
+      lv = lane < cn ? a.part_l[row0 + c0 + lane] : 0.f;
     }
-    if (lane >= n) {  // stale scratch past nparts (possibly NaN) never enters the sums
+    if (lane >= cn) {
       mv = -INFINITY;
       lv = 0.f;
     }
     float x[CH][V];
 #pragma unroll
     for (int i = 0; i < CH; ++i) {
-      if (i < n) {
+      if (i < cn) {
         if constexpr (V == 4) {
           const float4 t = *reinterpret_cast<const float4*>(po + static_cast<size_t>(c0 + i) * D);
           x[i][0] = t.x; x[i][1] = t.y; x[i][2] = t.z; x[i][3] = t.w;
@@ -674,15 +760,58 @@ __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce(const DecodeA
 #pragma unroll
     for (int i = 0; i < CH; ++i) {
       const float wi = __shfl_sync(FULL, w, i);
-      if (i < n) {
+      if (i < cn) {
 #pragma unroll
         for (int v = 0; v < V; ++v) acc[v] += wi * x[i][v];
       }
     }
   }
-  const size_t orow = (static_cast<size_t>(b) * a.Hq + h) * D + lane * V;
 #pragma unroll
-  for (int v = 0; v < V; ++v) store_out<QT>(a, orow + v, acc[v] / ls);
+  for (int v = 0; v < V; ++v) store_out<QT>(a, orow * D + lane * V + v, acc[v] / ls);
+}
+
+// Merge the partitions of each (sequence, query head).  One warp per query
+// head, G warps per CTA (one CTA per sequence and kv head).  The first
+// chunk's (m, l) are read together with the context length (rows up to
+// max_parts always exist); partial rows only for partitions that exist.
+template <typename QT, int D>
+__global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce(const DecodeArgs a) {
+  const int bg = blockIdx.x, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int h = g * a.G + static_cast<int>(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  dev::grid_dependency_wait();  // partials of decode_main are complete and visible
+  const size_t row0 = (static_cast<size_t>(b) * a.Hq + h) * a.max_parts;
+  const float mv = lane < min(16, a.max_parts) ? a.part_m[row0 + lane] : -INFINITY;
+  const float lv = lane < min(16, a.max_parts) ? a.part_l[row0 + lane] : 0.f;
+  const int L = checked_len(a, b, false);
+  const int nblk = (L + 15) >> 4;
+  const int nparts = (nblk + a.bpp - 1) / a.bpp;
+  if (nparts <= 1) return;  // written by decode_main (zero rows included)
+  merge_rows<QT, D>(a, row0, nparts, mv, lv, static_cast<size_t>(b) * a.Hq + h, lane);
+}
+
+// The grouped form: one CTA per (group k, member m, kv head g).  A member's
+// partitions are its shared-prefix partitions (written by the group's
+// prefix items) followed by its tail partitions.
+template <typename QT, int D>
+__global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce_grouped(const DecodeArgs a) {
+  const int g = blockIdx.x % a.Hkv, km = blockIdx.x / a.Hkv;
+  const int m = km % a.max_members, k = km / a.max_members;
+  const int h = g * a.G + static_cast<int>(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  dev::grid_dependency_wait();  // partials of decode_main are complete and visible
+  const int gs0 = a.group_start[k], gs1 = a.group_start[k + 1], pre = a.prefix_blocks[k];
+  const int members = gs1 - gs0;
+  if (gs0 < 0 || members <= 0 || gs1 > a.B || members > a.max_members || m >= members) return;
+  const int Lm = lane < members ? checked_len(a, gs0 + lane, false) : 0;
+  const int E = group_prefix(pre, members, Lm, lane);
+  const int b = gs0 + m, L = __shfl_sync(0xffffffffu, Lm, m);
+  const int nblk = (L + 15) >> 4;
+  if (nblk == 0) return;  // zero rows written by decode_main
+  const int nparts = (E + a.bpp - 1) / a.bpp + (nblk - E + a.bpp - 1) / a.bpp;
+  if (nparts <= 1) return;
+  const size_t row0 = (static_cast<size_t>(b) * a.Hq + h) * a.max_parts;
+  const float mv = lane < min(16, nparts) ? a.part_m[row0 + lane] : -INFINITY;
+  const float lv = lane < min(16, nparts) ? a.part_l[row0 + lane] : 0.f;
+  merge_rows<QT, D>(a, row0, nparts, mv, lv, static_cast<size_t>(b) * a.Hq + h, lane);
 }
 
 // ---- host side -------------------------------------------------------------------
@@ -733,6 +862,12 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   a.v_scale_w = const_cast<float*>(l.v_scale);
   a.new_dtype = l.new_dtype;
   a.fuse_write = l.slot_mapping != nullptr;
+  a.group_start = l.group_start;
+  a.prefix_blocks = l.prefix_blocks;
+  a.n_groups = l.n_groups;
+  a.max_members = l.max_members;
+  a.pre_parts = l.plan.pre_parts;
+  a.tail_parts = l.plan.tail_parts;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: no CUDA device");
@@ -753,7 +888,10 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   if (setup_err[dev] != cudaSuccess)
     return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(setup_err[dev]));
 
-  const dim3 grid(static_cast<unsigned>(l.B * l.Hkv), static_cast<unsigned>(l.plan.max_parts));
+  const bool grouped = l.n_groups > 0;
+  const dim3 grid = grouped ? dim3(static_cast<unsigned>(l.n_groups * l.Hkv),
+                                   static_cast<unsigned>(l.plan.pre_parts + l.max_members * l.plan.tail_parts))
+                            : dim3(static_cast<unsigned>(l.B * l.Hkv), static_cast<unsigned>(l.plan.max_parts));
   const int W = l.plan.item_warps;
   cudaError_t e;
   if (W == 4)
@@ -762,7 +900,11 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
     e = launch_dependent(decode_main<KT, QT, D, 2>, grid, dim3(64), TL::smem(2), stream, tmK, tmV, a);
   else
     e = launch_dependent(decode_main<KT, QT, D, 1>, grid, dim3(32), TL::smem(1), stream, tmK, tmV, a);
-  if (e == cudaSuccess && l.plan.max_parts > 1)
+  if (e == cudaSuccess && grouped)
+    e = launch_dependent(decode_reduce_grouped<QT, D>,
+                         dim3(static_cast<unsigned>(l.n_groups * l.max_members * l.Hkv)),
+                         dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
+  else if (e == cudaSuccess && l.plan.max_parts > 1)
     e = launch_dependent(decode_reduce<QT, D>, dim3(static_cast<unsigned>(l.B * l.Hkv)),
                          dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
   if (e == cudaSuccess) e = cudaGetLastError();

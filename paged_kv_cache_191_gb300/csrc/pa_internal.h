@@ -40,6 +40,9 @@ struct DecodePlan {
   int32_t max_parts;        // partitions of the longest allowed context
   size_t workspace_bytes;   // 0 when max_parts == 1
   int32_t item_warps;       // warps sharing one partition (1, 2 or 4)
+  // shared-prefix groups: grid rows of prefix partitions and of tail
+  // partitions per member (max_parts = pre_parts + tail_parts); 0 otherwise
+  int32_t pre_parts = 0, tail_parts = 0;
 };
 pa_status plan_decode(int32_t B, int32_t num_q_heads, int32_t max_context_len,
                       const pa_cache_desc* desc, int32_t split_tokens, DecodePlan* plan);
@@ -67,6 +70,10 @@ struct DecodeLaunch {
   const void* v_new = nullptr;
   const int64_t* slot_mapping = nullptr;
   int32_t new_dtype = 0;
+  // shared-prefix groups (pa_decode_append_grouped), else n_groups == 0
+  const int32_t* group_start = nullptr;
+  const int32_t* prefix_blocks = nullptr;
+  int32_t n_groups = 0, max_members = 0;
 };
 pa_status launch_decode(const DecodeLaunch& a, void* stream);
 

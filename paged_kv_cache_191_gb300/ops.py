@@ -20,6 +20,7 @@ F16, BF16, FP8_E4M3, F32, INT8 = 0, 1, 2, 3, 4
 BLOCK_SIZE = 16
 DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_CONTEXT_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 DEVERR_QUERY_RANGE = 16
+DEVERR_GROUP = 32
 
 _TORCH_DT = {torch.float16: F16, torch.bfloat16: BF16, torch.float32: F32,
              torch.uint8: FP8_E4M3, torch.float8_e4m3fn: FP8_E4M3, torch.int8: INT8}
@@ -79,6 +80,11 @@ SIGNATURES = {
                                    _I32, _F, _P, _I32, C.POINTER(CacheDesc), _P, C.c_size_t, _I32, _P]),
     "pa_decode_static_ws": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F, _P,
                                       _I32, C.POINTER(CacheDesc), _I32, _P]),
+    "pa_decode_grouped_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32, _I32, C.POINTER(CacheDesc),
+                                                      _I32]),
+    "pa_decode_append_grouped": (C.c_int, [_P, _P, _I32, _P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
+                                           _I32, _F, _P, _P, _I32, _I32, _I32, _P, _I32, C.POINTER(CacheDesc),
+                                           _P, C.c_size_t, _I32, _P]),
     "pa_chunked_prefill_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32, C.POINTER(CacheDesc),
                                                        _I32]),
     "pa_chunked_prefill": (C.c_int, [_P, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
@@ -317,6 +323,51 @@ def decode_append(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
                                   int(max_context_len), B, Hq, float(scale), _ptr(out), _TORCH_DT[odt],
                                   C.byref(desc), _ptr(workspace), ws_bytes, int(split_tokens), _stream(stream)),
            "pa_decode_append")
+    return out
+
+
+def decode_append_grouped(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables, context_lens,
+                          max_context_len, scale, group_start, prefix_blocks, max_group_size, max_prefix_blocks,
+                          out=None, out_dtype=None, k_scale=None, v_scale=None, workspace=None, split_tokens=0,
+                          stream=None):
+    """decode_append with shared-prefix groups: group k is sequences
+    group_start[k] .. group_start[k+1]-1 (int32 [n_groups + 1], device),
+    sharing their first prefix_blocks[k] blocks (int32 [n_groups], device);
+    each shared tile is read once for the whole group."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (slot_mapping, "slot_mapping"), (q, "q"),
+                 (k_cache, "k_cache"), (v_cache, "v_cache"), (block_tables, "block_tables"),
+                 (context_lens, "context_lens"), (group_start, "group_start"), (prefix_blocks, "prefix_blocks")):
+        _dev(t, n)
+    desc = cache_desc(k_cache)
+    B, Hq, D = q.shape
+    n_groups = group_start.numel() - 1
+    if group_start.dtype != torch.int32 or prefix_blocks.dtype != torch.int32 or prefix_blocks.numel() != n_groups:
+        raise ValueError("group_start must be int32 [n_groups + 1], prefix_blocks int32 [n_groups]")
+    if k_new.shape != (B, desc.num_kv_heads, D) or v_new.shape != k_new.shape or k_new.dtype != v_new.dtype:
+        raise ValueError("k_new, v_new must be [B, num_kv_heads, head_dim] of one dtype")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != B:
+        raise ValueError("slot_mapping must be int64 [B]")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be int32 [B, max_blocks]")
+    if context_lens.dtype != torch.int32 or context_lens.numel() != B:
+        raise ValueError("context_lens must be int32 [B]")
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=odt, device=q.device)
+    else:
+        _dev(out, "out")
+        odt = out.dtype
+    need = int(lib().pa_decode_grouped_workspace_size(B, Hq, int(max_context_len), n_groups, int(max_group_size),
+                                                      int(max_prefix_blocks), C.byref(desc), int(split_tokens)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().pa_decode_append_grouped(
+        _ptr(k_new), _ptr(v_new), _TORCH_DT[k_new.dtype], _ptr(slot_mapping), _ptr(q), _TORCH_DT[q.dtype],
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), int(max_context_len), B, Hq, float(scale), _ptr(group_start), _ptr(prefix_blocks),
+        n_groups, int(max_group_size), int(max_prefix_blocks), _ptr(out), _TORCH_DT[odt], C.byref(desc),
+        _ptr(workspace), ws_bytes, int(split_tokens), _stream(stream)), "pa_decode_append_grouped")
     return out
 
 
