@@ -89,3 +89,54 @@ def test_cache_write_and_copy_reject_bad_arguments(palib):
     assert lib.pa_copy_blocks(FAKE, FAKE, None, None, FAKE, 0, C.byref(d), None) == ops.PA_OK
     d8 = _desc(kv_dtype=ops.FP8_E4M3)
     assert lib.pa_copy_blocks(FAKE, FAKE, None, None, FAKE, 2, C.byref(d8), None) == ops.PA_ERR_INVALID
+
+
+def _grouped(desc, **kw):
+    a = dict(kn=FAKE, vn=FAKE, ndt=ops.F16, slots=FAKE, q=FAKE, q_dtype=ops.F16, k=FAKE, v=FAKE, ks=None, vs=None,
+             bt=FAKE, maxb=8, cl=FAKE, maxl=128, B=8, Hq=4, scale=0.1, gs=FAKE, pre=FAKE, ng=2, mg=4, mp=4,
+             out=FAKE, odt=ops.F16, ws=None, wsb=0, split=0)
+    a.update(kw)
+    return ops.lib().pa_decode_append_grouped(
+        a["kn"], a["vn"], a["ndt"], a["slots"], a["q"], a["q_dtype"], a["k"], a["v"], a["ks"], a["vs"], a["bt"],
+        a["maxb"], a["cl"], a["maxl"], a["B"], a["Hq"], a["scale"], a["gs"], a["pre"], a["ng"], a["mg"], a["mp"],
+        a["out"], a["odt"], C.byref(desc), a["ws"], a["wsb"], a["split"], None)
+
+
+@pytest.mark.parametrize("call_kw,status", [
+    ({"mg": 5}, ops.PA_ERR_UNSUPPORTED),           # 5 members x G = 2 -> 10 query columns > 8
+    ({"ng": 0}, ops.PA_ERR_INVALID),
+    ({"ng": 9}, ops.PA_ERR_INVALID),               # more groups than sequences
+    ({"mp": -1}, ops.PA_ERR_INVALID),
+    ({"gs": None}, ops.PA_ERR_INVALID),
+    ({"pre": FAKE + 2}, ops.PA_ERR_INVALID),       # misaligned
+    ({"slots": None}, ops.PA_ERR_INVALID),
+    ({}, ops.PA_ERR_INVALID),                      # a grouped call always needs its workspace
+])
+def test_grouped_decode_rejects_bad_arguments(palib, call_kw, status):
+    assert _grouped(_desc(), **call_kw) == status
+    assert palib.pa_last_error()
+
+
+def test_grouped_workspace_size(palib):
+    d = _desc()  # Hkv = 2; Hq = 4 -> G = 2
+    # 128-token contexts (8 blocks), prefix of 4 blocks, 512-token partitions:
+    # one prefix partition + one tail partition per member
+    ws = palib.pa_decode_grouped_workspace_size(8, 4, 128, 2, 4, 4, C.byref(d), 0)
+    assert ws >= 8 * 4 * 2 * (128 + 2) * 4 and ws % 256 == 0
+    assert palib.pa_decode_grouped_workspace_size(8, 4, 128, 2, 5, 4, C.byref(d), 0) == 0  # 10 columns
+    assert palib.pa_decode_grouped_workspace_size(8, 4, 128, 0, 4, 4, C.byref(d), 0) == 0
+
+
+def test_chunked_prefill_scale_rules(palib):
+    """1-byte caches need 16-byte aligned scales and a 16-bit q; 16-bit caches take none."""
+    lib = ops.lib()
+
+    def call(desc, q_dtype, ks, vs):
+        return lib.pa_chunked_prefill(FAKE, q_dtype, FAKE, 4, 4, FAKE, FAKE, ks, vs, FAKE, 4, FAKE, 64, 1, 4, 0.1,
+                                      FAKE, ops.F32, C.byref(desc), None, 0, 0, None)
+    d8 = _desc(kv_dtype=ops.FP8_E4M3)
+    assert call(d8, ops.F16, None, None) == ops.PA_ERR_INVALID
+    assert call(d8, ops.F16, FAKE + 4, FAKE) == ops.PA_ERR_INVALID
+    assert call(d8, ops.FP8_E4M3, FAKE, FAKE) == ops.PA_ERR_INVALID
+    assert call(_desc(), ops.F16, FAKE, FAKE) == ops.PA_ERR_INVALID
+    assert call(_desc(), ops.BF16, None, None) == ops.PA_ERR_INVALID
