@@ -762,7 +762,9 @@ def run_ours(args, rank, world, local_rank):
         "timing": timing,
         "e2e": e2e,
         "swap": swap,
-        "gpu_launches": st.launches_per_step() * args.steps,
+        # + one pa_copy_blocks launch in every shared-prefix step that copies
+        "gpu_launches": st.launches_per_step() * args.steps + (sum(1 for h in st.history if h[2] > 0)
+                                                               if shared else 0),
         "clocks": clocks.summary(wall0, wall1),
         "cpu_baseline": cpu,
     }
