@@ -330,8 +330,9 @@ class DecodeStep:
         for b in self.ids:
             self.alloc.alloc_seq(b, int(self.w.context_lens[b]) - 1)
 
-    def host_prepare(self):
-        """a1: reset if due, append one slot per sequence, tables -> pinned."""
+    def host_prepare(self, ptrs=None):
+        """a1: reset if due, append one slot per sequence, tables -> pinned
+        (this step's ring buffer, or the (slots, lens, tables) pointers given)."""
         ops = self.ops
         if self.steps_since_reset == RESET_EVERY:
             for b in self.ids:
@@ -339,15 +340,19 @@ class DecodeStep:
             self._admit()
             self.cur_lens = self.lens0.copy() - 1
             self.steps_since_reset = 0
-        buf = self.meta_host[self.ring]
-        if self.ring_used[self.ring]:
-            t0 = time.perf_counter()
-            self.drv.sync(self.ring_ev[self.ring])
-            self.blocked_s += time.perf_counter() - t0
-        base = buf.data_ptr()
-        slots_p = C.cast(base, C.POINTER(C.c_int64))
-        lens_p = C.cast(base + self.B * 8, C.POINTER(C.c_int32))
-        tab_p = C.cast(base + self.B * 12, C.POINTER(C.c_int32))
+        if ptrs is not None:
+            buf = None
+            slots_p, lens_p, tab_p = ptrs
+        else:
+            buf = self.meta_host[self.ring]
+            if self.ring_used[self.ring]:
+                t0 = time.perf_counter()
+                self.drv.sync(self.ring_ev[self.ring])
+                self.blocked_s += time.perf_counter() - t0
+            base = buf.data_ptr()
+            slots_p = C.cast(base, C.POINTER(C.c_int64))
+            lens_p = C.cast(base + self.B * 8, C.POINTER(C.c_int32))
+            tab_p = C.cast(base + self.B * 12, C.POINTER(C.c_int32))
         ops._check(self.L.pa_append_slots(self.alloc._h, self.ids_c, self.B, slots_p, self.pairs_c,
                                           C.byref(self.ncow)), "pa_append_slots")
         ops._check(self.L.pa_block_tables(self.alloc._h, self.ids_c, self.B, tab_p, self.cap, lens_p),
@@ -867,10 +872,39 @@ def measure_swap(st, stream, n_seqs=8, reps=5):
 
 
 def run_e2e(st, args, stream):
-    """Same step through ops.* with pinned host q/k/v in and out back, synced."""
+    """Same step through the public API with pinned host inputs in and the
+    output back, synced every step: DecodeSession (one staging copy of the
+    step's q / k_new / v_new and block-manager output, one fused launch, one
+    output copy) for the decode workloads; ops.* calls for the shared-prefix
+    workload."""
     import torch
     ops = st.ops
     n = max(1, min(args.e2e_steps, args.steps))
+    if not isinstance(st, SharedPrefixStep):
+        from paged_kv_cache_191_gb300.session import DecodeSession
+        sess = DecodeSession(st.kc, st.vc, st.B, st.Hq, st.cap, st.max_len, st.w.scale, st.q.dtype,
+                             k_scale=st.ks, v_scale=st.vs, split_tokens=st.split)
+        for r in range(sess.ring):  # the model's outputs for the step (the same every step here)
+            q, k, v = sess.inputs(slot=r)
+            q.copy_(st.w.q)
+            k.copy_(st.w.new_k)
+            v.copy_(st.w.new_v)
+        total_b = 0
+        with torch.cuda.stream(stream):
+            stream.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(n):
+                st.host_prepare(sess.meta_ptrs())
+                _, s = st.step_bytes()
+                total_b += s
+                out = sess.step(stream)
+            t1 = time.perf_counter()
+        return {"value": round(total_b / (t1 - t0) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(sess.nbytes), "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+                "steps": n, "tokens_per_s": round(st.B * n / (t1 - t0), 1),
+                "api": "paged_kv_cache_191_gb300.session.DecodeSession (block manager writes into a pinned staging "
+                       "buffer beside q / k_new / v_new; one H2D copy, pa_decode_append, one D2H copy of the "
+                       "output, stream sync per step)"}
     hq = st.w.q.pin_memory()
     hk, hv = st.w.new_k.pin_memory(), st.w.new_v.pin_memory()
     hout = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()

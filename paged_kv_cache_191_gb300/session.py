@@ -1,0 +1,111 @@
+"""Decode steps with host inputs at low host overhead.
+
+A DecodeSession binds a cache and a batch shape once.  Each step's inputs
+live in one pinned host staging buffer:
+
+    slots int64 [B] | context_lens int32 [B] | block_tables int32 [B, max_blocks]
+    | q [B, Hq, D] | k_new [B, Hkv, D] | v_new [B, Hkv, D]
+
+(each part 16-byte aligned).  The caller fills the buffer: the block manager
+writes slots, lengths and tables straight into it through the pointers that
+`meta_ptrs()` returns, and the model writes q / k_new / v_new through
+`inputs()`.  step() then issues one host-to-device copy of the buffer, one
+pa_decode_append launch (cache write fused into attention) and one
+device-to-host copy of the output, and waits for it.  The ctypes arguments
+of the launch are built once.  Host buffers rotate over a small ring, so the
+next step can be filled while the device finishes the previous copy.
+"""
+import ctypes as C
+
+import torch
+
+from . import ops
+
+
+def _align16(n):
+    return (n + 15) & ~15
+
+
+class DecodeSession:
+    def __init__(self, k_cache, v_cache, batch, num_q_heads, max_blocks, max_context_len, scale,
+                 dtype, k_scale=None, v_scale=None, out_dtype=None, split_tokens=0, ring=2):
+        for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+            ops._dev(t, n)
+        L = ops.lib()
+        self.desc = ops.cache_desc(k_cache)
+        self.B, self.Hq, self.Hkv, self.D = batch, num_q_heads, self.desc.num_kv_heads, self.desc.head_dim
+        self.max_blocks, self.max_context_len = max_blocks, max_context_len
+        dev = k_cache.device
+        e = torch.empty((), dtype=dtype).element_size()
+        B, Hq, Hkv, D = self.B, self.Hq, self.Hkv, self.D
+        sizes = [B * 8, B * 4, B * max_blocks * 4, B * Hq * D * e, B * Hkv * D * e, B * Hkv * D * e]
+        self.offsets, off = [], 0
+        for n in sizes:
+            self.offsets.append(off)
+            off += _align16(n)
+        self.nbytes = off
+        self.host = [torch.zeros(off, dtype=torch.uint8).pin_memory() for _ in range(ring)]
+        self.dev = torch.zeros(off, dtype=torch.uint8, device=dev)
+        odt = out_dtype or dtype
+        self.out = torch.empty((B, Hq, D), dtype=odt, device=dev)
+        self.out_host = [torch.empty((B, Hq, D), dtype=odt).pin_memory() for _ in range(ring)]
+        ws = int(L.pa_decode_workspace_size(B, Hq, max_context_len, C.byref(self.desc), split_tokens))
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.dtype, self.odt, self.ring, self.i = dtype, odt, ring, 0
+        self.done = [torch.cuda.Event() for _ in range(ring)]
+        self.used = [False] * ring
+        base = self.dev.data_ptr()
+        o = self.offsets
+        P = C.c_void_p
+        ptr = (lambda t: P(t.data_ptr()) if t is not None else None)
+        # pa_decode_append(k_new, v_new, new_dtype, slots, q, q_dtype, k_cache, v_cache, k_scale, v_scale,
+        #                  tables, max_blocks, lens, max_context_len, B, Hq, scale, out, out_dtype, desc,
+        #                  workspace, workspace_bytes, split_tokens, stream)
+        self._head = (P(base + o[4]), P(base + o[5]), ops._TORCH_DT[dtype], P(base + o[0]), P(base + o[3]),
+                      ops._TORCH_DT[dtype], ptr(k_cache), ptr(v_cache), ptr(k_scale), ptr(v_scale),
+                      P(base + o[2]), max_blocks, P(base + o[1]), max_context_len, B, Hq, C.c_float(scale),
+                      ptr(self.out), ops._TORCH_DT[odt], C.byref(self.desc), ptr(self.ws), self.ws.numel(),
+                      split_tokens)
+        self._keep = (k_cache, v_cache, k_scale, v_scale)
+        self._L = L
+
+    def _wait_slot(self):
+        if self.used[self.i]:
+            self.done[self.i].synchronize()
+
+    def meta_ptrs(self):
+        """(slots, lens, tables) ctypes pointers into the current host buffer."""
+        self._wait_slot()
+        base = self.host[self.i].data_ptr()
+        o = self.offsets
+        return (C.cast(base + o[0], C.POINTER(C.c_int64)), C.cast(base + o[1], C.POINTER(C.c_int32)),
+                C.cast(base + o[2], C.POINTER(C.c_int32)))
+
+    def inputs(self, slot=None):
+        """(q, k_new, v_new) host tensors viewing the current host buffer (or
+        ring slot `slot`, e.g. to fill every slot ahead)."""
+        if slot is None:
+            self._wait_slot()
+        h, o = self.host[self.i if slot is None else slot], self.offsets
+        B, Hq, Hkv, D = self.B, self.Hq, self.Hkv, self.D
+        e = torch.empty((), dtype=self.dtype).element_size()
+        q = h[o[3]: o[3] + B * Hq * D * e].view(self.dtype).view(B, Hq, D)
+        k = h[o[4]: o[4] + B * Hkv * D * e].view(self.dtype).view(B, Hkv, D)
+        v = h[o[5]: o[5] + B * Hkv * D * e].view(self.dtype).view(B, Hkv, D)
+        return q, k, v
+
+    def step(self, stream=None):
+        """Copy the current host buffer in, decode, copy the output back and
+        wait for it; returns the pinned host output [B, Hq, D]."""
+        stream = stream or torch.cuda.current_stream()
+        i = self.i
+        with torch.cuda.stream(stream):
+            self.dev.copy_(self.host[i], non_blocking=True)
+            ops._check(self._L.pa_decode_append(*self._head, C.c_void_p(stream.cuda_stream)), "pa_decode_append")
+            out = self.out_host[i]
+            out.copy_(self.out, non_blocking=True)
+            self.done[i].record(stream)
+        self.used[i] = True
+        self.i = (i + 1) % self.ring
+        self.done[i].synchronize()
+        return out

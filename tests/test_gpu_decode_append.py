@@ -91,3 +91,41 @@ def test_fused_fp8_scales_are_race_free(rep, Hkv, fmt):
     """Every kv head of a token reads the token's fresh scale: repeated runs
     with many heads per sequence (the scale row is shared by all of them)."""
     test_fused_equals_write_then_decode(8 * (Hkv // 2) if Hkv > 2 else 8, Hkv, fmt, "bf16", 0)
+
+
+@pytest.mark.parametrize("kv", ["f16", "fp8"])
+def test_decode_session_equals_decode_append(kv):
+    """DecodeSession (one staging copy, one fused launch, one output copy per
+    step) gives the same output and cache as ops.decode_append, step after
+    step while the ring of host buffers rotates."""
+    from paged_kv_cache_191_gb300.session import DecodeSession
+    w = W.random_small(123, B=6, Hq=8, Hkv=2, D=128, kv_dtype=kv, max_len=600, min_len=1)
+    ml, mb = int(w.context_lens.max()), w.block_tables.shape[1]
+    if kv == "fp8":
+        kc, vc, ks, vs = fp8_caches(w)
+        kc2, vc2, ks2, vs2 = fp8_caches(w)
+    else:
+        kc, vc, ks, vs = w.k_pool.to(DEV), w.v_pool.to(DEV), None, None
+        kc2, vc2, ks2, vs2 = w.k_pool.to(DEV), w.v_pool.to(DEV), None, None
+    sess = DecodeSession(kc, vc, w.B, w.Hq, mb, ml, w.scale, torch.float16, k_scale=ks, v_scale=vs,
+                         out_dtype=torch.float32)
+    rng = W.rng_for(9)
+    for step in range(3):
+        k_new = W.randn(rng, (w.B, w.Hkv, 128), torch.float16)
+        v_new = W.randn(rng, (w.B, w.Hkv, 128), torch.float16)
+        slots_p, lens_p, tab_p = sess.meta_ptrs()
+        np.ctypeslib.as_array(slots_p, (w.B,))[:] = last_slots(w)
+        np.ctypeslib.as_array(lens_p, (w.B,))[:] = w.context_lens
+        np.ctypeslib.as_array(tab_p, (w.B, mb))[:] = w.block_tables
+        q, k, v = sess.inputs()
+        q.copy_(w.q)
+        k.copy_(k_new)
+        v.copy_(v_new)
+        got = sess.step().clone()
+        want = ops.decode_append(k_new.to(DEV), v_new.to(DEV), torch.from_numpy(last_slots(w)).to(DEV),
+                                 w.q.to(DEV), kc2, vc2, torch.from_numpy(w.block_tables).to(DEV),
+                                 torch.from_numpy(w.context_lens).to(DEV), ml, w.scale, out_dtype=torch.float32,
+                                 k_scale=ks2, v_scale=vs2)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want.cpu()), step
+        assert torch.equal(kc.cpu(), kc2.cpu()) and torch.equal(vc.cpu(), vc2.cpu()), step
