@@ -9,11 +9,12 @@ live in one pinned host staging buffer:
 (each part 16-byte aligned).  The caller fills the buffer: the block manager
 writes slots, lengths and tables straight into it through the pointers that
 `meta_ptrs()` returns, and the model writes q / k_new / v_new through
-`inputs()`.  step() then issues one host-to-device copy of the buffer, one
+`inputs()`.  launch() then issues one host-to-device copy of the buffer, one
 pa_decode_append launch (cache write fused into attention) and one
-device-to-host copy of the output, and waits for it.  The ctypes arguments
-of the launch are built once.  Host buffers rotate over a small ring, so the
-next step can be filled while the device finishes the previous copy.
+device-to-host copy of the output; wait() returns the output once it is on
+the host (step() does both).  The ctypes arguments of the launch are built
+once.  Host buffers rotate over a small ring, so the next step's buffer can
+be filled (block manager, model) while the device runs the current one.
 """
 import ctypes as C
 
@@ -94,18 +95,26 @@ class DecodeSession:
         v = h[o[5]: o[5] + B * Hkv * D * e].view(self.dtype).view(B, Hkv, D)
         return q, k, v
 
-    def step(self, stream=None):
-        """Copy the current host buffer in, decode, copy the output back and
-        wait for it; returns the pinned host output [B, Hq, D]."""
+    def launch(self, stream=None):
+        """Enqueue the current host buffer's step (copy in, decode, copy the
+        output back) and move to the next ring slot, which the caller may
+        fill while the device works; returns a handle for wait()."""
         stream = stream or torch.cuda.current_stream()
         i = self.i
         with torch.cuda.stream(stream):
             self.dev.copy_(self.host[i], non_blocking=True)
             ops._check(self._L.pa_decode_append(*self._head, C.c_void_p(stream.cuda_stream)), "pa_decode_append")
-            out = self.out_host[i]
-            out.copy_(self.out, non_blocking=True)
+            self.out_host[i].copy_(self.out, non_blocking=True)
             self.done[i].record(stream)
         self.used[i] = True
         self.i = (i + 1) % self.ring
-        self.done[i].synchronize()
-        return out
+        return i
+
+    def wait(self, handle):
+        """The pinned host output [B, Hq, D] of a launched step, once ready."""
+        self.done[handle].synchronize()
+        return self.out_host[handle]
+
+    def step(self, stream=None):
+        """launch() and wait(): the output of the current host buffer's step."""
+        return self.wait(self.launch(stream))
