@@ -933,10 +933,16 @@ def run_e2e(st, args, stream):
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
-            ops.cache_write(dk, dv, st.slots_dev, st.kc, st.vc, st.ks, st.vs, stream=stream)
-            ops.decode(dq, st.kc, st.vc, st.tables_dev, st.lens_dev, st.max_len, st.w.scale,
-                       out=st.out, k_scale=st.ks, v_scale=st.vs, workspace=st.ws,
-                       split_tokens=st.split, stream=stream)
+            if st.grouped:  # the fused write + grouped decode, as in the timed steps
+                ops.decode_append_grouped(dk, dv, st.slots_dev, dq, st.kc, st.vc, st.tables_dev, st.lens_dev,
+                                          st.max_len, st.w.scale, st.group_start, st.prefix_blocks, st.w.beams,
+                                          st.w.prompt_len // 16, out=st.out, workspace=st.ws,
+                                          split_tokens=st.split, stream=stream)
+            else:
+                ops.cache_write(dk, dv, st.slots_dev, st.kc, st.vc, st.ks, st.vs, stream=stream)
+                ops.decode(dq, st.kc, st.vc, st.tables_dev, st.lens_dev, st.max_len, st.w.scale,
+                           out=st.out, k_scale=st.ks, v_scale=st.vs, workspace=st.ws,
+                           split_tokens=st.split, stream=stream)
             hout.copy_(st.out, non_blocking=True)
             stream.synchronize()
         t1 = time.perf_counter()
@@ -946,7 +952,9 @@ def run_e2e(st, args, stream):
     return {"value": round(total_b / (t1 - t0) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
             "tokens_per_s": round(st.B * n / (t1 - t0), 1),
-            "api": "paged_kv_cache_191_gb300.ops (pinned host buffers, stream sync per step)"}
+            "api": "paged_kv_cache_191_gb300.ops (pinned host buffers, copy_blocks + decode_append_grouped, "
+                   "stream sync per step)" if st.grouped else
+                   "paged_kv_cache_191_gb300.ops (pinned host buffers, stream sync per step)"}
 
 
 # ---- multi-token workloads (chunked prefill, speculative verify) ------------------
