@@ -695,6 +695,7 @@ def run_ours(args, rank, world, local_rank):
         if shared:
             dec_b, step_b, dec_logical = st.count_bytes()
             copies = sum(h[2] for h in st.history) / args.steps
+            cow_launches = sum(1 for h in st.history if h[2] > 0)  # one pa_copy_blocks per copying step
         stream.synchronize()
         wall1 = time.time()
     torch.cuda.synchronize()
@@ -767,9 +768,7 @@ def run_ours(args, rank, world, local_rank):
         "timing": timing,
         "e2e": e2e,
         "swap": swap,
-        # + one pa_copy_blocks launch in every shared-prefix step that copies
-        "gpu_launches": st.launches_per_step() * args.steps + (sum(1 for h in st.history if h[2] > 0)
-                                                               if shared else 0),
+        "gpu_launches": st.launches_per_step() * args.steps + (cow_launches if shared else 0),
         "clocks": clocks.summary(wall0, wall1),
         "cpu_baseline": cpu,
     }
