@@ -205,9 +205,11 @@ size_t pa_decode_grouped_workspace_size(int32_t B, int32_t num_q_heads, int32_t 
  * pa_decode_append_grouped -- pa_decode_append for a batch whose sequences
  * come in groups sharing the leading blocks of their tables: the beams or
  * samples of one prompt after fork, which share those blocks by reference
- * count and copy on write ([LLM-INF] 2.2, [KV-CB] 4.2).  The results are
- * those of pa_decode_append up to float32 summation order.  What changes is
- * how the shared blocks are read.  One work item per (group, kv head,
+ * count and copy on write ([LLM-INF] 2.2, [KV-CB] 4.2).  It computes what
+ * pa_decode_append computes.  Results differ only by rounding, because the
+ * partitions differ: the float32 summation order and the 16-bit rounding of the
+ * softmax weights against each partition's running max.  What changes is how
+ * the shared blocks are read.  One work item per (group, kv head,
  * partition of the shared prefix) loads each shared K/V tile once and scores
  * it against the queries of every member of the group; pa_decode_append reads
  * the tile once per member.  The members' private tails run as ordinary
