@@ -31,7 +31,7 @@ def no_device_errors():
     assert ops.device_errors(clear=True) == 0
 
 
-def grouped_case(seed, sizes, prefix, Hq, Hkv, kv, tail_max=60, zero=()):
+def grouped_case(seed, sizes, prefix, Hq, Hkv, kv, tail_max=60, zero=(), D=128):
     """Lengths 16 * P_k + tail (tail in [1, tail_max]); members of group k
     share their first P_k table entries with the group's first member."""
     rng = W.rng_for(seed)
@@ -41,7 +41,7 @@ def grouped_case(seed, sizes, prefix, Hq, Hkv, kv, tail_max=60, zero=()):
             lens.append(16 * prefix[k] + int(rng.integers(1, tail_max + 1)))
     for b in zero:
         lens[b] = 0
-    w = W.make_decode(f"grouped{seed}", seed + 5, len(lens), Hq, Hkv, 128, kv, lens, pool_factor=1.3)
+    w = W.make_decode(f"grouped{seed}", seed + 5, len(lens), Hq, Hkv, D, kv, lens, pool_factor=1.3)
     start = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     tables = w.block_tables.copy()
     for k in range(len(sizes)):
@@ -76,8 +76,8 @@ def run(w, start, claimed, split=0, grouped=True, max_size=None):
     rng = W.rng_for(17)
     q = w.q.to(torch.bfloat16) if w.kv_dtype == "bf16" else w.q
     tdt = q.dtype
-    k_new = W.randn(rng, (w.B, w.Hkv, 128), tdt).to(DEV)
-    v_new = W.randn(rng, (w.B, w.Hkv, 128), tdt).to(DEV)
+    k_new = W.randn(rng, (w.B, w.Hkv, w.D), tdt).to(DEV)
+    v_new = W.randn(rng, (w.B, w.Hkv, w.D), tdt).to(DEV)
     sl = torch.from_numpy(last_slots(w)).to(DEV)
     bt = torch.from_numpy(np.ascontiguousarray(w.block_tables, dtype=np.int32)).to(DEV)
     cl = torch.from_numpy(np.ascontiguousarray(w.context_lens, dtype=np.int32)).to(DEV)
@@ -97,7 +97,7 @@ def run(w, start, claimed, split=0, grouped=True, max_size=None):
     return out.cpu().numpy(), [t.cpu() if t is not None else None for t in (kc, vc, ks, vs)], (k_new, v_new, q)
 
 
-CASES = [  # Hq, Hkv, kv, group sizes, shared prefix blocks
+CASES = [  # Hq, Hkv, kv, group sizes, shared prefix blocks (head_dim 128; last case 64)
     (8, 8, "f16", [4, 1, 3], [5, 0, 3]),
     (16, 8, "f16", [4, 2, 1, 3], [6, 2, 0, 4]),
     (16, 8, "bf16", [3, 4], [9, 1]),
@@ -105,13 +105,15 @@ CASES = [  # Hq, Hkv, kv, group sizes, shared prefix blocks
     (32, 4, "bf16", [1, 1, 1], [4, 2, 0]),
     (8, 2, "fp8", [2, 1, 2], [6, 0, 3]),
     (16, 8, "int8", [4, 3], [5, 2]),
+    (4, 4, "bf16", [3, 2, 4], [4, 6, 1]),
 ]
 
 
 @pytest.mark.parametrize("Hq,Hkv,kv,sizes,prefix", CASES, ids=lambda v: str(v))
 @pytest.mark.parametrize("split", [0, 32])
 def test_grouped_matches_oracle_and_ungrouped(Hq, Hkv, kv, sizes, prefix, split):
-    w, start = grouped_case(50 + Hq + Hkv + len(sizes), sizes, prefix, Hq, Hkv, kv)
+    D = 64 if (Hq, Hkv) == (4, 4) else 128
+    w, start = grouped_case(50 + Hq + Hkv + len(sizes), sizes, prefix, Hq, Hkv, kv, D=D)
     got, dev_caches, (k_new, v_new, q) = run(w, start, prefix, split)
     plain, plain_caches, _ = run(w, start, prefix, split, grouped=False)
     for a, b in zip(dev_caches, plain_caches):  # the fused writes are the same
