@@ -1496,19 +1496,118 @@ def run_reference_prefill(args, world):
     }), flush=True)
 
 
+def shared_prefix_view(w):
+    """The shared-prefix workload's first step as a plain decode batch, built
+    on the host block manager alone (every beam forked from its group's
+    prompt, then grown by its tail)."""
+    from types import SimpleNamespace
+    from paged_kv_cache_191_gb300 import ops
+    alloc = ops.BlockAllocator(w.num_blocks, w.free_order)
+    roots = [10 ** 9 + g for g in range(w.groups)]
+    for r in roots:
+        alloc.alloc_seq(r, w.prompt_len)
+    ids = list(range(w.B))
+    alloc.fork_seqs([roots[i // w.beams] for i in ids], ids)
+    tails = w.tail_lens.reshape(-1)
+    for i in ids:
+        alloc.append_tokens(i, int(tails[i]), want_slots=False)
+    cap = -(-(w.prompt_len + int(tails.max())) // 16)
+    tables, lens = alloc.tables(ids, cap)
+    return SimpleNamespace(name=w.name, B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, kv_dtype="f16", context_lens=lens,
+                           block_tables=tables, k_pool=w.k_pool, v_pool=w.v_pool, q=w.q, scale=w.scale)
+
+
+def run_reference_serving(args, world):
+    """Reference arm for the serving loop: the oracle scheduler over the same
+    request trace, the oracle's cache writes and swaps on a host mirror of the
+    pools, and the oracle's multi-token attention for each iteration's items
+    (in order, until the step's time budget is spent), in one host process."""
+    from oracle.attention import paged_prefill
+    from oracle.scheduler import Scheduler as OSched
+    from paged_kv_cache_191_gb300 import workloads as W
+    tr = W.serving_llama7b()
+    sched = OSched(tr.num_blocks, tr.max_batch, tr.max_tokens, tr.host_blocks)
+    Hq, Hkv, D = tr.Hq, tr.Hkv, tr.D
+    kc = np.zeros((tr.num_blocks, Hkv, 16, D), np.float16)
+    vc = np.zeros_like(kc)
+    kh = np.zeros((tr.host_blocks, Hkv, 16, D), np.float16)
+    vh = np.zeros_like(kh)
+    rng = np.random.default_rng(tr.seed)
+    T_max = tr.max_batch + tr.max_tokens
+    bq = rng.standard_normal((T_max, Hq, D)).astype(np.float16)
+    bk = rng.standard_normal((T_max, Hkv, D)).astype(np.float16)
+    bv = rng.standard_normal((T_max, Hkv, D)).astype(np.float16)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    scale = 1.0 / np.sqrt(D)
+    it = 0
+
+    def one():
+        nonlocal it
+        for rid, p, m in tr.arrivals(it):
+            sched.add(rid, p, m)
+        r = sched.step()
+        it += 1
+        for g, h in r.swap_out:
+            kh[h], vh[h] = kc[g], vc[g]
+        row = 0
+        work = []
+        for rid, kind, start, slots in r.items:
+            sl = np.asarray(slots, dtype=np.int64)
+            kc[sl // 16, :, sl % 16, :] = bk[row: row + len(sl)]
+            vc[sl // 16, :, sl % 16, :] = bv[row: row + len(sl)]
+            work.append((row, len(sl), start + len(sl), list(sched.alloc.tables[rid])))
+            row += len(sl)
+        t = time.perf_counter()
+        done = 0
+        for r0, n, L, tab in work:  # attention before the swap-ins, as on the device
+            if time.perf_counter() - t > budget:
+                break
+            paged_prefill(bq[r0: r0 + n], [0, n], kc, vc, np.asarray([tab]), np.array([L]), scale)
+            done += n
+        for h, g in r.swap_in:
+            kc[g], vc[g] = kh[h], vh[h]
+        return done
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    tokens = sum(one() for _ in range(args.steps))
+    t1 = time.perf_counter()
+    val = round(tokens / (t1 - t0), 2)
+    sample = (f"{args.steps} iterations of {tr.name} after {args.warmup} warm-up: oracle scheduler, cache "
+              f"writes and swaps in full, attention of each iteration's items in order within "
+              f"{budget:.2f} s, one host process")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_SERVING, "value": val, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round((t1 - t0) * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": tr.name, "q_heads": Hq, "kv_heads": Hkv, "head_dim": D, "parallelism": "host"},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def run_reference(args, rank, world):
     """Reference arm: the float64 CPU oracle on host cores, K bounded steps."""
     if rank != 0:
         return
     if args.config in PREFILL_CONFIGS:
         return run_reference_prefill(args, world)
-    w = load_workload(args.config)
+    if args.config in SERVING_CONFIGS:
+        return run_reference_serving(args, world)
+    shared = args.config == "shared_prefix_16x4"
+    sw = load_workload(args.config)
+    w = shared_prefix_view(sw) if shared else sw
     cores = cpu_cores()
     fp8 = w.kv_dtype in ("fp8", "int8")
     e = 1 if fp8 else 2
     seqs = list(range(w.B))
     tasks = oracle_tasks(w, seqs, codes=w.kv_dtype if fp8 else None)
     per = [decode_bytes([int(w.context_lens[b])], w.Hq, w.Hkv, w.D, e, 2, 2) for b in seqs]
+    if shared:  # unique bytes: each beam carries a 1/beams share of its group's prompt
+        tails = sw.tail_lens.reshape(-1)
+        per = [decode_bytes([int(tails[b])], w.Hq, w.Hkv, w.D, e, 2, 2)
+               + sw.prompt_len * w.Hkv * w.D * 2 * e / sw.beams for b in seqs]
     budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step
     with _pool(cores) as pool:
         t = time.perf_counter()
