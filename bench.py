@@ -94,17 +94,37 @@ def barrier(world):
 
 
 # ---- measured peaks, profile traffic, clocks -----------------------------------
+def _number(v):
+    """A positive float from a number or from a {"value": number} / {"median": number} record."""
+    if isinstance(v, dict):
+        for k in ("value", "median", "gbs", "mean"):
+            if k in v:
+                return _number(v[k])
+        return None
+    try:
+        x = float(v)
+    except (TypeError, ValueError):
+        return None
+    return x if x > 0 else None
+
+
 def hbm_peak():
+    """The measured HBM copy bandwidth (GB/s) from MEASURED_PEAKS.json, else
+    the fallback; a file in an unexpected shape falls back too."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        for key in ("hbm_gbs", "hbm_copy_gbs", "hbm_GBps"):
-            if key in d:
-                return float(d[key]), "measured"
-        for v in d.values():
-            if isinstance(v, dict) and "hbm_gbs" in v:
-                return float(v["hbm_gbs"]), "measured"
+        if isinstance(d, dict):
+            for key in ("hbm_gbs", "hbm_copy_gbs", "hbm_GBps"):
+                x = _number(d.get(key))
+                if x:
+                    return x, "measured"
+            for v in d.values():
+                if isinstance(v, dict):
+                    x = _number(v.get("hbm_gbs"))
+                    if x:
+                        return x, "measured"
     except (OSError, ValueError):
         pass
     return FALLBACK_HBM_GBS, "fallback"
