@@ -1,6 +1,9 @@
 /*
- * pagedkv.h -- C ABI of libpagedkv.so: paged-KV decode attention for GB300
- * (sm_103a), plus the host-side block manager that feeds it.
+ * pagedkv.h -- C ABI of libpagedkv.so: paged-KV attention for GB300 (sm_103a)
+ * -- decode (plain, fused with the cache write, grouped over shared
+ * prefixes), multi-token chunks, cache write, block copy and swap -- plus the
+ * host-side block manager, the continuous-batching scheduler and the serving
+ * iteration that drive it.
  *
  * Sources, cited by page title and section:
  *   [LLM-INF] "LLM推理引擎深度实战：从PagedAttention到分布式推理部署" (ybb.press)
@@ -8,7 +11,7 @@
  *                 on-demand allocation, copy-on-write via refcounts;
  *             2.3 the attention kernel resolves the page table itself and
  *                 gathers scattered K/V, transparent to the model;
- *             5.3 FP8 KV cache with per-token or per-channel scales;
+ *             5.3 FP8 (and INT8) KV cache with per-token or per-channel scales;
  *             3.1 continuous (iteration-level) batching;
  *             3.2 preemption by swapping to host memory or dropping;
  *             3.3 first-come-first-served scheduling;
@@ -28,8 +31,9 @@
  * - A KV cache is two device arrays k_cache, v_cache, each laid out
  *   [num_blocks][num_kv_heads][16][head_dim] in kv_dtype, so one (block,
  *   kv head) tile of 16 tokens is contiguous.  FP8 caches hold E4M3 codes and
- *   carry two float32 arrays k_scale, v_scale laid out [num_blocks][16]: one
- *   scale per stored token, shared by all of that token's heads and dims.
+ *   INT8 caches symmetric int8 codes; both carry two float32 arrays k_scale,
+ *   v_scale laid out [num_blocks][16]: one scale per stored token, shared by
+ *   all of that token's heads and dims.
  * - "slot" s addresses block s / 16, row s % 16.
  * - Ownership: the caller owns and allocates every device buffer (queues,
  *   tables, caches, outputs, workspace).  The library never allocates device
