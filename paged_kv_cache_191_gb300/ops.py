@@ -371,6 +371,44 @@ def decode_append_grouped(k_new, v_new, slot_mapping, q, k_cache, v_cache, block
     return out
 
 
+def prefix_groups(block_tables, context_lens, max_group_size):
+    """Host helper for decode_append_grouped: split the batch, in order, into
+    groups of consecutive sequences that share leading table entries (the
+    beams of one prompt after fork), at most max_group_size long.
+
+    block_tables int [B, max_blocks], context_lens int [B] (host arrays).  A
+    group's prefix counts the leading entries every member holds equally
+    among the whole blocks before each member's last token (the part the
+    grouped decode may share).  A sequence joins the group before it while
+    that keeps the shared prefix at least one block; every other sequence
+    starts a group.  Returns (group_start int32 [n + 1], prefix_blocks int32
+    [n])."""
+    import numpy as np
+    tables = np.asarray(block_tables)
+    lens = np.asarray(context_lens, dtype=np.int64)
+    B = len(lens)
+    if max_group_size < 1:
+        raise ValueError("max_group_size must be >= 1")
+    usable = np.where(lens > 0, (lens - 1) // BLOCK_SIZE, 0)  # whole blocks before the last token
+    starts, prefixes = [], []
+    b = 0
+    while b < B:
+        g0, pre = b, int(usable[b])
+        b += 1
+        while b < B and b - g0 < max_group_size:
+            lim = min(pre, int(usable[b]))
+            same = tables[g0, :lim] == tables[b, :lim]
+            common = int(lim if same.all() else np.argmin(same))
+            if common < 1:
+                break
+            pre = common
+            b += 1
+        starts.append(g0)
+        prefixes.append(pre if b - g0 > 1 else 0)
+    starts.append(B)
+    return np.asarray(starts, dtype=np.int32), np.asarray(prefixes, dtype=np.int32)
+
+
 def copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None, stream=None):
     """Copy whole blocks for each (src, dst) row of pairs (int64 [n, 2])."""
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (pairs, "pairs")):
