@@ -1071,10 +1071,11 @@ class PrefillStep:
 
 def _prefill_oracle_task(task):
     from oracle.attention import paged_prefill
-    q, qs, kb, vb, L, scale, kvs = task
+    q, qs, kb, vb, L, scale, kvs = task[:7]
+    rows = task[7] if len(task) > 7 else None  # a subset of (token, head) rows
     tab = np.arange(kb.shape[0], dtype=np.int64)[None, :]
     paged_prefill(q, qs, kb, vb, tab, np.array([L]), scale,
-                  k_scale=kvs[0] if kvs else None, v_scale=kvs[1] if kvs else None)
+                  k_scale=kvs[0] if kvs else None, v_scale=kvs[1] if kvs else None, rows=rows)
     return L
 
 
@@ -1473,6 +1474,60 @@ def cpu_baseline(w, seconds):
             "tokens_per_s": round(rounds * w.B / (t1 - t0), 2)}
 
 
+def _per_kv_head(tasks, per):
+    """Decode oracle tasks split per kv head: (G query heads, one kv head's
+    blocks), each carrying its share of the sequence's algorithmic bytes."""
+    out, out_per = [], []
+    for (q, kb, vb, n, scale, ks, vs), p in zip(tasks, per):
+        Hkv = kb.shape[1]
+        G = q.shape[0] // Hkv
+        for g in range(Hkv):
+            out.append((q[g * G:(g + 1) * G], kb[:, g:g + 1], vb[:, g:g + 1], n, scale, ks, vs))
+            out_per.append(p / Hkv)
+    return out, out_per
+
+
+def _per_head_slice(tasks, per, G, slice_tokens=64):
+    """Multi-token oracle tasks split per (kv head, slice of query tokens):
+    the rows of that slice for that kv head's G query heads."""
+    out, out_per = [], []
+    for (q, qs, kb, vb, L, scale, kvs), p in zip(tasks, per):
+        n, Hkv = q.shape[0], kb.shape[1]
+        for g in range(Hkv):
+            qg, kbg, vbg = q[:, g * G:(g + 1) * G], kb[:, g:g + 1], vb[:, g:g + 1]
+            for t0 in range(0, n, slice_tokens):
+                t1 = min(n, t0 + slice_tokens)
+                rows = [(t, h) for t in range(t0, t1) for h in range(G)]
+                out.append((qg, qs, kbg, vbg, L, scale, kvs, rows))
+                out_per.append(p / Hkv * (t1 - t0) / n)
+    return out, out_per
+
+
+def _bounded_oracle_loop(pool, fn, tasks, per, steps, warmup, cores, total_s=150.0):
+    """W + K steps of the oracle over the tasks (cycled), each step as many
+    tasks as one calibrated round of the pool fits in total_s / (W + K)
+    seconds, so the whole run stays near total_s whatever K is (at one task
+    per step at least).  Returns (bytes done, seconds, tasks per step)."""
+    budget = total_s / max(1, steps + warmup)
+    pool.map(fn, tasks[:cores], chunksize=1)  # workers start and import the oracle
+    t = time.perf_counter()
+    pool.map(fn, [tasks[(cores + j) % len(tasks)] for j in range(cores)], chunksize=1)
+    round_s = time.perf_counter() - t  # one task on each worker
+    n = int(max(1, min(len(tasks), cores * budget / max(round_s, 1e-6))))
+    k = 0
+    for _ in range(warmup):
+        pool.map(fn, [tasks[(k + j) % len(tasks)] for j in range(n)], chunksize=1)
+        k += n
+    done_b = 0.0
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        idx = [(k + j) % len(tasks) for j in range(n)]
+        pool.map(fn, [tasks[i] for i in idx], chunksize=1)
+        done_b += sum(per[i] for i in idx)
+        k += n
+    return done_b, time.perf_counter() - t0, n
+
+
 def run_reference_prefill(args, world):
     """Reference arm for the multi-token workloads: the oracle over a bounded
     sample of sequences per step, on host cores."""
@@ -1480,30 +1535,17 @@ def run_reference_prefill(args, world):
     w = W.PREFILL_CONFIGS[args.config]()
     tasks, per = prefill_oracle_tasks(w)
     cores = cpu_cores()
-    budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step
     with _pool(cores) as pool:
         if w.kv_dtype in ("fp8", "int8"):  # the cache's codes and scales (set-up, not timed)
             tasks = pool.map(_quantise_prefill_task, [t[:6] + (w.kv_dtype,) for t in tasks], chunksize=1)
-        t = time.perf_counter()
-        pool.map(_prefill_oracle_task, tasks[:cores], chunksize=1)
-        per_task = (time.perf_counter() - t) / max(1, min(cores, len(tasks))) * cores
-        n_per_step = int(max(1, min(len(tasks), budget / max(per_task / cores, 1e-6))))
-        order = [i % len(tasks) for i in range(n_per_step * (args.steps + args.warmup))]
-        k = 0
-        for _ in range(args.warmup):
-            pool.map(_prefill_oracle_task, [tasks[order[k + j]] for j in range(n_per_step)], chunksize=1)
-            k += n_per_step
-        t0 = time.perf_counter()
-        done_b = 0
-        for _ in range(args.steps):
-            idx = [order[k + j] for j in range(n_per_step)]
-            pool.map(_prefill_oracle_task, [tasks[i] for i in idx], chunksize=1)
-            done_b += sum(per[i] for i in idx)
-            k += n_per_step
-        t1 = time.perf_counter()
+        keep = [i for i, t in enumerate(tasks) if t[0].shape[0] > 0]
+        tasks, per = _per_head_slice([tasks[i] for i in keep], [per[i] for i in keep], w.Hq // w.Hkv)
+        done_b, secs, n_per_step = _bounded_oracle_loop(pool, _prefill_oracle_task, tasks, per, args.steps,
+                                                        args.warmup, cores)
+    t0, t1 = 0.0, secs
     val = round(done_b / (t1 - t0) / 1e9, 4)
-    sample = (f"each step: {n_per_step} of {w.B} sequences (all {w.Hq} heads) of {w.name}, "
-              f"float64 NumPy oracle, spawn pool of {cores} workers")
+    sample = (f"each step: {n_per_step} of the {len(tasks)} (sequence, kv head, 64-token slice) tasks of "
+              f"{w.name}, cycled; float64 NumPy oracle, spawn pool of {cores} workers")
     print(json.dumps({
         "impl": "reference", "metric": METRIC_PREFILL, "value": val, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -1578,12 +1620,17 @@ def run_reference_serving(args, world):
             work.append((row, len(sl), start + len(sl), list(sched.alloc.tables[rid])))
             row += len(sl)
         t = time.perf_counter()
-        done = 0
+        done = 0.0
+        G = Hq // Hkv
         for r0, n, L, tab in work:  # attention before the swap-ins, as on the device
-            if time.perf_counter() - t > budget:
-                break
-            paged_prefill(bq[r0: r0 + n], [0, n], kc, vc, np.asarray([tab]), np.array([L]), scale)
-            done += n
+            for g in range(Hkv):     # in (kv head, 64-token slice) pieces, within the step's budget
+                for t0 in range(0, n, 64):
+                    if time.perf_counter() - t > budget:
+                        break
+                    rows = [(x, h) for x in range(t0, min(n, t0 + 64)) for h in range(g * G, (g + 1) * G)]
+                    paged_prefill(bq[r0: r0 + n], [0, n], kc, vc, np.asarray([tab]), np.array([L]), scale,
+                                  rows=rows)
+                    done += len(rows) / Hq  # in query tokens
         for h, g in r.swap_in:
             kc[g], vc[g] = kh[h], vh[h]
         return done
@@ -1595,8 +1642,8 @@ def run_reference_serving(args, world):
     t1 = time.perf_counter()
     val = round(tokens / (t1 - t0), 2)
     sample = (f"{args.steps} iterations of {tr.name} after {args.warmup} warm-up: oracle scheduler, cache "
-              f"writes and swaps in full, attention of each iteration's items in order within "
-              f"{budget:.2f} s, one host process")
+              f"writes and swaps in full, attention of each iteration's items in (kv head, 64-token slice) "
+              f"pieces in order within {budget * 1e3:.1f} ms, one host process")
     print(json.dumps({
         "impl": "reference", "metric": METRIC_SERVING, "value": val, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round((t1 - t0) * 1e3 / args.steps, 3),
@@ -1622,33 +1669,20 @@ def run_reference(args, rank, world):
     fp8 = w.kv_dtype in ("fp8", "int8")
     e = 1 if fp8 else 2
     seqs = list(range(w.B))
+    seqs = [b for b in seqs if int(w.context_lens[b]) > 0]
     tasks = oracle_tasks(w, seqs, codes=w.kv_dtype if fp8 else None)
     per = [decode_bytes([int(w.context_lens[b])], w.Hq, w.Hkv, w.D, e, 2, 2) for b in seqs]
     if shared:  # unique bytes: each beam carries a 1/beams share of its group's prompt
         tails = sw.tail_lens.reshape(-1)
         per = [decode_bytes([int(tails[b])], w.Hq, w.Hkv, w.D, e, 2, 2)
                + sw.prompt_len * w.Hkv * w.D * 2 * e / sw.beams for b in seqs]
-    budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step
+    tasks, per = _per_kv_head(tasks, per)
     with _pool(cores) as pool:
-        t = time.perf_counter()
-        pool.map(_oracle_task, tasks[:cores], chunksize=1)
-        per_task = (time.perf_counter() - t) / max(1, min(cores, len(tasks))) * cores
-        n_per_step = int(max(1, min(len(tasks), budget / max(per_task / cores, 1e-6))))
-        order = [i % len(tasks) for i in range(n_per_step * (args.steps + args.warmup))]
-        k = 0
-        for _ in range(args.warmup):
-            pool.map(_oracle_task, [tasks[order[k + j]] for j in range(n_per_step)], chunksize=1)
-            k += n_per_step
-        t0 = time.perf_counter()
-        done_b = 0
-        for _ in range(args.steps):
-            idx = [order[k + j] for j in range(n_per_step)]
-            pool.map(_oracle_task, [tasks[i] for i in idx], chunksize=1)
-            done_b += sum(per[i] for i in idx)
-            k += n_per_step
-        t1 = time.perf_counter()
+        done_b, secs, n_per_step = _bounded_oracle_loop(pool, _oracle_task, tasks, per, args.steps, args.warmup,
+                                                        cores)
+    t0, t1 = 0.0, secs
     val = round(done_b / (t1 - t0) / 1e9, 4)
-    sample = (f"each step: {n_per_step} of {w.B} sequences (all {w.Hq} heads) of {w.name}, "
+    sample = (f"each step: {n_per_step} of the {len(tasks)} (sequence, kv head) tasks of {w.name}, cycled; "
               f"float64 NumPy oracle, spawn pool of {cores} workers")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
