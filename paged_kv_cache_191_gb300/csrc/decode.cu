@@ -31,7 +31,15 @@
 //   per-token V scale multiplies p before the PV product.
 // * A one-partition sequence is written directly; otherwise the partition
 //   writes (o, m, l) and decode_reduce merges the partitions with log-sum-exp
-//   weights, launched as a programmatic dependent.
+//   weights, launched as a programmatic dependent (triggered once every item
+//   has started, so its CTAs are resident when the last items finish).
+// * Shared prefixes (pa_decode_append_grouped; "LLM推理引擎深度实战" 2.2 and
+//   "大模型推理引擎优化：KV Cache 与连续批处理" 4.2 share blocks by refcount): the
+//   beams of one prompt hold the same blocks for the prompt.  A prefix item
+//   reads each shared tile once and scores it against the queries of every
+//   member of the group, as extra MMA columns (members x G <= 8).  Members'
+//   tails are ordinary items, and decode_reduce_grouped merges each member's
+//   prefix and tail partitions.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
