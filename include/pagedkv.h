@@ -92,9 +92,9 @@ typedef enum {
 typedef struct {
   int32_t num_blocks;    /* physical blocks in the pool, > 0 */
   int32_t num_kv_heads;  /* Hkv, > 0 */
-  int32_t head_dim;      /* D: 64 or 128 (FP8: 128) */
+  int32_t head_dim;      /* D: 64 or 128 (FP8 / INT8: 128) */
   int32_t block_size;    /* must be PA_BLOCK_SIZE */
-  int32_t kv_dtype;      /* pa_dtype: F16, BF16 or FP8_E4M3 */
+  int32_t kv_dtype;      /* pa_dtype: F16, BF16, FP8_E4M3 or INT8 */
 } pa_cache_desc;
 
 /* Message for the calling thread's last failed call ("" if none). */
