@@ -114,11 +114,13 @@ int32_t pa_version(void);
  * slot_mapping device int64 [num_tokens]; slot < 0 skips the row (padding).
  *              Slots must be distinct; a slot >= num_blocks*16 is skipped and
  *              flagged PA_DEVERR_SLOT_RANGE.
- * k_scale, v_scale  FP8 only (else NULL): device float32 [num_blocks][16].
- *              FP8 rows are quantised per token: amax = max|x| over all
- *              heads and dims of the token, scale = amax/448 (float32 RN
- *              division; 1 when amax = 0), code = E4M3(x/scale) with
- *              round-to-nearest-even and saturation to +-448.
+ * k_scale, v_scale  FP8 / INT8 caches only (else NULL): device float32
+ *              [num_blocks][16].  Rows are quantised per token: amax =
+ *              max|x| over all heads and dims of the token.  FP8: scale =
+ *              amax/448 (float32 RN division; 1 when amax = 0), code =
+ *              E4M3(x/scale) with round-to-nearest-even and saturation to
+ *              +-448.  INT8: scale = amax/127 (1 when amax = 0), code =
+ *              x/scale rounded half to even and clamped to [-127, 127].
  */
 pa_status pa_cache_write(const void* k, const void* v, int32_t in_dtype,
                          const int64_t* slot_mapping, int64_t num_tokens,
@@ -143,8 +145,9 @@ size_t pa_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_cont
  * context_lens[b] = 0 gives a zero row.
  *
  * q            device [B][num_q_heads][head_dim] in q_dtype.  For F16/BF16
- *              caches q_dtype must equal kv_dtype; for FP8 caches F16 or BF16.
- * k_scale, v_scale  FP8 caches only (else NULL), as in pa_cache_write.
+ *              caches q_dtype must equal kv_dtype; for FP8 / INT8 caches F16
+ *              or BF16.
+ * k_scale, v_scale  FP8 / INT8 caches only (else NULL), as in pa_cache_write.
  * block_tables device int32 [B][max_blocks_per_seq]; entries past
  *              ceil(context_lens[b]/16) are never read.
  * context_lens device int32 [B]; each must be <= max_context_len and
@@ -160,6 +163,10 @@ size_t pa_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_cont
  * Work: one CTA per (sequence, kv head, partition); all G query heads of a
  * kv head share every K/V tile load; partitions are merged by a second
  * kernel when more than one exists.
+ *
+ * Determinism: work is mapped statically and no atomic operation enters the
+ * arithmetic, so the same inputs, shape and split_tokens give bit-identical
+ * outputs on every run, whatever the physical block ids the tables name.
  */
 pa_status pa_decode(const void* q, int32_t q_dtype,
                     const void* k_cache, const void* v_cache,
@@ -176,7 +183,7 @@ pa_status pa_decode(const void* q, int32_t q_dtype,
  * pa_decode_append -- pa_cache_write of this step's tokens fused into
  * pa_decode: sequence b's new token (row b of k_new, v_new [B][Hkv][head_dim]
  * in new_dtype) is stored at slot_mapping[b] (< 0: none), then attention runs
- * as in pa_decode.  Results, cache contents and FP8 scales are identical to
+ * as in pa_decode.  Results, cache contents and FP8 / INT8 scales are identical to
  * the two calls in sequence; the store is done inside the decode launch by the
  * work item that reads that block, before it reads it.  Requires the
  * block-manager invariant that slot_mapping[b] is the slot of sequence b's
@@ -348,7 +355,7 @@ pa_status pa_decode_static_ws(const void* q, int32_t q_dtype,
  * [LLM-INF] 2.2 and [KV-CB] 4.2: before a shared block is written, its
  * contents are copied to a private block.  For each pair (src, dst) in
  * `pairs` (device int64 [num_pairs][2]) the whole K block, V block and, for
- * FP8, both 16-entry scale rows are copied.  No dst may repeat or appear as a
+ * FP8 / INT8 caches, both 16-entry scale rows are copied.  No dst may repeat or appear as a
  * src (the block manager never emits such pairs); ids outside the pool are
  * skipped and flagged PA_DEVERR_BLOCK_RANGE.
  */
@@ -360,8 +367,8 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_
  * pa_swap_blocks -- move whole blocks between two pools of the same shape,
  * for preemption and resume: a request's pages go to CPU memory when the GPU
  * runs short and come back when it is scheduled again ([LLM-INF] 3.2).
- * Each pool is laid out like a cache, k and v [num_blocks][Hkv][16][D] (+ FP8
- * scale rows [num_blocks][16]); either may be device memory or page-locked
+ * Each pool is laid out like a cache, k and v [num_blocks][Hkv][16][D] (+ FP8 /
+ * INT8 scale rows [num_blocks][16]); either may be device memory or page-locked
  * host memory that the device addresses directly (cudaHostAlloc /
  * cudaHostRegister under unified addressing, e.g. torch pin_memory()).
  * pairs: device-accessible int64 [num_pairs][2], (src block of the src pool,
@@ -577,14 +584,16 @@ void pa_serve_destroy(pa_serve* e);
  * must be launched before the next one is made. */
 pa_status pa_serve_plan(pa_serve* e, pa_sched_step_out* decisions, int64_t* num_tokens);
 /* Launch the planned iteration on `stream`: q: device [>= T][num_q_heads][D],
- * k_new / v_new: device [>= T][Hkv][D], all in_dtype (= the cache dtype),
+ * k_new / v_new: device [>= T][Hkv][D], all in_dtype (the cache dtype; F16
+ * or BF16 for FP8 / INT8 caches),
  * row t for the t-th new token (items in order; decodes come first); out:
  * device [>= T][num_q_heads][D] in in_dtype. */
 pa_status pa_serve_launch(pa_serve* e, const void* q, const void* k_new, const void* v_new, int32_t in_dtype,
                           void* out, void* stream);
 /* pa_serve_plan followed by pa_serve_launch.
  * One iteration.  q: device [>= T][num_q_heads][D], k_new / v_new: device
- * [>= T][Hkv][D], all in_dtype (= the cache dtype), row t for the t-th new
+ * [>= T][Hkv][D], all in_dtype (the cache dtype; F16 or BF16 for FP8 / INT8
+ * caches), row t for the t-th new
  * token of the step (items in order; decodes come first); out: device
  * [>= T][num_q_heads][D] in in_dtype.  decisions: arrays as for
  * pa_sched_step, or NULL to keep them internal.  Blocks the host only to
