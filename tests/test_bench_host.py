@@ -1,5 +1,7 @@
 """Host-side pieces of bench.py that need no GPU: reading the measured peak,
-and the algorithmic byte counts of a decode launch."""
+the algorithmic byte and flop counts of the decode and multi-token launches,
+and the DRAM-traffic record that is valid only for the kernel source it was
+taken on."""
 import json
 
 import numpy as np
@@ -37,3 +39,40 @@ def test_decode_bytes_formula():
     assert bench.decode_bytes(lens, Hq, Hkv, D, 2, 2, 4) == kv + tables + io
     # 1-byte codes add two float32 scales per token
     assert bench.decode_bytes(lens, Hq, Hkv, D, 1, 2, 4) == kv // 2 + int(lens.sum()) * 8 + tables + io
+
+
+class _PrefillShape:
+    def __init__(self, lens, qlens, Hq=4, Hkv=2, D=64, kv_dtype="f16"):
+        self.context_lens, self.q_lens = lens, qlens
+        self.Hq, self.Hkv, self.D, self.kv_dtype = Hq, Hkv, D, kv_dtype
+        self.T = int(sum(qlens))
+
+
+@pytest.mark.parametrize("kv", ["f16", "fp8"])
+def test_prefill_cost_by_brute_force(kv):
+    """Bytes: K+V of every context token once (+ two float32 scales per token for
+    1-byte caches), 16-bit q and out rows, table entries, lengths and q_start;
+    flops: 4 * D per (query row, visible key), counted key by key."""
+    lens, qlens = [1, 16, 17, 40, 5], [1, 3, 17, 40, 0]
+    w = _PrefillShape(lens, qlens, kv_dtype=kv)
+    e = 1 if kv == "fp8" else 2
+    keys = 0
+    for L, n in zip(lens, qlens):
+        for i in range(n):
+            keys += sum(1 for t in range(L) if t <= L - n + i)
+    kv_bytes = sum(lens) * w.Hkv * w.D * 2 * e + (sum(lens) * 8 if e == 1 else 0)
+    io = w.T * w.Hq * w.D * 2 * 2
+    meta = sum((L + 15) // 16 for L in lens) * 4 + len(lens) * 4 + (len(lens) + 1) * 4
+    assert bench.prefill_cost(w) == (kv_bytes + io + meta, 4 * w.D * w.Hq * keys)
+
+
+def test_traffic_record_follows_the_kernel_source(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic_decode_demo.txt").write_text(
+        "kernel: x\ndram_bytes_per_launch: 12345\nkernel_source_sha256_16: abc\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc")
+    assert bench.profiled_traffic("demo") == 12345.0
+    assert bench.profiled_traffic("other") is None  # no record for that workload
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "changed")
+    assert bench.profiled_traffic("demo") is None  # stale after a kernel edit
