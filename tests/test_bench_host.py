@@ -1,7 +1,7 @@
 """Host-side pieces of bench.py that need no GPU: reading the measured peak,
 the algorithmic byte and flop counts of the decode and multi-token launches,
-and the DRAM-traffic record that is valid only for the kernel source it was
-taken on."""
+the DRAM-traffic record that is valid only for the kernel source it was
+taken on, and the clock summary of the timed window."""
 import json
 
 import numpy as np
@@ -76,3 +76,27 @@ def test_traffic_record_follows_the_kernel_source(tmp_path, monkeypatch):
     assert bench.profiled_traffic("other") is None  # no record for that workload
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "changed")
     assert bench.profiled_traffic("demo") is None  # stale after a kernel edit
+
+
+def test_clock_summary_reads_the_timed_window():
+    import time as _t
+    base = _t.mktime(_t.strptime("2026/12/02 10:00:00", "%Y/%m/%d %H:%M:%S"))
+    s = bench.ClockSampler(0)
+    s.lines = [
+        "2026/12/02 10:00:00.100, 1200, 2070, 300.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:01.100, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 10:00:01.300, 2060, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:01.500, 2070, 2070, 940.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:03.000, 1000, 2070, 200.0, 0x0, Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ]
+    got = s.summary(base + 1.0, base + 1.6)
+    assert got["samples"] == 3 and got["window"] == "timed region"
+    assert got["sm_mhz"] == 2070.0 and got["sm_max_mhz"] == 2070.0
+    assert got["reasons"] == ["sw_power_cap"]  # the hw_slowdown sample lies outside the window
+    # a timed region between two samples falls back to the whole run
+    got = s.summary(base + 2.0, base + 2.01)
+    assert got["samples"] == 5 and got["window"].startswith("whole run")
+    assert got["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    s.lines = []
+    assert s.summary(0, 1)["samples"] == 0
