@@ -49,21 +49,27 @@ METRIC_SERVING = "continuous-batching serving iterations: tokens/s through sched
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=3000)
-    p.add_argument("--warmup", type=int, default=50)
-    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--gpus", type=int, default=1,
+                   help="GPUs of the job (N > 1: launch one process per GPU with torch.distributed.run)")
+    p.add_argument("--steps", type=int, default=3000, help="timed steps")
+    p.add_argument("--warmup", type=int, default=50, help="untimed warm-up steps before them")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours",
+                   help="reference: the float64 oracle on the host cores, bounded samples per step")
     p.add_argument("--config", default="llama7b_b32",
                    choices=["tiny", "llama7b_b32", "gqa70b_b64", "longctx_b8_f16", "longctx_b8_fp8", "longctx_b8_int8",
-                            "shared_prefix_16x4"] + list(PREFILL_CONFIGS) + list(SERVING_CONFIGS))
+                            "shared_prefix_16x4"] + list(PREFILL_CONFIGS) + list(SERVING_CONFIGS),
+                   help="workload: decode batches (default llama7b_b32), beam search over shared prompts, "
+                        "multi-token attention mixes, or continuous-batching serving iterations")
     p.add_argument("--split", type=int, default=0, help="split_tokens (0 = library choice)")
-    p.add_argument("--e2e-steps", type=int, default=300)
+    p.add_argument("--e2e-steps", type=int, default=300,
+                   help="steps of the end-to-end measurement (host buffers in and out, waited per step)")
     p.add_argument("--unfused", action="store_true",
                    help="pa_cache_write + pa_decode instead of the fused pa_decode_append")
-    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the oracle on the host cores")
     p.add_argument("--ungrouped", action="store_true",
                    help="shared_prefix_16x4: read shared prompt blocks once per beam (pa_decode_append)")
-    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="wall-clock budget of the oracle baseline sample")
     return p.parse_args(argv)
 
 
