@@ -68,6 +68,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the oracle on the host cores")
     p.add_argument("--ungrouped", action="store_true",
                    help="shared_prefix_16x4: read shared prompt blocks once per beam (pa_decode_append)")
+    p.add_argument("--headline-only", action="store_true",
+                   help="time only --config (by default every decode workload runs and appears under `workloads`)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="wall-clock budget of the oracle baseline sample")
     return p.parse_args(argv)
@@ -161,9 +163,12 @@ def profiled_traffic(config):
 
 
 class ClockSampler:
+    """nvidia-smi clock / throttle samples over the whole run; summaries are
+    taken over the wall-clock windows in which the measured launches ran."""
     QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, index):
         self.proc = None
@@ -174,7 +179,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -189,8 +194,9 @@ class ClockSampler:
             self.proc.kill()
             out, _ = self.proc.communicate()
         self.lines = [l for l in out.splitlines() if l.strip()]
+        self.proc = None
 
-    def summary(self, t0, t1):
+    def rows(self):
         rows = []
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
@@ -202,19 +208,24 @@ class ClockSampler:
                 rows.append((ts, float(f[1]), float(f[2]), f[5:9]))
             except (ValueError, IndexError):
                 continue
+        return rows
+
+    def summary(self, windows, label="timed region"):
+        """Median SM clock, max clock and active throttle reasons over the
+        samples that fall inside any (t0, t1) wall-clock window."""
+        rows = self.rows()
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "window": "no nvidia-smi samples"}
-        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
-        window = "timed region"
+        inside = [r for r in rows if any(t0 <= r[0] <= t1 for t0, t1 in windows)]
         if not inside:
-            inside = rows
-            window = "whole run (timed region shorter than the 100 ms sampling period)"
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": f"no sample inside the {label} ({len(rows)} samples in the run)"}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in inside),
                 "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
-                "samples": len(inside), "window": window}
+                "samples": len(inside), "window": label}
 
 
 # ---- thin CUDA driver access for the timed loop (copies and events) --------------
@@ -681,23 +692,29 @@ class SharedPrefixStep(DecodeStep):
         return dec_u, step_u, dec_l
 
 
-def run_ours(args, rank, world, local_rank):
-    import torch
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w = load_workload(args.config)
-    shared = args.config == "shared_prefix_16x4"
+DECODE_WORKLOADS = ("llama7b_b32", "gqa70b_b64", "longctx_b8_f16", "longctx_b8_fp8", "longctx_b8_int8",
+                    "shared_prefix_16x4")
+CLOCK_HOLD_S = 0.6   # the sampler's period is 50 ms: hold a short timed region's load this long
+
+
+def build_step(name, args, dev):
+    """Device state and host logic of one decode workload."""
+    w = load_workload(name)
+    shared = name == "shared_prefix_16x4"
     st = (SharedPrefixStep if shared else DecodeStep)(w, args.split, args.steps + args.warmup, dev)
     st.fused = not args.unfused
     if shared:
         st.grouped = not args.ungrouped
-    stream = torch.cuda.Stream(device=dev)
-    total_steps = args.warmup + args.steps
-    st.prebuild(stream)
+    return w, st, shared
+
+
+def time_steps(st, shared, stream, args, world):
+    """W warm-up steps, a barrier, then exactly K steps between two events on
+    the launch stream, each decode launch bracketed by its own event pair."""
+    import torch
     dec_events = [(st.drv.event(True), st.drv.event(True)) for _ in range(args.steps)]
     t_start, t_end = st.drv.event(True), st.drv.event(True)
-    clocks = ClockSampler(local_rank)
-    clocks.start()
+    r = {}
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             st.enqueue(st.host_prepare())
@@ -719,24 +736,107 @@ def run_ours(args, rank, world, local_rank):
         st.drv.record(t_end, st.sp)
         host_done = time.time()
         if shared:
-            dec_b, step_b, dec_logical = st.count_bytes()
-            copies = sum(h[2] for h in st.history) / args.steps
-            cow_launches = sum(1 for h in st.history if h[2] > 0)  # one pa_copy_blocks per copying step
+            dec_b, step_b, r["dec_logical"] = st.count_bytes()
+            r["copies"] = sum(h[2] for h in st.history) / args.steps
+            r["cow_launches"] = sum(1 for h in st.history if h[2] > 0)  # one pa_copy_blocks per copying step
         stream.synchronize()
         wall1 = time.time()
     torch.cuda.synchronize()
     barrier(world)
-    clocks.stop()
     errs = st.ops.device_errors(clear=True)
     if errs:
         raise RuntimeError(f"device error flags {errs:#x} during the benchmark")
-    local_s = st.drv.elapsed_ms(t_start, t_end) / 1e3
-    dec_ms = sum(st.drv.elapsed_ms(a, b) for a, b in dec_events) / args.steps
+    r.update(local_s=st.drv.elapsed_ms(t_start, t_end) / 1e3,
+             dec_list=[st.drv.elapsed_ms(a, b) for a, b in dec_events],
+             dec_b=dec_b, step_b=step_b, wall0=wall0, wall1=wall1, host_done=host_done,
+             blocked_s=st.blocked_s)
+    r["dec_ms"] = sum(r["dec_list"]) / args.steps
+    return r
+
+
+def decode_call(st):
+    """(function, arguments) of the last step's decode launch: re-issuing it
+    rewrites the same slots with the same rows, so every repeat is the same work."""
+    i = st.dbuf ^ 1
+    if st.fused and getattr(st, "grouped", False) and isinstance(st, SharedPrefixStep):
+        return st.L.pa_decode_append_grouped, st.grouped_args[i]
+    if st.fused:
+        return st.L.pa_decode_append, st.append_args[i]
+    return st.L.pa_decode, st.decode_args[i]
+
+
+def clock_windows(st, stream, r):
+    """Wall-clock windows in which this workload's decode launches ran: the
+    timed region and, when it is shorter than CLOCK_HOLD_S, the same launch
+    re-issued back to back (untimed) until it has run that long, so that the
+    clock sampler sees the SM clock under this load."""
+    import torch
+    windows = [(r["wall0"], r["wall1"])]
+    label = "timed region"
+    span = r["wall1"] - r["wall0"]
+    if span < CLOCK_HOLD_S:
+        fn, fargs = decode_call(st)
+        n = max(1, int((CLOCK_HOLD_S - span) / max(r["dec_ms"] / 1e3, 1e-6)))
+        with torch.cuda.stream(stream):
+            stream.synchronize()
+            h0 = time.time()
+            for k in range(n):
+                st.ops._check(fn(*fargs), "decode")
+                if k % 256 == 255:  # keep the launch queue short
+                    stream.synchronize()
+            stream.synchronize()
+            h1 = time.time()
+        windows.append((h0, h1))
+        label = (f"timed region ({span * 1e3:.1f} ms) + {n} more launches of the last step's decode, "
+                 f"back to back, {(h1 - h0) * 1e3:.0f} ms")
+    return windows, label
+
+
+def launch_kernel_name(st, shared):
+    if shared and st.fused and st.grouped:
+        return ("pa_decode_append_grouped (decode_main over shared-prefix groups with the fused "
+                "cache write + decode_reduce_grouped)")
+    if st.fused:
+        return "pa_decode_append (decode_main with the fused cache write + decode_reduce)"
+    return "pa_decode (decode_main + decode_reduce)"
+
+
+def workload_entry(name, w, st, shared, r, args, peak, clock):
+    """One decode workload's figures for the JSON line's `workloads` table."""
+    avg = r["dec_b"] / args.steps
+    achieved = avg / (r["dec_ms"] / 1e3) / 1e9
+    e = {"kv_dtype": w.kv_dtype, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+         "launch_ms": round(r["dec_ms"], 5), "per_launch_ms": pct(r["dec_list"]),
+         "bytes_per_launch": int(avg), "kv_gbs": round(achieved, 2), "frac": round(achieved / peak, 4),
+         "tokens_per_s": round(st.B / (r["dec_ms"] / 1e3), 1),
+         "ms_per_step": round(r["local_s"] * 1e3 / args.steps, 5),
+         "step_gbs": round(r["step_b"] / r["local_s"] / 1e9, 2),
+         "gpu_launches": st.launches_per_step() * args.steps + r.get("cow_launches", 0),
+         "kernel": launch_kernel_name(st, shared), "traffic": profiled_traffic(name), "clocks": clock}
+    if shared:
+        e["bytes"] = "unique physical bytes (shared blocks once per step)"
+        e["logical_kv_gbs"] = round(r["dec_logical"] / args.steps / (r["dec_ms"] / 1e3) / 1e9, 2)
+        e["copies_per_step"] = round(r["copies"], 2)
+    return e
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    clocks = ClockSampler(local_rank)
+    clocks.start()  # before set-up: the sampler's first lines take a moment to arrive
+    w, st, shared = build_step(args.config, args, dev)
+    stream = torch.cuda.Stream(device=dev)
+    st.prebuild(stream)
+    r = time_steps(st, shared, stream, args, world)
+    local_s, dec_ms, dec_b, step_b = r["local_s"], r["dec_ms"], r["dec_b"], r["step_b"]
     max_s, tot_bytes = aggregate(local_s, float(step_b), world)
     _, tot_tokens = aggregate(local_s, float(st.B * args.steps), world)
+    windows, label = clock_windows(st, stream, r)
 
     # e2e: public Python API, host (pinned) inputs in, result out, every step
-    dec_list = [st.drv.elapsed_ms(a, b) for a, b in dec_events]
+    dec_list = r["dec_list"]
     timing = timing_detail(st, stream, dec_list) if not shared else {"per_launch_ms": pct(dec_list)}
     e2e = run_e2e(st, args, stream)
     swap = measure_swap(st, stream)
@@ -747,6 +847,34 @@ def run_ours(args, rank, world, local_rank):
     avg_dec_bytes = dec_b / args.steps
     achieved = avg_dec_bytes / (dec_ms / 1e3) / 1e9
     traffic = profiled_traffic(args.config)
+    head_entry = workload_entry(args.config, w, st, shared, r, args, peak, None)
+    launches = head_entry["gpu_launches"]
+    del st
+    torch.cuda.empty_cache()
+
+    # every other decode workload, same steps / warm-up, in the same process
+    others = {}
+    if not args.headline_only:
+        for name in DECODE_WORKLOADS:
+            if name == args.config:
+                continue
+            ow, ost, oshared = build_step(name, args, dev)
+            ost.prebuild(stream)
+            orr = time_steps(ost, oshared, stream, args, world)
+            ow_windows, ow_label = clock_windows(ost, stream, orr)
+            entry = workload_entry(name, ow, ost, oshared, orr, args, peak, None)
+            others[name] = (entry, ow_windows, ow_label)
+            launches += entry["gpu_launches"]
+            del ow, ost
+            torch.cuda.empty_cache()
+    clocks.stop()
+    all_windows = list(windows)
+    head_entry["clocks"] = clocks.summary(windows, label)
+    workloads = {args.config: head_entry}
+    for name, (entry, ow_windows, ow_label) in others.items():
+        entry["clocks"] = clocks.summary(ow_windows, ow_label)
+        all_windows += ow_windows
+        workloads[name] = entry
     res = {
         "metric": METRIC,
         "value": round(tot_bytes / max_s / 1e9, 2),
@@ -764,42 +892,48 @@ def run_ours(args, rank, world, local_rank):
         "config": {
             "workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
             "block_size": 16, "kv_dtype": w.kv_dtype,
-            "context_lens": f"start {int(st.lens0.min())}..{int(st.lens0.max())} (mean {st.lens0.mean():.0f}),"
-                            f" +1 per step, batch re-admitted every {RESET_EVERY} steps",
+            "context_lens": f"start {int(st_lens0(w, shared).min())}..{int(st_lens0(w, shared).max())} "
+                            f"(mean {st_lens0(w, shared).mean():.0f}), +1 per step, batch re-admitted every "
+                            f"{RESET_EVERY} steps",
             **({"sharing": "16 groups x 4 beams share a 1024-token prompt; beams reselected from "
                            "parents every step (fork + release), copy-on-write before each decode; "
                            "bytes count shared blocks once (logical bytes reported separately)",
                 "prompt_reads": ("once per group of 4 beams (pa_decode_append_grouped)"
-                                 if st.fused and st.grouped else "once per beam")}
+                                 if not args.unfused and not args.ungrouped else "once per beam")}
                if shared else {}),
             "split_tokens": args.split or "auto",
             "l2": f"no flush: K+V per step {avg_dec_bytes / 1e6:.0f} MB vs 129 MB L2",
             "parallelism": f"replicas x{world}",
         },
         "tokens_per_s": round(tot_tokens / max_s, 1),
-        **({"logical_decode_gbs": round(dec_logical / args.steps / (dec_ms / 1e3) / 1e9, 2),
-            "copies_per_step": round(copies, 2)} if shared else {}),
-        "host_us_per_step": {"busy": round((host_done - wall0 - st.blocked_s) * 1e6 / args.steps, 2),
-                             "blocked_on_gpu": round(st.blocked_s * 1e6 / args.steps, 2)},
+        **({"logical_decode_gbs": round(r["dec_logical"] / args.steps / (dec_ms / 1e3) / 1e9, 2),
+            "copies_per_step": round(r["copies"], 2)} if shared else {}),
+        "host_us_per_step": {"busy": round((r["host_done"] - r["wall0"] - r["blocked_s"]) * 1e6 / args.steps, 2),
+                             "blocked_on_gpu": round(r["blocked_s"] * 1e6 / args.steps, 2)},
         "kv_gbs_decode_only": round(achieved, 2),
         "pct_of_nominal_8TBs": round(100 * tot_bytes / max_s / 1e9 / NOMINAL_HBM_GBS, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "traffic": traffic,
-                     "kernel": ("pa_decode_append_grouped (decode_main over shared-prefix groups with the fused "
-                                "cache write + decode_reduce_grouped)" if shared and st.fused and st.grouped else
-                                "pa_decode_append (decode_main with the fused cache write + decode_reduce)"
-                                if st.fused else "pa_decode (decode_main + decode_reduce)"),
+                     "traffic": traffic, "kernel": head_entry["kernel"],
                      "bytes_per_launch": int(avg_dec_bytes), "launch_ms": round(dec_ms, 5)},
         "timing": timing,
         "e2e": e2e,
         "swap": swap,
-        "gpu_launches": st.launches_per_step() * args.steps + (cow_launches if shared else 0),
-        "clocks": clocks.summary(wall0, wall1),
+        "gpu_launches": launches,
+        "clocks": clocks.summary(all_windows, "timed regions of every workload in this line (and their "
+                                              "clock holds)"),
         "cpu_baseline": cpu,
+        "workloads": workloads,
     }
     if rank == 0:
         print(json.dumps(res), flush=True)
+
+
+def st_lens0(w, shared):
+    """Starting context lengths of a decode workload (shared prefix: prompt + tail)."""
+    if shared:
+        return np.full(w.B, w.prompt_len) + w.tail_lens.reshape(-1)
+    return np.asarray(w.context_lens, dtype=np.int64)
 
 
 def pct(xs):
@@ -1236,7 +1370,7 @@ def run_prefill(args, rank, world, local_rank):
                      "launch_ms": round(k_ms, 5)},
         "e2e": e2e,
         "gpu_launches": st.launches_per_step() * args.steps,
-        "clocks": clocks.summary(wall0, wall1),
+        "clocks": clocks.summary([(wall0, wall1)]),
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -1395,7 +1529,7 @@ def run_serving(args, rank, world, local_rank):
                 "api": "paged_kv_cache_191_gb300.serving.ServingLoop plan / launch: the iteration's q / K / V "
                        "rows in from pinned host memory, its attention output back, stream sync per iteration"},
         "gpu_launches": int(stats["attn_launches"]),
-        "clocks": clocks.summary(wall0, wall1),
+        "clocks": clocks.summary([(wall0, wall1)]),
         "cpu_baseline": None,
     }
     if rank == 0:

@@ -331,9 +331,17 @@ pa_status pa_chunked_prefill(const void* q, int32_t q_dtype, const int32_t* q_st
  * inputs and outputs.
  * - A shape whose pa_decode_workspace_size exceeds PA_STATIC_WS_BYTES returns
  *   PA_ERR_INVALID and launches nothing.
- * - The first call made with a device current sets the array up on that
- *   device (one cudaGetSymbolAddress); make it before any stream capture.
- *   The array stays resident on that device until the process exits.
+ * - The first call made in a context looks the array's address up there
+ *   (one cudaGetSymbolAddress) and caches it under the context's unique id,
+ *   so a call in another context -- a second context on the device, or the
+ *   new primary context after cudaDeviceReset -- looks it up again.  Make the
+ *   first call in a context before any stream capture.
+ * - Residency: with lazy module loading (the CUDA default) the array takes
+ *   PA_STATIC_WS_BYTES of device memory in a context from the first call of
+ *   this entry point there; with CUDA_MODULE_LOADING=EAGER in every context
+ *   the library's device code is loaded into, whether or not this entry point
+ *   is ever called.  It stays until the context is destroyed or the process
+ *   exits.
  * - All calls on a device share the array, which keeps the last call's
  *   contents; calls whose kernels overlap on the GPU race on it, so
  *   serialise them (one stream, or events).

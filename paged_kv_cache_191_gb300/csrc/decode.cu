@@ -58,6 +58,10 @@ __device__ uint32_t g_decode_err;
 #define PA_RING_KB 16  // two 8 KB stages for 16-bit D=128: ~12 CTAs per SM
 #endif
 constexpr int kRingBytes = PA_RING_KB * 1024;  // K/V stage ring of one warp-CTA
+#ifndef PA_L2_PF
+#define PA_L2_PF 0  // tiles of a warp prefetched into L2 beyond its shared-memory ring
+#endif
+constexpr int kL2Ahead = PA_L2_PF;
 constexpr int kMaxDevices = 64;
 
 struct DecodeArgs {
@@ -411,11 +415,31 @@ __global__ void __launch_bounds__(32 * W)
       dev::bulk_load(dev::smem_addr(s_scale + s * 32 + 16), a.v_scale + static_cast<size_t>(pb) * 16, 64, bar);
     }
   };
+  auto prefetch = [&](int pb) {  // lane 0 only: the tile's K and V into L2
+    if constexpr (TL::ONE_BOX) {
+      dev::tma_prefetch_l2_5d(&tmK, 0, 0, 0, g, pb);
+      dev::tma_prefetch_l2_5d(&tmV, 0, 0, 0, g, pb);
+    } else {
+#pragma unroll
+      for (int bx = 0; bx < TL::NBOX; ++bx) {
+        dev::tma_prefetch_l2_3d(&tmK, bx * TL::BOXE, g * 16, pb);
+        dev::tma_prefetch_l2_3d(&tmV, bx * TL::BOXE, g * 16, pb);
+      }
+    }
+  };
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
     const int j = wid + i * W;
     const int pb = block_id(min(j, 63));
     if (j < nb && lane == 0) issue(pb, i);
+  }
+  if constexpr (kL2Ahead > 0) {
+#pragma unroll
+    for (int i = NS; i < NS + kL2Ahead; ++i) {
+      const int j = wid + i * W;
+      const int pb = block_id(min(j, 63));
+      if (j < nb && lane == 0) prefetch(pb);
+    }
   }
 
   // Every CTA of this grid has started once all of them pass here, so the
@@ -434,6 +458,7 @@ __global__ void __launch_bounds__(32 * W)
     if (j >= nb) break;
     const int s = i % NS;
     const int next_pb = block_id(min(j + NS * W, 63));  // block id of the refill (all lanes shuffle)
+    const int pf_pb = kL2Ahead > 0 ? block_id(min(j + (NS + kL2Ahead) * W, 63)) : 0;
     if (!dev::mbar_wait_bounded(bar_full + 8 * s, (i / NS) & 1)) {
       if (lane == 0) atomicOr(&g_decode_err, PA_DEVERR_TIMEOUT);
       // let this warp's other copies in flight land (bounded), then stop
@@ -509,6 +534,9 @@ __global__ void __launch_bounds__(32 * W)
     if (lane == 0 && j + NS * W < nb) {
       dev::fence_proxy_async_smem();
       issue(next_pb, s);
+    }
+    if constexpr (kL2Ahead > 0) {
+      if (lane == 0 && j + (NS + kL2Ahead) * W < nb) prefetch(pf_pb);
     }
 
     // ---- S^T = K . Q^T -----------------------------------------------------

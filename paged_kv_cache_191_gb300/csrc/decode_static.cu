@@ -11,16 +11,26 @@
 // - Size: PA_STATIC_WS_BYTES (32 MiB).  Shapes whose workspace
 //   (pa_decode_workspace_size) is larger are rejected with PA_ERR_INVALID
 //   before anything is launched.
-// - Residency: the array is part of the library's device code, so it occupies
-//   32 MiB on every device where this entry point has been used, until the
-//   process exits.
-// - Set-up: the first call made with a device current looks up the array's
-//   device address on that device (cudaGetSymbolAddress, once per device,
-//   return code checked).  Make that first call before any stream capture.
-// - Sharing: every call on a device uses the same array and it keeps the last
-//   call's contents.  Nothing in it needs clearing (every partial a call reads
-//   was written earlier in the same call), but two calls whose kernels overlap
-//   on the GPU race on it: serialise such calls (one stream, or events).
+// - Residency: the array is the device code of this file's module, which
+//   holds no kernel.  Under lazy module loading (the CUDA default) that
+//   module, and so the 32 MiB, is loaded into a context by the first call of
+//   this entry point there; with eager loading (CUDA_MODULE_LOADING=EAGER) it
+//   is loaded into every context the library's modules are loaded into,
+//   whether or not this entry point is ever called.  Either way it stays
+//   until the context is destroyed or the process exits.
+// - Set-up: the first call made in a context looks up the array's device
+//   address there (cudaGetSymbolAddress, return code checked) and caches it
+//   under the context's unique id (cuCtxGetId).  A later call in another
+//   context -- a second context on the device, or the new primary context
+//   after cudaDeviceReset -- looks it up again, so a stale address is never
+//   launched.  Make the first call in a context before any stream capture.
+// - Sharing: every call in a context uses the same array and it keeps the
+//   last call's contents.  Nothing in it needs clearing (every partial a call
+//   reads was written earlier in the same call), but two calls whose kernels
+//   overlap on the GPU race on it: serialise such calls (one stream, or
+//   events).
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "pa_internal.h"
@@ -30,26 +40,67 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_ws[PA_STATIC_WS_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_setup_mu;
-void* g_static_ws_addr[kMaxDevices] = {};  // device address of g_static_ws, per device
 
-// Device address of the static scratch on the current device (set up once).
+// The array's address as last looked up on a device, and the context it
+// belongs to.
+struct WsAddr {
+  bool valid = false;
+  unsigned long long ctx_id = 0;
+  void* addr = nullptr;
+};
+std::mutex g_setup_mu;
+WsAddr g_ws[kMaxDevices];
+
+// Unique id of the context current on this thread; false when there is none
+// yet (the runtime creates the primary context lazily) or it cannot be read.
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the static scratch in the current context.  The cached
+// address is reused only while the current context is the one it was looked
+// up in; anything else (no context yet, an id that cannot be read, another
+// context) looks it up again.
 pa_status static_ws_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return pa::fail(PA_ERR_CUDA, "pa_decode_static_ws: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices)
     return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_static_ws: device index %d >= %d", dev, kMaxDevices);
+  unsigned long long id = 0;
+  bool have_id = current_context_id(&id);
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_static_ws_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_ws);
-    if (e != cudaSuccess || !p)
-      return pa::fail(PA_ERR_CUDA, "pa_decode_static_ws: cudaGetSymbolAddress failed: %s",
-                      cudaGetErrorString(e));
-    g_static_ws_addr[dev] = p;
+  WsAddr& c = g_ws[dev];
+  if (have_id && c.valid && c.ctx_id == id) {
+    *out = c.addr;
+    return PA_OK;
   }
-  *out = g_static_ws_addr[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_ws);
+  if (e != cudaSuccess || !p)
+    return pa::fail(PA_ERR_CUDA, "pa_decode_static_ws: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+  if (!have_id) have_id = current_context_id(&id);  // the lookup made the primary context current
+  c.valid = have_id;
+  c.ctx_id = id;
+  c.addr = p;
+  *out = p;
   return PA_OK;
 }
 

@@ -90,13 +90,16 @@ def test_clock_summary_reads_the_timed_window():
         "2026/12/02 10:00:03.000, 1000, 2070, 200.0, 0x0, Active, Not Active, Not Active, Not Active",
         "garbage line",
     ]
-    got = s.summary(base + 1.0, base + 1.6)
+    got = s.summary([(base + 1.0, base + 1.6)])
     assert got["samples"] == 3 and got["window"] == "timed region"
     assert got["sm_mhz"] == 2070.0 and got["sm_max_mhz"] == 2070.0
     assert got["reasons"] == ["sw_power_cap"]  # the hw_slowdown sample lies outside the window
-    # a timed region between two samples falls back to the whole run
-    got = s.summary(base + 2.0, base + 2.01)
-    assert got["samples"] == 5 and got["window"].startswith("whole run")
+    # several windows: the timed region plus a clock hold that covers the late sample
+    got = s.summary([(base + 1.0, base + 1.2), (base + 2.9, base + 3.1)], "timed region + hold")
+    assert got["samples"] == 2 and got["window"] == "timed region + hold"
     assert got["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    # a window between two samples holds none: reported as such, never the whole run
+    got = s.summary([(base + 2.0, base + 2.01)])
+    assert got["samples"] == 0 and got["sm_mhz"] is None and "no sample inside" in got["window"]
     s.lines = []
-    assert s.summary(0, 1)["samples"] == 0
+    assert s.summary([(0, 1)])["samples"] == 0

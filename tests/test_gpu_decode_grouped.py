@@ -153,3 +153,81 @@ def test_mismatched_tables_and_bad_groups_are_flagged():
     w, start = grouped_case(94, [3, 2], [4, 2], 8, 8, "f16")
     run(w, start, [4, 2], max_size=2)  # a group of 3 above the stated bound: skipped
     assert ops.device_errors(clear=True) & ops.DEVERR_GROUP
+
+
+# ---- the shared-prefix beam-search workload at its stated size -------------------------
+def test_shared_prefix_16x4_full_size():
+    """16 groups x 4 beams, a 1024-token prompt shared by every beam of its
+    group (64 blocks at refcount 4) and tails of 1-256 tokens, stepped the way
+    the benchmark steps it: beam reselection, one appended slot per beam with
+    copy-on-write where siblings share a partial block, pa_copy_blocks, then
+    the grouped fused write + decode over the whole batch.  The C++ block
+    manager and the oracle's model run in lockstep (slots, copy pairs and
+    tables identical), caches stay bit-identical to the oracle's, and every
+    (beam, head) row matches the float64 oracle within the f16 tolerance --
+    the grouped call and the plain fused call alike.
+
+    Source: "大模型推理引擎优化：KV Cache 与连续批处理" 4.2 and
+    "LLM推理引擎深度实战：从PagedAttention到分布式推理部署" 2.2 (shared blocks
+    by refcount, copied on write)."""
+    from oracle.allocator import BlockAllocator as OAlloc
+    from oracle.cache_ops import copy_blocks as o_copy
+
+    w = W.config_shared_prefix()
+    B, beams = w.B, w.beams
+    ca = ops.BlockAllocator(w.num_blocks, w.free_order)
+    oa = OAlloc(w.num_blocks, w.free_order)
+    roots = [10 ** 9 + g for g in range(w.groups)]
+    for r in roots:
+        ca.alloc_seq(r, w.prompt_len)
+        oa.alloc_seq(r, w.prompt_len)
+    ids = list(range(B))
+    parents = [roots[i // beams] for i in range(B)]
+    ca.fork_seqs(parents, ids)
+    oa.fork_seqs(parents, ids)
+    tails = w.tail_lens.reshape(-1)
+    for i in ids:
+        got = ca.append_tokens(i, int(tails[i]))
+        want = oa.append_tokens(i, int(tails[i]))
+        assert got == (want[0], want[1]) and want[1][0] < 0  # the prompt fills its last block
+    kc, vc = w.k_pool.to(DEV), w.v_pool.to(DEV)
+    okc, ovc = np_exact(w.k_pool), np_exact(w.v_pool)
+    cap = -(-(w.prompt_len + int(tails.max()) + 8) // 16)
+    gs = torch.arange(0, B + 1, beams, dtype=torch.int32, device=DEV)
+    pre = torch.full((w.groups,), w.prompt_len // 16, dtype=torch.int32, device=DEV)
+    rng = W.rng_for(23)
+    q = w.q.to(DEV)
+    total_cow = 0
+    for step in range(3):
+        par = (np.arange(w.groups)[:, None] * beams + w.parents[step]).reshape(-1).tolist()
+        ca.reselect(ids, par)
+        oa.reselect(ids, par)
+        slots, pairs = ca.append_slots(ids)
+        want = oa.append_slots(ids)
+        assert slots == [x[0] for x in want]
+        assert pairs == [(x[1], x[2]) for x in want if x[1] >= 0]
+        tables, lens = ca.tables(ids, cap)
+        for i, s in enumerate(ids):
+            tab, n = oa.table(s)
+            assert list(tables[i][:len(tab)]) == tab and lens[i] == n
+        total_cow += len(pairs)
+        if pairs:
+            ops.copy_blocks(kc, vc, torch.tensor(pairs, dtype=torch.int64, device=DEV))
+            okc, ovc, _, _ = o_copy(okc, ovc, pairs)
+        nk = W.randn(rng, (B, w.Hkv, w.D), torch.float16)
+        nv = W.randn(rng, (B, w.Hkv, w.D), torch.float16)
+        sl = torch.tensor(slots, dtype=torch.int64, device=DEV)
+        bt, cl = torch.from_numpy(tables).to(DEV), torch.from_numpy(lens).to(DEV)
+        ml = int(lens.max())
+        out = ops.decode_append_grouped(nk.to(DEV), nv.to(DEV), sl, q, kc, vc, bt, cl, ml, w.scale, gs, pre, beams,
+                                        w.prompt_len // 16, out_dtype=torch.float32)
+        # the plain fused call on the same state: it stores the same rows again
+        plain = ops.decode_append(nk.to(DEV), nv.to(DEV), sl, q, kc, vc, bt, cl, ml, w.scale,
+                                  out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        okc, ovc, _, _ = o_write(np_exact(nk), np_exact(nv), np.array(slots), okc, ovc)
+        ref = paged_decode(np_exact(w.q), okc, ovc, tables, lens, w.scale)
+        assert_close(out.cpu().numpy(), ref, TOL["f16"], f"grouped step {step}")
+        assert_close(plain.cpu().numpy(), ref, TOL["f16"], f"plain step {step}")
+    assert total_cow > 0, "reselection is meant to exercise copy-on-write"
+    assert np.array_equal(np_exact(kc), okc) and np.array_equal(np_exact(vc), ovc)

@@ -79,3 +79,17 @@ def test_shapes_beyond_the_static_array_are_rejected():
     assert b"static array" in ops.lib().pa_last_error()
     torch.cuda.synchronize()
     assert not out.any(), "a rejected call must launch nothing"
+
+
+def test_static_scratch_follows_the_current_context():
+    """The array's address is per context: calls in the primary context, in a
+    second context on the same device, and in the primary context again must
+    each use their own context's copy (a child process drives the contexts
+    through the driver API, without torch)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-m", "tests.static_ws_contexts"], cwd=root, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), r.stdout + r.stderr
