@@ -79,6 +79,14 @@ pa_status plan_decode(int32_t B, int32_t Hq, int32_t max_context_len, const pa_c
   } else {
     plan->workspace_bytes = 0;
   }
+  // 16-bit caches run the dynamic schedule: the workspace also holds its two
+  // control words (padded to 256 bytes) and the item list (8 bytes an item)
+  plan->dynamic = PA_DECODE_DYN && !quantised(d->kv_dtype);
+  plan->dyn_offset = plan->workspace_bytes;
+  if (plan->dynamic) {
+    const size_t items = static_cast<size_t>(B) * d->num_kv_heads * parts;
+    plan->workspace_bytes += (256 + items * 8 + 255) & ~static_cast<size_t>(255);
+  }
   return PA_OK;
 }
 
@@ -208,6 +216,7 @@ static pa_status plan_grouped(int32_t B, int32_t Hq, int32_t max_context_len, co
   if (pre + static_cast<int64_t>(gr.max_size) * tail > 65535 ||
       static_cast<int64_t>(gr.n) * d->num_kv_heads * gr.max_size > (int64_t{1} << 31) - 1)
     return fail(PA_ERR_UNSUPPORTED, "pa_decode_append_grouped: grid too large");
+  plan->dynamic = 0;  // groups run on the static grid
   plan->pre_parts = static_cast<int32_t>(pre);
   plan->tail_parts = static_cast<int32_t>(tail);
   plan->max_parts = static_cast<int32_t>(pre + tail);

@@ -71,12 +71,21 @@ def test_decode_rejects_bad_arguments(palib, desc_kw, call_kw, status):
     assert palib.pa_last_error()
 
 
-def test_decode_workspace_size_is_zero_for_one_partition(palib):
+def test_decode_workspace_size(palib):
+    """16-bit caches run the dynamic schedule: two control words (padded to
+    256 bytes) and an 8-byte entry per (sequence, kv head, partition), after
+    the split-K partials when there is more than one partition.  1-byte caches
+    keep the static grid, which needs no workspace for one partition."""
     d = _desc()
-    assert palib.pa_decode_workspace_size(4, 4, 256, C.byref(d), 256) == 0
-    ws = palib.pa_decode_workspace_size(4, 4, 1000, C.byref(d), 256)
-    # 4 partitions of 256 tokens: o [B*Hq*4*128] f32 + m, l [B*Hq*4] f32
-    assert ws >= 4 * 4 * 4 * (128 + 2) * 4 and ws % 256 == 0
+    B, Hq, Hkv = 4, 4, 2
+    assert palib.pa_decode_workspace_size(B, Hq, 256, C.byref(d), 256) == (256 + B * Hkv * 8 + 255) // 256 * 256
+    ws = palib.pa_decode_workspace_size(B, Hq, 1000, C.byref(d), 256)
+    # 4 partitions of 256 tokens: o [B*Hq*4*128] f32 + m, l [B*Hq*4] f32, then the list
+    partials = (B * Hq * 4 * (128 + 2) * 4 + 255) // 256 * 256
+    assert ws == partials + (256 + B * Hkv * 4 * 8 + 255) // 256 * 256
+    d8 = _desc(kv_dtype=ops.FP8_E4M3)
+    assert palib.pa_decode_workspace_size(B, Hq, 256, C.byref(d8), 256) == 0
+    assert palib.pa_decode_workspace_size(B, Hq, 1000, C.byref(d8), 256) == partials
 
 
 def test_cache_write_and_copy_reject_bad_arguments(palib):
