@@ -10,6 +10,10 @@
 
 #include "pa_internal.h"
 
+#ifndef PA_FUSED_MERGE
+#define PA_FUSED_MERGE 1  // split-K partials merged by the decode kernel's last partition
+#endif
+
 namespace pa {
 
 static thread_local std::string g_last_error;
@@ -79,13 +83,16 @@ pa_status plan_decode(int32_t B, int32_t Hq, int32_t max_context_len, const pa_c
   } else {
     plan->workspace_bytes = 0;
   }
-  // 16-bit caches run the dynamic schedule: the workspace also holds its two
-  // control words (padded to 256 bytes) and the item list (8 bytes an item)
-  plan->dynamic = PA_DECODE_DYN && !quantised(d->kv_dtype);
-  plan->dyn_offset = plan->workspace_bytes;
-  if (plan->dynamic) {
-    const size_t items = static_cast<size_t>(B) * d->num_kv_heads * parts;
-    plan->workspace_bytes += (256 + items * 8 + 255) & ~static_cast<size_t>(255);
+  // Splits of at most 8 partitions merge in the decode kernel (one warp merges
+  // a pair's partials quickly enough to sit on the grid's critical path):
+  // one 8-byte arrival counter per (sequence, kv head) after the partials.
+  // Longer merges go to the merge kernel, which spreads them over a warp per
+  // query head.
+  plan->ticket_offset = 0;
+  if (PA_FUSED_MERGE && parts > 1 && parts <= 8) {
+    plan->ticket_offset = plan->workspace_bytes;
+    const size_t tickets = static_cast<size_t>(B) * d->num_kv_heads * 8;
+    plan->workspace_bytes += (tickets + 255) & ~static_cast<size_t>(255);
   }
   return PA_OK;
 }
@@ -216,7 +223,7 @@ static pa_status plan_grouped(int32_t B, int32_t Hq, int32_t max_context_len, co
   if (pre + static_cast<int64_t>(gr.max_size) * tail > 65535 ||
       static_cast<int64_t>(gr.n) * d->num_kv_heads * gr.max_size > (int64_t{1} << 31) - 1)
     return fail(PA_ERR_UNSUPPORTED, "pa_decode_append_grouped: grid too large");
-  plan->dynamic = 0;  // groups run on the static grid
+  plan->ticket_offset = 0;  // groups merge in decode_reduce_grouped
   plan->pre_parts = static_cast<int32_t>(pre);
   plan->tail_parts = static_cast<int32_t>(tail);
   plan->max_parts = static_cast<int32_t>(pre + tail);

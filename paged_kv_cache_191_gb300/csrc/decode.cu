@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -92,10 +93,10 @@ struct DecodeArgs {
   const int32_t* prefix_blocks;
   int32_t n_groups, max_members;
   int32_t pre_parts, tail_parts;  // grid rows: shared-prefix partitions, tail partitions
-  // dynamic schedule (decode_plan + decode_dyn), else null: the item list and
-  // its control words {number of items, next item to claim}
-  int2* items;
-  int32_t* plan_ctl;
+  // in-kernel split-K merge (plain grid): one arrival counter per (sequence,
+  // kv head), stamped with this launch's epoch
+  unsigned long long* tickets;
+  uint32_t epoch;
 };
 
 // A group's usable shared prefix: whole blocks every member has before the
@@ -165,7 +166,7 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs& a, KT* kc, KT* v
   }
 }
 
-template <typename KT, int D>
+template <typename KT, int D, int RING_BYTES = kRingBytes>
 struct Tile {
   static constexpr int ROWB = D * static_cast<int>(sizeof(KT));  // bytes per token row
   static constexpr int BYTES = 16 * ROWB;                          // one (block, head) tile
@@ -174,7 +175,7 @@ struct Tile {
   // a tile two 128-byte swizzle spans wide is fetched as one 5-D box
   // (d_lo, row, d_hi, head, block): one TMA issue per tile instead of two
   static constexpr bool ONE_BOX = NBOX == 2;
-  static constexpr int NS = kRingBytes / (2 * BYTES);             // K+V stages per warp
+  static constexpr int NS = RING_BYTES / (2 * BYTES);             // K+V stages per warp
   static constexpr int RING = NS * 2 * BYTES;                      // one warp's ring
   // shared memory of a W-warp CTA: rings [W], code scales [W][NS][32] f32,
   // full barriers [W][NS]
@@ -210,6 +211,113 @@ __device__ __forceinline__ void store_out(const DecodeArgs& a, size_t idx, float
     static_cast<__half*>(a.out)[idx] = __float2half_rn(v);
   else
     static_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(v);
+}
+
+// ---- in-kernel split-K merge ------------------------------------------------------
+// The partitions of one (sequence b, kv head g) end at different times.  Each
+// writes its partial (o, m, l), makes it visible device-wide and takes a
+// ticket on the pair's arrival counter; the last to arrive merges all of
+// them into the G output rows at once.  The merges of early-finishing
+// sequences overlap the rest of the grid, and no second kernel has to wait
+// for the whole grid to end.  A counter holds {epoch, arrivals}: a launch
+// counts only arrivals stamped with its own epoch, so whatever the workspace
+// held before (another launch's counts, uninitialised bytes) reads as zero,
+// and the last arrival puts the counter back to {epoch, 0}.
+
+// Thread 0's ticket: true if this partition is the pair's last to arrive.
+__device__ __forceinline__ bool take_ticket(const DecodeArgs& a, int b, int g, int np) {
+  unsigned long long* t = a.tickets + static_cast<size_t>(b) * a.Hkv + g;
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(t);
+  uint32_t cnt = 0;
+  for (int it = 0; it < 65536; ++it) {  // bounded: at most np CTAs ever race here
+    cnt = static_cast<uint32_t>(old >> 32) == a.epoch ? static_cast<uint32_t>(old) : 0u;
+    const unsigned long long want = (static_cast<unsigned long long>(a.epoch) << 32) | (cnt + 1u);
+    const unsigned long long prev = atomicCAS(t, old, want);
+    if (prev == old) return cnt + 1u == static_cast<uint32_t>(np);
+    old = prev;
+  }
+  atomicOr(&g_decode_err, PA_DEVERR_TIMEOUT);
+  return false;
+}
+
+// One warp merges the np partitions of (b, g) into the G output rows of the
+// kv head: out = sum_p w_p o_p with w_p = exp2(m_p - M) / sum_q exp2(m_q - M) l_q.
+// Partials written by other CTAs are read at L2 (ld.global.cg).  `sw` is
+// G * np floats of this warp's idle shared memory.  np <= 64.
+template <typename QT, int D>
+__device__ __forceinline__ void merge_pair(const DecodeArgs& a, int b, int g, int np, int lane, float* sw) {
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int V = D / 32;  // dims per lane
+  const size_t head0 = static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * a.G;
+  {  // weights: 4 lanes per head (c = lane / 4), partitions p = lane % 4, +4, ...
+    const int c = lane >> 2, sub = lane & 3;
+    const bool on = c < a.G;
+    const size_t row = (head0 + (on ? c : 0)) * a.max_parts;
+    float mv[16], lv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int p = sub + 4 * i;
+      const bool ok = on && p < np;
+      mv[i] = ok ? __ldcg(a.part_m + row + p) : -INFINITY;
+      lv[i] = ok ? __ldcg(a.part_l + row + p) : 0.f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) M = fmaxf(M, mv[i]);
+    M = fmaxf(M, __shfl_xor_sync(FULL, M, 1));
+    M = fmaxf(M, __shfl_xor_sync(FULL, M, 2));
+    float ls = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ls += exp2f(mv[i] - M) * lv[i];  // exp2(-inf) = 0 past np
+    ls += __shfl_xor_sync(FULL, ls, 1);
+    ls += __shfl_xor_sync(FULL, ls, 2);
+    const float inv = 1.f / ls;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int p = sub + 4 * i;
+      if (on && p < np) sw[c * np + p] = exp2f(mv[i] - M) * inv;
+    }
+  }
+  __syncwarp();
+  float acc[PA_MAX_GROUP][V];
+#pragma unroll
+  for (int c = 0; c < PA_MAX_GROUP; ++c)
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[c][v] = 0.f;
+  for (int p0 = 0; p0 < np; p0 += 4) {  // four partitions of every head in flight
+    float x[4][PA_MAX_GROUP][V];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < PA_MAX_GROUP; ++c) {
+        const bool ok = c < a.G && p0 + i < np;
+        const float* src = a.part_o + ((head0 + (ok ? c : 0)) * a.max_parts + p0 + i) * D + lane * V;
+        if constexpr (V == 4) {
+          const float4 t = ok ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[i][c][0] = t.x; x[i][c][1] = t.y; x[i][c][2] = t.z; x[i][c][3] = t.w;
+        } else {
+          const float2 t = ok ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
+          x[i][c][0] = t.x; x[i][c][1] = t.y;
+        }
+      }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < PA_MAX_GROUP; ++c) {
+        if (c < a.G && p0 + i < np) {
+          const float w = sw[c * np + p0 + i];
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[c][v] += w * x[i][c][v];
+        }
+      }
+  }
+#pragma unroll
+  for (int c = 0; c < PA_MAX_GROUP; ++c)
+    if (c < a.G)
+#pragma unroll
+      for (int v = 0; v < V; ++v) store_out<QT>(a, (head0 + c) * D + lane * V + v, acc[c][v]);
+  if (lane == 0)  // ready for the next launch with this epoch (a replayed graph)
+    a.tickets[static_cast<size_t>(b) * a.Hkv + g] = static_cast<unsigned long long>(a.epoch) << 32;
 }
 
 template <typename KT, typename QT, int D, int W>
@@ -668,6 +776,18 @@ __global__ void __launch_bounds__(32 * W)
         }
       }
     }
+    if (!direct && a.tickets) {
+      __shared__ int s_last;
+      const int np = (((L + 15) >> 4) + a.bpp - 1) / a.bpp;
+      __threadfence();  // this CTA's partial is visible before its ticket
+      __syncthreads();  // every warp is done with the rings
+      if (threadIdx.x == 0) s_last = take_ticket(a, b, g, np);
+      __syncthreads();
+      if (s_last && wid == 0) {
+        __threadfence();  // the other partitions' partials, published before their tickets
+        merge_pair<QT, D>(a, b, g, np, lane, reinterpret_cast<float*>(base));
+      }
+    }
     return;
   }
   const bool okA = hA < ncols, okB = hB < ncols;
@@ -714,434 +834,32 @@ __global__ void __launch_bounds__(32 * W)
       a.part_l[headB * a.max_parts + p] = l1;
     }
   }
-}
-
-// ---- dynamic schedule --------------------------------------------------------------
-// The static grid above leaves the placement of items on SMs to the hardware
-// block scheduler: cells of the grid past a short sequence's last partition
-// exit at once and free their slot, so the items that follow pile onto
-// whichever SMs those empty cells landed on, and the SMs with the most bytes
-// end the launch alone.  The dynamic schedule lists the items first, longest
-// first, and lets persistent warps claim them one at a time, so every SM
-// streams until the list is exhausted and the last items to finish are the
-// shortest.
-
-// One CTA builds the item list: every (sequence b, kv head g, partition p)
-// holding at least one block, as {b * Hkv + g, p}, sorted by the partition's
-// block count, largest first (a counting sort over 1 .. bpp).  It stores the
-// item count, zeroes the claim counter and writes the zero rows of empty
-// sequences.  The order inside one size class is not fixed (atomic slots);
-// nothing depends on it, since an item's arithmetic and output rows are the
-// same whichever warp claims it.
-template <typename QT, int D>
-__global__ void __launch_bounds__(1024) decode_plan(const DecodeArgs a) {
-  __shared__ int32_t cnt[65];  // items per size class, then the class's next free slot
-  dev::grid_dependency_wait();    // no earlier kernel still reads the list or the outputs
-  dev::grid_launch_dependents();  // decode_dyn's CTAs may become resident and set up
-  const int tid = static_cast<int>(threadIdx.x), nt = static_cast<int>(blockDim.x);
-  for (int i = tid; i <= a.bpp; i += nt) cnt[i] = 0;
-  __syncthreads();
-  for (int b = tid; b < a.B; b += nt) {
-    const int nblk = (checked_len(a, b, true) + 15) >> 4;
-    if (nblk == 0) {
-      for (int i = 0; i < a.Hq * D; ++i) store_out<QT>(a, static_cast<size_t>(b) * a.Hq * D + i, 0.f);
-      continue;
-    }
-    const int np = (nblk + a.bpp - 1) / a.bpp;
-    if (np > 1) atomicAdd(&cnt[a.bpp], (np - 1) * a.Hkv);
-    atomicAdd(&cnt[nblk - (np - 1) * a.bpp], a.Hkv);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int sz = a.bpp; sz >= 1; --sz) {
-      const int c = cnt[sz];
-      cnt[sz] = run;
-      run += c;
-    }
-    a.plan_ctl[0] = run;
-    a.plan_ctl[1] = 0;
-  }
-  __syncthreads();
-  for (int b = tid; b < a.B; b += nt) {
-    const int nblk = (checked_len(a, b, false) + 15) >> 4;
-    const int np = (nblk + a.bpp - 1) / a.bpp;
-    for (int p = 0; p < np; ++p) {
-      const int at = atomicAdd(&cnt[min(a.bpp, nblk - p * a.bpp)], a.Hkv);
-      for (int g = 0; g < a.Hkv; ++g) a.items[at + g] = make_int2(b * a.Hkv + g, p);
-    }
-  }
-}
-
-// Persistent one-warp CTAs over the item list (16-bit caches).  Each warp
-// claims an item (atomic counter), streams its tiles through the same TMA
-// ring and tensor-core arithmetic as decode_main, writes the item's output
-// or partial row, and moves on.  While one item streams, the next one is
-// claimed and prepared a phase per tile -- its list entry, then its length,
-// block ids, query fragments and new K/V row, then its fused cache write --
-// and its first tiles enter the ring as soon as the current item's last
-// tiles are issued, so the stream does not pause between items.  Tiles are
-// numbered per warp across items (stage = n % NS, phase = n / NS), which
-// keeps the mbarrier parities continuous.
-template <typename KT, typename QT, int D>
-__global__ void __launch_bounds__(32)
-    decode_dyn(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-               const DecodeArgs a) {
-  using TL = Tile<KT, D>;
-  static_assert(sizeof(KT) == 2, "the dynamic schedule serves 16-bit caches");
-  constexpr int NS = TL::NS;
-  constexpr int KSTEPS = D / 16;
-  constexpr int MT = D / 16;
-  constexpr int V = D / 32;  // new-row elements per lane
-  constexpr uint32_t STAGE_TX = 2 * TL::BYTES;
-  constexpr bool SPLIT_P = std::is_same<QT, __nv_bfloat16>::value;
-  constexpr unsigned FULL = 0xffffffffu;
-
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = dev::smem_addr(smem_raw);
-  const uint32_t tiles = (raw + 1023u) & ~1023u;
-  const uint32_t bar_full = tiles + TL::off_bar(1);
-  const int lane = static_cast<int>(threadIdx.x & 31), r = lane >> 2, q4 = lane & 3;
-  const int cap = min(a.max_context_len, a.max_blocks * 16);
-  const bool fuse = a.fuse_write != 0;
-
-  if (lane == 0) {
-    dev::prefetch_tensormap(&tmK);
-    dev::prefetch_tensormap(&tmV);
-    for (int s = 0; s < NS; ++s) dev::mbar_init(bar_full + 8 * s, 1);
-    dev::fence_barrier_init();
-  }
-  __syncwarp();
-  dev::grid_dependency_wait();    // the item list is complete and visible
-  dev::grid_launch_dependents();  // the merge kernel may take slots as warps finish
-  const int n_items = a.plan_ctl[0];
-
-  // ---- the next item, prepared in phases: 1 claimed, 2 entry, 3 loaded, 4 ready; 0 none
-  int n_state = 0, n_idx = 0;
-  int2 n_ent = make_int2(0, 0);
-  int n_b = 0, n_g = 0, n_j0 = 0, n_Lraw = 0, n_L = 0, n_nb = 0, n_t0 = 0, n_t1 = 0;
-  bool n_direct = false;
-  int64_t n_slot = -1;
-  uint32_t n_qf[KSTEPS][2];
-  float n_kv[2][V];
-  auto claim = [&]() {
-    n_idx = 0;
-    if (lane == 0) n_idx = atomicAdd(a.plan_ctl + 1, 1);
-    n_state = 1;
-  };
-  auto phase_entry = [&]() {
-    const int idx = __shfl_sync(FULL, n_idx, 0);
-    if (idx >= n_items) {
-      n_state = 0;
-      return;
-    }
-    n_ent = a.items[idx];
-    n_state = 2;
-  };
-  auto phase_load = [&]() {
-    n_b = n_ent.x / a.Hkv;
-    n_g = n_ent.x - n_b * a.Hkv;
-    n_j0 = n_ent.y * a.bpp;
-    n_Lraw = a.context_lens[n_b];
-    const int32_t* row = a.block_tables + static_cast<size_t>(n_b) * a.max_blocks + n_j0;
-    const int row_left = a.max_blocks - n_j0;
-    n_t0 = (lane < a.bpp && lane < row_left) ? row[lane] : 0;
-    n_t1 = (lane + 32 < a.bpp && lane + 32 < row_left) ? row[lane + 32] : 0;
-    const QT* qrow = static_cast<const QT*>(a.q) +
-                     (static_cast<size_t>(n_b) * a.Hq + n_g * a.G + (r < a.G ? r : 0)) * D;
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-      n_qf[kk][0] = r < a.G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * q4) : 0u;
-      n_qf[kk][1] = r < a.G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * q4) : 0u;
-    }
-    if (fuse) {  // the new token's row of kv head g, used if this item holds the last block
-      n_slot = a.slot_mapping[n_b];
-      const size_t rn = (static_cast<size_t>(n_b) * a.Hkv + n_g) * D;
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        n_kv[0][v] = load_in(a.k_new, rn + lane + 32 * v, a.new_dtype);
-        n_kv[1][v] = load_in(a.v_new, rn + lane + 32 * v, a.new_dtype);
-      }
-    }
-    n_state = 3;
-  };
-  auto phase_ready = [&]() {
-    int L = n_Lraw;
-    if (L < 0 || L > cap) L = max(0, min(L, cap));  // flagged by decode_plan
-    const int nblk = (L + 15) >> 4;
-    n_L = L;
-    n_nb = min(a.bpp, nblk - n_j0);
-    if (n_nb <= 0) {  // cannot happen with the list decode_plan built; claim another
-      claim();
-      return;
-    }
-    n_direct = (nblk + a.bpp - 1) / a.bpp == 1;
-    const bool bad = (lane < n_nb && (n_t0 < 0 || n_t0 >= a.num_blocks)) ||
-                     (lane + 32 < n_nb && (n_t1 < 0 || n_t1 >= a.num_blocks));
-    if (bad) {
-      atomicOr(&g_decode_err, PA_DEVERR_BLOCK_RANGE);  // read a valid block instead; flagged
-      if (n_t0 < 0 || n_t0 >= a.num_blocks) n_t0 = 0;
-      if (n_t1 < 0 || n_t1 >= a.num_blocks) n_t1 = 0;
-    }
-    if (fuse && n_j0 + n_nb == nblk) {
-      // this item holds the sequence's last token: store the new row of kv
-      // head g before any tile of the item is requested, visible to the TMA
-      if (n_slot >= static_cast<int64_t>(a.num_blocks) * 16) {
-        if (lane == 0) atomicOr(&g_decode_err, PA_DEVERR_SLOT_RANGE);
-      } else if (n_slot >= 0) {
-        const size_t dst = ((static_cast<size_t>(n_slot / 16) * a.Hkv + n_g) * 16 + n_slot % 16) * D;
-        KT* kc = static_cast<KT*>(a.k_cache_w);
-        KT* vc = static_cast<KT*>(a.v_cache_w);
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-          if constexpr (std::is_same<KT, __half>::value) {
-            kc[dst + lane + 32 * v] = __float2half_rn(n_kv[0][v]);
-            vc[dst + lane + 32 * v] = __float2half_rn(n_kv[1][v]);
-          } else {
-            kc[dst + lane + 32 * v] = __float2bfloat16_rn(n_kv[0][v]);
-            vc[dst + lane + 32 * v] = __float2bfloat16_rn(n_kv[1][v]);
-          }
-        }
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-      }
-      __syncwarp();
-    }
-    n_state = 4;
-  };
-  auto advance = [&]() {
-    if (n_state == 1)
-      phase_entry();
-    else if (n_state == 2)
-      phase_load();
-    else if (n_state == 3)
-      phase_ready();
-  };
-
-  // ---- the current item
-  claim();
-  while (n_state != 0 && n_state != 4) advance();
-  if (n_state == 0) return;
-  int b, g, p, j0, L, nb, t0, t1;
-  bool direct;
-  uint32_t qf[KSTEPS][2];
-  auto promote = [&]() {
-    b = n_b;
-    g = n_g;
-    p = n_ent.y;
-    j0 = n_j0;
-    L = n_L;
-    nb = n_nb;
-    t0 = n_t0;
-    t1 = n_t1;
-    direct = n_direct;
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-      qf[kk][0] = n_qf[kk][0];
-      qf[kk][1] = n_qf[kk][1];
-    }
-  };
-  promote();
-
-  uint32_t vbase = 0, iss = 0, con = 0;  // per-warp tile numbers: current item's first, next to issue, next to use
-  auto fill = [&](uint32_t done) {  // issue tiles while a stage is free (every lane runs it)
-    while (iss < done + NS) {
-      const int jc = static_cast<int>(iss - vbase);
-      int pb, gg;
-      if (jc < nb) {
-        pb = __shfl_sync(FULL, jc < 32 ? t0 : t1, jc & 31);
-        gg = g;
-      } else if (n_state == 4 && jc - nb < n_nb) {
-        const int jn = jc - nb;
-        pb = __shfl_sync(FULL, jn < 32 ? n_t0 : n_t1, jn & 31);
-        gg = n_g;
-      } else {
-        break;
-      }
-      if (lane == 0) {
-        const int s = static_cast<int>(iss % NS);
-        const uint32_t bar = bar_full + 8 * s;
-        const uint32_t kdst = tiles + s * 2 * TL::BYTES, vdst = kdst + TL::BYTES;
-        dev::fence_proxy_async_smem();  // the stage's last reads precede the refill
-        dev::mbar_arrive_expect_tx(bar, STAGE_TX);
-        if constexpr (TL::ONE_BOX) {
-          dev::tma_load_5d(kdst, &tmK, bar, 0, 0, 0, gg, pb);
-          dev::tma_load_5d(vdst, &tmV, bar, 0, 0, 0, gg, pb);
-        } else {
-#pragma unroll
-          for (int bx = 0; bx < TL::NBOX; ++bx) {
-            dev::tma_load_3d(kdst + bx * 2048, &tmK, bar, bx * TL::BOXE, gg * 16, pb);
-            dev::tma_load_3d(vdst + bx * 2048, &tmV, bar, bx * TL::BOXE, gg * 16, pb);
-          }
-        }
-      }
-      ++iss;
-    }
-  };
-  claim();  // before fill: a ready next item would lend its tiles to the ring
-  fill(0);
-
-  float o[MT][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const float sl2 = a.scale_log2;
-  const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int vrow = (lane & 7) + (lane >> 4) * 8;
-
-  for (;;) {
-    advance();  // one phase of the next item per tile
-    const int s = static_cast<int>(con % NS);
-    if (!dev::mbar_wait_bounded(bar_full + 8 * s, (con / NS) & 1)) {
-      if (lane == 0) atomicOr(&g_decode_err, PA_DEVERR_TIMEOUT);
-      for (uint32_t v = con + 1; v < iss; ++v)  // let the copies in flight land (bounded), then stop
-        dev::mbar_wait_bounded(bar_full + 8 * (v % NS), (v / NS) & 1, 100000000ull);
-      return;
-    }
-    const uint32_t kb = tiles + s * 2 * TL::BYTES, vb = kb + TL::BYTES;
-    const int j = static_cast<int>(con - vbase);
-    const int nvalid = min(16, L - (j0 + j) * 16);
-    uint32_t kf[KSTEPS][4], vf[MT][4];
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) dev::ldmatrix_x4(kf[kk], kb + swz(krow, 2 * kk + (lane >> 4)));
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) dev::ldmatrix_x4_trans(vf[mt], vb + swz(vrow, 2 * mt + ((lane >> 3) & 1)));
-    if (nvalid < 16) {  // rows past the context: weight 0, and 0 * NaN is NaN, so clear them
-      const int tq = 2 * q4;
-      const uint32_t mk0 = (tq < nvalid ? 0xFFFFu : 0u) | (tq + 1 < nvalid ? 0xFFFF0000u : 0u);
-      const uint32_t mk8 = (tq + 8 < nvalid ? 0xFFFFu : 0u) | (tq + 9 < nvalid ? 0xFFFF0000u : 0u);
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        vf[mt][0] &= mk0;
-        vf[mt][1] &= mk0;
-        vf[mt][2] &= mk8;
-        vf[mt][3] &= mk8;
-      }
-    }
+  if (!direct && a.tickets) {
+    const int np = (((L + 15) >> 4) + a.bpp - 1) / a.bpp;
+    __threadfence();  // this warp's partial is visible before its ticket
     __syncwarp();
-    fill(con + 1);
-
-    // S^T = K . Q^T, online softmax, O^T += V^T . P^T (as in decode_main)
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) dev::Mma<QT>::run(sacc, kf[kk], qf[kk][0], qf[kk][1]);
-    const bool v_r = r < nvalid, v_r8 = r + 8 < nvalid;
-    const float x0 = v_r ? sacc[0] * sl2 : -INFINITY;
-    const float x1 = v_r ? sacc[1] * sl2 : -INFINITY;
-    const float x2 = v_r8 ? sacc[2] * sl2 : -INFINITY;
-    const float x3 = v_r8 ? sacc[3] * sl2 : -INFINITY;
-    float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      bm0 = fmaxf(bm0, __shfl_xor_sync(FULL, bm0, off));
-      bm1 = fmaxf(bm1, __shfl_xor_sync(FULL, bm1, off));
+    const bool last = __shfl_sync(FULL, lane == 0 ? take_ticket(a, b, g, np) : false, 0);
+    if (last) {
+      __threadfence();  // the other partitions' partials, published before their tickets
+      merge_pair<QT, D>(a, b, g, np, lane, reinterpret_cast<float*>(base));
     }
-    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1), p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-    const uint32_t ph_r = dev::pack2<QT>(p0, p1), ph_r8 = dev::pack2<QT>(p2, p3);
-    uint32_t pl_r = 0, pl_r8 = 0;
-    if constexpr (SPLIT_P) {
-      const float2 h_r = dev::unpack2<QT>(ph_r), h_r8 = dev::unpack2<QT>(ph_r8);
-      pl_r = dev::pack2<QT>(p0 - h_r.x, p1 - h_r.y);
-      pl_r8 = dev::pack2<QT>(p2 - h_r8.x, p3 - h_r8.y);
-      l0 = l0 * al0 + (p0 + p2);
-      l1 = l1 * al1 + (p1 + p3);
-    } else {
-      const float2 h_r = dev::unpack2<QT>(ph_r), h_r8 = dev::unpack2<QT>(ph_r8);
-      l0 = l0 * al0 + (h_r.x + h_r8.x);
-      l1 = l1 * al1 + (h_r.y + h_r8.y);
-    }
-    const uint32_t bh0 = dev::movmatrix_trans(ph_r), bh1 = dev::movmatrix_trans(ph_r8);
-    uint32_t bl0 = 0, bl1 = 0;
-    if constexpr (SPLIT_P) {
-      bl0 = dev::movmatrix_trans(pl_r);
-      bl1 = dev::movmatrix_trans(pl_r8);
-    }
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
-      dev::Mma<QT>::run(o[mt], vf[mt], bh0, bh1);
-      if constexpr (SPLIT_P) dev::Mma<QT>::run(o[mt], vf[mt], bl0, bl1);
-    }
-    ++con;
-    if (static_cast<int>(con - vbase) < nb) continue;
-
-    // ---- the item is done: its output row, or its partial (o, m, l) --------------
-    float ls0 = l0, ls1 = l1;
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      ls0 += __shfl_xor_sync(FULL, ls0, off);
-      ls1 += __shfl_xor_sync(FULL, ls1, off);
-    }
-    const int hA = 2 * q4, hB = 2 * q4 + 1;
-    const bool okA = hA < a.G, okB = hB < a.G;
-    const size_t headA = static_cast<size_t>(b) * a.Hq + g * a.G + hA;
-    const size_t headB = headA + 1;
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      const int d_r = 16 * mt + r, d_r8 = d_r + 8;
-      if (direct) {
-        if (okA) {
-          store_out<QT>(a, headA * D + d_r, o[mt][0] / ls0);
-          store_out<QT>(a, headA * D + d_r8, o[mt][2] / ls0);
-        }
-        if (okB) {
-          store_out<QT>(a, headB * D + d_r, o[mt][1] / ls1);
-          store_out<QT>(a, headB * D + d_r8, o[mt][3] / ls1);
-        }
-      } else {
-        const size_t rowA = headA * a.max_parts + p, rowB = headB * a.max_parts + p;
-        if (okA) {
-          a.part_o[rowA * D + d_r] = o[mt][0];
-          a.part_o[rowA * D + d_r8] = o[mt][2];
-        }
-        if (okB) {
-          a.part_o[rowB * D + d_r] = o[mt][1];
-          a.part_o[rowB * D + d_r8] = o[mt][3];
-        }
-      }
-    }
-    if (!direct && lane < 4) {
-      if (okA) {
-        a.part_m[headA * a.max_parts + p] = m0;
-        a.part_l[headA * a.max_parts + p] = ls0;
-      }
-      if (okB) {
-        a.part_m[headB * a.max_parts + p] = m1;
-        a.part_l[headB * a.max_parts + p] = ls1;
-      }
-    }
-
-    // ---- make the next item current ----------------------------------------------
-    while (n_state != 0 && n_state != 4) advance();
-    if (n_state == 0) break;  // nothing in flight: only a ready item's tiles are ever issued ahead
-    vbase += nb;
-    promote();
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    m0 = m1 = -INFINITY;
-    l0 = l1 = 0.f;
-    claim();   // before fill: the promoted item's state must not pass for a ready next item
-    fill(con);
   }
 }
 
 // Merge n partition rows of one query head (rows row0 .. row0 + n - 1) with
-// log-sum-exp weights into output row `orow`.  Partitions are taken 16 at a
-// time: lane i holds partition i's (m, l), every lane holds its D/32 dims of
-// the chunk's partial rows, and chunks merge online (running max).  `mv`, `lv`
-// are the first chunk's (m, l) as the caller loaded them; lanes past n are
-// reset here, so stale scratch never enters a sum.
+// log-sum-exp weights into output row `orow`.  Partitions are taken 32 at a
+// time: lane i holds partition i's (m, l), so the chunk's weights are known
+// after one round trip; every lane then reads its D/32 dims of the chunk's
+// partial rows 16 partitions at a time, all loads of a batch in flight
+// together.  Chunks merge online (running max).  `mv`, `lv` are the first
+// chunk's (m, l) as the caller loaded them; lanes past n are reset here, so
+// stale scratch never enters a sum.
 template <typename QT, int D>
 __device__ __forceinline__ void merge_rows(const DecodeArgs& a, size_t row0, int n, float mv, float lv,
                                            size_t orow, int lane) {
   constexpr unsigned FULL = 0xffffffffu;
-  constexpr int CH = 16;      // partitions per chunk
+  constexpr int CH = 32;      // partitions per chunk (one per lane)
+  constexpr int RB = 16;      // partial rows per load batch
   constexpr int V = D / 32;   // dims per lane (4 or 2)
   const float* po = a.part_o + row0 * D + lane * V;
   float M = -INFINITY, ls = 0.f, acc[V];
@@ -1157,19 +875,6 @@ __device__ __forceinline__ void merge_rows(const DecodeArgs& a, size_t row0, int
       mv = -INFINITY;
       lv = 0.f;
     }
-    float x[CH][V];
-#pragma unroll
-    for (int i = 0; i < CH; ++i) {
-      if (i < cn) {
-        if constexpr (V == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(po + static_cast<size_t>(c0 + i) * D);
-          x[i][0] = t.x; x[i][1] = t.y; x[i][2] = t.z; x[i][3] = t.w;
-        } else {
-          const float2 t = *reinterpret_cast<const float2*>(po + static_cast<size_t>(c0 + i) * D);
-          x[i][0] = t.x; x[i][1] = t.y;
-        }
-      }
-    }
     float cm = mv;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, off));
@@ -1183,12 +888,27 @@ __device__ __forceinline__ void merge_rows(const DecodeArgs& a, size_t row0, int
     ls = ls * rescale + wl;
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] *= rescale;
+    for (int i0 = 0; i0 < cn; i0 += RB) {
+      float x[RB][V];
 #pragma unroll
-    for (int i = 0; i < CH; ++i) {
-      const float wi = __shfl_sync(FULL, w, i);
-      if (i < cn) {
+      for (int i = 0; i < RB; ++i) {
+        if (i0 + i < cn) {
+          if constexpr (V == 4) {
+            const float4 t = *reinterpret_cast<const float4*>(po + static_cast<size_t>(c0 + i0 + i) * D);
+            x[i][0] = t.x; x[i][1] = t.y; x[i][2] = t.z; x[i][3] = t.w;
+          } else {
+            const float2 t = *reinterpret_cast<const float2*>(po + static_cast<size_t>(c0 + i0 + i) * D);
+            x[i][0] = t.x; x[i][1] = t.y;
+          }
+        }
+      }
 #pragma unroll
-        for (int v = 0; v < V; ++v) acc[v] += wi * x[i][v];
+      for (int i = 0; i < RB; ++i) {
+        const float wi = __shfl_sync(FULL, w, (i0 + i) & 31);
+        if (i0 + i < cn) {
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[v] += wi * x[i][v];
+        }
       }
     }
   }
@@ -1206,8 +926,8 @@ __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce(const DecodeA
   const int h = g * a.G + static_cast<int>(threadIdx.x >> 5), lane = threadIdx.x & 31;
   dev::grid_dependency_wait();  // partials of decode_main are complete and visible
   const size_t row0 = (static_cast<size_t>(b) * a.Hq + h) * a.max_parts;
-  const float mv = lane < min(16, a.max_parts) ? a.part_m[row0 + lane] : -INFINITY;
-  const float lv = lane < min(16, a.max_parts) ? a.part_l[row0 + lane] : 0.f;
+  const float mv = lane < a.max_parts ? a.part_m[row0 + lane] : -INFINITY;
+  const float lv = lane < a.max_parts ? a.part_l[row0 + lane] : 0.f;
   const int L = checked_len(a, b, false);
   const int nblk = (L + 15) >> 4;
   const int nparts = (nblk + a.bpp - 1) / a.bpp;
@@ -1235,8 +955,8 @@ __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce_grouped(const
   const int nparts = (E + a.bpp - 1) / a.bpp + (nblk - E + a.bpp - 1) / a.bpp;
   if (nparts <= 1) return;
   const size_t row0 = (static_cast<size_t>(b) * a.Hq + h) * a.max_parts;
-  const float mv = lane < min(16, nparts) ? a.part_m[row0 + lane] : -INFINITY;
-  const float lv = lane < min(16, nparts) ? a.part_l[row0 + lane] : 0.f;
+  const float mv = lane < nparts ? a.part_m[row0 + lane] : -INFINITY;
+  const float lv = lane < nparts ? a.part_l[row0 + lane] : 0.f;
   merge_rows<QT, D>(a, row0, nparts, mv, lv, static_cast<size_t>(b) * a.Hq + h, lane);
 }
 
@@ -1246,6 +966,17 @@ pa_status make_map(CUtensorMap* m, const void* cache, int Hkv, int num_blocks, C
   using TL = Tile<KT, D>;
   static_assert(TL::ONE_BOX == (TL::ROWB == 256), "the 5-D box covers exactly two swizzle spans");
   return make_kv_map(m, cache, Hkv, num_blocks, TL::ROWB, static_cast<int>(sizeof(KT)), dt, "pa_decode");
+}
+
+// A fresh stamp for each launch's arrival counters (never 0 or all ones, the
+// values zeroed and 0xFF-filled memory would show).
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t v;
+  do {
+    v = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  } while (v == 0u || v == 0xFFFFFFFFu);
+  return v;
 }
 
 template <typename KT, typename QT, int D>
@@ -1294,12 +1025,11 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   a.max_members = l.max_members;
   a.pre_parts = l.plan.pre_parts;
   a.tail_parts = l.plan.tail_parts;
-  a.items = nullptr;
-  a.plan_ctl = nullptr;
-  if (l.plan.dynamic) {  // after the partials: control words, then the item list
-    uint8_t* w = static_cast<uint8_t*>(l.workspace) + l.plan.dyn_offset;
-    a.plan_ctl = reinterpret_cast<int32_t*>(w);
-    a.items = reinterpret_cast<int2*>(w + 256);
+  a.tickets = nullptr;
+  a.epoch = 0;
+  if (l.plan.ticket_offset) {  // after the partials: the arrival counters
+    a.tickets = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(l.workspace) + l.plan.ticket_offset);
+    a.epoch = next_epoch();
   }
 
   int dev = 0;
@@ -1321,36 +1051,6 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   if (setup_err[dev] != cudaSuccess)
     return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(setup_err[dev]));
 
-  if constexpr (sizeof(KT) == 2) {
-  if (l.plan.dynamic) {
-    static std::once_flag dyn_once[kMaxDevices];
-    static int dyn_slots[kMaxDevices];  // resident decode_dyn CTAs on the whole device
-    static cudaError_t dyn_err[kMaxDevices];
-    std::call_once(dyn_once[dev], [dev] {
-      int per_sm = 0, sms = 0;
-      cudaError_t e = cudaFuncSetAttribute(decode_dyn<KT, QT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           TL::smem(1));
-      if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_dyn<KT, QT, D>, 32, TL::smem(1));
-      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      dyn_slots[dev] = std::max(1, per_sm) * std::max(1, sms);
-      dyn_err[dev] = e;
-    });
-    if (dyn_err[dev] != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(dyn_err[dev]));
-    const int64_t max_items = static_cast<int64_t>(l.B) * l.Hkv * l.plan.max_parts;
-    const unsigned ctas = static_cast<unsigned>(std::min<int64_t>(max_items, dyn_slots[dev]));
-    cudaError_t e = launch_dependent(decode_plan<QT, D>, dim3(1), dim3(1024), 0, stream, a);
-    if (e == cudaSuccess)
-      e = launch_dependent(decode_dyn<KT, QT, D>, dim3(ctas), dim3(32), TL::smem(1), stream, tmK, tmV, a);
-    if (e == cudaSuccess && l.plan.max_parts > 1)
-      e = launch_dependent(decode_reduce<QT, D>, dim3(static_cast<unsigned>(l.B * l.Hkv)),
-                           dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode launch: %s", cudaGetErrorString(e));
-    return PA_OK;
-  }
-  }
-
   const bool grouped = l.n_groups > 0;
   const dim3 grid = grouped ? dim3(static_cast<unsigned>(l.n_groups * l.Hkv),
                                    static_cast<unsigned>(l.plan.pre_parts + l.max_members * l.plan.tail_parts))
@@ -1367,7 +1067,7 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
     e = launch_dependent(decode_reduce_grouped<QT, D>,
                          dim3(static_cast<unsigned>(l.n_groups * l.max_members * l.Hkv)),
                          dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
-  else if (e == cudaSuccess && l.plan.max_parts > 1)
+  else if (e == cudaSuccess && l.plan.max_parts > 1 && !a.tickets)
     e = launch_dependent(decode_reduce<QT, D>, dim3(static_cast<unsigned>(l.B * l.Hkv)),
                          dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
   if (e == cudaSuccess) e = cudaGetLastError();

@@ -33,27 +33,21 @@ inline bool quantised(int32_t dt) { return dt == PA_DTYPE_FP8_E4M3 || dt == PA_D
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 16-bit caches decode on the dynamic schedule (item list + persistent
-// warps) unless built with -DPA_DECODE_DYN=0 (the static grid).
-#ifndef PA_DECODE_DYN
-#define PA_DECODE_DYN 1
-#endif
-
 // Split-K plan for one pa_decode shape (pure function of its arguments and
 // the device's SM count).
 struct DecodePlan {
   int32_t blocks_per_part;  // 16-token blocks per partition
   int32_t max_parts;        // partitions of the longest allowed context
-  size_t workspace_bytes;   // partials (max_parts > 1) + the dynamic schedule's list; may be 0
+  size_t workspace_bytes;   // 0 when max_parts == 1
   int32_t item_warps;       // warps sharing one partition (1, 2 or 4)
   // shared-prefix groups: grid rows of prefix partitions and of tail
   // partitions per member (max_parts = pre_parts + tail_parts); 0 otherwise
   int32_t pre_parts = 0, tail_parts = 0;
-  // dynamic schedule (16-bit caches, no groups): an item-list kernel, then
-  // persistent warps claiming items; its control words and list start at
-  // byte dyn_offset of the workspace, after the partials
-  int32_t dynamic = 0;
-  size_t dyn_offset = 0;
+  // plain grid with max_parts > 1: the split-K partials are merged inside the
+  // decode kernel by the last partition of each (sequence, kv head) to
+  // finish; their arrival counters start at this byte of the workspace
+  // (0: no counters, a merge kernel runs instead)
+  size_t ticket_offset = 0;
 };
 pa_status plan_decode(int32_t B, int32_t num_q_heads, int32_t max_context_len,
                       const pa_cache_desc* desc, int32_t split_tokens, DecodePlan* plan);

@@ -72,20 +72,20 @@ def test_decode_rejects_bad_arguments(palib, desc_kw, call_kw, status):
 
 
 def test_decode_workspace_size(palib):
-    """16-bit caches run the dynamic schedule: two control words (padded to
-    256 bytes) and an 8-byte entry per (sequence, kv head, partition), after
-    the split-K partials when there is more than one partition.  1-byte caches
-    keep the static grid, which needs no workspace for one partition."""
+    """One partition needs no workspace.  A split needs the partials (o, m, l
+    per sequence, query head and partition) and, when it has at most 8
+    partitions, one 8-byte arrival counter per (sequence, kv head) after them
+    for the in-kernel merge."""
     d = _desc()
     B, Hq, Hkv = 4, 4, 2
-    assert palib.pa_decode_workspace_size(B, Hq, 256, C.byref(d), 256) == (256 + B * Hkv * 8 + 255) // 256 * 256
+    assert palib.pa_decode_workspace_size(B, Hq, 256, C.byref(d), 256) == 0
     ws = palib.pa_decode_workspace_size(B, Hq, 1000, C.byref(d), 256)
-    # 4 partitions of 256 tokens: o [B*Hq*4*128] f32 + m, l [B*Hq*4] f32, then the list
+    # 4 partitions of 256 tokens: o [B*Hq*4*128] f32 + m, l [B*Hq*4] f32, then the counters
     partials = (B * Hq * 4 * (128 + 2) * 4 + 255) // 256 * 256
-    assert ws == partials + (256 + B * Hkv * 4 * 8 + 255) // 256 * 256
-    d8 = _desc(kv_dtype=ops.FP8_E4M3)
-    assert palib.pa_decode_workspace_size(B, Hq, 256, C.byref(d8), 256) == 0
-    assert palib.pa_decode_workspace_size(B, Hq, 1000, C.byref(d8), 256) == partials
+    assert ws == partials + (B * Hkv * 8 + 255) // 256 * 256
+    # 16 partitions: merged by the merge kernel, no counters
+    ws16 = palib.pa_decode_workspace_size(B, Hq, 4000, C.byref(d), 256)
+    assert ws16 == (B * Hq * 16 * (128 + 2) * 4 + 255) // 256 * 256
 
 
 def test_cache_write_and_copy_reject_bad_arguments(palib):
