@@ -60,6 +60,12 @@ __device__ uint32_t g_decode_err;
 #endif
 constexpr int kRingBytes = PA_RING_KB * 1024;  // K/V stage ring of one warp-CTA
 constexpr int kMaxDevices = 64;
+#ifndef PA_EARLY_ISSUE
+#define PA_EARLY_ISSUE 1
+#endif
+#ifndef PA_P_ASC
+#define PA_P_ASC 0
+#endif
 
 struct DecodeArgs {
   const void* q;
@@ -393,7 +399,7 @@ __global__ void __launch_bounds__(32 * W)
   if (a.n_groups == 0) {
     b = blockIdx.x / a.Hkv;
     g = blockIdx.x - b * a.Hkv;
-    p = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+    p = PA_P_ASC ? static_cast<int>(blockIdx.y) : static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
     seq0 = b;
     ncols = a.G;
     j0 = p * a.bpp;
@@ -478,10 +484,13 @@ __global__ void __launch_bounds__(32 * W)
     if (t0 < 0 || t0 >= a.num_blocks) t0 = 0;
     if (t1 < 0 || t1 >= a.num_blocks) t1 = 0;
   }
-  if (a.fuse_write && write_new && wid == 0) {
-    // This partition holds the sequence's last token: store the new row of
-    // kv head g before any tile of it is read, and make the stores visible
-    // to the TMA (async proxy) reads that follow.
+  // This partition holds the sequence's last token: store the new row of kv
+  // head g before the tile holding it is read, and make the stores visible to
+  // the TMA (async proxy) reads that follow.  When that tile is not among the
+  // ring's first fills (one warp, more blocks than stages), the first tiles
+  // are requested before the store, so the store does not delay them.
+  const bool defer_write = W == 1 && PA_EARLY_ISSUE && nb > NS;
+  auto fused_write = [&]() {
     const int64_t slot = a.slot_mapping[b];
     if (slot >= static_cast<int64_t>(a.num_blocks) * 16) {
       if (lane == 0) atomicOr(&g_decode_err, PA_DEVERR_SLOT_RANGE);
@@ -490,7 +499,8 @@ __global__ void __launch_bounds__(32 * W)
                            static_cast<KT*>(const_cast<void*>(a.v_cache_w)), b, g, slot, lane);
       asm volatile("fence.proxy.async.global;" ::: "memory");
     }
-  }
+  };
+  if (a.fuse_write && write_new && wid == 0 && !defer_write) fused_write();
   if (lane == 0) {
     dev::prefetch_tensormap(&tmK);
     dev::prefetch_tensormap(&tmV);
@@ -528,6 +538,10 @@ __global__ void __launch_bounds__(32 * W)
     const int j = wid + i * W;
     const int pb = block_id(min(j, 63));
     if (j < nb && lane == 0) issue(pb, i);
+  }
+  if (a.fuse_write && write_new && defer_write) {
+    fused_write();  // before any refill: the last block is requested by a refill
+    __syncwarp();
   }
   // Every CTA of this grid has started once all of them pass here, so the
   // merge kernel may be scheduled now: its CTAs become resident as slots
