@@ -274,14 +274,14 @@ __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int b, int g, in
     M = fmaxf(M, __shfl_xor_sync(FULL, M, 2));
     float ls = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ls += exp2f(mv[i] - M) * lv[i];  // exp2(-inf) = 0 past np
+    for (int i = 0; i < 16; ++i) ls += dev::ex2(mv[i] - M) * lv[i];  // exp2(-inf) = 0 past np
     ls += __shfl_xor_sync(FULL, ls, 1);
     ls += __shfl_xor_sync(FULL, ls, 2);
     const float inv = 1.f / ls;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int p = sub + 4 * i;
-      if (on && p < np) sw[c * np + p] = exp2f(mv[i] - M) * inv;
+      if (on && p < np) sw[c * np + p] = dev::ex2(mv[i] - M) * inv;
     }
   }
   __syncwarp();
@@ -642,10 +642,8 @@ __global__ void __launch_bounds__(32 * W)
     for (int kk = 0; kk < KSTEPS; ++kk) {
       uint32_t af[4];
       if constexpr (Q8) {
-        af[0] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(kf[kk][0] & 0xffffu));
-        af[1] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(kf[kk][1] & 0xffffu));
-        af[2] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(kf[kk][0] >> 16));
-        af[3] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(kf[kk][1] >> 16));
+        dev::code8x4_to<KT, QT>(kf[kk][0], af[0], af[2]);
+        dev::code8x4_to<KT, QT>(kf[kk][1], af[1], af[3]);
       } else {
         af[0] = kf[kk][0];
         af[1] = kf[kk][1];
@@ -668,10 +666,10 @@ __global__ void __launch_bounds__(32 * W)
       bm1 = fmaxf(bm1, __shfl_xor_sync(FULL, bm1, off));
     }
     const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    const float al0 = dev::ex2(m0 - mn0), al1 = dev::ex2(m1 - mn1);
     m0 = mn0;
     m1 = mn1;
-    float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1), p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+    float p0 = dev::ex2(x0 - mn0), p1 = dev::ex2(x1 - mn1), p2 = dev::ex2(x2 - mn0), p3 = dev::ex2(x3 - mn1);
 
     uint32_t ph_r, ph_r8, pl_r = 0, pl_r8 = 0;
     if constexpr (Q8) {
@@ -717,10 +715,8 @@ __global__ void __launch_bounds__(32 * W)
         const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
         const uint32_t xy = dev::prmt(vf[mt >> 1][0], vf[mt >> 1][1], sel);
         const uint32_t zv = dev::prmt(vf[mt >> 1][2], vf[mt >> 1][3], sel);
-        af[0] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(xy & 0xffffu));
-        af[1] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(xy >> 16));
-        af[2] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(zv & 0xffffu));
-        af[3] = dev::code8x2_to<KT, QT>(static_cast<uint16_t>(zv >> 16));
+        dev::code8x4_to<KT, QT>(xy, af[0], af[1]);
+        dev::code8x4_to<KT, QT>(zv, af[2], af[3]);
       } else {
         af[0] = vf[mt][0];
         af[1] = vf[mt][1];
@@ -774,7 +770,7 @@ __global__ void __launch_bounds__(32 * W)
 #pragma unroll
       for (int w = 0; w < W; ++w) {
         const float* ov = reinterpret_cast<const float*>(base + w * TL::RING);
-        const float f = exp2f(ov[8 * D + h] - M);  // 0 for a warp without blocks
+        const float f = dev::ex2(ov[8 * D + h] - M);  // 0 for a warp without blocks
         acc += f * ov[h * D + d];
         ls += f * ov[8 * D + 8 + h];
       }
@@ -893,9 +889,9 @@ __device__ __forceinline__ void merge_rows(const DecodeArgs& a, size_t row0, int
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, off));
     const float nm = fmaxf(M, cm);
-    const float rescale = exp2f(M - nm);  // 0 on the first chunk
+    const float rescale = dev::ex2(M - nm);  // 0 on the first chunk
     M = nm;
-    const float w = exp2f(mv - nm);       // this lane's partition weight
+    const float w = dev::ex2(mv - nm);       // this lane's partition weight
     float wl = w * lv;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(FULL, wl, off);

@@ -257,6 +257,28 @@ __device__ __forceinline__ uint32_t i8x2_to<__nv_bfloat16>(uint16_t codes) {
   return pack2<__nv_bfloat16>(f.x, f.y);  // exact: |c| <= 128 fits 8 bits
 }
 
+// Four E4M3 codes (byte i = code i) -> f16 pairs, exactly: lo = codes 0, 1;
+// hi = codes 2, 3.  One register split and two paired conversions.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+// Four INT8 codes -> f16 pairs, exactly (the exponent-byte construction of
+// i8x2_to, one sign flip for all four codes).
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  const __half2 bias = __half2half2(__ushort_as_half(0x6480u));  // 1152
+  uint32_t a = prmt(x, 0x64646464u, 0x4140u), b = prmt(x, 0x64646464u, 0x4342u);
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
 // Two 1-byte codes of a quantised cache -> two 16-bit floats of type T:
 // E4M3 for uint8_t storage, INT8 for int8_t storage.
 template <typename KT, typename T>
@@ -265,6 +287,29 @@ __device__ __forceinline__ uint32_t code8x2_to(uint16_t codes) {
     return i8x2_to<T>(codes);
   else
     return e4m3x2_to<T>(codes);
+}
+
+// Four 1-byte codes -> two pairs of 16-bit floats of type T (lo = codes 0,
+// 1; hi = codes 2, 3), exactly.
+template <typename KT, typename T>
+__device__ __forceinline__ void code8x4_to(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (std::is_same<T, __half>::value) {
+    if constexpr (std::is_same<KT, int8_t>::value)
+      i8x4_to_f16(w, lo, hi);
+    else
+      e4m3x4_to_f16(w, lo, hi);
+  } else {
+    lo = code8x2_to<KT, T>(static_cast<uint16_t>(w & 0xffffu));
+    hi = code8x2_to<KT, T>(static_cast<uint16_t>(w >> 16));
+  }
+}
+
+// 2^x for softmax weights (ex2.approx.ftz: about 2^-22 relative error;
+// 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 }  // namespace dev

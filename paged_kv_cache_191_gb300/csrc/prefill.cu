@@ -340,10 +340,11 @@ __global__ void __launch_bounds__(kThreads, PA_PREFILL_MINB)
             for (int kk = 0; kk < KSTEPS; ++kk) {
               float(&acc0)[4] = (kk & 1) ? sd[0] : sc[0];
               float(&acc1)[4] = (kk & 1) ? sd[1] : sc[1];
-              dev::Mma<T>::run(acc0, qf[kk], dev::code8x2_to<KT, T>(static_cast<uint16_t>(wx[kk] & 0xffffu)),
-                               dev::code8x2_to<KT, T>(static_cast<uint16_t>(wx[kk] >> 16)));
-              dev::Mma<T>::run(acc1, qf[kk], dev::code8x2_to<KT, T>(static_cast<uint16_t>(wy[kk] & 0xffffu)),
-                               dev::code8x2_to<KT, T>(static_cast<uint16_t>(wy[kk] >> 16)));
+              uint32_t bx0, bx1, by0, by1;
+              dev::code8x4_to<KT, T>(wx[kk], bx0, bx1);
+              dev::code8x4_to<KT, T>(wy[kk], by0, by1);
+              dev::Mma<T>::run(acc0, qf[kk], bx0, bx1);
+              dev::Mma<T>::run(acc1, qf[kk], by0, by1);
             }
           } else {
 #pragma unroll
