@@ -665,11 +665,27 @@ __global__ void __launch_bounds__(32 * W)
       bm0 = fmaxf(bm0, __shfl_xor_sync(FULL, bm0, off));
       bm1 = fmaxf(bm1, __shfl_xor_sync(FULL, bm1, off));
     }
-    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-    const float al0 = dev::ex2(m0 - mn0), al1 = dev::ex2(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    float p0 = dev::ex2(x0 - mn0), p1 = dev::ex2(x1 - mn1), p2 = dev::ex2(x2 - mn0), p3 = dev::ex2(x3 - mn1);
+    // The reference max of each head moves only when a tile's max exceeds it
+    // by more than 8 (log2 units; one warp vote moves every head at once).
+    // Otherwise the weights exp2(x - m) stay <= 2^8 against the old reference
+    // and O and l keep their scale, so most tiles skip the rescale.  The
+    // first tile always moves it (m = -inf).
+    float al0 = 1.f, al1 = 1.f;
+    if (__any_sync(FULL, bm0 > m0 + 8.f || bm1 > m1 + 8.f)) {
+      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+      al0 = dev::ex2(m0 - mn0);
+      al1 = dev::ex2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
+    float p0 = dev::ex2(x0 - m0), p1 = dev::ex2(x1 - m1), p2 = dev::ex2(x2 - m0), p3 = dev::ex2(x3 - m1);
 
     uint32_t ph_r, ph_r8, pl_r = 0, pl_r8 = 0;
     if constexpr (Q8) {
@@ -706,10 +722,6 @@ __global__ void __launch_bounds__(32 * W)
     // ---- O^T += V^T . P^T ------------------------------------------------------
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
       uint32_t af[4];
       if constexpr (Q8) {
         const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
