@@ -506,21 +506,33 @@ class SharedPrefixStep(DecodeStep):
         self.cap = -(-self.max_len // 16)
         self.kc, self.vc = w.k_pool.to(device), w.v_pool.to(device)
         self.ks = self.vs = None
-        self.q = w.q.to(device)
-        self.new_k, self.new_v = w.new_k.to(device), w.new_v.to(device)
+        # the step's model inputs (q, k_new, v_new) packed in one device buffer,
+        # so the end-to-end run moves them with one copy
+        nq, nkv = self.B * self.Hq * self.D, self.B * self.Hkv * self.D
+        self.qkv = torch.empty(nq + 2 * nkv, dtype=w.q.dtype, device=device)
+        self.q = self.qkv[:nq].view(self.B, self.Hq, self.D)
+        self.new_k = self.qkv[nq: nq + nkv].view(self.B, self.Hkv, self.D)
+        self.new_v = self.qkv[nq + nkv:].view(self.B, self.Hkv, self.D)
+        self.q.copy_(w.q)
+        self.new_k.copy_(w.new_k)
+        self.new_v.copy_(w.new_v)
         self.out = torch.empty((self.B, self.Hq, self.D), dtype=w.q.dtype, device=device)
         self.desc = ops.cache_desc(self.kc)
         self.ws_bytes = ops.decode_workspace_size(self.B, self.Hq, self.max_len, self.kc, split_tokens)
-        # shared-prefix groups: each group's beams share the prompt's blocks
+        # shared-prefix groups: the beams of one prompt; each step's shared
+        # prefix is the longest run of leading table entries all of a group's
+        # beams hold (the prompt, and tail blocks inherited from a common
+        # ancestor), staged with the step's metadata
         self.grouped = True
-        self.group_start = torch.arange(0, self.B + 1, w.beams, dtype=torch.int32, device=device)
-        self.prefix_blocks = torch.full((w.groups,), w.prompt_len // 16, dtype=torch.int32, device=device)
+        self.group_start_host = np.arange(0, self.B + 1, w.beams, dtype=np.int32)
+        self.group_start = torch.from_numpy(self.group_start_host).to(device)
         gws = int(self.L.pa_decode_grouped_workspace_size(self.B, self.Hq, self.max_len, w.groups, w.beams,
-                                                          w.prompt_len // 16, C.byref(self.desc), split_tokens))
+                                                          self.cap, C.byref(self.desc), split_tokens))
         self.ws = torch.empty(max(self.ws_bytes, gws, 16), dtype=torch.uint8, device=device)
         self.split = split_tokens
-        # meta: slots int64[B] | pairs int64[B, 2] | lens int32[B] | tables int32[B, cap]
-        self.meta_bytes = self.B * 8 + self.B * 16 + self.B * 4 + self.B * self.cap * 4
+        # meta: slots int64[B] | pairs int64[B, 2] | lens int32[B] | tables int32[B, cap] | prefix int32[groups]
+        self.pre_off = self.B * 8 + self.B * 16 + self.B * 4 + self.B * self.cap * 4
+        self.meta_bytes = self.pre_off + w.groups * 4
         self.meta_host = [torch.empty(self.meta_bytes, dtype=torch.uint8).pin_memory() for _ in range(RING)]
         self.meta_devs = [torch.empty(self.meta_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
         self.use_meta(0)
@@ -543,15 +555,27 @@ class SharedPrefixStep(DecodeStep):
         self.slots_dev = self.meta_dev[: B * 8].view(T.int64)
         self.pairs_dev = self.meta_dev[B * 8: B * 24].view(T.int64).view(B, 2)
         self.lens_dev = self.meta_dev[B * 24: B * 28].view(T.int32)
-        self.tables_dev = self.meta_dev[B * 28:].view(T.int32).view(B, self.cap)
+        self.tables_dev = self.meta_dev[B * 28: self.pre_off].view(T.int32).view(B, self.cap)
+        self.prefix_dev = self.meta_dev[self.pre_off:].view(T.int32)
 
     def prebuild(self, stream):
         super().prebuild(stream)
         w = self.w
-        extra = (C.c_void_p(self.group_start.data_ptr()), C.c_void_p(self.prefix_blocks.data_ptr()), w.groups,
-                 w.beams, w.prompt_len // 16)
         # pa_decode_append's arguments with the group description after `scale`
-        self.grouped_args = [a[:17] + extra + a[17:] for a in self.append_args]
+        self.grouped_args = []
+        for i, a in enumerate(self.append_args):
+            pre = C.c_void_p(self.meta_devs[i].data_ptr() + self.pre_off)
+            extra = (C.c_void_p(self.group_start.data_ptr()), pre, w.groups, w.beams, self.cap)
+            self.grouped_args.append(a[:17] + extra + a[17:])
+
+    def stage_prefix(self, raw):
+        """Each group's shared prefix (ops.shared_table_prefix) from the tables
+        and lengths the block manager just staged in `raw`, the pinned
+        metadata buffer, written beside them."""
+        w, B = self.w, self.B
+        tables = raw[B * 28: self.pre_off].view(np.int32).reshape(B, self.cap)
+        lens = raw[B * 24: B * 28].view(np.int32)
+        self.ops.shared_table_prefix(tables, lens, self.group_start_host, out=raw[self.pre_off:].view(np.int32))
 
     def _fresh(self, n):
         ids = np.arange(self.next_id, self.next_id + n, dtype=np.uint64)
@@ -595,6 +619,7 @@ class SharedPrefixStep(DecodeStep):
         self.ops._check(self.L.pa_block_tables(self.alloc._h, self.ids_c, B, C.cast(base + B * 28, C.POINTER(C.c_int32)),
                                                self.cap, C.cast(base + B * 24, C.POINTER(C.c_int32))),
                         "pa_block_tables")
+        self.stage_prefix(buf.numpy())
         self.n_cow = self.ncow_c.value
         self.steps_since_reset += 1
         self.step_idx += 1
@@ -650,7 +675,7 @@ class SharedPrefixStep(DecodeStep):
         B = self.B
         raw = buf.numpy()
         lens = raw[B * 24: B * 28].view(np.int32).copy()
-        tables = raw[B * 28:].view(np.int32).reshape(B, self.cap).copy()
+        tables = raw[B * 28: self.pre_off].view(np.int32).reshape(B, self.cap).copy()
         self.history.append((tables, lens, self.n_cow))
         return 0, 0
 
@@ -1067,53 +1092,38 @@ def run_e2e(st, args, stream):
                 "api": "paged_kv_cache_191_gb300.session.DecodeSession (block manager writes into a pinned staging "
                        "buffer beside q / k_new / v_new, the next step's while the current one runs; one H2D copy, "
                        "pa_decode_append, one D2H copy of the output, waited for every step)"}
-    hq = st.w.q.pin_memory()
-    hk, hv = st.w.new_k.pin_memory(), st.w.new_v.pin_memory()
+    # Shared-prefix beam search: the timed step's own path (block manager ->
+    # pinned metadata with the groups' prefixes -> one copy; copy-on-write
+    # copies; the grouped fused decode) plus the model's inputs from pinned
+    # host memory (q, k_new, v_new packed: one copy) and the output back (one
+    # copy), waited for every step.
+    hqkv = torch.empty(st.qkv.shape, dtype=st.qkv.dtype).pin_memory()
+    hqkv.copy_(st.qkv)
     hout = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    dq = torch.empty_like(st.q)
-    dk, dv = torch.empty_like(st.new_k), torch.empty_like(st.new_v)
-    total_b = 0
-    h2d = hq.numel() * hq.element_size() + 2 * hk.numel() * hk.element_size() + st.meta_bytes
-    d2h = hout.numel() * hout.element_size()
-    shared = isinstance(st, SharedPrefixStep)
-    if shared:
-        st.history.clear()
+    st.history.clear()
+    drv, sp = st.drv, st.sp
     with torch.cuda.stream(stream):
         stream.synchronize()
         t0 = time.perf_counter()
         for _ in range(n):
             buf = st.host_prepare()
-            _, s = st.step_bytes()
-            total_b += s
-            st.use_meta(0)
-            st.meta_dev.copy_(buf, non_blocking=True)
-            if getattr(st, "n_cow", 0):
-                ops.copy_blocks(st.kc, st.vc, st.pairs_dev[: st.n_cow], stream=stream)
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            if st.grouped:  # the fused write + grouped decode, as in the timed steps
-                ops.decode_append_grouped(dk, dv, st.slots_dev, dq, st.kc, st.vc, st.tables_dev, st.lens_dev,
-                                          st.max_len, st.w.scale, st.group_start, st.prefix_blocks, st.w.beams,
-                                          st.w.prompt_len // 16, out=st.out, workspace=st.ws,
-                                          split_tokens=st.split, stream=stream)
-            else:
-                ops.cache_write(dk, dv, st.slots_dev, st.kc, st.vc, st.ks, st.vs, stream=stream)
-                ops.decode(dq, st.kc, st.vc, st.tables_dev, st.lens_dev, st.max_len, st.w.scale,
-                           out=st.out, k_scale=st.ks, v_scale=st.vs, workspace=st.ws,
-                           split_tokens=st.split, stream=stream)
+            st.step_bytes()
+            drv.h2d(st.qkv.data_ptr(), hqkv.data_ptr(), hqkv.numel() * hqkv.element_size(), sp)
+            st.enqueue(buf)
             hout.copy_(st.out, non_blocking=True)
             stream.synchronize()
         t1 = time.perf_counter()
-    if shared:
-        total_b = st.count_bytes()[1]
-        st.history.clear()
+    total_b = st.count_bytes()[1]
+    st.history.clear()
+    h2d = st.meta_bytes + hqkv.numel() * hqkv.element_size()
+    d2h = hout.numel() * hout.element_size()
     return {"value": round(total_b / (t1 - t0) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
             "tokens_per_s": round(st.B * n / (t1 - t0), 1),
-            "api": "paged_kv_cache_191_gb300.ops (pinned host buffers, copy_blocks + decode_append_grouped, "
-                   "stream sync per step)" if st.grouped else
-                   "paged_kv_cache_191_gb300.ops (pinned host buffers, stream sync per step)"}
+            "api": "libpagedkv C ABI through the benchmark's step (block manager writes slots, copy pairs, tables "
+                   "and each group's shared prefix into a pinned staging buffer; one H2D copy of it and one of the "
+                   "packed q / k_new / v_new; pa_copy_blocks; pa_decode_append_grouped; one D2H copy of the "
+                   "output; waited for every step)"}
 
 
 # ---- multi-token workloads (chunked prefill, speculative verify) ------------------

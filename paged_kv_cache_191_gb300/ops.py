@@ -409,6 +409,38 @@ def prefix_groups(block_tables, context_lens, max_group_size):
     return np.asarray(starts, dtype=np.int32), np.asarray(prefixes, dtype=np.int32)
 
 
+def shared_table_prefix(block_tables, context_lens, group_start, out=None):
+    """Host helper for decode_append_grouped over fixed groups (the beams of
+    one prompt): for each group, the number of leading table entries that all
+    of its members hold, counted up to the longest member's blocks.  The
+    kernel clamps it further to the whole blocks before each member's last
+    token.  block_tables int [B, max_blocks], context_lens int [B],
+    group_start int [n + 1]; returns (or fills `out`) int32 [n]."""
+    import numpy as np
+    tables = np.asarray(block_tables)
+    lens = np.asarray(context_lens)
+    gs = np.asarray(group_start)
+    n = len(gs) - 1
+    res = np.zeros(n, dtype=np.int32) if out is None else out
+    sizes = np.diff(gs)
+    if n and (sizes == sizes[0]).all() and sizes[0] > 0:  # equal groups: one vectorised pass
+        k = int(sizes[0])
+        nblk = int((int(lens[gs[0]:gs[-1]].max()) + BLOCK_SIZE - 1) // BLOCK_SIZE) if gs[-1] > gs[0] else 0
+        t = tables[gs[0]:gs[-1], :nblk].reshape(n, k, nblk)
+        same = (t == t[:, :1, :]).all(axis=1)
+        res[:] = np.where(same.all(axis=1), nblk, np.argmin(same, axis=1))
+        return res
+    for i in range(n):
+        a, b = int(gs[i]), int(gs[i + 1])
+        if b <= a:
+            res[i] = 0
+            continue
+        nblk = int((int(lens[a:b].max()) + BLOCK_SIZE - 1) // BLOCK_SIZE)
+        same = (tables[a:b, :nblk] == tables[a, :nblk]).all(axis=0)
+        res[i] = nblk if same.all() else int(np.argmin(same))
+    return res
+
+
 def copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None, stream=None):
     """Copy whole blocks for each (src, dst) row of pairs (int64 [n, 2])."""
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (pairs, "pairs")):

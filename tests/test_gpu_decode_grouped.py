@@ -165,7 +165,9 @@ def test_shared_prefix_16x4_full_size():
     manager and the oracle's model run in lockstep (slots, copy pairs and
     tables identical), caches stay bit-identical to the oracle's, and every
     (beam, head) row matches the float64 oracle within the f16 tolerance --
-    the grouped call and the plain fused call alike.
+    the grouped call and the plain fused call alike.  Each group's shared
+    prefix is staged per step as the benchmark does: the prompt plus the tail
+    blocks its beams inherited from a common ancestor.
 
     Source: "大模型推理引擎优化：KV Cache 与连续批处理" 4.2 and
     "LLM推理引擎深度实战：从PagedAttention到分布式推理部署" 2.2 (shared blocks
@@ -193,12 +195,12 @@ def test_shared_prefix_16x4_full_size():
     kc, vc = w.k_pool.to(DEV), w.v_pool.to(DEV)
     okc, ovc = np_exact(w.k_pool), np_exact(w.v_pool)
     cap = -(-(w.prompt_len + int(tails.max()) + 8) // 16)
-    gs = torch.arange(0, B + 1, beams, dtype=torch.int32, device=DEV)
-    pre = torch.full((w.groups,), w.prompt_len // 16, dtype=torch.int32, device=DEV)
+    gs_host = np.arange(0, B + 1, beams, dtype=np.int32)
+    gs = torch.from_numpy(gs_host).to(DEV)
     rng = W.rng_for(23)
     q = w.q.to(DEV)
-    total_cow = 0
-    for step in range(3):
+    total_cow = total_extra = 0
+    for step in range(6):
         par = (np.arange(w.groups)[:, None] * beams + w.parents[step]).reshape(-1).tolist()
         ca.reselect(ids, par)
         oa.reselect(ids, par)
@@ -219,8 +221,14 @@ def test_shared_prefix_16x4_full_size():
         sl = torch.tensor(slots, dtype=torch.int64, device=DEV)
         bt, cl = torch.from_numpy(tables).to(DEV), torch.from_numpy(lens).to(DEV)
         ml = int(lens.max())
+        # each group's shared prefix as the benchmark stages it: the prompt and
+        # the tail blocks its beams inherited from a common ancestor
+        pre_host = ops.shared_table_prefix(tables, lens, gs_host)
+        assert (pre_host >= w.prompt_len // 16).all()
+        total_extra += int((pre_host - w.prompt_len // 16).sum())
+        pre = torch.from_numpy(pre_host).to(DEV)
         out = ops.decode_append_grouped(nk.to(DEV), nv.to(DEV), sl, q, kc, vc, bt, cl, ml, w.scale, gs, pre, beams,
-                                        w.prompt_len // 16, out_dtype=torch.float32)
+                                        cap, out_dtype=torch.float32)
         # the plain fused call on the same state: it stores the same rows again
         plain = ops.decode_append(nk.to(DEV), nv.to(DEV), sl, q, kc, vc, bt, cl, ml, w.scale,
                                   out_dtype=torch.float32)
@@ -230,4 +238,5 @@ def test_shared_prefix_16x4_full_size():
         assert_close(out.cpu().numpy(), ref, TOL["f16"], f"grouped step {step}")
         assert_close(plain.cpu().numpy(), ref, TOL["f16"], f"plain step {step}")
     assert total_cow > 0, "reselection is meant to exercise copy-on-write"
+    assert total_extra > 0, "some group is meant to share tail blocks beyond the prompt"
     assert np.array_equal(np_exact(kc), okc) and np.array_equal(np_exact(vc), ovc)

@@ -46,3 +46,43 @@ def test_empty_and_unrelated_sequences_start_their_own_groups():
     tables = np.array([[1, 2], [1, 2], [3, 4], [5, 6]])
     gs, pre = ops.prefix_groups(tables, np.array([0, 20, 20, 20]), 4)
     assert gs.tolist() == [0, 1, 2, 3, 4] and pre.tolist() == [0, 0, 0, 0]
+
+
+def _prefix_by_definition(tables, lens, gs):
+    out = []
+    for i in range(len(gs) - 1):
+        rows = tables[gs[i]:gs[i + 1]]
+        nblk = -(-int(lens[gs[i]:gs[i + 1]].max()) // 16)
+        n = 0
+        while n < nblk and all(r[n] == rows[0][n] for r in rows):
+            n += 1
+        out.append(n)
+    return out
+
+
+@pytest.mark.parametrize("equal_groups", [True, False])
+def test_shared_table_prefix_matches_its_definition(palib, equal_groups):
+    """Beams of three prompts reselected from parents for several steps (as
+    beam search does), so groups share the prompt and tail blocks inherited
+    from common ancestors: the helper's count equals the leading entries
+    every member holds, for equal and unequal group sizes."""
+    rng = np.random.Generator(np.random.PCG64(8))
+    sizes = [4, 4, 4] if equal_groups else [4, 2, 3]
+    a = ops.BlockAllocator(600, rng.permutation(600))
+    ids, gs = [], [0]
+    for g, n in enumerate(sizes):
+        a.alloc_seq(10_000 + g, 32 * 16 + 7 * g)
+        kids = list(range(len(ids), len(ids) + n))
+        a.fork_seqs([10_000 + g] * n, kids)
+        for k in kids:
+            a.append_tokens(k, int(rng.integers(1, 60)), want_slots=False)
+        ids += kids
+        gs.append(len(ids))
+    for step in range(12):
+        par = [gs[g] + int(rng.integers(0, sizes[g])) - gs[g] for g in range(len(sizes)) for _ in range(sizes[g])]
+        par = [gs[g] + p for g, p in zip([g for g in range(len(sizes)) for _ in range(sizes[g])], par)]
+        a.reselect(ids, par)
+        a.append_slots(ids)
+        tables, lens = a.tables(ids, 80)
+        got = ops.shared_table_prefix(tables, lens, np.asarray(gs))
+        assert got.tolist() == _prefix_by_definition(tables, lens, gs)
