@@ -478,7 +478,14 @@ class DecodeStep:
         return self._bytes_table[k]
 
     def launches_per_step(self):
-        return (1 if self.fused else 2) + (1 if self.ws_bytes else 0)
+        """Kernels one step launches: the decode call's own count (main kernel,
+        plus the merge kernel when the library plans one) and the separate
+        cache write when the write is not fused; the grouped call always
+        follows its main kernel with decode_reduce_grouped."""
+        if getattr(self, "grouped", False) and self.fused:
+            return 2
+        _, _, kernels = self.ops.decode_plan_info(self.B, self.Hq, self.max_len, self.kc, self.split)
+        return kernels + (0 if self.fused else 1)
 
 
 class SharedPrefixStep(DecodeStep):
@@ -1216,7 +1223,9 @@ class PrefillStep:
             ev[1].record(stream)
 
     def launches_per_step(self):
-        return 2 + (1 if self.ws_bytes else 0)
+        """pa_cache_write, then what pa_chunked_prefill launches (its own count)."""
+        w = self.w
+        return 1 + self.ops.chunked_prefill_plan_info(w.T, w.B, w.Hq, self.max_q, self.max_len, self.kc, self.split)[3]
 
 
 def _prefill_oracle_task(task):

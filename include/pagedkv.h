@@ -136,6 +136,20 @@ size_t pa_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_cont
                                 const pa_cache_desc* desc, int32_t split_tokens);
 
 /*
+ * pa_decode_plan_info -- the split pa_decode / pa_decode_append would use for
+ * the same arguments, for callers that size, log or profile their steps (host
+ * only; nothing is launched).  partitions: partitions of the longest allowed
+ * context; blocks_per_partition: 16-token blocks per partition; kernels:
+ * kernels one call launches (1 when one partition covers the context or the
+ * decode kernel merges the partitions itself -- at most 8 of them; 2 when a
+ * merge kernel follows).  Any output pointer may be NULL.  PA_ERR_INVALID /
+ * PA_ERR_UNSUPPORTED as pa_decode would return for the shape.
+ */
+pa_status pa_decode_plan_info(int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                              const pa_cache_desc* desc, int32_t split_tokens,
+                              int32_t* partitions, int32_t* blocks_per_partition, int32_t* kernels);
+
+/*
  * pa_decode -- one decode step of paged attention.
  * [LLM-INF] 2.3: the kernel translates logical token t of sequence b into
  * physical block block_tables[b][t/16], row t%16, and gathers K/V from there.
@@ -266,6 +280,21 @@ pa_status pa_decode_append_grouped(const void* k_new, const void* v_new, int32_t
 size_t pa_chunked_prefill_workspace_size(int32_t num_tokens, int32_t B, int32_t num_q_heads,
                                          int32_t max_q_len, int32_t max_context_len,
                                          const pa_cache_desc* desc, int32_t split_tokens);
+
+/*
+ * pa_chunked_prefill_plan_info -- what pa_chunked_prefill would launch for
+ * the same arguments (host only).  tensor_cores: 1 for the tcgen05 kernel
+ * (128-row tiles), 0 for the mma.sync kernel (64-row tiles); partitions and
+ * blocks_per_partition of the multi-token kernel; kernels: kernels one call
+ * launches at most (over a 1-byte cache the one-token sequences first go
+ * through the decode kernel, and a call with max_q_len 1 launches only
+ * those).  Any output pointer may be NULL.
+ */
+pa_status pa_chunked_prefill_plan_info(int32_t num_tokens, int32_t B, int32_t num_q_heads,
+                                       int32_t max_q_len, int32_t max_context_len,
+                                       const pa_cache_desc* desc, int32_t split_tokens,
+                                       int32_t* tensor_cores, int32_t* partitions,
+                                       int32_t* blocks_per_partition, int32_t* kernels);
 
 /*
  * pa_chunked_prefill -- paged attention for several query tokens per

@@ -147,6 +147,16 @@ pa_status plan_prefill(int32_t T, int32_t B, int32_t Hq, int32_t max_q_len, int3
   } else {
     plan->workspace_bytes = 0;
   }
+  // Over a 1-byte cache the multi-token kernel converts every tile per warp,
+  // which a one-row tile of a decode step riding in the call cannot repay:
+  // those sequences go to the decode kernel, whose workspace follows.
+  plan->route_single = quantised(d->kv_dtype) ? 1 : 0;
+  plan->dec_offset = plan->workspace_bytes;
+  if (plan->route_single) {
+    pa_status st = plan_decode(B, Hq, max_context_len, d, 0, &plan->dec);
+    if (st != PA_OK) return st;
+    plan->workspace_bytes += plan->dec.workspace_bytes;
+  }
   return PA_OK;
 }
 
@@ -198,6 +208,29 @@ size_t pa_decode_workspace_size(int32_t B, int32_t num_q_heads, int32_t max_cont
   if (pa::plan_decode(B, num_q_heads, max_context_len, desc, split_tokens, &plan) != PA_OK)
     return 0;
   return plan.workspace_bytes;
+}
+
+// Kernels a decode call with this plan launches: the main kernel, and the
+// merge kernel unless one partition covers the context or the main kernel
+// merges its partitions itself.
+static int32_t decode_kernels(const pa::DecodePlan& plan) {
+  return 1 + (plan.max_parts > 1 && plan.ticket_offset == 0 ? 1 : 0);
+}
+
+pa_status pa_decode_plan_info(int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                              const pa_cache_desc* desc, int32_t split_tokens, int32_t* partitions,
+                              int32_t* blocks_per_partition, int32_t* kernels) {
+  pa_status st = pa::check_desc(desc, "pa_decode_plan_info");
+  if (st != PA_OK) return st;
+  if (B < 0 || num_q_heads <= 0 || max_context_len < 0)
+    return fail(PA_ERR_INVALID, "pa_decode_plan_info: B, num_q_heads or max_context_len out of range");
+  pa::DecodePlan plan;
+  st = pa::plan_decode(B, num_q_heads, max_context_len, desc, split_tokens, &plan);
+  if (st != PA_OK) return st;
+  if (partitions) *partitions = plan.max_parts;
+  if (blocks_per_partition) *blocks_per_partition = plan.blocks_per_part;
+  if (kernels) *kernels = decode_kernels(plan);
+  return PA_OK;
 }
 
 // Shared-prefix groups of a grouped decode call (none: n_groups == 0).
@@ -404,6 +437,25 @@ static pa_status check_prefill(int32_t T, int32_t B, int32_t num_q_heads, int32_
     return fail(PA_ERR_INVALID, "pa_chunked_prefill: num_q_heads must be a multiple of num_kv_heads");
   if (num_q_heads / desc->num_kv_heads > PA_MAX_GROUP)
     return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: more than %d query heads per kv head", PA_MAX_GROUP);
+  return PA_OK;
+}
+
+pa_status pa_chunked_prefill_plan_info(int32_t num_tokens, int32_t B, int32_t num_q_heads, int32_t max_q_len,
+                                       int32_t max_context_len, const pa_cache_desc* desc, int32_t split_tokens,
+                                       int32_t* tensor_cores, int32_t* partitions,
+                                       int32_t* blocks_per_partition, int32_t* kernels) {
+  pa_status st = check_prefill(num_tokens, B, num_q_heads, max_q_len, max_context_len, desc);
+  if (st != PA_OK) return st;
+  pa::PrefillPlan plan;
+  st = pa::plan_prefill(num_tokens, B, num_q_heads, max_q_len, max_context_len, desc, split_tokens, &plan);
+  if (st != PA_OK) return st;
+  if (tensor_cores) *tensor_cores = plan.tc;
+  if (partitions) *partitions = plan.max_parts;
+  if (blocks_per_partition) *blocks_per_partition = plan.blocks_per_part;
+  if (kernels) {
+    const int32_t multi = max_q_len > 1 || !plan.route_single ? 1 + (plan.max_parts > 1 ? 1 : 0) : 0;
+    *kernels = multi + (plan.route_single ? decode_kernels(plan.dec) : 0);
+  }
   return PA_OK;
 }
 

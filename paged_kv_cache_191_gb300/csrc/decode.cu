@@ -103,6 +103,11 @@ struct DecodeArgs {
   // kv head), stamped with this launch's epoch
   unsigned long long* tickets;
   uint32_t epoch;
+  // the one-token sequences of a multi-token call (else null): sequence b's
+  // query and output row is q_start[b] of q_rows; sequences with another
+  // number of query tokens are left to the multi-token kernel
+  const int32_t* q_start;
+  int32_t q_rows;
 };
 
 // A group's usable shared prefix: whole blocks every member has before the
@@ -251,7 +256,8 @@ __device__ __forceinline__ bool take_ticket(const DecodeArgs& a, int b, int g, i
 // Partials written by other CTAs are read at L2 (ld.global.cg).  `sw` is
 // G * np floats of this warp's idle shared memory.  np <= 64.
 template <typename QT, int D>
-__device__ __forceinline__ void merge_pair(const DecodeArgs& a, int b, int g, int np, int lane, float* sw) {
+__device__ __forceinline__ void merge_pair(const DecodeArgs& a, int b, int g, int np, int lane, float* sw,
+                                           int64_t oshift) {
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int V = D / 32;  // dims per lane
   const size_t head0 = static_cast<size_t>(b) * a.Hq + static_cast<size_t>(g) * a.G;
@@ -321,7 +327,8 @@ __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int b, int g, in
   for (int c = 0; c < PA_MAX_GROUP; ++c)
     if (c < a.G)
 #pragma unroll
-      for (int v = 0; v < V; ++v) store_out<QT>(a, (head0 + c) * D + lane * V + v, acc[c][v]);
+      for (int v = 0; v < V; ++v)
+        store_out<QT>(a, static_cast<size_t>(static_cast<int64_t>((head0 + c) * D + lane * V + v) + oshift), acc[c][v]);
   if (lane == 0)  // ready for the next launch with this epoch (a replayed graph)
     a.tickets[static_cast<size_t>(b) * a.Hkv + g] = static_cast<unsigned long long>(a.epoch) << 32;
 }
@@ -362,6 +369,7 @@ __global__ void __launch_bounds__(32 * W)
   // sequence seq0 + c / G.
   int b, g, p;       // table owner (and fused-write sequence), kv head, partition of its rows
   int seq0, ncols;   // query columns
+  int qb = -1;       // query / output row of sequence seq0 (seq0 unless the call maps rows)
   int j0, L, nb;     // first block, owner's length, blocks of this item
   bool direct;       // one partition covers the rows: write the output itself
   bool write_new;    // this item reads the owner's last block (fused write)
@@ -371,7 +379,7 @@ __global__ void __launch_bounds__(32 * W)
   auto load_q = [&]() {
     const int c = r < ncols ? r : 0;
     const QT* qrow = static_cast<const QT*>(a.q) +
-                     (static_cast<size_t>(seq0 + c / a.G) * a.Hq + g * a.G + c % a.G) * D;
+                     (static_cast<size_t>((qb >= 0 ? qb : seq0) + c / a.G) * a.Hq + g * a.G + c % a.G) * D;
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
       if (r < ncols) {
@@ -389,8 +397,9 @@ __global__ void __launch_bounds__(32 * W)
     }
   };
   auto zero_rows = [&](int bz) {  // empty context: zero rows of (bz, g)
+    const size_t ob = qb >= 0 && bz == seq0 ? qb : bz;
     for (int i = lane; i < a.G * D; i += 32)
-      store_out<QT>(a, (static_cast<size_t>(bz) * a.Hq + g * a.G + i / D) * D + i % D, 0.f);
+      store_out<QT>(a, (ob * a.Hq + g * a.G + i / D) * D + i % D, 0.f);
   };
 
   // Launched as a dependent of the preceding kernel (normally the cache
@@ -410,6 +419,11 @@ __global__ void __launch_bounds__(32 * W)
     const int row_left = a.max_blocks - j0;
     t0 = (lane < a.bpp && lane < row_left) ? row[lane] : 0;
     t1 = (lane + 32 < a.bpp && lane + 32 < row_left) ? row[lane + 32] : 0;
+    if (a.q_start) {  // one-token rows of a multi-token call only
+      const int s0 = a.q_start[b], s1 = a.q_start[b + 1];
+      if (s1 - s0 != 1 || s0 < 0 || s1 > a.q_rows) return;
+      qb = s0;
+    }
     load_q();
     L = checked_len(a, b, lane == 0 && p == 0);
     const int nblk = (L + 15) >> 4;
@@ -477,6 +491,8 @@ __global__ void __launch_bounds__(32 * W)
       load_q();
     }
   }
+  // output rows are query rows: shifted when the call maps sequences to rows
+  const int64_t oshift = qb >= 0 ? static_cast<int64_t>(qb - seq0) * a.Hq * D : 0;
   const bool bad = (lane < nb && (t0 < 0 || t0 >= a.num_blocks)) ||
                    (lane + 32 < nb && (t1 < 0 || t1 >= a.num_blocks));
   if (bad) {
@@ -788,7 +804,7 @@ __global__ void __launch_bounds__(32 * W)
       }
       const size_t head = static_cast<size_t>(seq0 + h / a.G) * a.Hq + g * a.G + h % a.G;
       if (direct) {
-        store_out<QT>(a, head * D + d, acc / ls);
+        store_out<QT>(a, static_cast<size_t>(static_cast<int64_t>(head * D + d) + oshift), acc / ls);
       } else {
         const size_t rowp = head * a.max_parts + p;
         a.part_o[rowp * D + d] = acc;
@@ -807,7 +823,7 @@ __global__ void __launch_bounds__(32 * W)
       __syncthreads();
       if (s_last && wid == 0) {
         __threadfence();  // the other partitions' partials, published before their tickets
-        merge_pair<QT, D>(a, b, g, np, lane, reinterpret_cast<float*>(base));
+        merge_pair<QT, D>(a, b, g, np, lane, reinterpret_cast<float*>(base), oshift);
       }
     }
     return;
@@ -826,13 +842,14 @@ __global__ void __launch_bounds__(32 * W)
       d_r8 = d_r + 8;
     }
     if (direct) {
+      const int64_t oA = static_cast<int64_t>(headA * D) + oshift, oB = static_cast<int64_t>(headB * D) + oshift;
       if (okA) {
-        store_out<QT>(a, headA * D + d_r, o[mt][0] / l0);
-        store_out<QT>(a, headA * D + d_r8, o[mt][2] / l0);
+        store_out<QT>(a, static_cast<size_t>(oA + d_r), o[mt][0] / l0);
+        store_out<QT>(a, static_cast<size_t>(oA + d_r8), o[mt][2] / l0);
       }
       if (okB) {
-        store_out<QT>(a, headB * D + d_r, o[mt][1] / l1);
-        store_out<QT>(a, headB * D + d_r8, o[mt][3] / l1);
+        store_out<QT>(a, static_cast<size_t>(oB + d_r), o[mt][1] / l1);
+        store_out<QT>(a, static_cast<size_t>(oB + d_r8), o[mt][3] / l1);
       }
     } else {
       const size_t rowA = headA * a.max_parts + p, rowB = headB * a.max_parts + p;
@@ -863,7 +880,7 @@ __global__ void __launch_bounds__(32 * W)
     const bool last = __shfl_sync(FULL, lane == 0 ? take_ticket(a, b, g, np) : false, 0);
     if (last) {
       __threadfence();  // the other partitions' partials, published before their tickets
-      merge_pair<QT, D>(a, b, g, np, lane, reinterpret_cast<float*>(base));
+      merge_pair<QT, D>(a, b, g, np, lane, reinterpret_cast<float*>(base), oshift);
     }
   }
 }
@@ -954,7 +971,13 @@ __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce(const DecodeA
   const int nblk = (L + 15) >> 4;
   const int nparts = (nblk + a.bpp - 1) / a.bpp;
   if (nparts <= 1) return;  // written by decode_main (zero rows included)
-  merge_rows<QT, D>(a, row0, nparts, mv, lv, static_cast<size_t>(b) * a.Hq + h, lane);
+  int ob = b;
+  if (a.q_start) {  // one-token rows of a multi-token call only
+    const int s0 = a.q_start[b], s1 = a.q_start[b + 1];
+    if (s1 - s0 != 1 || s0 < 0 || s1 > a.q_rows) return;
+    ob = s0;
+  }
+  merge_rows<QT, D>(a, row0, nparts, mv, lv, static_cast<size_t>(ob) * a.Hq + h, lane);
 }
 
 // The grouped form: one CTA per (group k, member m, kv head g).  A member's
@@ -1047,6 +1070,8 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   a.max_members = l.max_members;
   a.pre_parts = l.plan.pre_parts;
   a.tail_parts = l.plan.tail_parts;
+  a.q_start = l.q_start;
+  a.q_rows = l.q_rows;
   a.tickets = nullptr;
   a.epoch = 0;
   if (l.plan.ticket_offset) {  // after the partials: the arrival counters

@@ -79,6 +79,10 @@ struct DecodeLaunch {
   const int32_t* group_start = nullptr;
   const int32_t* prefix_blocks = nullptr;
   int32_t n_groups = 0, max_members = 0;
+  // rows of a multi-token call (pa_chunked_prefill over a 1-byte cache): only
+  // sequences with one query token, whose query / output row is q_start[b]
+  const int32_t* q_start = nullptr;
+  int32_t q_rows = 0;
 };
 pa_status launch_decode(const DecodeLaunch& a, void* stream);
 
@@ -88,7 +92,12 @@ struct PrefillPlan {
   int32_t row_tiles;        // row tiles per (sequence, kv head) for max_q_len
   int32_t blocks_per_part;  // 16-token blocks per partition
   int32_t max_parts;        // partitions of the longest allowed context
-  size_t workspace_bytes;   // 0 when max_parts == 1
+  size_t workspace_bytes;   // 0 when max_parts == 1 and no one-token routing
+  // 1-byte caches: one-token sequences of the call go to the decode kernel,
+  // with this plan, its workspace at byte dec_offset
+  int32_t route_single = 0;
+  DecodePlan dec;
+  size_t dec_offset = 0;
 };
 // Whether pa_chunked_prefill runs its tcgen05 kernel (128-row tiles) for
 // this shape: head_dim 128 and more than 64 rows per (sequence, kv head).

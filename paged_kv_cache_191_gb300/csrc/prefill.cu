@@ -81,6 +81,7 @@ struct PrefillArgs {
   int32_t out_f32;
   const float* k_scale;  // FP8 / INT8 caches: [num_blocks][16] per-token scales
   const float* v_scale;
+  int32_t skip_single;   // sequences with one query token are served by the decode kernel
 };
 
 // Shared memory of prefill_main: the K/V stage ring, full and empty
@@ -128,6 +129,7 @@ __device__ __forceinline__ SeqView seq_view(const PrefillArgs& a, int b, bool re
     v.L = max(0, min(v.L, cap));
   }
   if (v.n > v.L && report) atomicOr(&g_prefill_err, PA_DEVERR_CONTEXT_LEN);  // early tokens get no keys
+  if (a.skip_single && v.n == 1) v.n = 0;  // its row is the decode kernel's
   return v;
 }
 
@@ -1176,6 +1178,39 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
   a.out_f32 = l.out_dtype == PA_DTYPE_F32;
   a.k_scale = l.k_scale;
   a.v_scale = l.v_scale;
+  a.skip_single = l.plan.route_single;
+
+  if (l.plan.route_single) {
+    // one-token sequences (decode steps riding in the call) first, through the
+    // decode kernel: a one-row tile would waste the multi-token kernel's CTA
+    DecodeLaunch d;
+    d.q = l.q;
+    d.q_dtype = l.q_dtype;
+    d.k_cache = l.k_cache;
+    d.v_cache = l.v_cache;
+    d.k_scale = l.k_scale;
+    d.v_scale = l.v_scale;
+    d.block_tables = l.block_tables;
+    d.max_blocks = l.max_blocks;
+    d.context_lens = l.context_lens;
+    d.max_context_len = l.max_context_len;
+    d.B = l.B;
+    d.Hq = l.Hq;
+    d.Hkv = l.Hkv;
+    d.D = l.D;
+    d.num_blocks = l.num_blocks;
+    d.kv_dtype = l.kv_dtype;
+    d.scale = l.scale;
+    d.out = l.out;
+    d.out_dtype = l.out_dtype;
+    d.workspace = static_cast<uint8_t*>(l.workspace) + l.plan.dec_offset;
+    d.plan = l.plan.dec;
+    d.q_start = l.q_start;
+    d.q_rows = l.T;
+    pa_status ds = launch_decode(d, stream);
+    if (ds != PA_OK) return ds;
+    if (l.max_q_len <= 1) return PA_OK;  // nothing left for the multi-token kernel
+  }
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(PA_ERR_CUDA, "pa_chunked_prefill: no CUDA device");

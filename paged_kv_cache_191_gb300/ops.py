@@ -74,6 +74,9 @@ SIGNATURES = {
     "pa_version": (_I32, []),
     "pa_cache_write": (C.c_int, [_P, _P, _I32, _P, _I64, _P, _P, _P, _P, C.POINTER(CacheDesc), _P]),
     "pa_decode_workspace_size": (C.c_size_t, [_I32, _I32, _I32, C.POINTER(CacheDesc), _I32]),
+    "pa_decode_plan_info": (C.c_int, [_I32, _I32, _I32, C.POINTER(CacheDesc), _I32, _I32P, _I32P, _I32P]),
+    "pa_chunked_prefill_plan_info": (C.c_int, [_I32, _I32, _I32, _I32, _I32, C.POINTER(CacheDesc), _I32,
+                                               _I32P, _I32P, _I32P, _I32P]),
     "pa_decode": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _F, _P, _I32,
                             C.POINTER(CacheDesc), _P, C.c_size_t, _I32, _P]),
     "pa_decode_append": (C.c_int, [_P, _P, _I32, _P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
@@ -202,6 +205,25 @@ def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None
     _check(lib().pa_cache_write(_ptr(k), _ptr(v), _TORCH_DT[k.dtype], _ptr(slot_mapping), T,
                                 _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                 C.byref(desc), _stream(stream)), "pa_cache_write")
+
+
+def decode_plan_info(B, num_q_heads, max_context_len, k_cache, split_tokens=0):
+    """(partitions, blocks per partition, kernels launched) of a decode call."""
+    desc = cache_desc(k_cache)
+    p, bpp, k = C.c_int32(), C.c_int32(), C.c_int32()
+    _check(lib().pa_decode_plan_info(B, num_q_heads, max_context_len, C.byref(desc), split_tokens, C.byref(p),
+                                     C.byref(bpp), C.byref(k)), "pa_decode_plan_info")
+    return p.value, bpp.value, k.value
+
+
+def chunked_prefill_plan_info(num_tokens, B, num_q_heads, max_q_len, max_context_len, k_cache, split_tokens=0):
+    """(tensor cores, partitions, blocks per partition, kernels launched) of a multi-token call."""
+    desc = cache_desc(k_cache)
+    tc, p, bpp, k = C.c_int32(), C.c_int32(), C.c_int32(), C.c_int32()
+    _check(lib().pa_chunked_prefill_plan_info(num_tokens, B, num_q_heads, max_q_len, max_context_len, C.byref(desc),
+                                              split_tokens, C.byref(tc), C.byref(p), C.byref(bpp), C.byref(k)),
+           "pa_chunked_prefill_plan_info")
+    return tc.value, p.value, bpp.value, k.value
 
 
 def decode_workspace_size(B, num_q_heads, max_context_len, k_cache, split_tokens=0):

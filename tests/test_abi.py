@@ -149,3 +149,31 @@ def test_chunked_prefill_scale_rules(palib):
     assert call(d8, ops.FP8_E4M3, FAKE, FAKE) == ops.PA_ERR_INVALID
     assert call(_desc(), ops.F16, FAKE, FAKE) == ops.PA_ERR_INVALID
     assert call(_desc(), ops.BF16, None, None) == ops.PA_ERR_INVALID
+
+
+def test_plan_info_counts_the_kernels_a_call_launches(palib):
+    """pa_decode_plan_info: one partition -> 1 kernel; up to 8 partitions ->
+    1 (the decode kernel merges them); more -> 2 (a merge kernel follows).
+    pa_chunked_prefill_plan_info over a 1-byte cache adds the decode
+    kernel's launches for the one-token sequences, and a call whose longest
+    query is one token launches only those."""
+    d = _desc()
+    assert ops.decode_plan_info(4, 4, 256, _torch_like(d), 256) == (1, 16, 1)
+    assert ops.decode_plan_info(4, 4, 2048, _torch_like(d), 256) == (8, 16, 1)
+    assert ops.decode_plan_info(4, 4, 4096, _torch_like(d), 256) == (16, 16, 2)
+    d8 = _desc(kv_dtype=ops.FP8_E4M3)
+    tc, parts, bpp, k = ops.chunked_prefill_plan_info(70, 8, 4, 40, 300, _torch_like(d8), 0)
+    assert tc == 0 and k == 1 + (1 if parts > 1 else 0) + ops.decode_plan_info(8, 4, 300, _torch_like(d8))[2]
+    assert ops.chunked_prefill_plan_info(8, 8, 4, 1, 300, _torch_like(d8), 0)[3] == \
+        ops.decode_plan_info(8, 4, 300, _torch_like(d8))[2]
+    # 16-bit caches: the multi-token kernel serves every sequence
+    tc, parts, bpp, k = ops.chunked_prefill_plan_info(70, 8, 4, 40, 300, _torch_like(d), 0)
+    assert k == 1 + (1 if parts > 1 else 0)
+
+
+def _torch_like(desc):
+    """A CPU tensor with the cache shape and dtype a desc describes (the plan
+    calls read only its shape and dtype)."""
+    import torch
+    dt = {ops.F16: torch.float16, ops.BF16: torch.bfloat16, ops.FP8_E4M3: torch.uint8, ops.INT8: torch.int8}
+    return torch.empty((desc.num_blocks, desc.num_kv_heads, desc.block_size, desc.head_dim), dtype=dt[desc.kv_dtype])

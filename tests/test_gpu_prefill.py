@@ -265,3 +265,18 @@ def test_quantised_16bit_output_and_stale_rows(fmt):
     out = gpu_prefill_q8(w, (kc, vc, ks, vs), out_dtype=torch.float16).float().numpy()
     err = np.abs(out - ref)
     assert np.all(err <= TOL[fmt] + half_ulp(ref, torch.float16)), float(np.nanmax(err))
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("q_lens,max_prior", [([1] * 6, 9000), ([1, 0, 40, 1, 1, 7], 6000), ([1, 1, 0, 1], 2500)])
+def test_quantised_one_token_rows(fmt, q_lens, max_prior):
+    """Over a 1-byte cache the one-token sequences of a call are served by the
+    decode kernel (its query / output row is q_start[b]) and the rest by the
+    multi-token kernel.  Decode-only batches, mixed batches with empty
+    sequences before the one-token rows, and contexts long enough for the
+    in-kernel merge (<= 8 partitions) and the merge kernel (more): every row
+    within the FP8 / INT8 tolerance of the oracle on the same stored codes."""
+    w = W.random_prefill_small(520 + len(q_lens) + max_prior, 16, 4, 128, "f16", q_lens, max_prior=max_prior)
+    pools = quantised_pools(w, fmt)
+    assert_close(gpu_prefill_q8(w, pools).numpy(), oracle_q8(w, pools), TOL[fmt],
+                 f"{fmt} q_lens {q_lens} prior <= {max_prior}")
