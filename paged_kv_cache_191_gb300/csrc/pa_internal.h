@@ -101,9 +101,9 @@ struct PrefillPlan {
 };
 // Whether pa_chunked_prefill runs its tcgen05 kernel (128-row tiles) for
 // this shape: head_dim 128 and more than 64 rows per (sequence, kv head).
+// 1-byte caches too: their codes are converted to 16-bit in shared memory.
 inline bool prefill_uses_tc(int32_t max_q_len, int32_t num_q_heads, const pa_cache_desc* d) {
-  return d->head_dim == 128 && !quantised(d->kv_dtype) &&
-         static_cast<int64_t>(max_q_len) * (num_q_heads / d->num_kv_heads) > 64;
+  return d->head_dim == 128 && static_cast<int64_t>(max_q_len) * (num_q_heads / d->num_kv_heads) > 64;
 }
 pa_status plan_prefill(int32_t num_tokens, int32_t B, int32_t num_q_heads, int32_t max_q_len,
                        int32_t max_context_len, const pa_cache_desc* desc, int32_t split_tokens,

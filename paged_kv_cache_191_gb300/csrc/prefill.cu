@@ -678,8 +678,10 @@ struct Smem {  // byte offsets from the 1024-aligned base
   static constexpr int V0 = K0 + kStages * 16384;              // V ring, same layout
   static constexpr int HALF = 16384;                           // one K or V chunk
   static constexpr int IDS = V0 + kStages * 16384;             // the partition's block ids [kMaxIds]
-  static constexpr int BAR = IDS + kMaxIds * 4;
-  static constexpr int NBAR = 4 * kStages + 8;
+  static constexpr int KSC = IDS + kMaxIds * 4;                 // 1-byte caches: K scales of 4 chunks [4][64]
+  static constexpr int VSC = KSC + 4 * 64 * 4;                  // and V scales [4][64] f32
+  static constexpr int BAR = VSC + 4 * 64 * 4;
+  static constexpr int NBAR = 6 * kStages + 8;
   static constexpr int TSLOT = BAR + NBAR * 8;
   static constexpr int SMEM = TSLOT + 16 + 1024;
 };
@@ -768,7 +770,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
 }
 }  // namespace tcg
 
-template <typename T>
+template <typename KT, typename T>
 __global__ void __launch_bounds__(tcg::kThreads, 2)
     prefill_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const PrefillArgs a) {
@@ -776,6 +778,7 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
   using L = Smem;
   constexpr int D = 128;
   constexpr bool SPLIT = std::is_same<T, __nv_bfloat16>::value;
+  constexpr bool Q8 = sizeof(KT) == 1;  // 1-byte codes (E4M3 / INT8) converted to T on the way in
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -821,6 +824,8 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
   auto pfull = [&](int i) { return bar + 8 * (4 * kStages + 3 + i); };  // P(c) in TMEM (over S(c))
   auto pfree = [&](int i) { return bar + 8 * (4 * kStages + 5 + i); };  // O += P(c) V(c) complete
   const uint32_t mdone = bar + 8 * (4 * kStages + 7);
+  auto kcode = [&](int s) { return bar + 8 * (4 * kStages + 8 + s); };            // 1-byte codes landed
+  auto vcode = [&](int s) { return bar + 8 * (5 * kStages + 8 + s); };
   auto kstage = [&](int s) { return base + L::K0 + s * L::HALF; };
   auto vstage = [&](int s) { return base + L::V0 + s * L::HALF; };
 
@@ -830,6 +835,8 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
       dev::mbar_init(kempty(s), 1);
       dev::mbar_init(vfull(s), 1);
       dev::mbar_init(vempty(s), 1);
+      dev::mbar_init(kcode(s), 1);
+      dev::mbar_init(vcode(s), 1);
     }
     dev::mbar_init(qfull, 4);
     for (int i = 0; i < 2; ++i) {
@@ -871,7 +878,100 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
       if (__any_sync(FULL, bad) && lane == 0) atomicOr(&g_prefill_err, PA_DEVERR_BLOCK_RANGE);
       __syncwarp();
     }
-    if (lane == 0) {
+    if constexpr (Q8) {
+      // 1-byte codes.  Lane 0 requests a chunk's codes (4 blocks of 16 rows x
+      // 128 B, 128-byte swizzled) into the upper half of a free stage; a K
+      // request also brings the chunk's 64 K and 64 V per-token scales into
+      // slot c % 4 of the scale rings.  When the codes have landed the warp
+      // reads them all, then rewrites the whole stage as T values (exact) in
+      // the layout the UMMA descriptors read, and arrives on the full barrier.
+      // A scale slot is reused by the K request of chunk c + 4, which waits
+      // for S(c + 2), which waits for the softmax of chunk c.
+      if (lane == 0) {
+        dev::prefetch_tensormap(&tmK);
+        dev::prefetch_tensormap(&tmV);
+      }
+      const int last = min(nb, kMaxIds) - 1;
+      auto request = [&](const CUtensorMap* m, uint32_t stage, uint32_t cb, int c, bool scales) {  // lane 0
+        dev::mbar_arrive_expect_tx(cb, 8192 + (scales ? 512 : 0));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int pb = ids[min(4 * c + k, last)];
+          dev::tma_load_3d(stage + 8192 + k * 2048, m, cb, 0, g * 16, pb);
+          if (scales) {
+            dev::bulk_load(base + L::KSC + (c & 3) * 256 + 64 * k, a.k_scale + static_cast<size_t>(pb) * 16, 64, cb);
+            dev::bulk_load(base + L::VSC + (c & 3) * 256 + 64 * k, a.v_scale + static_cast<size_t>(pb) * 16, 64, cb);
+          }
+        }
+      };
+      auto convert = [&](uint32_t stage) {  // every lane: 16 chunks of 16 codes
+        uint8_t* st = gb + (stage - base);
+        uint4 w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int i = lane + 32 * j, k = i >> 7, t = (i >> 3) & 15, c16 = i & 7;
+          w[j] = *reinterpret_cast<const uint4*>(st + 8192 + k * 2048 + t * 128 + ((c16 ^ (t & 7)) << 4));
+        }
+        __syncwarp();  // every code is in registers before the stage is rewritten
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int i = lane + 32 * j, k = i >> 7, t = (i >> 3) & 15, c16 = i & 7;
+          const int kr = 16 * k + t, cc = 2 * (c16 & 3);
+          uint32_t f[8];
+          dev::code8x4_to<KT, T>(w[j].x, f[0], f[1]);
+          dev::code8x4_to<KT, T>(w[j].y, f[2], f[3]);
+          dev::code8x4_to<KT, T>(w[j].z, f[4], f[5]);
+          dev::code8x4_to<KT, T>(w[j].w, f[6], f[7]);
+          uint8_t* row = st + (c16 >> 2) * 8192 + kr * 128;
+          *reinterpret_cast<uint4*>(row + ((cc ^ (kr & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+          *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (kr & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
+        }
+        dev::fence_proxy_async_smem();  // the rewritten stage is read by the tensor cores
+        __syncwarp();
+      };
+      int ik = 0, iv = 0, ck = 0, cv = 0;  // chunks requested (K, V), chunks converted (K, V)
+      bool ok = true;
+      uint64_t t0 = dev::global_timer_ns();
+      while (ok && cv < nc) {
+        int act = 0;
+        if (lane == 0) {
+          if (ik < nc && (ik < kStages || dev::mbar_test(kempty(ik % kStages), ((ik / kStages) - 1) & 1))) act |= 1;
+          if (iv < ik && (iv < kStages || dev::mbar_test(vempty(iv % kStages), ((iv / kStages) - 1) & 1))) act |= 2;
+          if (ck < ik && dev::mbar_test(kcode(ck % kStages), (ck / kStages) & 1)) act |= 4;
+          if (cv < ck && cv < iv && dev::mbar_test(vcode(cv % kStages), (cv / kStages) & 1)) act |= 8;
+        }
+        act = __shfl_sync(FULL, act, 0);
+        if (act & 1) {
+          if (lane == 0) request(&tmK, kstage(ik % kStages), kcode(ik % kStages), ik, true);
+          ++ik;
+        }
+        if (act & 2) {
+          if (lane == 0) request(&tmV, vstage(iv % kStages), vcode(iv % kStages), iv, false);
+          ++iv;
+        }
+        if (act & 4) {
+          convert(kstage(ck % kStages));
+          if (lane == 0) mbar_arrive(kfull(ck % kStages));
+          ++ck;
+        }
+        if (act & 8) {
+          convert(vstage(cv % kStages));
+          if (lane == 0) mbar_arrive(vfull(cv % kStages));
+          ++cv;
+        }
+        if (act) {
+          t0 = dev::global_timer_ns();
+        } else if (dev::global_timer_ns() - t0 > 2000000000ull) {
+          if (lane == 0) atomicOr(&g_prefill_err, PA_DEVERR_TIMEOUT);
+          ok = false;
+        }
+      }
+      // no copy may still be landing when the CTA exits
+      if (lane == 0) {
+        for (int i = ck; i < ik; ++i) dev::mbar_wait_bounded(kcode(i % kStages), (i / kStages) & 1, 100000000ull);
+        for (int i = cv; i < iv; ++i) dev::mbar_wait_bounded(vcode(i % kStages), (i / kStages) & 1, 100000000ull);
+      }
+    } else if (lane == 0) {
       dev::prefetch_tensormap(&tmK);
       dev::prefetch_tensormap(&tmV);
       const int last = min(nb, kMaxIds) - 1;
@@ -1028,17 +1128,24 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
       // raw scores; the scale (> 0) is applied to the max and folded into
       // the exponent's FFMA below
       const int key0 = (j0 + 4 * c) * 16;
+      // 1-byte caches: the chunk's per-token K and V scales (slot c % 4)
+      const float* ksc = reinterpret_cast<const float*>(gb + L::KSC + (c & 3) * 256);
+      const float* vsc = reinterpret_cast<const float*>(gb + L::VSC + (c & 3) * 256);
       float cm[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) cm[k] = -INFINITY;
       if (key0 + kKeys - 1 <= pos && key0 + kKeys <= kend) {  // every key of the chunk is visible
 #pragma unroll
-        for (int j = 0; j < kKeys; ++j) cm[j & 7] = fmaxf(cm[j & 7], x[j]);
+        for (int j = 0; j < kKeys; ++j) {
+          if constexpr (Q8) x[j] *= ksc[j];
+          cm[j & 7] = fmaxf(cm[j & 7], x[j]);
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < kKeys; ++j) {
           const int t = key0 + j;
-          x[j] = (t <= pos && t < kend) ? x[j] : -INFINITY;
+          // a masked key's stale scale may be NaN: it never multiplies
+          x[j] = (t <= pos && t < kend) ? (Q8 ? x[j] * ksc[j] : x[j]) : -INFINITY;
           cm[j & 7] = fmaxf(cm[j & 7], x[j]);
         }
       }
@@ -1078,13 +1185,25 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
       for (int j = 0; j < kKeys; j += 2) {
         const float p0 = ex2(fmaf(x[j], sl2, nref));
         const float p1 = ex2(fmaf(x[j + 1], sl2, nref));
-        hi[j >> 1] = dev::pack2<T>(p0, p1);
-        const float2 h = dev::unpack2<T>(hi[j >> 1]);
-        if constexpr (SPLIT) {
-          lo[j >> 1] = dev::pack2<T>(p0 - h.x, p1 - h.y);
+        if constexpr (Q8) {
+          // the product takes p * v_scale (the V codes carry no scale); l sums p.
+          // A masked key has p = 0 exactly and a possibly stale (NaN) scale.
+          const float q0 = p0 == 0.f ? 0.f : p0 * vsc[j], q1 = p1 == 0.f ? 0.f : p1 * vsc[j + 1];
+          hi[j >> 1] = dev::pack2<T>(q0, q1);
+          if constexpr (SPLIT) {
+            const float2 h = dev::unpack2<T>(hi[j >> 1]);
+            lo[j >> 1] = dev::pack2<T>(q0 - h.x, q1 - h.y);
+          }
           ls[(j >> 1) & 7] += p0 + p1;
         } else {
-          ls[(j >> 1) & 7] += h.x + h.y;  // normalise with the rounded weights the product uses
+          hi[j >> 1] = dev::pack2<T>(p0, p1);
+          const float2 h = dev::unpack2<T>(hi[j >> 1]);
+          if constexpr (SPLIT) {
+            lo[j >> 1] = dev::pack2<T>(p0 - h.x, p1 - h.y);
+            ls[(j >> 1) & 7] += p0 + p1;
+          } else {
+            ls[(j >> 1) & 7] += h.x + h.y;  // normalise with the rounded weights the product uses
+          }
         }
       }
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
@@ -1142,9 +1261,9 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
 template <typename KT, typename T, int D>
 pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t stream) {
   using TL = PTile<KT, D>;
-  constexpr bool SAME = std::is_same<KT, T>::value;  // 16-bit cache read as the query type
-  // tcgen05 kernel (128-row tiles) or mma.sync kernel (64-row tiles), as planned
-  const bool TC = SAME && D == 128 && l.plan.tc;
+  // tcgen05 kernel (128-row tiles; 1-byte codes converted to T in shared
+  // memory) or mma.sync kernel (64-row tiles), as planned
+  const bool TC = D == 128 && l.plan.tc;
   constexpr int EB = static_cast<int>(sizeof(KT));
   CUtensorMap tmK, tmV;
   pa_status st = make_kv_map(&tmK, l.k_cache, l.Hkv, l.num_blocks, TL::ROWB, EB, dt, "pa_chunked_prefill", !TC);
@@ -1221,9 +1340,9 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
   std::call_once(once[dev], [dev] {
     cudaError_t e =
         cudaFuncSetAttribute(prefill_main<KT, T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, TL::SMEM);
-    if constexpr (SAME && D == 128)
+    if constexpr (D == 128)
       if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(prefill_tc<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, TS::SMEM);
+        e = cudaFuncSetAttribute(prefill_tc<KT, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, TS::SMEM);
     setup_err[dev] = e;
   });
   if (setup_err[dev] != cudaSuccess)
@@ -1231,9 +1350,9 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
 
   const dim3 grid(static_cast<unsigned>(l.B * l.Hkv * l.plan.row_tiles), static_cast<unsigned>(l.plan.max_parts));
   cudaError_t e;
-  if constexpr (SAME && D == 128) {
+  if constexpr (D == 128) {
     if (TC)
-      e = launch_dependent(prefill_tc<T>, grid, dim3(tcg::kThreads), TS::SMEM, stream, tmK, tmV, a);
+      e = launch_dependent(prefill_tc<KT, T>, grid, dim3(tcg::kThreads), TS::SMEM, stream, tmK, tmV, a);
     else
       e = launch_dependent(prefill_main<KT, T, D>, grid, dim3(kThreads), TL::SMEM, stream, tmK, tmV, a);
   } else {
