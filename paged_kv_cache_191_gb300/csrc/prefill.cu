@@ -858,6 +858,35 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
   fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + L::TSLOT);
 
+  // 1-byte codes -> T in place: the codes of a chunk (upper half of its
+  // stage, 4 blocks of 16 rows x 128 B, 128-byte swizzled) are read into
+  // registers by the whole warp, then the stage is rewritten as 16-bit values
+  // (exact) in the 128-byte-swizzled K-major layout the UMMA descriptors read.
+  auto convert = [&](uint32_t stage) {  // every lane: 16 chunks of 16 codes
+    uint8_t* st = gb + (stage - base);
+    uint4 w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int i = lane + 32 * j, k = i >> 7, t = (i >> 3) & 15, c16 = i & 7;
+      w[j] = *reinterpret_cast<const uint4*>(st + 8192 + k * 2048 + t * 128 + ((c16 ^ (t & 7)) << 4));
+    }
+    __syncwarp();  // every code is in registers before the stage is rewritten
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int i = lane + 32 * j, k = i >> 7, t = (i >> 3) & 15, c16 = i & 7;
+      const int kr = 16 * k + t, cc = 2 * (c16 & 3);
+      uint32_t f[8];
+      dev::code8x4_to<KT, T>(w[j].x, f[0], f[1]);
+      dev::code8x4_to<KT, T>(w[j].y, f[2], f[3]);
+      dev::code8x4_to<KT, T>(w[j].z, f[4], f[5]);
+      dev::code8x4_to<KT, T>(w[j].w, f[6], f[7]);
+      uint8_t* row = st + (c16 >> 2) * 8192 + kr * 128;
+      *reinterpret_cast<uint4*>(row + ((cc ^ (kr & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (kr & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
+    }
+    dev::fence_proxy_async_smem();  // the rewritten stage is read by the tensor cores
+    __syncwarp();
+  };
   if (wid == 0) {
     // ---- producer: the warp stages the partition's block ids in shared memory
     // (coalesced, checked), then lane 0 polls both rings and issues whichever
@@ -879,14 +908,13 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
       __syncwarp();
     }
     if constexpr (Q8) {
-      // 1-byte codes.  Lane 0 requests a chunk's codes (4 blocks of 16 rows x
-      // 128 B, 128-byte swizzled) into the upper half of a free stage; a K
-      // request also brings the chunk's 64 K and 64 V per-token scales into
-      // slot c % 4 of the scale rings.  When the codes have landed the warp
-      // reads them all, then rewrites the whole stage as T values (exact) in
-      // the layout the UMMA descriptors read, and arrives on the full barrier.
-      // A scale slot is reused by the K request of chunk c + 4, which waits
-      // for S(c + 2), which waits for the softmax of chunk c.
+      // 1-byte codes.  Lane 0 requests a chunk's codes into the upper half of
+      // a free stage; a K request also brings the chunk's 64 K and 64 V
+      // per-token scales into slot c % 4 of the scale rings.  When a K chunk's
+      // codes have landed the warp converts it and arrives on the full
+      // barrier; V chunks are converted by the MMA warp just before their
+      // product.  A scale slot is reused by the K request of chunk c + 4,
+      // which waits for S(c + 2), which waits for the softmax of chunk c.
       if (lane == 0) {
         dev::prefetch_tensormap(&tmK);
         dev::prefetch_tensormap(&tmV);
@@ -904,41 +932,15 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
           }
         }
       };
-      auto convert = [&](uint32_t stage) {  // every lane: 16 chunks of 16 codes
-        uint8_t* st = gb + (stage - base);
-        uint4 w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int i = lane + 32 * j, k = i >> 7, t = (i >> 3) & 15, c16 = i & 7;
-          w[j] = *reinterpret_cast<const uint4*>(st + 8192 + k * 2048 + t * 128 + ((c16 ^ (t & 7)) << 4));
-        }
-        __syncwarp();  // every code is in registers before the stage is rewritten
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int i = lane + 32 * j, k = i >> 7, t = (i >> 3) & 15, c16 = i & 7;
-          const int kr = 16 * k + t, cc = 2 * (c16 & 3);
-          uint32_t f[8];
-          dev::code8x4_to<KT, T>(w[j].x, f[0], f[1]);
-          dev::code8x4_to<KT, T>(w[j].y, f[2], f[3]);
-          dev::code8x4_to<KT, T>(w[j].z, f[4], f[5]);
-          dev::code8x4_to<KT, T>(w[j].w, f[6], f[7]);
-          uint8_t* row = st + (c16 >> 2) * 8192 + kr * 128;
-          *reinterpret_cast<uint4*>(row + ((cc ^ (kr & 7)) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
-          *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (kr & 7)) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
-        }
-        dev::fence_proxy_async_smem();  // the rewritten stage is read by the tensor cores
-        __syncwarp();
-      };
-      int ik = 0, iv = 0, ck = 0, cv = 0;  // chunks requested (K, V), chunks converted (K, V)
+      int ik = 0, iv = 0, ck = 0;  // chunks requested (K, V), K chunks converted
       bool ok = true;
       uint64_t t0 = dev::global_timer_ns();
-      while (ok && cv < nc) {
+      while (ok && (iv < nc || ck < nc)) {
         int act = 0;
         if (lane == 0) {
           if (ik < nc && (ik < kStages || dev::mbar_test(kempty(ik % kStages), ((ik / kStages) - 1) & 1))) act |= 1;
           if (iv < ik && (iv < kStages || dev::mbar_test(vempty(iv % kStages), ((iv / kStages) - 1) & 1))) act |= 2;
           if (ck < ik && dev::mbar_test(kcode(ck % kStages), (ck / kStages) & 1)) act |= 4;
-          if (cv < ck && cv < iv && dev::mbar_test(vcode(cv % kStages), (cv / kStages) & 1)) act |= 8;
         }
         act = __shfl_sync(FULL, act, 0);
         if (act & 1) {
@@ -954,11 +956,6 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
           if (lane == 0) mbar_arrive(kfull(ck % kStages));
           ++ck;
         }
-        if (act & 8) {
-          convert(vstage(cv % kStages));
-          if (lane == 0) mbar_arrive(vfull(cv % kStages));
-          ++cv;
-        }
         if (act) {
           t0 = dev::global_timer_ns();
         } else if (dev::global_timer_ns() - t0 > 2000000000ull) {
@@ -966,10 +963,12 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
           ok = false;
         }
       }
-      // no copy may still be landing when the CTA exits
+      // no copy may still be landing when the CTA exits (the last V chunks'
+      // phases have normally completed already: the MMA warp waited for them)
       if (lane == 0) {
         for (int i = ck; i < ik; ++i) dev::mbar_wait_bounded(kcode(i % kStages), (i / kStages) & 1, 100000000ull);
-        for (int i = cv; i < iv; ++i) dev::mbar_wait_bounded(vcode(i % kStages), (i / kStages) & 1, 100000000ull);
+        for (int i = max(0, iv - kStages); i < iv; ++i)
+          dev::mbar_wait_bounded(vcode(i % kStages), (i / kStages) & 1, 100000000ull);
       }
     } else if (lane == 0) {
       dev::prefetch_tensormap(&tmK);
@@ -1047,11 +1046,14 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
       }
       go = 0;
       if (lane == 0 && cp < cs && dev::mbar_test(pfull(cp & 1), (cp >> 1) & 1) &&
-          dev::mbar_test(vfull(cp % kStages), (cp / kStages) & 1))
+          dev::mbar_test(Q8 ? vcode(cp % kStages) : vfull(cp % kStages), (cp / kStages) & 1))
         go = 1;
       if (__shfl_sync(FULL, go, 0)) {
         fence_after();
         const int sv_ = cp % kStages;
+        // 1-byte codes: V(cp) -> 16-bit in place, here (converting earlier
+        // delays the S products that keep the tensor pipe busy)
+        if constexpr (Q8) convert(vstage(sv_));
         const int key0 = (j0 + 4 * cp) * 16;
         const int first_bad = max(0, min(kKeys, kend - key0));  // V rows from here on are zeroed
         if (first_bad < kKeys) {
