@@ -175,12 +175,16 @@ pa_status pa_decode_plan_info(int32_t B, int32_t num_q_heads, int32_t max_contex
  *              to let the library choose from the shape and the SM count.
  *
  * Work: one CTA per (sequence, kv head, partition); all G query heads of a
- * kv head share every K/V tile load; partitions are merged by a second
- * kernel when more than one exists.
+ * kv head share every K/V tile load.  When a context splits into at most 8
+ * partitions, the last partition of each (sequence, kv head) to finish
+ * merges them inside the same kernel (arrival counters in the workspace,
+ * stamped per launch, so their prior contents never matter); longer splits
+ * are merged by a second kernel.  pa_decode_plan_info reports the split.
  *
- * Determinism: work is mapped statically and no atomic operation enters the
- * arithmetic, so the same inputs, shape and split_tokens give bit-identical
- * outputs on every run, whatever the physical block ids the tables name.
+ * Determinism: work is mapped statically; the arrival counter only decides
+ * which CTA merges, and the merge sums the partitions in a fixed order, so
+ * the same inputs, shape and split_tokens give bit-identical outputs on
+ * every run, whatever the physical block ids the tables name.
  */
 pa_status pa_decode(const void* q, int32_t q_dtype,
                     const void* k_cache, const void* v_cache,
@@ -275,7 +279,8 @@ pa_status pa_decode_append_grouped(const void* k_new, const void* v_new, int32_t
 /*
  * pa_chunked_prefill_workspace_size -- bytes of device workspace
  * pa_chunked_prefill needs for the same arguments; 0 when one partition
- * covers max_context_len (or on an invalid argument).
+ * covers max_context_len and nothing goes to the decode kernel (or on an
+ * invalid argument).
  */
 size_t pa_chunked_prefill_workspace_size(int32_t num_tokens, int32_t B, int32_t num_q_heads,
                                          int32_t max_q_len, int32_t max_context_len,
@@ -332,8 +337,14 @@ pa_status pa_chunked_prefill_plan_info(int32_t num_tokens, int32_t B, int32_t nu
  * Work: one CTA per (sequence, kv head, 64-row tile of (token, head) rows,
  * partition); K/V tiles of a partition are loaded once per CTA by TMA and
  * shared by its four compute warps; partitions are merged by a second
- * kernel when a row's keys span more than one.  16-bit caches at head_dim
- * 128 with more than 64 rows per kv head use 128-row tiles on tcgen05.
+ * kernel when a row's keys span more than one.  At head_dim 128 with more
+ * than 64 rows per kv head the tiles are 128 rows on tcgen05 (FP8 / INT8
+ * codes are converted to 16-bit in shared memory on the way to the tensor
+ * cores).  Over an FP8 / INT8 cache the sequences with one query token (the
+ * decode steps riding in the call) are served first by the decode kernel,
+ * whose workspace follows the multi-token kernel's; a call whose max_q_len
+ * is 1 launches only the decode kernel.  pa_chunked_prefill_plan_info
+ * reports what a call launches.
  */
 pa_status pa_chunked_prefill(const void* q, int32_t q_dtype, const int32_t* q_start,
                              int32_t num_tokens, int32_t max_q_len,

@@ -25,10 +25,11 @@
 //   after cudaDeviceReset -- looks it up again, so a stale address is never
 //   launched.  Make the first call in a context before any stream capture.
 // - Sharing: every call in a context uses the same array and it keeps the
-//   last call's contents.  Nothing in it needs clearing (every partial a call
-//   reads was written earlier in the same call), but two calls whose kernels
-//   overlap on the GPU race on it: serialise such calls (one stream, or
-//   events).
+//   last call's contents.  Nothing in it needs clearing: every partial a call
+//   reads was written earlier in the same call, and the split-K arrival
+//   counters count only arrivals tagged with the call's own epoch, so leftover
+//   bytes read as no arrivals.  Two calls whose kernels overlap on the GPU
+//   race on it: serialise such calls (one stream, or events).
 #include <cudaTypedefs.h>
 
 #include <mutex>

@@ -162,8 +162,13 @@ def test_plan_info_counts_the_kernels_a_call_launches(palib):
     assert ops.decode_plan_info(4, 4, 2048, _torch_like(d), 256) == (8, 16, 1)
     assert ops.decode_plan_info(4, 4, 4096, _torch_like(d), 256) == (16, 16, 2)
     d8 = _desc(kv_dtype=ops.FP8_E4M3)
+    dec8 = ops.decode_plan_info(8, 4, 300, _torch_like(d8))[2]
+    # 40 tokens x 2 heads per kv head = 80 rows: the tcgen05 kernel (128-row tiles)
     tc, parts, bpp, k = ops.chunked_prefill_plan_info(70, 8, 4, 40, 300, _torch_like(d8), 0)
-    assert tc == 0 and k == 1 + (1 if parts > 1 else 0) + ops.decode_plan_info(8, 4, 300, _torch_like(d8))[2]
+    assert tc == 1 and k == 1 + (1 if parts > 1 else 0) + dec8
+    # 30 x 2 = 60 rows: the 64-row kernel
+    tc, parts, bpp, k = ops.chunked_prefill_plan_info(60, 8, 4, 30, 300, _torch_like(d8), 0)
+    assert tc == 0 and k == 1 + (1 if parts > 1 else 0) + dec8
     assert ops.chunked_prefill_plan_info(8, 8, 4, 1, 300, _torch_like(d8), 0)[3] == \
         ops.decode_plan_info(8, 4, 300, _torch_like(d8))[2]
     # 16-bit caches: the multi-token kernel serves every sequence
