@@ -278,9 +278,11 @@ pa_status pa_decode_append_grouped(const void* k_new, const void* v_new, int32_t
 
 /*
  * pa_chunked_prefill_workspace_size -- bytes of device workspace
- * pa_chunked_prefill needs for the same arguments; 0 when one partition
- * covers max_context_len and nothing goes to the decode kernel (or on an
- * invalid argument).
+ * pa_chunked_prefill needs for the same arguments, and for a call with a
+ * smaller max_q_len that the decode kernel serves (its split-K partials grow
+ * with B * max_q_len rather than num_tokens); 0 when one partition covers
+ * max_context_len and nothing goes to the decode kernel (or on an invalid
+ * argument).
  */
 size_t pa_chunked_prefill_workspace_size(int32_t num_tokens, int32_t B, int32_t num_q_heads,
                                          int32_t max_q_len, int32_t max_context_len,
@@ -343,8 +345,12 @@ pa_status pa_chunked_prefill_plan_info(int32_t num_tokens, int32_t B, int32_t nu
  * cores).  Over an FP8 / INT8 cache the sequences with one query token (the
  * decode steps riding in the call) are served first by the decode kernel,
  * whose workspace follows the multi-token kernel's; a call whose max_q_len
- * is 1 launches only the decode kernel.  pa_chunked_prefill_plan_info
- * reports what a call launches.
+ * is 1 launches only the decode kernel.  Over a 16-bit cache a call with
+ * max_q_len <= 8 and max_q_len * num_q_heads / num_kv_heads <= 32 runs
+ * entirely in the decode kernel, one CTA per (sequence, kv head, query
+ * token, partition), the columns of one (sequence, kv head) neighbours so
+ * that their K/V reads meet in L2; malformed sequences are flagged as
+ * above.  pa_chunked_prefill_plan_info reports what a call launches.
  */
 pa_status pa_chunked_prefill(const void* q, int32_t q_dtype, const int32_t* q_start,
                              int32_t num_tokens, int32_t max_q_len,

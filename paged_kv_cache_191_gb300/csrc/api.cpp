@@ -13,6 +13,12 @@
 #ifndef PA_FUSED_MERGE
 #define PA_FUSED_MERGE 1  // split-K partials merged by the decode kernel's last partition
 #endif
+#ifndef PA_FUSED_MERGE_MAX
+#define PA_FUSED_MERGE_MAX 8  // most partitions merged that way
+#endif
+#ifndef PA_Q8_WARPS
+#define PA_Q8_WARPS 4  // warps sharing one partition over a 1-byte cache
+#endif
 
 namespace pa {
 
@@ -75,7 +81,7 @@ pa_status plan_decode(int32_t B, int32_t Hq, int32_t max_context_len, const pa_c
   // 1-byte codes cost more register-side work per byte (exact conversion of
   // the codes), so four warps share a partition there; 16-bit caches keep
   // one warp per partition (measured best for both).
-  plan->item_warps = quantised(d->kv_dtype) ? 4 : 1;
+  plan->item_warps = quantised(d->kv_dtype) ? PA_Q8_WARPS : 1;
   if (parts > 1) {
     const size_t rows = static_cast<size_t>(B) * Hq * parts;
     size_t bytes = rows * d->head_dim * sizeof(float) + 2 * rows * sizeof(float);
@@ -89,7 +95,7 @@ pa_status plan_decode(int32_t B, int32_t Hq, int32_t max_context_len, const pa_c
   // Longer merges go to the merge kernel, which spreads them over a warp per
   // query head.
   plan->ticket_offset = 0;
-  if (PA_FUSED_MERGE && parts > 1 && parts <= 8) {
+  if (PA_FUSED_MERGE && parts > 1 && parts <= PA_FUSED_MERGE_MAX) {
     plan->ticket_offset = plan->workspace_bytes;
     const size_t tickets = static_cast<size_t>(B) * d->num_kv_heads * 8;
     plan->workspace_bytes += (tickets + 255) & ~static_cast<size_t>(255);
@@ -97,10 +103,45 @@ pa_status plan_decode(int32_t B, int32_t Hq, int32_t max_context_len, const pa_c
   return PA_OK;
 }
 
+bool prefill_routes_short(int32_t max_q_len, int32_t Hq, const pa_cache_desc* d) {
+  const int64_t G = Hq / d->num_kv_heads;
+  return !quantised(d->kv_dtype) && max_q_len >= 1 && max_q_len <= kShortTokens && max_q_len * G <= 32;
+}
+
 pa_status plan_prefill(int32_t T, int32_t B, int32_t Hq, int32_t max_q_len, int32_t max_context_len,
                        const pa_cache_desc* d, int32_t split_tokens, PrefillPlan* plan) {
   const int64_t G = Hq / d->num_kv_heads;
   const int64_t nblk_max = max_context_len <= 0 ? 1 : (max_context_len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+  if (split_tokens > 0 && (split_tokens % PA_BLOCK_SIZE || split_tokens > 4096))
+    return fail(PA_ERR_INVALID, "split_tokens must be a multiple of 16 in [16, 4096]");
+  // the decode kernel's partitions: the call's split up to 1024 tokens, else
+  // the library's choice
+  const int32_t dsplit = split_tokens > 0 ? std::min<int32_t>(split_tokens, 1024) : 0;
+  // Short queries over a 16-bit cache -- decode steps sent through this
+  // call, a speculative verification of one or two draft tokens -- would
+  // leave most of a 64-row tile empty.  The decode kernel serves them
+  // instead: one grid column per (sequence, kv head, query token), the G
+  // heads of the token as MMA columns, the columns of one (sequence, kv
+  // head) side by side so that their reads of the same K/V tiles meet in L2.
+  // Each column streams the tiles again from L2, so the route pays only up
+  // to half a tile of rows (32): at 5 tokens x 8 heads the 64-row kernel is
+  // as fast, and over 1-byte caches, where every column would convert the
+  // codes again, it is faster.
+  if (prefill_routes_short(max_q_len, Hq, d)) {
+    if (static_cast<int64_t>(B) * max_q_len * d->num_kv_heads > INT32_MAX)
+      return fail(PA_ERR_UNSUPPORTED, "too many query rows for one grid");
+    pa_status st = plan_decode(B * max_q_len, Hq, max_context_len, d, dsplit, &plan->dec);
+    if (st != PA_OK) return st;
+    plan->route_short = 1;
+    plan->route_single = 0;
+    plan->tc = 0;
+    plan->row_tiles = 1;
+    plan->blocks_per_part = plan->dec.blocks_per_part;
+    plan->max_parts = plan->dec.max_parts;
+    plan->workspace_bytes = plan->dec.workspace_bytes;
+    plan->dec_offset = 0;
+    return PA_OK;
+  }
   // Rows of one (sequence, kv head) are (query token, head of the group)
   // pairs.  More than 64 of them at head_dim 128 run the tcgen05 kernel
   // (128-row tiles); otherwise the mma.sync kernel (64-row tiles) wastes less
@@ -109,8 +150,6 @@ pa_status plan_prefill(int32_t T, int32_t B, int32_t Hq, int32_t max_q_len, int3
   const int64_t tiles = max_q_len <= 0 ? 1 : (static_cast<int64_t>(max_q_len) * G + tile_rows - 1) / tile_rows;
   int64_t bpp;
   if (split_tokens > 0) {
-    if (split_tokens % PA_BLOCK_SIZE || split_tokens > 4096)
-      return fail(PA_ERR_INVALID, "split_tokens must be a multiple of 16 in [16, 4096]");
     bpp = split_tokens / PA_BLOCK_SIZE;
   } else {
     // Row tiles that can hold rows: at most one partial tile per sequence
@@ -153,7 +192,7 @@ pa_status plan_prefill(int32_t T, int32_t B, int32_t Hq, int32_t max_q_len, int3
   plan->route_single = quantised(d->kv_dtype) ? 1 : 0;
   plan->dec_offset = plan->workspace_bytes;
   if (plan->route_single) {
-    pa_status st = plan_decode(B, Hq, max_context_len, d, 0, &plan->dec);
+    pa_status st = plan_decode(B, Hq, max_context_len, d, dsplit, &plan->dec);
     if (st != PA_OK) return st;
     plan->workspace_bytes += plan->dec.workspace_bytes;
   }
@@ -453,8 +492,12 @@ pa_status pa_chunked_prefill_plan_info(int32_t num_tokens, int32_t B, int32_t nu
   if (partitions) *partitions = plan.max_parts;
   if (blocks_per_partition) *blocks_per_partition = plan.blocks_per_part;
   if (kernels) {
-    const int32_t multi = max_q_len > 1 || !plan.route_single ? 1 + (plan.max_parts > 1 ? 1 : 0) : 0;
-    *kernels = multi + (plan.route_single ? decode_kernels(plan.dec) : 0);
+    if (plan.route_short) {
+      *kernels = decode_kernels(plan.dec);
+    } else {
+      const int32_t multi = max_q_len > 1 || !plan.route_single ? 1 + (plan.max_parts > 1 ? 1 : 0) : 0;
+      *kernels = multi + (plan.route_single ? decode_kernels(plan.dec) : 0);
+    }
   }
   return PA_OK;
 }
@@ -467,7 +510,17 @@ size_t pa_chunked_prefill_workspace_size(int32_t num_tokens, int32_t B, int32_t 
   if (pa::plan_prefill(num_tokens, B, num_q_heads, max_q_len, max_context_len, desc, split_tokens, &plan) !=
       PA_OK)
     return 0;
-  return plan.workspace_bytes;
+  // A call with fewer query tokens per sequence may take the decode route,
+  // whose workspace grows with B x tokens instead of num_tokens: cover those
+  // plans too, so the size holds for every call up to these bounds.
+  size_t bytes = plan.workspace_bytes;
+  for (int32_t q = 1; q < max_q_len && q <= pa::kShortTokens; ++q) {
+    if (!pa::prefill_routes_short(q, num_q_heads, desc)) continue;
+    pa::PrefillPlan p2;
+    if (pa::plan_prefill(num_tokens, B, num_q_heads, q, max_context_len, desc, split_tokens, &p2) == PA_OK)
+      bytes = std::max(bytes, p2.workspace_bytes);
+  }
+  return bytes;
 }
 
 pa_status pa_chunked_prefill(const void* q, int32_t q_dtype, const int32_t* q_start, int32_t num_tokens,

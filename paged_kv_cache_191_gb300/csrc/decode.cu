@@ -103,11 +103,15 @@ struct DecodeArgs {
   // kv head), stamped with this launch's epoch
   unsigned long long* tickets;
   uint32_t epoch;
-  // the one-token sequences of a multi-token call (else null): sequence b's
-  // query and output row is q_start[b] of q_rows; sequences with another
-  // number of query tokens are left to the multi-token kernel
+  // rows of a multi-token call (else null): sequence b brings the n_b =
+  // q_start[b+1] - q_start[b] query tokens q_start[b] .. of q_rows, the last
+  // n_b of its context; token t attends causally to the first L_b - n_b + 1 + t
+  // keys and is served by the grid column (b, g, t), t < q_tokens.  Sequences
+  // with n_b > q_tokens are left to the multi-token kernel (with q_tokens = 1,
+  // the one-token sequences only), unless q_report: then the decode kernel
+  // serves the whole call and flags them as the multi-token kernel would.
   const int32_t* q_start;
-  int32_t q_rows;
+  int32_t q_rows, q_tokens, q_report;
 };
 
 // A group's usable shared prefix: whole blocks every member has before the
@@ -370,6 +374,7 @@ __global__ void __launch_bounds__(32 * W)
   int b, g, p;       // table owner (and fused-write sequence), kv head, partition of its rows
   int seq0, ncols;   // query columns
   int qb = -1;       // query / output row of sequence seq0 (seq0 unless the call maps rows)
+  int pseq;          // row base of this item's split-K partials and arrival counter
   int j0, L, nb;     // first block, owner's length, blocks of this item
   bool direct;       // one partition covers the rows: write the output itself
   bool write_new;    // this item reads the owner's last block (fused write)
@@ -406,10 +411,15 @@ __global__ void __launch_bounds__(32 * W)
   // write): everything below may read what it wrote.
   dev::grid_dependency_wait();
   if (a.n_groups == 0) {
-    b = blockIdx.x / a.Hkv;
-    g = blockIdx.x - b * a.Hkv;
+    // grid column (b, g, t): the q_tokens query tokens of (b, g) are
+    // neighbours, so their reads of the same K/V tiles meet in L2
+    const int tq = a.q_tokens;
+    const int bg = static_cast<int>(blockIdx.x) / tq, t = static_cast<int>(blockIdx.x) - bg * tq;
+    b = bg / a.Hkv;
+    g = bg - b * a.Hkv;
     p = PA_P_ASC ? static_cast<int>(blockIdx.y) : static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
     seq0 = b;
+    pseq = b;
     ncols = a.G;
     j0 = p * a.bpp;
     // The length, this partition's block ids (one or two per lane, read up to
@@ -419,13 +429,26 @@ __global__ void __launch_bounds__(32 * W)
     const int row_left = a.max_blocks - j0;
     t0 = (lane < a.bpp && lane < row_left) ? row[lane] : 0;
     t1 = (lane + 32 < a.bpp && lane + 32 < row_left) ? row[lane + 32] : 0;
-    if (a.q_start) {  // one-token rows of a multi-token call only
-      const int s0 = a.q_start[b], s1 = a.q_start[b + 1];
-      if (s1 - s0 != 1 || s0 < 0 || s1 > a.q_rows) return;
-      qb = s0;
+    const bool report = lane == 0 && g == 0 && p == 0 && t == 0;
+    int n = 1;
+    if (a.q_start) {  // rows of a multi-token call
+      const int s0 = a.q_start[b];
+      n = a.q_start[b + 1] - s0;
+      if (s0 < 0 || n < 0 || n > tq || s0 > a.q_rows - n) {
+        if (a.q_report && report) atomicOr(&g_decode_err, PA_DEVERR_QUERY_RANGE);
+        return;
+      }
+      if (t >= n) return;
+      qb = s0 + t;
+      pseq = b * tq + t;
     }
     load_q();
-    L = checked_len(a, b, lane == 0 && p == 0);
+    L = checked_len(a, b, lane == 0 && p == 0 && t == 0);
+    if (a.q_start) {
+      // more query tokens than context: the early tokens have no keys
+      if (n > L && a.q_report && report) atomicOr(&g_decode_err, PA_DEVERR_CONTEXT_LEN);
+      L = max(0, L - n + 1 + t);  // causal: the keys up to this token's position
+    }
     const int nblk = (L + 15) >> 4;
     if (j0 >= nblk) {
       if (p == 0) zero_rows(b);
@@ -452,6 +475,7 @@ __global__ void __launch_bounds__(32 * W)
       nb = min(a.bpp, E - j0);
       b = gs0;
       seq0 = gs0;
+      pseq = gs0;
       ncols = members * a.G;
       L = __shfl_sync(FULL, Lm, 0);
       direct = false;
@@ -473,6 +497,7 @@ __global__ void __launch_bounds__(32 * W)
       if (m >= members) return;
       b = gs0 + m;
       seq0 = b;
+      pseq = b;
       ncols = a.G;
       L = __shfl_sync(FULL, Lm, m);
       const int nblk = (L + 15) >> 4, pp = (E + a.bpp - 1) / a.bpp;
@@ -492,7 +517,7 @@ __global__ void __launch_bounds__(32 * W)
     }
   }
   // output rows are query rows: shifted when the call maps sequences to rows
-  const int64_t oshift = qb >= 0 ? static_cast<int64_t>(qb - seq0) * a.Hq * D : 0;
+  const int64_t oshift = qb >= 0 ? static_cast<int64_t>(qb - pseq) * a.Hq * D : 0;
   const bool bad = (lane < nb && (t0 < 0 || t0 >= a.num_blocks)) ||
                    (lane + 32 < nb && (t1 < 0 || t1 >= a.num_blocks));
   if (bad) {
@@ -802,7 +827,7 @@ __global__ void __launch_bounds__(32 * W)
         acc += f * ov[h * D + d];
         ls += f * ov[8 * D + 8 + h];
       }
-      const size_t head = static_cast<size_t>(seq0 + h / a.G) * a.Hq + g * a.G + h % a.G;
+      const size_t head = static_cast<size_t>(pseq + h / a.G) * a.Hq + g * a.G + h % a.G;
       if (direct) {
         store_out<QT>(a, static_cast<size_t>(static_cast<int64_t>(head * D + d) + oshift), acc / ls);
       } else {
@@ -819,18 +844,18 @@ __global__ void __launch_bounds__(32 * W)
       const int np = (((L + 15) >> 4) + a.bpp - 1) / a.bpp;
       __threadfence();  // this CTA's partial is visible before its ticket
       __syncthreads();  // every warp is done with the rings
-      if (threadIdx.x == 0) s_last = take_ticket(a, b, g, np);
+      if (threadIdx.x == 0) s_last = take_ticket(a, pseq, g, np);
       __syncthreads();
       if (s_last && wid == 0) {
         __threadfence();  // the other partitions' partials, published before their tickets
-        merge_pair<QT, D>(a, b, g, np, lane, reinterpret_cast<float*>(base), oshift);
+        merge_pair<QT, D>(a, pseq, g, np, lane, reinterpret_cast<float*>(base), oshift);
       }
     }
     return;
   }
   const bool okA = hA < ncols, okB = hB < ncols;
-  const size_t headA = static_cast<size_t>(seq0 + hA / a.G) * a.Hq + g * a.G + hA % a.G;
-  const size_t headB = static_cast<size_t>(seq0 + hB / a.G) * a.Hq + g * a.G + hB % a.G;
+  const size_t headA = static_cast<size_t>(pseq + hA / a.G) * a.Hq + g * a.G + hA % a.G;
+  const size_t headB = static_cast<size_t>(pseq + hB / a.G) * a.Hq + g * a.G + hB % a.G;
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     int d_r, d_r8;
@@ -877,10 +902,10 @@ __global__ void __launch_bounds__(32 * W)
     const int np = (((L + 15) >> 4) + a.bpp - 1) / a.bpp;
     __threadfence();  // this warp's partial is visible before its ticket
     __syncwarp();
-    const bool last = __shfl_sync(FULL, lane == 0 ? take_ticket(a, b, g, np) : false, 0);
+    const bool last = __shfl_sync(FULL, lane == 0 ? take_ticket(a, pseq, g, np) : false, 0);
     if (last) {
       __threadfence();  // the other partitions' partials, published before their tickets
-      merge_pair<QT, D>(a, b, g, np, lane, reinterpret_cast<float*>(base), oshift);
+      merge_pair<QT, D>(a, pseq, g, np, lane, reinterpret_cast<float*>(base), oshift);
     }
   }
 }
@@ -956,27 +981,33 @@ __device__ __forceinline__ void merge_rows(const DecodeArgs& a, size_t row0, int
 }
 
 // Merge the partitions of each (sequence, query head).  One warp per query
-// head, G warps per CTA (one CTA per sequence and kv head).  The first
-// chunk's (m, l) are read together with the context length (rows up to
-// max_parts always exist); partial rows only for partitions that exist.
+// head, G warps per CTA (one CTA per sequence and kv head, and query token
+// when the call maps rows).  The first chunk's (m, l) are read together with
+// the context length (rows up to max_parts always exist); partial rows only
+// for partitions that exist.
 template <typename QT, int D>
 __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce(const DecodeArgs a) {
-  const int bg = blockIdx.x, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int tq = a.q_tokens;
+  const int bg = static_cast<int>(blockIdx.x) / tq, t = static_cast<int>(blockIdx.x) - bg * tq;
+  const int b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int h = g * a.G + static_cast<int>(threadIdx.x >> 5), lane = threadIdx.x & 31;
   dev::grid_dependency_wait();  // partials of decode_main are complete and visible
-  const size_t row0 = (static_cast<size_t>(b) * a.Hq + h) * a.max_parts;
+  int ob = b, pseq = b, n = 1;
+  if (a.q_start) {  // rows of a multi-token call: as decode_main maps them
+    const int s0 = a.q_start[b];
+    n = a.q_start[b + 1] - s0;
+    if (s0 < 0 || n < 0 || n > tq || s0 > a.q_rows - n || t >= n) return;
+    ob = s0 + t;
+    pseq = b * tq + t;
+  }
+  const size_t row0 = (static_cast<size_t>(pseq) * a.Hq + h) * a.max_parts;
   const float mv = lane < a.max_parts ? a.part_m[row0 + lane] : -INFINITY;
   const float lv = lane < a.max_parts ? a.part_l[row0 + lane] : 0.f;
-  const int L = checked_len(a, b, false);
+  int L = checked_len(a, b, false);
+  if (a.q_start) L = max(0, L - n + 1 + t);
   const int nblk = (L + 15) >> 4;
   const int nparts = (nblk + a.bpp - 1) / a.bpp;
   if (nparts <= 1) return;  // written by decode_main (zero rows included)
-  int ob = b;
-  if (a.q_start) {  // one-token rows of a multi-token call only
-    const int s0 = a.q_start[b], s1 = a.q_start[b + 1];
-    if (s1 - s0 != 1 || s0 < 0 || s1 > a.q_rows) return;
-    ob = s0;
-  }
   merge_rows<QT, D>(a, row0, nparts, mv, lv, static_cast<size_t>(ob) * a.Hq + h, lane);
 }
 
@@ -1040,7 +1071,8 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   a.k_scale = l.k_scale;
   a.v_scale = l.v_scale;
   a.out = l.out;
-  const size_t rows = static_cast<size_t>(l.B) * l.Hq * l.plan.max_parts;
+  const int tq = l.q_start ? l.q_tokens : 1;  // grid columns per (sequence, kv head)
+  const size_t rows = static_cast<size_t>(l.B) * tq * l.Hq * l.plan.max_parts;
   a.part_o = l.plan.max_parts > 1 ? static_cast<float*>(l.workspace) : nullptr;
   a.part_m = a.part_o ? a.part_o + rows * D : nullptr;
   a.part_l = a.part_m ? a.part_m + rows : nullptr;
@@ -1072,6 +1104,8 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   a.tail_parts = l.plan.tail_parts;
   a.q_start = l.q_start;
   a.q_rows = l.q_rows;
+  a.q_tokens = tq;
+  a.q_report = l.q_start ? l.q_report : 0;
   a.tickets = nullptr;
   a.epoch = 0;
   if (l.plan.ticket_offset) {  // after the partials: the arrival counters
@@ -1101,7 +1135,7 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   const bool grouped = l.n_groups > 0;
   const dim3 grid = grouped ? dim3(static_cast<unsigned>(l.n_groups * l.Hkv),
                                    static_cast<unsigned>(l.plan.pre_parts + l.max_members * l.plan.tail_parts))
-                            : dim3(static_cast<unsigned>(l.B * l.Hkv), static_cast<unsigned>(l.plan.max_parts));
+                            : dim3(static_cast<unsigned>(l.B * l.Hkv * tq), static_cast<unsigned>(l.plan.max_parts));
   const int W = l.plan.item_warps;
   cudaError_t e;
   if (W == 4)
@@ -1115,7 +1149,7 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
                          dim3(static_cast<unsigned>(l.n_groups * l.max_members * l.Hkv)),
                          dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
   else if (e == cudaSuccess && l.plan.max_parts > 1 && !a.tickets)
-    e = launch_dependent(decode_reduce<QT, D>, dim3(static_cast<unsigned>(l.B * l.Hkv)),
+    e = launch_dependent(decode_reduce<QT, D>, dim3(static_cast<unsigned>(l.B * l.Hkv * tq)),
                          dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode launch: %s", cudaGetErrorString(e));

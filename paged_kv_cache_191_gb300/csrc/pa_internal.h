@@ -79,10 +79,14 @@ struct DecodeLaunch {
   const int32_t* group_start = nullptr;
   const int32_t* prefix_blocks = nullptr;
   int32_t n_groups = 0, max_members = 0;
-  // rows of a multi-token call (pa_chunked_prefill over a 1-byte cache): only
-  // sequences with one query token, whose query / output row is q_start[b]
+  // rows of a multi-token call (pa_chunked_prefill): sequence b's n_b query
+  // tokens are rows q_start[b] .. of q_rows, one grid column per token up to
+  // q_tokens; longer sequences are skipped (left to the multi-token kernel)
+  // unless q_report, when they are flagged as out of range
   const int32_t* q_start = nullptr;
   int32_t q_rows = 0;
+  int32_t q_tokens = 1;
+  int32_t q_report = 0;
 };
 pa_status launch_decode(const DecodeLaunch& a, void* stream);
 
@@ -94,17 +98,31 @@ struct PrefillPlan {
   int32_t max_parts;        // partitions of the longest allowed context
   size_t workspace_bytes;   // 0 when max_parts == 1 and no one-token routing
   // 1-byte caches: one-token sequences of the call go to the decode kernel,
-  // with this plan, its workspace at byte dec_offset
+  // with plan dec, its workspace at byte dec_offset
   int32_t route_single = 0;
+  // short queries over a 16-bit cache (at most kShortTokens per sequence and
+  // 32 rows per kv head): the decode kernel serves the whole call, one grid
+  // column per query token (plan dec for B x max_q_len rows, workspace at
+  // byte 0)
+  int32_t route_short = 0;
   DecodePlan dec;
   size_t dec_offset = 0;
 };
+constexpr int32_t kShortTokens = 8;
 // Whether pa_chunked_prefill runs its tcgen05 kernel (128-row tiles) for
 // this shape: head_dim 128 and more than 64 rows per (sequence, kv head).
 // 1-byte caches too: their codes are converted to 16-bit in shared memory.
+#ifndef PA_TC_MIN_ROWS
+#define PA_TC_MIN_ROWS 64
+#endif
 inline bool prefill_uses_tc(int32_t max_q_len, int32_t num_q_heads, const pa_cache_desc* d) {
-  return d->head_dim == 128 && static_cast<int64_t>(max_q_len) * (num_q_heads / d->num_kv_heads) > 64;
+  return d->head_dim == 128 &&
+         static_cast<int64_t>(max_q_len) * (num_q_heads / d->num_kv_heads) > PA_TC_MIN_ROWS;
 }
+// Whether pa_chunked_prefill sends the whole call to the decode kernel: a
+// 16-bit cache, at most kShortTokens query tokens per sequence and 32 rows
+// per kv head.
+bool prefill_routes_short(int32_t max_q_len, int32_t num_q_heads, const pa_cache_desc* d);
 pa_status plan_prefill(int32_t num_tokens, int32_t B, int32_t num_q_heads, int32_t max_q_len,
                        int32_t max_context_len, const pa_cache_desc* desc, int32_t split_tokens,
                        PrefillPlan* plan);

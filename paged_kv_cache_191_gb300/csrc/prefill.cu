@@ -1260,9 +1260,44 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
   }
 }
 
+// The decode kernel's launch for the rows of a multi-token call it serves:
+// every sequence (q_tokens = max_q_len, out-of-range sequences flagged), or
+// only the one-token sequences (q_tokens = 1, the rest left to the
+// multi-token kernel).
+DecodeLaunch rows_to_decode(const PrefillLaunch& l, int32_t q_tokens, int32_t q_report) {
+  DecodeLaunch d;
+  d.q = l.q;
+  d.q_dtype = l.q_dtype;
+  d.k_cache = l.k_cache;
+  d.v_cache = l.v_cache;
+  d.k_scale = l.k_scale;
+  d.v_scale = l.v_scale;
+  d.block_tables = l.block_tables;
+  d.max_blocks = l.max_blocks;
+  d.context_lens = l.context_lens;
+  d.max_context_len = l.max_context_len;
+  d.B = l.B;
+  d.Hq = l.Hq;
+  d.Hkv = l.Hkv;
+  d.D = l.D;
+  d.num_blocks = l.num_blocks;
+  d.kv_dtype = l.kv_dtype;
+  d.scale = l.scale;
+  d.out = l.out;
+  d.out_dtype = l.out_dtype;
+  d.workspace = static_cast<uint8_t*>(l.workspace) + l.plan.dec_offset;
+  d.plan = l.plan.dec;
+  d.q_start = l.q_start;
+  d.q_rows = l.T;
+  d.q_tokens = q_tokens;
+  d.q_report = q_report;
+  return d;
+}
+
 template <typename KT, typename T, int D>
 pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t stream) {
   using TL = PTile<KT, D>;
+  if (l.plan.route_short) return launch_decode(rows_to_decode(l, l.max_q_len, 1), stream);
   // tcgen05 kernel (128-row tiles; 1-byte codes converted to T in shared
   // memory) or mma.sync kernel (64-row tiles), as planned
   const bool TC = D == 128 && l.plan.tc;
@@ -1304,31 +1339,7 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
   if (l.plan.route_single) {
     // one-token sequences (decode steps riding in the call) first, through the
     // decode kernel: a one-row tile would waste the multi-token kernel's CTA
-    DecodeLaunch d;
-    d.q = l.q;
-    d.q_dtype = l.q_dtype;
-    d.k_cache = l.k_cache;
-    d.v_cache = l.v_cache;
-    d.k_scale = l.k_scale;
-    d.v_scale = l.v_scale;
-    d.block_tables = l.block_tables;
-    d.max_blocks = l.max_blocks;
-    d.context_lens = l.context_lens;
-    d.max_context_len = l.max_context_len;
-    d.B = l.B;
-    d.Hq = l.Hq;
-    d.Hkv = l.Hkv;
-    d.D = l.D;
-    d.num_blocks = l.num_blocks;
-    d.kv_dtype = l.kv_dtype;
-    d.scale = l.scale;
-    d.out = l.out;
-    d.out_dtype = l.out_dtype;
-    d.workspace = static_cast<uint8_t*>(l.workspace) + l.plan.dec_offset;
-    d.plan = l.plan.dec;
-    d.q_start = l.q_start;
-    d.q_rows = l.T;
-    pa_status ds = launch_decode(d, stream);
+    pa_status ds = launch_decode(rows_to_decode(l, 1, 0), stream);
     if (ds != PA_OK) return ds;
     if (l.max_q_len <= 1) return PA_OK;  // nothing left for the multi-token kernel
   }

@@ -176,6 +176,33 @@ def test_plan_info_counts_the_kernels_a_call_launches(palib):
     assert k == 1 + (1 if parts > 1 else 0)
 
 
+def test_short_queries_go_to_the_decode_kernel(palib):
+    """A 16-bit cache with at most 8 query tokens per sequence and 32 rows per
+    kv head: the decode kernel serves the whole call, one grid column per
+    query token, so the plan is the decode plan for B x max_q_len rows.
+    More rows, or a 1-byte cache, keep the multi-token kernels.  The
+    workspace size covers every call up to its bounds, short ones included."""
+    dg = _desc(num_kv_heads=8, kv_dtype=ops.BF16)
+    for mq in (1, 2, 4):
+        tc, parts, bpp, k = ops.chunked_prefill_plan_info(64 * mq, 64, 64, mq, 4096, _torch_like(dg), 0)
+        assert (tc, parts, bpp, k) == (0, *ops.decode_plan_info(64 * mq, 64, 4096, _torch_like(dg)))
+    # 5 tokens x 8 heads = 40 rows: the 64-row kernel (one launch, + its merge when split)
+    tc, parts, bpp, k = ops.chunked_prefill_plan_info(64 * 5, 64, 64, 5, 4096, _torch_like(dg), 0)
+    assert tc == 0 and k == 1 + (parts > 1)
+    # G = 1: up to 8 tokens take the decode route
+    d1 = _desc(num_kv_heads=32, kv_dtype=ops.F16)
+    assert ops.chunked_prefill_plan_info(8 * 8, 8, 32, 8, 2048, _torch_like(d1), 0)[1:] == \
+        ops.decode_plan_info(8 * 8, 32, 2048, _torch_like(d1))
+    # 1-byte codes, 2 tokens: the multi-token kernel (+ the decode kernel for one-token sequences)
+    d8 = _desc(num_kv_heads=8, kv_dtype=ops.FP8_E4M3)
+    tc, parts, bpp, k = ops.chunked_prefill_plan_info(64 * 2, 64, 64, 2, 4096, _torch_like(d8), 0)
+    assert k == 1 + (parts > 1) + ops.decode_plan_info(64, 64, 4096, _torch_like(d8))[2]
+    # sizes: a bound of 512 query tokens covers a 2-token call of the same batch
+    lib = ops.lib()
+    size = lambda mq: lib.pa_chunked_prefill_workspace_size(2076, 32, 32, mq, 2048, C.byref(d1), 0)
+    assert size(512) >= size(2) > 0
+
+
 def _torch_like(desc):
     """A CPU tensor with the cache shape and dtype a desc describes (the plan
     calls read only its shape and dtype)."""

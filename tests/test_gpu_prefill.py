@@ -133,6 +133,35 @@ def test_more_queries_than_context_gives_zero_rows_and_flags():
     assert torch.count_nonzero(out[:8]) == 0
 
 
+@pytest.mark.parametrize("split", [0, 16])
+def test_short_queries_through_the_decode_kernel(split):
+    """Up to 32 rows per kv head over a 16-bit cache run in the decode kernel,
+    one grid column per query token: causal rows, a sequence with more query
+    tokens than context (zero rows, flagged), an empty sequence, and the
+    split-K merge of rows with different key counts."""
+    w = W.random_prefill_small(47, 8, 2, 128, "f16", [4, 3, 0, 4, 1], max_prior=70)
+    lens = w.context_lens.copy()
+    lens[1] = 2  # 3 queries, 2 keys: its first token sees none
+    out = gpu_prefill(w, lens=lens, split_tokens=split)
+    assert ops.device_errors(clear=True) & ops.DEVERR_CONTEXT_LEN
+    ref = oracle(w, lens=lens)
+    assert_close(out.numpy(), ref, TOL["f16"], f"short queries split {split}")
+    qs = w.q_start
+    assert torch.count_nonzero(out[qs[1]]) == 0
+
+
+def test_two_token_verify_full_size():
+    """A one-draft-token verification at the speculative-verify workload's
+    shapes (64 sequences, 64 q / 8 kv heads, bf16, contexts log-uniform in
+    [16, 4096]) through the decode route, every row against the oracle."""
+    w = W.config_spec_verify(gamma=1)
+    ml = int(w.context_lens.max())
+    assert ops.chunked_prefill_plan_info(w.T, w.B, w.Hq, 2, ml, w.k_pool)[1:] == \
+        ops.decode_plan_info(2 * w.B, w.Hq, ml, w.k_pool)
+    out = gpu_prefill(w).numpy()
+    assert_close(out, oracle(w), TOL["bf16"], "two-token verify")
+
+
 def test_bad_query_range_is_flagged_and_skipped():
     w = W.random_prefill_small(43, 4, 4, 64, "f16", [5, 5], max_prior=10)
     bad = np.array([0, 7, 3], np.int32)  # sequence 1 would have -4 tokens
