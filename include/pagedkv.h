@@ -342,10 +342,12 @@ pa_status pa_chunked_prefill_plan_info(int32_t num_tokens, int32_t B, int32_t nu
  * kernel when a row's keys span more than one.  At head_dim 128 with more
  * than 64 rows per kv head the tiles are 128 rows on tcgen05 (FP8 / INT8
  * codes are converted to 16-bit in shared memory on the way to the tensor
- * cores).  Over an FP8 / INT8 cache the sequences with one query token (the
- * decode steps riding in the call) are served first by the decode kernel,
- * whose workspace follows the multi-token kernel's; a call whose max_q_len
- * is 1 launches only the decode kernel.  Over a 16-bit cache a call with
+ * cores).  The sequences with one query token (the decode steps riding in
+ * the call) are served by the decode kernel, whose workspace follows the
+ * multi-token kernel's, on a second stream of the calling thread that the
+ * call forks from `stream` and joins back to it (the multi-token grid's last
+ * wave leaves SMs to the decode rows); a call whose max_q_len is 1 launches
+ * only the decode kernel, on `stream`.  Over a 16-bit cache a call with
  * max_q_len <= 8 and max_q_len * num_q_heads / num_kv_heads <= 32 runs
  * entirely in the decode kernel, one CTA per (sequence, kv head, query
  * token, partition), the columns of one (sequence, kv head) neighbours so

@@ -16,6 +16,9 @@
 #ifndef PA_FUSED_MERGE_MAX
 #define PA_FUSED_MERGE_MAX 8  // most partitions merged that way
 #endif
+#ifndef PA_ROUTE_SINGLE16
+#define PA_ROUTE_SINGLE16 0  // one-token sequences of a 16-bit multi-token call to the decode kernel
+#endif
 #ifndef PA_Q8_WARPS
 #define PA_Q8_WARPS 4  // warps sharing one partition over a 1-byte cache
 #endif
@@ -186,10 +189,11 @@ pa_status plan_prefill(int32_t T, int32_t B, int32_t Hq, int32_t max_q_len, int3
   } else {
     plan->workspace_bytes = 0;
   }
-  // Over a 1-byte cache the multi-token kernel converts every tile per warp,
-  // which a one-row tile of a decode step riding in the call cannot repay:
-  // those sequences go to the decode kernel, whose workspace follows.
-  plan->route_single = quantised(d->kv_dtype) ? 1 : 0;
+  // A decode step riding in the call would fill one row of a multi-token
+  // tile: those one-token sequences go to the decode kernel, whose workspace
+  // follows.  It runs on a second stream beside the multi-token grid, whose
+  // last wave leaves SMs to it.
+  plan->route_single = 1;
   plan->dec_offset = plan->workspace_bytes;
   if (plan->route_single) {
     pa_status st = plan_decode(B, Hq, max_context_len, d, dsplit, &plan->dec);

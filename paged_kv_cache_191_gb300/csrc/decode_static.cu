@@ -36,21 +36,7 @@
 
 #include "pa_internal.h"
 
-namespace {
-
-static __device__ __align__(256) unsigned char g_static_ws[PA_STATIC_WS_BYTES];
-
-constexpr int kMaxDevices = 64;
-
-// The array's address as last looked up on a device, and the context it
-// belongs to.
-struct WsAddr {
-  bool valid = false;
-  unsigned long long ctx_id = 0;
-  void* addr = nullptr;
-};
-std::mutex g_setup_mu;
-WsAddr g_ws[kMaxDevices];
+namespace pa {
 
 // Unique id of the context current on this thread; false when there is none
 // yet (the runtime creates the primary context lazily) or it cannot be read.
@@ -75,6 +61,24 @@ bool current_context_id(unsigned long long* id) {
   return get_id(ctx, id) == CUDA_SUCCESS;
 }
 
+}  // namespace pa
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_ws[PA_STATIC_WS_BYTES];
+
+constexpr int kMaxDevices = 64;
+
+// The array's address as last looked up on a device, and the context it
+// belongs to.
+struct WsAddr {
+  bool valid = false;
+  unsigned long long ctx_id = 0;
+  void* addr = nullptr;
+};
+std::mutex g_setup_mu;
+WsAddr g_ws[kMaxDevices];
+
 // Device address of the static scratch in the current context.  The cached
 // address is reused only while the current context is the one it was looked
 // up in; anything else (no context yet, an id that cannot be read, another
@@ -86,7 +90,7 @@ pa_status static_ws_address(void** out) {
   if (dev < 0 || dev >= kMaxDevices)
     return pa::fail(PA_ERR_UNSUPPORTED, "pa_decode_static_ws: device index %d >= %d", dev, kMaxDevices);
   unsigned long long id = 0;
-  bool have_id = current_context_id(&id);
+  bool have_id = pa::current_context_id(&id);
   std::lock_guard<std::mutex> lock(g_setup_mu);
   WsAddr& c = g_ws[dev];
   if (have_id && c.valid && c.ctx_id == id) {
@@ -97,7 +101,7 @@ pa_status static_ws_address(void** out) {
   e = cudaGetSymbolAddress(&p, g_static_ws);
   if (e != cudaSuccess || !p)
     return pa::fail(PA_ERR_CUDA, "pa_decode_static_ws: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
-  if (!have_id) have_id = current_context_id(&id);  // the lookup made the primary context current
+  if (!have_id) have_id = pa::current_context_id(&id);  // the lookup made the primary context current
   c.valid = have_id;
   c.ctx_id = id;
   c.addr = p;

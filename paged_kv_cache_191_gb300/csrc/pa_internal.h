@@ -97,8 +97,9 @@ struct PrefillPlan {
   int32_t blocks_per_part;  // 16-token blocks per partition
   int32_t max_parts;        // partitions of the longest allowed context
   size_t workspace_bytes;   // 0 when max_parts == 1 and no one-token routing
-  // 1-byte caches: one-token sequences of the call go to the decode kernel,
-  // with plan dec, its workspace at byte dec_offset
+  // one-token sequences of the call go to the decode kernel (on a side
+  // stream when the call also has longer ones), with plan dec, its
+  // workspace at byte dec_offset
   int32_t route_single = 0;
   // short queries over a 16-bit cache (at most kShortTokens per sequence and
   // 32 rows per kv head): the decode kernel serves the whole call, one grid
@@ -179,6 +180,10 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
+// Unique id of the CUDA context current on this thread (cuCtxGetId); false
+// when there is none yet or it cannot be read.
+bool current_context_id(unsigned long long* id);
 
 // Per-translation-unit device error words, OR-ed by pa_device_errors.
 pa_status read_errors_decode(uint32_t* flags, bool clear);

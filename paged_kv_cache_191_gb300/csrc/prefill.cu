@@ -1260,6 +1260,41 @@ __global__ void __launch_bounds__(tcg::kThreads, 2)
   }
 }
 
+#ifndef PA_FORK_SINGLE
+#define PA_FORK_SINGLE 1
+#endif
+
+// A second stream of the calling thread in the current context, with the
+// events that fork it from and join it back to the caller's stream.  The
+// decode kernel for the one-token sequences of a call runs there, beside the
+// multi-token kernel: SMs left idle by the multi-token grid (its last wave)
+// stream the decode rows meanwhile.  Created on first use per thread and
+// device, and again when the context changed (a device reset); never freed.
+struct SideStream {
+  unsigned long long ctx = 0;
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+pa_status side_stream(int dev, SideStream** out) {
+  thread_local SideStream sides[kMaxDevices];
+  SideStream& sd = sides[dev];
+  unsigned long long ctx = 0;
+  if (!current_context_id(&ctx)) return fail(PA_ERR_CUDA, "pa_chunked_prefill: no current CUDA context");
+  if (!sd.s || sd.ctx != ctx) {
+    cudaError_t e = cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      sd.s = nullptr;
+      return fail(PA_ERR_CUDA, "pa_chunked_prefill: side stream: %s", cudaGetErrorString(e));
+    }
+    sd.ctx = ctx;
+  }
+  *out = &sd;
+  return PA_OK;
+}
+
 // The decode kernel's launch for the rows of a multi-token call it serves:
 // every sequence (q_tokens = max_q_len, out-of-range sequences flagged), or
 // only the one-token sequences (q_tokens = 1, the rest left to the
@@ -1336,17 +1371,28 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
   a.v_scale = l.v_scale;
   a.skip_single = l.plan.route_single;
 
-  if (l.plan.route_single) {
-    // one-token sequences (decode steps riding in the call) first, through the
-    // decode kernel: a one-row tile would waste the multi-token kernel's CTA
-    pa_status ds = launch_decode(rows_to_decode(l, 1, 0), stream);
-    if (ds != PA_OK) return ds;
-    if (l.max_q_len <= 1) return PA_OK;  // nothing left for the multi-token kernel
-  }
-
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(PA_ERR_CUDA, "pa_chunked_prefill: no CUDA device");
   if (dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "pa_chunked_prefill: device index %d", dev);
+  // One-token sequences (decode steps riding in the call) go to the decode
+  // kernel: a one-row tile would waste the multi-token kernel's CTA.  With
+  // multi-token sequences as well, that launch goes on the side stream,
+  // forked here (after what the caller enqueued before the call) and joined
+  // back after the multi-token kernel.
+  SideStream* side = nullptr;
+  if (l.plan.route_single) {
+    if (l.max_q_len <= 1) return launch_decode(rows_to_decode(l, 1, 0), stream);
+    if (PA_FORK_SINGLE) {
+      pa_status ss = side_stream(dev, &side);
+      if (ss != PA_OK) return ss;
+      cudaError_t e = cudaEventRecord(side->fork, stream);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
+      if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_chunked_prefill: fork: %s", cudaGetErrorString(e));
+    } else {
+      pa_status ds = launch_decode(rows_to_decode(l, 1, 0), stream);
+      if (ds != PA_OK) return ds;
+    }
+  }
   static std::once_flag once[kMaxDevices];
   static cudaError_t setup_err[kMaxDevices];
   using TS = tcg::Smem;
@@ -1376,8 +1422,15 @@ pa_status launch_t(const PrefillLaunch& l, CUtensorMapDataType dt, cudaStream_t 
                          dim3(static_cast<unsigned>((static_cast<int64_t>(l.T) * l.Hq + kReduceRows - 1) / kReduceRows)),
                          dim3(32 * kReduceRows), 0, stream, a);
   if (e == cudaSuccess) e = cudaGetLastError();
+  pa_status ds = PA_OK;
+  if (side) {  // the decode rows on the side stream, then the join (also after a failed launch)
+    if (e == cudaSuccess) ds = launch_decode(rows_to_decode(l, 1, 0), side->s);
+    cudaError_t j = cudaEventRecord(side->join, side->s);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(stream, side->join, 0);
+    if (j != cudaSuccess && e == cudaSuccess) e = j;
+  }
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_chunked_prefill launch: %s", cudaGetErrorString(e));
-  return PA_OK;
+  return ds;
 }
 
 }  // namespace

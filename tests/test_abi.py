@@ -154,9 +154,9 @@ def test_chunked_prefill_scale_rules(palib):
 def test_plan_info_counts_the_kernels_a_call_launches(palib):
     """pa_decode_plan_info: one partition -> 1 kernel; up to 8 partitions ->
     1 (the decode kernel merges them); more -> 2 (a merge kernel follows).
-    pa_chunked_prefill_plan_info over a 1-byte cache adds the decode
-    kernel's launches for the one-token sequences, and a call whose longest
-    query is one token launches only those."""
+    pa_chunked_prefill_plan_info adds the decode kernel's launches for the
+    one-token sequences, and a call whose longest query is one token
+    launches only those."""
     d = _desc()
     assert ops.decode_plan_info(4, 4, 256, _torch_like(d), 256) == (1, 16, 1)
     assert ops.decode_plan_info(4, 4, 2048, _torch_like(d), 256) == (8, 16, 1)
@@ -171,9 +171,9 @@ def test_plan_info_counts_the_kernels_a_call_launches(palib):
     assert tc == 0 and k == 1 + (1 if parts > 1 else 0) + dec8
     assert ops.chunked_prefill_plan_info(8, 8, 4, 1, 300, _torch_like(d8), 0)[3] == \
         ops.decode_plan_info(8, 4, 300, _torch_like(d8))[2]
-    # 16-bit caches: the multi-token kernel serves every sequence
+    # 16-bit caches alike: the decode kernel takes the one-token sequences
     tc, parts, bpp, k = ops.chunked_prefill_plan_info(70, 8, 4, 40, 300, _torch_like(d), 0)
-    assert k == 1 + (1 if parts > 1 else 0)
+    assert k == 1 + (1 if parts > 1 else 0) + ops.decode_plan_info(8, 4, 300, _torch_like(d))[2]
 
 
 def test_short_queries_go_to_the_decode_kernel(palib):
@@ -186,9 +186,10 @@ def test_short_queries_go_to_the_decode_kernel(palib):
     for mq in (1, 2, 4):
         tc, parts, bpp, k = ops.chunked_prefill_plan_info(64 * mq, 64, 64, mq, 4096, _torch_like(dg), 0)
         assert (tc, parts, bpp, k) == (0, *ops.decode_plan_info(64 * mq, 64, 4096, _torch_like(dg)))
-    # 5 tokens x 8 heads = 40 rows: the 64-row kernel (one launch, + its merge when split)
+    # 5 tokens x 8 heads = 40 rows: the 64-row kernel (+ its merge when split),
+    # and the decode kernel for one-token sequences
     tc, parts, bpp, k = ops.chunked_prefill_plan_info(64 * 5, 64, 64, 5, 4096, _torch_like(dg), 0)
-    assert tc == 0 and k == 1 + (parts > 1)
+    assert tc == 0 and k == 1 + (parts > 1) + ops.decode_plan_info(64, 64, 4096, _torch_like(dg))[2]
     # G = 1: up to 8 tokens take the decode route
     d1 = _desc(num_kv_heads=32, kv_dtype=ops.F16)
     assert ops.chunked_prefill_plan_info(8 * 8, 8, 32, 8, 2048, _torch_like(d1), 0)[1:] == \
