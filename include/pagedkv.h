@@ -277,6 +277,59 @@ pa_status pa_decode_append_grouped(const void* k_new, const void* v_new, int32_t
                                    int32_t split_tokens, void* stream);
 
 /*
+ * pa_decode_append_segments -- pa_decode_append for groups whose members
+ * share blocks in any pattern, not only a common prefix: after beam search
+ * reselects, sibling beams hold their parent's blocks, so the members' tables
+ * form a tree ([LLM-INF] 2.2 copy on write, [KV-CB] 4.2).  The caller lists
+ * the segments: runs of table positions whose blocks a subset of a group's
+ * members all hold (ops.shared_table_segments computes them from the block
+ * tables).  Each item reads its blocks once and scores them against the
+ * queries of every member it lists; a merge kernel combines each member's
+ * items.  It computes what pa_decode_append computes, up to rounding (the
+ * partitions differ), reading each block of the batch once.
+ *
+ * group_start   device int32 [n_groups + 1], as for pa_decode_append_grouped;
+ *               the groups cover sequences 0 .. B-1.
+ * items         device int32 [n_items][4], 16-byte aligned, sorted by group:
+ *               {group k, member list, first block j0, nb | nm << 8}.  The nm
+ *               (1..8) members are indices within group k, 4 bits each, the
+ *               first one's table row is read; every listed member holds the
+ *               same blocks at table positions j0 .. j0 + nb - 1 (nb 1..64).
+ *               An item of several members lies before each member's last
+ *               block (where the fused write lands).  Every position below a
+ *               member's block count is in exactly one item listing it.
+ * group_items   device int32 [n_groups + 1]: group k's items are
+ *               group_items[k] .. group_items[k+1] - 1 (at most
+ *               max_group_items of them).
+ * n_items       host: rows of items (0 is allowed: every row is then zero).
+ * max_group_items host bound on items per group (1..65535); it sizes the
+ *               workspace (pa_decode_segments_workspace_size).
+ * An item with bad fields is skipped and sets PA_DEVERR_GROUP (its members'
+ * rows are then unspecified), as do members whose blocks differ.  Other
+ * arguments and errors as pa_decode_append_grouped.
+ */
+pa_status pa_decode_append_segments(const void* k_new, const void* v_new, int32_t new_dtype,
+                                    const int64_t* slot_mapping, const void* q, int32_t q_dtype,
+                                    void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, int32_t max_context_len,
+                                    int32_t B, int32_t num_q_heads, float scale,
+                                    const int32_t* group_start, int32_t n_groups, int32_t max_group_size,
+                                    const int32_t* items, const int32_t* group_items, int32_t n_items,
+                                    int32_t max_group_items, void* out, int32_t out_dtype,
+                                    const pa_cache_desc* desc, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/*
+ * pa_decode_segments_workspace_size -- bytes of device workspace
+ * pa_decode_append_segments needs: the split-K partials of B sequences x
+ * num_q_heads x max_group_items (0 on an invalid argument).
+ */
+size_t pa_decode_segments_workspace_size(int32_t B, int32_t num_q_heads, int32_t n_groups,
+                                         int32_t max_group_size, int32_t max_group_items,
+                                         const pa_cache_desc* desc);
+
+/*
  * pa_chunked_prefill_workspace_size -- bytes of device workspace
  * pa_chunked_prefill needs for the same arguments, and for a call with a
  * smaller max_q_len that the decode kernel serves (its split-K partials grow

@@ -281,7 +281,30 @@ struct Groups {
   const int32_t* start = nullptr;
   const int32_t* prefix = nullptr;
   int32_t n = 0, max_size = 0, max_prefix = 0;
+  // segment items instead of prefixes (pa_decode_append_segments)
+  const int32_t* items = nullptr;
+  const int32_t* group_items = nullptr;
+  int32_t n_items = 0, max_items = 0;
 };
+
+// The segment grid: one CTA per (item, kv head); each member's partials
+// take max_items slots (the items of its group); a merge kernel follows.
+static pa_status plan_segments(int32_t B, int32_t Hq, const pa_cache_desc* d, const Groups& gr,
+                               pa::DecodePlan* plan) {
+  if (gr.n <= 0 || gr.n > B || gr.max_size <= 0 || gr.max_size > 8 || gr.n_items < 0 || gr.max_items <= 0 ||
+      gr.max_items > 65535)
+    return fail(PA_ERR_INVALID, "pa_decode_append_segments: n_groups, max_group_size, n_items or max_group_items "
+                                "out of range");
+  if (static_cast<int64_t>(gr.max_size) * (Hq / d->num_kv_heads) > 8)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_append_segments: max_group_size * G above 8 query columns");
+  plan->ticket_offset = 0;  // merged by decode_reduce_segments
+  plan->pre_parts = plan->tail_parts = 0;
+  plan->max_parts = gr.max_items;
+  const size_t rows = static_cast<size_t>(B) * Hq * gr.max_items;
+  const size_t bytes = rows * d->head_dim * sizeof(float) + 2 * rows * sizeof(float);
+  plan->workspace_bytes = (bytes + 255) & ~static_cast<size_t>(255);
+  return PA_OK;
+}
 
 // The grouped grid's partition counts on top of the plain plan: prefix
 // partitions of the longest allowed shared prefix, tail partitions of the
@@ -349,7 +372,14 @@ static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache
   pa::DecodePlan plan;
   st = pa::plan_decode(B, num_q_heads, max_context_len, desc, split_tokens, &plan);
   if (st != PA_OK) return st;
-  if (gr.n > 0) {
+  if (gr.n > 0 && gr.max_items > 0) {
+    if (!gr.start || !gr.group_items || (gr.n_items > 0 && !gr.items) ||
+        (reinterpret_cast<uintptr_t>(gr.start) & 3u) || (reinterpret_cast<uintptr_t>(gr.group_items) & 3u) ||
+        (reinterpret_cast<uintptr_t>(gr.items) & 15u))
+      return fail(PA_ERR_INVALID, "pa_decode_append_segments: group_start / items / group_items NULL or misaligned");
+    st = plan_segments(B, num_q_heads, desc, gr, &plan);
+    if (st != PA_OK) return st;
+  } else if (gr.n > 0) {
     if (!gr.start || !gr.prefix || (reinterpret_cast<uintptr_t>(gr.start) & 3u) ||
         (reinterpret_cast<uintptr_t>(gr.prefix) & 3u))
       return fail(PA_ERR_INVALID, "pa_decode_append_grouped: group_start / prefix_blocks NULL or misaligned");
@@ -402,6 +432,10 @@ static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache
   a.prefix_blocks = gr.prefix;
   a.n_groups = gr.n;
   a.max_members = gr.max_size;
+  a.segments = gr.max_items > 0 ? 1 : 0;
+  a.seg_items = gr.items;
+  a.seg_group_items = gr.group_items;
+  a.n_seg_items = gr.n_items;
   return pa::launch_decode(a, stream);
 }
 
@@ -466,6 +500,48 @@ pa_status pa_decode_append_grouped(const void* k_new, const void* v_new, int32_t
   return decode_impl(q, q_dtype, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
                      context_lens, max_context_len, B, num_q_heads, scale, out, out_dtype, desc, workspace,
                      workspace_bytes, split_tokens, stream, k_new, v_new, new_dtype, slot_mapping, gr);
+}
+
+size_t pa_decode_segments_workspace_size(int32_t B, int32_t num_q_heads, int32_t n_groups, int32_t max_group_size,
+                                         int32_t max_group_items, const pa_cache_desc* desc) {
+  if (pa::check_desc(desc, "pa_decode_segments_workspace_size") != PA_OK || B <= 0 || num_q_heads <= 0 ||
+      num_q_heads % desc->num_kv_heads)
+    return 0;
+  pa::DecodePlan plan;
+  if (pa::plan_decode(B, num_q_heads, 0, desc, 0, &plan) != PA_OK) return 0;
+  Groups gr;
+  gr.n = n_groups;
+  gr.max_size = max_group_size;
+  gr.max_items = max_group_items;
+  if (plan_segments(B, num_q_heads, desc, gr, &plan) != PA_OK) return 0;
+  return plan.workspace_bytes;
+}
+
+pa_status pa_decode_append_segments(const void* k_new, const void* v_new, int32_t new_dtype,
+                                    const int64_t* slot_mapping, const void* q, int32_t q_dtype, void* k_cache,
+                                    void* v_cache, float* k_scale, float* v_scale, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                    int32_t max_context_len, int32_t B, int32_t num_q_heads, float scale,
+                                    const int32_t* group_start, int32_t n_groups, int32_t max_group_size,
+                                    const int32_t* items, const int32_t* group_items, int32_t n_items,
+                                    int32_t max_group_items, void* out, int32_t out_dtype,
+                                    const pa_cache_desc* desc, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  if (!slot_mapping) return fail(PA_ERR_INVALID, "pa_decode_append_segments: slot_mapping is NULL");
+  if (B <= 0) return B == 0 ? PA_OK : fail(PA_ERR_INVALID, "pa_decode_append_segments: B < 0");
+  if (n_groups <= 0 || max_group_items <= 0)
+    return fail(PA_ERR_INVALID, "pa_decode_append_segments: n_groups and max_group_items must be > 0");
+  Groups gr;
+  gr.start = group_start;
+  gr.n = n_groups;
+  gr.max_size = max_group_size;
+  gr.items = items;
+  gr.group_items = group_items;
+  gr.n_items = n_items;
+  gr.max_items = max_group_items;
+  return decode_impl(q, q_dtype, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                     context_lens, max_context_len, B, num_q_heads, scale, out, out_dtype, desc, workspace,
+                     workspace_bytes, 0, stream, k_new, v_new, new_dtype, slot_mapping, gr);
 }
 
 static pa_status check_prefill(int32_t T, int32_t B, int32_t num_q_heads, int32_t max_q_len,

@@ -99,6 +99,14 @@ struct DecodeArgs {
   const int32_t* prefix_blocks;
   int32_t n_groups, max_members;
   int32_t pre_parts, tail_parts;  // grid rows: shared-prefix partitions, tail partitions
+  // segments of groups (pa_decode_append_segments), else null: item i =
+  // {group k, member list (4 bits per member index within the group, nm of
+  // them), first block j0, nb | nm << 8}, the items of group k being
+  // seg_group_items[k] .. seg_group_items[k+1]-1; item i's partials are
+  // slot i - seg_group_items[k] of each of its members
+  const int4* seg_items;
+  const int32_t* seg_group_items;
+  int32_t n_seg_items;
   // in-kernel split-K merge (plain grid): one arrival counter per (sequence,
   // kv head), stamped with this launch's epoch
   unsigned long long* tickets;
@@ -370,9 +378,11 @@ __global__ void __launch_bounds__(32 * W)
   // whose columns are the G heads of every member (members x G <= 8), read
   // through member 0's table; the other rows are partitions of one member's
   // tail (blocks after the prefix).  Column c is query head g*G + c % G of
-  // sequence seq0 + c / G.
+  // sequence seq0 + c / G (segment items: seq0 + member c / G of the item's
+  // member list).
   int b, g, p;       // table owner (and fused-write sequence), kv head, partition of its rows
   int seq0, ncols;   // query columns
+  uint32_t mlist = 0x76543210u;  // column c reads sequence seq0 + member c / G of this list (4 bits each)
   int qb = -1;       // query / output row of sequence seq0 (seq0 unless the call maps rows)
   int pseq;          // row base of this item's split-K partials and arrival counter
   int j0, L, nb;     // first block, owner's length, blocks of this item
@@ -383,8 +393,9 @@ __global__ void __launch_bounds__(32 * W)
   int t0, t1;        // block ids j0 + lane, j0 + 32 + lane
   auto load_q = [&]() {
     const int c = r < ncols ? r : 0;
+    const int cm = static_cast<int>((mlist >> (4 * (c / a.G))) & 15u);
     const QT* qrow = static_cast<const QT*>(a.q) +
-                     (static_cast<size_t>((qb >= 0 ? qb : seq0) + c / a.G) * a.Hq + g * a.G + c % a.G) * D;
+                     (static_cast<size_t>((qb >= 0 ? qb : seq0) + cm) * a.Hq + g * a.G + c % a.G) * D;
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
       if (r < ncols) {
@@ -410,7 +421,63 @@ __global__ void __launch_bounds__(32 * W)
   // Launched as a dependent of the preceding kernel (normally the cache
   // write): everything below may read what it wrote.
   dev::grid_dependency_wait();
-  if (a.n_groups == 0) {
+  if (a.seg_items) {
+    // segment item: nb blocks from j0 that the nm listed members of group k
+    // all hold (the owner's table row is read); every block is before each
+    // listed member's last one, except in a one-member item
+    const int4 it = a.seg_items[blockIdx.x];
+    g = static_cast<int>(blockIdx.y);
+    const int k = it.x;
+    mlist = static_cast<uint32_t>(it.y);
+    j0 = it.z;
+    nb = it.w & 0xff;
+    const int nm = (it.w >> 8) & 0xff;
+    const bool lane0 = lane == 0 && g == 0;
+    if (k < 0 || k >= a.n_groups) {
+      if (lane0) atomicOr(&g_decode_err, PA_DEVERR_GROUP);
+      return;
+    }
+    const int gs0 = a.group_start[k], members = a.group_start[k + 1] - gs0;
+    const int is0 = a.seg_group_items[k];
+    p = static_cast<int>(blockIdx.x) - is0;  // the item's partial slot
+    bool bad = gs0 < 0 || members <= 0 || gs0 + members > a.B || nm < 1 || nm > members || nm * a.G > 8 ||
+               nb < 1 || nb > 64 || j0 < 0 || p < 0 || p >= a.max_parts || is0 < 0 ||
+               a.seg_group_items[k + 1] <= static_cast<int>(blockIdx.x) || a.seg_group_items[k + 1] > a.n_seg_items;
+    const int mi = lane < nm ? static_cast<int>((mlist >> (4 * lane)) & 15u) : 0;
+    bad = bad || __any_sync(FULL, lane < nm && mi >= members);
+    if (bad) {
+      if (lane0) atomicOr(&g_decode_err, PA_DEVERR_GROUP);
+      return;
+    }
+    seq0 = gs0;
+    pseq = gs0;
+    b = gs0 + static_cast<int>(mlist & 15u);  // the owner: the first listed member
+    ncols = nm * a.G;
+    const int Lm = lane < nm ? checked_len(a, gs0 + mi, false) : 0;
+    L = __shfl_sync(FULL, Lm, 0);
+    const int nblk = (L + 15) >> 4;
+    direct = false;
+    write_new = nm == 1 && j0 + nb == nblk;
+    // a multi-member item must lie before every member's last block (that
+    // block takes this step's token and is the member's own)
+    const int lastb = (Lm - 1) >> 4;
+    if ((nm > 1 && __any_sync(FULL, lane < nm && j0 + nb > lastb)) || j0 + nb > nblk) {
+      if (lane0) atomicOr(&g_decode_err, PA_DEVERR_GROUP);
+      return;
+    }
+    const int32_t* row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + j0;
+    t0 = lane < nb ? row[lane] : 0;
+    t1 = lane + 32 < nb ? row[lane + 32] : 0;
+    load_q();
+    // every listed member must hold the same blocks here
+    bool differ = false;
+    for (int m = 1; m < nm; ++m) {
+      const int sm = gs0 + static_cast<int>((mlist >> (4 * m)) & 15u);
+      const int32_t* rm = a.block_tables + static_cast<size_t>(sm) * a.max_blocks + j0;
+      differ |= (lane < nb && rm[lane] != t0) || (lane + 32 < nb && rm[lane + 32] != t1);
+    }
+    if (__any_sync(FULL, differ) && lane == 0) atomicOr(&g_decode_err, PA_DEVERR_GROUP);
+  } else if (a.n_groups == 0) {
     // grid column (b, g, t): the q_tokens query tokens of (b, g) are
     // neighbours, so their reads of the same K/V tiles meet in L2
     const int tq = a.q_tokens;
@@ -827,7 +894,8 @@ __global__ void __launch_bounds__(32 * W)
         acc += f * ov[h * D + d];
         ls += f * ov[8 * D + 8 + h];
       }
-      const size_t head = static_cast<size_t>(pseq + h / a.G) * a.Hq + g * a.G + h % a.G;
+      const size_t head =
+          static_cast<size_t>(pseq + static_cast<int>((mlist >> (4 * (h / a.G))) & 15u)) * a.Hq + g * a.G + h % a.G;
       if (direct) {
         store_out<QT>(a, static_cast<size_t>(static_cast<int64_t>(head * D + d) + oshift), acc / ls);
       } else {
@@ -854,8 +922,9 @@ __global__ void __launch_bounds__(32 * W)
     return;
   }
   const bool okA = hA < ncols, okB = hB < ncols;
-  const size_t headA = static_cast<size_t>(pseq + hA / a.G) * a.Hq + g * a.G + hA % a.G;
-  const size_t headB = static_cast<size_t>(pseq + hB / a.G) * a.Hq + g * a.G + hB % a.G;
+  const int mA = static_cast<int>((mlist >> (4 * (hA / a.G))) & 15u), mB = static_cast<int>((mlist >> (4 * (hB / a.G))) & 15u);
+  const size_t headA = static_cast<size_t>(pseq + mA) * a.Hq + g * a.G + hA % a.G;
+  const size_t headB = static_cast<size_t>(pseq + mB) * a.Hq + g * a.G + hB % a.G;
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     int d_r, d_r8;
@@ -1036,6 +1105,90 @@ __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce_grouped(const
   merge_rows<QT, D>(a, row0, nparts, mv, lv, static_cast<size_t>(b) * a.Hq + h, lane);
 }
 
+// The segment form: one CTA per (sequence b, kv head g), a warp per query
+// head.  Sequence b is member m of group k; its partials are the slots of the
+// group's items that list m (lane i looks at item i of a chunk of 32), merged
+// with log-sum-exp weights in slot order.  A member no item lists gets zero
+// rows.
+template <typename QT, int D>
+__global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce_segments(const DecodeArgs a) {
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int V = D / 32;
+  const int b = static_cast<int>(blockIdx.x) / a.Hkv, g = static_cast<int>(blockIdx.x) - b * a.Hkv;
+  const int h = g * a.G + static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  dev::grid_dependency_wait();  // partials of decode_main are complete and visible
+  if (a.group_start[0] > b || a.group_start[a.n_groups] <= b) return;  // in no group: not served
+  int lo = 0, hi = a.n_groups;  // the group k with group_start[k] <= b < group_start[k + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a.group_start[mid] <= b) lo = mid; else hi = mid;
+  }
+  const int m = b - a.group_start[lo];
+  const int is0 = a.seg_group_items[lo];
+  // the group's items, within the item array and the member's slots
+  const int n = is0 < 0 || is0 > a.n_seg_items ? 0
+                                                : min(min(a.seg_group_items[lo + 1], a.n_seg_items) - is0, a.max_parts);
+  const size_t row0 = (static_cast<size_t>(b) * a.Hq + h) * a.max_parts;
+  const float* po = a.part_o + row0 * D + lane * V;
+  float M = -INFINITY, ls = 0.f, acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    const int i = c0 + lane;
+    bool valid = false;
+    if (i < n) {
+      const int4 it = a.seg_items[is0 + i];
+      const int nm = (it.w >> 8) & 0xff;
+      for (int j = 0; j < nm && j < 8; ++j) valid |= static_cast<int>((static_cast<uint32_t>(it.y) >> (4 * j)) & 15u) == m;
+    }
+    const float mv = valid ? __ldcg(a.part_m + row0 + i) : -INFINITY;
+    const float lv = valid ? __ldcg(a.part_l + row0 + i) : 0.f;
+    float cm = mv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, off));
+    const float nm_ = fmaxf(M, cm);
+    if (nm_ == -INFINITY) continue;  // nothing of this member so far
+    const float rescale = dev::ex2(M - nm_);  // 0 on its first partials
+    M = nm_;
+    const float w = valid ? dev::ex2(mv - nm_) : 0.f;
+    float wl = w * lv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(FULL, wl, off);
+    ls = ls * rescale + wl;
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] *= rescale;
+    const unsigned vm = __ballot_sync(FULL, valid);
+    for (int q0 = 0; q0 < 32; q0 += 8) {  // valid rows 8 lanes at a time, their loads in flight together
+      if (!((vm >> q0) & 0xffu)) continue;
+      float x[8][V];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if ((vm >> (q0 + j)) & 1u) {
+          const float* src = po + static_cast<size_t>(c0 + q0 + j) * D;
+          if constexpr (V == 4) {
+            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+            x[j][0] = t.x; x[j][1] = t.y; x[j][2] = t.z; x[j][3] = t.w;
+          } else {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+            x[j][0] = t.x; x[j][1] = t.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float wj = __shfl_sync(FULL, w, q0 + j);
+        if ((vm >> (q0 + j)) & 1u) {
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[v] += wj * x[j][v];
+        }
+      }
+    }
+  }
+  const float inv = ls > 0.f ? 1.f / ls : 0.f;
+#pragma unroll
+  for (int v = 0; v < V; ++v) store_out<QT>(a, (static_cast<size_t>(b) * a.Hq + h) * D + lane * V + v, acc[v] * inv);
+}
+
 // ---- host side -------------------------------------------------------------------
 template <typename KT, int D>
 pa_status make_map(CUtensorMap* m, const void* cache, int Hkv, int num_blocks, CUtensorMapDataType dt) {
@@ -1073,7 +1226,8 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   a.out = l.out;
   const int tq = l.q_start ? l.q_tokens : 1;  // grid columns per (sequence, kv head)
   const size_t rows = static_cast<size_t>(l.B) * tq * l.Hq * l.plan.max_parts;
-  a.part_o = l.plan.max_parts > 1 ? static_cast<float*>(l.workspace) : nullptr;
+  // partials: a split, or segment items (whose rows are always partials)
+  a.part_o = l.plan.max_parts > 1 || l.segments ? static_cast<float*>(l.workspace) : nullptr;
   a.part_m = a.part_o ? a.part_o + rows * D : nullptr;
   a.part_l = a.part_m ? a.part_m + rows : nullptr;
   a.B = l.B;
@@ -1102,6 +1256,9 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   a.max_members = l.max_members;
   a.pre_parts = l.plan.pre_parts;
   a.tail_parts = l.plan.tail_parts;
+  a.seg_items = l.segments ? reinterpret_cast<const int4*>(l.seg_items) : nullptr;
+  a.seg_group_items = l.seg_group_items;
+  a.n_seg_items = l.n_seg_items;
   a.q_start = l.q_start;
   a.q_rows = l.q_rows;
   a.q_tokens = tq;
@@ -1132,6 +1289,26 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   if (setup_err[dev] != cudaSuccess)
     return fail(PA_ERR_CUDA, "pa_decode: %s", cudaGetErrorString(setup_err[dev]));
 
+  if (l.segments) {
+    // one CTA per (segment item, kv head), then the merge of each member's items
+    cudaError_t e = cudaSuccess;
+    if (l.n_seg_items > 0) {
+      const dim3 sgrid(static_cast<unsigned>(l.n_seg_items), static_cast<unsigned>(l.Hkv));
+      const int W = l.plan.item_warps;
+      if (W == 4)
+        e = launch_dependent(decode_main<KT, QT, D, 4>, sgrid, dim3(128), TL::smem(4), stream, tmK, tmV, a);
+      else if (W == 2)
+        e = launch_dependent(decode_main<KT, QT, D, 2>, sgrid, dim3(64), TL::smem(2), stream, tmK, tmV, a);
+      else
+        e = launch_dependent(decode_main<KT, QT, D, 1>, sgrid, dim3(32), TL::smem(1), stream, tmK, tmV, a);
+    }
+    if (e == cudaSuccess)
+      e = launch_dependent(decode_reduce_segments<QT, D>, dim3(static_cast<unsigned>(l.B * l.Hkv)),
+                           dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode launch: %s", cudaGetErrorString(e));
+    return PA_OK;
+  }
   const bool grouped = l.n_groups > 0;
   const dim3 grid = grouped ? dim3(static_cast<unsigned>(l.n_groups * l.Hkv),
                                    static_cast<unsigned>(l.plan.pre_parts + l.max_members * l.plan.tail_parts))

@@ -167,7 +167,8 @@ def test_shared_prefix_16x4_full_size():
     (beam, head) row matches the float64 oracle within the f16 tolerance --
     the grouped call and the plain fused call alike.  Each group's shared
     prefix is staged per step as the benchmark does: the prompt plus the tail
-    blocks its beams inherited from a common ancestor.
+    blocks its beams inherited from a common ancestor.  The segment call
+    (every block read once, whichever beams share it) matches too.
 
     Source: "大模型推理引擎优化：KV Cache 与连续批处理" 4.2 and
     "LLM推理引擎深度实战：从PagedAttention到分布式推理部署" 2.2 (shared blocks
@@ -199,7 +200,7 @@ def test_shared_prefix_16x4_full_size():
     gs = torch.from_numpy(gs_host).to(DEV)
     rng = W.rng_for(23)
     q = w.q.to(DEV)
-    total_cow = total_extra = 0
+    total_cow = total_extra = total_pairs = 0
     for step in range(6):
         par = (np.arange(w.groups)[:, None] * beams + w.parents[step]).reshape(-1).tolist()
         ca.reselect(ids, par)
@@ -229,14 +230,23 @@ def test_shared_prefix_16x4_full_size():
         pre = torch.from_numpy(pre_host).to(DEV)
         out = ops.decode_append_grouped(nk.to(DEV), nv.to(DEV), sl, q, kc, vc, bt, cl, ml, w.scale, gs, pre, beams,
                                         cap, out_dtype=torch.float32)
-        # the plain fused call on the same state: it stores the same rows again
+        # the plain fused call and the segment call on the same state: they
+        # store the same rows again
         plain = ops.decode_append(nk.to(DEV), nv.to(DEV), sl, q, kc, vc, bt, cl, ml, w.scale,
                                   out_dtype=torch.float32)
+        items, gi = ops.shared_table_segments(tables, lens, gs_host)
+        nm = (items[:, 3] >> 8) & 0xff
+        total_pairs += int(((nm > 1) & (nm < beams)).sum())
+        seg = ops.decode_append_segments(nk.to(DEV), nv.to(DEV), sl, q, kc, vc, bt, cl, ml, w.scale, gs,
+                                         torch.from_numpy(items).to(DEV), torch.from_numpy(gi).to(DEV), beams,
+                                         int(np.diff(gi).max()), out_dtype=torch.float32)
         torch.cuda.synchronize()
         okc, ovc, _, _ = o_write(np_exact(nk), np_exact(nv), np.array(slots), okc, ovc)
         ref = paged_decode(np_exact(w.q), okc, ovc, tables, lens, w.scale)
         assert_close(out.cpu().numpy(), ref, TOL["f16"], f"grouped step {step}")
         assert_close(plain.cpu().numpy(), ref, TOL["f16"], f"plain step {step}")
+        assert_close(seg.cpu().numpy(), ref, TOL["f16"], f"segments step {step}")
     assert total_cow > 0, "reselection is meant to exercise copy-on-write"
+    assert total_pairs > 0, "some blocks are meant to be shared by part of a group"
     assert total_extra > 0, "some group is meant to share tail blocks beyond the prompt"
     assert np.array_equal(np_exact(kc), okc) and np.array_equal(np_exact(vc), ovc)
