@@ -66,6 +66,9 @@ def parse_args(argv=None):
     p.add_argument("--unfused", action="store_true",
                    help="pa_cache_write + pa_decode instead of the fused pa_decode_append")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the oracle on the host cores")
+    p.add_argument("--prefix-groups", action="store_true",
+                   help="shared_prefix_16x4: pa_decode_append_grouped (each group's common prefix read once) "
+                        "instead of pa_decode_append_segments (every shared block read once)")
     p.add_argument("--ungrouped", action="store_true",
                    help="shared_prefix_16x4: read shared prompt blocks once per beam (pa_decode_append)")
     p.add_argument("--headline-only", action="store_true",
@@ -480,8 +483,8 @@ class DecodeStep:
     def launches_per_step(self):
         """Kernels one step launches: the decode call's own count (main kernel,
         plus the merge kernel when the library plans one) and the separate
-        cache write when the write is not fused; the grouped call always
-        follows its main kernel with decode_reduce_grouped."""
+        cache write when the write is not fused; the grouped and segment
+        calls always follow their main kernel with their merge kernel."""
         if getattr(self, "grouped", False) and self.fused:
             return 2
         _, _, kernels = self.ops.decode_plan_info(self.B, self.Hq, self.max_len, self.kc, self.split)
@@ -526,20 +529,34 @@ class SharedPrefixStep(DecodeStep):
         self.out = torch.empty((self.B, self.Hq, self.D), dtype=w.q.dtype, device=device)
         self.desc = ops.cache_desc(self.kc)
         self.ws_bytes = ops.decode_workspace_size(self.B, self.Hq, self.max_len, self.kc, split_tokens)
-        # shared-prefix groups: the beams of one prompt; each step's shared
-        # prefix is the longest run of leading table entries all of a group's
-        # beams hold (the prompt, and tail blocks inherited from a common
-        # ancestor), staged with the step's metadata
+        # groups: the beams of one prompt.  Segments (default): the runs of
+        # table positions each subset of a group's beams holds (the prompt,
+        # blocks inherited from a parent, private tails), every block read
+        # once; prefix groups: each group's longest common run of leading
+        # table entries read once, the rest per beam.  Either is computed per
+        # step from the block manager's tables and staged with the metadata.
         self.grouped = True
+        self.segments = True
         self.group_start_host = np.arange(0, self.B + 1, w.beams, dtype=np.int32)
         self.group_start = torch.from_numpy(self.group_start_host).to(device)
+        self.max_group_items = 32   # items per group: ~7 segments of <= 32 blocks for 4 beams
+        self.blocks_per_item = 32
         gws = int(self.L.pa_decode_grouped_workspace_size(self.B, self.Hq, self.max_len, w.groups, w.beams,
                                                           self.cap, C.byref(self.desc), split_tokens))
-        self.ws = torch.empty(max(self.ws_bytes, gws, 16), dtype=torch.uint8, device=device)
+        sws = int(self.L.pa_decode_segments_workspace_size(self.B, self.Hq, w.groups, w.beams,
+                                                           self.max_group_items, C.byref(self.desc)))
+        self.ws = torch.empty(max(self.ws_bytes, gws, sws, 16), dtype=torch.uint8, device=device)
         self.split = split_tokens
         # meta: slots int64[B] | pairs int64[B, 2] | lens int32[B] | tables int32[B, cap] | prefix int32[groups]
+        #       | items int32[max_items][4] (16-byte aligned); a step copies the part it uses
         self.pre_off = self.B * 8 + self.B * 16 + self.B * 4 + self.B * self.cap * 4
-        self.meta_bytes = self.pre_off + w.groups * 4
+        self.it_off = (self.pre_off + w.groups * 4 + 15) // 16 * 16
+        self.max_items = w.groups * self.max_group_items
+        self.most_c = C.c_int32()
+        self.meta_bytes = self.it_off + self.max_items * 16
+        self.copy_bytes = self.pre_off + w.groups * 4
+        self.n_items = 0
+        self.n_items_c = C.c_int32()
         self.meta_host = [torch.empty(self.meta_bytes, dtype=torch.uint8).pin_memory() for _ in range(RING)]
         self.meta_devs = [torch.empty(self.meta_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
         self.use_meta(0)
@@ -563,17 +580,41 @@ class SharedPrefixStep(DecodeStep):
         self.pairs_dev = self.meta_dev[B * 8: B * 24].view(T.int64).view(B, 2)
         self.lens_dev = self.meta_dev[B * 24: B * 28].view(T.int32)
         self.tables_dev = self.meta_dev[B * 28: self.pre_off].view(T.int32).view(B, self.cap)
-        self.prefix_dev = self.meta_dev[self.pre_off:].view(T.int32)
+        self.prefix_dev = self.meta_dev[self.pre_off: self.pre_off + self.w.groups * 4].view(T.int32)
 
     def prebuild(self, stream):
         super().prebuild(stream)
         w = self.w
         # pa_decode_append's arguments with the group description after `scale`
-        self.grouped_args = []
+        self.grouped_args, self.segment_args = [], []
         for i, a in enumerate(self.append_args):
             pre = C.c_void_p(self.meta_devs[i].data_ptr() + self.pre_off)
             extra = (C.c_void_p(self.group_start.data_ptr()), pre, w.groups, w.beams, self.cap)
             self.grouped_args.append(a[:17] + extra + a[17:])
+            # pa_decode_append_segments: no split_tokens; n_items (index 21) is set per step
+            seg = (C.c_void_p(self.group_start.data_ptr()), w.groups, w.beams,
+                   C.c_void_p(self.meta_devs[i].data_ptr() + self.it_off), 0, self.max_group_items)
+            self.segment_args.append(a[:17] + seg + a[17:22] + a[23:])
+
+    def seg_call_args(self, i):
+        a = self.segment_args[i]
+        return a[:21] + (self.n_items,) + a[22:]
+
+    def stage_segments(self, base):
+        """Each group's segment items (pa_table_segments) from the tables and
+        lengths the block manager just staged in the pinned metadata buffer at
+        `base`, written beside them."""
+        B, w = self.B, self.w
+        st = self.L.pa_table_segments(C.c_void_p(base + B * 28), self.cap, C.c_void_p(base + B * 24),
+                                      self.group_start_host.ctypes.data_as(C.c_void_p), w.groups,
+                                      self.blocks_per_item, C.c_void_p(base + self.it_off), self.max_items,
+                                      C.byref(self.n_items_c), C.byref(self.most_c))
+        if st:
+            self.ops._check(st, "pa_table_segments")
+        self.n_items = self.n_items_c.value
+        if self.most_c.value > self.max_group_items:
+            raise RuntimeError("a group needs more than max_group_items segment items")
+        self.copy_bytes = self.it_off + self.n_items * 16
 
     def stage_prefix(self, raw):
         """Each group's shared prefix (ops.shared_table_prefix) from the tables
@@ -582,7 +623,8 @@ class SharedPrefixStep(DecodeStep):
         w, B = self.w, self.B
         tables = raw[B * 28: self.pre_off].view(np.int32).reshape(B, self.cap)
         lens = raw[B * 24: B * 28].view(np.int32)
-        self.ops.shared_table_prefix(tables, lens, self.group_start_host, out=raw[self.pre_off:].view(np.int32))
+        self.ops.shared_table_prefix(tables, lens, self.group_start_host,
+                                     out=raw[self.pre_off: self.pre_off + w.groups * 4].view(np.int32))
 
     def _fresh(self, n):
         ids = np.arange(self.next_id, self.next_id + n, dtype=np.uint64)
@@ -626,7 +668,11 @@ class SharedPrefixStep(DecodeStep):
         self.ops._check(self.L.pa_block_tables(self.alloc._h, self.ids_c, B, C.cast(base + B * 28, C.POINTER(C.c_int32)),
                                                self.cap, C.cast(base + B * 24, C.POINTER(C.c_int32))),
                         "pa_block_tables")
-        self.stage_prefix(buf.numpy())
+        if self.grouped and self.segments:
+            self.stage_segments(base)
+        else:
+            self.stage_prefix(buf.numpy())
+            self.copy_bytes = self.pre_off + w.groups * 4
         self.n_cow = self.ncow_c.value
         self.steps_since_reset += 1
         self.step_idx += 1
@@ -637,7 +683,7 @@ class SharedPrefixStep(DecodeStep):
         L, drv, sp, cp, i = self.L, self.drv, self.sp, self.cp, self.dbuf
         if self.used_rec[i]:
             drv.wait(cp, self.used_done[i])
-        drv.h2d(self.meta_devs[i].data_ptr(), buf.data_ptr(), self.meta_bytes, cp)
+        drv.h2d(self.meta_devs[i].data_ptr(), buf.data_ptr(), self.copy_bytes, cp)
         drv.record(self.ring_ev[self.ring], cp)
         drv.record(self.copy_done[i], cp)
         self.ring_used[self.ring] = True
@@ -649,7 +695,14 @@ class SharedPrefixStep(DecodeStep):
                                   C.byref(self.desc), sp)
             if st:
                 self.ops._check(st, "pa_copy_blocks")
-        if self.fused and self.grouped:
+        if self.fused and self.grouped and self.segments:
+            if ev_pair is not None:
+                drv.record(ev_pair[0], sp)
+            self.last_seg_args = self.seg_call_args(i)
+            st = L.pa_decode_append_segments(*self.last_seg_args)
+            if st:
+                self.ops._check(st, "pa_decode_append_segments")
+        elif self.fused and self.grouped:
             if ev_pair is not None:
                 drv.record(ev_pair[0], sp)
             st = L.pa_decode_append_grouped(*self.grouped_args[i])
@@ -720,7 +773,7 @@ class SharedPrefixStep(DecodeStep):
             copy = ncow * 2 * 2 * block_bytes
             dec_u += d + (write if self.fused else 0)
             dec_l += dl
-            step_u += d + write + copy + self.meta_bytes
+            step_u += d + write + copy + self.copy_bytes
         return dec_u, step_u, dec_l
 
 
@@ -737,6 +790,7 @@ def build_step(name, args, dev):
     st.fused = not args.unfused
     if shared:
         st.grouped = not args.ungrouped
+        st.segments = not args.prefix_groups
     return w, st, shared
 
 
@@ -791,6 +845,8 @@ def decode_call(st):
     rewrites the same slots with the same rows, so every repeat is the same work."""
     i = st.dbuf ^ 1
     if st.fused and getattr(st, "grouped", False) and isinstance(st, SharedPrefixStep):
+        if st.segments:
+            return st.L.pa_decode_append_segments, st.last_seg_args
         return st.L.pa_decode_append_grouped, st.grouped_args[i]
     if st.fused:
         return st.L.pa_decode_append, st.append_args[i]
@@ -825,6 +881,9 @@ def clock_windows(st, stream, r):
 
 
 def launch_kernel_name(st, shared):
+    if shared and st.fused and st.grouped and st.segments:
+        return ("pa_decode_append_segments (decode_main over the groups' shared-block segments with the fused "
+                "cache write + decode_reduce_segments)")
     if shared and st.fused and st.grouped:
         return ("pa_decode_append_grouped (decode_main over shared-prefix groups with the fused "
                 "cache write + decode_reduce_grouped)")
@@ -930,7 +989,9 @@ def run_ours(args, rank, world, local_rank):
             **({"sharing": "16 groups x 4 beams share a 1024-token prompt; beams reselected from "
                            "parents every step (fork + release), copy-on-write before each decode; "
                            "bytes count shared blocks once (logical bytes reported separately)",
-                "prompt_reads": ("once per group of 4 beams (pa_decode_append_grouped)"
+                "prompt_reads": ("every shared block once (pa_decode_append_segments)"
+                                 if not args.unfused and not args.ungrouped and not args.prefix_groups
+                                 else "once per group of 4 beams (pa_decode_append_grouped)"
                                  if not args.unfused and not args.ungrouped else "once per beam")}
                if shared else {}),
             "split_tokens": args.split or "auto",
@@ -1122,15 +1183,15 @@ def run_e2e(st, args, stream):
         t1 = time.perf_counter()
     total_b = st.count_bytes()[1]
     st.history.clear()
-    h2d = st.meta_bytes + hqkv.numel() * hqkv.element_size()
+    h2d = st.copy_bytes + hqkv.numel() * hqkv.element_size()
     d2h = hout.numel() * hout.element_size()
     return {"value": round(total_b / (t1 - t0) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
             "tokens_per_s": round(st.B * n / (t1 - t0), 1),
             "api": "libpagedkv C ABI through the benchmark's step (block manager writes slots, copy pairs, tables "
-                   "and each group's shared prefix into a pinned staging buffer; one H2D copy of it and one of the "
-                   "packed q / k_new / v_new; pa_copy_blocks; pa_decode_append_grouped; one D2H copy of the "
-                   "output; waited for every step)"}
+                   "and the groups' segment items (pa_table_segments) into a pinned staging buffer; one H2D copy "
+                   "of it and one of the packed q / k_new / v_new; pa_copy_blocks; pa_decode_append_segments; one "
+                   "D2H copy of the output; waited for every step)"}
 
 
 # ---- multi-token workloads (chunked prefill, speculative verify) ------------------

@@ -282,7 +282,7 @@ pa_status pa_decode_append_grouped(const void* k_new, const void* v_new, int32_t
  * reselects, sibling beams hold their parent's blocks, so the members' tables
  * form a tree ([LLM-INF] 2.2 copy on write, [KV-CB] 4.2).  The caller lists
  * the segments: runs of table positions whose blocks a subset of a group's
- * members all hold (ops.shared_table_segments computes them from the block
+ * members all hold (pa_table_segments computes them from the block
  * tables).  Each item reads its blocks once and scores them against the
  * queries of every member it lists; a merge kernel combines each member's
  * items.  It computes what pa_decode_append computes, up to rounding (the
@@ -290,20 +290,21 @@ pa_status pa_decode_append_grouped(const void* k_new, const void* v_new, int32_t
  *
  * group_start   device int32 [n_groups + 1], as for pa_decode_append_grouped;
  *               the groups cover sequences 0 .. B-1.
- * items         device int32 [n_items][4], 16-byte aligned, sorted by group:
- *               {group k, member list, first block j0, nb | nm << 8}.  The nm
- *               (1..8) members are indices within group k, 4 bits each, the
- *               first one's table row is read; every listed member holds the
- *               same blocks at table positions j0 .. j0 + nb - 1 (nb 1..64).
- *               An item of several members lies before each member's last
- *               block (where the fused write lands).  Every position below a
- *               member's block count is in exactly one item listing it.
- * group_items   device int32 [n_groups + 1]: group k's items are
- *               group_items[k] .. group_items[k+1] - 1 (at most
- *               max_group_items of them).
- * n_items       host: rows of items (0 is allowed: every row is then zero).
- * max_group_items host bound on items per group (1..65535); it sizes the
- *               workspace (pa_decode_segments_workspace_size).
+ * items         device int32 [n_items][4], 16-byte aligned, in any order (the
+ *               order they are dispatched in: longest first balances best):
+ *               {group k, member list, first block j0, nb | nm << 8 |
+ *               slot << 16}.  The nm (1..8) members are indices within group
+ *               k, 4 bits each, the first one's table row is read; every
+ *               listed member holds the same blocks at table positions j0 ..
+ *               j0 + nb - 1 (nb 1..64).  An item of several members lies
+ *               before each member's last block (where the fused write
+ *               lands).  Every position below a member's block count is in
+ *               exactly one item listing it.  slot (< max_group_items) is the
+ *               item's partial slot: the items listing one member have
+ *               distinct slots.
+ * n_items       host: rows of items (0 .. 65535; 0: every row is zero).
+ * max_group_items host bound on slots (1..65535); it sizes the workspace
+ *               (pa_decode_segments_workspace_size).
  * An item with bad fields is skipped and sets PA_DEVERR_GROUP (its members'
  * rows are then unspecified), as do members whose blocks differ.  Other
  * arguments and errors as pa_decode_append_grouped.
@@ -315,10 +316,34 @@ pa_status pa_decode_append_segments(const void* k_new, const void* v_new, int32_
                                     const int32_t* context_lens, int32_t max_context_len,
                                     int32_t B, int32_t num_q_heads, float scale,
                                     const int32_t* group_start, int32_t n_groups, int32_t max_group_size,
-                                    const int32_t* items, const int32_t* group_items, int32_t n_items,
-                                    int32_t max_group_items, void* out, int32_t out_dtype,
+                                    const int32_t* items, int32_t n_items, int32_t max_group_items, void* out,
+                                    int32_t out_dtype,
                                     const pa_cache_desc* desc, void* workspace, size_t workspace_bytes,
                                     void* stream);
+
+/*
+ * pa_table_segments -- the items of pa_decode_append_segments from the block
+ * tables (host only; nothing is launched).  Per group and table position j,
+ * the members whose tables hold the same block at j form a class, except that
+ * at and after a member's last block (the block its next token is written
+ * to) the member is alone; a segment is a maximal run of positions over which
+ * a member's class stays the same.  Each segment is listed once, by its lowest
+ * member, cut into items of at most blocks_per_item blocks; a group's items
+ * take slots 0, 1, ... in the order (lowest member, first position), and the
+ * list is sorted longest first (ties in that order, groups in turn).
+ *
+ * block_tables  host int32 [n_sequences][max_blocks].
+ * context_lens  host int32, 0 .. max_blocks * 16.
+ * group_start   host int32 [n_groups + 1]; groups of 0 .. 8 members.
+ * items         host int32 [max_items][4] out, the layout of
+ *               pa_decode_append_segments; *n_items out; *max_slots out (the
+ *               most items of one group), may be NULL.
+ * PA_ERR_INVALID on a bad argument or more than max_items items (at most the
+ * members' blocks summed are ever needed).
+ */
+pa_status pa_table_segments(const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
+                            const int32_t* group_start, int32_t n_groups, int32_t blocks_per_item,
+                            int32_t* items, int32_t max_items, int32_t* n_items, int32_t* max_slots);
 
 /*
  * pa_decode_segments_workspace_size -- bytes of device workspace

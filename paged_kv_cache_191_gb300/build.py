@@ -20,7 +20,8 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
           "--expt-relaxed-constexpr"]
-SOURCES = ["decode.cu", "decode_static.cu", "prefill.cu", "cache_ops.cu", "api.cpp", "allocator.cpp", "scheduler.cpp", "serve.cpp"]
+SOURCES = ["decode.cu", "decode_static.cu", "prefill.cu", "cache_ops.cu", "api.cpp", "allocator.cpp", "scheduler.cpp",
+           "serve.cpp", "segments.cpp"]
 HEADERS = ["device_common.cuh", "pa_internal.h", "kv_map.h"]
 
 

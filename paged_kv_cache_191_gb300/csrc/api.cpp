@@ -283,7 +283,6 @@ struct Groups {
   int32_t n = 0, max_size = 0, max_prefix = 0;
   // segment items instead of prefixes (pa_decode_append_segments)
   const int32_t* items = nullptr;
-  const int32_t* group_items = nullptr;
   int32_t n_items = 0, max_items = 0;
 };
 
@@ -291,8 +290,8 @@ struct Groups {
 // take max_items slots (the items of its group); a merge kernel follows.
 static pa_status plan_segments(int32_t B, int32_t Hq, const pa_cache_desc* d, const Groups& gr,
                                pa::DecodePlan* plan) {
-  if (gr.n <= 0 || gr.n > B || gr.max_size <= 0 || gr.max_size > 8 || gr.n_items < 0 || gr.max_items <= 0 ||
-      gr.max_items > 65535)
+  if (gr.n <= 0 || gr.n > B || gr.max_size <= 0 || gr.max_size > 8 || gr.n_items < 0 || gr.n_items > 65535 ||
+      gr.max_items <= 0 || gr.max_items > 65535)
     return fail(PA_ERR_INVALID, "pa_decode_append_segments: n_groups, max_group_size, n_items or max_group_items "
                                 "out of range");
   if (static_cast<int64_t>(gr.max_size) * (Hq / d->num_kv_heads) > 8)
@@ -373,10 +372,9 @@ static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache
   st = pa::plan_decode(B, num_q_heads, max_context_len, desc, split_tokens, &plan);
   if (st != PA_OK) return st;
   if (gr.n > 0 && gr.max_items > 0) {
-    if (!gr.start || !gr.group_items || (gr.n_items > 0 && !gr.items) ||
-        (reinterpret_cast<uintptr_t>(gr.start) & 3u) || (reinterpret_cast<uintptr_t>(gr.group_items) & 3u) ||
+    if (!gr.start || (gr.n_items > 0 && !gr.items) || (reinterpret_cast<uintptr_t>(gr.start) & 3u) ||
         (reinterpret_cast<uintptr_t>(gr.items) & 15u))
-      return fail(PA_ERR_INVALID, "pa_decode_append_segments: group_start / items / group_items NULL or misaligned");
+      return fail(PA_ERR_INVALID, "pa_decode_append_segments: group_start / items NULL or misaligned");
     st = plan_segments(B, num_q_heads, desc, gr, &plan);
     if (st != PA_OK) return st;
   } else if (gr.n > 0) {
@@ -434,7 +432,6 @@ static pa_status decode_impl(const void* q, int32_t q_dtype, const void* k_cache
   a.max_members = gr.max_size;
   a.segments = gr.max_items > 0 ? 1 : 0;
   a.seg_items = gr.items;
-  a.seg_group_items = gr.group_items;
   a.n_seg_items = gr.n_items;
   return pa::launch_decode(a, stream);
 }
@@ -523,8 +520,8 @@ pa_status pa_decode_append_segments(const void* k_new, const void* v_new, int32_
                                     int32_t max_blocks_per_seq, const int32_t* context_lens,
                                     int32_t max_context_len, int32_t B, int32_t num_q_heads, float scale,
                                     const int32_t* group_start, int32_t n_groups, int32_t max_group_size,
-                                    const int32_t* items, const int32_t* group_items, int32_t n_items,
-                                    int32_t max_group_items, void* out, int32_t out_dtype,
+                                    const int32_t* items, int32_t n_items, int32_t max_group_items, void* out,
+                                    int32_t out_dtype,
                                     const pa_cache_desc* desc, void* workspace, size_t workspace_bytes,
                                     void* stream) {
   if (!slot_mapping) return fail(PA_ERR_INVALID, "pa_decode_append_segments: slot_mapping is NULL");
@@ -536,7 +533,6 @@ pa_status pa_decode_append_segments(const void* k_new, const void* v_new, int32_
   gr.n = n_groups;
   gr.max_size = max_group_size;
   gr.items = items;
-  gr.group_items = group_items;
   gr.n_items = n_items;
   gr.max_items = max_group_items;
   return decode_impl(q, q_dtype, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,

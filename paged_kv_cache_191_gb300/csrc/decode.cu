@@ -101,11 +101,9 @@ struct DecodeArgs {
   int32_t pre_parts, tail_parts;  // grid rows: shared-prefix partitions, tail partitions
   // segments of groups (pa_decode_append_segments), else null: item i =
   // {group k, member list (4 bits per member index within the group, nm of
-  // them), first block j0, nb | nm << 8}, the items of group k being
-  // seg_group_items[k] .. seg_group_items[k+1]-1; item i's partials are
-  // slot i - seg_group_items[k] of each of its members
+  // them), first block j0, nb | nm << 8 | slot << 16}; its partials are
+  // partial slot `slot` of each of its members
   const int4* seg_items;
-  const int32_t* seg_group_items;
   int32_t n_seg_items;
   // in-kernel split-K merge (plain grid): one arrival counter per (sequence,
   // kv head), stamped with this launch's epoch
@@ -425,24 +423,22 @@ __global__ void __launch_bounds__(32 * W)
     // segment item: nb blocks from j0 that the nm listed members of group k
     // all hold (the owner's table row is read); every block is before each
     // listed member's last one, except in a one-member item
-    const int4 it = a.seg_items[blockIdx.x];
-    g = static_cast<int>(blockIdx.y);
+    const int4 it = a.seg_items[blockIdx.y];
+    g = static_cast<int>(blockIdx.x);
     const int k = it.x;
     mlist = static_cast<uint32_t>(it.y);
     j0 = it.z;
     nb = it.w & 0xff;
     const int nm = (it.w >> 8) & 0xff;
+    p = (it.w >> 16) & 0xffff;  // the item's partial slot
     const bool lane0 = lane == 0 && g == 0;
     if (k < 0 || k >= a.n_groups) {
       if (lane0) atomicOr(&g_decode_err, PA_DEVERR_GROUP);
       return;
     }
     const int gs0 = a.group_start[k], members = a.group_start[k + 1] - gs0;
-    const int is0 = a.seg_group_items[k];
-    p = static_cast<int>(blockIdx.x) - is0;  // the item's partial slot
     bool bad = gs0 < 0 || members <= 0 || gs0 + members > a.B || nm < 1 || nm > members || nm * a.G > 8 ||
-               nb < 1 || nb > 64 || j0 < 0 || p < 0 || p >= a.max_parts || is0 < 0 ||
-               a.seg_group_items[k + 1] <= static_cast<int>(blockIdx.x) || a.seg_group_items[k + 1] > a.n_seg_items;
+               nb < 1 || nb > 64 || j0 < 0 || p >= a.max_parts;
     const int mi = lane < nm ? static_cast<int>((mlist >> (4 * lane)) & 15u) : 0;
     bad = bad || __any_sync(FULL, lane < nm && mi >= members);
     if (bad) {
@@ -1107,16 +1103,18 @@ __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce_grouped(const
 
 // The segment form: one CTA per (sequence b, kv head g), a warp per query
 // head.  Sequence b is member m of group k; its partials are the slots of the
-// group's items that list m (lane i looks at item i of a chunk of 32), merged
-// with log-sum-exp weights in slot order.  A member no item lists gets zero
-// rows.
+// items that list it.  The items are the caller's input, so each warp finds
+// those slots before the decode kernel's partials are complete (it is
+// launched early as a programmatic dependent): lane j ends up holding the
+// j-th one.  After the wait the partials merge with log-sum-exp weights in
+// item order, in one round trip when there are at most 32 (else chunk by
+// chunk).  A member no item lists gets zero rows.
 template <typename QT, int D>
 __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce_segments(const DecodeArgs a) {
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int V = D / 32;
   const int b = static_cast<int>(blockIdx.x) / a.Hkv, g = static_cast<int>(blockIdx.x) - b * a.Hkv;
   const int h = g * a.G + static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
-  dev::grid_dependency_wait();  // partials of decode_main are complete and visible
   if (a.group_start[0] > b || a.group_start[a.n_groups] <= b) return;  // in no group: not served
   int lo = 0, hi = a.n_groups;  // the group k with group_start[k] <= b < group_start[k + 1]
   while (hi - lo > 1) {
@@ -1124,25 +1122,38 @@ __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce_segments(cons
     if (a.group_start[mid] <= b) lo = mid; else hi = mid;
   }
   const int m = b - a.group_start[lo];
-  const int is0 = a.seg_group_items[lo];
-  // the group's items, within the item array and the member's slots
-  const int n = is0 < 0 || is0 > a.n_seg_items ? 0
-                                                : min(min(a.seg_group_items[lo + 1], a.n_seg_items) - is0, a.max_parts);
+  // item i (lane i of a chunk) lists member m: its slot, else -1
+  auto slot_of = [&](int i) {
+    if (i >= a.n_seg_items) return -1;
+    const int4 it = a.seg_items[i];
+    const int nm = (it.w >> 8) & 0xff, slot = (it.w >> 16) & 0xffff;
+    if (it.x != lo || slot >= a.max_parts) return -1;
+    for (int j = 0; j < nm && j < 8; ++j)
+      if (static_cast<int>((static_cast<uint32_t>(it.y) >> (4 * j)) & 15u) == m) return slot;
+    return -1;
+  };
+  int mine = -1, count = 0;
+  for (int c0 = 0; c0 < a.n_seg_items; c0 += 32) {
+    const int s = slot_of(c0 + lane);
+    const unsigned vm = __ballot_sync(FULL, s >= 0);
+    const int k = lane - count;  // this lane takes the chunk's k-th listed slot
+    const bool take = k >= 0 && k < __popc(vm);
+    const int got = __shfl_sync(FULL, s, take ? static_cast<int>(__fns(vm, 0, k + 1)) : lane);
+    if (take) mine = got;
+    count += __popc(vm);
+  }
+  dev::grid_dependency_wait();  // partials of decode_main are complete and visible
   const size_t row0 = (static_cast<size_t>(b) * a.Hq + h) * a.max_parts;
   const float* po = a.part_o + row0 * D + lane * V;
   float M = -INFINITY, ls = 0.f, acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  for (int c0 = 0; c0 < n; c0 += 32) {
-    const int i = c0 + lane;
-    bool valid = false;
-    if (i < n) {
-      const int4 it = a.seg_items[is0 + i];
-      const int nm = (it.w >> 8) & 0xff;
-      for (int j = 0; j < nm && j < 8; ++j) valid |= static_cast<int>((static_cast<uint32_t>(it.y) >> (4 * j)) & 15u) == m;
-    }
-    const float mv = valid ? __ldcg(a.part_m + row0 + i) : -INFINITY;
-    const float lv = valid ? __ldcg(a.part_l + row0 + i) : 0.f;
+  const int chunks = count <= 32 ? 1 : (a.n_seg_items + 31) / 32;
+  for (int c = 0; c < chunks && count > 0; ++c) {
+    const int slot = count <= 32 ? mine : slot_of(32 * c + lane);
+    const bool valid = slot >= 0;
+    const float mv = valid ? __ldcg(a.part_m + row0 + slot) : -INFINITY;
+    const float lv = valid ? __ldcg(a.part_l + row0 + slot) : 0.f;
     float cm = mv;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, off));
@@ -1163,8 +1174,9 @@ __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce_segments(cons
       float x[8][V];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
+        const int sj = __shfl_sync(FULL, slot, q0 + j);
         if ((vm >> (q0 + j)) & 1u) {
-          const float* src = po + static_cast<size_t>(c0 + q0 + j) * D;
+          const float* src = po + static_cast<size_t>(sj) * D;
           if constexpr (V == 4) {
             const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
             x[j][0] = t.x; x[j][1] = t.y; x[j][2] = t.z; x[j][3] = t.w;
@@ -1257,7 +1269,6 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
   a.pre_parts = l.plan.pre_parts;
   a.tail_parts = l.plan.tail_parts;
   a.seg_items = l.segments ? reinterpret_cast<const int4*>(l.seg_items) : nullptr;
-  a.seg_group_items = l.seg_group_items;
   a.n_seg_items = l.n_seg_items;
   a.q_start = l.q_start;
   a.q_rows = l.q_rows;
@@ -1293,7 +1304,8 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
     // one CTA per (segment item, kv head), then the merge of each member's items
     cudaError_t e = cudaSuccess;
     if (l.n_seg_items > 0) {
-      const dim3 sgrid(static_cast<unsigned>(l.n_seg_items), static_cast<unsigned>(l.Hkv));
+      // kv heads fastest: the items (listed longest first) are dispatched in order
+      const dim3 sgrid(static_cast<unsigned>(l.Hkv), static_cast<unsigned>(l.n_seg_items));
       const int W = l.plan.item_warps;
       if (W == 4)
         e = launch_dependent(decode_main<KT, QT, D, 4>, sgrid, dim3(128), TL::smem(4), stream, tmK, tmV, a);

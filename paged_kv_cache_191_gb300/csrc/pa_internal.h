@@ -79,11 +79,10 @@ struct DecodeLaunch {
   const int32_t* group_start = nullptr;
   const int32_t* prefix_blocks = nullptr;
   int32_t n_groups = 0, max_members = 0;
-  // segments of groups (pa_decode_append_segments), else null: int32
-  // [n_seg_items][4] items, int32 [n_groups + 1] item ranges
+  // segments of groups (pa_decode_append_segments): int32 [n_seg_items][4]
+  // items
   int32_t segments = 0;
   const int32_t* seg_items = nullptr;
-  const int32_t* seg_group_items = nullptr;
   int32_t n_seg_items = 0;
   // rows of a multi-token call (pa_chunked_prefill): sequence b's n_b query
   // tokens are rows q_start[b] .. of q_rows, one grid column per token up to

@@ -90,8 +90,9 @@ SIGNATURES = {
                                            _P, C.c_size_t, _I32, _P]),
     "pa_decode_segments_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32, C.POINTER(CacheDesc)]),
     "pa_decode_append_segments": (C.c_int, [_P, _P, _I32, _P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32,
-                                            _I32, _I32, _F, _P, _I32, _I32, _P, _P, _I32, _I32, _P, _I32,
+                                            _I32, _I32, _F, _P, _I32, _I32, _P, _I32, _I32, _P, _I32,
                                             C.POINTER(CacheDesc), _P, C.c_size_t, _P]),
+    "pa_table_segments": (C.c_int, [_P, _I32, _P, _P, _I32, _I32, _P, _I32, _P, _P]),
     "pa_chunked_prefill_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32, C.POINTER(CacheDesc),
                                                        _I32]),
     "pa_chunked_prefill": (C.c_int, [_P, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
@@ -398,23 +399,22 @@ def decode_append_grouped(k_new, v_new, slot_mapping, q, k_cache, v_cache, block
 
 
 def decode_append_segments(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables, context_lens,
-                           max_context_len, scale, group_start, items, group_items, max_group_size, max_group_items,
+                           max_context_len, scale, group_start, items, max_group_size, max_group_items,
                            out=None, out_dtype=None, k_scale=None, v_scale=None, workspace=None, stream=None):
     """decode_append over groups whose members share blocks in any pattern:
-    items (int32 [n_items, 4], device) lists, per group, the runs of table
-    positions a subset of the members all hold (shared_table_segments builds
-    them); group_items (int32 [n_groups + 1], device) delimits each group's
-    items.  Each block is read once for every member that holds it."""
+    items (int32 [n_items, 4], device) lists the runs of table positions a
+    subset of a group's members all hold, each with its partial slot
+    (shared_table_segments builds them).  Each block is read once for every
+    member that holds it."""
     for t, n in ((k_new, "k_new"), (v_new, "v_new"), (slot_mapping, "slot_mapping"), (q, "q"),
                  (k_cache, "k_cache"), (v_cache, "v_cache"), (block_tables, "block_tables"),
-                 (context_lens, "context_lens"), (group_start, "group_start"), (items, "items"),
-                 (group_items, "group_items")):
+                 (context_lens, "context_lens"), (group_start, "group_start"), (items, "items")):
         _dev(t, n)
     desc = cache_desc(k_cache)
     B, Hq, D = q.shape
     n_groups = group_start.numel() - 1
-    if group_start.dtype != torch.int32 or group_items.dtype != torch.int32 or group_items.numel() != n_groups + 1:
-        raise ValueError("group_start and group_items must be int32 [n_groups + 1]")
+    if group_start.dtype != torch.int32:
+        raise ValueError("group_start must be int32 [n_groups + 1]")
     if items.dtype != torch.int32 or items.dim() != 2 or items.shape[1] != 4:
         raise ValueError("items must be int32 [n_items, 4]")
     if k_new.shape != (B, desc.num_kv_heads, D) or v_new.shape != k_new.shape or k_new.dtype != v_new.dtype:
@@ -440,80 +440,41 @@ def decode_append_segments(k_new, v_new, slot_mapping, q, k_cache, v_cache, bloc
         _ptr(k_new), _ptr(v_new), _TORCH_DT[k_new.dtype], _ptr(slot_mapping), _ptr(q), _TORCH_DT[q.dtype],
         _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), int(max_context_len), B, Hq, float(scale), _ptr(group_start), n_groups,
-        int(max_group_size), _ptr(items), _ptr(group_items), items.shape[0], int(max_group_items), _ptr(out),
+        int(max_group_size), _ptr(items), items.shape[0], int(max_group_items), _ptr(out),
         _TORCH_DT[odt], C.byref(desc), _ptr(workspace), ws_bytes, _stream(stream)), "pa_decode_append_segments")
     return out
 
 
 def shared_table_segments(block_tables, context_lens, group_start, blocks_per_item=32):
-    """Host helper for decode_append_segments: the items of each group.  At
-    table position j, the members of a group whose blocks there are the same
-    physical block form a class (a member alone at its last block, which
-    takes this step's token, and wherever it holds a block no other member
-    does); a segment is a maximal run of positions over which a class stays
-    the same, and it is cut into items of at most blocks_per_item (<= 64)
-    blocks.  block_tables int [B, max_blocks], context_lens int [B],
-    group_start int [n + 1] covering 0 .. B-1.  Returns (items int32
-    [n_items, 4] = {group, member list (4 bits per member index), first
-    block, n_blocks | n_members << 8}, group_items int32 [n + 1])."""
+    """Host helper for decode_append_segments (pa_table_segments): the items
+    of the groups.  At table position j, the members of a group whose blocks
+    there are the same physical block form a class (a member alone at and
+    after its last block, which takes this step's token); a segment is a
+    maximal run of positions over which a class stays the same, cut into
+    items of at most blocks_per_item (<= 64) blocks.  A group's items take
+    slots 0, 1, ... in the order (lowest member, position); the list is
+    sorted longest first.  block_tables int [B, max_blocks], context_lens int
+    [B], group_start int [n + 1].  Returns (items int32 [n_items, 4] =
+    {group, member list (4 bits per member index), first block,
+    n_blocks | n_members << 8 | slot << 16}, the most slots of one group)."""
     import numpy as np
-    if not 1 <= blocks_per_item <= 64:
-        raise ValueError("blocks_per_item must be in 1 .. 64")
-    tables = np.asarray(block_tables)
-    lens = np.asarray(context_lens).astype(np.int64)
-    gs = np.asarray(group_start).astype(np.int64)
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    gs = np.ascontiguousarray(group_start, dtype=np.int32)
+    if tables.ndim != 2 or lens.shape != (tables.shape[0],):
+        raise ValueError("block_tables must be [B, max_blocks] and context_lens [B]")
     n = len(gs) - 1
-    sizes = np.diff(gs)
-    if n <= 0:
-        return np.zeros((0, 4), np.int32), np.zeros(max(n, 0) + 1, np.int32)
-    M = int(sizes.max())
-    if M > 8:
-        raise ValueError("groups of at most 8 members")
-    nblk_all = (lens + BLOCK_SIZE - 1) // BLOCK_SIZE
-    P = max(int(nblk_all[gs[0]:gs[-1]].max()) if gs[-1] > gs[0] else 0, 1)
-    # member m of group k is sequence gs[k] + m (padding: inactive)
-    mem = np.arange(M)[None, :]
-    valid = mem < sizes[:, None]                                   # [n, M]
-    seq = np.where(valid, gs[:-1, None] + mem, gs[0])
-    T = tables[seq, :P]                                            # [n, M, P]
-    L = np.where(valid, lens[seq], 0)
-    nblk = (L + BLOCK_SIZE - 1) // BLOCK_SIZE
-    last = np.where(L > 0, (L - 1) // BLOCK_SIZE, -1)
-    pos = np.arange(P)[None, None, :]
-    active = pos < nblk[:, :, None]                                # [n, M, P]
-    share = pos < last[:, :, None]                                 # positions a member may share
-    eq = (T[:, :, None, :] == T[:, None, :, :]) & (share[:, :, None, :] & share[:, None, :, :])
-    eq |= np.eye(M, dtype=bool)[None, :, :, None] & active[:, :, None, :]
-    bits = (1 << np.arange(M)).astype(np.int64)
-    cls = (eq * bits[None, None, :, None]).sum(axis=2)             # [n, M, P]: class of member m at j (0: inactive)
-    chg = np.ones((n, M, P), dtype=bool)
-    chg[:, :, 1:] = cls[:, :, 1:] != cls[:, :, :-1]
-    owner = (cls & -cls) == bits[None, :, None]                    # m is the class's lowest member
-    starts = chg & (cls != 0) & owner
-    # next class change after each position (P if none)
-    idx = np.where(chg, np.arange(P)[None, None, :], P)
-    nxt = np.minimum.accumulate(idx[:, :, ::-1], axis=-1)[:, :, ::-1]
-    nxt_gt = np.concatenate([nxt[:, :, 1:], np.full((n, M, 1), P)], axis=-1)
-    k, m, j0 = np.nonzero(starts)                                  # sorted by group, then member, then position
-    c = cls[k, m, j0]
-    j1 = nxt_gt[k, m, j0]
-    # member lists: indices of the class's members, 4 bits each
-    mbits = (c[:, None] >> np.arange(M)[None, :]) & 1              # [s, M]
-    nm = mbits.sum(axis=1)
-    rank = np.cumsum(mbits, axis=1) - 1
-    mlist = (mbits * (np.arange(M)[None, :] << (4 * np.maximum(rank, 0)))).sum(axis=1)
-    # cut into items of at most blocks_per_item blocks
-    npieces = (j1 - j0 + blocks_per_item - 1) // blocks_per_item
-    rep_ = np.repeat(np.arange(len(k)), npieces)
-    piece = np.arange(int(npieces.sum())) - np.repeat(np.cumsum(npieces) - npieces, npieces)
-    it_j0 = j0[rep_] + piece * blocks_per_item
-    it_nb = np.minimum(blocks_per_item, j1[rep_] - it_j0)
-    items = np.stack([k[rep_], mlist[rep_], it_j0, it_nb | (nm[rep_] << 8)], axis=1).astype(np.int32)
-    order = np.argsort(items[:, 0], kind="stable")
-    items = np.ascontiguousarray(items[order])
-    gi = np.zeros(n + 1, dtype=np.int32)
-    np.cumsum(np.bincount(items[:, 0], minlength=n), out=gi[1:])
-    return items, gi
+    if n < 0 or (n > 0 and (gs[0] < 0 or gs[-1] > tables.shape[0])):
+        raise ValueError("group_start out of range")
+    cap = int(((lens.astype(np.int64) + BLOCK_SIZE - 1) // BLOCK_SIZE).sum()) + 1
+    items = np.empty((cap, 4), dtype=np.int32)
+    count, most = C.c_int32(), C.c_int32()
+    st = lib().pa_table_segments(tables.ctypes.data_as(C.c_void_p), tables.shape[1], lens.ctypes.data_as(C.c_void_p),
+                                 gs.ctypes.data_as(C.c_void_p), n, int(blocks_per_item),
+                                 items.ctypes.data_as(C.c_void_p), cap, C.byref(count), C.byref(most))
+    if st != PA_OK:
+        raise ValueError(lib().pa_last_error().decode())
+    return items[:count.value].copy(), most.value
 
 
 def prefix_groups(block_tables, context_lens, max_group_size):

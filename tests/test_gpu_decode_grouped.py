@@ -234,12 +234,11 @@ def test_shared_prefix_16x4_full_size():
         # store the same rows again
         plain = ops.decode_append(nk.to(DEV), nv.to(DEV), sl, q, kc, vc, bt, cl, ml, w.scale,
                                   out_dtype=torch.float32)
-        items, gi = ops.shared_table_segments(tables, lens, gs_host)
+        items, most = ops.shared_table_segments(tables, lens, gs_host)
         nm = (items[:, 3] >> 8) & 0xff
         total_pairs += int(((nm > 1) & (nm < beams)).sum())
         seg = ops.decode_append_segments(nk.to(DEV), nv.to(DEV), sl, q, kc, vc, bt, cl, ml, w.scale, gs,
-                                         torch.from_numpy(items).to(DEV), torch.from_numpy(gi).to(DEV), beams,
-                                         int(np.diff(gi).max()), out_dtype=torch.float32)
+                                         torch.from_numpy(items).to(DEV), beams, most, out_dtype=torch.float32)
         torch.cuda.synchronize()
         okc, ovc, _, _ = o_write(np_exact(nk), np_exact(nv), np.array(slots), okc, ovc)
         ref = paged_decode(np_exact(w.q), okc, ovc, tables, lens, w.scale)

@@ -61,7 +61,7 @@ def tree_case(seed, Hq, Hkv, kv, D=128, groups=3, size=4, prompt=5, zero=()):
     return w, start
 
 
-def run(w, start, bpi=32, plain=False, items=None, gi=None, max_items=None):
+def run(w, start, bpi=32, plain=False, items=None, max_items=None):
     rng = W.rng_for(17)
     q = w.q.to(torch.bfloat16) if w.kv_dtype == "bf16" else w.q
     k_new = W.randn(rng, (w.B, w.Hkv, w.D), q.dtype).to(DEV)
@@ -75,14 +75,14 @@ def run(w, start, bpi=32, plain=False, items=None, gi=None, max_items=None):
         out = ops.decode_append(k_new, v_new, sl, q.to(DEV), kc, vc, bt, cl, ml, w.scale, out_dtype=torch.float32,
                                 k_scale=ks, v_scale=vs)
     else:
+        most = None
         if items is None:
-            items, gi = ops.shared_table_segments(w.block_tables, w.context_lens, start, bpi)
-        mi = max_items or max(int(np.diff(gi).max()), 1)
+            items, most = ops.shared_table_segments(w.block_tables, w.context_lens, start, bpi)
+        mi = max_items or max(most or 0, 1)
         out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32, device=DEV)
         ops.decode_append_segments(k_new, v_new, sl, q.to(DEV), kc, vc, bt, cl, ml, w.scale,
                                    torch.from_numpy(start).to(DEV), torch.from_numpy(items).to(DEV).view(-1, 4),
-                                   torch.from_numpy(gi).to(DEV), int(np.diff(start).max()), mi, out=out,
-                                   k_scale=ks, v_scale=vs)
+                                   int(np.diff(start).max()), mi, out=out, k_scale=ks, v_scale=vs)
     torch.cuda.synchronize()
     return out.cpu().numpy(), [t.cpu() if t is not None else None for t in (kc, vc, ks, vs)], (k_new, v_new, q)
 
@@ -103,7 +103,7 @@ CASES = [  # Hq, Hkv, kv, group size, items of at most bpi blocks
 def test_segments_match_oracle_and_plain(Hq, Hkv, kv, size, bpi):
     D = 64 if (Hq, Hkv) == (4, 4) else 128
     w, start = tree_case(70 + Hq + Hkv + size, Hq, Hkv, kv, D=D, size=size)
-    items, gi = ops.shared_table_segments(w.block_tables, w.context_lens, start, bpi)
+    items, _ = ops.shared_table_segments(w.block_tables, w.context_lens, start, bpi)
     if size > 1:  # the tree is exercised: items shared by the whole group and by pairs
         nms = (items[:, 3] >> 8) & 0xff
         assert (nms == size).any() and ((nms > 1) & (nms < size)).any() or size == 2
@@ -123,6 +123,18 @@ def test_segments_match_oracle_and_plain(Hq, Hkv, kv, size, bpi):
     assert_close(got, ref, TOL[kv], f"segments {Hq}/{Hkv} {kv} size {size} bpi {bpi}")
 
 
+def test_members_in_more_than_32_items():
+    """One-block items over a 40-block prompt: every member is listed by more
+    than 32 items, which the merge takes chunk by chunk."""
+    w, start = tree_case(85, 8, 8, "f16", prompt=40)
+    items, _ = ops.shared_table_segments(w.block_tables, w.context_lens, start, 1)
+    got, _, (k_new, v_new, q) = run(w, start, bpi=1)
+    okc, ovc, _, _ = o_write(np_exact(k_new.cpu()), np_exact(v_new.cpu()), last_slots(w), np_exact(w.k_pool),
+                             np_exact(w.v_pool))
+    ref = paged_decode(np_exact(q), okc, ovc, w.block_tables, w.context_lens, w.scale)
+    assert_close(got, ref, TOL["f16"], "one-block items")
+
+
 def test_empty_member_and_no_items():
     """An empty member is in no item and gets zero rows; with no items at all
     every row is zero."""
@@ -134,18 +146,22 @@ def test_empty_member_and_no_items():
     assert_close(got, paged_decode(np_exact(q), okc, ovc, w.block_tables, w.context_lens, w.scale), TOL["f16"],
                  "empty member")
     none = np.zeros((0, 4), np.int32)
-    got, _, _ = run(w, start, items=none, gi=np.zeros(len(start), np.int32), max_items=4)
+    got, _, _ = run(w, start, items=none, max_items=4)
     assert np.all(got == 0.0)
 
 
 def test_bad_items_and_differing_blocks_are_flagged():
     w, start = tree_case(83, 8, 8, "f16")
-    items, gi = ops.shared_table_segments(w.block_tables, w.context_lens, start, 32)
+    items, most = ops.shared_table_segments(w.block_tables, w.context_lens, start, 32)
     bad = items.copy()
     k = int(np.argmax((bad[:, 3] >> 8) & 0xff))
     bad[k, 1] = (bad[k, 1] & ~0xf) | 9  # member 9 of a group of 4
-    run(w, start, items=bad, gi=gi)
+    run(w, start, items=bad, max_items=most)
+    assert ops.device_errors(clear=True) & ops.DEVERR_GROUP
+    bad = items.copy()
+    bad[0, 3] = (bad[0, 3] & 0xffff) | (most << 16)  # a slot past the bound
+    run(w, start, items=bad, max_items=most)
     assert ops.device_errors(clear=True) & ops.DEVERR_GROUP
     w.block_tables[1, 0] = w.block_tables[1, w.context_lens[1] // 16 - 1]  # member 1 leaves the prompt's block 0
-    run(w, start, items=items, gi=gi)
+    run(w, start, items=items, max_items=most)
     assert ops.device_errors(clear=True) & ops.DEVERR_GROUP

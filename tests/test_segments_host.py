@@ -41,11 +41,16 @@ def segments_by_definition(tables, lens, gs, bpi):
 
 
 def decode_items(items):
+    """(group, members, first block, blocks) of each item, sorted."""
     res = []
     for k, ml, j0, w in items.tolist():
         nm = (w >> 8) & 0xff
         res.append((k, tuple(((ml & 0xffffffff) >> (4 * i)) & 15 for i in range(nm)), j0, w & 0xff))
     return sorted(res)
+
+
+def slots_of(items):
+    return [((w & 0xffffffff) >> 16) & 0xffff for w in items[:, 3].tolist()]
 
 
 def tree_tables(rng, n_groups, size, prompt_blocks, max_tail):
@@ -77,10 +82,19 @@ def tree_tables(rng, n_groups, size, prompt_blocks, max_tail):
 def test_segments_match_their_definition(seed, size, bpi):
     rng = np.random.default_rng(seed)
     tables, lens, gs = tree_tables(rng, 5, size, int(rng.integers(0, 9)), 5)
-    items, gi = ops.shared_table_segments(tables, lens, gs, bpi)
+    items, most = ops.shared_table_segments(tables, lens, gs, bpi)
     assert decode_items(items) == segments_by_definition(tables, lens, gs, bpi)
-    assert gi[0] == 0 and gi[-1] == len(items) and (np.diff(items[:, 0]) >= 0).all()
-    assert all(gi[k] <= i < gi[k + 1] for i, k in enumerate(items[:, 0]))
+    # longest first; a group's items hold slots 0 .. n_k - 1, in (owner, position) order
+    nb = items[:, 3] & 0xff
+    assert (np.diff(nb) <= 0).all()
+    slots = slots_of(items)
+    for k in range(len(gs) - 1):
+        mine = [i for i in range(len(items)) if items[i, 0] == k]
+        assert sorted(slots[i] for i in mine) == list(range(len(mine)))
+        by_slot = sorted(mine, key=lambda i: slots[i])
+        firsts = [(int(items[i, 1]) & 15, int(items[i, 2])) for i in by_slot]
+        assert firsts == sorted(firsts)
+    assert most == max(np.bincount(items[:, 0], minlength=len(gs) - 1))
 
 
 def test_every_block_is_read_once():
@@ -91,7 +105,7 @@ def test_every_block_is_read_once():
     rng = np.random.default_rng(9)
     tables, lens, gs = tree_tables(rng, 6, 4, 12, 6)
     lens[3] = 0  # an empty member holds nothing
-    items, gi = ops.shared_table_segments(tables, lens, gs, 8)
+    items, _ = ops.shared_table_segments(tables, lens, gs, 8)
     seen = {}
     for k, ml, j0, nb, members in ((k, ml, j0, nb, m) for k, ml, j0, nb_w in items.tolist()
                                    for nb, m in [(nb_w & 0xff, [((ml & 0xffffffff) >> (4 * i)) & 15
@@ -121,7 +135,7 @@ def test_shared_last_block_is_read_per_member():
     """Two members claiming the same block at their last position (a missed
     copy on write) read it separately: the fused write lands there."""
     tables = np.array([[7, 8], [7, 8]], np.int32)
-    items, gi = ops.shared_table_segments(tables, np.array([20, 25]), np.array([0, 2]), 32)
+    items, _ = ops.shared_table_segments(tables, np.array([20, 25]), np.array([0, 2]), 32)
     assert decode_items(items) == [(0, (0,), 1, 1), (0, (0, 1), 0, 1), (0, (1,), 1, 1)]
 
 
