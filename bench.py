@@ -21,6 +21,7 @@ oracle on host cores instead (bounded sample per step).
 """
 import argparse
 import ctypes as C
+import gc
 import hashlib
 import json
 import math
@@ -696,9 +697,12 @@ class SharedPrefixStep(DecodeStep):
             if st:
                 self.ops._check(st, "pa_copy_blocks")
         if self.fused and self.grouped and self.segments:
+            # the argument tuple is built before the start event: nothing that
+            # allocates (and may run the garbage collector) sits between the
+            # event and the launch
+            self.last_seg_args = self.seg_call_args(i)
             if ev_pair is not None:
                 drv.record(ev_pair[0], sp)
-            self.last_seg_args = self.seg_call_args(i)
             st = L.pa_decode_append_segments(*self.last_seg_args)
             if st:
                 self.ops._check(st, "pa_decode_append_segments")
@@ -811,6 +815,10 @@ def time_steps(st, shared, stream, args, world):
         torch.cuda.synchronize()
         dec_b = step_b = 0
         st.blocked_s = 0.0
+        # no garbage-collector pause inside the timed steps: a pause between a
+        # launch's start event and its submission would count in its time
+        gc_was = gc.isenabled()
+        gc.disable()
         wall0 = time.time()
         st.drv.record(t_start, st.sp)
         for i in range(args.steps):
@@ -821,6 +829,8 @@ def time_steps(st, shared, stream, args, world):
             st.enqueue(buf, dec_events[i])
         st.drv.record(t_end, st.sp)
         host_done = time.time()
+        if gc_was:
+            gc.enable()
         if shared:
             dec_b, step_b, r["dec_logical"] = st.count_bytes()
             r["copies"] = sum(h[2] for h in st.history) / args.steps
@@ -1353,6 +1363,8 @@ def run_prefill(args, rank, world, local_rank):
         stream.synchronize()
         barrier(world)
         torch.cuda.synchronize()
+        gc_was = gc.isenabled()
+        gc.disable()  # no collector pause between a launch's start event and its submission
         wall0 = time.time()
         t0e.record(stream)
         for i in range(args.steps):
@@ -1360,6 +1372,8 @@ def run_prefill(args, rank, world, local_rank):
         t1e.record(stream)
         stream.synchronize()
         wall1 = time.time()
+        if gc_was:
+            gc.enable()
     torch.cuda.synchronize()
     barrier(world)
     clocks.stop()
