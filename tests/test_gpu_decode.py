@@ -206,6 +206,25 @@ def test_fp8_small(qdt, split, fmt):
     assert np.abs(got - ref16).max() < 0.25
 
 
+@pytest.mark.parametrize("qscale", [300.0, 1e-3, 0.0])
+@pytest.mark.parametrize("qdt", ["f16", "bf16"])
+def test_fp8_query_range(qscale, qdt):
+    """Over an E4M3 cache, query rows far outside E4M3's range (|q| up to
+    ~1200, beyond its 448) or deep in its subnormals (|q| ~ 1e-3), and
+    all-zero rows, match the oracle: Q stays in its own 16-bit type and only
+    the cache's codes are converted."""
+    w = W.random_small(53, B=4, Hq=16, Hkv=4, D=128, kv_dtype="fp8", max_len=300)
+    q = w.q.float() * qscale
+    q[1, 3] = 0.0  # one all-zero row among the others
+    w.q = q.to(torch.bfloat16 if qdt == "bf16" else torch.float16)
+    kc, vc, ks, vs = fp8_pool_gpu(w)
+    (okc, ovc, oks, ovs), _ = fp8_pool_oracle(w)
+    ref = paged_decode(np_exact(w.q), okc, ovc, w.block_tables, w.context_lens, w.scale, oks, ovs)
+    got = gpu_decode(w, pools=(kc, vc), scales=(ks, vs)).numpy()
+    assert np.isfinite(got).all()
+    assert_close(got, ref, TOL["fp8"], f"q x {qscale} {qdt}")
+
+
 # ---- full-size workloads, every row ------------------------------------------------
 @pytest.mark.parametrize("cfg", ["llama7b_b32", "gqa70b_b64", "longctx_b8_f16"])
 def test_full_size_all_rows(cfg):
