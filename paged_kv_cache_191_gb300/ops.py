@@ -445,7 +445,7 @@ def decode_append_segments(k_new, v_new, slot_mapping, q, k_cache, v_cache, bloc
     return out
 
 
-def shared_table_segments(block_tables, context_lens, group_start, blocks_per_item=32):
+def shared_table_segments(block_tables, context_lens, group_start, blocks_per_item=40):
     """Host helper for decode_append_segments (pa_table_segments): the items
     of the groups.  At table position j, the members of a group whose blocks
     there are the same physical block form a class (a member alone at and
