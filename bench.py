@@ -72,6 +72,9 @@ def parse_args(argv=None):
                         "instead of pa_decode_append_segments (every shared block read once)")
     p.add_argument("--ungrouped", action="store_true",
                    help="shared_prefix_16x4: read shared prompt blocks once per beam (pa_decode_append)")
+    p.add_argument("--fixed-grid", action="store_true",
+                   help="decode batches: always pa_decode_append's fixed grid, never the host-planned list of "
+                        "live partitions that pa_decode_items_plan picks for skewed lengths")
     p.add_argument("--headline-only", action="store_true",
                    help="time only --config (by default every decode workload runs and appears under `workloads`)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -150,15 +153,18 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config):
+def profiled_traffic(config, api):
     """DRAM bytes per decode launch from the committed ncu summary, or None
-    when the kernel source changed since the counters were taken."""
+    when the kernel source changed since the counters were taken or the
+    record is of another entry point (`api`, launch_api())."""
     path = os.path.join(ROOT, "profiles", f"traffic_decode_{config}.txt")
     try:
         kv = dict(line.split(":", 1) for line in open(path) if ":" in line)
     except OSError:
         return None
     if kv.get("kernel_source_sha256_16", "").strip() != kernel_source_hash():
+        return None
+    if kv.get("api", "").strip() != api:
         return None
     try:
         return float(kv["dram_bytes_per_launch"])
@@ -339,11 +345,27 @@ class DecodeStep:
         self.out = torch.empty((self.B, self.Hq, self.D), dtype=w.q.dtype, device=device)
         self.desc = ops.cache_desc(self.kc)
         self.ws_bytes = ops.decode_workspace_size(self.B, self.Hq, self.max_len, self.kc, split_tokens)
-        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        # Items mode (set by build_step when pa_decode_items_plan picks it for
+        # the batch's starting lengths): each step lists the sequences' live
+        # partitions on the host (pa_table_segments over B one-member groups)
+        # and runs pa_decode_append_segments instead of the fixed grid.
+        self.items = False
+        self.items_plan = ops.decode_items_plan(self.lens0, self.Hq, self.max_len, self.kc, split_tokens)
+        _, self.blocks_per_item, self.items_per_seq = self.items_plan
+        sws = int(self.L.pa_decode_segments_workspace_size(self.B, self.Hq, self.B, 1, self.items_per_seq,
+                                                           C.byref(self.desc)))
+        self.ws = torch.empty(max(self.ws_bytes, sws, 16), dtype=torch.uint8, device=device)
         self.split = split_tokens
+        self.group_start_host = np.arange(self.B + 1, dtype=np.int32)
+        self.group_start = torch.from_numpy(self.group_start_host).to(device)
 
         # one pinned meta buffer per ring slot: slots int64[B] | lens int32[B] | tables int32[B, cap]
-        self.meta_bytes = self.B * 8 + self.B * 4 + self.B * self.cap * 4
+        #   | items int32[B * items_per_seq][4] (16-byte aligned; items mode); a step copies the part it uses
+        self.it_off = (self.B * 8 + self.B * 4 + self.B * self.cap * 4 + 15) // 16 * 16
+        self.max_items = self.B * self.items_per_seq
+        self.meta_bytes = self.it_off + self.max_items * 16
+        self.copy_bytes = self.it_off
+        self.n_items, self.n_items_c = 0, C.c_int32()
         self.meta_host = [torch.empty(self.meta_bytes, dtype=torch.uint8).pin_memory()
                           for _ in range(RING)]
         # two device copies of the meta buffer: step i+1's upload (on a copy
@@ -365,7 +387,8 @@ class DecodeStep:
         self.meta_dev = self.meta_devs[i]
         self.slots_dev = self.meta_dev[: self.B * 8].view(self.torch.int64)
         self.lens_dev = self.meta_dev[self.B * 8: self.B * 12].view(self.torch.int32)
-        self.tables_dev = self.meta_dev[self.B * 12:].view(self.torch.int32).view(self.B, self.cap)
+        self.tables_dev = self.meta_dev[self.B * 12: self.B * 12 + self.B * self.cap * 4].view(
+            self.torch.int32).view(self.B, self.cap)
 
     def _admit(self):
         for b in self.ids:
@@ -398,6 +421,14 @@ class DecodeStep:
                                           C.byref(self.ncow)), "pa_append_slots")
         ops._check(self.L.pa_block_tables(self.alloc._h, self.ids_c, self.B, tab_p, self.cap, lens_p),
                    "pa_block_tables")
+        if self.items and buf is not None:
+            ops._check(self.L.pa_table_segments(C.c_void_p(base + self.B * 12), self.cap, C.c_void_p(base + self.B * 8),
+                                                self.group_start_host.ctypes.data_as(C.c_void_p), self.B,
+                                                self.blocks_per_item, C.c_void_p(base + self.it_off),
+                                                self.max_items, C.byref(self.n_items_c), None),
+                       "pa_table_segments")
+            self.n_items = self.n_items_c.value
+            self.copy_bytes = self.it_off + self.n_items * 16
         self.cur_lens += 1
         self.steps_since_reset += 1
         return buf
@@ -428,6 +459,12 @@ class DecodeStep:
             wa, da = self.write_args[-1], self.decode_args[-1]
             # pa_decode_append(k_new, v_new, new_dtype, slot_mapping, <pa_decode args but workspace...>)
             self.append_args.append((wa[0], wa[1], wa[2], wa[3]) + da)
+        # pa_decode_append_segments over one-member groups: no split_tokens;
+        # n_items (index 21) is set per step
+        if self.items:
+            self.item_args = [a[:17] + (C.c_void_p(self.group_start.data_ptr()), self.B, 1,
+                                        C.c_void_p(self.meta_devs[i].data_ptr() + self.it_off), 0,
+                                        self.items_per_seq) + a[17:22] + a[23:] for i, a in enumerate(self.append_args)]
         self.use_meta(0)
         self.dbuf = 0
         self.copy_done = [self.drv.event() for _ in range(2)]
@@ -439,13 +476,21 @@ class DecodeStep:
         L, drv, sp, cp, i = self.L, self.drv, self.sp, self.cp, self.dbuf
         if self.used_rec[i]:            # the kernels that read this device buffer are done
             drv.wait(cp, self.used_done[i])
-        drv.h2d(self.meta_devs[i].data_ptr(), buf.data_ptr(), self.meta_bytes, cp)
+        drv.h2d(self.meta_devs[i].data_ptr(), buf.data_ptr(), self.copy_bytes, cp)
         drv.record(self.ring_ev[self.ring], cp)
         drv.record(self.copy_done[i], cp)
         self.ring_used[self.ring] = True
         self.ring = (self.ring + 1) % RING
         drv.wait(sp, self.copy_done[i])
-        if self.fused:
+        if self.fused and self.items:
+            a = self.item_args[i]
+            self.last_item_args = a[:21] + (self.n_items,) + a[22:]  # built before the start event
+            if ev_pair is not None:
+                drv.record(ev_pair[0], sp)
+            st = L.pa_decode_append_segments(*self.last_item_args)
+            if st:
+                self.ops._check(st, "pa_decode_append_segments")
+        elif self.fused:
             if ev_pair is not None:
                 drv.record(ev_pair[0], sp)
             st = L.pa_decode_append(*self.append_args[i])
@@ -472,21 +517,25 @@ class DecodeStep:
         dec = decode_bytes(lens, self.Hq, self.Hkv, self.D, e, qe, qe)
         write = 2 * self.B * self.Hkv * self.D * (qe + e) + (2 * self.B * 4 if self.fp8 else 0) + self.B * 8
         # the timed launch is decode plus, when fused, the cache write
-        return dec + (write if self.fused else 0), dec + write + self.meta_bytes
+        return dec + (write if self.fused else 0), dec + write + self.it_off
 
-    def step_bytes(self):
-        """(decode bytes, whole-step bytes) of the step just prepared."""
+    def step_bytes(self, items=True):
+        """(decode bytes, whole-step bytes) of the step just prepared (items
+        mode: plus the item list the launch reads and the step copies)."""
         k = self.steps_since_reset  # 1..RESET_EVERY: lengths are lens0 - 1 + k
         if not hasattr(self, "_bytes_table"):
             self._bytes_table = [self._bytes_of(self.lens0 - 1 + j) for j in range(RESET_EVERY + 1)]
-        return self._bytes_table[k]
+        d, s = self._bytes_table[k]
+        if self.items and items:
+            d, s = d + 16 * self.n_items, s + self.copy_bytes - self.it_off
+        return d, s
 
     def launches_per_step(self):
         """Kernels one step launches: the decode call's own count (main kernel,
         plus the merge kernel when the library plans one) and the separate
         cache write when the write is not fused; the grouped and segment
         calls always follow their main kernel with their merge kernel."""
-        if getattr(self, "grouped", False) and self.fused:
+        if (getattr(self, "grouped", False) or self.items) and self.fused:
             return 2
         _, _, kernels = self.ops.decode_plan_info(self.B, self.Hq, self.max_len, self.kc, self.split)
         return kernels + (0 if self.fused else 1)
@@ -506,6 +555,7 @@ class SharedPrefixStep(DecodeStep):
         self.w = w
         self.B, self.Hq, self.Hkv, self.D = w.B, w.Hq, w.Hkv, w.D
         self.fp8 = False
+        self.items = False  # the groups' segment items instead (below)
         self.dev = device
         self.alloc = ops.BlockAllocator(w.num_blocks, w.free_order)
         self.roots = [10 ** 9 + g for g in range(w.groups)]
@@ -795,6 +845,8 @@ def build_step(name, args, dev):
     if shared:
         st.grouped = not args.ungrouped
         st.segments = not args.prefix_groups
+    else:
+        st.items = st.fused and st.items_plan[0] and not args.fixed_grid
     return w, st, shared
 
 
@@ -858,6 +910,8 @@ def decode_call(st):
         if st.segments:
             return st.L.pa_decode_append_segments, st.last_seg_args
         return st.L.pa_decode_append_grouped, st.grouped_args[i]
+    if st.fused and st.items:
+        return st.L.pa_decode_append_segments, st.last_item_args
     if st.fused:
         return st.L.pa_decode_append, st.append_args[i]
     return st.L.pa_decode, st.decode_args[i]
@@ -890,6 +944,15 @@ def clock_windows(st, stream, r):
     return windows, label
 
 
+def launch_api(st, shared):
+    """The entry point a decode workload's timed launch goes through."""
+    if shared and st.fused and st.grouped:
+        return "pa_decode_append_segments" if st.segments else "pa_decode_append_grouped"
+    if st.fused:
+        return "pa_decode_append_segments (one-member groups)" if st.items else "pa_decode_append"
+    return "pa_decode"
+
+
 def launch_kernel_name(st, shared):
     if shared and st.fused and st.grouped and st.segments:
         return ("pa_decode_append_segments (decode_main over the groups' shared-block segments with the fused "
@@ -897,6 +960,9 @@ def launch_kernel_name(st, shared):
     if shared and st.fused and st.grouped:
         return ("pa_decode_append_grouped (decode_main over shared-prefix groups with the fused "
                 "cache write + decode_reduce_grouped)")
+    if st.fused and st.items:
+        return ("pa_decode_append_segments over one-member groups (decode_main over the live partitions the host "
+                "lists with pa_table_segments, fused cache write + decode_reduce_segments)")
     if st.fused:
         return "pa_decode_append (decode_main with the fused cache write + decode_reduce)"
     return "pa_decode (decode_main + decode_reduce)"
@@ -913,7 +979,8 @@ def workload_entry(name, w, st, shared, r, args, peak, clock):
          "ms_per_step": round(r["local_s"] * 1e3 / args.steps, 5),
          "step_gbs": round(r["step_b"] / r["local_s"] / 1e9, 2),
          "gpu_launches": st.launches_per_step() * args.steps + r.get("cow_launches", 0),
-         "kernel": launch_kernel_name(st, shared), "traffic": profiled_traffic(name), "clocks": clock}
+         "kernel": launch_kernel_name(st, shared), "api": launch_api(st, shared),
+         "traffic": profiled_traffic(name, launch_api(st, shared)), "clocks": clock}
     if shared:
         e["bytes"] = "unique physical bytes (shared blocks once per step)"
         e["logical_kv_gbs"] = round(r["dec_logical"] / args.steps / (r["dec_ms"] / 1e3) / 1e9, 2)
@@ -947,7 +1014,7 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = hbm_peak()
     avg_dec_bytes = dec_b / args.steps
     achieved = avg_dec_bytes / (dec_ms / 1e3) / 1e9
-    traffic = profiled_traffic(args.config)
+    traffic = profiled_traffic(args.config, launch_api(st, shared))
     head_entry = workload_entry(args.config, w, st, shared, r, args, peak, None)
     launches = head_entry["gpu_launches"]
     del st
@@ -1017,7 +1084,7 @@ def run_ours(args, rank, world, local_rank):
         "pct_of_nominal_8TBs": round(100 * tot_bytes / max_s / 1e9 / NOMINAL_HBM_GBS, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "traffic": traffic, "kernel": head_entry["kernel"],
+                     "traffic": traffic, "kernel": head_entry["kernel"], "api": head_entry["api"],
                      "bytes_per_launch": int(avg_dec_bytes), "launch_ms": round(dec_ms, 5)},
         "timing": timing,
         "e2e": e2e,
@@ -1052,8 +1119,7 @@ def timing_detail(st, stream, dec_ms, reps=100):
     events), back to back on the stream, and replayed from a CUDA graph."""
     torch = st.torch
     L, drv, sp = st.L, st.drv, st.sp
-    args = st.append_args[st.dbuf ^ 1] if st.fused else st.decode_args[st.dbuf ^ 1]
-    fn = L.pa_decode_append if st.fused else L.pa_decode
+    fn, args = decode_call(st)
     out = {"per_launch_ms": pct(dec_ms)}
     l2 = int(getattr(torch.cuda.get_device_properties(st.dev), "L2_cache_size", 128 << 20))
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=st.dev)
@@ -1145,31 +1211,37 @@ def run_e2e(st, args, stream):
     if not isinstance(st, SharedPrefixStep):
         from paged_kv_cache_191_gb300.session import DecodeSession
         sess = DecodeSession(st.kc, st.vc, st.B, st.Hq, st.cap, st.max_len, st.w.scale, st.q.dtype,
-                             k_scale=st.ks, v_scale=st.vs, split_tokens=st.split)
+                             k_scale=st.ks, v_scale=st.vs, split_tokens=st.split,
+                             items="auto" if st.items else False)
         for r in range(sess.ring):  # the model's outputs for the step (the same every step here)
             q, k, v = sess.inputs(slot=r)
             q.copy_(st.w.q)
             k.copy_(st.w.new_k)
             v.copy_(st.w.new_v)
-        total_b = 0
+        total_b = h2d_b = listed = 0
         with torch.cuda.stream(stream):
             stream.synchronize()
             t0 = time.perf_counter()
             st.host_prepare(sess.meta_ptrs())
             for k in range(n):
-                _, s = st.step_bytes()
-                total_b += s
+                _, s = st.step_bytes(items=False)
                 h = sess.launch(stream)
+                total_b += s + sess.last_copy_bytes - sess.nbytes  # the session's item list, when it lists
+                h2d_b += sess.last_copy_bytes
+                listed += sess.last_items is not None
                 if k + 1 < n:  # the block manager prepares the next step while this one runs
                     st.host_prepare(sess.meta_ptrs())
                 out = sess.wait(h)
             t1 = time.perf_counter()
         return {"value": round(total_b / (t1 - t0) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": int(sess.nbytes), "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+                "h2d_bytes_per_step": int(h2d_b // n), "d2h_bytes_per_step": int(out.numel() * out.element_size()),
                 "steps": n, "tokens_per_s": round(st.B * n / (t1 - t0), 1),
+                "steps_with_item_list": listed,
                 "api": "paged_kv_cache_191_gb300.session.DecodeSession (block manager writes into a pinned staging "
                        "buffer beside q / k_new / v_new, the next step's while the current one runs; one H2D copy, "
-                       "pa_decode_append, one D2H copy of the output, waited for every step)"}
+                       "pa_decode_append -- or, when pa_decode_items_plan picks it for the step's lengths, the "
+                       "live partitions listed by pa_table_segments and pa_decode_append_segments -- one D2H copy "
+                       "of the output, waited for every step)"}
     # Shared-prefix beam search: the timed step's own path (block manager ->
     # pinned metadata with the groups' prefixes -> one copy; copy-on-write
     # copies; the grouped fused decode) plus the model's inputs from pinned

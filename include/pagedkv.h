@@ -286,7 +286,9 @@ pa_status pa_decode_append_grouped(const void* k_new, const void* v_new, int32_t
  * tables).  Each item reads its blocks once and scores them against the
  * queries of every member it lists; a merge kernel combines each member's
  * items.  It computes what pa_decode_append computes, up to rounding (the
- * partitions differ), reading each block of the batch once.
+ * partitions differ), reading each block of the batch once.  A batch without
+ * shared blocks is B one-member groups: its items are then the sequences'
+ * live partitions (pa_decode_items_plan says when that beats the fixed grid).
  *
  * group_start   device int32 [n_groups + 1], as for pa_decode_append_grouped;
  *               the groups cover sequences 0 .. B-1.
@@ -353,6 +355,35 @@ pa_status pa_table_segments(const int32_t* block_tables, int32_t max_blocks, con
 size_t pa_decode_segments_workspace_size(int32_t B, int32_t num_q_heads, int32_t n_groups,
                                          int32_t max_group_size, int32_t max_group_items,
                                          const pa_cache_desc* desc);
+
+/*
+ * pa_decode_items_plan -- whether a batch without shared blocks decodes
+ * faster as a host-planned list of its live partitions than over
+ * pa_decode_append's fixed grid (host only; nothing is launched).  The fixed
+ * grid gives every sequence max_parts partitions per kv head (a block table
+ * maps only the blocks below a sequence's length, [LLM-INF] 2.2), and the
+ * cells past a short sequence's end exit at once;
+ * with skewed lengths most cells are empty.  The list is B one-member groups
+ * (group_start = 0, 1, ..., B) for pa_decode_append_segments, whose items
+ * pa_table_segments cuts from each sequence's length -- the same partitions,
+ * none empty.
+ *
+ * context_lens  host int32 [B], 0 .. max_context_len: this step's lengths.
+ * Other inputs as pa_decode_plan_info.
+ * *use_items    out: 1 when fewer than half of the fixed grid's cells hold
+ *               blocks, the split has more than one partition and G <= 8
+ *               (measured on GB300: 28 % live cells, 6 % faster; 62 % and
+ *               75 %, as fast or slower); else 0.
+ * *blocks_per_item out (may be NULL): the plan's partition length, for
+ *               pa_table_segments.
+ * *max_items_per_seq out (may be NULL): partitions of the longest allowed
+ *               context: max_group_items of the call and of its workspace.
+ * PA_ERR_INVALID on a null pointer or a length out of range; errors of
+ * pa_decode_plan_info otherwise.
+ */
+pa_status pa_decode_items_plan(const int32_t* context_lens, int32_t B, int32_t num_q_heads,
+                               int32_t max_context_len, const pa_cache_desc* desc, int32_t split_tokens,
+                               int32_t* use_items, int32_t* blocks_per_item, int32_t* max_items_per_seq);
 
 /*
  * pa_chunked_prefill_workspace_size -- bytes of device workspace

@@ -93,6 +93,7 @@ SIGNATURES = {
                                             _I32, _I32, _F, _P, _I32, _I32, _P, _I32, _I32, _P, _I32,
                                             C.POINTER(CacheDesc), _P, C.c_size_t, _P]),
     "pa_table_segments": (C.c_int, [_P, _I32, _P, _P, _I32, _I32, _P, _I32, _P, _P]),
+    "pa_decode_items_plan": (C.c_int, [_P, _I32, _I32, _I32, C.POINTER(CacheDesc), _I32, _I32P, _I32P, _I32P]),
     "pa_chunked_prefill_workspace_size": (C.c_size_t, [_I32, _I32, _I32, _I32, _I32, C.POINTER(CacheDesc),
                                                        _I32]),
     "pa_chunked_prefill": (C.c_int, [_P, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
@@ -475,6 +476,23 @@ def shared_table_segments(block_tables, context_lens, group_start, blocks_per_it
     if st != PA_OK:
         raise ValueError(lib().pa_last_error().decode())
     return items[:count.value].copy(), most.value
+
+
+def decode_items_plan(context_lens, num_q_heads, max_context_len, k_cache, split_tokens=0):
+    """pa_decode_items_plan: (use_items, blocks_per_item, max_items_per_seq)
+    for a batch without shared blocks, from its host context lengths.
+    use_items says whether decode_append_segments over one-member groups
+    (the sequences' live partitions, shared_table_segments with group_start
+    0..B) beats decode_append's fixed grid: fewer than half of that grid's
+    cells hold blocks."""
+    import numpy as np
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    desc = cache_desc(k_cache)
+    use, bpi, most = C.c_int32(), C.c_int32(), C.c_int32()
+    _check(lib().pa_decode_items_plan(lens.ctypes.data_as(C.c_void_p), lens.shape[0], num_q_heads, max_context_len,
+                                      C.byref(desc), split_tokens, C.byref(use), C.byref(bpi), C.byref(most)),
+           "pa_decode_items_plan")
+    return bool(use.value), bpi.value, most.value
 
 
 def prefix_groups(block_tables, context_lens, max_group_size):

@@ -210,3 +210,40 @@ def _torch_like(desc):
     import torch
     dt = {ops.F16: torch.float16, ops.BF16: torch.bfloat16, ops.FP8_E4M3: torch.uint8, ops.INT8: torch.int8}
     return torch.empty((desc.num_blocks, desc.num_kv_heads, desc.block_size, desc.head_dim), dtype=dt[desc.kv_dtype])
+
+
+def test_items_plan_follows_the_live_cell_count(palib):
+    """pa_decode_items_plan: the item list when fewer than half of the fixed
+    grid's (sequence, partition) cells hold blocks, the split has more than
+    one partition and G <= 8; blocks_per_item is the plan's partition length
+    and max_items_per_seq its partition count."""
+    import numpy as np
+    dg = _desc(num_kv_heads=8, kv_dtype=ops.BF16)
+    rng = np.random.default_rng(5)
+    skewed = np.exp(rng.uniform(np.log(16), np.log(4096), 64)).astype(np.int32)   # log-uniform lengths
+    uniform = rng.integers(1, 2049, 32).astype(np.int32)
+    assert ops.decode_items_plan(skewed, 64, 4096, _torch_like(dg)) == (True, 32, 8)
+    d1 = _desc(num_kv_heads=32)
+    assert ops.decode_items_plan(uniform, 32, 2048, _torch_like(d1)) == (False, 32, 4)
+    # the rule, checked against its definition on random batches
+    for trial in range(40):
+        B = int(rng.integers(1, 80))
+        maxl = int(rng.integers(1, 9000))
+        lens = (rng.integers(0, maxl + 1, B) if trial % 2 else
+                np.minimum(maxl, np.exp(rng.uniform(0, np.log(maxl + 1), B)))).astype(np.int32)
+        for Hq, d in ((64, dg), (32, d1)):
+            parts, bpp, _ = ops.decode_plan_info(B, Hq, maxl, _torch_like(d))
+            live = int(((lens + 15) // 16 + bpp - 1).__floordiv__(bpp).sum())
+            want = parts > 1 and 2 * live < B * parts
+            assert ops.decode_items_plan(lens, Hq, maxl, _torch_like(d)) == (want, bpp, max(1, parts))
+    # G = 16 never lists: a member's query heads fill one MMA's 8 columns
+    d16 = _desc(num_kv_heads=4, kv_dtype=ops.BF16)
+    assert ops.decode_items_plan(skewed, 64, 4096, _torch_like(d16))[0] is False
+    # one partition (a 256-token split of 256-token contexts): nothing to skip
+    assert ops.decode_items_plan(np.full(8, 16, np.int32), 64, 256, _torch_like(dg), 256) == (False, 16, 1)
+    # a length past max_context_len, and a null pointer
+    with pytest.raises(RuntimeError):
+        ops.decode_items_plan(np.array([5000], np.int32), 64, 4096, _torch_like(dg))
+    use = C.c_int32()
+    assert palib.pa_decode_items_plan(None, 1, 64, 4096, C.byref(dg), 0, C.byref(use), None, None) == \
+        ops.PA_ERR_INVALID

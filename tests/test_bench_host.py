@@ -69,13 +69,15 @@ def test_prefill_cost_by_brute_force(kv):
 def test_traffic_record_follows_the_kernel_source(tmp_path, monkeypatch):
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "traffic_decode_demo.txt").write_text(
-        "kernel: x\ndram_bytes_per_launch: 12345\nkernel_source_sha256_16: abc\n")
+        "kernel: x\napi: pa_decode_append\ndram_bytes_per_launch: 12345\nkernel_source_sha256_16: abc\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc")
-    assert bench.profiled_traffic("demo") == 12345.0
-    assert bench.profiled_traffic("other") is None  # no record for that workload
+    assert bench.profiled_traffic("demo", "pa_decode_append") == 12345.0
+    assert bench.profiled_traffic("other", "pa_decode_append") is None  # no record for that workload
+    # a record of another entry point (the fixed grid against the item list) does not count
+    assert bench.profiled_traffic("demo", "pa_decode_append_segments (one-member groups)") is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "changed")
-    assert bench.profiled_traffic("demo") is None  # stale after a kernel edit
+    assert bench.profiled_traffic("demo", "pa_decode_append") is None  # stale after a kernel edit
 
 
 def test_clock_summary_reads_the_timed_window():

@@ -108,7 +108,7 @@ def test_decode_session_equals_decode_append(kv):
         kc, vc, ks, vs = w.k_pool.to(DEV), w.v_pool.to(DEV), None, None
         kc2, vc2, ks2, vs2 = w.k_pool.to(DEV), w.v_pool.to(DEV), None, None
     sess = DecodeSession(kc, vc, w.B, w.Hq, mb, ml, w.scale, torch.float16, k_scale=ks, v_scale=vs,
-                         out_dtype=torch.float32)
+                         out_dtype=torch.float32, items=False)
     rng = W.rng_for(9)
     for step in range(3):
         k_new = W.randn(rng, (w.B, w.Hkv, 128), torch.float16)
@@ -129,3 +129,80 @@ def test_decode_session_equals_decode_append(kv):
         torch.cuda.synchronize()
         assert torch.equal(got, want.cpu()), step
         assert torch.equal(kc.cpu(), kc2.cpu()) and torch.equal(vc.cpu(), vc2.cpu()), step
+
+
+@pytest.mark.parametrize("kv,mode", [("f16", True), ("f16", "auto"), ("fp8", "auto"), ("bf16", "auto")])
+def test_decode_session_items(kv, mode):
+    """DecodeSession in items mode over a batch with log-uniform lengths
+    (most cells of the fixed grid empty, so "auto" lists too): the session
+    lists the live partitions on the host and runs
+    pa_decode_append_segments.  Output within 5e-4 of ops.decode_append and
+    within tolerance of the oracle, caches and scales bit-identical, step
+    after step.  A uniform batch under "auto" stays on the fixed grid and
+    matches ops.decode_append bit for bit."""
+    from paged_kv_cache_191_gb300.session import DecodeSession
+    rng = np.random.default_rng(31)
+    lens = np.exp(rng.uniform(np.log(8), np.log(1500), 24)).astype(np.int32)
+    w = W.make_decode("skewed", 44, 24, 16, 4, 128, kv, lens, pool_factor=1.3)
+    ml, mb = int(w.context_lens.max()), w.block_tables.shape[1]
+    dt = torch.bfloat16 if kv == "bf16" else torch.float16
+    if kv == "fp8":
+        kc, vc, ks, vs = fp8_caches(w)
+        kc2, vc2, ks2, vs2 = fp8_caches(w)
+    else:
+        kc, vc, ks, vs = w.k_pool.to(DEV), w.v_pool.to(DEV), None, None
+        kc2, vc2, ks2, vs2 = w.k_pool.to(DEV), w.v_pool.to(DEV), None, None
+    assert ops.decode_items_plan(w.context_lens, w.Hq, ml, kc)[0]
+    sess = DecodeSession(kc, vc, w.B, w.Hq, mb, ml, w.scale, dt, k_scale=ks, v_scale=vs,
+                         out_dtype=torch.float32, items=mode)
+    rng = W.rng_for(10)
+    for step in range(3):
+        k_new = W.randn(rng, (w.B, w.Hkv, 128), dt)
+        v_new = W.randn(rng, (w.B, w.Hkv, 128), dt)
+        slots_p, lens_p, tab_p = sess.meta_ptrs()
+        np.ctypeslib.as_array(slots_p, (w.B,))[:] = last_slots(w)
+        np.ctypeslib.as_array(lens_p, (w.B,))[:] = w.context_lens
+        np.ctypeslib.as_array(tab_p, (w.B, mb))[:] = w.block_tables
+        q, k, v = sess.inputs()
+        q.copy_(w.q)
+        k.copy_(k_new)
+        v.copy_(v_new)
+        got = sess.step().clone().numpy()
+        assert sess.last_items and sess.last_copy_bytes == sess.nbytes + 16 * sess.last_items
+        want = ops.decode_append(k_new.to(DEV), v_new.to(DEV), torch.from_numpy(last_slots(w)).to(DEV),
+                                 w.q.to(DEV), kc2, vc2, torch.from_numpy(w.block_tables).to(DEV),
+                                 torch.from_numpy(w.context_lens).to(DEV), ml, w.scale, out_dtype=torch.float32,
+                                 k_scale=ks2, v_scale=vs2)
+        torch.cuda.synchronize()
+        assert np.abs(got - want.cpu().numpy()).max() <= 5e-4, step
+        assert torch.equal(kc.cpu(), kc2.cpu()) and torch.equal(vc.cpu(), vc2.cpu()), step
+        if kv == "fp8":
+            assert torch.equal(ks.cpu(), ks2.cpu()) and torch.equal(vs.cpu(), vs2.cpu()), step
+            ref = paged_decode(np_exact(w.q), kc.cpu().numpy(), vc.cpu().numpy(), w.block_tables, w.context_lens,
+                               w.scale, k_scale=ks.cpu().numpy(), v_scale=vs.cpu().numpy())
+        else:
+            ref = paged_decode(np_exact(w.q), np_exact(kc.cpu()), np_exact(vc.cpu()), w.block_tables,
+                               w.context_lens, w.scale)
+        assert_close(got, ref, TOL[kv], f"session items {kv} step {step}")
+    # uniform lengths: "auto" keeps the fixed grid
+    wu = W.make_decode("uniform", 45, 8, 16, 4, 128, "f16", np.full(8, 700, np.int32), pool_factor=1.3)
+    mlu, mbu = 700, wu.block_tables.shape[1]
+    kcu, vcu = wu.k_pool.to(DEV), wu.v_pool.to(DEV)
+    kcu2, vcu2 = wu.k_pool.to(DEV), wu.v_pool.to(DEV)
+    assert not ops.decode_items_plan(wu.context_lens, wu.Hq, mlu, kcu)[0]
+    sess = DecodeSession(kcu, vcu, wu.B, wu.Hq, mbu, mlu, wu.scale, torch.float16, out_dtype=torch.float32)
+    slots_p, lens_p, tab_p = sess.meta_ptrs()
+    np.ctypeslib.as_array(slots_p, (wu.B,))[:] = last_slots(wu)
+    np.ctypeslib.as_array(lens_p, (wu.B,))[:] = wu.context_lens
+    np.ctypeslib.as_array(tab_p, (wu.B, mbu))[:] = wu.block_tables
+    q, k, v = sess.inputs()
+    q.copy_(wu.q)
+    k.copy_(wu.new_k)
+    v.copy_(wu.new_v)
+    got = sess.step().clone()
+    assert sess.last_items is None and sess.last_copy_bytes == sess.nbytes
+    want = ops.decode_append(wu.new_k.to(DEV), wu.new_v.to(DEV), torch.from_numpy(last_slots(wu)).to(DEV),
+                             wu.q.to(DEV), kcu2, vcu2, torch.from_numpy(wu.block_tables).to(DEV),
+                             torch.from_numpy(wu.context_lens).to(DEV), mlu, wu.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want.cpu())

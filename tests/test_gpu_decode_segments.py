@@ -165,3 +165,61 @@ def test_bad_items_and_differing_blocks_are_flagged():
     w.block_tables[1, 0] = w.block_tables[1, w.context_lens[1] // 16 - 1]  # member 1 leaves the prompt's block 0
     run(w, start, items=items, max_items=most)
     assert ops.device_errors(clear=True) & ops.DEVERR_GROUP
+
+
+@pytest.mark.parametrize("cfg", ["gqa70b_b64", "llama7b_b32"])
+def test_one_member_groups_full_size_all_rows(cfg):
+    """A batch without sharing as B one-member groups: the items are each
+    sequence's live partitions, cut with the partition length
+    pa_decode_items_plan gives.  At the full workload size every row matches
+    the oracle, the plain call within 5e-4, and the fused writes leave the
+    same caches.  The log-uniform GQA batch is one the planner lists; the
+    uniform llama batch is one it leaves on the fixed grid (run here anyway)."""
+    w = W.CONFIGS[cfg]()
+    start = np.arange(w.B + 1, dtype=np.int32)
+    ml = int(w.context_lens.max())
+    kc_probe = torch.empty((1, w.Hkv, 16, w.D), dtype=w.q.dtype)
+    use, bpi, most = ops.decode_items_plan(w.context_lens, w.Hq, ml, kc_probe)
+    assert use == (cfg == "gqa70b_b64")
+    items, slots = ops.shared_table_segments(w.block_tables, w.context_lens, start, bpi)
+    assert slots <= most and ((items[:, 3] >> 8) & 0xff == 1).all()
+    got, dev_caches, (k_new, v_new, q) = run(w, start, bpi, items=items, max_items=most)
+    plain, plain_caches, _ = run(w, start, plain=True)
+    for a, b in zip(dev_caches, plain_caches):
+        assert a is None or torch.equal(a, b)
+    assert np.abs(got - plain).max() <= 5e-4, float(np.abs(got - plain).max())
+    okc, ovc, _, _ = o_write(np_exact(k_new.cpu()), np_exact(v_new.cpu()), last_slots(w), np_exact(w.k_pool),
+                             np_exact(w.v_pool))
+    ref = paged_decode(np_exact(q), okc, ovc, w.block_tables, w.context_lens, w.scale)
+    assert_close(got, ref, TOL[w.kv_dtype], f"{cfg} one-member groups")
+
+
+@pytest.mark.parametrize("kv", ["f16", "fp8"])
+@pytest.mark.parametrize("bpi", [4, 1])
+def test_one_member_groups_edge_lengths(kv, bpi):
+    """One-member groups over lengths 0, 5, 16, 17, 300 and 1100, items of 4
+    blocks (at most 18 a member) and of one block (69 for the longest: the
+    merge takes them in three chunks).  An empty member gets zero rows and
+    every row matches the oracle and the plain call; a second launch on the
+    same inputs gives the same rows."""
+    lens = [0, 5, 16, 17, 300, 1100]
+    w = W.make_decode(f"edges{bpi}{kv}", 61, len(lens), 8, 4, 128, kv, lens, pool_factor=1.2)
+    start = np.arange(w.B + 1, dtype=np.int32)
+    items, most = ops.shared_table_segments(w.block_tables, w.context_lens, start, bpi)
+    assert most == -(-69 // bpi)
+    got, dev_caches, (k_new, v_new, q) = run(w, start, bpi, items=items, max_items=most)
+    assert np.all(got[0] == 0.0)
+    plain, plain_caches, _ = run(w, start, plain=True)
+    for a, b in zip(dev_caches, plain_caches):
+        assert a is None or torch.equal(a, b)
+    assert np.abs(got - plain).max() <= 5e-4, float(np.abs(got - plain).max())
+    if kv == "fp8":
+        kc, vc, ks, vs = (t.numpy() for t in dev_caches)
+        ref = paged_decode(np_exact(q), kc, vc, w.block_tables, w.context_lens, w.scale, k_scale=ks, v_scale=vs)
+    else:
+        okc, ovc, _, _ = o_write(np_exact(k_new.cpu()), np_exact(v_new.cpu()), last_slots(w), np_exact(w.k_pool),
+                                 np_exact(w.v_pool))
+        ref = paged_decode(np_exact(q), okc, ovc, w.block_tables, w.context_lens, w.scale)
+    assert_close(got, ref, TOL[kv], f"one-member edges {kv} bpi {bpi}")
+    again, _, _ = run(w, start, bpi, items=items, max_items=most)
+    assert np.array_equal(again, got)
