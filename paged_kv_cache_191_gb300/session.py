@@ -65,6 +65,9 @@ class DecodeSession:
         self.nbytes = self.offsets[6]  # bytes copied per step without items
         self.host = [torch.zeros(off, dtype=torch.uint8).pin_memory() for _ in range(ring)]
         self.dev = torch.zeros(off, dtype=torch.uint8, device=dev)
+        # views of the part copied without items (made once: slicing costs host time per step)
+        self._host_meta = [h[: self.nbytes] for h in self.host]
+        self._dev_meta = self.dev[: self.nbytes]
         odt = out_dtype or dtype
         self.out = torch.empty((B, Hq, D), dtype=odt, device=dev)
         self.out_host = [torch.empty((B, Hq, D), dtype=odt).pin_memory() for _ in range(ring)]
@@ -149,7 +152,10 @@ class DecodeSession:
                 n_copy = o[6] + n_items * 16
         self.last_items, self.last_copy_bytes = n_items, n_copy
         with torch.cuda.stream(stream):
-            self.dev[:n_copy].copy_(self.host[i][:n_copy], non_blocking=True)
+            if n_items is None:
+                self._dev_meta.copy_(self._host_meta[i], non_blocking=True)
+            else:
+                self.dev[:n_copy].copy_(self.host[i][:n_copy], non_blocking=True)
             sp = C.c_void_p(stream.cuda_stream)
             if n_items is None:
                 ops._check(L.pa_decode_append(*self._head, sp), "pa_decode_append")
