@@ -60,6 +60,9 @@ __device__ uint32_t g_decode_err;
 #endif
 constexpr int kRingBytes = PA_RING_KB * 1024;  // K/V stage ring of one warp-CTA
 constexpr int kMaxDevices = 64;
+#ifndef PA_MERGE_SPEC
+#define PA_MERGE_SPEC 1  // the merge kernel loads its first 32 partial rows with the length
+#endif
 #ifndef PA_EARLY_ISSUE
 #define PA_EARLY_ISSUE 1
 #endif
@@ -1046,16 +1049,22 @@ __device__ __forceinline__ void merge_rows(const DecodeArgs& a, size_t row0, int
 }
 
 // Merge the partitions of each (sequence, query head).  One warp per query
-// head, G warps per CTA (one CTA per sequence and kv head, and query token
-// when the call maps rows).  The first chunk's (m, l) are read together with
-// the context length (rows up to max_parts always exist); partial rows only
-// for partitions that exist.
+// head and 32 dims, G warps per CTA (grid: sequence and kv head -- and query
+// token when the call maps rows -- by D / 32 dim slices).  Partitions are
+// taken 32 at a time, lane p holding partition p's (m, l) and every lane
+// reading its dim of all 32 partial rows, so one round trip brings a chunk:
+// the first chunk's loads go out together with the context length (the
+// workspace holds max_parts rows, and rows past the split are masked before
+// use: they may hold stale bytes).  Chunks merge online (running max).
 template <typename QT, int D>
 __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce(const DecodeArgs a) {
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int CH = 32;  // partitions per chunk: one per lane
   const int tq = a.q_tokens;
   const int bg = static_cast<int>(blockIdx.x) / tq, t = static_cast<int>(blockIdx.x) - bg * tq;
   const int b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int h = g * a.G + static_cast<int>(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int d = static_cast<int>(blockIdx.y) * 32 + lane;  // this lane's dim
   dev::grid_dependency_wait();  // partials of decode_main are complete and visible
   int ob = b, pseq = b, n = 1;
   if (a.q_start) {  // rows of a multi-token call: as decode_main maps them
@@ -1066,14 +1075,53 @@ __global__ void __launch_bounds__(32 * PA_MAX_GROUP) decode_reduce(const DecodeA
     pseq = b * tq + t;
   }
   const size_t row0 = (static_cast<size_t>(pseq) * a.Hq + h) * a.max_parts;
-  const float mv = lane < a.max_parts ? a.part_m[row0 + lane] : -INFINITY;
-  const float lv = lane < a.max_parts ? a.part_l[row0 + lane] : 0.f;
+  const int pre = min(CH, a.max_parts);
+  float mv = lane < pre ? __ldcg(a.part_m + row0 + lane) : -INFINITY;
+  float lv = lane < pre ? __ldcg(a.part_l + row0 + lane) : 0.f;
+  float x[CH];
+  if (PA_MERGE_SPEC) {
+#pragma unroll
+    for (int p = 0; p < CH; ++p) x[p] = p < pre ? __ldcg(a.part_o + (row0 + p) * D + d) : 0.f;
+  }
   int L = checked_len(a, b, false);
   if (a.q_start) L = max(0, L - n + 1 + t);
   const int nblk = (L + 15) >> 4;
   const int nparts = (nblk + a.bpp - 1) / a.bpp;
   if (nparts <= 1) return;  // written by decode_main (zero rows included)
-  merge_rows<QT, D>(a, row0, nparts, mv, lv, static_cast<size_t>(ob) * a.Hq + h, lane);
+  float M = -INFINITY, ls = 0.f, acc = 0.f;
+  for (int c0 = 0; c0 < nparts; c0 += CH) {
+    const int cn = min(CH, nparts - c0);
+    if (c0 > 0) {
+      mv = lane < cn ? __ldcg(a.part_m + row0 + c0 + lane) : -INFINITY;
+      lv = lane < cn ? __ldcg(a.part_l + row0 + c0 + lane) : 0.f;
+    }
+    if (c0 > 0 || !PA_MERGE_SPEC) {
+#pragma unroll
+      for (int p = 0; p < CH; ++p) x[p] = p < cn ? __ldcg(a.part_o + (row0 + c0 + p) * D + d) : 0.f;
+    }
+    if (lane >= cn) {
+      mv = -INFINITY;
+      lv = 0.f;
+    }
+#pragma unroll
+    for (int p = 0; p < CH; ++p)
+      if (p >= cn) x[p] = 0.f;  // rows past the split: stale, never weighed
+    float cm = mv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, off));
+    const float nm = fmaxf(M, cm);
+    const float rescale = dev::ex2(M - nm);  // 0 on the first chunk
+    M = nm;
+    const float w = lane < cn ? dev::ex2(mv - nm) : 0.f;  // this lane's partition weight
+    float wl = w * lv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(FULL, wl, off);
+    ls = ls * rescale + wl;
+    acc *= rescale;
+#pragma unroll
+    for (int p = 0; p < CH; ++p) acc += __shfl_sync(FULL, w, p) * x[p];
+  }
+  store_out<QT>(a, (static_cast<size_t>(ob) * a.Hq + h) * D + d, acc / ls);
 }
 
 // The grouped form: one CTA per (group k, member m, kv head g).  A member's
@@ -1338,7 +1386,7 @@ pa_status launch_t(const DecodeLaunch& l, CUtensorMapDataType dt, cudaStream_t s
                          dim3(static_cast<unsigned>(l.n_groups * l.max_members * l.Hkv)),
                          dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
   else if (e == cudaSuccess && l.plan.max_parts > 1 && !a.tickets)
-    e = launch_dependent(decode_reduce<QT, D>, dim3(static_cast<unsigned>(l.B * l.Hkv * tq)),
+    e = launch_dependent(decode_reduce<QT, D>, dim3(static_cast<unsigned>(l.B * l.Hkv * tq), D / 32),
                          dim3(static_cast<unsigned>(32 * a.G)), 0, stream, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_decode launch: %s", cudaGetErrorString(e));
